@@ -1,0 +1,211 @@
+"""CPU oracle for the W8A8 quantized verify pass.
+
+TEST INFRASTRUCTURE. Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import this package. The product path
+(``quantized_verification_gb300``) never imports it, and this package imports
+nothing from there.
+
+The arithmetic lives in ``qv_oracle.c`` (plain C, scalar loops, binary32
+operations one at a time, compiled without contraction or fast-math). This
+module compiles it with gcc on first use and wraps it with ctypes and numpy.
+Every function names the passage of the Quasar summaries it follows; the
+readings taken where the summaries are silent are listed in ``qv_oracle.c``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+SOURCE = os.path.join(_HERE, "qv_oracle.c")
+DEFAULT_LIB = os.path.join(_HERE, "libqv_oracle.so")
+
+# -ffp-contract=off: gcc contracts a*b+c into fma by default on aarch64;
+# every fp32 operation of the oracle must round on its own.
+CFLAGS = ["-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off",
+          "-fno-fast-math", "-fno-finite-math-only", "-frounding-math"]
+
+
+def build(src: str = SOURCE, out: str = DEFAULT_LIB, force: bool = False) -> str:
+    """Compile the oracle into a shared library; returns its path."""
+    if (not force and os.path.exists(out)
+            and os.path.getmtime(out) >= os.path.getmtime(src)):
+        return out
+    tmp = out + f".tmp{os.getpid()}"
+    subprocess.run(["gcc", *CFLAGS, "-o", tmp, src, "-lm"], check=True)
+    os.replace(tmp, out)
+    return out
+
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int64
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+class Oracle:
+    """ctypes view of one compiled oracle library (the default one, or a
+    deliberately broken copy built by the mutation tests)."""
+
+    def __init__(self, lib_path: str):
+        L = ctypes.CDLL(lib_path)
+        self._L = L
+        L.qvo_bf16_to_f32.restype = ctypes.c_float
+        L.qvo_bf16_to_f32.argtypes = [ctypes.c_uint16]
+        L.qvo_f32_to_bf16_rne.restype = ctypes.c_uint16
+        L.qvo_f32_to_bf16_rne.argtypes = [ctypes.c_float]
+        L.qvo_bf16_to_f32_array.argtypes = [_P, _P, _I]
+        L.qvo_f32_to_bf16_array.argtypes = [_P, _P, _I]
+        L.qvo_quantize_rows_f32.argtypes = [_P, _I, _I, _P, _P, _P]
+        L.qvo_quantize_rows_bf16.argtypes = [_P, _I, _I, _P, _P, _P]
+        L.qvo_int8_matmul.restype = ctypes.c_int64
+        L.qvo_int8_matmul.argtypes = [_P, _P, _I, _I, _I, _P]
+        L.qvo_dequant_one.restype = ctypes.c_float
+        L.qvo_dequant_one.argtypes = [ctypes.c_int32, ctypes.c_float, ctypes.c_float]
+        L.qvo_dequant.argtypes = [_P, _P, _P, _I, _I, _P]
+        L.qvo_argmax_rows.argtypes = [_P, _I, _I, _P, _P]
+        L.qvo_lm_head_argmax.argtypes = [_P, _P, _P, _P, _I, _I, _I, _P, _P]
+        L.qvo_accept.argtypes = [_P, _P, _I, _I, _P, _P]
+        L.qvo_linear_f64.argtypes = [_P, _P, _I, _I, _I, _P]
+
+    # -- bf16 ------------------------------------------------------------
+    def bf16_to_f32(self, h: np.ndarray) -> np.ndarray:
+        """Exact widening of bf16 bit patterns (uint16) to binary32."""
+        h = np.ascontiguousarray(h, dtype=np.uint16)
+        f = np.empty(h.shape, dtype=np.float32)
+        self._L.qvo_bf16_to_f32_array(_ptr(h), _ptr(f), h.size)
+        return f
+
+    def f32_to_bf16(self, f: np.ndarray) -> np.ndarray:
+        """binary32 -> bf16 bit patterns, round to nearest even."""
+        f = np.ascontiguousarray(f, dtype=np.float32)
+        h = np.empty(f.shape, dtype=np.uint16)
+        self._L.qvo_f32_to_bf16_array(_ptr(f), _ptr(h), f.size)
+        return h
+
+    # -- a0 / a1 ---------------------------------------------------------
+    def quantize_rows(self, x: np.ndarray, mul: np.ndarray | None = None,
+                      bf16: bool = False):
+        """Per-row symmetric int8 quantization (a0 weights, a1 activations).
+
+        Quasar, gist.science/ja summary, section 2.2 items 2-3 (weights and
+        activations to INT8; the activation is multiplied by the smoothing
+        factor first); gist.science/de summary, section 2 "Online-Prozess".
+        ``x`` is float32 [rows, K], or uint16 bf16 patterns with ``bf16=True``.
+        Returns (q int8 [rows, K], s float32 [rows]).
+        """
+        dt = np.uint16 if bf16 else np.float32
+        x = np.ascontiguousarray(x, dtype=dt)
+        rows, K = x.shape
+        q = np.empty((rows, K), dtype=np.int8)
+        s = np.empty(rows, dtype=np.float32)
+        m = None
+        if mul is not None:
+            m = np.ascontiguousarray(mul, dtype=np.float32)
+            assert m.shape == (K,)
+        fn = self._L.qvo_quantize_rows_bf16 if bf16 else self._L.qvo_quantize_rows_f32
+        fn(_ptr(x), rows, K, _ptr(m) if m is not None else None, _ptr(q), _ptr(s))
+        return q, s
+
+    # -- a2 ----------------------------------------------------------------
+    def int8_matmul(self, xq: np.ndarray, wq: np.ndarray) -> np.ndarray:
+        """Exact integer sums acc[m, n] = sum_k xq[m, k] * wq[n, k]
+        (gist.science/ja summary, section 2.2 item 3: INT8 GEMM, INT32
+        accumulation). Raises if a sum does not fit int32."""
+        xq = np.ascontiguousarray(xq, dtype=np.int8)
+        wq = np.ascontiguousarray(wq, dtype=np.int8)
+        M, K = xq.shape
+        N, K2 = wq.shape
+        assert K == K2
+        acc = np.empty((M, N), dtype=np.int32)
+        ov = self._L.qvo_int8_matmul(_ptr(xq), _ptr(wq), M, N, K, _ptr(acc))
+        if ov:
+            raise OverflowError(f"{ov} sums exceed int32")
+        return acc
+
+    def dequant(self, acc: np.ndarray, sx: np.ndarray, sw: np.ndarray) -> np.ndarray:
+        """y = fl(fl(acc) * fl(sx[m] * sw[n])) (dequantization back to high
+        precision, gist.science/ja summary, section 2.2 item 3)."""
+        acc = np.ascontiguousarray(acc, dtype=np.int32)
+        sx = np.ascontiguousarray(sx, dtype=np.float32)
+        sw = np.ascontiguousarray(sw, dtype=np.float32)
+        M, N = acc.shape
+        y = np.empty((M, N), dtype=np.float32)
+        self._L.qvo_dequant(_ptr(acc), _ptr(sx), _ptr(sw), M, N, _ptr(y))
+        return y
+
+    def w8a8_linear(self, xq, sx, wq, sw):
+        """a2: returns (y float32 [M, N], acc int32 [M, N])."""
+        acc = self.int8_matmul(xq, wq)
+        return self.dequant(acc, sx, sw), acc
+
+    # -- a3 ----------------------------------------------------------------
+    def argmax_rows(self, y: np.ndarray):
+        """Greedy token per row, lowest index on ties (gist.science/it
+        summary, section 2 item 3; greedy decoding, gist.science/ja summary,
+        section 4). Returns (tok int32 [M], max float32 [M])."""
+        y = np.ascontiguousarray(y, dtype=np.float32)
+        M, N = y.shape
+        tok = np.empty(M, dtype=np.int32)
+        mv = np.empty(M, dtype=np.float32)
+        self._L.qvo_argmax_rows(_ptr(y), M, N, _ptr(tok), _ptr(mv))
+        return tok, mv
+
+    def lm_head_argmax(self, xq, sx, wq, sw):
+        """a3: LM head logits formed one by one and reduced on the fly."""
+        xq = np.ascontiguousarray(xq, dtype=np.int8)
+        wq = np.ascontiguousarray(wq, dtype=np.int8)
+        sx = np.ascontiguousarray(sx, dtype=np.float32)
+        sw = np.ascontiguousarray(sw, dtype=np.float32)
+        M, K = xq.shape
+        V = wq.shape[0]
+        tok = np.empty(M, dtype=np.int32)
+        mv = np.empty(M, dtype=np.float32)
+        self._L.qvo_lm_head_argmax(_ptr(xq), _ptr(sx), _ptr(wq), _ptr(sw),
+                                   M, V, K, _ptr(tok), _ptr(mv))
+        return tok, mv
+
+    # -- a4 ----------------------------------------------------------------
+    def accept(self, t: np.ndarray, d: np.ndarray, B: int, gamma: int):
+        """Greedy acceptance (gist.science/fr summary, lay explanation;
+        L >= 1 from gist.science/ja summary, section 4).
+        Returns (len int32 [B], out int32 [B, gamma+1])."""
+        t = np.ascontiguousarray(t, dtype=np.int32).reshape(B * (gamma + 1))
+        d = np.ascontiguousarray(d, dtype=np.int32).reshape(max(B * gamma, 0))
+        ln = np.empty(B, dtype=np.int32)
+        out = np.empty(B * (gamma + 1), dtype=np.int32)
+        self._L.qvo_accept(_ptr(t), _ptr(d) if d.size else None, B, gamma,
+                           _ptr(ln), _ptr(out))
+        return ln, out.reshape(B, gamma + 1)
+
+    # -- comparator reference -------------------------------------------------
+    def linear_f64(self, x: np.ndarray, w: np.ndarray) -> np.ndarray:
+        """Unquantized y = x w^T in binary64 over binary32 inputs (the
+        high-precision verifier the W8A8 one replaces; gist.science/ja
+        summary, section 2.3)."""
+        x = np.ascontiguousarray(x, dtype=np.float32)
+        w = np.ascontiguousarray(w, dtype=np.float32)
+        M, K = x.shape
+        N = w.shape[0]
+        y = np.empty((M, N), dtype=np.float64)
+        self._L.qvo_linear_f64(_ptr(x), _ptr(w), M, N, K, _ptr(y))
+        return y
+
+
+_default: Oracle | None = None
+_lock = threading.Lock()
+
+
+def get() -> Oracle:
+    """The oracle built from ``qv_oracle.c`` (compiled on first use)."""
+    global _default
+    with _lock:
+        if _default is None:
+            _default = Oracle(build())
+        return _default

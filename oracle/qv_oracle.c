@@ -1,0 +1,305 @@
+/*
+ * qv_oracle.c -- plain, slow CPU oracle for the W8A8 quantized verify pass.
+ *
+ * TEST INFRASTRUCTURE. Only the test suite, the package smoke check and the
+ * CPU-baseline leg of the benchmark load this library. The product path (the
+ * CUDA library under quantized_verification_gb300/csrc) never links, loads or
+ * calls it, and this file includes nothing from there.
+ *
+ * What it computes, and where the pages say so
+ * (all pages summarise "Quasar: Quantized Self-Speculative Acceleration for
+ * Rapid Inference via Memory-Efficient Verification"; pages are named by
+ * site and language):
+ *
+ *   a0  per-output-channel symmetric int8 weight quantization
+ *       -- gist.science/ja summary, section 2.2 "Enhanced SmoothQuant",
+ *          item 2 (offline preparation: weights quantized to INT8);
+ *          gist.science/it summary, section 2 "Pipeline di Esecuzione".
+ *   a1  dynamic per-token symmetric int8 activation quantization, after an
+ *       optional per-input-channel smoothing multiply
+ *       -- gist.science/ja summary, section 2.2 item 3 (online inference:
+ *          scale the BF16 input by the smoothing factor, convert to INT8);
+ *          gist.science/de summary, section 2 "Methodik", "Online-Prozess";
+ *          the smoothing identity Y = (W diag(s)^-1)(diag(s) X) of the
+ *          gist.science/ja summary, section 2.2 item 1.
+ *   a2  INT8 GEMM with exact INT32 accumulation, then dequantization back to
+ *       high precision before any non-linear layer
+ *       -- gist.science/ja summary, section 2.2 item 3;
+ *          gist.science/fr summary, section 2 "Pipeline Technique".
+ *   a3  greedy (T=0) verify token = argmax over the dequantized vocabulary
+ *       logits, which stay in high precision for the acceptance test
+ *       -- gist.science/it summary, section 2 item 3 ("Campionamento di
+ *          Rifiuto Lossless"); greedy setting, gist.science/ja summary,
+ *          section 4 "main results".
+ *   a4  acceptance: the longest draft prefix equal to the verifier's tokens,
+ *       plus one token from the verifier (so at least one token per step)
+ *       -- gist.science/fr summary, lay explanation (a wrong guess is
+ *          rejected and generation restarts from there); acceptance length
+ *          L >= 1 implied by L ~ 1.03 for the pruned verifier,
+ *          gist.science/ja summary, section 4.
+ *
+ * Readings where the pages are silent (each is listed with its reason in the
+ * design notes of the repository):
+ *   - scale s = fl32(amax / 127) by IEEE division; q = rne(fl32(x / s)),
+ *     i.e. division by s, then round-half-to-even, then clamp to [-127, 127];
+ *     -128 is never produced.
+ *   - a row whose scale is 0 (all zeros, or amax/127 underflows) gets q = 0
+ *     and s = 0.
+ *   - smoothing: x' = fl32(x * c[k]) before amax; c == NULL is the identity.
+ *   - dequant: y = fl32( fl32((float)acc) * fl32(sx * sw) ), every operation
+ *     rounded to nearest-even, no fused multiply-add.
+ *   - argmax ties go to the lowest index; -0 compares equal to +0.
+ *   - acceptance: row j of sequence b holds the verifier token t[b][j] that
+ *     follows prefix position j; draft d[b][j] is accepted iff it equals
+ *     t[b][j] and all earlier drafts were accepted; the verifier token at the
+ *     first mismatch (or after the last draft) is always emitted.
+ *
+ * Floating point: every fp32 operation is a single IEEE binary32 operation
+ * in round-to-nearest-even. The library must be compiled with
+ * -ffp-contract=off and without -ffast-math (the build script does so).
+ * These choices are also the ones that decide integers (quantized codes,
+ * argmax), so they are taken in fp32, the precision the GPU path uses.
+ * The unquantized comparator reference (qvo_linear_f64) is fp64.
+ */
+#include <stdint.h>
+#include <stddef.h>
+#include <string.h>
+#include <math.h>
+
+/* ------------------------------------------------------------------ */
+/* bf16 <-> fp32                                                        */
+/* ------------------------------------------------------------------ */
+
+/* A bf16 value is the upper 16 bits of a binary32 pattern: widening is exact. */
+float qvo_bf16_to_f32(uint16_t h)
+{
+    uint32_t u = ((uint32_t)h) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+/* Narrow binary32 to bf16 rounding to nearest, ties to even, on the 16
+ * discarded bits. NaN inputs are outside the contract. */
+uint16_t qvo_f32_to_bf16_rne(float f)
+{
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    uint32_t upper = u >> 16;
+    uint32_t lower = u & 0xFFFFu;
+    if (lower > 0x8000u || (lower == 0x8000u && (upper & 1u)))
+        upper += 1u;
+    return (uint16_t)upper;
+}
+
+void qvo_bf16_to_f32_array(const uint16_t* h, float* f, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i) f[i] = qvo_bf16_to_f32(h[i]);
+}
+
+void qvo_f32_to_bf16_array(const float* f, uint16_t* h, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i) h[i] = qvo_f32_to_bf16_rne(f[i]);
+}
+
+/* ------------------------------------------------------------------ */
+/* a0 / a1: symmetric per-row int8 quantization                         */
+/* ------------------------------------------------------------------ */
+
+/* Round a binary32 value to the nearest integer, ties to even. Written out
+ * with floor so that it does not depend on the FPU rounding mode. */
+static float round_half_even(float v)
+{
+    float f = floorf(v);
+    float diff = v - f;            /* exact: v and f are within one unit */
+    if (diff > 0.5f) return f + 1.0f;
+    if (diff < 0.5f) return f;
+    /* exact tie: pick the even neighbour */
+    return (fmodf(f, 2.0f) == 0.0f) ? f : f + 1.0f;
+}
+
+/*
+ * Quantize `rows` rows of length K, one scale per row.
+ *   x    : rows*K binary32 values, row-major
+ *   mul  : K per-column multipliers (smoothing), or NULL for the identity
+ *   q    : rows*K int8 codes out
+ *   s    : rows scales out
+ * The same routine serves weights (one row per output channel, mul = NULL)
+ * and activations (one row per token).
+ */
+void qvo_quantize_rows_f32(const float* x, int64_t rows, int64_t K,
+                           const float* mul, int8_t* q, float* s)
+{
+    for (int64_t r = 0; r < rows; ++r) {
+        const float* xr = x + r * K;
+        /* amax over the (optionally smoothed) row */
+        float amax = 0.0f;
+        for (int64_t k = 0; k < K; ++k) {
+            float v = mul ? xr[k] * mul[k] : xr[k];
+            float a = fabsf(v);
+            if (a > amax) amax = a;
+        }
+        float scale = amax / 127.0f;
+        s[r] = scale;
+        for (int64_t k = 0; k < K; ++k) {
+            if (scale == 0.0f) { q[r * K + k] = 0; continue; }
+            float v = mul ? xr[k] * mul[k] : xr[k];
+            float t = round_half_even(v / scale);
+            if (t > 127.0f) t = 127.0f;
+            if (t < -127.0f) t = -127.0f;
+            q[r * K + k] = (int8_t)t;
+        }
+    }
+}
+
+/* Same as above for bf16 input: each element is widened exactly first. */
+void qvo_quantize_rows_bf16(const uint16_t* x, int64_t rows, int64_t K,
+                            const float* mul, int8_t* q, float* s)
+{
+    for (int64_t r = 0; r < rows; ++r) {
+        float amax = 0.0f;
+        for (int64_t k = 0; k < K; ++k) {
+            float v = qvo_bf16_to_f32(x[r * K + k]);
+            if (mul) v = v * mul[k];
+            float a = fabsf(v);
+            if (a > amax) amax = a;
+        }
+        float scale = amax / 127.0f;
+        s[r] = scale;
+        for (int64_t k = 0; k < K; ++k) {
+            if (scale == 0.0f) { q[r * K + k] = 0; continue; }
+            float v = qvo_bf16_to_f32(x[r * K + k]);
+            if (mul) v = v * mul[k];
+            float t = round_half_even(v / scale);
+            if (t > 127.0f) t = 127.0f;
+            if (t < -127.0f) t = -127.0f;
+            q[r * K + k] = (int8_t)t;
+        }
+    }
+}
+
+/* ------------------------------------------------------------------ */
+/* a2: int8 x int8 -> exact integer sums, then dequantization            */
+/* ------------------------------------------------------------------ */
+
+/*
+ * acc[m][n] = sum_k xq[m][k] * wq[n][k], the exact integer sum.
+ * Summed in int64; returns the number of sums that do not fit int32 (0 for
+ * every K the library accepts), and stores the low 32 bits regardless.
+ */
+int64_t qvo_int8_matmul(const int8_t* xq, const int8_t* wq,
+                        int64_t M, int64_t N, int64_t K, int32_t* acc)
+{
+    int64_t overflow = 0;
+    for (int64_t m = 0; m < M; ++m) {
+        for (int64_t n = 0; n < N; ++n) {
+            int64_t sum = 0;
+            const int8_t* a = xq + m * K;
+            const int8_t* b = wq + n * K;
+            for (int64_t k = 0; k < K; ++k)
+                sum += (int64_t)a[k] * (int64_t)b[k];
+            if (sum > INT32_MAX || sum < INT32_MIN) ++overflow;
+            acc[m * N + n] = (int32_t)sum;
+        }
+    }
+    return overflow;
+}
+
+/* y = fl32( fl32((float)acc) * fl32(sx[m] * sw[n]) ). */
+float qvo_dequant_one(int32_t acc, float sx, float sw)
+{
+    float a = (float)acc;          /* int -> float, round to nearest even */
+    float scale = sx * sw;
+    return a * scale;
+}
+
+void qvo_dequant(const int32_t* acc, const float* sx, const float* sw,
+                 int64_t M, int64_t N, float* y)
+{
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t n = 0; n < N; ++n)
+            y[m * N + n] = qvo_dequant_one(acc[m * N + n], sx[m], sw[n]);
+}
+
+/* ------------------------------------------------------------------ */
+/* a3: greedy argmax over each row                                      */
+/* ------------------------------------------------------------------ */
+
+/* tok[m] = lowest index of the maximum of y[m][:]; maxv[m] that maximum.
+ * Comparison is the plain float '>' so -0 == +0 and the first index wins. */
+void qvo_argmax_rows(const float* y, int64_t M, int64_t N,
+                     int32_t* tok, float* maxv)
+{
+    for (int64_t m = 0; m < M; ++m) {
+        int64_t best = 0;
+        float bv = y[m * N];
+        for (int64_t n = 1; n < N; ++n) {
+            if (y[m * N + n] > bv) { bv = y[m * N + n]; best = n; }
+        }
+        tok[m] = (int32_t)best;
+        if (maxv) maxv[m] = bv;
+    }
+}
+
+/* LM head: logits are formed one at a time with the a2 arithmetic and
+ * reduced on the fly, never stored. Same result as dequant + argmax. */
+void qvo_lm_head_argmax(const int8_t* xq, const float* sx,
+                        const int8_t* wq, const float* sw,
+                        int64_t M, int64_t V, int64_t K,
+                        int32_t* tok, float* maxv)
+{
+    for (int64_t m = 0; m < M; ++m) {
+        int64_t best = -1;
+        float bv = 0.0f;
+        for (int64_t v = 0; v < V; ++v) {
+            int64_t sum = 0;
+            for (int64_t k = 0; k < K; ++k)
+                sum += (int64_t)xq[m * K + k] * (int64_t)wq[v * K + k];
+            float y = qvo_dequant_one((int32_t)sum, sx[m], sw[v]);
+            if (best < 0 || y > bv) { bv = y; best = v; }
+        }
+        tok[m] = (int32_t)best;
+        if (maxv) maxv[m] = bv;
+    }
+}
+
+/* ------------------------------------------------------------------ */
+/* a4: greedy acceptance                                                 */
+/* ------------------------------------------------------------------ */
+
+/*
+ * t   : B*(gamma+1) verifier tokens; row j of sequence b is t[b*(gamma+1)+j]
+ * d   : B*gamma draft tokens; d[b*gamma+j] is the (j+1)-th drafted token
+ * len : B accepted lengths, in [1, gamma+1]
+ * out : B*(gamma+1) emitted tokens, t[b][0..len-1], then -1
+ */
+void qvo_accept(const int32_t* t, const int32_t* d, int64_t B, int64_t gamma,
+                int32_t* len, int32_t* out)
+{
+    int64_t G = gamma + 1;
+    for (int64_t b = 0; b < B; ++b) {
+        int64_t k = 0;
+        while (k < gamma && d[b * gamma + k] == t[b * G + k]) ++k;
+        len[b] = (int32_t)(k + 1);
+        for (int64_t j = 0; j < G; ++j)
+            out[b * G + j] = (j <= k) ? t[b * G + j] : -1;
+    }
+}
+
+/* ------------------------------------------------------------------ */
+/* Unquantized reference for the BF16-weight comparator                 */
+/* ------------------------------------------------------------------ */
+
+/* y[m][n] = sum_k x[m][k] * w[n][k] in binary64 (inputs are binary32, which
+ * holds every bf16 value exactly). */
+void qvo_linear_f64(const float* x, const float* w, int64_t M, int64_t N,
+                    int64_t K, double* y)
+{
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t n = 0; n < N; ++n) {
+            double sum = 0.0;
+            for (int64_t k = 0; k < K; ++k)
+                sum += (double)x[m * K + k] * (double)w[n * K + k];
+            y[m * N + n] = sum;
+        }
+}

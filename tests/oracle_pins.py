@@ -1,0 +1,347 @@
+"""Pins for the CPU oracle: checks against things other than the oracle.
+
+Each ``pin_*`` function takes an ``oracle.Oracle`` and raises AssertionError
+when the oracle disagrees with what the Quasar summaries and plain
+mathematics fix: the hand-worked example under ``tests/golden``, exact
+rational arithmetic (``tests/exact.py``), brute force on tiny inputs, library
+routines that compute the same textbook quantity (numpy integer matmul,
+numpy argmax, torch bf16 conversion, numpy binary32 arithmetic), and the
+invariants of the method. The mutation tests run every pin against
+deliberately broken copies of the oracle to show that each plausible mistake
+fails at least one of them.
+"""
+from __future__ import annotations
+
+import itertools
+import json
+import os
+from fractions import Fraction
+
+import numpy as np
+
+from exact import dequant_exact, f32, quantize_row_exact, rne_int, round_to_f32
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+def _bf16_bits(a_f32: np.ndarray) -> np.ndarray:
+    """bf16 patterns of values that are exactly representable in bf16."""
+    u = np.ascontiguousarray(a_f32, dtype=np.float32).view(np.uint32)
+    assert np.all((u & 0xFFFF) == 0), "value not exact in bf16"
+    return (u >> 16).astype(np.uint16)
+
+
+# ---------------------------------------------------------------------------
+# worked example
+# ---------------------------------------------------------------------------
+
+def pin_worked_example(o):
+    g = _golden("worked_2x3x4.json")
+    x = np.array(g["x_f32"], dtype=np.float32)
+    w = np.array(g["w_f32"], dtype=np.float32)
+    for bf16 in (False, True):
+        xin = _bf16_bits(x) if bf16 else x
+        win = _bf16_bits(w) if bf16 else w
+        xq, sx = o.quantize_rows(xin, bf16=bf16)
+        wq, sw = o.quantize_rows(win, bf16=bf16)
+        assert xq.tolist() == g["xq"], (bf16, xq)
+        assert sx.tolist() == g["sx"]
+        assert wq.tolist() == g["wq"], (bf16, wq)
+        assert sw.tolist() == g["sw"]
+    xq = np.array(g["xq"], dtype=np.int8)
+    wq = np.array(g["wq"], dtype=np.int8)
+    sx = np.array(g["sx"], dtype=np.float32)
+    sw = np.array(g["sw"], dtype=np.float32)
+    y, acc = o.w8a8_linear(xq, sx, wq, sw)
+    assert acc.tolist() == g["acc"]
+    assert np.array_equal(y, np.array(g["y_num_over_8192"], dtype=np.float64) / 8192)
+    tok, mv = o.argmax_rows(y)
+    assert tok.tolist() == g["tokens"]
+    assert mv.tolist() == [v / 8192 for v in g["max_logit_num_over_8192"]]
+    tok2, mv2 = o.lm_head_argmax(xq, sx, wq, sw)
+    assert tok2.tolist() == g["tokens"]
+    assert mv2.tolist() == mv.tolist()
+    t = np.array(g["tokens"], dtype=np.int32)
+    for case in g["accept_cases"]:
+        ln, out = o.accept(t, np.array(case["draft"], dtype=np.int32), 1, 1)
+        assert ln.tolist() == [case["len"]], case
+        assert out.tolist() == [case["out"]], case
+
+
+# ---------------------------------------------------------------------------
+# a0 / a1 quantization
+# ---------------------------------------------------------------------------
+
+def _hard_quant_rows(rng, n_rows=6, K=64):
+    """Rows containing values whose quotient x/s lands within an ulp of a
+    rounding boundary, found with numpy binary32 arithmetic: there division
+    by s and multiplication by 127/amax give different codes."""
+    rows = []
+    for _ in range(n_rows):
+        amax = np.float32(rng.uniform(0.5, 4.0))
+        s = np.float32(amax / np.float32(127))
+        r = np.float32(np.float32(127) / amax)
+        cand = (rng.uniform(-amax, amax, size=400000)).astype(np.float32)
+        q_div = np.rint(cand / s)
+        q_mul = np.rint(cand * r)
+        hard = cand[q_div != q_mul]
+        picked = list(hard[: K - 1])
+        while len(picked) < K - 1:
+            picked.append(np.float32(rng.uniform(-amax, amax)))
+        row = np.array([amax] + picked, dtype=np.float32)
+        rng.shuffle(row)
+        rows.append(row)
+    return np.stack(rows)
+
+
+def pin_quantize_exact_rational(o):
+    rng = np.random.default_rng(1234)
+    K = 64
+    rows = [
+        rng.standard_normal(K).astype(np.float32),
+        (rng.standard_normal(K) * 1e-3).astype(np.float32),
+        (rng.standard_normal(K) * 3e4).astype(np.float32),
+        # tiny row with subnormal quotients / scales
+        (rng.standard_normal(K) * 1e-38).astype(np.float32),
+    ]
+    outl = rng.standard_normal(K).astype(np.float32)
+    outl[[3, 17]] *= 20
+    rows.append(outl)
+    x = np.concatenate([np.stack(rows), _hard_quant_rows(rng)])
+    q, s = o.quantize_rows(x)
+    for i in range(x.shape[0]):
+        q_ref, s_ref = quantize_row_exact(x[i])
+        assert np.float32(s[i]) == s_ref, (i, s[i], s_ref)
+        assert q[i].tolist() == q_ref, i
+
+
+def pin_quantize_ties(o):
+    # amax = 127/64 gives s = 1/64 exactly; x = (j + 1/2)/64 are exact ties
+    js = np.arange(-126, 126)
+    row = np.concatenate([[127.0], (js + 0.5)]) / 64.0
+    x = row.astype(np.float32)[None, :]
+    q, s = o.quantize_rows(x)
+    assert s[0] == np.float32(1 / 64)
+    expect = [127] + [rne_int(Fraction(2 * j + 1, 2)) for j in js]
+    assert q[0].tolist() == expect
+
+
+def pin_quantize_invariants(o):
+    rng = np.random.default_rng(99)
+    x = rng.standard_normal((32, 200)).astype(np.float32)
+    x[:, rng.choice(200, 4, replace=False)] *= 20
+    q, s = o.quantize_rows(x)
+    assert np.all(np.abs(q.astype(np.int32)) <= 127)
+    assert np.all(s >= 0)
+    idx = np.argmax(np.abs(x), axis=1)
+    for i in range(32):
+        assert q[i, idx[i]] == (127 if x[i, idx[i]] > 0 else -127)
+        # codes reproduce the row to within half a step
+        err = np.abs(q[i].astype(np.float64) * float(s[i]) - x[i].astype(np.float64))
+        assert np.all(err <= 0.5 * float(s[i]) * (1 + 1e-6) + 1e-30)
+    # an all-zero row and a row whose amax/127 underflows to zero
+    z = np.zeros((2, 16), dtype=np.float32)
+    z[1, 5] = np.float32(63 * 2.0 ** -149)
+    qz, sz = o.quantize_rows(z)
+    assert np.all(qz == 0) and np.all(sz == 0)
+
+
+def pin_quantize_smoothing(o):
+    rng = np.random.default_rng(7)
+    K = 48
+    x = rng.standard_normal((5, K)).astype(np.float32)
+    c = rng.uniform(0.25, 4.0, K).astype(np.float32)
+    q, s = o.quantize_rows(x, c)
+    xs = (x * c).astype(np.float32)       # numpy binary32 multiply: one rounding
+    q2, s2 = o.quantize_rows(xs)
+    assert np.array_equal(q, q2) and np.array_equal(s, s2)
+    for i in range(2):
+        q_ref, s_ref = quantize_row_exact(x[i], c)
+        assert q[i].tolist() == q_ref and s[i] == s_ref
+    # bf16 input path with smoothing
+    xb = o.f32_to_bf16(x)
+    qb, sb = o.quantize_rows(xb, c, bf16=True)
+    xw = o.bf16_to_f32(xb)
+    qb2, sb2 = o.quantize_rows((xw * c).astype(np.float32))
+    assert np.array_equal(qb, qb2) and np.array_equal(sb, sb2)
+    # identity multiplier equals no multiplier
+    q3, s3 = o.quantize_rows(x, np.ones(K, np.float32))
+    q4, s4 = o.quantize_rows(x)
+    assert np.array_equal(q3, q4) and np.array_equal(s3, s4)
+
+
+# ---------------------------------------------------------------------------
+# a2 integer GEMM and dequantization
+# ---------------------------------------------------------------------------
+
+def pin_int8_matmul_bruteforce(o):
+    rng = np.random.default_rng(5)
+    for (M, N, K) in [(1, 1, 1), (2, 3, 5), (3, 7, 8), (4, 8, 6)]:
+        xq = rng.integers(-127, 128, (M, K)).astype(np.int8)
+        wq = rng.integers(-127, 128, (N, K)).astype(np.int8)
+        acc = o.int8_matmul(xq, wq)
+        for m in range(M):
+            for n in range(N):
+                ref = sum(int(xq[m, k]) * int(wq[n, k]) for k in range(K))
+                assert acc[m, n] == ref, (M, N, K, m, n)
+    # enumerate every pair of 1-element rows over a small code range
+    vals = np.arange(-127, 128, 9, dtype=np.int8)
+    acc = o.int8_matmul(vals[:, None], vals[:, None])
+    assert np.array_equal(acc, np.outer(vals.astype(np.int64), vals.astype(np.int64)))
+    # textbook: an integer matrix product
+    xq = rng.integers(-127, 128, (6, 300)).astype(np.int8)
+    wq = rng.integers(-127, 128, (40, 300)).astype(np.int8)
+    assert np.array_equal(o.int8_matmul(xq, wq),
+                          xq.astype(np.int64) @ wq.astype(np.int64).T)
+
+
+def pin_int8_matmul_range(o):
+    # the largest K with exact int32 sums: floor((2^31-1)/127^2) = 133144
+    K = (2 ** 31 - 1) // (127 * 127)
+    assert K == 133144
+    x = np.full((1, K), 127, np.int8)
+    w = np.concatenate([np.full((1, K), 127, np.int8), np.full((1, K), -127, np.int8)])
+    acc = o.int8_matmul(x, w)
+    assert acc.tolist() == [[K * 16129, -K * 16129]]
+    try:
+        o.int8_matmul(np.full((1, K + 1), 127, np.int8), np.full((1, K + 1), 127, np.int8))
+    except OverflowError:
+        pass
+    else:
+        raise AssertionError("K beyond the int32 limit was not reported")
+
+
+def pin_dequant_exact(o):
+    rng = np.random.default_rng(11)
+    M, N = 3, 50
+    acc = rng.integers(-2 ** 28, 2 ** 28, (M, N)).astype(np.int32)
+    acc[0, :5] = [0, 1, -1, 2 ** 24 + 1, -(2 ** 25) - 3]      # rounding of int -> float
+    sx = (rng.uniform(1e-3, 1e-1, M)).astype(np.float32)
+    sw = (rng.uniform(1e-5, 1e-3, N)).astype(np.float32)
+    y = o.dequant(acc, sx, sw)
+    for m in range(M):
+        for n in range(N):
+            ref = dequant_exact(int(acc[m, n]), sx[m], sw[n])
+            assert y[m, n] == ref, (m, n, y[m, n], ref)
+            exact = Fraction(int(acc[m, n])) * f32(sx[m]) * f32(sw[n])
+            if exact != 0:
+                assert abs(f32(y[m, n]) - exact) <= abs(exact) * Fraction(3, 2 ** 24)
+    # numpy binary32 arithmetic does the same two products
+    ynp = acc.astype(np.float32) * (sx[:, None] * sw[None, :]).astype(np.float32)
+    assert np.array_equal(y, ynp.astype(np.float32))
+
+
+# ---------------------------------------------------------------------------
+# a3 argmax
+# ---------------------------------------------------------------------------
+
+def pin_argmax(o):
+    rng = np.random.default_rng(21)
+    y = rng.integers(-5, 6, (40, 17)).astype(np.float32)    # many ties
+    y[0] = 0.0
+    y[1, :] = -1.0
+    y[1, 4] = -0.0
+    y[1, 9] = 0.0                                            # -0 and +0 tie
+    tok, mv = o.argmax_rows(y)
+    for m in range(y.shape[0]):
+        ref = sorted(range(y.shape[1]), key=lambda n: (-float(y[m, n]), n))[0]
+        assert tok[m] == ref, (m, tok[m], ref)
+        assert mv[m] == y[m].max()
+    assert np.array_equal(tok, np.argmax(y, axis=1).astype(np.int32))
+    assert tok[1] == 4
+    # lm head on random codes equals an independent composition
+    xq = rng.integers(-127, 128, (4, 24)).astype(np.int8)
+    wq = rng.integers(-127, 128, (37, 24)).astype(np.int8)
+    wq[20] = wq[3]                                            # duplicate rows tie
+    sx = rng.uniform(0.01, 0.02, 4).astype(np.float32)
+    sw = np.full(37, np.float32(0.004))
+    t2, m2 = o.lm_head_argmax(xq, sx, wq, sw)
+    acc = xq.astype(np.int64) @ wq.astype(np.int64).T
+    ynp = acc.astype(np.float32) * (sx[:, None] * sw[None, :]).astype(np.float32)
+    assert np.array_equal(t2, np.argmax(ynp, axis=1).astype(np.int32))
+    assert np.array_equal(m2, ynp.max(axis=1))
+
+
+# ---------------------------------------------------------------------------
+# a4 acceptance
+# ---------------------------------------------------------------------------
+
+def _accept_by_definition(t_row, d_row, gamma):
+    best = 0
+    for i in range(gamma + 1):           # i drafts accepted iff the first i all match
+        if all(d_row[j] == t_row[j] for j in range(i)):
+            best = i
+    out = list(t_row[: best + 1]) + [-1] * (gamma - best)
+    return best + 1, out
+
+
+def pin_accept_enumeration(o):
+    V = 3
+    for gamma in range(0, 4):
+        for t_row in itertools.product(range(V), repeat=gamma + 1):
+            drafts = list(itertools.product(range(V), repeat=gamma))
+            B = len(drafts)
+            t = np.array([t_row] * B, dtype=np.int32)
+            d = np.array(drafts, dtype=np.int32).reshape(B, gamma)
+            ln, out = o.accept(t, d, B, gamma)
+            for b in range(B):
+                L, ref = _accept_by_definition(t_row, drafts[b], gamma)
+                assert ln[b] == L and out[b].tolist() == ref, (gamma, t_row, drafts[b])
+                assert 1 <= ln[b] <= gamma + 1
+                assert list(out[b, : ln[b] - 1]) == list(drafts[b][: ln[b] - 1])
+                assert out[b, ln[b] - 1] == t_row[ln[b] - 1]
+
+
+# ---------------------------------------------------------------------------
+# bf16 conversion and the fp64 comparator reference
+# ---------------------------------------------------------------------------
+
+def pin_bf16(o):
+    import torch
+    rng = np.random.default_rng(3)
+    f = (rng.standard_normal(5000) * np.exp(rng.uniform(-20, 20, 5000))).astype(np.float32)
+    ties = np.array([0x3F808000, 0x3F818000, 0xBF808000, 0x3F80C000, 0x3F804000,
+                     0x00008000, 0x00018000], dtype=np.uint32).view(np.float32)
+    f = np.concatenate([f, ties])
+    h = o.f32_to_bf16(f)
+    ref = torch.from_numpy(f).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(h, ref)
+    assert h[-7:].tolist() == [0x3F80, 0x3F82, 0xBF80, 0x3F81, 0x3F80, 0x0000, 0x0002]
+    back = o.bf16_to_f32(h)
+    assert np.array_equal(back.view(np.uint32), h.astype(np.uint32) << 16)
+
+
+def pin_linear_f64(o):
+    rng = np.random.default_rng(8)
+    M, N, K = 3, 5, 40
+    x = rng.standard_normal((M, K)).astype(np.float32)
+    w = (rng.standard_normal((N, K)) * 0.02).astype(np.float32)
+    y = o.linear_f64(x, w)
+    for m in range(M):
+        for n in range(N):
+            exact = sum(f32(x[m, k]) * f32(w[n, k]) for k in range(K))
+            mag = sum(abs(f32(x[m, k]) * f32(w[n, k])) for k in range(K))
+            assert abs(Fraction(float(y[m, n])) - exact) <= mag * Fraction(K, 2 ** 52)
+    ynp = x.astype(np.float64) @ w.astype(np.float64).T
+    assert np.allclose(y, ynp, rtol=1e-12, atol=1e-15)
+
+
+ALL_PINS = [
+    pin_worked_example,
+    pin_quantize_exact_rational,
+    pin_quantize_ties,
+    pin_quantize_invariants,
+    pin_quantize_smoothing,
+    pin_int8_matmul_bruteforce,
+    pin_int8_matmul_range,
+    pin_dequant_exact,
+    pin_argmax,
+    pin_accept_enumeration,
+    pin_bf16,
+    pin_linear_f64,
+]

@@ -1,0 +1,59 @@
+"""Mutation tests: plant a plausible mistake in a copy of the oracle's C
+source, build it on the CPU, and check that at least one pin catches it.
+The oracle itself is never modified."""
+import os
+
+import pytest
+
+import oracle as oracle_pkg
+import oracle_pins
+
+# (name, original snippet, mutated snippet)
+MUTANTS = [
+    ("round_ties_up",
+     "return (fmodf(f, 2.0f) == 0.0f) ? f : f + 1.0f;", "return f + 1.0f;"),
+    ("truncate_instead_of_round",
+     "float t = round_half_even(v / scale);", "float t = truncf(v / scale);"),
+    ("multiply_by_127_over_amax",
+     "float t = round_half_even(v / scale);",
+     "float t = round_half_even(v * (127.0f / amax));"),
+    ("drop_last_k",
+     "for (int64_t k = 0; k < K; ++k)\n                sum += (int64_t)a[k] * (int64_t)b[k];",
+     "for (int64_t k = 0; k < K - 1; ++k)\n                sum += (int64_t)a[k] * (int64_t)b[k];"),
+    ("transposed_weight",
+     "sum += (int64_t)a[k] * (int64_t)b[k];",
+     "sum += (int64_t)a[k] * (int64_t)wq[k * N + n];"),
+    ("dequant_drops_weight_scale", "float scale = sx * sw;", "float scale = sx;"),
+    ("dequant_other_order", "return a * scale;", "return (a * sx) * sw;"),
+    ("argmax_last_tie", "if (y[m * N + n] > bv)", "if (y[m * N + n] >= bv)"),
+    ("lm_head_last_tie", "if (best < 0 || y > bv)", "if (best < 0 || y >= bv)"),
+    ("accept_no_bonus", "len[b] = (int32_t)(k + 1);", "len[b] = (int32_t)k;"),
+    ("accept_out_short", "out[b * G + j] = (j <= k) ? t[b * G + j] : -1;",
+     "out[b * G + j] = (j < k) ? t[b * G + j] : -1;"),
+    ("accept_shifted_compare", "d[b * gamma + k] == t[b * G + k]",
+     "d[b * gamma + k] == t[b * G + k + 1]"),
+    ("bf16_ties_away", "(lower == 0x8000u && (upper & 1u))", "(lower == 0x8000u)"),
+    ("amax_ignores_smoothing",
+     "float v = mul ? xr[k] * mul[k] : xr[k];\n            float a = fabsf(v);",
+     "float v = xr[k];\n            float a = fabsf(v);"),
+    ("linear_f64_in_float", "double sum = 0.0;", "float sum = 0.0f;"),
+]
+
+
+@pytest.mark.parametrize("name,orig,mut", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_mutant_is_caught(tmp_path, name, orig, mut):
+    with open(oracle_pkg.SOURCE) as f:
+        src = f.read()
+    assert src.count(orig) >= 1, f"snippet for {name} not found"
+    bad = src.replace(orig, mut, 1)
+    csrc = tmp_path / f"{name}.c"
+    csrc.write_text(bad)
+    lib = oracle_pkg.build(str(csrc), str(tmp_path / f"lib{name}.so"), force=True)
+    o = oracle_pkg.Oracle(lib)
+    caught = []
+    for pin in oracle_pins.ALL_PINS:
+        try:
+            pin(o)
+        except (AssertionError, OverflowError, ValueError) as e:  # noqa: PERF203
+            caught.append(pin.__name__)
+    assert caught, f"no pin catches mutant {name}"
