@@ -1,0 +1,246 @@
+/*
+ * qv.h -- C ABI of libqv, the GB300 (sm_103a) W8A8 quantized verify pass.
+ *
+ * The method: "Quasar: Quantized Self-Speculative Acceleration for Rapid
+ * Inference via Memory-Efficient Verification". The verify pass of
+ * speculative decoding runs on a W8A8 copy of the target model: activations
+ * are quantized per token to symmetric int8, multiplied by per-output-channel
+ * symmetric int8 weights with exact int32 accumulation, dequantized back to
+ * high precision, and the greedy verifier tokens decide how many draft tokens
+ * are accepted. Passages are cited by the summary page (site and language)
+ * and its section.
+ *
+ * Conventions shared by every entry point
+ *   - All pointers except `stream` are DEVICE pointers of the current device
+ *     (device or managed memory; checked with cudaPointerGetAttributes, a
+ *     host pointer is rejected with QV_ERR_INVALID_ARG).
+ *     The caller allocates and owns every buffer, including workspaces;
+ *     libqv allocates no device memory and never synchronizes the device.
+ *   - Every call only enqueues work on `stream` (NULL = legacy default
+ *     stream) and returns immediately.
+ *   - Matrices are row-major and densely packed: element (r, c) of an
+ *     R x C matrix is at r*C + c.
+ *   - Arguments are validated on the host before anything is enqueued. A call
+ *     that returns a status other than QV_OK has enqueued nothing and left
+ *     every output untouched; qv_last_error() then describes the problem.
+ *     QV_ERR_CUDA reports a failed launch (the CUDA error is in the message).
+ *   - int8 and bf16 buffers must be 16-byte aligned; fp32 and int32 buffers
+ *     4-byte aligned. K must be a positive multiple of 16 and at most
+ *     QV_MAX_K, the largest K for which every int32 sum of K products of
+ *     codes in [-127, 127] is exact.
+ *   - Kernels of this library may begin before the previous kernel on the
+ *     same stream has finished (programmatic dependent launch). Before that
+ *     wait completes they read only weight codes (`wq`); everything else is
+ *     read after all earlier work on the stream is complete and visible.
+ *     Weight codes therefore must not be written by a kernel that is still
+ *     running when the call is enqueued; qv_quantize_weight never lets its
+ *     successor start early, so quantize-then-use on one stream is safe.
+ *   - Results are deterministic: every call returns identical bits for
+ *     identical inputs (the bf16 comparator excepted, see qv_bf16_linear).
+ */
+#ifndef QV_H
+#define QV_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#if defined(__GNUC__)
+#define QV_API __attribute__((visibility("default")))
+#else
+#define QV_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    QV_OK = 0,
+    QV_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, bad size        */
+    QV_ERR_UNSUPPORTED = 2,   /* shape outside what the kernels handle    */
+    QV_ERR_WORKSPACE = 3,     /* workspace missing or too small           */
+    QV_ERR_CUDA = 4           /* a CUDA call failed                        */
+} qv_status;
+
+typedef enum { QV_F32 = 0, QV_BF16 = 1 } qv_dtype;
+
+typedef enum {
+    QV_OP_LINEAR = 0,         /* qv_w8a8_linear                            */
+    QV_OP_LM_HEAD = 1,        /* qv_lm_head_argmax (N = vocabulary size V) */
+    QV_OP_BF16_LINEAR = 2     /* qv_bf16_linear                            */
+} qv_op;
+
+/* floor((2^31 - 1) / 127^2): the int32 accumulation stays exact up to here. */
+#define QV_MAX_K 133144
+/* Largest number of verify tokens (rows of activations) per call. */
+#define QV_MAX_M 256
+
+/*
+ * qv_quantize_act -- a1: dynamic per-token symmetric int8 activation
+ * quantization, with an optional smoothing multiply.
+ *
+ *   Quasar, gist.science/ja summary, section 2.2 "Enhanced SmoothQuant",
+ *   item 3: the BF16 input activation is scaled by the per-channel smoothing
+ *   factor and converted to INT8 online; item 1 gives the smoothing identity
+ *   Y = (W diag(s)^-1)(diag(s) X). gist.science/de summary, section 2
+ *   "Methodik", "Online-Prozess". Per-token granularity and the rounding rule
+ *   are this library's reading of the summaries (they give neither).
+ *
+ * For every row m < M (one token):
+ *   x'[k]  = fl32(x[m][k] * act_mul[k])      (x'[k] = x[m][k] if act_mul NULL)
+ *   amax   = max_k |x'[k]|
+ *   sx[m]  = fl32(amax / 127)                (IEEE division)
+ *   xq[m][k] = clamp(round_half_even(fl32(x'[k] / sx[m])), -127, 127),
+ *              or 0 for every k when sx[m] == 0.
+ *
+ *   x       [M*K] fp32 or bf16 (x_dtype), 16-byte aligned
+ *   act_mul [K] fp32 multipliers already in "multiply" form, or NULL
+ *   xq      [M*K] int8 out, 16-byte aligned
+ *   sx      [M] fp32 out
+ *   1 <= M <= 65535 (rows are independent; M is not bounded by QV_MAX_M here).
+ * Non-finite inputs are outside the contract.
+ */
+QV_API qv_status qv_quantize_act(const void* x, qv_dtype x_dtype, int M, int K,
+                          const float* act_mul, int8_t* xq, float* sx,
+                          cudaStream_t stream);
+
+/*
+ * qv_w8a8_linear -- a2: int8 x int8 GEMM with exact int32 accumulation and a
+ * fused dequantization epilogue.
+ *
+ *   Quasar, gist.science/ja summary, section 2.2 item 3: INT8 GEMM,
+ *   accumulation in INT32, dequantization to high precision before the
+ *   non-linear layers; gist.science/fr summary, section 2 "Pipeline
+ *   Technique" (INT8 tensor cores, results dequantized).
+ *
+ *   acc[m][n] = sum_k xq[m][k] * wq[n][k]            (exact integer)
+ *   y[m][n]   = fl32( fl32((float)acc[m][n]) * fl32(sx[m] * sw[n]) )
+ *               stored as fp32, or rounded to bf16 (nearest even) when
+ *               y_dtype == QV_BF16.
+ *
+ *   xq  [M*K] int8, sx [M] fp32      -- from qv_quantize_act
+ *   wq  [N*K] int8, sw [N] fp32      -- from qv_quantize_weight (row n =
+ *                                       output channel n, K contiguous)
+ *   y   [M*N] fp32 or bf16 out
+ *   acc_debug [M*N] int32 out, or NULL: the exact accumulators
+ *   workspace: at least qv_workspace_bytes(QV_OP_LINEAR, M, K, N) bytes,
+ *     16-byte aligned, ZERO-FILLED before its first use. Every call leaves
+ *     it zero-filled again when its work completes, so one workspace can be
+ *     reused by any sequence of stream-ordered calls. Calls that run
+ *     concurrently (different streams) need separate workspaces.
+ *   1 <= M <= QV_MAX_M, N >= 1. Codes of -128 are accepted; the sums are
+ *   exact whenever they fit int32, which codes in [-127, 127] guarantee.
+ */
+QV_API qv_status qv_w8a8_linear(const int8_t* xq, const float* sx, int M, int K,
+                         const int8_t* wq, const float* sw, int N,
+                         void* y, qv_dtype y_dtype, int32_t* acc_debug,
+                         void* workspace, size_t workspace_bytes,
+                         cudaStream_t stream);
+
+/*
+ * qv_lm_head_argmax -- a3: the W8A8 LM head fused with the greedy argmax.
+ *
+ *   The logits stay in high precision for the acceptance test:
+ *   gist.science/it summary, section 2 item 3 ("Campionamento di Rifiuto
+ *   Lossless"); greedy decoding (T=0), gist.science/ja summary, section 4.
+ *
+ *   y[m][v]     = the qv_w8a8_linear value for N = V (never stored)
+ *   tokens[m]   = the smallest v with y[m][v] == max_v' y[m][v']
+ *   max_logit[m]= that maximum (optional)
+ * Ties go to the lowest index; -0 and +0 compare equal. NaN is outside the
+ * contract.
+ *
+ *   wq [V*K] int8, sw [V] fp32, tokens [M] int32 out, max_logit [M] or NULL
+ *   workspace: qv_workspace_bytes(QV_OP_LM_HEAD, M, K, V) bytes, same
+ *   zero-fill contract as qv_w8a8_linear.
+ *   1 <= M <= QV_MAX_M, 1 <= V.
+ */
+QV_API qv_status qv_lm_head_argmax(const int8_t* xq, const float* sx, int M, int K,
+                            const int8_t* wq, const float* sw, int V,
+                            int32_t* tokens, float* max_logit,
+                            void* workspace, size_t workspace_bytes,
+                            cudaStream_t stream);
+
+/*
+ * qv_accept -- a4: greedy acceptance of the longest matching draft prefix
+ * plus one verifier token.
+ *
+ *   gist.science/fr summary, lay explanation: a wrong draft token is
+ *   rejected and generation continues from the verifier's token; at least
+ *   one token is produced per step (acceptance length L ~ 1.03 for a nearly
+ *   useless verifier, gist.science/ja summary, section 4). At T = 0 the
+ *   rejection-sampling rule of gist.science/it summary, section 2 item 3
+ *   reduces to exact matching against the argmax.
+ *
+ * Sequence b has gamma+1 verify rows: verify_tokens[b*(gamma+1) + j] is the
+ * verifier's token after prefix position j (j = 0 is the last accepted
+ * token); draft[b*gamma + j] is the (j+1)-th drafted token.
+ *   k = the largest i <= gamma with draft[b][j] == verify[b][j] for all j < i
+ *   accept_len[b]       = k + 1                       (in [1, gamma+1])
+ *   out_tokens[b][j]    = verify[b][j] for j <= k, else -1
+ * Token ids are compared as raw int32. B >= 1, 0 <= gamma <= 1023;
+ * draft may be NULL when gamma == 0.
+ */
+QV_API qv_status qv_accept(const int32_t* verify_tokens, const int32_t* draft,
+                    int B, int gamma, int32_t* accept_len,
+                    int32_t* out_tokens, cudaStream_t stream);
+
+/*
+ * qv_quantize_weight -- a0 (setup, not on the timed path): per-output-channel
+ * symmetric int8 weight quantization. Same rule as qv_quantize_act with one
+ * row per output channel and no smoothing multiply:
+ *   sw[n] = fl32(amax_n / 127), wq[n][k] = clamp(rne(fl32(w[n][k] / sw[n])))
+ *   Quasar, gist.science/ja summary, section 2.2 item 2 (weights quantized
+ *   to INT8 offline); gist.science/it summary, section 2 "Preparazione
+ *   Offline".
+ *   w [N*K] fp32 or bf16, wq [N*K] int8 out, sw [N] fp32 out; 1 <= N.
+ * The kernel it launches lets no successor start before it has finished.
+ */
+QV_API qv_status qv_quantize_weight(const void* w, qv_dtype w_dtype, int N, int K,
+                             int8_t* wq, float* sw, cudaStream_t stream);
+
+/*
+ * qv_bf16_linear -- the high-precision verifier being replaced, as a traffic
+ * comparator: y = x w^T with bf16 operands and fp32 accumulation.
+ *   The verify pass "in full precision (BF16)" whose weight traffic the
+ *   method halves: gist.science/ja summary, sections 2.1 and 2.3;
+ *   gist.science/de summary, section 3 item 4 (T_verify ~ M*2B/BW versus
+ *   M*1B/BW).
+ *   x [M*K] bf16, w [N*K] bf16, y [M*N] fp32 out.
+ *   workspace: qv_workspace_bytes(QV_OP_BF16_LINEAR, M, K, N) bytes, same
+ *   zero-fill contract as qv_w8a8_linear. Partial sums of one output are
+ *   added in an order that may change from call to call, so results may
+ *   differ in the last bits between calls.
+ *   1 <= M <= QV_MAX_M.
+ */
+QV_API qv_status qv_bf16_linear(const uint16_t* x, int M, int K, const uint16_t* w,
+                         int N, float* y, void* workspace,
+                         size_t workspace_bytes, cudaStream_t stream);
+
+/* Workspace bytes an op needs for the given shape (N = V for the LM head);
+ * 0 for an invalid shape. Host function, enqueues nothing. */
+QV_API size_t qv_workspace_bytes(qv_op op, int M, int K, int N);
+
+/* Message for the last non-OK status returned on the calling thread
+ * (thread-local; "" if none). Host function. */
+QV_API const char* qv_last_error(void);
+
+/*
+ * qv_device_error -- reads and clears the library's device-side error word.
+ * Kernels never trap: a wait inside a kernel that exceeds its time limit
+ * (about one second) sets a bit here and the kernel returns early with
+ * undefined outputs. 0 means no such event since the last read.
+ * Synchronizes the current device. Host function.
+ */
+QV_API qv_status qv_device_error(unsigned int* code);
+
+/* Number of SMs the kernels size their grids for on the current device
+ * (queried once per device). Host function. */
+QV_API int qv_num_sms(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QV_H */

@@ -1,0 +1,135 @@
+// k_quant.cu -- per-row symmetric int8 quantization (a1 activations, one row
+// per token; a0 weights, one row per output channel).
+//
+//   Quasar, gist.science/ja summary, section 2.2 "Enhanced SmoothQuant",
+//   items 2-3: weights quantized to INT8 offline; BF16 activations scaled by
+//   the smoothing factor and converted to INT8 online.
+//
+// One CTA per row. Pass 1 reads the row with 16-byte loads and forms
+// amax = max |x * c| (warp shuffles, then one shared-memory step); pass 2
+// re-reads the row (cache-resident) and writes the codes. Every floating
+// point step is a single IEEE operation in round-to-nearest-even:
+//   s = fl(amax / 127), q = clamp(rne(fl(x' / s)), -127, 127), q = 0 if s == 0.
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "qv_internal.h"
+#include "qv_ptx.cuh"
+
+namespace qv {
+namespace {
+
+constexpr int kQuantThreads = 256;
+
+template <bool BF16>
+struct Vec;
+template <>
+struct Vec<true> {       // 8 bf16 per 16-byte load
+    static constexpr int E = 8;
+    static __device__ __forceinline__ void unpack(const uint4& r, float (&e)[8]) {
+        const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            e[2 * j] = __uint_as_float(w[j] << 16);
+            e[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+        }
+    }
+};
+template <>
+struct Vec<false> {      // 4 fp32 per 16-byte load
+    static constexpr int E = 4;
+    static __device__ __forceinline__ void unpack(const uint4& r, float (&e)[4]) {
+        e[0] = __uint_as_float(r.x);
+        e[1] = __uint_as_float(r.y);
+        e[2] = __uint_as_float(r.z);
+        e[3] = __uint_as_float(r.w);
+    }
+};
+
+__device__ __forceinline__ int8_t code_of(float v, float s) {
+    if (s == 0.f) return 0;
+    int q = __float2int_rn(__fdiv_rn(v, s));
+    q = q > 127 ? 127 : (q < -127 ? -127 : q);
+    return (int8_t)q;
+}
+
+template <bool BF16>
+__global__ void __launch_bounds__(kQuantThreads)
+quantize_rows_kernel(const uint8_t* __restrict__ x, int K, const float* __restrict__ mul,
+                     int8_t* __restrict__ q, float* __restrict__ scale, int early_dependents) {
+    using V = Vec<BF16>;
+    constexpr int E = V::E;
+    if (early_dependents) allow_dependent_launch();
+    grid_dependency_wait();
+
+    const int row = blockIdx.x;
+    const int nvec = K / E;
+    const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)row * K * (BF16 ? 2 : 4));
+
+    float amax = 0.f;
+    for (int v = threadIdx.x; v < nvec; v += kQuantThreads) {
+        float e[E];
+        V::unpack(__ldg(xr + v), e);
+#pragma unroll
+        for (int j = 0; j < E; ++j) {
+            const float val = mul ? __fmul_rn(e[j], __ldg(mul + v * E + j)) : e[j];
+            amax = fmaxf(amax, fabsf(val));
+        }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    __shared__ float warp_max[kQuantThreads / 32];
+    if ((threadIdx.x & 31) == 0) warp_max[threadIdx.x >> 5] = amax;
+    __syncthreads();
+    amax = warp_max[0];
+#pragma unroll
+    for (int w = 1; w < kQuantThreads / 32; ++w) amax = fmaxf(amax, warp_max[w]);
+    const float s = __fdiv_rn(amax, 127.0f);
+    if (threadIdx.x == 0) scale[row] = s;
+
+    int8_t* qr = q + (size_t)row * K;
+    for (int v = threadIdx.x; v < nvec; v += kQuantThreads) {
+        float e[E];
+        V::unpack(__ldg(xr + v), e);
+        uint32_t packed[E / 4];
+#pragma unroll
+        for (int w = 0; w < E / 4; ++w) {
+            uint32_t word = 0;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int idx = 4 * w + j;
+                const float val = mul ? __fmul_rn(e[idx], __ldg(mul + v * E + idx)) : e[idx];
+                word |= (uint32_t)(uint8_t)code_of(val, s) << (8 * j);
+            }
+            packed[w] = word;
+        }
+        if constexpr (E == 8)
+            *reinterpret_cast<uint2*>(qr + v * 8) = make_uint2(packed[0], packed[1]);
+        else
+            *reinterpret_cast<uint32_t*>(qr + v * 4) = packed[0];
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_quantize_rows(const void* x, bool bf16, int rows, int K, const float* mul,
+                                 int8_t* q, float* scale, bool early_dependents, cudaStream_t s) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(rows);
+    cfg.blockDim = dim3(kQuantThreads);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const uint8_t* xb = static_cast<const uint8_t*>(x);
+    const int early = early_dependents ? 1 : 0;
+    if (bf16) return cudaLaunchKernelEx(&cfg, quantize_rows_kernel<true>, xb, K, mul, q, scale, early);
+    return cudaLaunchKernelEx(&cfg, quantize_rows_kernel<false>, xb, K, mul, q, scale, early);
+}
+
+}  // namespace qv

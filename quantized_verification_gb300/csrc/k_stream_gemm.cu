@@ -1,0 +1,680 @@
+// k_stream_gemm.cu -- weight-streaming GEMMs for skinny M on sm_103a.
+//
+//  * w8a8_stream_kernel: y = dequant(xq . wq^T) (qv_w8a8_linear) and the LM
+//    head fused with the greedy argmax (qv_lm_head_argmax).
+//      Quasar, gist.science/ja summary, section 2.2 item 3 (INT8 GEMM with
+//      INT32 accumulation, dequantization to high precision);
+//      gist.science/it summary, section 2 item 3 (logits kept precise for
+//      the acceptance test).
+//  * bf16_stream_kernel: the BF16-weight verifier used as the traffic
+//    comparator (gist.science/ja summary, section 2.3; gist.science/de
+//    summary, section 3 item 4).
+//
+// Design (both kernels):
+//  - The weight matrix [N][K] is cut into tiles of 128 output channels x 128
+//    bytes of K. Tiles are ordered channel-tile major, K minor, and each CTA
+//    takes one contiguous, equally sized range of that order (stream-K), so
+//    every SM streams the same number of bytes whatever N and K are.
+//  - One producer thread moves tiles with 2-D TMA (128-byte swizzle) into a
+//    ring of shared-memory stages guarded by mbarriers. The activation slice
+//    of the same K range (M rows padded to MP, out-of-range rows zero-filled
+//    by TMA) travels with each weight tile.
+//  - Four consumer warps each own 32 output channels of a tile and run
+//    m16n8k16 mma.sync with the output channels as the MMA's M and the
+//    tokens as its N (token count padded to a multiple of 8).
+//  - W8A8: int8 codes are widened exactly to binary16 in registers. Products
+//    are at most 128^2 = 2^14, one tile sums 128 of them (|sum| <= 2^21),
+//    so every fp32 partial is an exact integer; after each tile the fp32
+//    partials are converted to int32 (exact) and added in int32.
+//  - A channel tile whose K range is split over CTAs is combined with int32
+//    atomic adds into the workspace (exact, so order does not matter); the
+//    CTA whose contribution completes the tile runs the epilogue, reading and
+//    zeroing the sums in one atomic exchange, so the workspace is left zeroed.
+//    No CTA ever waits for another.
+//  - The LM head reduces each finished channel tile to one 64-bit key per
+//    token, (order-preserving bits of y) << 32 | (0xFFFFFFFF - v), combined
+//    with atomicMax: the largest key is the largest logit and, among equal
+//    logits, the lowest index. The last tile to finish decodes the keys.
+//  - Programmatic dependent launch: weight tiles (never written by the
+//    preceding kernels of this library) are requested before waiting for the
+//    preceding kernel; activations, scales and workspace only afterwards.
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "qv_internal.h"
+#include "qv_ptx.cuh"
+
+namespace qv {
+
+__device__ unsigned int g_stream_gemm_error;
+
+namespace {
+
+constexpr int BN = kTileN;            // output channels per tile
+constexpr int BKB = kTileKBytes;      // bytes of K per tile (one 128-byte row)
+constexpr int kConsumerWarps = 4;
+constexpr int kConsumerThreads = kConsumerWarps * 32;
+constexpr int kThreads = kConsumerThreads + 32;   // + one producer warp
+constexpr int kWTileBytes = BN * BKB;             // 16 KB
+
+template <int NG>
+struct Cfg {
+    static constexpr int MP = 8 * NG;                        // padded tokens
+    static constexpr int XBytes = MP * BKB;                  // activation slice
+    static constexpr int XSlot = ((XBytes + 1023) / 1024) * 1024;
+    static constexpr int StageBytes = kWTileBytes + XSlot;
+    static constexpr int Stages = NG == 1 ? 6 : NG == 2 ? 6 : NG == 4 ? 5 : 4;
+    static constexpr int StgWords = BN * MP;                 // epilogue staging
+    static constexpr int SmemBytes =
+        1024 /*alignment slack*/ + Stages * StageBytes + StgWords * 4 +
+        2 * Stages * 8 + kConsumerWarps * MP * 8 + MP * 4 + 64;
+};
+
+__device__ __forceinline__ void consumer_sync() {
+    asm volatile("bar.sync 1, %0;" :: "n"(kConsumerThreads) : "memory");
+}
+
+// Order-preserving map of a float to uint32 (larger float -> larger key);
+// -0 is folded onto +0 first.
+__device__ __forceinline__ uint32_t ordered_bits(float f) {
+    uint32_t u = __float_as_uint(f);
+    if (u == 0x80000000u) u = 0u;
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float unordered_bits(uint32_t o) {
+    uint32_t u = (o & 0x80000000u) ? (o & 0x7FFFFFFFu) : ~o;
+    return __uint_as_float(u);
+}
+
+__device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long v) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        unsigned long long o = __shfl_xor_sync(0xffffffffu, v, off);
+        v = o > v ? o : v;
+    }
+    return v;
+}
+
+// Shared-memory carve-up common to both kernels.
+template <int Stages, int StageBytes, int StgWords, int MP>
+struct Smem {
+    uint8_t* stages;          // Stages x StageBytes, 1024-aligned
+    int32_t* stg;             // BN x MP staging words
+    uint64_t* full;
+    uint64_t* empty;
+    unsigned long long* red;  // kConsumerWarps x MP
+    float* sx;                // MP
+    volatile int* abort;
+    volatile int* flag;
+
+    __device__ __forceinline__ explicit Smem(uint8_t* raw) {
+        uintptr_t base = (reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023);
+        uint8_t* p = reinterpret_cast<uint8_t*>(base);
+        stages = p;
+        p += Stages * StageBytes;
+        stg = reinterpret_cast<int32_t*>(p);
+        p += StgWords * 4;
+        full = reinterpret_cast<uint64_t*>(p);
+        p += Stages * 8;
+        empty = reinterpret_cast<uint64_t*>(p);
+        p += Stages * 8;
+        red = reinterpret_cast<unsigned long long*>(p);
+        p += kConsumerWarps * MP * 8;
+        sx = reinterpret_cast<float*>(p);
+        p += MP * 4;
+        abort = reinterpret_cast<volatile int*>(p);
+        flag = reinterpret_cast<volatile int*>(p + 4);
+    }
+    __device__ __forceinline__ uint8_t* w_tile(int s) { return stages + s * StageBytes; }
+    __device__ __forceinline__ uint8_t* x_tile(int s) { return stages + s * StageBytes + kWTileBytes; }
+};
+
+// Producer: stream tiles [a, b) into the ring. Weight tiles of the first
+// ring fill are requested before the grid dependency wait.
+template <int Stages, class SM>
+__device__ __forceinline__ void produce(SM& sm, const CUtensorMap* tw, const CUtensorMap* tx,
+                                        int a, int b, int KT, int kx_elems_per_tile,
+                                        unsigned tx_bytes) {
+    prefetch_tensormap(tw);
+    prefetch_tensormap(tx);
+    const uint64_t pol_w = policy_evict_first();
+    const uint64_t pol_x = policy_evict_last();
+    const int n = b - a;
+    const int pre = n < Stages ? n : Stages;
+    for (int j = 0; j < pre; ++j) {
+        const int tile = a + j, nt = tile / KT, kt = tile - nt * KT;
+        mbar_arrive_expect_tx(&sm.full[j], tx_bytes);
+        tma_load_2d(sm.w_tile(j), tw, kt * kx_elems_per_tile, nt * BN, &sm.full[j], pol_w);
+    }
+    grid_dependency_wait();
+    for (int j = 0; j < pre; ++j) {
+        const int tile = a + j, kt = tile % KT;
+        tma_load_2d(sm.x_tile(j), tx, kt * kx_elems_per_tile, 0, &sm.full[j], pol_x);
+    }
+    int issued = pre;
+    int s = pre % Stages;
+    int round = pre / Stages;
+    for (int j = pre; j < n; ++j) {
+        if (!mbar_wait_bounded(&sm.empty[s], (round - 1) & 1, sm.abort)) {
+            atomicOr(&g_stream_gemm_error, kErrEmptyWait);
+            break;
+        }
+        const int tile = a + j, nt = tile / KT, kt = tile - nt * KT;
+        mbar_arrive_expect_tx(&sm.full[s], tx_bytes);
+        tma_load_2d(sm.w_tile(s), tw, kt * kx_elems_per_tile, nt * BN, &sm.full[s], pol_w);
+        tma_load_2d(sm.x_tile(s), tx, kt * kx_elems_per_tile, 0, &sm.full[s], pol_x);
+        ++issued;
+        if (++s == Stages) { s = 0; ++round; }
+    }
+    // Do not leave the CTA while copies into its shared memory are in flight.
+    const int first = issued > Stages ? issued - Stages : 0;
+    for (int j = first; j < issued; ++j) {
+        const int st = j % Stages, par = (j / Stages) & 1;
+        if (mbar_try_wait(&sm.full[st], par)) continue;
+        unsigned long long t0 = global_timer_ns();
+        while (!mbar_try_wait(&sm.full[st], par)) {
+            if (global_timer_ns() - t0 > kWaitLimitNs) {
+                atomicOr(&g_stream_gemm_error, kErrDrainWait);
+                return;
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// W8A8 kernel
+// ---------------------------------------------------------------------------
+struct W8A8Params {
+    int M, N, K, KT, NT;
+    long long T;
+    const float* sx;
+    const float* sw;
+    void* y;
+    int y_bf16;
+    int32_t* acc_debug;
+    int32_t* tokens;
+    float* max_logit;
+    int32_t* ws_acc;
+    unsigned* ws_cnt;
+    unsigned long long* keys;
+    unsigned* done;
+};
+
+template <int NG, int EPI>
+__global__ void __launch_bounds__(kThreads, 1)
+w8a8_stream_kernel(const __grid_constant__ CUtensorMap tmap_w,
+                   const __grid_constant__ CUtensorMap tmap_x, const W8A8Params p) {
+    using C = Cfg<NG>;
+    constexpr int MP = C::MP;
+    constexpr int Stages = C::Stages;
+    extern __shared__ uint8_t smem_raw[];
+    Smem<Stages, C::StageBytes, C::StgWords, MP> sm(smem_raw);
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const long long G = gridDim.x;
+    const int a = (int)((long long)blockIdx.x * p.T / G);
+    const int b = (int)((long long)(blockIdx.x + 1) * p.T / G);
+
+    if (tid == 0) {
+        for (int s = 0; s < Stages; ++s) {
+            mbar_init(&sm.full[s], 1);
+            mbar_init(&sm.empty[s], kConsumerWarps);
+        }
+        *sm.abort = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+    allow_dependent_launch();
+
+    if (warp == kConsumerWarps) {
+        if (lane == 0)
+            produce<Stages>(sm, &tmap_w, &tmap_x, a, b, p.KT, BKB,
+                            (unsigned)(kWTileBytes + C::XBytes));
+        return;
+    }
+
+    // ---------------- consumers ----------------
+    grid_dependency_wait();
+    if (tid < MP) sm.sx[tid] = tid < p.M ? p.sx[tid] : 0.f;
+    consumer_sync();
+
+    const int li = lane & 7, lj = lane >> 3;
+    const int g = lane >> 2, t4 = lane & 3;
+    // ldmatrix lane offsets: weight rows of the two 16-row blocks, and the
+    // swizzled chunk positions (128-byte swizzle: chunk ^= row % 8).
+    uint32_t w_row_off[2];
+#pragma unroll
+    for (int blk = 0; blk < 2; ++blk)
+        w_row_off[blk] = (uint32_t)((32 * warp + 16 * blk + li + 8 * (lj & 1)) * BKB);
+    uint32_t w_chunk_off[4];
+#pragma unroll
+    for (int cp = 0; cp < 4; ++cp)
+        w_chunk_off[cp] = (uint32_t)((((2 * cp) + (lj >> 1)) ^ li) << 4);
+    uint32_t x_chunk_off[2];
+#pragma unroll
+    for (int cq = 0; cq < 2; ++cq) x_chunk_off[cq] = (uint32_t)(((4 * cq + lj) ^ li) << 4);
+
+    int32_t acci[2][NG][4];
+    int s = 0, phase = 0;
+    int i = a;
+    while (i < b) {
+        const int nt = i / p.KT;
+        const int seg_begin = i;
+        const int seg_end = min(b, (nt + 1) * p.KT);
+#pragma unroll
+        for (int blk = 0; blk < 2; ++blk)
+#pragma unroll
+            for (int gr = 0; gr < NG; ++gr)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) acci[blk][gr][e] = 0;
+
+        for (; i < seg_end; ++i) {
+            if (!mbar_wait_bounded(&sm.full[s], phase, sm.abort))
+                atomicOr(&g_stream_gemm_error, kErrFullWait);
+            const uint32_t wb = smem_u32(sm.w_tile(s));
+            const uint32_t xb = smem_u32(sm.x_tile(s));
+            float accf[2][NG][4];
+#pragma unroll
+            for (int blk = 0; blk < 2; ++blk)
+#pragma unroll
+                for (int gr = 0; gr < NG; ++gr)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) accf[blk][gr][e] = 0.f;
+
+#pragma unroll
+            for (int cq = 0; cq < 2; ++cq) {
+                // B fragments (tokens) for the four chunks 4cq .. 4cq+3.
+                uint32_t bx[NG][4][2];
+#pragma unroll
+                for (int gr = 0; gr < NG; ++gr) {
+                    uint32_t r[4];
+                    ldmatrix_x4(xb + (uint32_t)((8 * gr + li) * BKB) + x_chunk_off[cq],
+                                r[0], r[1], r[2], r[3]);
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) widen_i8x4_f16(r[c], bx[gr][c][0], bx[gr][c][1]);
+                }
+#pragma unroll
+                for (int blk = 0; blk < 2; ++blk) {
+#pragma unroll
+                    for (int cp = 0; cp < 2; ++cp) {
+                        uint32_t r0, r1, r2, r3;
+                        ldmatrix_x4(wb + w_row_off[blk] + w_chunk_off[2 * cq + cp], r0, r1, r2, r3);
+                        uint32_t a0l, a0h, a1l, a1h;
+                        widen_i8x4_f16(r0, a0l, a0h);   // row g,   chunk c
+                        widen_i8x4_f16(r1, a1l, a1h);   // row g+8, chunk c
+#pragma unroll
+                        for (int gr = 0; gr < NG; ++gr)
+                            mma_f16_16816(accf[blk][gr], a0l, a1l, a0h, a1h,
+                                          bx[gr][2 * cp][0], bx[gr][2 * cp][1]);
+                        widen_i8x4_f16(r2, a0l, a0h);   // row g,   chunk c+1
+                        widen_i8x4_f16(r3, a1l, a1h);   // row g+8, chunk c+1
+#pragma unroll
+                        for (int gr = 0; gr < NG; ++gr)
+                            mma_f16_16816(accf[blk][gr], a0l, a1l, a0h, a1h,
+                                          bx[gr][2 * cp + 1][0], bx[gr][2 * cp + 1][1]);
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.empty[s]);
+            if (++s == Stages) { s = 0; phase ^= 1; }
+#pragma unroll
+            for (int blk = 0; blk < 2; ++blk)
+#pragma unroll
+                for (int gr = 0; gr < NG; ++gr)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) acci[blk][gr][e] += __float2int_rn(accf[blk][gr][e]);
+        }
+
+        // -------- segment end: stage the int32 sums [row][token] --------
+#pragma unroll
+        for (int blk = 0; blk < 2; ++blk) {
+            const int r0 = 32 * warp + 16 * blk + g;
+#pragma unroll
+            for (int gr = 0; gr < NG; ++gr) {
+                const int col = 8 * gr + 2 * t4;
+                *reinterpret_cast<int2*>(&sm.stg[r0 * MP + col]) = make_int2(acci[blk][gr][0], acci[blk][gr][1]);
+                *reinterpret_cast<int2*>(&sm.stg[(r0 + 8) * MP + col]) = make_int2(acci[blk][gr][2], acci[blk][gr][3]);
+            }
+        }
+        consumer_sync();
+
+        const int seg_len = seg_end - seg_begin;
+        const bool whole = seg_len == p.KT;
+        int32_t* gacc = p.ws_acc + (size_t)nt * BN * MP;
+        if (!whole) {
+            for (int e = tid; e < BN * MP; e += kConsumerThreads) {
+                const int r = e / MP, m = e - (e / MP) * MP;
+                if (m < p.M && nt * BN + r < p.N) atomicAdd(&gacc[e], sm.stg[e]);
+            }
+            __threadfence();
+            consumer_sync();
+            if (tid == 0) {
+                __threadfence();
+                const unsigned prev = atomicAdd(&p.ws_cnt[nt], (unsigned)seg_len);
+                *sm.flag = (prev + (unsigned)seg_len == (unsigned)p.KT) ? 1 : 0;
+            }
+            consumer_sync();
+        }
+        const bool finisher = whole || *sm.flag;
+        if (finisher) {
+            if (!whole) __threadfence();
+            const int r = tid;                 // one output channel per thread
+            const int n = nt * BN + r;
+            const bool valid = n < p.N;
+            const float swn = valid ? p.sw[n] : 0.f;
+            if (EPI == (int)Epi::Linear) {
+                if (valid) {
+                    for (int m = 0; m < p.M; ++m) {
+                        const int32_t acc = whole ? sm.stg[r * MP + m] : atomicExch(&gacc[r * MP + m], 0);
+                        if (p.acc_debug) p.acc_debug[(size_t)m * p.N + n] = acc;
+                        const float yv = __fmul_rn(__int2float_rn(acc), __fmul_rn(sm.sx[m], swn));
+                        if (p.y_bf16)
+                            reinterpret_cast<__nv_bfloat16*>(p.y)[(size_t)m * p.N + n] = __float2bfloat16_rn(yv);
+                        else
+                            reinterpret_cast<float*>(p.y)[(size_t)m * p.N + n] = yv;
+                    }
+                }
+            } else {
+                for (int m = 0; m < p.M; ++m) {
+                    unsigned long long key = 0ull;
+                    if (valid) {
+                        const int32_t acc = whole ? sm.stg[r * MP + m] : atomicExch(&gacc[r * MP + m], 0);
+                        const float yv = __fmul_rn(__int2float_rn(acc), __fmul_rn(sm.sx[m], swn));
+                        key = ((unsigned long long)ordered_bits(yv) << 32) |
+                              (unsigned long long)(0xFFFFFFFFu - (unsigned)n);
+                    }
+                    key = warp_max_u64(key);
+                    if (lane == 0) sm.red[warp * MP + m] = key;
+                }
+                consumer_sync();
+                if (tid < p.M) {
+                    unsigned long long k = sm.red[tid];
+#pragma unroll
+                    for (int w = 1; w < kConsumerWarps; ++w) {
+                        const unsigned long long o = sm.red[w * MP + tid];
+                        k = o > k ? o : k;
+                    }
+                    atomicMax(&p.keys[tid], k);
+                }
+                __threadfence();
+                consumer_sync();
+                if (tid == 0) {
+                    __threadfence();
+                    const unsigned prev = atomicAdd(p.done, 1u);
+                    *sm.flag = (prev + 1u == (unsigned)p.NT) ? 2 : 0;
+                }
+                consumer_sync();
+                if (*sm.flag == 2) {
+                    __threadfence();
+                    if (tid < p.M) {
+                        const unsigned long long k = atomicExch(&p.keys[tid], 0ull);
+                        p.tokens[tid] = (int32_t)(0xFFFFFFFFu - (unsigned)(k & 0xFFFFFFFFull));
+                        if (p.max_logit) p.max_logit[tid] = unordered_bits((unsigned)(k >> 32));
+                    }
+                    if (tid == 0) atomicExch(p.done, 0u);
+                }
+            }
+            if (!whole && tid == 0) atomicExch(&p.ws_cnt[nt], 0u);
+        }
+        consumer_sync();   // staging buffer and flags are reused by the next segment
+    }
+}
+
+// ---------------------------------------------------------------------------
+// BF16 comparator kernel: same pipeline, bf16 operands, fp32 accumulation.
+// A tile holds 128 channels x 64 bf16 (128 bytes) of K.
+// ---------------------------------------------------------------------------
+struct Bf16Params {
+    int M, N, K, KT, NT;
+    long long T;
+    float* y;
+    float* ws_acc;
+    unsigned* ws_cnt;
+};
+
+template <int NG>
+__global__ void __launch_bounds__(kThreads, 1)
+bf16_stream_kernel(const __grid_constant__ CUtensorMap tmap_w,
+                   const __grid_constant__ CUtensorMap tmap_x, const Bf16Params p) {
+    using C = Cfg<NG>;
+    constexpr int MP = C::MP;
+    constexpr int Stages = C::Stages;
+    extern __shared__ uint8_t smem_raw[];
+    Smem<Stages, C::StageBytes, C::StgWords, MP> sm(smem_raw);
+    float* stgf = reinterpret_cast<float*>(sm.stg);
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const long long G = gridDim.x;
+    const int a = (int)((long long)blockIdx.x * p.T / G);
+    const int b = (int)((long long)(blockIdx.x + 1) * p.T / G);
+
+    if (tid == 0) {
+        for (int s = 0; s < Stages; ++s) {
+            mbar_init(&sm.full[s], 1);
+            mbar_init(&sm.empty[s], kConsumerWarps);
+        }
+        *sm.abort = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+    allow_dependent_launch();
+
+    if (warp == kConsumerWarps) {
+        if (lane == 0)
+            produce<Stages>(sm, &tmap_w, &tmap_x, a, b, p.KT, BKB / 2,
+                            (unsigned)(kWTileBytes + C::XBytes));
+        return;
+    }
+    grid_dependency_wait();
+
+    const int li = lane & 7, lj = lane >> 3;
+    const int g = lane >> 2, t4 = lane & 3;
+    uint32_t w_row_off[2];
+#pragma unroll
+    for (int blk = 0; blk < 2; ++blk)
+        w_row_off[blk] = (uint32_t)((32 * warp + 16 * blk + li + 8 * (lj & 1)) * BKB);
+    uint32_t w_chunk_off[4];
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks) w_chunk_off[ks] = (uint32_t)((((2 * ks) + (lj >> 1)) ^ li) << 4);
+    uint32_t x_chunk_off[2];
+#pragma unroll
+    for (int cq = 0; cq < 2; ++cq) x_chunk_off[cq] = (uint32_t)(((4 * cq + lj) ^ li) << 4);
+
+    float acc[2][NG][4];
+    int s = 0, phase = 0;
+    int i = a;
+    while (i < b) {
+        const int nt = i / p.KT;
+        const int seg_begin = i;
+        const int seg_end = min(b, (nt + 1) * p.KT);
+#pragma unroll
+        for (int blk = 0; blk < 2; ++blk)
+#pragma unroll
+            for (int gr = 0; gr < NG; ++gr)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) acc[blk][gr][e] = 0.f;
+
+        for (; i < seg_end; ++i) {
+            if (!mbar_wait_bounded(&sm.full[s], phase, sm.abort))
+                atomicOr(&g_stream_gemm_error, kErrFullWait);
+            const uint32_t wb = smem_u32(sm.w_tile(s));
+            const uint32_t xb = smem_u32(sm.x_tile(s));
+#pragma unroll
+            for (int cq = 0; cq < 2; ++cq) {
+                // x chunks 4cq..4cq+3 = k-steps 2cq (chunks 0,1) and 2cq+1 (chunks 2,3)
+                uint32_t bx[NG][4];
+#pragma unroll
+                for (int gr = 0; gr < NG; ++gr)
+                    ldmatrix_x4(xb + (uint32_t)((8 * gr + li) * BKB) + x_chunk_off[cq],
+                                bx[gr][0], bx[gr][1], bx[gr][2], bx[gr][3]);
+#pragma unroll
+                for (int blk = 0; blk < 2; ++blk) {
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int ks = 2 * cq + h;
+                        uint32_t r0, r1, r2, r3;
+                        ldmatrix_x4(wb + w_row_off[blk] + w_chunk_off[ks], r0, r1, r2, r3);
+#pragma unroll
+                        for (int gr = 0; gr < NG; ++gr)
+                            mma_bf16_16816(acc[blk][gr], r0, r1, r2, r3, bx[gr][2 * h], bx[gr][2 * h + 1]);
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.empty[s]);
+            if (++s == Stages) { s = 0; phase ^= 1; }
+        }
+
+#pragma unroll
+        for (int blk = 0; blk < 2; ++blk) {
+            const int r0 = 32 * warp + 16 * blk + g;
+#pragma unroll
+            for (int gr = 0; gr < NG; ++gr) {
+                const int col = 8 * gr + 2 * t4;
+                *reinterpret_cast<float2*>(&stgf[r0 * MP + col]) = make_float2(acc[blk][gr][0], acc[blk][gr][1]);
+                *reinterpret_cast<float2*>(&stgf[(r0 + 8) * MP + col]) = make_float2(acc[blk][gr][2], acc[blk][gr][3]);
+            }
+        }
+        consumer_sync();
+        const int seg_len = seg_end - seg_begin;
+        const bool whole = seg_len == p.KT;
+        float* gacc = p.ws_acc + (size_t)nt * BN * MP;
+        if (!whole) {
+            for (int e = tid; e < BN * MP; e += kConsumerThreads) {
+                const int r = e / MP, m = e - (e / MP) * MP;
+                if (m < p.M && nt * BN + r < p.N) atomicAdd(&gacc[e], stgf[e]);
+            }
+            __threadfence();
+            consumer_sync();
+            if (tid == 0) {
+                __threadfence();
+                const unsigned prev = atomicAdd(&p.ws_cnt[nt], (unsigned)seg_len);
+                *sm.flag = (prev + (unsigned)seg_len == (unsigned)p.KT) ? 1 : 0;
+            }
+            consumer_sync();
+        }
+        if (whole || *sm.flag) {
+            if (!whole) __threadfence();
+            const int r = tid;
+            const int n = nt * BN + r;
+            if (n < p.N) {
+                for (int m = 0; m < p.M; ++m) {
+                    const float v = whole ? stgf[r * MP + m] : atomicExch(&gacc[r * MP + m], 0.f);
+                    p.y[(size_t)m * p.N + n] = v;
+                }
+            }
+            if (!whole && tid == 0) atomicExch(&p.ws_cnt[nt], 0u);
+        }
+        consumer_sync();
+    }
+}
+
+template <class P, class... Args>
+cudaError_t launch_ex(void (*kern)(Args...), int grid, int smem, cudaStream_t s,
+                      const CUtensorMap& tw, const CUtensorMap& tx, const P& params) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, tw, tx, params);
+}
+
+}  // namespace
+
+WsLayout ws_layout(int mp, int n, bool lm_head) {
+    WsLayout L;
+    const int nt = ceil_div(n, BN);
+    auto al16 = [](size_t v) { return (v + 15) & ~size_t(15); };
+    L.acc = 0;
+    size_t off = al16((size_t)nt * BN * mp * 4);
+    L.counters = off;
+    off = al16(off + (size_t)nt * 4);
+    L.keys = off;
+    if (lm_head) off = al16(off + (size_t)mp * 8);
+    L.done = off;
+    if (lm_head) off = al16(off + 4);
+    L.total = off;
+    return L;
+}
+
+cudaError_t launch_w8a8_stream(const W8A8Launch& a, int num_sms, cudaStream_t s) {
+    const int NG = a.MP / 8;
+    const bool lm = a.epi == Epi::LmHead;
+    WsLayout L = ws_layout(a.MP, a.N, lm);
+    W8A8Params p;
+    p.M = a.M; p.N = a.N; p.K = a.K;
+    p.KT = ceil_div(a.K, BKB);
+    p.NT = ceil_div(a.N, BN);
+    p.T = (long long)p.KT * p.NT;
+    p.sx = a.sx; p.sw = a.sw; p.y = a.y; p.y_bf16 = a.y_bf16; p.acc_debug = a.acc_debug;
+    p.tokens = a.tokens; p.max_logit = a.max_logit;
+    uint8_t* ws = static_cast<uint8_t*>(a.ws);
+    p.ws_acc = reinterpret_cast<int32_t*>(ws + L.acc);
+    p.ws_cnt = reinterpret_cast<unsigned*>(ws + L.counters);
+    p.keys = reinterpret_cast<unsigned long long*>(ws + L.keys);
+    p.done = reinterpret_cast<unsigned*>(ws + L.done);
+    const int grid = (int)(p.T < num_sms ? p.T : num_sms);
+#define QV_W8A8_CASE(NGV)                                                                    \
+    case NGV:                                                                                \
+        return lm ? launch_ex(w8a8_stream_kernel<NGV, (int)Epi::LmHead>, grid,               \
+                              Cfg<NGV>::SmemBytes, s, a.tmap_w, a.tmap_x, p)                 \
+                  : launch_ex(w8a8_stream_kernel<NGV, (int)Epi::Linear>, grid,               \
+                              Cfg<NGV>::SmemBytes, s, a.tmap_w, a.tmap_x, p);
+    switch (NG) {
+        QV_W8A8_CASE(1)
+        QV_W8A8_CASE(2)
+        QV_W8A8_CASE(4)
+        QV_W8A8_CASE(8)
+        default: return cudaErrorInvalidValue;
+    }
+#undef QV_W8A8_CASE
+}
+
+cudaError_t launch_bf16_stream(const Bf16Launch& a, int num_sms, cudaStream_t s) {
+    const int NG = a.MP / 8;
+    WsLayout L = ws_layout(a.MP, a.N, false);
+    Bf16Params p;
+    p.M = a.M; p.N = a.N; p.K = a.K;
+    p.KT = ceil_div(a.K, BKB / 2);
+    p.NT = ceil_div(a.N, BN);
+    p.T = (long long)p.KT * p.NT;
+    p.y = a.y;
+    uint8_t* ws = static_cast<uint8_t*>(a.ws);
+    p.ws_acc = reinterpret_cast<float*>(ws + L.acc);
+    p.ws_cnt = reinterpret_cast<unsigned*>(ws + L.counters);
+    const int grid = (int)(p.T < num_sms ? p.T : num_sms);
+#define QV_BF16_CASE(NGV) \
+    case NGV: return launch_ex(bf16_stream_kernel<NGV>, grid, Cfg<NGV>::SmemBytes, s, a.tmap_w, a.tmap_x, p);
+    switch (NG) {
+        QV_BF16_CASE(1)
+        QV_BF16_CASE(2)
+        QV_BF16_CASE(4)
+        QV_BF16_CASE(8)
+        default: return cudaErrorInvalidValue;
+    }
+#undef QV_BF16_CASE
+}
+
+cudaError_t read_and_clear_stream_gemm_error(unsigned* code) {
+    unsigned zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(code, g_stream_gemm_error, sizeof(unsigned));
+    if (e != cudaSuccess) return e;
+    return cudaMemcpyToSymbol(g_stream_gemm_error, &zero, sizeof(unsigned));
+}
+
+}  // namespace qv

@@ -1,0 +1,344 @@
+// qv_abi.cu -- the C ABI of libqv (declared in include/qv.h): argument
+// validation, TMA descriptor encoding and dispatch to the kernels. Every
+// check happens before anything is enqueued, so a rejected call leaves all
+// outputs untouched.
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <mutex>
+
+#include "../../include/qv.h"
+#include "qv_internal.h"
+
+namespace {
+
+thread_local char g_last_error[512] = "";
+
+qv_status fail(qv_status st, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+qv_status ok() {
+    g_last_error[0] = '\0';
+    return QV_OK;
+}
+
+qv_status cuda_fail(cudaError_t e, const char* what) {
+    return fail(QV_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Every buffer a kernel touches must be device (or managed) memory of the
+// current device: a host pointer handed to a kernel would fault the GPU.
+qv_status check_dev(const void* p, const char* name) {
+    if (!p) return QV_OK;   // optional buffers; required ones are checked for null first
+    cudaPointerAttributes at;
+    cudaError_t e = cudaPointerGetAttributes(&at, p);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(QV_ERR_INVALID_ARG, "%s: not a CUDA allocation (%s)", name, cudaGetErrorName(e));
+    }
+    if (at.type != cudaMemoryTypeDevice && at.type != cudaMemoryTypeManaged)
+        return fail(QV_ERR_INVALID_ARG, "%s: not device memory", name);
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || at.device != dev)
+        return fail(QV_ERR_INVALID_ARG, "%s: memory of device %d, current device is %d", name, at.device, dev);
+    return QV_OK;
+}
+
+#define QV_CHECK_DEV(p)                                   \
+    do {                                                  \
+        qv_status st_ = check_dev((p), #p);               \
+        if (st_ != QV_OK) return st_;                     \
+    } while (0)
+
+// ------------------------------------------------------------------ device info
+constexpr int kMaxDevices = 64;
+int g_sms[kMaxDevices] = {0};
+std::mutex g_mu;
+
+int sms_of_current_device(cudaError_t* err) {
+    int dev = 0;
+    *err = cudaGetDevice(&dev);
+    if (*err != cudaSuccess) return 0;
+    if (dev >= 0 && dev < kMaxDevices && g_sms[dev] > 0) return g_sms[dev];
+    int n = 0;
+    *err = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (*err != cudaSuccess) return 0;
+    if (dev >= 0 && dev < kMaxDevices) g_sms[dev] = n;
+    return n;
+}
+
+// ------------------------------------------------------------------ TMA descriptors
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+qv_status get_encoder() {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_encode) return QV_OK;
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                     cudaEnableDefault, &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
+        return fail(QV_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    return QV_OK;
+}
+
+// Row-major [rows][inner] matrix with a 128-byte swizzled box of
+// box_inner x box_rows elements; out-of-range elements read as zero.
+qv_status encode_2d(CUtensorMap* map, CUtensorMapDataType dt, size_t elem_bytes, const void* base,
+                    uint64_t inner, uint64_t rows, uint32_t box_inner, uint32_t box_rows) {
+    qv_status st = get_encoder();
+    if (st != QV_OK) return st;
+    const cuuint64_t dims[2] = {inner, rows};
+    const cuuint64_t strides[1] = {inner * elem_bytes};
+    const cuuint32_t box[2] = {box_inner, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(QV_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
+    return QV_OK;
+}
+
+// Padded token count of one streaming-GEMM launch for Mc rows: 8, 16, 32 or 64.
+int mp_for(int mc) {
+    const int p = qv::pad_tokens(mc);
+    return p <= 8 ? 8 : p <= 16 ? 16 : p <= 32 ? 32 : 64;
+}
+
+qv_status check_k(int K) {
+    if (K < 16 || K % 16 != 0 || K > QV_MAX_K)
+        return fail(QV_ERR_INVALID_ARG, "K=%d must be a positive multiple of 16 and <= %d", K, QV_MAX_K);
+    return QV_OK;
+}
+
+qv_status check_gemm_common(const void* xq, const void* sx, int M, int K, const void* wq,
+                            const void* sw, int N, const void* ws, size_t ws_bytes, qv_op op) {
+    if (!xq || !sx || !wq || !sw) return fail(QV_ERR_INVALID_ARG, "null input pointer");
+    if (M < 1 || M > QV_MAX_M) return fail(QV_ERR_INVALID_ARG, "M=%d outside [1, %d]", M, QV_MAX_M);
+    if (N < 1) return fail(QV_ERR_INVALID_ARG, "N=%d must be >= 1", N);
+    qv_status st = check_k(K);
+    if (st != QV_OK) return st;
+    if (!aligned(xq, 16) || !aligned(wq, 16)) return fail(QV_ERR_INVALID_ARG, "xq and wq must be 16-byte aligned");
+    if (!aligned(sx, 4) || !aligned(sw, 4)) return fail(QV_ERR_INVALID_ARG, "sx and sw must be 4-byte aligned");
+    const size_t need = qv_workspace_bytes(op, M, K, N);
+    if (!ws) return fail(QV_ERR_WORKSPACE, "workspace is null (%zu bytes needed)", need);
+    if (!aligned(ws, 16)) return fail(QV_ERR_WORKSPACE, "workspace must be 16-byte aligned");
+    if (ws_bytes < need) return fail(QV_ERR_WORKSPACE, "workspace has %zu bytes, %zu needed", ws_bytes, need);
+    QV_CHECK_DEV(xq);
+    QV_CHECK_DEV(sx);
+    QV_CHECK_DEV(wq);
+    QV_CHECK_DEV(sw);
+    QV_CHECK_DEV(ws);
+    return QV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* qv_last_error(void) { return g_last_error; }
+
+int qv_num_sms(void) {
+    cudaError_t e;
+    const int n = sms_of_current_device(&e);
+    return e == cudaSuccess ? n : 0;
+}
+
+size_t qv_workspace_bytes(qv_op op, int M, int K, int N) {
+    if (M < 1 || M > QV_MAX_M || N < 1 || K < 16 || K % 16 != 0 || K > QV_MAX_K) return 0;
+    const int mp = mp_for(M < qv::kMaxMPerLaunch ? M : qv::kMaxMPerLaunch);
+    switch (op) {
+        case QV_OP_LINEAR: return qv::ws_layout(mp, N, false).total;
+        case QV_OP_LM_HEAD: return qv::ws_layout(mp, N, true).total;
+        case QV_OP_BF16_LINEAR: return qv::ws_layout(mp, N, false).total;
+    }
+    return 0;
+}
+
+qv_status qv_quantize_act(const void* x, qv_dtype x_dtype, int M, int K, const float* act_mul,
+                          int8_t* xq, float* sx, cudaStream_t stream) {
+    if (!x || !xq || !sx) return fail(QV_ERR_INVALID_ARG, "null pointer");
+    if (x_dtype != QV_F32 && x_dtype != QV_BF16) return fail(QV_ERR_INVALID_ARG, "x_dtype must be QV_F32 or QV_BF16");
+    if (M < 1 || M > 65535) return fail(QV_ERR_INVALID_ARG, "M=%d outside [1, 65535]", M);
+    qv_status st = check_k(K);
+    if (st != QV_OK) return st;
+    if (!aligned(x, 16) || !aligned(xq, 16)) return fail(QV_ERR_INVALID_ARG, "x and xq must be 16-byte aligned");
+    if (!aligned(sx, 4) || (act_mul && !aligned(act_mul, 4))) return fail(QV_ERR_INVALID_ARG, "sx/act_mul must be 4-byte aligned");
+    QV_CHECK_DEV(x);
+    QV_CHECK_DEV(act_mul);
+    QV_CHECK_DEV(xq);
+    QV_CHECK_DEV(sx);
+    cudaError_t e = qv::launch_quantize_rows(x, x_dtype == QV_BF16, M, K, act_mul, xq, sx, true, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "qv_quantize_act launch");
+    return ok();
+}
+
+qv_status qv_quantize_weight(const void* w, qv_dtype w_dtype, int N, int K, int8_t* wq, float* sw,
+                             cudaStream_t stream) {
+    if (!w || !wq || !sw) return fail(QV_ERR_INVALID_ARG, "null pointer");
+    if (w_dtype != QV_F32 && w_dtype != QV_BF16) return fail(QV_ERR_INVALID_ARG, "w_dtype must be QV_F32 or QV_BF16");
+    if (N < 1 || N > 0x7FFFFFFF) return fail(QV_ERR_INVALID_ARG, "N=%d must be >= 1", N);
+    qv_status st = check_k(K);
+    if (st != QV_OK) return st;
+    if (!aligned(w, 16) || !aligned(wq, 16)) return fail(QV_ERR_INVALID_ARG, "w and wq must be 16-byte aligned");
+    if (!aligned(sw, 4)) return fail(QV_ERR_INVALID_ARG, "sw must be 4-byte aligned");
+    QV_CHECK_DEV(w);
+    QV_CHECK_DEV(wq);
+    QV_CHECK_DEV(sw);
+    cudaError_t e = qv::launch_quantize_rows(w, w_dtype == QV_BF16, N, K, nullptr, wq, sw, false, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "qv_quantize_weight launch");
+    return ok();
+}
+
+qv_status qv_w8a8_linear(const int8_t* xq, const float* sx, int M, int K, const int8_t* wq,
+                         const float* sw, int N, void* y, qv_dtype y_dtype, int32_t* acc_debug,
+                         void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    qv_status st = check_gemm_common(xq, sx, M, K, wq, sw, N, workspace, workspace_bytes, QV_OP_LINEAR);
+    if (st != QV_OK) return st;
+    if (!y) return fail(QV_ERR_INVALID_ARG, "y is null");
+    if (y_dtype != QV_F32 && y_dtype != QV_BF16) return fail(QV_ERR_INVALID_ARG, "y_dtype must be QV_F32 or QV_BF16");
+    if (!aligned(y, y_dtype == QV_F32 ? 4 : 2) || (acc_debug && !aligned(acc_debug, 4)))
+        return fail(QV_ERR_INVALID_ARG, "y/acc_debug misaligned");
+    QV_CHECK_DEV(y);
+    QV_CHECK_DEV(acc_debug);
+    cudaError_t e;
+    const int sms = sms_of_current_device(&e);
+    if (e != cudaSuccess) return cuda_fail(e, "device query");
+    qv::W8A8Launch L = {};
+    if ((st = encode_2d(&L.tmap_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, wq, (uint64_t)K, (uint64_t)N,
+                        qv::kTileKBytes, qv::kTileN)) != QV_OK)
+        return st;
+    const size_t ybytes = y_dtype == QV_F32 ? 4 : 2;
+    for (int m0 = 0; m0 < M; m0 += qv::kMaxMPerLaunch) {
+        const int mc = M - m0 < qv::kMaxMPerLaunch ? M - m0 : qv::kMaxMPerLaunch;
+        L.M = mc; L.N = N; L.K = K; L.MP = mp_for(mc);
+        if ((st = encode_2d(&L.tmap_x, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, xq + (size_t)m0 * K,
+                            (uint64_t)K, (uint64_t)mc, qv::kTileKBytes, (uint32_t)L.MP)) != QV_OK)
+            return st;
+        L.sx = sx + m0; L.sw = sw;
+        L.y = static_cast<uint8_t*>(y) + (size_t)m0 * N * ybytes;
+        L.y_bf16 = y_dtype == QV_BF16;
+        L.acc_debug = acc_debug ? acc_debug + (size_t)m0 * N : nullptr;
+        L.tokens = nullptr; L.max_logit = nullptr;
+        L.ws = workspace;
+        L.epi = qv::Epi::Linear;
+        e = qv::launch_w8a8_stream(L, sms, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "qv_w8a8_linear launch");
+    }
+    return ok();
+}
+
+qv_status qv_lm_head_argmax(const int8_t* xq, const float* sx, int M, int K, const int8_t* wq,
+                            const float* sw, int V, int32_t* tokens, float* max_logit,
+                            void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    qv_status st = check_gemm_common(xq, sx, M, K, wq, sw, V, workspace, workspace_bytes, QV_OP_LM_HEAD);
+    if (st != QV_OK) return st;
+    if (!tokens) return fail(QV_ERR_INVALID_ARG, "tokens is null");
+    if (!aligned(tokens, 4) || (max_logit && !aligned(max_logit, 4)))
+        return fail(QV_ERR_INVALID_ARG, "tokens/max_logit misaligned");
+    QV_CHECK_DEV(tokens);
+    QV_CHECK_DEV(max_logit);
+    cudaError_t e;
+    const int sms = sms_of_current_device(&e);
+    if (e != cudaSuccess) return cuda_fail(e, "device query");
+    qv::W8A8Launch L = {};
+    if ((st = encode_2d(&L.tmap_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, wq, (uint64_t)K, (uint64_t)V,
+                        qv::kTileKBytes, qv::kTileN)) != QV_OK)
+        return st;
+    for (int m0 = 0; m0 < M; m0 += qv::kMaxMPerLaunch) {
+        const int mc = M - m0 < qv::kMaxMPerLaunch ? M - m0 : qv::kMaxMPerLaunch;
+        L.M = mc; L.N = V; L.K = K; L.MP = mp_for(mc);
+        if ((st = encode_2d(&L.tmap_x, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, xq + (size_t)m0 * K,
+                            (uint64_t)K, (uint64_t)mc, qv::kTileKBytes, (uint32_t)L.MP)) != QV_OK)
+            return st;
+        L.sx = sx + m0; L.sw = sw;
+        L.y = nullptr; L.y_bf16 = 0; L.acc_debug = nullptr;
+        L.tokens = tokens + m0;
+        L.max_logit = max_logit ? max_logit + m0 : nullptr;
+        L.ws = workspace;
+        L.epi = qv::Epi::LmHead;
+        e = qv::launch_w8a8_stream(L, sms, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "qv_lm_head_argmax launch");
+    }
+    return ok();
+}
+
+qv_status qv_accept(const int32_t* verify_tokens, const int32_t* draft, int B, int gamma,
+                    int32_t* accept_len, int32_t* out_tokens, cudaStream_t stream) {
+    if (!verify_tokens || !accept_len || !out_tokens) return fail(QV_ERR_INVALID_ARG, "null pointer");
+    if (B < 1) return fail(QV_ERR_INVALID_ARG, "B=%d must be >= 1", B);
+    if (gamma < 0 || gamma > 1023) return fail(QV_ERR_INVALID_ARG, "gamma=%d outside [0, 1023]", gamma);
+    if (gamma > 0 && !draft) return fail(QV_ERR_INVALID_ARG, "draft is null with gamma > 0");
+    if (!aligned(verify_tokens, 4) || !aligned(accept_len, 4) || !aligned(out_tokens, 4) ||
+        (draft && !aligned(draft, 4)))
+        return fail(QV_ERR_INVALID_ARG, "int32 buffers must be 4-byte aligned");
+    QV_CHECK_DEV(verify_tokens);
+    QV_CHECK_DEV(draft);
+    QV_CHECK_DEV(accept_len);
+    QV_CHECK_DEV(out_tokens);
+    cudaError_t e = qv::launch_accept(verify_tokens, draft, B, gamma, accept_len, out_tokens, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "qv_accept launch");
+    return ok();
+}
+
+qv_status qv_bf16_linear(const uint16_t* x, int M, int K, const uint16_t* w, int N, float* y,
+                         void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    if (!x || !w || !y) return fail(QV_ERR_INVALID_ARG, "null pointer");
+    if (M < 1 || M > QV_MAX_M) return fail(QV_ERR_INVALID_ARG, "M=%d outside [1, %d]", M, QV_MAX_M);
+    if (N < 1) return fail(QV_ERR_INVALID_ARG, "N=%d must be >= 1", N);
+    qv_status st = check_k(K);
+    if (st != QV_OK) return st;
+    if (!aligned(x, 16) || !aligned(w, 16)) return fail(QV_ERR_INVALID_ARG, "x and w must be 16-byte aligned");
+    if (!aligned(y, 4)) return fail(QV_ERR_INVALID_ARG, "y must be 4-byte aligned");
+    const size_t need = qv_workspace_bytes(QV_OP_BF16_LINEAR, M, K, N);
+    if (!workspace) return fail(QV_ERR_WORKSPACE, "workspace is null (%zu bytes needed)", need);
+    if (!aligned(workspace, 16)) return fail(QV_ERR_WORKSPACE, "workspace must be 16-byte aligned");
+    if (workspace_bytes < need) return fail(QV_ERR_WORKSPACE, "workspace has %zu bytes, %zu needed", workspace_bytes, need);
+    QV_CHECK_DEV(x);
+    QV_CHECK_DEV(w);
+    QV_CHECK_DEV(y);
+    QV_CHECK_DEV(workspace);
+    cudaError_t e;
+    const int sms = sms_of_current_device(&e);
+    if (e != cudaSuccess) return cuda_fail(e, "device query");
+    qv::Bf16Launch L = {};
+    if ((st = encode_2d(&L.tmap_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, w, (uint64_t)K, (uint64_t)N,
+                        qv::kTileKBytes / 2, qv::kTileN)) != QV_OK)
+        return st;
+    for (int m0 = 0; m0 < M; m0 += qv::kMaxMPerLaunch) {
+        const int mc = M - m0 < qv::kMaxMPerLaunch ? M - m0 : qv::kMaxMPerLaunch;
+        L.M = mc; L.N = N; L.K = K; L.MP = mp_for(mc);
+        if ((st = encode_2d(&L.tmap_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x + (size_t)m0 * K,
+                            (uint64_t)K, (uint64_t)mc, qv::kTileKBytes / 2, (uint32_t)L.MP)) != QV_OK)
+            return st;
+        L.y = y + (size_t)m0 * N;
+        L.ws = workspace;
+        e = qv::launch_bf16_stream(L, sms, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "qv_bf16_linear launch");
+    }
+    return ok();
+}
+
+qv_status qv_device_error(unsigned int* code) {
+    if (!code) return fail(QV_ERR_INVALID_ARG, "code is null");
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+    e = qv::read_and_clear_stream_gemm_error(code);
+    if (e != cudaSuccess) return cuda_fail(e, "reading the device error word");
+    return ok();
+}
+
+}  // extern "C"

@@ -1,0 +1,65 @@
+// qv_internal.h -- host-side interfaces between the C ABI (qv_abi.cu) and the
+// kernel translation units. Not part of the public ABI.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime_api.h>
+
+namespace qv {
+
+// Streaming-GEMM tile: BN output channels x BK bytes of the reduction axis.
+constexpr int kTileN = 128;
+constexpr int kTileKBytes = 128;
+
+// Largest padded token count one streaming-GEMM launch handles; larger M is
+// processed in slices of this many rows.
+constexpr int kMaxMPerLaunch = 64;
+
+inline int ceil_div(long long a, long long b) { return (int)((a + b - 1) / b); }
+inline int pad_tokens(int m) { return ((m + 7) / 8) * 8; }
+
+// Workspace layout of one streaming-GEMM call (all offsets in bytes, 16-byte
+// aligned): [acc: Npad*MP 4-byte words][tile counters: NT words][keys: MP
+// 8-byte words][done counter].
+struct WsLayout {
+    size_t acc = 0, counters = 0, keys = 0, done = 0, total = 0;
+};
+WsLayout ws_layout(int mp, int n, bool lm_head);
+
+enum class Epi : int { Linear = 0, LmHead = 1 };
+
+struct W8A8Launch {
+    CUtensorMap tmap_w;       // int8 [N rows][K], box {128, 128}, 128B swizzle
+    CUtensorMap tmap_x;       // int8 [M rows][K], box {128, MP}, 128B swizzle
+    int M, N, K, MP;
+    const float* sx;
+    const float* sw;
+    void* y;                  // Linear: [M*N] fp32 or bf16
+    int y_bf16;
+    int32_t* acc_debug;       // Linear: [M*N] or null
+    int32_t* tokens;          // LmHead: [M]
+    float* max_logit;         // LmHead: [M] or null
+    void* ws;
+    Epi epi;
+};
+
+struct Bf16Launch {
+    CUtensorMap tmap_w;       // bf16 [N rows][K], box {64, 128}, 128B swizzle
+    CUtensorMap tmap_x;       // bf16 [M rows][K], box {64, MP}, 128B swizzle
+    int M, N, K, MP;
+    float* y;                 // [M*N] fp32
+    void* ws;
+};
+
+cudaError_t launch_w8a8_stream(const W8A8Launch& a, int num_sms, cudaStream_t s);
+cudaError_t launch_bf16_stream(const Bf16Launch& a, int num_sms, cudaStream_t s);
+cudaError_t launch_quantize_rows(const void* x, bool bf16, int rows, int K,
+                                 const float* mul, int8_t* q, float* scale,
+                                 bool early_dependents, cudaStream_t s);
+cudaError_t launch_accept(const int32_t* t, const int32_t* d, int B, int gamma,
+                          int32_t* len, int32_t* out, cudaStream_t s);
+cudaError_t read_and_clear_stream_gemm_error(unsigned* code);
+
+}  // namespace qv

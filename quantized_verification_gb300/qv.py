@@ -1,0 +1,206 @@
+"""Thin ctypes binding of libqv (include/qv.h), one Python function per C
+entry point, same names. It only marshals arguments: shapes come from the
+tensors, pointers from ``data_ptr()``, the stream from torch. Every step of the
+computation runs in libqv's CUDA kernels; there is no fallback. If libqv.so
+is missing the first call raises, naming the build command.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libqv.so")
+
+QV_OK, QV_ERR_INVALID_ARG, QV_ERR_UNSUPPORTED, QV_ERR_WORKSPACE, QV_ERR_CUDA = range(5)
+QV_F32, QV_BF16 = 0, 1
+QV_OP_LINEAR, QV_OP_LM_HEAD, QV_OP_BF16_LINEAR = 0, 1, 2
+QV_MAX_K = 133144
+QV_MAX_M = 256
+
+# Symbols include/qv.h declares (checked against the library by the tests).
+EXPORTS = ("qv_quantize_act", "qv_w8a8_linear", "qv_lm_head_argmax", "qv_accept",
+           "qv_quantize_weight", "qv_bf16_linear", "qv_workspace_bytes",
+           "qv_last_error", "qv_device_error", "qv_num_sms")
+
+
+class QVError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"libqv status {status}: {message}")
+        self.status = status
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libqv.so (once). Raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"{path} is missing: build it with "
+                "`python -m quantized_verification_gb300.build`")
+        L = ctypes.CDLL(path)
+        P, I, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+        st = ctypes.c_int
+        L.qv_quantize_act.argtypes = [P, I, I, I, P, P, P, P]
+        L.qv_w8a8_linear.argtypes = [P, P, I, I, P, P, I, P, I, P, P, S, P]
+        L.qv_lm_head_argmax.argtypes = [P, P, I, I, P, P, I, P, P, P, S, P]
+        L.qv_accept.argtypes = [P, P, I, I, P, P, P]
+        L.qv_quantize_weight.argtypes = [P, I, I, I, P, P, P]
+        L.qv_bf16_linear.argtypes = [P, I, I, P, I, P, P, S, P]
+        L.qv_workspace_bytes.argtypes = [I, I, I, I]
+        L.qv_workspace_bytes.restype = S
+        L.qv_last_error.argtypes = []
+        L.qv_last_error.restype = ctypes.c_char_p
+        L.qv_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint)]
+        L.qv_num_sms.argtypes = []
+        L.qv_num_sms.restype = I
+        for name in ("qv_quantize_act", "qv_w8a8_linear", "qv_lm_head_argmax", "qv_accept",
+                     "qv_quantize_weight", "qv_bf16_linear", "qv_device_error"):
+            getattr(L, name).restype = st
+        _lib = L
+        return L
+
+
+def _check(status: int):
+    if status != QV_OK:
+        raise QVError(status, load().qv_last_error().decode())
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("expected a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError("tensor must live on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError("tensor must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _dtype(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return QV_F32
+    if t.dtype == torch.bfloat16:
+        return QV_BF16
+    raise TypeError(f"unsupported dtype {t.dtype} (float32 or bfloat16)")
+
+
+def _need(cond: bool, msg: str):
+    if not cond:
+        raise ValueError(msg)
+
+
+# ---------------------------------------------------------------------------
+def qv_quantize_act(x, xq, sx, act_mul=None, stream=None):
+    """x [M, K] fp32/bf16 -> xq [M, K] int8, sx [M] fp32."""
+    M, K = x.shape
+    _need(xq.shape == (M, K) and xq.dtype == torch.int8, "xq must be int8 [M, K]")
+    _need(sx.shape == (M,) and sx.dtype == torch.float32, "sx must be float32 [M]")
+    if act_mul is not None:
+        _need(act_mul.shape == (K,) and act_mul.dtype == torch.float32, "act_mul must be float32 [K]")
+    _check(load().qv_quantize_act(_ptr(x), _dtype(x), M, K, _ptr(act_mul), _ptr(xq), _ptr(sx),
+                                  ctypes.c_void_p(_stream(stream))))
+
+
+def qv_quantize_weight(w, wq, sw, stream=None):
+    """w [N, K] fp32/bf16 -> wq [N, K] int8, sw [N] fp32."""
+    N, K = w.shape
+    _need(wq.shape == (N, K) and wq.dtype == torch.int8, "wq must be int8 [N, K]")
+    _need(sw.shape == (N,) and sw.dtype == torch.float32, "sw must be float32 [N]")
+    _check(load().qv_quantize_weight(_ptr(w), _dtype(w), N, K, _ptr(wq), _ptr(sw),
+                                     ctypes.c_void_p(_stream(stream))))
+
+
+def qv_w8a8_linear(xq, sx, wq, sw, y, workspace, acc_debug=None, stream=None):
+    """y [M, N] (fp32 or bf16) = dequant(xq wq^T); acc_debug [M, N] int32."""
+    M, K = xq.shape
+    N = wq.shape[0]
+    _need(wq.shape == (N, K) and wq.dtype == torch.int8 and xq.dtype == torch.int8, "int8 xq [M,K], wq [N,K]")
+    _need(sx.shape == (M,) and sw.shape == (N,), "sx [M], sw [N]")
+    _need(sx.dtype == torch.float32 and sw.dtype == torch.float32, "scales must be float32")
+    _need(y.shape == (M, N), "y must be [M, N]")
+    if acc_debug is not None:
+        _need(acc_debug.shape == (M, N) and acc_debug.dtype == torch.int32, "acc_debug int32 [M, N]")
+    _need(workspace.dtype == torch.uint8, "workspace must be a uint8 tensor")
+    _check(load().qv_w8a8_linear(_ptr(xq), _ptr(sx), M, K, _ptr(wq), _ptr(sw), N, _ptr(y),
+                                 _dtype(y), _ptr(acc_debug), _ptr(workspace), workspace.numel(),
+                                 ctypes.c_void_p(_stream(stream))))
+
+
+def qv_lm_head_argmax(xq, sx, wq, sw, tokens, workspace, max_logit=None, stream=None):
+    """tokens [M] int32 = greedy argmax over the W8A8 LM-head logits."""
+    M, K = xq.shape
+    V = wq.shape[0]
+    _need(wq.shape == (V, K) and wq.dtype == torch.int8 and xq.dtype == torch.int8, "int8 xq [M,K], wq [V,K]")
+    _need(sx.shape == (M,) and sw.shape == (V,), "sx [M], sw [V]")
+    _need(tokens.shape == (M,) and tokens.dtype == torch.int32, "tokens int32 [M]")
+    if max_logit is not None:
+        _need(max_logit.shape == (M,) and max_logit.dtype == torch.float32, "max_logit float32 [M]")
+    _need(workspace.dtype == torch.uint8, "workspace must be a uint8 tensor")
+    _check(load().qv_lm_head_argmax(_ptr(xq), _ptr(sx), M, K, _ptr(wq), _ptr(sw), V, _ptr(tokens),
+                                    _ptr(max_logit), _ptr(workspace), workspace.numel(),
+                                    ctypes.c_void_p(_stream(stream))))
+
+
+def qv_accept(verify_tokens, draft, accept_len, out_tokens, stream=None):
+    """verify_tokens [B, gamma+1], draft [B, gamma] -> accept_len [B], out_tokens [B, gamma+1]."""
+    B, G = verify_tokens.shape
+    gamma = G - 1
+    _need(draft is None or (draft.shape == (B, gamma) and draft.dtype == torch.int32), "draft int32 [B, gamma]")
+    _need(verify_tokens.dtype == torch.int32, "verify_tokens int32")
+    _need(accept_len.shape == (B,) and accept_len.dtype == torch.int32, "accept_len int32 [B]")
+    _need(out_tokens.shape == (B, G) and out_tokens.dtype == torch.int32, "out_tokens int32 [B, gamma+1]")
+    d = draft if (draft is not None and draft.numel() > 0) else None
+    _check(load().qv_accept(_ptr(verify_tokens), _ptr(d), B, gamma, _ptr(accept_len),
+                            _ptr(out_tokens), ctypes.c_void_p(_stream(stream))))
+
+
+def qv_bf16_linear(x, w, y, workspace, stream=None):
+    """y [M, N] fp32 = x [M, K] bf16 . w [N, K] bf16^T."""
+    M, K = x.shape
+    N = w.shape[0]
+    _need(x.dtype == torch.bfloat16 and w.dtype == torch.bfloat16 and w.shape == (N, K), "bf16 x [M,K], w [N,K]")
+    _need(y.shape == (M, N) and y.dtype == torch.float32, "y float32 [M, N]")
+    _need(workspace.dtype == torch.uint8, "workspace must be a uint8 tensor")
+    _check(load().qv_bf16_linear(_ptr(x), M, K, _ptr(w), N, _ptr(y), _ptr(workspace),
+                                 workspace.numel(), ctypes.c_void_p(_stream(stream))))
+
+
+def qv_workspace_bytes(op: int, M: int, K: int, N: int) -> int:
+    return int(load().qv_workspace_bytes(op, M, K, N))
+
+
+def qv_device_error() -> int:
+    code = ctypes.c_uint(0)
+    _check(load().qv_device_error(ctypes.byref(code)))
+    return int(code.value)
+
+
+def qv_num_sms() -> int:
+    return int(load().qv_num_sms())
+
+
+def workspace(op: int, M: int, K: int, N: int, device=None) -> torch.Tensor:
+    """A zero-filled workspace of the size the op needs (torch allocation)."""
+    nbytes = qv_workspace_bytes(op, M, K, N)
+    if nbytes == 0:
+        raise ValueError(f"invalid shape for workspace: M={M} K={K} N={N}")
+    return torch.zeros(nbytes, dtype=torch.uint8, device=device or "cuda")

@@ -1,0 +1,78 @@
+"""C-ABI checks that need no GPU: the library builds, loads, exports every
+symbol include/qv.h declares, and rejects bad arguments on the host before
+touching CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from quantized_verification_gb300 import build, qv
+    build.build()
+    return qv.load()
+
+
+def declared_symbols():
+    names = set()
+    inc = os.path.join(ROOT, "include")
+    for f in os.listdir(inc):
+        if f.endswith(".h"):
+            src = open(os.path.join(inc, f)).read()
+            names |= set(re.findall(r"^QV_API\s+[\w\s\*]+?\b(qv_\w+)\s*\(", src, flags=re.M))
+    return names
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_symbols()
+    assert {"qv_quantize_act", "qv_w8a8_linear", "qv_lm_head_argmax", "qv_accept"} <= names
+    for n in names:
+        assert hasattr(lib, n), n
+    from quantized_verification_gb300 import qv
+    assert set(qv.EXPORTS) == names
+
+
+def test_workspace_sizes(lib):
+    from quantized_verification_gb300 import qv
+    # linear: Npad*MP int32 + counters; M=5 -> MP=8
+    assert qv.qv_workspace_bytes(qv.QV_OP_LINEAR, 5, 4096, 4096) == 4096 * 8 * 4 + 32 * 4
+    assert qv.qv_workspace_bytes(qv.QV_OP_LINEAR, 5, 4096, 1000) == 1024 * 8 * 4 + 8 * 4
+    assert qv.qv_workspace_bytes(qv.QV_OP_LM_HEAD, 5, 4096, 151936) > 151936 * 8 * 4
+    assert qv.qv_workspace_bytes(qv.QV_OP_LINEAR, 0, 4096, 16) == 0
+    assert qv.qv_workspace_bytes(qv.QV_OP_LINEAR, 5, 100, 16) == 0     # K % 16
+    assert qv.qv_workspace_bytes(qv.QV_OP_LINEAR, 257, 4096, 16) == 0  # M > QV_MAX_M
+    assert qv.qv_workspace_bytes(qv.QV_OP_LINEAR, 5, 133152, 16) == 0  # K > QV_MAX_K
+
+
+def test_host_validation_without_gpu(lib):
+    from quantized_verification_gb300 import qv
+    P = ctypes.c_void_p
+    fake = P(0x1000)
+    assert lib.qv_quantize_act(None, 0, 4, 256, None, fake, fake, None) == qv.QV_ERR_INVALID_ARG
+    assert b"null" in lib.qv_last_error()
+    assert lib.qv_quantize_act(fake, 0, 4, 250, None, fake, fake, None) == qv.QV_ERR_INVALID_ARG
+    assert b"multiple of 16" in lib.qv_last_error()
+    assert lib.qv_quantize_act(P(0x1001), 0, 4, 256, None, fake, fake, None) == qv.QV_ERR_INVALID_ARG
+    assert b"aligned" in lib.qv_last_error()
+    assert lib.qv_quantize_act(fake, 7, 4, 256, None, fake, fake, None) == qv.QV_ERR_INVALID_ARG
+    assert lib.qv_w8a8_linear(fake, fake, 0, 256, fake, fake, 8, fake, 0, None, fake, 1 << 20, None) == qv.QV_ERR_INVALID_ARG
+    assert lib.qv_w8a8_linear(fake, fake, 4, 256, fake, fake, 8, fake, 0, None, None, 0, None) == qv.QV_ERR_WORKSPACE
+    assert lib.qv_w8a8_linear(fake, fake, 4, 256, fake, fake, 8, fake, 0, None, fake, 16, None) == qv.QV_ERR_WORKSPACE
+    assert b"needed" in lib.qv_last_error()
+    assert lib.qv_lm_head_argmax(fake, fake, 4, 133152, fake, fake, 8, fake, None, fake, 1 << 20, None) == qv.QV_ERR_INVALID_ARG
+    assert lib.qv_accept(fake, None, 2, 3, fake, fake, None) == qv.QV_ERR_INVALID_ARG
+    assert lib.qv_accept(fake, fake, 0, 3, fake, fake, None) == qv.QV_ERR_INVALID_ARG
+    assert lib.qv_accept(fake, fake, 2, -1, fake, fake, None) == qv.QV_ERR_INVALID_ARG
+    assert lib.qv_bf16_linear(fake, 300, 256, fake, 8, fake, fake, 1 << 20, None) == qv.QV_ERR_INVALID_ARG
+
+
+def test_binding_rejects_host_tensors(lib):
+    import torch
+    from quantized_verification_gb300 import qv
+    x = torch.zeros(4, 256)
+    with pytest.raises(ValueError):
+        qv.qv_quantize_act(x, torch.zeros(4, 256, dtype=torch.int8), torch.zeros(4))
