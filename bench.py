@@ -1,0 +1,415 @@
+"""Benchmark: W8A8 verify-pass tokens/s and weight-stream GB/s on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step = one full verify pass of the Qwen3-8B-shaped stack at M = 5 tokens
+(batch 1, gamma = 4): per layer four act-quant + W8A8-linear phases (q|k|v, o,
+gate|up, down; 36 layers, 6.95 GB int8), the final act quant, the LM head
+4096 -> 151936 fused with the greedy argmax, and the acceptance of gamma = 4
+drafts. Weights are seeded synthetic (N(0, 0.02), bf16, quantized per output
+channel), activations seeded N(0, 1) with 1% outlier channels x20. Inputs are
+resident in HBM before timing; the 7.57 GB of weights per step exceed the
+129 MB L2, so no flush is needed between steps.
+
+Rank 0 prints one JSON line. With torchrun (N > 1) every rank runs an
+independent replica (the path is not sharded); value = all tokens / max time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "W8A8 verify-pass tokens/s and weight-stream GB/s (fraction of GB300 HBM peak)"
+UNIT = "tokens/s"
+WORKLOAD = ("qwen3-8b-shaped W8A8 verify step, M=5 (B=1, gamma=4): 36 layers x (qkv 4096->6144, "
+            "o 4096->4096, gate|up 4096->24576, down 12288->4096) + LM head 4096->151936 argmax + accept")
+FALLBACK_HBM_GBS = 6800.0
+
+# DRAM bytes per algorithmic byte of the dominant kernel from one ncu capture,
+# valid only for the kernel source it was taken on (sha256 of
+# csrc/k_stream_gemm.cu); traffic is reported as null otherwise.
+NCU_TRAFFIC = {"source_sha256": None, "dram_bytes_per_algorithmic_byte": None}
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu: str):
+        self.gpu = gpu
+        self.lines = []
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(self.gpu)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        threading.Thread(target=self._read, daemon=True).start()
+        time.sleep(0.3)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+
+    def summary(self, t0: float, t1: float):
+        rows = []
+        for (ts, line) in self.lines:
+            if not (t0 <= ts <= t1):
+                continue
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                rows.append({"sm": float(parts[2]), "max": float(parts[3]), "power": float(parts[4]),
+                             "hw_slowdown": parts[6], "hw_thermal": parts[7], "sw_thermal": parts[8],
+                             "sw_power_cap": parts[9]})
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        names = {"hw_slowdown": "hw_slowdown", "hw_thermal": "hw_thermal_slowdown",
+                 "sw_thermal": "sw_thermal_slowdown", "sw_power_cap": "sw_power_cap"}
+        reasons = sorted({names[k] for r in rows for k in names if r[k].lower() == "active"})
+        return {"sm_mhz": statistics.median(r["sm"] for r in rows), "sm_max_mhz": max(r["max"] for r in rows),
+                "reasons": reasons, "samples": len(rows),
+                "power_w_median": statistics.median(r["power"] for r in rows)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle: the baseline leg (and the reference arm)
+# ---------------------------------------------------------------------------
+class OracleStep:
+    """The oracle on the same workload shapes, one slice of output channels at a
+    time, so a bounded sample can be timed and scaled to the full step by its
+    share of the step's multiply-accumulates."""
+
+    def __init__(self, M=5, B=1, gamma=4, seed=0, rows_cap=4096):
+        import numpy as np
+        import torch
+
+        import oracle
+        from quantized_verification_gb300 import synth
+        self.o = oracle.get()
+        self.M, self.B, self.gamma = M, B, gamma
+        m = synth.QWEN3_8B
+        h, kv, ffn, V = m["hidden"], m["kv"], m["ffn"], m["vocab"]
+        self.layers = m["layers"]
+        self.phases = [("qkv", h, h + 2 * kv), ("o", h, h), ("gate_up", h, 2 * ffn), ("down", ffn, h)]
+        self.lm = ("lm_head", h, V)
+        rng = np.random.default_rng(seed)
+        # host weights (bf16 patterns) for the first `rows_cap` output channels of
+        # each projection and of the LM head, quantized once (setup, untimed);
+        # slices wrap around them, the cost per channel being the same
+        self.wq, self.sw, self.x, self.rows = {}, {}, {}, {}
+        for (name, K, N) in self.phases + [self.lm]:
+            rows = min(N, rows_cap)
+            self.rows[name] = rows
+            w = synth.weights(rows, K, synth.subseed(seed, "cpu_w", name))
+            wb = w.view(torch.int16).numpy().view(np.uint16)
+            self.wq[name], self.sw[name] = self.o.quantize_rows(wb, bf16=True)
+            xb = synth.activations(M, K, synth.subseed(seed, "cpu_x", name))
+            self.x[name] = xb.view(torch.int16).numpy().view(np.uint16)
+        self.total_macs = M * (self.layers * sum(N * K for (_, K, N) in self.phases) + V * h)
+        self.t_tokens = rng.integers(0, V, (B, gamma + 1)).astype(np.int32)
+        self.drafts = self.t_tokens[:, :gamma].copy()
+
+    def run_slice(self, name, n0, n1):
+        """act quant of the phase input + W8A8 linear (or LM-head argmax) over
+        output channels [n0, n1); returns the MACs done."""
+        K = self.x[name].shape[1]
+        xq, sx = self.o.quantize_rows(self.x[name], bf16=True)
+        if name == "lm_head":
+            self.o.lm_head_argmax(xq, sx, self.wq[name][n0:n1], self.sw[name][n0:n1])
+        else:
+            self.o.w8a8_linear(xq, sx, self.wq[name][n0:n1], self.sw[name][n0:n1])
+        return self.M * K * (n1 - n0)
+
+    def timed_sample(self, seconds: float):
+        """Slices round-robin over the phases and the LM head (+ accept) for
+        about `seconds`; returns (elapsed, macs)."""
+        names = [p[0] for p in self.phases] + ["lm_head"]
+        pos = {n: 0 for n in names}
+        macs, t0, i = 0, time.perf_counter(), 0
+        while True:
+            n = names[i % len(names)]
+            a = pos[n]
+            b = min(a + 256, self.rows[n])
+            macs += self.run_slice(n, a, b)
+            pos[n] = 0 if b >= self.rows[n] else b
+            i += 1
+            self.o.accept(self.t_tokens, self.drafts, self.B, self.gamma)
+            el = time.perf_counter() - t0
+            if el >= seconds:
+                return el, macs
+
+
+def cpu_baseline(seconds: float):
+    st = OracleStep()
+    el, macs = st.timed_sample(seconds)
+    step_s = el * st.total_macs / macs
+    return {"value": st.M / step_s, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"plain C oracle, 1 thread: act quant + W8A8 linear / LM-head argmax over 256-channel "
+                      f"slices of the step's projections round-robin + accept, {el:.1f} s, "
+                      f"{macs / 1e9:.2f} GMAC of the step's {st.total_macs / 1e9:.1f} GMAC, scaled by MAC share"}
+
+
+def run_reference(args, rank, world):
+    """The oracle as it stands, on the host cores, same metric and workload."""
+    if rank != 0:
+        return 0
+    st = OracleStep()
+    budget = min(2.0, 150.0 / max(args.steps + args.warmup, 1))
+    for _ in range(args.warmup):
+        st.timed_sample(budget / 4)
+    el_total, macs_total = 0.0, 0
+    for _ in range(args.steps):
+        el, macs = st.timed_sample(budget)
+        el_total += el
+        macs_total += macs
+    step_s = el_total * st.total_macs / macs_total
+    value = st.M / step_s
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int8/int32/fp32",
+            "data": "synthetic", "config": {"workload": WORKLOAD, "M": st.M, "B": st.B, "gamma": st.gamma,
+                                            "parallelism": "replicas"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": f"each step: {budget:.2f} s of 256-channel slices round-robin over the "
+                                       f"projections and LM head + accept; scaled to the full step by MAC share"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+def read_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_sha():
+    with open(os.path.join(ROOT, "quantized_verification_gb300", "csrc", "k_stream_gemm.cu"), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()
+
+
+def time_graph(torch, graph, n, stream):
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(n):
+        graph.replay()
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / n
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--layers", type=int, default=None, help="layer count override (testing only)")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-comparator", action="store_true")
+    ap.add_argument("--kernel-reps", type=int, default=20)
+    args = ap.parse_args()
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+
+    import torch
+    import torch.distributed as dist
+
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+
+    from quantized_verification_gb300 import build, qv, synth
+    from quantized_verification_gb300.stack import VerifyStack
+    build.build()
+
+    t_setup = time.time()
+    stack = VerifyStack(layers=args.layers, B=1, gamma=4, seed=1234 + rank, device=str(dev),
+                        keep_bf16=not args.no_comparator)
+    stack.enqueue()                 # drafts agree with the verifier for a geometric(0.7) prefix
+    torch.cuda.synchronize()
+    t_ver = stack.tokens.view(stack.B, stack.gamma + 1).cpu()
+    stack.drafts.copy_(synth.geometric_drafts(t_ver, stack.V, 0.7, seed=99 + rank))
+    step_graph = stack.capture()
+    path = "per-op ABI calls (act quant + W8A8 linear per phase, LM head argmax, accept) in one CUDA graph"
+    launches = stack.launches_per_step()
+    log(f"setup {time.time() - t_setup:.1f} s; weight bytes/step {stack.weight_bytes() / 1e9:.3f} GB")
+    stream = torch.cuda.current_stream()
+
+    for _ in range(max(args.warmup, 3)):
+        step_graph.replay()
+    torch.cuda.synchronize()
+    cvd = os.environ.get("CUDA_VISIBLE_DEVICES")
+    clocks = ClockSampler(cvd.split(",")[local].strip() if cvd else str(local))
+    clocks.start()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    w0 = time.time()
+    ms = time_graph(torch, step_graph, args.steps, stream)
+    w1 = time.time()
+    if world > 1:
+        dist.barrier()
+    clocks.stop()
+    ms_t = torch.tensor([ms], device=dev)
+    if world > 1:
+        dist.all_reduce(ms_t, op=dist.ReduceOp.MAX)
+    ms_max = float(ms_t.item())
+    value = world * stack.M / (ms_max / 1e3)
+    clk = clocks.summary(w0, w1)
+    alg_bytes = stack.algorithmic_bytes()
+    log(f"step {ms:.4f} ms ({alg_bytes / (ms * 1e-3) / 1e9:.1f} GB/s algorithmic), clocks {clk}")
+    assert qv.qv_device_error() == 0, "a kernel hit its wait limit"
+    peak, peak_kind = read_peaks()
+
+    # ---- dominant kernel: qv_w8a8_linear on the step's 144 projections, back
+    # to back in one graph (PDL between launches), activations pre-quantized
+    M = stack.M
+    lin_bytes = stack.linear_launch_bytes()
+    xqs = []
+    for l in range(stack.layers):
+        for p, (name, K, N) in enumerate(stack.phases):
+            xq = torch.empty(M, K, dtype=torch.int8, device=dev)
+            sxp = torch.empty(M, device=dev)
+            qv.qv_quantize_act(stack.inputs[l][p], xq, sxp)
+            xqs.append((xq, sxp))
+    torch.cuda.synchronize()
+
+    def lin_seq(s):
+        j = 0
+        for l in range(stack.layers):
+            for p, (name, K, N) in enumerate(stack.phases):
+                wq, sw = stack.weights[l][p]
+                qv.qv_w8a8_linear(xqs[j][0], xqs[j][1], wq, sw, stack.y[: M * N].view(M, N), stack.ws, stream=s)
+                j += 1
+    gl = VerifyStack._capture(lin_seq, dev)
+    lin_ms = time_graph(torch, gl, args.kernel_reps, stream)
+    achieved = sum(lin_bytes) / (lin_ms * 1e-3) / 1e9
+    traffic = None
+    if NCU_TRAFFIC["source_sha256"] == kernel_source_sha() and NCU_TRAFFIC["dram_bytes_per_algorithmic_byte"]:
+        traffic = NCU_TRAFFIC["dram_bytes_per_algorithmic_byte"] * sum(lin_bytes) / len(lin_bytes)
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                "traffic": traffic, "kernel": "w8a8_stream_kernel (qv_w8a8_linear)",
+                "bytes_per_launch": sum(lin_bytes) / len(lin_bytes),
+                "launch_ms_mean": lin_ms / len(lin_bytes),
+                "timing": "144 launches of the step's projections back to back in one CUDA graph, "
+                          "CUDA events on the launching stream",
+                "peak_source": f"{peak_kind} hbm_gbs (copy, burst)"}
+    log(f"w8a8 linear kernel: {achieved:.1f} GB/s = {achieved / peak:.3f} of {peak_kind} {peak}")
+    del gl, xqs
+
+    # ---- BF16-weight comparator on the same shapes
+    comparator = None
+    if not args.no_comparator:
+        stack.prepare_bf16()
+        gb = VerifyStack._capture(stack.enqueue_bf16, dev)
+        for _ in range(3):
+            gb.replay()
+        bf_ms = time_graph(torch, gb, max(10, args.steps // 4), stream)
+        comparator = {"bf16_ms_per_step": bf_ms, "w8a8_ms_per_step": ms, "speedup": bf_ms / ms,
+                      "bf16_weight_bytes": stack.bf16_weight_bytes(),
+                      "bf16_stream_gbs": stack.bf16_weight_bytes() / (bf_ms * 1e-3) / 1e9,
+                      "note": "same shapes; qv_bf16_linear for every projection and the LM head "
+                              "(logits written, argmax not included)"}
+        log(f"bf16 comparator {bf_ms:.4f} ms/step, speedup {bf_ms / ms:.3f}x")
+        del gb
+
+    # ---- e2e through the public API from host buffers
+    host_in, host_d = stack.pinned_host_inputs()
+    out_len = torch.empty(stack.B, dtype=torch.int32).pin_memory()
+    out_tok = torch.empty(stack.B, stack.gamma + 1, dtype=torch.int32).pin_memory()
+    for _ in range(3):
+        stack.step_from_host(host_in, host_d, out_len, out_tok, graph=step_graph)
+    torch.cuda.synchronize()
+    n_e2e = max(10, args.steps // 4)
+    h2d = d2h = 0
+    t0 = time.perf_counter()
+    for _ in range(n_e2e):
+        h2d, d2h = stack.step_from_host(host_in, host_d, out_len, out_tok, graph=step_graph)
+        torch.cuda.current_stream().synchronize()      # the host reads the step's result
+        _ = int(out_len[0])
+    e2e_s = (time.perf_counter() - t0) / n_e2e
+    e2e = {"value": world * stack.M / e2e_s, "unit": UNIT, "h2d_bytes_per_step": h2d,
+           "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        cpu = cpu_baseline(args.cpu_seconds)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "int8 x int8 -> int32, fp32 dequant", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "M": stack.M, "B": stack.B, "gamma": stack.gamma,
+                       "layers": stack.layers, "weight_bytes_per_step": stack.weight_bytes(),
+                       "algorithmic_bytes_per_step": alg_bytes,
+                       "weight_stream_gbs": stack.weight_bytes() / (ms_max * 1e-3) / 1e9,
+                       "weight_stream_frac_of_peak": stack.weight_bytes() / (ms_max * 1e-3) / 1e9 / peak,
+                       "l2": "inputs larger than L2: 7.57 GB of weights per step vs 129 MB L2, no flush",
+                       "parallelism": "replicas" if world > 1 else "single GPU",
+                       "path": path,
+                       "timing": "CUDA graph replay of whole steps, CUDA events on the launching stream"},
+            "roofline": roofline,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": launches * args.steps,
+            "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"],
+                       "samples": clk["samples"]},
+            "comparator": comparator,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

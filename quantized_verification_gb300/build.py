@@ -48,15 +48,17 @@ def _headers_mtime() -> float:
     return max(os.path.getmtime(h) for h in hs)
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | None = None) -> str:
-    """Compile and link libqv.so; returns its path. Skips up-to-date objects."""
+def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | None = None,
+          build_dir: str = BUILD, out: str = LIB) -> str:
+    """Compile and link libqv.so (or `out`); returns its path. Skips up-to-date
+    objects. `extra_flags` (e.g. -D tuning macros) go to every nvcc call."""
     nvcc = _nvcc()
-    os.makedirs(BUILD, exist_ok=True)
+    os.makedirs(build_dir, exist_ok=True)
     hdr = _headers_mtime()
     flags = NVCC_FLAGS + list(extra_flags or [])
     jobs = []
     for src in sources():
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
         stale = (force or not os.path.exists(obj)
                  or os.path.getmtime(obj) < max(os.path.getmtime(src), hdr))
         jobs.append((src, obj, stale))
@@ -79,14 +81,14 @@ def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | N
                 print(msg, file=sys.stderr)
 
     objs = [j[1] for j in jobs]
-    if force or not os.path.exists(LIB) or any(os.path.getmtime(o) > os.path.getmtime(LIB) for o in objs):
-        tmp = LIB + f".tmp{os.getpid()}"
+    if force or not os.path.exists(out) or any(os.path.getmtime(o) > os.path.getmtime(out) for o in objs):
+        tmp = out + f".tmp{os.getpid()}"
         cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs, "-lcudart_static"]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, out)
+    return out
 
 
 if __name__ == "__main__":

@@ -19,13 +19,15 @@
 //    ring of shared-memory stages guarded by mbarriers. The activation slice
 //    of the same K range (M rows padded to MP, out-of-range rows zero-filled
 //    by TMA) travels with each weight tile.
-//  - Four consumer warps each own 32 output channels of a tile and run
-//    m16n8k16 mma.sync with the output channels as the MMA's M and the
-//    tokens as its N (token count padded to a multiple of 8).
-//  - W8A8: int8 codes are widened exactly to binary16 in registers. Products
-//    are at most 128^2 = 2^14, one tile sums 128 of them (|sum| <= 2^21),
-//    so every fp32 partial is an exact integer; after each tile the fp32
-//    partials are converted to int32 (exact) and added in int32.
+//  - Eight consumer warps each own 16 output channels of a tile and run
+//    mma.sync with the output channels as the MMA's M and the tokens as its
+//    N (token count padded to a multiple of 8).
+//  - W8A8 with up to 8 tokens: int8 m16n8k32 MMA, exact int32 accumulation,
+//    the ldmatrix words being the MMA fragments as they are. With more
+//    tokens: int8 codes are widened exactly to binary16 in registers and run
+//    through the f16 m16n8k16 MMA; products are at most 128^2 = 2^14, one
+//    tile sums 128 of them (|sum| <= 2^21), so every fp32 partial is an
+//    exact integer; after each tile it is converted to int32 and added.
 //  - A channel tile whose K range is split over CTAs is combined with int32
 //    atomic adds into the workspace (exact, so order does not matter); the
 //    CTA whose contribution completes the tile runs the epilogue, reading and
@@ -56,10 +58,32 @@ namespace {
 
 constexpr int BN = kTileN;            // output channels per tile
 constexpr int BKB = kTileKBytes;      // bytes of K per tile (one 128-byte row)
-constexpr int kConsumerWarps = 4;
-constexpr int kConsumerThreads = kConsumerWarps * 32;
-constexpr int kThreads = kConsumerThreads + 32;   // + one producer warp
+constexpr int kMaxConsumerWarps = 8;
 constexpr int kWTileBytes = BN * BKB;             // 16 KB
+
+// Consumer warps per CTA (one more warp produces), and how many of the four
+// 32-byte chunk pairs of each tile row go through the int8 tensor path; the
+// rest are widened to binary16 and go through the f16 path. With 8 tokens or
+// fewer the int8 path alone keeps up with HBM; with more tokens it would be
+// the bottleneck and the f16 path is faster (measured on GB300).
+#ifndef QV_W8A8_WARPS
+#define QV_W8A8_WARPS 8
+#endif
+#ifndef QV_S8_PAIRS_NARROW
+#define QV_S8_PAIRS_NARROW 4
+#endif
+#ifndef QV_S8_PAIRS_WIDE
+#define QV_S8_PAIRS_WIDE 0
+#endif
+#ifndef QV_BF16_WARPS
+#define QV_BF16_WARPS 8
+#endif
+constexpr int kW8A8Warps = QV_W8A8_WARPS;
+constexpr int kBf16Warps = QV_BF16_WARPS;
+template <int NG>
+__host__ __device__ constexpr int s8_pairs() { return NG == 1 ? QV_S8_PAIRS_NARROW : QV_S8_PAIRS_WIDE; }
+static_assert(kW8A8Warps == 4 || kW8A8Warps == 8, "4 or 8 consumer warps");
+static_assert(kBf16Warps == 4 || kBf16Warps == 8, "4 or 8 consumer warps");
 
 template <int NG>
 struct Cfg {
@@ -71,11 +95,12 @@ struct Cfg {
     static constexpr int StgWords = BN * MP;                 // epilogue staging
     static constexpr int SmemBytes =
         1024 /*alignment slack*/ + Stages * StageBytes + StgWords * 4 +
-        2 * Stages * 8 + kConsumerWarps * MP * 8 + MP * 4 + 64;
+        2 * Stages * 8 + kMaxConsumerWarps * MP * 8 + MP * 4 + 64;
 };
 
+template <int CW>
 __device__ __forceinline__ void consumer_sync() {
-    asm volatile("bar.sync 1, %0;" :: "n"(kConsumerThreads) : "memory");
+    asm volatile("bar.sync 1, %0;" :: "n"(CW * 32) : "memory");
 }
 
 // Order-preserving map of a float to uint32 (larger float -> larger key);
@@ -106,7 +131,7 @@ struct Smem {
     int32_t* stg;             // BN x MP staging words
     uint64_t* full;
     uint64_t* empty;
-    unsigned long long* red;  // kConsumerWarps x MP
+    unsigned long long* red;  // kMaxConsumerWarps x MP
     float* sx;                // MP
     volatile int* abort;
     volatile int* flag;
@@ -123,7 +148,7 @@ struct Smem {
         empty = reinterpret_cast<uint64_t*>(p);
         p += Stages * 8;
         red = reinterpret_cast<unsigned long long*>(p);
-        p += kConsumerWarps * MP * 8;
+        p += kMaxConsumerWarps * MP * 8;
         sx = reinterpret_cast<float*>(p);
         p += MP * 4;
         abort = reinterpret_cast<volatile int*>(p);
@@ -186,6 +211,100 @@ __device__ __forceinline__ void produce(SM& sm, const CUtensorMap* tw, const CUt
 }
 
 // ---------------------------------------------------------------------------
+// One weight tile (128 channels x 128 bytes of K, 128-byte swizzled) against
+// the activation tile (MP tokens x the same 128 bytes, same swizzle), both in
+// shared memory: acci += exact int32 partial sums of this warp's channels.
+// Chunk pairs P < S8P use the int8 m16n8k32 MMA directly on the ldmatrix
+// words; the others widen the codes exactly to binary16 and use the f16
+// m16n8k16 MMA, whose fp32 partials (|sum| <= 2^21) are exact integers.
+// The f16 products use a fixed permutation of K within each 16-byte chunk
+// (logical k 2t,2t+1 <-> bytes 4t,4t+1 and 2t+8,2t+9 <-> bytes 4t+2,4t+3),
+// applied identically to both operands, which leaves every sum unchanged.
+// ---------------------------------------------------------------------------
+template <int BPW>
+struct TileLanes {
+    uint32_t w_row_off[BPW];   // byte offset of this lane's ldmatrix row, per 16-row block
+    uint32_t w_chunk_off[4];   // swizzled chunk offset per chunk pair
+    uint32_t x_chunk_off[2];   // swizzled chunk offset per group of four chunks
+    uint32_t x_row_off;        // byte offset of this lane's activation row
+    __device__ __forceinline__ TileLanes(int first_row, int lane) {
+        const int li = lane & 7, lj = lane >> 3;
+#pragma unroll
+        for (int blk = 0; blk < BPW; ++blk)
+            w_row_off[blk] = (uint32_t)((first_row + 16 * blk + li + 8 * (lj & 1)) * BKB);
+#pragma unroll
+        for (int cp = 0; cp < 4; ++cp)
+            w_chunk_off[cp] = (uint32_t)((((2 * cp) + (lj >> 1)) ^ li) << 4);
+#pragma unroll
+        for (int cq = 0; cq < 2; ++cq) x_chunk_off[cq] = (uint32_t)(((4 * cq + lj) ^ li) << 4);
+        x_row_off = (uint32_t)(li * BKB);
+    }
+};
+
+template <int NG, int BPW, int S8P>
+__device__ __forceinline__ void w8a8_tile_mma(uint32_t wb, uint32_t xb, const TileLanes<BPW>& L,
+                                              int32_t (&acci)[BPW][NG][4]) {
+    float accf[BPW][NG][4];
+#pragma unroll
+    for (int blk = 0; blk < BPW; ++blk)
+#pragma unroll
+        for (int gr = 0; gr < NG; ++gr)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) accf[blk][gr][e] = 0.f;
+#pragma unroll
+    for (int cq = 0; cq < 2; ++cq) {
+        // Activation words (tokens = MMA columns) for chunks 4cq .. 4cq+3.
+        uint32_t bw[NG][4];
+#pragma unroll
+        for (int gr = 0; gr < NG; ++gr)
+            ldmatrix_x4(xb + (uint32_t)(8 * gr * BKB) + L.x_row_off + L.x_chunk_off[cq],
+                        bw[gr][0], bw[gr][1], bw[gr][2], bw[gr][3]);
+        uint32_t bh[NG][4][2];
+#pragma unroll
+        for (int gr = 0; gr < NG; ++gr)
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+                if (2 * cq + c / 2 >= S8P) widen_i8x4_f16(bw[gr][c], bh[gr][c][0], bh[gr][c][1]);
+#pragma unroll
+        for (int blk = 0; blk < BPW; ++blk) {
+#pragma unroll
+            for (int cp = 0; cp < 2; ++cp) {
+                const int P = 2 * cq + cp;      // chunk pair: chunks 2P, 2P+1
+                uint32_t r0, r1, r2, r3;
+                ldmatrix_x4(wb + L.w_row_off[blk] + L.w_chunk_off[P], r0, r1, r2, r3);
+                if (P < S8P) {
+#pragma unroll
+                    for (int gr = 0; gr < NG; ++gr)
+                        mma_s8_16832(acci[blk][gr], r0, r1, r2, r3, bw[gr][2 * cp], bw[gr][2 * cp + 1]);
+                } else {
+                    uint32_t a0l, a0h, a1l, a1h;
+                    widen_i8x4_f16(r0, a0l, a0h);   // row g,   chunk 2P
+                    widen_i8x4_f16(r1, a1l, a1h);   // row g+8, chunk 2P
+#pragma unroll
+                    for (int gr = 0; gr < NG; ++gr)
+                        mma_f16_16816(accf[blk][gr], a0l, a1l, a0h, a1h,
+                                      bh[gr][2 * cp][0], bh[gr][2 * cp][1]);
+                    widen_i8x4_f16(r2, a0l, a0h);   // row g,   chunk 2P+1
+                    widen_i8x4_f16(r3, a1l, a1h);   // row g+8, chunk 2P+1
+#pragma unroll
+                    for (int gr = 0; gr < NG; ++gr)
+                        mma_f16_16816(accf[blk][gr], a0l, a1l, a0h, a1h,
+                                      bh[gr][2 * cp + 1][0], bh[gr][2 * cp + 1][1]);
+                }
+            }
+        }
+    }
+    if (S8P < 4) {
+#pragma unroll
+        for (int blk = 0; blk < BPW; ++blk)
+#pragma unroll
+            for (int gr = 0; gr < NG; ++gr)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) acci[blk][gr][e] += __float2int_rn(accf[blk][gr][e]);
+    }
+}
+
+// ---------------------------------------------------------------------------
 // W8A8 kernel
 // ---------------------------------------------------------------------------
 struct W8A8Params {
@@ -205,12 +324,17 @@ struct W8A8Params {
 };
 
 template <int NG, int EPI>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__((kW8A8Warps + 1) * 32, 1)
 w8a8_stream_kernel(const __grid_constant__ CUtensorMap tmap_w,
                    const __grid_constant__ CUtensorMap tmap_x, const W8A8Params p) {
     using C = Cfg<NG>;
     constexpr int MP = C::MP;
     constexpr int Stages = C::Stages;
+    constexpr int CW = kW8A8Warps;
+    constexpr int CT = CW * 32;
+    constexpr int RW = BN / CW;          // output channels per consumer warp
+    constexpr int BPW = RW / 16;         // 16-channel MMA blocks per warp
+    constexpr int S8P = s8_pairs<NG>();
     extern __shared__ uint8_t smem_raw[];
     Smem<Stages, C::StageBytes, C::StgWords, MP> sm(smem_raw);
 
@@ -223,7 +347,7 @@ w8a8_stream_kernel(const __grid_constant__ CUtensorMap tmap_w,
     if (tid == 0) {
         for (int s = 0; s < Stages; ++s) {
             mbar_init(&sm.full[s], 1);
-            mbar_init(&sm.empty[s], kConsumerWarps);
+            mbar_init(&sm.empty[s], CW);
         }
         *sm.abort = 0;
         fence_barrier_init();
@@ -231,7 +355,7 @@ w8a8_stream_kernel(const __grid_constant__ CUtensorMap tmap_w,
     __syncthreads();
     allow_dependent_launch();
 
-    if (warp == kConsumerWarps) {
+    if (warp == CW) {
         if (lane == 0)
             produce<Stages>(sm, &tmap_w, &tmap_x, a, b, p.KT, BKB,
                             (unsigned)(kWTileBytes + C::XBytes));
@@ -241,25 +365,12 @@ w8a8_stream_kernel(const __grid_constant__ CUtensorMap tmap_w,
     // ---------------- consumers ----------------
     grid_dependency_wait();
     if (tid < MP) sm.sx[tid] = tid < p.M ? p.sx[tid] : 0.f;
-    consumer_sync();
+    consumer_sync<CW>();
 
-    const int li = lane & 7, lj = lane >> 3;
     const int g = lane >> 2, t4 = lane & 3;
-    // ldmatrix lane offsets: weight rows of the two 16-row blocks, and the
-    // swizzled chunk positions (128-byte swizzle: chunk ^= row % 8).
-    uint32_t w_row_off[2];
-#pragma unroll
-    for (int blk = 0; blk < 2; ++blk)
-        w_row_off[blk] = (uint32_t)((32 * warp + 16 * blk + li + 8 * (lj & 1)) * BKB);
-    uint32_t w_chunk_off[4];
-#pragma unroll
-    for (int cp = 0; cp < 4; ++cp)
-        w_chunk_off[cp] = (uint32_t)((((2 * cp) + (lj >> 1)) ^ li) << 4);
-    uint32_t x_chunk_off[2];
-#pragma unroll
-    for (int cq = 0; cq < 2; ++cq) x_chunk_off[cq] = (uint32_t)(((4 * cq + lj) ^ li) << 4);
+    const TileLanes<BPW> L(RW * warp, lane);
 
-    int32_t acci[2][NG][4];
+    int32_t acci[BPW][NG][4];
     int s = 0, phase = 0;
     int i = a;
     while (i < b) {
@@ -267,7 +378,7 @@ w8a8_stream_kernel(const __grid_constant__ CUtensorMap tmap_w,
         const int seg_begin = i;
         const int seg_end = min(b, (nt + 1) * p.KT);
 #pragma unroll
-        for (int blk = 0; blk < 2; ++blk)
+        for (int blk = 0; blk < BPW; ++blk)
 #pragma unroll
             for (int gr = 0; gr < NG; ++gr)
 #pragma unroll
@@ -276,65 +387,16 @@ w8a8_stream_kernel(const __grid_constant__ CUtensorMap tmap_w,
         for (; i < seg_end; ++i) {
             if (!mbar_wait_bounded(&sm.full[s], phase, sm.abort))
                 atomicOr(&g_stream_gemm_error, kErrFullWait);
-            const uint32_t wb = smem_u32(sm.w_tile(s));
-            const uint32_t xb = smem_u32(sm.x_tile(s));
-            float accf[2][NG][4];
-#pragma unroll
-            for (int blk = 0; blk < 2; ++blk)
-#pragma unroll
-                for (int gr = 0; gr < NG; ++gr)
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) accf[blk][gr][e] = 0.f;
-
-#pragma unroll
-            for (int cq = 0; cq < 2; ++cq) {
-                // B fragments (tokens) for the four chunks 4cq .. 4cq+3.
-                uint32_t bx[NG][4][2];
-#pragma unroll
-                for (int gr = 0; gr < NG; ++gr) {
-                    uint32_t r[4];
-                    ldmatrix_x4(xb + (uint32_t)((8 * gr + li) * BKB) + x_chunk_off[cq],
-                                r[0], r[1], r[2], r[3]);
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) widen_i8x4_f16(r[c], bx[gr][c][0], bx[gr][c][1]);
-                }
-#pragma unroll
-                for (int blk = 0; blk < 2; ++blk) {
-#pragma unroll
-                    for (int cp = 0; cp < 2; ++cp) {
-                        uint32_t r0, r1, r2, r3;
-                        ldmatrix_x4(wb + w_row_off[blk] + w_chunk_off[2 * cq + cp], r0, r1, r2, r3);
-                        uint32_t a0l, a0h, a1l, a1h;
-                        widen_i8x4_f16(r0, a0l, a0h);   // row g,   chunk c
-                        widen_i8x4_f16(r1, a1l, a1h);   // row g+8, chunk c
-#pragma unroll
-                        for (int gr = 0; gr < NG; ++gr)
-                            mma_f16_16816(accf[blk][gr], a0l, a1l, a0h, a1h,
-                                          bx[gr][2 * cp][0], bx[gr][2 * cp][1]);
-                        widen_i8x4_f16(r2, a0l, a0h);   // row g,   chunk c+1
-                        widen_i8x4_f16(r3, a1l, a1h);   // row g+8, chunk c+1
-#pragma unroll
-                        for (int gr = 0; gr < NG; ++gr)
-                            mma_f16_16816(accf[blk][gr], a0l, a1l, a0h, a1h,
-                                          bx[gr][2 * cp + 1][0], bx[gr][2 * cp + 1][1]);
-                    }
-                }
-            }
+            w8a8_tile_mma<NG, BPW, S8P>(smem_u32(sm.w_tile(s)), smem_u32(sm.x_tile(s)), L, acci);
             __syncwarp();
             if (lane == 0) mbar_arrive(&sm.empty[s]);
             if (++s == Stages) { s = 0; phase ^= 1; }
-#pragma unroll
-            for (int blk = 0; blk < 2; ++blk)
-#pragma unroll
-                for (int gr = 0; gr < NG; ++gr)
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) acci[blk][gr][e] += __float2int_rn(accf[blk][gr][e]);
         }
 
         // -------- segment end: stage the int32 sums [row][token] --------
 #pragma unroll
-        for (int blk = 0; blk < 2; ++blk) {
-            const int r0 = 32 * warp + 16 * blk + g;
+        for (int blk = 0; blk < BPW; ++blk) {
+            const int r0 = RW * warp + 16 * blk + g;
 #pragma unroll
             for (int gr = 0; gr < NG; ++gr) {
                 const int col = 8 * gr + 2 * t4;
@@ -342,31 +404,32 @@ w8a8_stream_kernel(const __grid_constant__ CUtensorMap tmap_w,
                 *reinterpret_cast<int2*>(&sm.stg[(r0 + 8) * MP + col]) = make_int2(acci[blk][gr][2], acci[blk][gr][3]);
             }
         }
-        consumer_sync();
+        consumer_sync<CW>();
 
         const int seg_len = seg_end - seg_begin;
         const bool whole = seg_len == p.KT;
         int32_t* gacc = p.ws_acc + (size_t)nt * BN * MP;
         if (!whole) {
-            for (int e = tid; e < BN * MP; e += kConsumerThreads) {
+            for (int e = tid; e < BN * MP; e += CT) {
                 const int r = e / MP, m = e - (e / MP) * MP;
                 if (m < p.M && nt * BN + r < p.N) atomicAdd(&gacc[e], sm.stg[e]);
             }
             __threadfence();
-            consumer_sync();
+            consumer_sync<CW>();
             if (tid == 0) {
                 __threadfence();
                 const unsigned prev = atomicAdd(&p.ws_cnt[nt], (unsigned)seg_len);
                 *sm.flag = (prev + (unsigned)seg_len == (unsigned)p.KT) ? 1 : 0;
             }
-            consumer_sync();
+            consumer_sync<CW>();
         }
         const bool finisher = whole || *sm.flag;
         if (finisher) {
             if (!whole) __threadfence();
-            const int r = tid;                 // one output channel per thread
+            // the first BN consumer threads (warps 0..3) own one output channel each
+            const int r = tid;
             const int n = nt * BN + r;
-            const bool valid = n < p.N;
+            const bool valid = r < BN && n < p.N;
             const float swn = valid ? p.sw[n] : 0.f;
             if (EPI == (int)Epi::Linear) {
                 if (valid) {
@@ -381,35 +444,37 @@ w8a8_stream_kernel(const __grid_constant__ CUtensorMap tmap_w,
                     }
                 }
             } else {
-                for (int m = 0; m < p.M; ++m) {
-                    unsigned long long key = 0ull;
-                    if (valid) {
-                        const int32_t acc = whole ? sm.stg[r * MP + m] : atomicExch(&gacc[r * MP + m], 0);
-                        const float yv = __fmul_rn(__int2float_rn(acc), __fmul_rn(sm.sx[m], swn));
-                        key = ((unsigned long long)ordered_bits(yv) << 32) |
-                              (unsigned long long)(0xFFFFFFFFu - (unsigned)n);
+                if (r < BN) {
+                    for (int m = 0; m < p.M; ++m) {
+                        unsigned long long key = 0ull;
+                        if (valid) {
+                            const int32_t acc = whole ? sm.stg[r * MP + m] : atomicExch(&gacc[r * MP + m], 0);
+                            const float yv = __fmul_rn(__int2float_rn(acc), __fmul_rn(sm.sx[m], swn));
+                            key = ((unsigned long long)ordered_bits(yv) << 32) |
+                                  (unsigned long long)(0xFFFFFFFFu - (unsigned)n);
+                        }
+                        key = warp_max_u64(key);
+                        if (lane == 0) sm.red[warp * MP + m] = key;
                     }
-                    key = warp_max_u64(key);
-                    if (lane == 0) sm.red[warp * MP + m] = key;
                 }
-                consumer_sync();
+                consumer_sync<CW>();
                 if (tid < p.M) {
                     unsigned long long k = sm.red[tid];
 #pragma unroll
-                    for (int w = 1; w < kConsumerWarps; ++w) {
+                    for (int w = 1; w < BN / 32; ++w) {
                         const unsigned long long o = sm.red[w * MP + tid];
                         k = o > k ? o : k;
                     }
                     atomicMax(&p.keys[tid], k);
                 }
                 __threadfence();
-                consumer_sync();
+                consumer_sync<CW>();
                 if (tid == 0) {
                     __threadfence();
                     const unsigned prev = atomicAdd(p.done, 1u);
                     *sm.flag = (prev + 1u == (unsigned)p.NT) ? 2 : 0;
                 }
-                consumer_sync();
+                consumer_sync<CW>();
                 if (*sm.flag == 2) {
                     __threadfence();
                     if (tid < p.M) {
@@ -422,7 +487,7 @@ w8a8_stream_kernel(const __grid_constant__ CUtensorMap tmap_w,
             }
             if (!whole && tid == 0) atomicExch(&p.ws_cnt[nt], 0u);
         }
-        consumer_sync();   // staging buffer and flags are reused by the next segment
+        consumer_sync<CW>();   // staging buffer and flags are reused by the next segment
     }
 }
 
@@ -439,12 +504,16 @@ struct Bf16Params {
 };
 
 template <int NG>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__((kBf16Warps + 1) * 32, 1)
 bf16_stream_kernel(const __grid_constant__ CUtensorMap tmap_w,
                    const __grid_constant__ CUtensorMap tmap_x, const Bf16Params p) {
     using C = Cfg<NG>;
     constexpr int MP = C::MP;
     constexpr int Stages = C::Stages;
+    constexpr int CW = kBf16Warps;
+    constexpr int CT = CW * 32;
+    constexpr int RW = BN / CW;
+    constexpr int BPW = RW / 16;
     extern __shared__ uint8_t smem_raw[];
     Smem<Stages, C::StageBytes, C::StgWords, MP> sm(smem_raw);
     float* stgf = reinterpret_cast<float*>(sm.stg);
@@ -458,7 +527,7 @@ bf16_stream_kernel(const __grid_constant__ CUtensorMap tmap_w,
     if (tid == 0) {
         for (int s = 0; s < Stages; ++s) {
             mbar_init(&sm.full[s], 1);
-            mbar_init(&sm.empty[s], kConsumerWarps);
+            mbar_init(&sm.empty[s], CW);
         }
         *sm.abort = 0;
         fence_barrier_init();
@@ -466,7 +535,7 @@ bf16_stream_kernel(const __grid_constant__ CUtensorMap tmap_w,
     __syncthreads();
     allow_dependent_launch();
 
-    if (warp == kConsumerWarps) {
+    if (warp == CW) {
         if (lane == 0)
             produce<Stages>(sm, &tmap_w, &tmap_x, a, b, p.KT, BKB / 2,
                             (unsigned)(kWTileBytes + C::XBytes));
@@ -476,10 +545,10 @@ bf16_stream_kernel(const __grid_constant__ CUtensorMap tmap_w,
 
     const int li = lane & 7, lj = lane >> 3;
     const int g = lane >> 2, t4 = lane & 3;
-    uint32_t w_row_off[2];
+    uint32_t w_row_off[BPW];
 #pragma unroll
-    for (int blk = 0; blk < 2; ++blk)
-        w_row_off[blk] = (uint32_t)((32 * warp + 16 * blk + li + 8 * (lj & 1)) * BKB);
+    for (int blk = 0; blk < BPW; ++blk)
+        w_row_off[blk] = (uint32_t)((RW * warp + 16 * blk + li + 8 * (lj & 1)) * BKB);
     uint32_t w_chunk_off[4];
 #pragma unroll
     for (int ks = 0; ks < 4; ++ks) w_chunk_off[ks] = (uint32_t)((((2 * ks) + (lj >> 1)) ^ li) << 4);
@@ -487,7 +556,7 @@ bf16_stream_kernel(const __grid_constant__ CUtensorMap tmap_w,
 #pragma unroll
     for (int cq = 0; cq < 2; ++cq) x_chunk_off[cq] = (uint32_t)(((4 * cq + lj) ^ li) << 4);
 
-    float acc[2][NG][4];
+    float acc[BPW][NG][4];
     int s = 0, phase = 0;
     int i = a;
     while (i < b) {
@@ -495,7 +564,7 @@ bf16_stream_kernel(const __grid_constant__ CUtensorMap tmap_w,
         const int seg_begin = i;
         const int seg_end = min(b, (nt + 1) * p.KT);
 #pragma unroll
-        for (int blk = 0; blk < 2; ++blk)
+        for (int blk = 0; blk < BPW; ++blk)
 #pragma unroll
             for (int gr = 0; gr < NG; ++gr)
 #pragma unroll
@@ -515,7 +584,7 @@ bf16_stream_kernel(const __grid_constant__ CUtensorMap tmap_w,
                     ldmatrix_x4(xb + (uint32_t)((8 * gr + li) * BKB) + x_chunk_off[cq],
                                 bx[gr][0], bx[gr][1], bx[gr][2], bx[gr][3]);
 #pragma unroll
-                for (int blk = 0; blk < 2; ++blk) {
+                for (int blk = 0; blk < BPW; ++blk) {
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
                         const int ks = 2 * cq + h;
@@ -533,8 +602,8 @@ bf16_stream_kernel(const __grid_constant__ CUtensorMap tmap_w,
         }
 
 #pragma unroll
-        for (int blk = 0; blk < 2; ++blk) {
-            const int r0 = 32 * warp + 16 * blk + g;
+        for (int blk = 0; blk < BPW; ++blk) {
+            const int r0 = RW * warp + 16 * blk + g;
 #pragma unroll
             for (int gr = 0; gr < NG; ++gr) {
                 const int col = 8 * gr + 2 * t4;
@@ -542,29 +611,29 @@ bf16_stream_kernel(const __grid_constant__ CUtensorMap tmap_w,
                 *reinterpret_cast<float2*>(&stgf[(r0 + 8) * MP + col]) = make_float2(acc[blk][gr][2], acc[blk][gr][3]);
             }
         }
-        consumer_sync();
+        consumer_sync<CW>();
         const int seg_len = seg_end - seg_begin;
         const bool whole = seg_len == p.KT;
         float* gacc = p.ws_acc + (size_t)nt * BN * MP;
         if (!whole) {
-            for (int e = tid; e < BN * MP; e += kConsumerThreads) {
+            for (int e = tid; e < BN * MP; e += CT) {
                 const int r = e / MP, m = e - (e / MP) * MP;
                 if (m < p.M && nt * BN + r < p.N) atomicAdd(&gacc[e], stgf[e]);
             }
             __threadfence();
-            consumer_sync();
+            consumer_sync<CW>();
             if (tid == 0) {
                 __threadfence();
                 const unsigned prev = atomicAdd(&p.ws_cnt[nt], (unsigned)seg_len);
                 *sm.flag = (prev + (unsigned)seg_len == (unsigned)p.KT) ? 1 : 0;
             }
-            consumer_sync();
+            consumer_sync<CW>();
         }
         if (whole || *sm.flag) {
             if (!whole) __threadfence();
             const int r = tid;
             const int n = nt * BN + r;
-            if (n < p.N) {
+            if (r < BN && n < p.N) {
                 for (int m = 0; m < p.M; ++m) {
                     const float v = whole ? stgf[r * MP + m] : atomicExch(&gacc[r * MP + m], 0.f);
                     p.y[(size_t)m * p.N + n] = v;
@@ -572,18 +641,18 @@ bf16_stream_kernel(const __grid_constant__ CUtensorMap tmap_w,
             }
             if (!whole && tid == 0) atomicExch(&p.ws_cnt[nt], 0u);
         }
-        consumer_sync();
+        consumer_sync<CW>();
     }
 }
 
 template <class P, class... Args>
-cudaError_t launch_ex(void (*kern)(Args...), int grid, int smem, cudaStream_t s,
+cudaError_t launch_ex(void (*kern)(Args...), int grid, int threads, int smem, cudaStream_t s,
                       const CUtensorMap& tw, const CUtensorMap& tx, const P& params) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(threads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
@@ -632,9 +701,11 @@ cudaError_t launch_w8a8_stream(const W8A8Launch& a, int num_sms, cudaStream_t s)
 #define QV_W8A8_CASE(NGV)                                                                    \
     case NGV:                                                                                \
         return lm ? launch_ex(w8a8_stream_kernel<NGV, (int)Epi::LmHead>, grid,               \
-                              Cfg<NGV>::SmemBytes, s, a.tmap_w, a.tmap_x, p)                 \
+                              (kW8A8Warps + 1) * 32, Cfg<NGV>::SmemBytes, s, a.tmap_w,       \
+                              a.tmap_x, p)                                                   \
                   : launch_ex(w8a8_stream_kernel<NGV, (int)Epi::Linear>, grid,               \
-                              Cfg<NGV>::SmemBytes, s, a.tmap_w, a.tmap_x, p);
+                              (kW8A8Warps + 1) * 32, Cfg<NGV>::SmemBytes, s, a.tmap_w,       \
+                              a.tmap_x, p);
     switch (NG) {
         QV_W8A8_CASE(1)
         QV_W8A8_CASE(2)
@@ -659,7 +730,7 @@ cudaError_t launch_bf16_stream(const Bf16Launch& a, int num_sms, cudaStream_t s)
     p.ws_cnt = reinterpret_cast<unsigned*>(ws + L.counters);
     const int grid = (int)(p.T < num_sms ? p.T : num_sms);
 #define QV_BF16_CASE(NGV) \
-    case NGV: return launch_ex(bf16_stream_kernel<NGV>, grid, Cfg<NGV>::SmemBytes, s, a.tmap_w, a.tmap_x, p);
+    case NGV: return launch_ex(bf16_stream_kernel<NGV>, grid, (kBf16Warps + 1) * 32, Cfg<NGV>::SmemBytes, s, a.tmap_w, a.tmap_x, p);
     switch (NG) {
         QV_BF16_CASE(1)
         QV_BF16_CASE(2)

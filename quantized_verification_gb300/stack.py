@@ -1,0 +1,228 @@
+"""W8A8 verify pass over a decoder-layer stack, built from the libqv calls.
+
+A verify step of M = B*(gamma+1) tokens runs, for every layer, the four
+quantize -> W8A8 linear phases of a decoder layer (q|k|v, o, gate|up, down),
+then the LM head fused with the greedy argmax and the acceptance of the
+longest matching draft prefix:
+
+    per layer: qv_quantize_act(h)    -> qv_w8a8_linear(Wqkv)      N = q+2kv
+               qv_quantize_act(attn) -> qv_w8a8_linear(Wo)
+               qv_quantize_act(h2)   -> qv_w8a8_linear(Wgate|up)  N = 2*ffn
+               qv_quantize_act(act)  -> qv_w8a8_linear(Wdown)
+    then       qv_quantize_act(h_final) -> qv_lm_head_argmax -> qv_accept
+
+(Quasar, gist.science/ja summary, section 2.2 item 3 for the quantized
+linears; gist.science/it summary, section 2 item 3 for the acceptance test.)
+Attention, normalisation and the activation function sit between these
+phases in a real model; they are not part of the quantized path and are not
+run: each phase reads its own seeded synthetic input of the right shape.
+q|k|v and gate|up share their input in a decoder layer, so their weights are
+stored concatenated along the output channels (each output column is computed
+independently, so the results are those of the separate projections).
+
+Weights are generated on the device (seeded), quantized once with
+qv_quantize_weight and kept resident in HBM; only the int8 codes and fp32
+scales are kept (and the bf16 originals when the comparator is wanted). One
+step is captured into a CUDA graph; consecutive kernels overlap through
+programmatic dependent launch.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import qv, synth
+
+
+class VerifyStack:
+    def __init__(self, model: dict = synth.QWEN3_8B, layers: int | None = None, B: int = 1,
+                 gamma: int = 4, seed: int = 0, device: str = "cuda", keep_bf16: bool = False,
+                 y_dtype=torch.float32):
+        self.model = model
+        self.layers = model["layers"] if layers is None else layers
+        self.B, self.gamma = B, gamma
+        self.M = B * (gamma + 1)
+        self.V = model["vocab"]
+        self.device = torch.device(device)
+        self.seed = seed
+        self.y_dtype = y_dtype
+        h = model["hidden"]
+        q = model.get("q", h)
+        kv = model["kv"]
+        ffn = model["ffn"]
+        # (name, K, N) of the four phases of a layer
+        self.phases = [("qkv", h, q + 2 * kv), ("o", q, h), ("gate_up", h, 2 * ffn), ("down", ffn, h)]
+        self.weights = []      # per layer: list of (wq, sw) per phase
+        self.weights_bf16 = [] if keep_bf16 else None
+        self.inputs = []       # per layer: list of bf16 [M, K] per phase
+        dev = self.device
+        for l in range(self.layers):
+            lw, lb, li = [], [], []
+            for (name, K, N) in self.phases:
+                w = synth.weights(N, K, synth.subseed(seed, "w", l, name), device=dev)
+                wq = torch.empty(N, K, dtype=torch.int8, device=dev)
+                sw = torch.empty(N, dtype=torch.float32, device=dev)
+                qv.qv_quantize_weight(w, wq, sw)
+                lw.append((wq, sw))
+                if keep_bf16:
+                    lb.append(w)
+                else:
+                    del w
+                li.append(synth.activations(self.M, K, synth.subseed(seed, "x", l, name), device=dev))
+            self.weights.append(lw)
+            if keep_bf16:
+                self.weights_bf16.append(lb)
+            self.inputs.append(li)
+        wl = synth.weights(self.V, h, synth.subseed(seed, "w", "lm_head"), device=dev)
+        self.lm_wq = torch.empty(self.V, h, dtype=torch.int8, device=dev)
+        self.lm_sw = torch.empty(self.V, dtype=torch.float32, device=dev)
+        qv.qv_quantize_weight(wl, self.lm_wq, self.lm_sw)
+        self.lm_bf16 = wl if keep_bf16 else None
+        del wl
+        self.h_final = synth.activations(self.M, h, synth.subseed(seed, "x", "final"), device=dev)
+        self.drafts = torch.zeros(B, max(gamma, 0), dtype=torch.int32, device=dev)
+
+        kmax = max(K for (_, K, _) in self.phases)
+        nmax = max(N for (_, _, N) in self.phases)
+        self.xq = torch.empty(self.M, max(kmax, h), dtype=torch.int8, device=dev)
+        self.sx = torch.empty(self.M, dtype=torch.float32, device=dev)
+        self.y = torch.empty(self.M * nmax, dtype=y_dtype, device=dev)
+        self.tokens = torch.empty(self.M, dtype=torch.int32, device=dev)
+        self.max_logit = torch.empty(self.M, dtype=torch.float32, device=dev)
+        self.accept_len = torch.empty(B, dtype=torch.int32, device=dev)
+        self.out_tokens = torch.empty(B, gamma + 1, dtype=torch.int32, device=dev)
+        ws_bytes = max([qv.qv_workspace_bytes(qv.QV_OP_LINEAR, self.M, K, N) for (_, K, N) in self.phases]
+                       + [qv.qv_workspace_bytes(qv.QV_OP_LM_HEAD, self.M, h, self.V)])
+        self.ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
+        self.graph = None
+        torch.cuda.synchronize(dev)
+
+    # ------------------------------------------------------------------ sizes
+    def weight_bytes(self) -> int:
+        """int8 weight bytes streamed by one step (linears + LM head)."""
+        per_layer = sum(N * K for (_, K, N) in self.phases)
+        return per_layer * self.layers + self.V * self.model["hidden"]
+
+    def algorithmic_bytes(self) -> int:
+        """All bytes one step must move at least: int8 weights and fp32 scales,
+        the activations read (bf16) and their int8 codes written and read back,
+        token scales, fp32/bf16 outputs, LM-head and acceptance I/O."""
+        M = self.M
+        yb = 4 if self.y_dtype == torch.float32 else 2
+        total = 0
+        for (_, K, N) in self.phases:
+            total += N * K + 4 * N                     # weights + channel scales
+            total += M * K * 2 + M * K + 4 * M         # act quant: read bf16, write int8 + scale
+            total += M * K + 4 * M + M * N * yb        # GEMM: read codes + scales, write y
+        total *= self.layers
+        h = self.model["hidden"]
+        total += M * h * 2 + M * h + 4 * M             # final act quant
+        total += self.V * h + 4 * self.V + M * h + 4 * M + 4 * M   # LM head + tokens
+        total += 4 * M + 4 * self.B * self.gamma + 4 * self.B + 4 * M  # accept I/O
+        return total
+
+    def linear_launch_bytes(self):
+        """Algorithmic bytes of each qv_w8a8_linear launch of a step, in order."""
+        M = self.M
+        yb = 4 if self.y_dtype == torch.float32 else 2
+        one = [N * K + 4 * N + M * K + 4 * M + M * N * yb for (_, K, N) in self.phases]
+        return one * self.layers
+
+    def _xq(self, K):
+        return self.xq.view(-1)[: self.M * K].view(self.M, K)
+
+    # ------------------------------------------------------------------ step
+    def enqueue(self, stream=None):
+        """Enqueue one verify step on `stream` (current stream if None)."""
+        M = self.M
+        ws = self.ws
+        for l in range(self.layers):
+            for p, (name, K, N) in enumerate(self.phases):
+                xq = self._xq(K)
+                qv.qv_quantize_act(self.inputs[l][p], xq, self.sx, stream=stream)
+                wq, sw = self.weights[l][p]
+                qv.qv_w8a8_linear(xq, self.sx, wq, sw, self.y[: M * N].view(M, N), ws, stream=stream)
+        xq = self._xq(self.model["hidden"])
+        qv.qv_quantize_act(self.h_final, xq, self.sx, stream=stream)
+        qv.qv_lm_head_argmax(xq, self.sx, self.lm_wq, self.lm_sw, self.tokens, ws,
+                             max_logit=self.max_logit, stream=stream)
+        qv.qv_accept(self.tokens.view(self.B, self.gamma + 1), self.drafts if self.gamma > 0 else None,
+                     self.accept_len, self.out_tokens, stream=stream)
+
+    def launches_per_step(self) -> int:
+        return self.layers * len(self.phases) * 2 + 3
+
+    @staticmethod
+    def _capture(fn, device):
+        s = torch.cuda.Stream(device=device)
+        s.wait_stream(torch.cuda.current_stream(device))
+        with torch.cuda.stream(s):
+            fn(s)
+        torch.cuda.current_stream(device).wait_stream(s)
+        torch.cuda.synchronize(device)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn(torch.cuda.current_stream(device))
+        return g
+
+    def capture(self):
+        """Capture one step into a CUDA graph (after one eager warm-up step)."""
+        self.graph = self._capture(self.enqueue, self.device)
+        return self.graph
+
+    def replay(self):
+        if self.graph is None:
+            self.capture()
+        self.graph.replay()
+
+    # ------------------------------------------------------------------ host API
+    def _step_inputs(self):
+        return [x for li in self.inputs for x in li] + [self.h_final]
+
+    def pinned_host_inputs(self):
+        """Pinned host copies of every per-step input (activations, drafts)."""
+        flat = self._step_inputs()
+        host = [torch.empty_like(x, device="cpu").pin_memory() for x in flat]
+        for hsrc, d in zip(host, flat):
+            hsrc.copy_(d)
+        drafts = torch.empty_like(self.drafts, device="cpu").pin_memory()
+        drafts.copy_(self.drafts)
+        return host, drafts
+
+    def step_from_host(self, host_inputs, host_drafts, out_len, out_tokens, graph=None):
+        """One verify step from host buffers: copy the step's inputs to the
+        device, run the captured step, copy the accepted lengths and tokens
+        back (into pinned host tensors). Returns bytes copied (h2d, d2h)."""
+        h2d = 0
+        for d, hsrc in zip(self._step_inputs(), host_inputs):
+            d.copy_(hsrc, non_blocking=True)
+            h2d += hsrc.numel() * hsrc.element_size()
+        self.drafts.copy_(host_drafts, non_blocking=True)
+        h2d += host_drafts.numel() * host_drafts.element_size()
+        (graph or self.graph).replay()
+        out_len.copy_(self.accept_len, non_blocking=True)
+        out_tokens.copy_(self.out_tokens, non_blocking=True)
+        d2h = out_len.numel() * 4 + out_tokens.numel() * 4
+        return h2d, d2h
+
+    # ------------------------------------------------------------------ comparator
+    def prepare_bf16(self):
+        assert self.weights_bf16 is not None, "construct with keep_bf16=True"
+        h = self.model["hidden"]
+        ws_bytes = max([qv.qv_workspace_bytes(qv.QV_OP_BF16_LINEAR, self.M, K, N) for (_, K, N) in self.phases]
+                       + [qv.qv_workspace_bytes(qv.QV_OP_BF16_LINEAR, self.M, h, self.V)])
+        self.ws_bf16 = torch.zeros(ws_bytes, dtype=torch.uint8, device=self.device)
+        self.logits_bf16 = torch.empty(self.M, self.V, dtype=torch.float32, device=self.device)
+        self.y32 = torch.empty(self.y.numel(), dtype=torch.float32, device=self.device)
+
+    def enqueue_bf16(self, stream=None):
+        """The same step with BF16 weights (qv_bf16_linear everywhere, LM-head
+        logits written in fp32): the high-precision verifier being replaced."""
+        M = self.M
+        for l in range(self.layers):
+            for p, (name, K, N) in enumerate(self.phases):
+                y = self.y32[: M * N].view(M, N)
+                qv.qv_bf16_linear(self.inputs[l][p], self.weights_bf16[l][p], y, self.ws_bf16, stream=stream)
+        qv.qv_bf16_linear(self.h_final, self.lm_bf16, self.logits_bf16, self.ws_bf16, stream=stream)
+
+    def bf16_weight_bytes(self) -> int:
+        return 2 * self.weight_bytes()
