@@ -239,6 +239,40 @@ QV_API qv_status qv_device_error(unsigned int* code);
  * (queried once per device). Host function. */
 QV_API int qv_num_sms(void);
 
+/* Bytes of the library's built-in scratch buffer (see qv_w8a8_linear_noalloc). */
+#define QV_NOALLOC_SCRATCH_BYTES (4u << 20)
+
+/*
+ * qv_w8a8_linear_noalloc -- qv_w8a8_linear for callers that cannot allocate
+ * device memory. The paper has no counterpart: this is a deployment aid.
+ *
+ * Who needs it: code that runs where cudaMalloc is off limits -- a plugin or
+ * callback handed only the input and output buffers of a host framework, code
+ * running under a memory budget owned by someone else, or a caller that must
+ * not allocate between steps -- and therefore cannot provide the zero-filled
+ * workspace qv_w8a8_linear asks for.
+ *
+ * Same arguments and same results (bit for bit) as qv_w8a8_linear, minus the
+ * workspace: the split-K partial sums live in a buffer of
+ * QV_NOALLOC_SCRATCH_BYTES compiled into the library (a static device array;
+ * every GPU that loads the library holds it until the process exits). The
+ * call itself allocates nothing.
+ *   - The first call on a device looks up the buffer's device address for
+ *     that device (once); make that first call before any stream capture.
+ *   - Shapes whose workspace, qv_workspace_bytes(QV_OP_LINEAR, M, K, N), is
+ *     larger than the buffer are rejected with QV_ERR_UNSUPPORTED (about
+ *     N <= 131000 at M <= 8, N <= 16000 at M = 64).
+ *   - Each call clears the part of the buffer it uses (cudaMemsetAsync on
+ *     `stream`) before its kernel runs. All calls on a device share the one
+ *     buffer: calls whose GPU work overlaps (different streams, no ordering
+ *     between them) race on it and give wrong results. Order them on one
+ *     stream, or use qv_w8a8_linear with a workspace per stream.
+ */
+QV_API qv_status qv_w8a8_linear_noalloc(const int8_t* xq, const float* sx, int M, int K,
+                                        const int8_t* wq, const float* sw, int N,
+                                        void* y, qv_dtype y_dtype, int32_t* acc_debug,
+                                        cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -147,6 +147,11 @@ qv_status check_gemm_common(const void* xq, const void* sx, int M, int K, const 
 
 }  // namespace
 
+namespace qv {
+// Lets other translation units of the library report through qv_last_error().
+qv_status report_error(qv_status st, const char* msg) { return fail(st, "%s", msg); }
+}  // namespace qv
+
 extern "C" {
 
 const char* qv_last_error(void) { return g_last_error; }

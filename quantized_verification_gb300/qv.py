@@ -24,7 +24,8 @@ QV_MAX_M = 256
 # Symbols include/qv.h declares (checked against the library by the tests).
 EXPORTS = ("qv_quantize_act", "qv_w8a8_linear", "qv_lm_head_argmax", "qv_accept",
            "qv_quantize_weight", "qv_bf16_linear", "qv_workspace_bytes",
-           "qv_last_error", "qv_device_error", "qv_num_sms")
+           "qv_last_error", "qv_device_error", "qv_num_sms", "qv_w8a8_linear_noalloc")
+QV_NOALLOC_SCRATCH_BYTES = 4 << 20
 
 
 class QVError(RuntimeError):
@@ -56,6 +57,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         L.qv_accept.argtypes = [P, P, I, I, P, P, P]
         L.qv_quantize_weight.argtypes = [P, I, I, I, P, P, P]
         L.qv_bf16_linear.argtypes = [P, I, I, P, I, P, P, S, P]
+        L.qv_w8a8_linear_noalloc.argtypes = [P, P, I, I, P, P, I, P, I, P, P]
         L.qv_workspace_bytes.argtypes = [I, I, I, I]
         L.qv_workspace_bytes.restype = S
         L.qv_last_error.argtypes = []
@@ -64,7 +66,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         L.qv_num_sms.argtypes = []
         L.qv_num_sms.restype = I
         for name in ("qv_quantize_act", "qv_w8a8_linear", "qv_lm_head_argmax", "qv_accept",
-                     "qv_quantize_weight", "qv_bf16_linear", "qv_device_error"):
+                     "qv_quantize_weight", "qv_bf16_linear", "qv_device_error",
+                     "qv_w8a8_linear_noalloc"):
             getattr(L, name).restype = st
         _lib = L
         return L
@@ -143,6 +146,18 @@ def qv_w8a8_linear(xq, sx, wq, sw, y, workspace, acc_debug=None, stream=None):
     _check(load().qv_w8a8_linear(_ptr(xq), _ptr(sx), M, K, _ptr(wq), _ptr(sw), N, _ptr(y),
                                  _dtype(y), _ptr(acc_debug), _ptr(workspace), workspace.numel(),
                                  ctypes.c_void_p(_stream(stream))))
+
+
+def qv_w8a8_linear_noalloc(xq, sx, wq, sw, y, acc_debug=None, stream=None):
+    """qv_w8a8_linear without a workspace argument, for callers that cannot
+    allocate device memory: the library's built-in scratch buffer is used."""
+    M, K = xq.shape
+    N = wq.shape[0]
+    _need(wq.shape == (N, K) and wq.dtype == torch.int8 and xq.dtype == torch.int8, "int8 xq [M,K], wq [N,K]")
+    _need(sx.shape == (M,) and sw.shape == (N,), "sx [M], sw [N]")
+    _need(y.shape == (M, N), "y must be [M, N]")
+    _check(load().qv_w8a8_linear_noalloc(_ptr(xq), _ptr(sx), M, K, _ptr(wq), _ptr(sw), N, _ptr(y),
+                                         _dtype(y), _ptr(acc_debug), ctypes.c_void_p(_stream(stream))))
 
 
 def qv_lm_head_argmax(xq, sx, wq, sw, tokens, workspace, max_logit=None, stream=None):
