@@ -68,7 +68,8 @@ typedef enum { QV_F32 = 0, QV_BF16 = 1 } qv_dtype;
 typedef enum {
     QV_OP_LINEAR = 0,         /* qv_w8a8_linear                            */
     QV_OP_LM_HEAD = 1,        /* qv_lm_head_argmax (N = vocabulary size V) */
-    QV_OP_BF16_LINEAR = 2     /* qv_bf16_linear                            */
+    QV_OP_BF16_LINEAR = 2,    /* qv_bf16_linear                            */
+    QV_OP_VERIFY_STACK = 3    /* qv_verify_stack (K, N = largest K, N / V) */
 } qv_op;
 
 /* floor((2^31 - 1) / 127^2): the int32 accumulation stays exact up to here. */
@@ -217,6 +218,59 @@ QV_API qv_status qv_quantize_weight(const void* w, qv_dtype w_dtype, int N, int 
 QV_API qv_status qv_bf16_linear(const uint16_t* x, int M, int K, const uint16_t* w,
                          int N, float* y, void* workspace,
                          size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * qv_verify_stack -- one whole verify pass in a single persistent launch:
+ * a sequence of quantize -> W8A8 linear phases (a1 + a2 per phase), then
+ * optionally the LM head with the greedy argmax (a3) and the acceptance (a4).
+ * It computes exactly what the per-op calls compute, in the same order, with
+ * bit-identical results: phase i equals qv_quantize_act(linears[i].x) followed
+ * by qv_w8a8_linear, the LM head equals qv_quantize_act + qv_lm_head_argmax,
+ * the acceptance equals qv_accept.
+ *   Quasar, gist.science/ja summary, section 2.2 item 3 (online quantize,
+ *   INT8 GEMM, dequantize, for every linear of the verifier's forward pass);
+ *   gist.science/it summary, section 2 item 3 (acceptance on the dequantized
+ *   logits).
+ * Phase i+1 starts only after every output of phase i is written (a
+ * device-wide barrier), as if its input depended on them; weight codes of
+ * later phases are streamed while earlier phases compute, since they never
+ * depend on activations.
+ *
+ *   linears   host array of n_linears descriptors (read during the call only);
+ *             each: x [M*K] (x_dtype, 16-byte aligned), act_mul [K] or NULL
+ *             (16-byte aligned), wq [N*K] int8, sw [N], y [M*N] fp32 or NULL
+ *             (output not stored).
+ *   lm_head   host descriptor of the LM head (N = V; its y is ignored), or
+ *             NULL to run the linears only.
+ *   tokens [M], max_logit [M] or NULL: as qv_lm_head_argmax (required with
+ *             lm_head).
+ *   accept_len [B], out_tokens [B*(gamma+1)]: as qv_accept, or both NULL to
+ *             skip acceptance; then B*(gamma+1) must equal M and draft
+ *             [B*gamma] must be given when gamma > 0.
+ *   workspace: qv_workspace_bytes(QV_OP_VERIFY_STACK, M, K_max, N_max) bytes
+ *             with K_max the largest K and N_max the largest N (or V),
+ *             zero-filled before first use; every call leaves its counters
+ *             and partial sums zero-filled (its int8 code area is scratch).
+ *   1 <= M <= 16. The kernel keeps one CTA resident on every SM (cooperative
+ *   launch); at most 150 phases (linears + LM head) run per launch and longer
+ *   stacks are split into consecutive launches on the stream.
+ */
+typedef struct {
+    const void* x;          /* [M*K] input activations, x_dtype of the call */
+    const float* act_mul;   /* [K] smoothing multipliers, or NULL           */
+    const int8_t* wq;       /* [N*K] int8 weight codes                       */
+    const float* sw;        /* [N] fp32 weight scales                        */
+    float* y;               /* [M*N] fp32 dequantized output, or NULL        */
+    int K, N;
+} qv_linear_desc;
+
+QV_API qv_status qv_verify_stack(const qv_linear_desc* linears, int n_linears,
+                                 const qv_linear_desc* lm_head, int M, qv_dtype x_dtype,
+                                 const int32_t* draft, int B, int gamma,
+                                 int32_t* tokens, float* max_logit,
+                                 int32_t* accept_len, int32_t* out_tokens,
+                                 void* workspace, size_t workspace_bytes,
+                                 cudaStream_t stream);
 
 /* Workspace bytes an op needs for the given shape (N = V for the LM head);
  * 0 for an invalid shape. Host function, enqueues nothing. */

@@ -46,6 +46,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <cstring>
 
 #include "qv_internal.h"
 #include "qv_ptx.cuh"
@@ -663,6 +664,552 @@ cudaError_t launch_ex(void (*kern)(Args...), int grid, int threads, int smem, cu
     return cudaLaunchKernelEx(&cfg, kern, tw, tx, params);
 }
 
+// ---------------------------------------------------------------------------
+// Persistent verify-stack kernel: a sequence of quantize -> W8A8 linear phases
+// and (optionally) the LM head with the greedy argmax and the acceptance, in
+// one cooperative launch (one CTA per SM, all resident).
+//
+//  - The producer warp streams the weight tiles of every phase, in phase
+//    order, through a deep ring; weights never depend on activations, so it
+//    runs ahead across phase boundaries and HBM stays busy while consumers
+//    wait for the previous phase.
+//  - Consumers start phase p once every CTA has finished phase p-1 (a grid
+//    barrier: an arrival counter in the workspace, read with acquire loads,
+//    waited on for at most kWaitLimitNs). They compute the per-token scales of
+//    the phase input (every CTA computes the same bits), quantize the
+//    128-byte activation chunks their tiles need into shared memory (all
+//    loads of a phase issued together), then run the same tile MMA and
+//    stream-K epilogue as the single-linear kernel.
+//  - The LM head's last finishing tile decodes the argmax keys and the same
+//    threads apply the acceptance rule.
+// ---------------------------------------------------------------------------
+struct StackPhase {
+    const void* x;            // [M][K] fp32 or bf16 input of the phase
+    const float* act_mul;     // [K] smoothing multipliers or null
+    const float* sw;          // [N]
+    float* y;                 // [M][N] fp32 output or null (LM head: unused)
+    int K, N, KT, NT;
+};
+
+struct StackParams {
+    CUtensorMap tmap_w[kMaxStackPhases];   // int8 [N rows][K], box {128, 128}, 128B swizzle
+    CUtensorMap tmap_x;                    // int8 codes [M rows][kmax], box {128, MP}, 128B swizzle
+    StackPhase ph[kMaxStackPhases];
+    int n_phases;             // phases in this launch
+    int lm_last;              // the last phase is the LM head (argmax + accept)
+    int M, x_bf16, kmax;
+    int B, gamma;
+    const int32_t* draft;
+    int32_t* tokens;
+    float* max_logit;
+    int32_t* accept_len;
+    int32_t* out_tokens;
+    int32_t* ws_acc;
+    unsigned* ws_cnt;
+    unsigned long long* keys;
+    unsigned* sync;           // [0] barrier arrivals [1] exits [2] abort [3] LM tiles done
+    int8_t* xq;               // [M][kmax] int8 codes of the current phase input
+};
+
+template <int NG>
+struct StackCfg {
+    static constexpr int MP = 8 * NG;
+    static constexpr int XBytes = MP * BKB;
+    static constexpr int XSlot = ((XBytes + 1023) / 1024) * 1024;
+    static constexpr int StageBytes = kWTileBytes + XSlot;
+    static constexpr int Stages = NG == 1 ? 12 : 11;
+    static constexpr int StgWords = BN * MP;
+    static constexpr int SmemBytes = 1024 + Stages * StageBytes + StgWords * 4 + 2 * Stages * 8 +
+                                     kMaxConsumerWarps * MP * 8 + 3 * MP * 4 +
+                                     kMaxConsumerWarps * MP * 4 + 64;
+};
+
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Thread 0 of the consumers waits until `target` arrivals were counted (or the
+// launch was aborted); returns false when the wait was cut short.
+__device__ __forceinline__ bool grid_wait(unsigned* sync, unsigned target) {
+    if (ld_acquire_gpu(&sync[0]) >= target) return true;
+    const unsigned long long t0 = global_timer_ns();
+    while (true) {
+        if (ld_acquire_gpu(&sync[2])) return false;
+        if (ld_acquire_gpu(&sync[0]) >= target) return true;
+        if (global_timer_ns() - t0 > kWaitLimitNs) {
+            atomicOr(&g_stream_gemm_error, kErrGridWait);
+            atomicExch(&sync[2], 1u);
+            return false;
+        }
+        __nanosleep(32);
+    }
+}
+
+// q = clamp(rne(fl32(x / s)), -127, 127), s != 0, decided from t = fl32(x * r)
+// with r = fl32(1 / s) when t is far from every half-integer, else from the
+// IEEE quotient. Error bound: r = (1/s)(1+d1), t = (x/s)(1+d1)(1+d2) and
+// fl32(x/s) = (x/s)(1+d3) with |di| <= 2^-24, so |t - fl32(x/s)| < 2^-22 |t|.
+// If the distance from t to the nearest half-integer exceeds 2^-20 |t|, both
+// lie strictly on the same side of it and round to the same integer.
+__device__ __forceinline__ int quant_code(float x, float s, float r) {
+    if (s == 0.f) return 0;
+    const float t = __fmul_rn(x, r);
+    float q = rintf(t);
+    const float margin = __fsub_rn(0.5f, fabsf(__fsub_rn(t, q)));
+    if (!(margin > __fmul_rn(fabsf(t), 0x1p-20f))) q = rintf(__fdiv_rn(x, s));
+    const int qi = __float2int_rn(q);
+    return qi > 127 ? 127 : (qi < -127 ? -127 : qi);
+}
+
+// The 8 bf16 or 4 fp32 elements of one 16-byte vector as binary32 (bf16 widened).
+__device__ __forceinline__ void unpack_vec(const uint4& r, bool bf16, float (&e)[8]) {
+    if (bf16) {
+        const uint32_t w4[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            e[2 * j] = __uint_as_float(w4[j] << 16);
+            e[2 * j + 1] = __uint_as_float(w4[j] & 0xFFFF0000u);
+        }
+    } else {
+        e[0] = __uint_as_float(r.x); e[1] = __uint_as_float(r.y);
+        e[2] = __uint_as_float(r.z); e[3] = __uint_as_float(r.w);
+        e[4] = e[5] = e[6] = e[7] = 0.f;
+    }
+}
+
+template <int NG>
+__global__ void __launch_bounds__((kW8A8Warps + 1) * 32, 1)
+verify_stack_kernel(const __grid_constant__ StackParams sp) {
+    using C = StackCfg<NG>;
+    constexpr int MP = C::MP;
+    constexpr int Stages = C::Stages;
+    constexpr int CW = kW8A8Warps;
+    constexpr int CT = CW * 32;
+    constexpr int RW = BN / CW;
+    constexpr int BPW = RW / 16;
+    constexpr int S8P = s8_pairs<NG>();
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* ring = base;                                        // Stages x (W tile + X tile)
+    int32_t* stg = reinterpret_cast<int32_t*>(ring + Stages * C::StageBytes);
+    uint64_t* full = reinterpret_cast<uint64_t*>(stg + C::StgWords);
+    uint64_t* empty = full + Stages;
+    unsigned long long* red = reinterpret_cast<unsigned long long*>(empty + Stages);
+    float* s_sx = reinterpret_cast<float*>(red + kMaxConsumerWarps * MP);
+    float* s_rx = s_sx + MP;                                     // fl32(1 / sx)
+    int32_t* s_tok = reinterpret_cast<int32_t*>(s_rx + MP);
+    float* s_amax = reinterpret_cast<float*>(s_tok + MP);        // [warp][MP]
+    volatile int* abort = reinterpret_cast<volatile int*>(s_amax + kMaxConsumerWarps * MP);
+    volatile int* flag = abort + 1;
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int G = gridDim.x;
+    const int P = sp.n_phases;
+    const int M = sp.M;
+    const bool xbf = sp.x_bf16 != 0;
+    const int esz = xbf ? 2 : 4;                                 // input element bytes
+    const int E = 16 / esz;                                      // elements per 16-byte vector
+
+    if (tid == 0) {
+        for (int st = 0; st < Stages; ++st) {
+            mbar_init(&full[st], 1);
+            mbar_init(&empty[st], CW);
+        }
+        *abort = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    // Grid barriers: every CTA arrives twice per phase p on sync[0]: once its
+    // share of the phase input is quantized (B(p): (2p+1) G arrivals in total)
+    // and once its tiles of phase p are done (A(p): (2p+2) G arrivals).
+    if (warp == CW) {
+        // ---------------- producer ----------------
+        // Weight tiles of every phase stream in phase order, ahead of the
+        // consumers; a stage's activation tile is requested once the phase's
+        // quantized input is complete (B(p) observed), possibly after its
+        // weight tile, so weights never wait for activations.
+        if (lane != 0) return;
+        const uint64_t pol_w = policy_evict_first();
+        const uint64_t pol_x = policy_evict_last();
+        prefetch_tensormap(&sp.tmap_x);
+        int pend_st[Stages], pend_ph[Stages], pend_kt[Stages];   // activation loads not yet issued
+        int pend_head = 0, pend_n = 0;
+        int ready = -1;                                           // last phase with B(p) complete
+        // Polls the barrier counter (one L2 round trip) only while an
+        // activation load waits for its phase, then issues what became ready.
+        auto refresh = [&]() {
+            if (pend_n == 0) return;
+            if (pend_ph[pend_head] > ready) {
+                const unsigned c = ld_acquire_gpu(&sp.sync[0]);
+                if (c >= (unsigned)G) {
+                    const int rp = (int)((c / (unsigned)G - 1u) / 2u);
+                    if (rp > ready) {
+                        ready = rp;
+                        fence_proxy_async_global();
+                    }
+                }
+            }
+            while (pend_n > 0 && pend_ph[pend_head] <= ready) {
+                const int s2 = pend_st[pend_head];
+                tma_load_2d(ring + s2 * C::StageBytes + kWTileBytes, &sp.tmap_x, pend_kt[pend_head] * BKB, 0,
+                            &full[s2], pol_x);
+                pend_head = (pend_head + 1) % Stages;
+                --pend_n;
+            }
+        };
+        int st = 0, round = 0;
+        long long issued = 0;
+        bool ok = true;
+        for (int p = 0; p < P && ok; ++p) {
+            const StackPhase& ph = sp.ph[p];
+            const CUtensorMap* tmap = &sp.tmap_w[p];
+            prefetch_tensormap(tmap);
+            const long long T = (long long)ph.KT * ph.NT;
+            const int a = (int)((long long)blockIdx.x * T / G);
+            const int b = (int)((long long)(blockIdx.x + 1) * T / G);
+            for (int j = a; j < b; ++j) {
+                if (issued >= Stages && !mbar_try_wait(&empty[st], (round - 1) & 1)) {
+                    const unsigned long long t0 = global_timer_ns();
+                    while (!mbar_try_wait(&empty[st], (round - 1) & 1)) {
+                        refresh();
+                        if (*abort || ld_acquire_gpu(&sp.sync[2])) { ok = false; break; }
+                        if (global_timer_ns() - t0 > kWaitLimitNs) {
+                            atomicOr(&g_stream_gemm_error, kErrEmptyWait);
+                            atomicExch(&sp.sync[2], 1u);
+                            *abort = 1;
+                            ok = false;
+                            break;
+                        }
+                    }
+                    if (!ok) break;
+                }
+                const int nt = j / ph.KT, kt = j - nt * ph.KT;
+                mbar_arrive_expect_tx(&full[st], (unsigned)(kWTileBytes + C::XBytes));
+                tma_load_2d(ring + st * C::StageBytes, tmap, kt * BKB, nt * BN, &full[st], pol_w);
+                if (p <= ready && pend_n == 0) {
+                    tma_load_2d(ring + st * C::StageBytes + kWTileBytes, &sp.tmap_x, kt * BKB, 0, &full[st], pol_x);
+                } else {
+                    const int tail = (pend_head + pend_n) % Stages;
+                    pend_st[tail] = st; pend_ph[tail] = p; pend_kt[tail] = kt;
+                    ++pend_n;
+                    if (pend_n == 1 || (issued & 3) == 0) refresh();
+                }
+                ++issued;
+                if (++st == Stages) { st = 0; ++round; }
+            }
+        }
+        // the last activation loads, then no copy may still be landing at exit
+        if (pend_n > 0) {
+            const unsigned long long t0 = global_timer_ns();
+            while (pend_n > 0) {
+                refresh();
+                if (pend_n == 0) break;
+                if (ld_acquire_gpu(&sp.sync[2]) || global_timer_ns() - t0 > kWaitLimitNs) {
+                    atomicOr(&g_stream_gemm_error, kErrDrainWait);
+                    break;
+                }
+                __nanosleep(64);
+            }
+        }
+        const long long first = issued > Stages ? issued - Stages : 0;
+        for (long long j = first; j < issued; ++j) {
+            const int s2 = (int)(j % Stages), par = (int)((j / Stages) & 1);
+            const unsigned long long t0 = global_timer_ns();
+            while (!mbar_try_wait(&full[s2], par)) {
+                if (global_timer_ns() - t0 > kWaitLimitNs) {
+                    atomicOr(&g_stream_gemm_error, kErrDrainWait);
+                    return;
+                }
+            }
+        }
+        return;
+    }
+
+    // ---------------- consumers ----------------
+    const int g = lane >> 2, t4 = lane & 3;
+    const TileLanes<BPW> L(RW * warp, lane);
+    int st = 0, phase_bit = 0;
+    int32_t acci[BPW][NG][4];
+
+    for (int p = 0; p < P; ++p) {
+        const StackPhase& ph = sp.ph[p];
+        const bool lm = sp.lm_last && p == P - 1;
+        const int K = ph.K, KT = ph.KT;
+        const long long T = (long long)KT * ph.NT;
+        const int a = (int)((long long)blockIdx.x * T / G);
+        const int b = (int)((long long)(blockIdx.x + 1) * T / G);
+        const uint8_t* xin = static_cast<const uint8_t*>(ph.x);
+
+        // ---- A(p-1): every CTA finished phase p-1 (its outputs may feed this input)
+        if (p > 0) {
+            if (tid == 0 && !grid_wait(sp.sync, (unsigned)(2 * p * G))) *abort = 1;
+            consumer_sync<CW>();
+        }
+
+        // ---- per-token scales of the phase input (amax / 127): every CTA
+        // computes the same bits; one memory round trip per round of loads
+        {
+            const int vpr = K / E;                                   // vectors per row
+            float part[MP];
+#pragma unroll
+            for (int m = 0; m < MP; ++m) part[m] = 0.f;
+            for (int v0 = 0; v0 < vpr; v0 += CT) {
+                const int v = v0 + tid;
+                uint4 r[MP];
+#pragma unroll
+                for (int m = 0; m < MP; ++m)
+                    if (m < M && v < vpr)
+                        r[m] = __ldg(reinterpret_cast<const uint4*>(xin + ((size_t)m * K + (size_t)v * E) * esz));
+                if (v < vpr) {
+                    float c[8] = {1.f, 1.f, 1.f, 1.f, 1.f, 1.f, 1.f, 1.f};
+                    if (ph.act_mul) {
+                        const float4* cm = reinterpret_cast<const float4*>(ph.act_mul + (size_t)v * E);
+                        const float4 c0 = __ldg(cm);
+                        c[0] = c0.x; c[1] = c0.y; c[2] = c0.z; c[3] = c0.w;
+                        if (xbf) {
+                            const float4 c1 = __ldg(cm + 1);
+                            c[4] = c1.x; c[5] = c1.y; c[6] = c1.z; c[7] = c1.w;
+                        }
+                    }
+#pragma unroll
+                    for (int m = 0; m < MP; ++m) {
+                        if (m >= M) break;
+                        float e[8];
+                        unpack_vec(r[m], xbf, e);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            if (j >= E) break;
+                            const float xx = ph.act_mul ? __fmul_rn(e[j], c[j]) : e[j];
+                            part[m] = fmaxf(part[m], fabsf(xx));
+                        }
+                    }
+                }
+            }
+#pragma unroll
+            for (int m = 0; m < MP; ++m) {
+                float v = part[m];
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
+                if (lane == 0) s_amax[warp * MP + m] = v;
+            }
+            consumer_sync<CW>();
+            if (tid < MP) {
+                float v = 0.f;
+                for (int w = 0; w < CW; ++w) v = fmaxf(v, s_amax[w * MP + tid]);
+                const float sx = tid < M ? __fdiv_rn(v, 127.0f) : 0.f;
+                s_sx[tid] = sx;
+                s_rx[tid] = sx != 0.f ? __frcp_rn(sx) : 0.f;
+            }
+            consumer_sync<CW>();
+        }
+
+        // ---- this CTA's share of the codes: (chunk, token) rows round-robin
+        // over the CTAs, one row of 128 codes per warp, 4 per lane
+        {
+            const int items = KT * M;
+            for (int it = blockIdx.x + G * warp; it < items; it += G * CW) {
+                const int kt = it / M, m = it - (it / M) * M;
+                const int k0 = kt * BKB + 4 * lane;
+                if (k0 < K) {
+                    float v[4];
+                    if (xbf) {
+                        const uint2 r = __ldg(reinterpret_cast<const uint2*>(xin + ((size_t)m * K + k0) * 2));
+                        v[0] = __uint_as_float(r.x << 16); v[1] = __uint_as_float(r.x & 0xFFFF0000u);
+                        v[2] = __uint_as_float(r.y << 16); v[3] = __uint_as_float(r.y & 0xFFFF0000u);
+                    } else {
+                        const uint4 r = __ldg(reinterpret_cast<const uint4*>(xin + ((size_t)m * K + k0) * 4));
+                        v[0] = __uint_as_float(r.x); v[1] = __uint_as_float(r.y);
+                        v[2] = __uint_as_float(r.z); v[3] = __uint_as_float(r.w);
+                    }
+                    float c[4] = {1.f, 1.f, 1.f, 1.f};
+                    if (ph.act_mul) {
+                        const float4 c0 = __ldg(reinterpret_cast<const float4*>(ph.act_mul + k0));
+                        c[0] = c0.x; c[1] = c0.y; c[2] = c0.z; c[3] = c0.w;
+                    }
+                    const float sxm = s_sx[m], rxm = s_rx[m];
+                    uint32_t word = 0;
+#pragma unroll
+                    for (int jj = 0; jj < 4; ++jj) {
+                        const float xx = ph.act_mul ? __fmul_rn(v[jj], c[jj]) : v[jj];
+                        word |= (uint32_t)(uint8_t)(int8_t)quant_code(xx, sxm, rxm) << (8 * jj);
+                    }
+                    *reinterpret_cast<uint32_t*>(sp.xq + (size_t)m * sp.kmax + k0) = word;
+                }
+            }
+            // B(p): the codes are visible to the other CTAs' TMA loads
+            fence_proxy_async_global();
+            __threadfence();
+            consumer_sync<CW>();
+            if (tid == 0) { __threadfence(); atomicAdd(&sp.sync[0], 1u); }
+        }
+
+        // ---- this CTA's tiles
+        int seg_begin = a;
+#pragma unroll
+        for (int blk = 0; blk < BPW; ++blk)
+#pragma unroll
+            for (int gr = 0; gr < NG; ++gr)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) acci[blk][gr][e] = 0;
+
+        for (int i = a; i < b; ++i) {
+            const int nt = i / KT;
+            const int kt = i - nt * KT;
+            if (!mbar_wait_bounded(&full[st], phase_bit, abort))
+                atomicOr(&g_stream_gemm_error, kErrFullWait);
+            uint8_t* stage = ring + st * C::StageBytes;
+            w8a8_tile_mma<NG, BPW, S8P>(smem_u32(stage), smem_u32(stage + kWTileBytes), L, acci);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[st]);
+            if (++st == Stages) { st = 0; phase_bit ^= 1; }
+
+            if (kt != KT - 1 && i != b - 1) continue;
+            // -------- segment end: stage [row][token] sums, combine, epilogue
+#pragma unroll
+            for (int blk = 0; blk < BPW; ++blk) {
+                const int r0 = RW * warp + 16 * blk + g;
+#pragma unroll
+                for (int gr = 0; gr < NG; ++gr) {
+                    const int col = 8 * gr + 2 * t4;
+                    *reinterpret_cast<int2*>(&stg[r0 * MP + col]) = make_int2(acci[blk][gr][0], acci[blk][gr][1]);
+                    *reinterpret_cast<int2*>(&stg[(r0 + 8) * MP + col]) = make_int2(acci[blk][gr][2], acci[blk][gr][3]);
+                    acci[blk][gr][0] = acci[blk][gr][1] = acci[blk][gr][2] = acci[blk][gr][3] = 0;
+                }
+            }
+            consumer_sync<CW>();
+            const int seg_len = i + 1 - seg_begin;
+            seg_begin = i + 1;
+            const bool whole = seg_len == KT;
+            int32_t* gacc = sp.ws_acc + (size_t)nt * BN * MP;
+            if (!whole) {
+                for (int e = tid; e < BN * MP; e += CT) {
+                    const int r = e / MP, m = e - (e / MP) * MP;
+                    if (m < M && nt * BN + r < ph.N) atomicAdd(&gacc[e], stg[e]);
+                }
+                __threadfence();
+                consumer_sync<CW>();
+                if (tid == 0) {
+                    __threadfence();
+                    const unsigned prev = atomicAdd(&sp.ws_cnt[nt], (unsigned)seg_len);
+                    *flag = (prev + (unsigned)seg_len == (unsigned)KT) ? 1 : 0;
+                }
+                consumer_sync<CW>();
+            }
+            if (whole || *flag) {
+                if (!whole) __threadfence();
+                const int r = tid;
+                const int n = nt * BN + r;
+                const bool valid = r < BN && n < ph.N;
+                const float swn = valid ? ph.sw[n] : 0.f;
+                // the finished tile's sums: from staging, or read from the
+                // workspace in one batch and cleared (no other CTA touches it now)
+                int32_t accs[MP];
+#pragma unroll
+                for (int m = 0; m < MP; ++m) accs[m] = 0;
+                if (valid) {
+                    if (whole) {
+#pragma unroll
+                        for (int m = 0; m < MP; ++m) accs[m] = stg[r * MP + m];
+                    } else {
+#pragma unroll
+                        for (int m = 0; m < MP; ++m) accs[m] = m < M ? __ldcg(&gacc[r * MP + m]) : 0;
+#pragma unroll
+                        for (int m = 0; m < MP; ++m)
+                            if (m < M) __stcg(&gacc[r * MP + m], 0);
+                    }
+                }
+                if (!lm) {
+                    if (valid && ph.y) {
+#pragma unroll
+                        for (int m = 0; m < MP; ++m) {
+                            if (m >= M) break;
+                            ph.y[(size_t)m * ph.N + n] = __fmul_rn(__int2float_rn(accs[m]), __fmul_rn(s_sx[m], swn));
+                        }
+                    }
+                } else {
+                    if (r < BN) {
+#pragma unroll
+                        for (int m = 0; m < MP; ++m) {
+                            if (m >= M) break;
+                            unsigned long long key = 0ull;
+                            if (valid) {
+                                const float yv = __fmul_rn(__int2float_rn(accs[m]), __fmul_rn(s_sx[m], swn));
+                                key = ((unsigned long long)ordered_bits(yv) << 32) |
+                                      (unsigned long long)(0xFFFFFFFFu - (unsigned)n);
+                            }
+                            key = warp_max_u64(key);
+                            if (lane == 0) red[warp * MP + m] = key;
+                        }
+                    }
+                    consumer_sync<CW>();
+                    if (tid < M) {
+                        unsigned long long k = red[tid];
+#pragma unroll
+                        for (int w = 1; w < BN / 32; ++w) {
+                            const unsigned long long o = red[w * MP + tid];
+                            k = o > k ? o : k;
+                        }
+                        atomicMax(&sp.keys[tid], k);
+                    }
+                    __threadfence();
+                    consumer_sync<CW>();
+                    if (tid == 0) {
+                        __threadfence();
+                        const unsigned prev = atomicAdd(&sp.sync[3], 1u);
+                        *flag = (prev + 1u == (unsigned)ph.NT) ? 2 : 0;
+                    }
+                    consumer_sync<CW>();
+                    if (*flag == 2) {
+                        // last LM tile: decode the argmax, then accept
+                        __threadfence();
+                        if (tid < M) {
+                            const unsigned long long k = atomicExch(&sp.keys[tid], 0ull);
+                            const int32_t t = (int32_t)(0xFFFFFFFFu - (unsigned)(k & 0xFFFFFFFFull));
+                            s_tok[tid] = t;
+                            sp.tokens[tid] = t;
+                            if (sp.max_logit) sp.max_logit[tid] = unordered_bits((unsigned)(k >> 32));
+                        }
+                        if (tid == 0) atomicExch(&sp.sync[3], 0u);
+                        consumer_sync<CW>();
+                        if (sp.accept_len) {
+                            const int Gm = sp.gamma + 1;
+                            for (int bq = tid; bq < sp.B; bq += CT) {
+                                const int32_t* tb = s_tok + bq * Gm;
+                                const int32_t* db = sp.draft + (size_t)bq * sp.gamma;
+                                int k = 0;
+                                while (k < sp.gamma && db[k] == tb[k]) ++k;
+                                sp.accept_len[bq] = k + 1;
+                                for (int jq = 0; jq < Gm; ++jq)
+                                    sp.out_tokens[(size_t)bq * Gm + jq] = jq <= k ? tb[jq] : -1;
+                            }
+                        }
+                    }
+                }
+                if (!whole && tid == 0) atomicExch(&sp.ws_cnt[nt], 0u);
+            }
+            consumer_sync<CW>();
+        }
+        // ---- A(p): this CTA is done with phase p
+        consumer_sync<CW>();
+        if (tid == 0) { __threadfence(); atomicAdd(&sp.sync[0], 1u); }
+    }
+    // last CTA out resets the barrier words for the next launch
+    if (tid == 0) {
+        __threadfence();
+        const unsigned prev = atomicAdd(&sp.sync[1], 1u);
+        if (prev + 1u == (unsigned)G) {
+            atomicExch(&sp.sync[0], 0u);
+            atomicExch(&sp.sync[2], 0u);
+            __threadfence();
+            atomicExch(&sp.sync[1], 0u);
+        }
+    }
+}
+
 }  // namespace
 
 WsLayout ws_layout(int mp, int n, bool lm_head) {
@@ -739,6 +1286,70 @@ cudaError_t launch_bf16_stream(const Bf16Launch& a, int num_sms, cudaStream_t s)
         default: return cudaErrorInvalidValue;
     }
 #undef QV_BF16_CASE
+}
+
+cudaError_t launch_verify_stack(const StackLaunch& a, int num_sms, cudaStream_t s) {
+    if (a.n_phases < 1 || a.n_phases > kMaxStackPhases) return cudaErrorInvalidValue;
+    static thread_local StackParams sp;     // ~27 KB: kept off the stack
+    memset(&sp, 0, sizeof sp);
+    for (int i = 0; i < a.n_phases; ++i) {
+        const StackLaunchPhase& h = a.phases[i];
+        StackPhase& d = sp.ph[i];
+        sp.tmap_w[i] = h.tmap_w;
+        d.x = h.x; d.act_mul = h.act_mul; d.sw = h.sw; d.y = h.y;
+        d.K = h.K; d.N = h.N;
+        d.KT = ceil_div(h.K, BKB);
+        d.NT = ceil_div(h.N, BN);
+    }
+    sp.n_phases = a.n_phases;
+    sp.lm_last = a.lm_last ? 1 : 0;
+    sp.M = a.M; sp.x_bf16 = a.x_bf16 ? 1 : 0;
+    sp.B = a.B; sp.gamma = a.gamma; sp.draft = a.draft;
+    sp.tokens = a.tokens; sp.max_logit = a.max_logit;
+    sp.accept_len = a.accept_len; sp.out_tokens = a.out_tokens;
+    WsLayout L = ws_layout(a.MP, a.n_max, true);
+    uint8_t* ws = static_cast<uint8_t*>(a.ws);
+    sp.ws_acc = reinterpret_cast<int32_t*>(ws + L.acc);
+    sp.ws_cnt = reinterpret_cast<unsigned*>(ws + L.counters);
+    sp.keys = reinterpret_cast<unsigned long long*>(ws + L.keys);
+    sp.sync = reinterpret_cast<unsigned*>(ws + L.done);
+    sp.xq = reinterpret_cast<int8_t*>(ws + stack_xq_offset(a.MP, a.n_max));
+    sp.kmax = a.kmax;
+    sp.tmap_x = a.tmap_x;
+
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(num_sms);
+    cfg.blockDim = dim3((kW8A8Warps + 1) * 32);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e;
+    if (a.MP == 8) {
+        cfg.dynamicSmemBytes = StackCfg<1>::SmemBytes;
+        e = cudaFuncSetAttribute(verify_stack_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 StackCfg<1>::SmemBytes);
+        if (e != cudaSuccess) return e;
+        return cudaLaunchKernelEx(&cfg, verify_stack_kernel<1>, sp);
+    }
+    if (a.MP == 16) {
+        cfg.dynamicSmemBytes = StackCfg<2>::SmemBytes;
+        e = cudaFuncSetAttribute(verify_stack_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 StackCfg<2>::SmemBytes);
+        if (e != cudaSuccess) return e;
+        return cudaLaunchKernelEx(&cfg, verify_stack_kernel<2>, sp);
+    }
+    return cudaErrorInvalidValue;
+}
+
+size_t stack_xq_offset(int mp, int n_max) {
+    return (ws_layout(mp, n_max, true).total + 255) & ~size_t(255);
+}
+
+size_t stack_ws_bytes(int mp, int M, int n_max, int kmax) {
+    return stack_xq_offset(mp, n_max) + (((size_t)M * kmax + 15) & ~size_t(15));
 }
 
 cudaError_t read_and_clear_stream_gemm_error(unsigned* code) {

@@ -12,7 +12,7 @@
 #include <cstdio>
 #include <mutex>
 
-#include "../../include/qv.h"
+#include "qv.h"
 #include "qv_internal.h"
 
 namespace {
@@ -169,6 +169,9 @@ size_t qv_workspace_bytes(qv_op op, int M, int K, int N) {
         case QV_OP_LINEAR: return qv::ws_layout(mp, N, false).total;
         case QV_OP_LM_HEAD: return qv::ws_layout(mp, N, true).total;
         case QV_OP_BF16_LINEAR: return qv::ws_layout(mp, N, false).total;
+        case QV_OP_VERIFY_STACK:
+            if (M > qv::kMaxStackM) return 0;
+            return qv::stack_ws_bytes(mp, M, N, K);
     }
     return 0;
 }
@@ -333,6 +336,103 @@ qv_status qv_bf16_linear(const uint16_t* x, int M, int K, const uint16_t* w, int
         L.ws = workspace;
         e = qv::launch_bf16_stream(L, sms, stream);
         if (e != cudaSuccess) return cuda_fail(e, "qv_bf16_linear launch");
+    }
+    return ok();
+}
+
+qv_status qv_verify_stack(const qv_linear_desc* linears, int n_linears, const qv_linear_desc* lm_head,
+                          int M, qv_dtype x_dtype, const int32_t* draft, int B, int gamma,
+                          int32_t* tokens, float* max_logit, int32_t* accept_len, int32_t* out_tokens,
+                          void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    if (n_linears < 0 || (n_linears > 0 && !linears)) return fail(QV_ERR_INVALID_ARG, "bad linears array");
+    if (n_linears == 0 && !lm_head) return fail(QV_ERR_INVALID_ARG, "nothing to run");
+    if (M < 1 || M > qv::kMaxStackM)
+        return fail(QV_ERR_UNSUPPORTED, "M=%d outside [1, %d] for the stack kernel", M, qv::kMaxStackM);
+    if (x_dtype != QV_F32 && x_dtype != QV_BF16) return fail(QV_ERR_INVALID_ARG, "x_dtype must be QV_F32 or QV_BF16");
+    int n_max = 0, k_max = 0;
+    auto check_desc = [&](const qv_linear_desc& d, int idx, bool lm) -> qv_status {
+        if (!d.x || !d.wq || !d.sw) return fail(QV_ERR_INVALID_ARG, "phase %d: null x/wq/sw", idx);
+        if (d.N < 1) return fail(QV_ERR_INVALID_ARG, "phase %d: N=%d", idx, d.N);
+        qv_status st = check_k(d.K);
+        if (st != QV_OK) return st;
+        if (!aligned(d.x, 16) || !aligned(d.wq, 16) || (d.act_mul && !aligned(d.act_mul, 16)))
+            return fail(QV_ERR_INVALID_ARG, "phase %d: x, wq and act_mul must be 16-byte aligned", idx);
+        if (!aligned(d.sw, 4) || (!lm && d.y && !aligned(d.y, 4)))
+            return fail(QV_ERR_INVALID_ARG, "phase %d: misaligned sw/y", idx);
+        if ((st = check_dev(d.x, "x")) != QV_OK || (st = check_dev(d.wq, "wq")) != QV_OK ||
+            (st = check_dev(d.sw, "sw")) != QV_OK || (st = check_dev(d.act_mul, "act_mul")) != QV_OK ||
+            (!lm && (st = check_dev(d.y, "y")) != QV_OK))
+            return st;
+        if (d.N > n_max) n_max = d.N;
+        if (d.K > k_max) k_max = d.K;
+        return QV_OK;
+    };
+    for (int i = 0; i < n_linears; ++i) {
+        qv_status st = check_desc(linears[i], i, false);
+        if (st != QV_OK) return st;
+    }
+    if (lm_head) {
+        qv_status st = check_desc(*lm_head, n_linears, true);
+        if (st != QV_OK) return st;
+        if (!tokens || !aligned(tokens, 4) || (max_logit && !aligned(max_logit, 4)))
+            return fail(QV_ERR_INVALID_ARG, "tokens required (4-byte aligned) with an LM head");
+        QV_CHECK_DEV(tokens);
+        QV_CHECK_DEV(max_logit);
+        if (accept_len || out_tokens) {
+            if (!accept_len || !out_tokens) return fail(QV_ERR_INVALID_ARG, "accept_len and out_tokens go together");
+            if (B < 1 || gamma < 0 || (long long)B * (gamma + 1) != M)
+                return fail(QV_ERR_INVALID_ARG, "B*(gamma+1) must equal M (B=%d gamma=%d M=%d)", B, gamma, M);
+            if (gamma > 0 && !draft) return fail(QV_ERR_INVALID_ARG, "draft is null with gamma > 0");
+            if (!aligned(accept_len, 4) || !aligned(out_tokens, 4) || (draft && !aligned(draft, 4)))
+                return fail(QV_ERR_INVALID_ARG, "int32 buffers must be 4-byte aligned");
+            QV_CHECK_DEV(accept_len);
+            QV_CHECK_DEV(out_tokens);
+            QV_CHECK_DEV(draft);
+        }
+    } else if (tokens || accept_len || out_tokens) {
+        return fail(QV_ERR_INVALID_ARG, "tokens/acceptance outputs need an LM head");
+    }
+    const size_t need = qv_workspace_bytes(QV_OP_VERIFY_STACK, M, k_max, n_max);
+    if (!workspace) return fail(QV_ERR_WORKSPACE, "workspace is null (%zu bytes needed)", need);
+    if (!aligned(workspace, 16)) return fail(QV_ERR_WORKSPACE, "workspace must be 16-byte aligned");
+    if (workspace_bytes < need) return fail(QV_ERR_WORKSPACE, "workspace has %zu bytes, %zu needed", workspace_bytes, need);
+    QV_CHECK_DEV(workspace);
+
+    cudaError_t e;
+    const int sms = sms_of_current_device(&e);
+    if (e != cudaSuccess) return cuda_fail(e, "device query");
+    static thread_local qv::StackLaunchPhase ph[qv::kMaxStackPhases];
+    const int total = n_linears + (lm_head ? 1 : 0);
+    const int mp = mp_for(M);
+    CUtensorMap tmap_x;
+    {
+        const int8_t* xq = static_cast<const int8_t*>(workspace) + qv::stack_xq_offset(mp, n_max);
+        qv_status st = encode_2d(&tmap_x, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, xq, (uint64_t)k_max,
+                                 (uint64_t)M, qv::kTileKBytes, (uint32_t)mp);
+        if (st != QV_OK) return st;
+    }
+    for (int first = 0; first < total; first += qv::kMaxStackPhases) {
+        const int count = total - first < qv::kMaxStackPhases ? total - first : qv::kMaxStackPhases;
+        for (int j = 0; j < count; ++j) {
+            const int idx = first + j;
+            const qv_linear_desc& d = idx < n_linears ? linears[idx] : *lm_head;
+            qv_status st = encode_2d(&ph[j].tmap_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, d.wq, (uint64_t)d.K,
+                                     (uint64_t)d.N, qv::kTileKBytes, qv::kTileN);
+            if (st != QV_OK) return st;
+            ph[j].x = d.x; ph[j].act_mul = d.act_mul; ph[j].sw = d.sw;
+            ph[j].y = idx < n_linears ? d.y : nullptr;
+            ph[j].K = d.K; ph[j].N = d.N;
+        }
+        qv::StackLaunch L = {};
+        L.phases = ph; L.n_phases = count;
+        L.lm_last = lm_head && first + count == total;
+        L.M = M; L.MP = mp; L.x_bf16 = x_dtype == QV_BF16;
+        L.B = B; L.gamma = gamma; L.draft = draft;
+        L.tokens = tokens; L.max_logit = max_logit;
+        L.accept_len = accept_len; L.out_tokens = out_tokens;
+        L.ws = workspace; L.n_max = n_max; L.kmax = k_max; L.tmap_x = tmap_x;
+        e = qv::launch_verify_stack(L, sms, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "qv_verify_stack launch");
     }
     return ok();
 }

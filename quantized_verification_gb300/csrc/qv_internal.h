@@ -53,7 +53,45 @@ struct Bf16Launch {
     void* ws;
 };
 
+// Phases (linears + the LM head) one persistent verify-stack launch holds;
+// longer stacks are split into several launches.
+constexpr int kMaxStackPhases = 150;
+// Largest token count of the persistent verify-stack kernel.
+constexpr int kMaxStackM = 16;
+
+struct StackLaunchPhase {
+    CUtensorMap tmap_w;
+    const void* x;
+    const float* act_mul;
+    const float* sw;
+    float* y;
+    int K, N;
+};
+
+struct StackLaunch {
+    const StackLaunchPhase* phases;
+    int n_phases;
+    bool lm_last;
+    int M, MP;
+    bool x_bf16;
+    int B, gamma;
+    const int32_t* draft;
+    int32_t* tokens;
+    float* max_logit;
+    int32_t* accept_len;
+    int32_t* out_tokens;
+    void* ws;
+    int n_max;                // largest N of the phases (workspace layout)
+    int kmax;                 // largest K of the phases (row stride of the codes)
+    CUtensorMap tmap_x;       // int8 codes [M rows][kmax] in the workspace, box {128, MP}
+};
+
+// Workspace bytes of qv_verify_stack and the offset of its int8 code buffer.
+size_t stack_ws_bytes(int mp, int M, int n_max, int kmax);
+size_t stack_xq_offset(int mp, int n_max);
+
 cudaError_t launch_w8a8_stream(const W8A8Launch& a, int num_sms, cudaStream_t s);
+cudaError_t launch_verify_stack(const StackLaunch& a, int num_sms, cudaStream_t s);
 cudaError_t launch_bf16_stream(const Bf16Launch& a, int num_sms, cudaStream_t s);
 cudaError_t launch_quantize_rows(const void* x, bool bf16, int rows, int K,
                                  const float* mul, int8_t* q, float* scale,

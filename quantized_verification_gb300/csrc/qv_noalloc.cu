@@ -9,7 +9,7 @@
 #include <cstdio>
 #include <mutex>
 
-#include "../../include/qv.h"
+#include "qv.h"
 #include "qv_internal.h"
 
 namespace qv {

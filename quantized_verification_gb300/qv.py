@@ -17,14 +17,22 @@ LIB_PATH = os.path.join(_PKG, "libqv.so")
 
 QV_OK, QV_ERR_INVALID_ARG, QV_ERR_UNSUPPORTED, QV_ERR_WORKSPACE, QV_ERR_CUDA = range(5)
 QV_F32, QV_BF16 = 0, 1
-QV_OP_LINEAR, QV_OP_LM_HEAD, QV_OP_BF16_LINEAR = 0, 1, 2
+QV_OP_LINEAR, QV_OP_LM_HEAD, QV_OP_BF16_LINEAR, QV_OP_VERIFY_STACK = 0, 1, 2, 3
 QV_MAX_K = 133144
 QV_MAX_M = 256
 
 # Symbols include/qv.h declares (checked against the library by the tests).
 EXPORTS = ("qv_quantize_act", "qv_w8a8_linear", "qv_lm_head_argmax", "qv_accept",
            "qv_quantize_weight", "qv_bf16_linear", "qv_workspace_bytes",
-           "qv_last_error", "qv_device_error", "qv_num_sms", "qv_w8a8_linear_noalloc")
+           "qv_last_error", "qv_device_error", "qv_num_sms", "qv_w8a8_linear_noalloc",
+           "qv_verify_stack")
+MAX_STACK_M = 16
+
+
+class LinearDesc(ctypes.Structure):
+    """qv_linear_desc of include/qv.h."""
+    _fields_ = [("x", ctypes.c_void_p), ("act_mul", ctypes.c_void_p), ("wq", ctypes.c_void_p),
+                ("sw", ctypes.c_void_p), ("y", ctypes.c_void_p), ("K", ctypes.c_int), ("N", ctypes.c_int)]
 QV_NOALLOC_SCRATCH_BYTES = 4 << 20
 
 
@@ -58,6 +66,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         L.qv_quantize_weight.argtypes = [P, I, I, I, P, P, P]
         L.qv_bf16_linear.argtypes = [P, I, I, P, I, P, P, S, P]
         L.qv_w8a8_linear_noalloc.argtypes = [P, P, I, I, P, P, I, P, I, P, P]
+        L.qv_verify_stack.argtypes = [ctypes.POINTER(LinearDesc), I, ctypes.POINTER(LinearDesc), I, I,
+                                      P, I, I, P, P, P, P, P, S, P]
         L.qv_workspace_bytes.argtypes = [I, I, I, I]
         L.qv_workspace_bytes.restype = S
         L.qv_last_error.argtypes = []
@@ -67,7 +77,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         L.qv_num_sms.restype = I
         for name in ("qv_quantize_act", "qv_w8a8_linear", "qv_lm_head_argmax", "qv_accept",
                      "qv_quantize_weight", "qv_bf16_linear", "qv_device_error",
-                     "qv_w8a8_linear_noalloc"):
+                     "qv_w8a8_linear_noalloc", "qv_verify_stack"):
             getattr(L, name).restype = st
         _lib = L
         return L
@@ -197,6 +207,36 @@ def qv_bf16_linear(x, w, y, workspace, stream=None):
     _need(workspace.dtype == torch.uint8, "workspace must be a uint8 tensor")
     _check(load().qv_bf16_linear(_ptr(x), M, K, _ptr(w), N, _ptr(y), _ptr(workspace),
                                  workspace.numel(), ctypes.c_void_p(_stream(stream))))
+
+
+def linear_desc(x, wq, sw, y=None, act_mul=None) -> LinearDesc:
+    """Descriptor of one quantize -> W8A8 linear phase (the tensors must stay
+    alive while the descriptor is used)."""
+    M, K = x.shape
+    N = wq.shape[0]
+    _need(wq.shape == (N, K) and wq.dtype == torch.int8, "wq int8 [N, K]")
+    _need(sw.shape == (N,) and sw.dtype == torch.float32, "sw float32 [N]")
+    if y is not None:
+        _need(y.shape == (M, N) and y.dtype == torch.float32, "y float32 [M, N]")
+    if act_mul is not None:
+        _need(act_mul.shape == (K,) and act_mul.dtype == torch.float32, "act_mul float32 [K]")
+    return LinearDesc(_ptr(x), _ptr(act_mul), _ptr(wq), _ptr(sw), _ptr(y), K, N)
+
+
+def qv_verify_stack(linears, lm_head, M, x_dtype, workspace, tokens=None, max_logit=None,
+                    draft=None, accept_len=None, out_tokens=None, stream=None):
+    """linears: list of LinearDesc; lm_head: LinearDesc or None; x_dtype: the
+    torch dtype of every phase input. B and gamma come from out_tokens [B, gamma+1]."""
+    n = len(linears)
+    arr = (LinearDesc * max(n, 1))(*linears)
+    B, gamma = (out_tokens.shape[0], out_tokens.shape[1] - 1) if out_tokens is not None else (0, 0)
+    dt = QV_BF16 if x_dtype == torch.bfloat16 else QV_F32
+    _need(workspace.dtype == torch.uint8, "workspace must be a uint8 tensor")
+    d = draft if (draft is not None and draft.numel() > 0) else None
+    _check(load().qv_verify_stack(arr, n, ctypes.byref(lm_head) if lm_head is not None else None, M, dt,
+                                  _ptr(d), B, gamma, _ptr(tokens), _ptr(max_logit), _ptr(accept_len),
+                                  _ptr(out_tokens), _ptr(workspace), workspace.numel(),
+                                  ctypes.c_void_p(_stream(stream))))
 
 
 def qv_workspace_bytes(op: int, M: int, K: int, N: int) -> int:

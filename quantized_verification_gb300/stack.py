@@ -148,8 +148,39 @@ class VerifyStack:
         qv.qv_accept(self.tokens.view(self.B, self.gamma + 1), self.drafts if self.gamma > 0 else None,
                      self.accept_len, self.out_tokens, stream=stream)
 
-    def launches_per_step(self) -> int:
+    def launches_per_step(self, fused: bool = False) -> int:
+        if fused:
+            return (self.layers * len(self.phases) + 1 + 149) // 150
         return self.layers * len(self.phases) * 2 + 3
+
+    # ------------------------------------------------------------------ fused step
+    def _fused_descs(self):
+        if getattr(self, "_descs", None) is None:
+            M = self.M
+            descs = []
+            for l in range(self.layers):
+                for p, (name, K, N) in enumerate(self.phases):
+                    wq, sw = self.weights[l][p]
+                    descs.append(qv.linear_desc(self.inputs[l][p], wq, sw, y=self.y[: M * N].view(M, N)))
+            lm = qv.linear_desc(self.h_final, self.lm_wq, self.lm_sw)
+            nmax = max([N for (_, _, N) in self.phases] + [self.V])
+            kmax = max([K for (_, K, _) in self.phases] + [self.model["hidden"]])
+            self.ws_stack = torch.zeros(qv.qv_workspace_bytes(qv.QV_OP_VERIFY_STACK, M, kmax, nmax),
+                                        dtype=torch.uint8, device=self.device)
+            self._descs = (descs, lm)
+        return self._descs
+
+    def enqueue_fused(self, stream=None):
+        """The same step through qv_verify_stack: one persistent launch (per
+        150 phases), bit-identical results."""
+        descs, lm = self._fused_descs()
+        qv.qv_verify_stack(descs, lm, self.M, torch.bfloat16, self.ws_stack, tokens=self.tokens,
+                           max_logit=self.max_logit, draft=self.drafts if self.gamma > 0 else None,
+                           accept_len=self.accept_len, out_tokens=self.out_tokens, stream=stream)
+
+    def capture_fused(self):
+        self.graph_fused = self._capture(self.enqueue_fused, self.device)
+        return self.graph_fused
 
     @staticmethod
     def _capture(fn, device):
