@@ -76,6 +76,9 @@ constexpr int kWTileBytes = BN * BKB;             // 16 KB
 #ifndef QV_S8_PAIRS_WIDE
 #define QV_S8_PAIRS_WIDE 0
 #endif
+#ifndef QV_TILE_ILP
+#define QV_TILE_ILP 0
+#endif
 #ifndef QV_BF16_WARPS
 #define QV_BF16_WARPS 8
 #endif
@@ -252,6 +255,19 @@ __device__ __forceinline__ void w8a8_tile_mma(uint32_t wb, uint32_t xb, const Ti
         for (int gr = 0; gr < NG; ++gr)
 #pragma unroll
             for (int e = 0; e < 4; ++e) accf[blk][gr][e] = 0.f;
+#if QV_TILE_ILP
+    // one int32 accumulator per chunk pair: the int8 MMAs of a tile are
+    // independent and can overlap in the tensor pipe; summed exactly below
+    int32_t acc8[S8P > 0 ? S8P : 1][BPW][NG][4];
+#pragma unroll
+    for (int P = 0; P < (S8P > 0 ? S8P : 1); ++P)
+#pragma unroll
+        for (int blk = 0; blk < BPW; ++blk)
+#pragma unroll
+            for (int gr = 0; gr < NG; ++gr)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) acc8[P][blk][gr][e] = 0;
+#endif
 #pragma unroll
     for (int cq = 0; cq < 2; ++cq) {
         // Activation words (tokens = MMA columns) for chunks 4cq .. 4cq+3.
@@ -276,7 +292,11 @@ __device__ __forceinline__ void w8a8_tile_mma(uint32_t wb, uint32_t xb, const Ti
                 if (P < S8P) {
 #pragma unroll
                     for (int gr = 0; gr < NG; ++gr)
+#if QV_TILE_ILP
+                        mma_s8_16832(acc8[P][blk][gr], r0, r1, r2, r3, bw[gr][2 * cp], bw[gr][2 * cp + 1]);
+#else
                         mma_s8_16832(acci[blk][gr], r0, r1, r2, r3, bw[gr][2 * cp], bw[gr][2 * cp + 1]);
+#endif
                 } else {
                     uint32_t a0l, a0h, a1l, a1h;
                     widen_i8x4_f16(r0, a0l, a0h);   // row g,   chunk 2P
@@ -303,6 +323,16 @@ __device__ __forceinline__ void w8a8_tile_mma(uint32_t wb, uint32_t xb, const Ti
 #pragma unroll
                 for (int e = 0; e < 4; ++e) acci[blk][gr][e] += __float2int_rn(accf[blk][gr][e]);
     }
+#if QV_TILE_ILP
+#pragma unroll
+    for (int P = 0; P < S8P; ++P)
+#pragma unroll
+        for (int blk = 0; blk < BPW; ++blk)
+#pragma unroll
+            for (int gr = 0; gr < NG; ++gr)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) acci[blk][gr][e] += acc8[P][blk][gr][e];
+#endif
 }
 
 // ---------------------------------------------------------------------------
@@ -707,7 +737,8 @@ struct StackParams {
     int32_t* ws_acc;
     unsigned* ws_cnt;
     unsigned long long* keys;
-    unsigned* sync;           // [0] barrier arrivals [1] exits [2] abort [3] LM tiles done
+    unsigned* sync;           // [0] B arrivals [1] exits [3] LM tiles done; [32] B flag; [64] A flag;
+                              // [96] abort; [128] A arrivals (each group on its own 128-byte line)
     int8_t* xq;               // [M][kmax] int8 codes of the current phase input
 };
 
@@ -730,20 +761,44 @@ __device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
     return v;
 }
 
-// Thread 0 of the consumers waits until `target` arrivals were counted (or the
-// launch was aborted); returns false when the wait was cut short.
-__device__ __forceinline__ bool grid_wait(unsigned* sync, unsigned target) {
-    if (ld_acquire_gpu(&sync[0]) >= target) return true;
+// Device-wide barriers of the stack kernel: B(p) "the phase-p input is
+// quantized" and A(p) "every output of phase p is written". Arrivals only
+// increment the barrier's own counter; the CTA whose arrival completes it
+// publishes p+1 on the barrier's flag, on a cache line of its own, so waiters
+// poll a line that changes once per barrier. B and A have separate counters: a
+// CTA without tiles in a phase reaches A(p) before others reach B(p).
+constexpr int kCountB = 0, kFlagB = 32, kFlagA = 64, kAbort = 96, kCountA = 128;
+
+__device__ __forceinline__ void st_release_gpu(unsigned* p, unsigned v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
+}
+
+// Thread 0 of a CTA: arrive on sync[count]; the arrival that makes it reach
+// `target` publishes `flag_value` on sync[flag].
+__device__ __forceinline__ void grid_arrive(unsigned* sync, int count, unsigned target, int flag,
+                                            unsigned flag_value) {
+    __threadfence();
+    const unsigned prev = atomicAdd(&sync[count], 1u);
+    if (prev + 1u == target) {
+        __threadfence();
+        st_release_gpu(&sync[flag], flag_value);
+    }
+}
+
+// Thread 0 of the consumers waits until sync[flag] >= value (or the launch was
+// aborted); returns false when the wait was cut short.
+__device__ __forceinline__ bool grid_wait(unsigned* sync, int flag, unsigned value) {
+    if (ld_acquire_gpu(&sync[flag]) >= value) return true;
     const unsigned long long t0 = global_timer_ns();
     while (true) {
-        if (ld_acquire_gpu(&sync[2])) return false;
-        if (ld_acquire_gpu(&sync[0]) >= target) return true;
+        __nanosleep(64);
+        if (ld_acquire_gpu(&sync[flag]) >= value) return true;
+        if (ld_acquire_gpu(&sync[kAbort])) return false;
         if (global_timer_ns() - t0 > kWaitLimitNs) {
             atomicOr(&g_stream_gemm_error, kErrGridWait);
-            atomicExch(&sync[2], 1u);
+            atomicExch(&sync[kAbort], 1u);
             return false;
         }
-        __nanosleep(32);
     }
 }
 
@@ -779,8 +834,15 @@ __device__ __forceinline__ void unpack_vec(const uint4& r, bool bf16, float (&e)
     }
 }
 
+#ifndef QV_STACK_L2_AHEAD
+#define QV_STACK_L2_AHEAD 24
+#endif
+// Weight tiles the L2 prefetch warp of the stack kernel runs ahead of the
+// shared-memory producer (per CTA; 24 tiles = 384 KB, 58 MB over 152 SMs).
+constexpr int kStackL2Ahead = QV_STACK_L2_AHEAD;
+
 template <int NG>
-__global__ void __launch_bounds__((kW8A8Warps + 1) * 32, 1)
+__global__ void __launch_bounds__((kW8A8Warps + 2) * 32, 1)
 verify_stack_kernel(const __grid_constant__ StackParams sp) {
     using C = StackCfg<NG>;
     constexpr int MP = C::MP;
@@ -803,6 +865,7 @@ verify_stack_kernel(const __grid_constant__ StackParams sp) {
     float* s_amax = reinterpret_cast<float*>(s_tok + MP);        // [warp][MP]
     volatile int* abort = reinterpret_cast<volatile int*>(s_amax + kMaxConsumerWarps * MP);
     volatile int* flag = abort + 1;
+    volatile long long* s_issued = reinterpret_cast<volatile long long*>(abort + 2);   // 8-aligned
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
@@ -819,13 +882,40 @@ verify_stack_kernel(const __grid_constant__ StackParams sp) {
             mbar_init(&empty[st], CW);
         }
         *abort = 0;
+        *s_issued = 0;
         fence_barrier_init();
     }
     __syncthreads();
 
-    // Grid barriers: every CTA arrives twice per phase p on sync[0]: once its
-    // share of the phase input is quantized (B(p): (2p+1) G arrivals in total)
-    // and once its tiles of phase p are done (A(p): (2p+2) G arrivals).
+    if (warp == CW + 1) {
+        // ---------------- L2 prefetch: the same tile order, ahead of the producer ----
+        // HBM keeps streaming while the consumers wait at phase boundaries; the
+        // producer's shared-memory loads then find the tiles in L2.
+        if (lane != 0) return;
+        long long n = 0;
+        for (int p = 0; p < P; ++p) {
+            const StackPhase& ph = sp.ph[p];
+            const CUtensorMap* tmap = &sp.tmap_w[p];
+            const long long T = (long long)ph.KT * ph.NT;
+            const int a = (int)((long long)blockIdx.x * T / G);
+            const int b = (int)((long long)(blockIdx.x + 1) * T / G);
+            for (int j = a; j < b; ++j, ++n) {
+                if (n - *s_issued > kStackL2Ahead) {
+                    const unsigned long long t0 = global_timer_ns();
+                    while (n - *s_issued > kStackL2Ahead) {
+                        if (*abort || global_timer_ns() - t0 > kWaitLimitNs) return;
+                        __nanosleep(200);
+                    }
+                }
+                const int nt = j / ph.KT, kt = j - nt * ph.KT;
+                tma_prefetch_l2_2d(tmap, kt * BKB, nt * BN);
+            }
+        }
+        return;
+    }
+
+    // Grid barriers: every CTA arrives once per phase on B (its share of the
+    // phase input is quantized) and once on A (its tiles of the phase are done).
     if (warp == CW) {
         // ---------------- producer ----------------
         // Weight tiles of every phase stream in phase order, ahead of the
@@ -844,13 +934,10 @@ verify_stack_kernel(const __grid_constant__ StackParams sp) {
         auto refresh = [&]() {
             if (pend_n == 0) return;
             if (pend_ph[pend_head] > ready) {
-                const unsigned c = ld_acquire_gpu(&sp.sync[0]);
-                if (c >= (unsigned)G) {
-                    const int rp = (int)((c / (unsigned)G - 1u) / 2u);
-                    if (rp > ready) {
-                        ready = rp;
-                        fence_proxy_async_global();
-                    }
+                const int rp = (int)ld_acquire_gpu(&sp.sync[kFlagB]) - 1;
+                if (rp > ready) {
+                    ready = rp;
+                    fence_proxy_async_global();
                 }
             }
             while (pend_n > 0 && pend_ph[pend_head] <= ready) {
@@ -872,14 +959,16 @@ verify_stack_kernel(const __grid_constant__ StackParams sp) {
             const int a = (int)((long long)blockIdx.x * T / G);
             const int b = (int)((long long)(blockIdx.x + 1) * T / G);
             for (int j = a; j < b; ++j) {
-                if (issued >= Stages && !mbar_try_wait(&empty[st], (round - 1) & 1)) {
+                if (issued >= Stages && !mbar_test_wait(&empty[st], (round - 1) & 1)) {
+                    // poll without suspending: pending activation loads must go
+                    // out as soon as their phase's codes are complete
                     const unsigned long long t0 = global_timer_ns();
-                    while (!mbar_try_wait(&empty[st], (round - 1) & 1)) {
+                    while (!mbar_test_wait(&empty[st], (round - 1) & 1)) {
                         refresh();
-                        if (*abort || ld_acquire_gpu(&sp.sync[2])) { ok = false; break; }
+                        if (*abort || ld_acquire_gpu(&sp.sync[kAbort])) { ok = false; break; }
                         if (global_timer_ns() - t0 > kWaitLimitNs) {
                             atomicOr(&g_stream_gemm_error, kErrEmptyWait);
-                            atomicExch(&sp.sync[2], 1u);
+                            atomicExch(&sp.sync[kAbort], 1u);
                             *abort = 1;
                             ok = false;
                             break;
@@ -899,6 +988,7 @@ verify_stack_kernel(const __grid_constant__ StackParams sp) {
                     if (pend_n == 1 || (issued & 3) == 0) refresh();
                 }
                 ++issued;
+                *s_issued = issued;
                 if (++st == Stages) { st = 0; ++round; }
             }
         }
@@ -908,7 +998,7 @@ verify_stack_kernel(const __grid_constant__ StackParams sp) {
             while (pend_n > 0) {
                 refresh();
                 if (pend_n == 0) break;
-                if (ld_acquire_gpu(&sp.sync[2]) || global_timer_ns() - t0 > kWaitLimitNs) {
+                if (ld_acquire_gpu(&sp.sync[kAbort]) || global_timer_ns() - t0 > kWaitLimitNs) {
                     atomicOr(&g_stream_gemm_error, kErrDrainWait);
                     break;
                 }
@@ -946,7 +1036,7 @@ verify_stack_kernel(const __grid_constant__ StackParams sp) {
 
         // ---- A(p-1): every CTA finished phase p-1 (its outputs may feed this input)
         if (p > 0) {
-            if (tid == 0 && !grid_wait(sp.sync, (unsigned)(2 * p * G))) *abort = 1;
+            if (tid == 0 && !grid_wait(sp.sync, kFlagA, (unsigned)p)) *abort = 1;
             consumer_sync<CW>();
         }
 
@@ -1042,9 +1132,8 @@ verify_stack_kernel(const __grid_constant__ StackParams sp) {
             }
             // B(p): the codes are visible to the other CTAs' TMA loads
             fence_proxy_async_global();
-            __threadfence();
             consumer_sync<CW>();
-            if (tid == 0) { __threadfence(); atomicAdd(&sp.sync[0], 1u); }
+            if (tid == 0) grid_arrive(sp.sync, kCountB, (unsigned)((p + 1) * G), kFlagB, (unsigned)(p + 1));
         }
 
         // ---- this CTA's tiles
@@ -1090,17 +1179,20 @@ verify_stack_kernel(const __grid_constant__ StackParams sp) {
                     const int r = e / MP, m = e - (e / MP) * MP;
                     if (m < M && nt * BN + r < ph.N) atomicAdd(&gacc[e], stg[e]);
                 }
-                __threadfence();
+                // one gpu-scope fence by the publishing thread after the CTA
+                // barrier orders every thread's adds before the count (the
+                // pattern of a grid-wide barrier); its acquire side likewise
                 consumer_sync<CW>();
                 if (tid == 0) {
                     __threadfence();
                     const unsigned prev = atomicAdd(&sp.ws_cnt[nt], (unsigned)seg_len);
-                    *flag = (prev + (unsigned)seg_len == (unsigned)KT) ? 1 : 0;
+                    const bool last = prev + (unsigned)seg_len == (unsigned)KT;
+                    if (last) __threadfence();
+                    *flag = last ? 1 : 0;
                 }
                 consumer_sync<CW>();
             }
             if (whole || *flag) {
-                if (!whole) __threadfence();
                 const int r = tid;
                 const int n = nt * BN + r;
                 const bool valid = r < BN && n < ph.N;
@@ -1155,17 +1247,17 @@ verify_stack_kernel(const __grid_constant__ StackParams sp) {
                         }
                         atomicMax(&sp.keys[tid], k);
                     }
-                    __threadfence();
                     consumer_sync<CW>();
                     if (tid == 0) {
                         __threadfence();
                         const unsigned prev = atomicAdd(&sp.sync[3], 1u);
-                        *flag = (prev + 1u == (unsigned)ph.NT) ? 2 : 0;
+                        const bool last = prev + 1u == (unsigned)ph.NT;
+                        if (last) __threadfence();
+                        *flag = last ? 2 : 0;
                     }
                     consumer_sync<CW>();
                     if (*flag == 2) {
                         // last LM tile: decode the argmax, then accept
-                        __threadfence();
                         if (tid < M) {
                             const unsigned long long k = atomicExch(&sp.keys[tid], 0ull);
                             const int32_t t = (int32_t)(0xFFFFFFFFu - (unsigned)(k & 0xFFFFFFFFull));
@@ -1195,15 +1287,18 @@ verify_stack_kernel(const __grid_constant__ StackParams sp) {
         }
         // ---- A(p): this CTA is done with phase p
         consumer_sync<CW>();
-        if (tid == 0) { __threadfence(); atomicAdd(&sp.sync[0], 1u); }
+        if (tid == 0) grid_arrive(sp.sync, kCountA, (unsigned)((p + 1) * G), kFlagA, (unsigned)(p + 1));
     }
     // last CTA out resets the barrier words for the next launch
     if (tid == 0) {
         __threadfence();
         const unsigned prev = atomicAdd(&sp.sync[1], 1u);
         if (prev + 1u == (unsigned)G) {
-            atomicExch(&sp.sync[0], 0u);
-            atomicExch(&sp.sync[2], 0u);
+            atomicExch(&sp.sync[kCountB], 0u);
+            atomicExch(&sp.sync[kCountA], 0u);
+            atomicExch(&sp.sync[kAbort], 0u);
+            atomicExch(&sp.sync[kFlagB], 0u);
+            atomicExch(&sp.sync[kFlagA], 0u);
             __threadfence();
             atomicExch(&sp.sync[1], 0u);
         }
@@ -1223,7 +1318,7 @@ WsLayout ws_layout(int mp, int n, bool lm_head) {
     L.keys = off;
     if (lm_head) off = al16(off + (size_t)mp * 8);
     L.done = off;
-    if (lm_head) off = al16(off + 4);
+    if (lm_head) off = al16(off + 5 * 128);   // counters and flags on separate 128-byte lines
     L.total = off;
     return L;
 }
@@ -1319,7 +1414,7 @@ cudaError_t launch_verify_stack(const StackLaunch& a, int num_sms, cudaStream_t 
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(num_sms);
-    cfg.blockDim = dim3((kW8A8Warps + 1) * 32);
+    cfg.blockDim = dim3((kW8A8Warps + 2) * 32);
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeCooperative;

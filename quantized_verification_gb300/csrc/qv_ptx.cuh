@@ -66,6 +66,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, unsigned parity) {
     return ok != 0;
 }
 
+// Non-blocking probe of the phase with the given parity (never suspends).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, unsigned parity) {
+    unsigned ok;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+    return ok != 0;
+}
+
 // Wait for the phase with the given parity to complete, for at most
 // kWaitLimitNs. Returns false (without waiting) once *abort is set, and sets
 // *abort itself when the limit runs out.
@@ -113,6 +123,13 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map,
         :: "r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)),
            "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
         : "memory");
+}
+
+// Prefetch the box at (x, y) of a 2-D tensor map into L2 (no shared memory,
+// no completion to wait for).
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int x, int y) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];"
+                 :: "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y) : "memory");
 }
 
 // ---------------------------------------------------------------- PDL
