@@ -5,11 +5,16 @@
 //   items 2-3: weights quantized to INT8 offline; BF16 activations scaled by
 //   the smoothing factor and converted to INT8 online.
 //
-// One CTA per row. Pass 1 reads the row with 16-byte loads and forms
-// amax = max |x * c| (warp shuffles, then one shared-memory step); pass 2
-// re-reads the row (cache-resident) and writes the codes. Every floating
-// point step is a single IEEE operation in round-to-nearest-even:
-//   s = fl(amax / 127), q = clamp(rne(fl(x' / s)), -127, 127), q = 0 if s == 0.
+// One CTA of 512 threads per row. Rows of up to 512 x 4 16-byte vectors
+// (16384 bf16 / 8192 fp32 elements) are read once into registers with all
+// loads in flight together; longer rows are read twice (amax pass, code
+// pass). amax = max |x * c| is reduced with warp shuffles and one
+// shared-memory step. Every floating point step is a single IEEE operation
+// in round-to-nearest-even:
+//   s = fl(amax / 127), q = clamp(rne(fl(x' / s)), -127, 127), q = 0 if s == 0,
+// where the quotient's rounding is decided from fl(x' * fl(1 / s)) unless
+// that product lies within 2^-20 of a half-integer (then from the quotient
+// itself; quant_code in qv_ptx.cuh gives the error bound).
 
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -22,7 +27,8 @@
 namespace qv {
 namespace {
 
-constexpr int kQuantThreads = 256;
+constexpr int kQuantThreads = 512;
+constexpr int kQuantRegVecs = 4;   // 16-byte vectors per thread kept in registers
 
 template <bool BF16>
 struct Vec;
@@ -49,11 +55,30 @@ struct Vec<false> {      // 4 fp32 per 16-byte load
     }
 };
 
-__device__ __forceinline__ int8_t code_of(float v, float s) {
-    if (s == 0.f) return 0;
-    int q = __float2int_rn(__fdiv_rn(v, s));
-    q = q > 127 ? 127 : (q < -127 ? -127 : q);
-    return (int8_t)q;
+// x' = fl(x * c) for the E elements of vector v (c = 1 without multipliers).
+template <int E>
+__device__ __forceinline__ void apply_mul(float (&e)[E], const float* __restrict__ mul, int v) {
+    if (mul) {
+#pragma unroll
+        for (int j = 0; j < E; ++j) e[j] = __fmul_rn(e[j], __ldg(mul + v * E + j));
+    }
+}
+
+template <int E>
+__device__ __forceinline__ void store_codes(int8_t* qr, int v, const float (&e)[E], float s, float r) {
+    uint32_t packed[E / 4];
+#pragma unroll
+    for (int w = 0; w < E / 4; ++w) {
+        uint32_t word = 0;
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            word |= (uint32_t)(uint8_t)(int8_t)quant_code(e[4 * w + j], s, r) << (8 * j);
+        packed[w] = word;
+    }
+    if constexpr (E == 8)
+        *reinterpret_cast<uint2*>(qr + v * 8) = make_uint2(packed[0], packed[1]);
+    else
+        *reinterpret_cast<uint32_t*>(qr + v * 4) = packed[0];
 }
 
 template <bool BF16>
@@ -66,50 +91,70 @@ quantize_rows_kernel(const uint8_t* __restrict__ x, int K, const float* __restri
     grid_dependency_wait();
 
     const int row = blockIdx.x;
+    const int tid = threadIdx.x;
     const int nvec = K / E;
+    const bool in_regs = nvec <= kQuantThreads * kQuantRegVecs;
     const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)row * K * (BF16 ? 2 : 4));
 
+    uint4 rv[kQuantRegVecs];
     float amax = 0.f;
-    for (int v = threadIdx.x; v < nvec; v += kQuantThreads) {
-        float e[E];
-        V::unpack(__ldg(xr + v), e);
+    if (in_regs) {
 #pragma unroll
-        for (int j = 0; j < E; ++j) {
-            const float val = mul ? __fmul_rn(e[j], __ldg(mul + v * E + j)) : e[j];
-            amax = fmaxf(amax, fabsf(val));
+        for (int u = 0; u < kQuantRegVecs; ++u) {
+            const int v = tid + u * kQuantThreads;
+            rv[u] = v < nvec ? __ldg(xr + v) : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int u = 0; u < kQuantRegVecs; ++u) {
+            const int v = tid + u * kQuantThreads;
+            if (v < nvec) {
+                float e[E];
+                V::unpack(rv[u], e);
+                apply_mul<E>(e, mul, v);
+#pragma unroll
+                for (int j = 0; j < E; ++j) amax = fmaxf(amax, fabsf(e[j]));
+            }
+        }
+    } else {
+        for (int v = tid; v < nvec; v += kQuantThreads) {
+            float e[E];
+            V::unpack(__ldg(xr + v), e);
+            apply_mul<E>(e, mul, v);
+#pragma unroll
+            for (int j = 0; j < E; ++j) amax = fmaxf(amax, fabsf(e[j]));
         }
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
     __shared__ float warp_max[kQuantThreads / 32];
-    if ((threadIdx.x & 31) == 0) warp_max[threadIdx.x >> 5] = amax;
+    if ((tid & 31) == 0) warp_max[tid >> 5] = amax;
     __syncthreads();
     amax = warp_max[0];
 #pragma unroll
     for (int w = 1; w < kQuantThreads / 32; ++w) amax = fmaxf(amax, warp_max[w]);
     const float s = __fdiv_rn(amax, 127.0f);
-    if (threadIdx.x == 0) scale[row] = s;
+    const float r = __frcp_rn(s);
+    if (tid == 0) scale[row] = s;
 
     int8_t* qr = q + (size_t)row * K;
-    for (int v = threadIdx.x; v < nvec; v += kQuantThreads) {
-        float e[E];
-        V::unpack(__ldg(xr + v), e);
-        uint32_t packed[E / 4];
+    if (in_regs) {
 #pragma unroll
-        for (int w = 0; w < E / 4; ++w) {
-            uint32_t word = 0;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int idx = 4 * w + j;
-                const float val = mul ? __fmul_rn(e[idx], __ldg(mul + v * E + idx)) : e[idx];
-                word |= (uint32_t)(uint8_t)code_of(val, s) << (8 * j);
+        for (int u = 0; u < kQuantRegVecs; ++u) {
+            const int v = tid + u * kQuantThreads;
+            if (v < nvec) {
+                float e[E];
+                V::unpack(rv[u], e);
+                apply_mul<E>(e, mul, v);
+                store_codes<E>(qr, v, e, s, r);
             }
-            packed[w] = word;
         }
-        if constexpr (E == 8)
-            *reinterpret_cast<uint2*>(qr + v * 8) = make_uint2(packed[0], packed[1]);
-        else
-            *reinterpret_cast<uint32_t*>(qr + v * 4) = packed[0];
+    } else {
+        for (int v = tid; v < nvec; v += kQuantThreads) {
+            float e[E];
+            V::unpack(__ldg(xr + v), e);
+            apply_mul<E>(e, mul, v);
+            store_codes<E>(qr, v, e, s, r);
+        }
     }
 }
 

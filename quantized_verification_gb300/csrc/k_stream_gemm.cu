@@ -50,6 +50,7 @@
 
 #include "qv_internal.h"
 #include "qv_ptx.cuh"
+#include "stream_common.cuh"
 
 namespace qv {
 
@@ -57,10 +58,6 @@ __device__ unsigned int g_stream_gemm_error;
 
 namespace {
 
-constexpr int BN = kTileN;            // output channels per tile
-constexpr int BKB = kTileKBytes;      // bytes of K per tile (one 128-byte row)
-constexpr int kMaxConsumerWarps = 8;
-constexpr int kWTileBytes = BN * BKB;             // 16 KB
 
 // Consumer warps per CTA (one more warp produces), and how many of the four
 // 32-byte chunk pairs of each tile row go through the int8 tensor path; the
@@ -89,44 +86,22 @@ __host__ __device__ constexpr int s8_pairs() { return NG == 1 ? QV_S8_PAIRS_NARR
 static_assert(kW8A8Warps == 4 || kW8A8Warps == 8, "4 or 8 consumer warps");
 static_assert(kBf16Warps == 4 || kBf16Warps == 8, "4 or 8 consumer warps");
 
-template <int NG>
+template <int NG, bool TMAX = true>
 struct Cfg {
     static constexpr int MP = 8 * NG;                        // padded tokens
     static constexpr int XBytes = MP * BKB;                  // activation slice
-    static constexpr int XSlot = ((XBytes + 1023) / 1024) * 1024;
+    // TMAX: the activation slice travels with each weight tile; otherwise
+    // the codes live in a per-CTA buffer after the carve-up below.
+    static constexpr int XSlot = TMAX ? ((XBytes + 1023) / 1024) * 1024 : 0;
     static constexpr int StageBytes = kWTileBytes + XSlot;
-    static constexpr int Stages = NG == 1 ? 6 : NG == 2 ? 6 : NG == 4 ? 5 : 4;
+    static constexpr int Stages = !TMAX ? 6 : NG == 1 ? 6 : NG == 2 ? 6 : NG == 4 ? 5 : 4;
     static constexpr int StgWords = BN * MP;                 // epilogue staging
     static constexpr int SmemBytes =
         1024 /*alignment slack*/ + Stages * StageBytes + StgWords * 4 +
         2 * Stages * 8 + kMaxConsumerWarps * MP * 8 + MP * 4 + 64;
+    static constexpr int XcOffset = ((SmemBytes + 1023) / 1024) * 1024;   // from the aligned base
 };
 
-template <int CW>
-__device__ __forceinline__ void consumer_sync() {
-    asm volatile("bar.sync 1, %0;" :: "n"(CW * 32) : "memory");
-}
-
-// Order-preserving map of a float to uint32 (larger float -> larger key);
-// -0 is folded onto +0 first.
-__device__ __forceinline__ uint32_t ordered_bits(float f) {
-    uint32_t u = __float_as_uint(f);
-    if (u == 0x80000000u) u = 0u;
-    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-__device__ __forceinline__ float unordered_bits(uint32_t o) {
-    uint32_t u = (o & 0x80000000u) ? (o & 0x7FFFFFFFu) : ~o;
-    return __uint_as_float(u);
-}
-
-__device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long v) {
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-        unsigned long long o = __shfl_xor_sync(0xffffffffu, v, off);
-        v = o > v ? o : v;
-    }
-    return v;
-}
 
 // Shared-memory carve-up common to both kernels.
 template <int Stages, int StageBytes, int StgWords, int MP>
@@ -162,57 +137,6 @@ struct Smem {
     __device__ __forceinline__ uint8_t* x_tile(int s) { return stages + s * StageBytes + kWTileBytes; }
 };
 
-// Producer: stream tiles [a, b) into the ring. Weight tiles of the first
-// ring fill are requested before the grid dependency wait.
-template <int Stages, class SM>
-__device__ __forceinline__ void produce(SM& sm, const CUtensorMap* tw, const CUtensorMap* tx,
-                                        int a, int b, int KT, int kx_elems_per_tile,
-                                        unsigned tx_bytes) {
-    prefetch_tensormap(tw);
-    prefetch_tensormap(tx);
-    const uint64_t pol_w = policy_evict_first();
-    const uint64_t pol_x = policy_evict_last();
-    const int n = b - a;
-    const int pre = n < Stages ? n : Stages;
-    for (int j = 0; j < pre; ++j) {
-        const int tile = a + j, nt = tile / KT, kt = tile - nt * KT;
-        mbar_arrive_expect_tx(&sm.full[j], tx_bytes);
-        tma_load_2d(sm.w_tile(j), tw, kt * kx_elems_per_tile, nt * BN, &sm.full[j], pol_w);
-    }
-    grid_dependency_wait();
-    for (int j = 0; j < pre; ++j) {
-        const int tile = a + j, kt = tile % KT;
-        tma_load_2d(sm.x_tile(j), tx, kt * kx_elems_per_tile, 0, &sm.full[j], pol_x);
-    }
-    int issued = pre;
-    int s = pre % Stages;
-    int round = pre / Stages;
-    for (int j = pre; j < n; ++j) {
-        if (!mbar_wait_bounded(&sm.empty[s], (round - 1) & 1, sm.abort)) {
-            atomicOr(&g_stream_gemm_error, kErrEmptyWait);
-            break;
-        }
-        const int tile = a + j, nt = tile / KT, kt = tile - nt * KT;
-        mbar_arrive_expect_tx(&sm.full[s], tx_bytes);
-        tma_load_2d(sm.w_tile(s), tw, kt * kx_elems_per_tile, nt * BN, &sm.full[s], pol_w);
-        tma_load_2d(sm.x_tile(s), tx, kt * kx_elems_per_tile, 0, &sm.full[s], pol_x);
-        ++issued;
-        if (++s == Stages) { s = 0; ++round; }
-    }
-    // Do not leave the CTA while copies into its shared memory are in flight.
-    const int first = issued > Stages ? issued - Stages : 0;
-    for (int j = first; j < issued; ++j) {
-        const int st = j % Stages, par = (j / Stages) & 1;
-        if (mbar_try_wait(&sm.full[st], par)) continue;
-        unsigned long long t0 = global_timer_ns();
-        while (!mbar_try_wait(&sm.full[st], par)) {
-            if (global_timer_ns() - t0 > kWaitLimitNs) {
-                atomicOr(&g_stream_gemm_error, kErrDrainWait);
-                return;
-            }
-        }
-    }
-}
 
 // ---------------------------------------------------------------------------
 // One weight tile (128 channels x 128 bytes of K, 128-byte swizzled) against
@@ -337,37 +261,138 @@ __device__ __forceinline__ void w8a8_tile_mma(uint32_t wb, uint32_t xb, const Ti
 
 // ---------------------------------------------------------------------------
 // W8A8 kernel
+//
+// XMODE 0: the int8 activation codes (qv_quantize_act's output) travel with
+// each weight tile by TMA. XMODE 1 / 2: the kernel quantizes the bf16 / fp32
+// activations itself (qv_w8a8_linear_act): after the grid-dependency wait
+// every CTA computes the per-token amax of x' = fl(x * c) over the whole row
+// (the same bits in every CTA), then quantizes only the K-tiles its own
+// stream-K range touches into a shared-memory buffer with the layout of the
+// TMA tile (128-byte rows, 128-byte swizzle), while the producer keeps
+// streaming weights. Codes and scales are those of qv_quantize_act, bit for
+// bit: s = fl(amax / 127), q = quant_code(x', s, fl(1 / s)).
 // ---------------------------------------------------------------------------
-struct W8A8Params {
-    int M, N, K, KT, NT;
-    long long T;
-    const float* sx;
-    const float* sw;
-    void* y;
-    int y_bf16;
-    int32_t* acc_debug;
-    int32_t* tokens;
-    float* max_logit;
-    int32_t* ws_acc;
-    unsigned* ws_cnt;
-    unsigned long long* keys;
-    unsigned* done;
+struct ActParams {
+    const void* x;            // [M][K] fp32 or bf16
+    const float* act_mul;     // [K] smoothing multipliers (16-byte aligned) or null
+    int xc_slots;             // K-tiles of codes the shared buffer holds (>= min(tiles per CTA, KT))
 };
 
-template <int NG, int EPI>
+// 16 elements of row `row` from column k0 as binary32, times the multipliers.
+template <bool BF16>
+__device__ __forceinline__ void load16_scaled(const void* x, const float* mul, int K, int row, int k0,
+                                              float (&e)[16]) {
+    if (BF16) {
+        const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(x) + (size_t)row * K + k0);
+        const uint4 v0 = __ldg(src), v1 = __ldg(src + 1);
+        const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            e[2 * j] = __uint_as_float(w[j] << 16);
+            e[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+        }
+    } else {
+        const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(x) + (size_t)row * K + k0);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float4 v = __ldg(src + j);
+            e[4 * j] = v.x; e[4 * j + 1] = v.y; e[4 * j + 2] = v.z; e[4 * j + 3] = v.w;
+        }
+    }
+    if (mul) {
+        const float4* m4 = reinterpret_cast<const float4*>(mul + k0);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float4 c = __ldg(m4 + j);
+            e[4 * j] = __fmul_rn(e[4 * j], c.x);
+            e[4 * j + 1] = __fmul_rn(e[4 * j + 1], c.y);
+            e[4 * j + 2] = __fmul_rn(e[4 * j + 2], c.z);
+            e[4 * j + 3] = __fmul_rn(e[4 * j + 3], c.w);
+        }
+    }
+}
+
+// Consumers of an XMODE 1/2 launch: per-token scales into sm_sx (and
+// reciprocals into s_rcp), then the codes of K-tiles kt0, kt0+1, ... (mod KT),
+// nslot of them, into xc (slot j = MP rows x 128 bytes, 128-byte swizzle).
+template <int MP, int CW, bool BF16>
+__device__ __forceinline__ void act_prologue(const W8A8Params& p, const ActParams& q, float* sm_sx,
+                                             unsigned* s_amax, float* s_rcp, uint8_t* xc, int kt0,
+                                             int nslot, int tid) {
+    constexpr int CT = CW * 32;
+    if (tid < MP) s_amax[tid] = 0u;
+    consumer_sync<CW>();
+    // amax over 16-element chunks: chunk c of the row-major M x K matrix
+    const int cpr = p.K / 16;
+    const int total = p.M * cpr;
+    for (int base = tid; base < total; base += 4 * CT) {
+        float mx[4];
+        int rows[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int c = base + u * CT;
+            mx[u] = 0.f;
+            rows[u] = -1;
+            if (c < total) {
+                const int row = c / cpr;
+                float e[16];
+                load16_scaled<BF16>(q.x, q.act_mul, p.K, row, (c - row * cpr) * 16, e);
+#pragma unroll
+                for (int j = 0; j < 16; ++j) mx[u] = fmaxf(mx[u], fabsf(e[j]));
+                rows[u] = row;
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            if (rows[u] >= 0) atomicMax(&s_amax[rows[u]], __float_as_uint(mx[u]));
+    }
+    consumer_sync<CW>();
+    if (tid < MP) {
+        const float sc = tid < p.M ? __fdiv_rn(__uint_as_float(s_amax[tid]), 127.0f) : 0.f;
+        sm_sx[tid] = sc;
+        s_rcp[tid] = __frcp_rn(sc);
+    }
+    consumer_sync<CW>();
+    const int items = nslot * MP * 8;
+    for (int it = tid; it < items; it += CT) {
+        const int j = it / (MP * 8);
+        const int rem = it - j * (MP * 8);
+        const int row = rem >> 3, ch = rem & 7;
+        int kt = kt0 + j;
+        if (kt >= p.KT) kt -= p.KT;
+        const int k0 = kt * BKB + ch * 16;
+        uint32_t w[4] = {0u, 0u, 0u, 0u};
+        if (row < p.M && k0 < p.K) {
+            float e[16];
+            load16_scaled<BF16>(q.x, q.act_mul, p.K, row, k0, e);
+            const float sc = sm_sx[row], rc = s_rcp[row];
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj)
+                w[jj >> 2] |= (uint32_t)(uint8_t)(int8_t)quant_code(e[jj], sc, rc) << (8 * (jj & 3));
+        }
+        *reinterpret_cast<uint4*>(xc + (size_t)j * MP * BKB + row * BKB + ((ch ^ (row & 7)) << 4)) =
+            make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    consumer_sync<CW>();
+}
+
+template <int NG, int EPI, int XMODE>
 __global__ void __launch_bounds__((kW8A8Warps + 1) * 32, 1)
 w8a8_stream_kernel(const __grid_constant__ CUtensorMap tmap_w,
-                   const __grid_constant__ CUtensorMap tmap_x, const W8A8Params p) {
-    using C = Cfg<NG>;
+                   const __grid_constant__ CUtensorMap tmap_x, const W8A8Params p, const ActParams q) {
+    constexpr bool TMAX = XMODE == 0;
+    using C = Cfg<NG, TMAX>;
     constexpr int MP = C::MP;
     constexpr int Stages = C::Stages;
     constexpr int CW = kW8A8Warps;
-    constexpr int CT = CW * 32;
     constexpr int RW = BN / CW;          // output channels per consumer warp
     constexpr int BPW = RW / 16;         // 16-channel MMA blocks per warp
     constexpr int S8P = s8_pairs<NG>();
     extern __shared__ uint8_t smem_raw[];
     Smem<Stages, C::StageBytes, C::StgWords, MP> sm(smem_raw);
+    uint8_t* xc = sm.stages + (C::XcOffset - 0);   // the carve-up starts at the aligned base
+    __shared__ unsigned s_amax[MP];
+    __shared__ float s_rcp[MP];
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
@@ -388,21 +413,28 @@ w8a8_stream_kernel(const __grid_constant__ CUtensorMap tmap_w,
 
     if (warp == CW) {
         if (lane == 0)
-            produce<Stages>(sm, &tmap_w, &tmap_x, a, b, p.KT, BKB,
-                            (unsigned)(kWTileBytes + C::XBytes));
+            produce<Stages>(&g_stream_gemm_error, sm, &tmap_w, TMAX ? &tmap_x : nullptr, a, b, p.KT,
+                            BKB, (unsigned)(kWTileBytes + (TMAX ? C::XBytes : 0)));
         return;
     }
 
     // ---------------- consumers ----------------
     grid_dependency_wait();
-    if (tid < MP) sm.sx[tid] = tid < p.M ? p.sx[tid] : 0.f;
-    consumer_sync<CW>();
+    const int kt0 = a % p.KT;
+    if (TMAX) {
+        if (tid < MP) sm.sx[tid] = tid < p.M ? p.sx[tid] : 0.f;
+        consumer_sync<CW>();
+    } else {
+        const int nslot = min(min(b - a, p.KT), q.xc_slots);   // the host sizes xc_slots to cover it
+        act_prologue<MP, CW, XMODE == 1>(p, q, sm.sx, s_amax, s_rcp, xc, kt0, nslot, tid);
+    }
 
     const int g = lane >> 2, t4 = lane & 3;
     const TileLanes<BPW> L(RW * warp, lane);
 
     int32_t acci[BPW][NG][4];
     int s = 0, phase = 0;
+    int slot = 0;                        // code slot of tile i (XMODE 1/2): (i - a) mod KT
     int i = a;
     while (i < b) {
         const int nt = i / p.KT;
@@ -418,10 +450,12 @@ w8a8_stream_kernel(const __grid_constant__ CUtensorMap tmap_w,
         for (; i < seg_end; ++i) {
             if (!mbar_wait_bounded(&sm.full[s], phase, sm.abort))
                 atomicOr(&g_stream_gemm_error, kErrFullWait);
-            w8a8_tile_mma<NG, BPW, S8P>(smem_u32(sm.w_tile(s)), smem_u32(sm.x_tile(s)), L, acci);
+            const uint32_t xb = TMAX ? smem_u32(sm.x_tile(s)) : smem_u32(xc + slot * (MP * BKB));
+            w8a8_tile_mma<NG, BPW, S8P>(smem_u32(sm.w_tile(s)), xb, L, acci);
             __syncwarp();
             if (lane == 0) mbar_arrive(&sm.empty[s]);
             if (++s == Stages) { s = 0; phase ^= 1; }
+            if (++slot == p.KT) slot = 0;
         }
 
         // -------- segment end: stage the int32 sums [row][token] --------
@@ -437,88 +471,7 @@ w8a8_stream_kernel(const __grid_constant__ CUtensorMap tmap_w,
         }
         consumer_sync<CW>();
 
-        const int seg_len = seg_end - seg_begin;
-        const bool whole = seg_len == p.KT;
-        int32_t* gacc = p.ws_acc + (size_t)nt * BN * MP;
-        if (!whole) {
-            for (int e = tid; e < BN * MP; e += CT) {
-                const int r = e / MP, m = e - (e / MP) * MP;
-                if (m < p.M && nt * BN + r < p.N) atomicAdd(&gacc[e], sm.stg[e]);
-            }
-            __threadfence();
-            consumer_sync<CW>();
-            if (tid == 0) {
-                __threadfence();
-                const unsigned prev = atomicAdd(&p.ws_cnt[nt], (unsigned)seg_len);
-                *sm.flag = (prev + (unsigned)seg_len == (unsigned)p.KT) ? 1 : 0;
-            }
-            consumer_sync<CW>();
-        }
-        const bool finisher = whole || *sm.flag;
-        if (finisher) {
-            if (!whole) __threadfence();
-            // the first BN consumer threads (warps 0..3) own one output channel each
-            const int r = tid;
-            const int n = nt * BN + r;
-            const bool valid = r < BN && n < p.N;
-            const float swn = valid ? p.sw[n] : 0.f;
-            if (EPI == (int)Epi::Linear) {
-                if (valid) {
-                    for (int m = 0; m < p.M; ++m) {
-                        const int32_t acc = whole ? sm.stg[r * MP + m] : atomicExch(&gacc[r * MP + m], 0);
-                        if (p.acc_debug) p.acc_debug[(size_t)m * p.N + n] = acc;
-                        const float yv = __fmul_rn(__int2float_rn(acc), __fmul_rn(sm.sx[m], swn));
-                        if (p.y_bf16)
-                            reinterpret_cast<__nv_bfloat16*>(p.y)[(size_t)m * p.N + n] = __float2bfloat16_rn(yv);
-                        else
-                            reinterpret_cast<float*>(p.y)[(size_t)m * p.N + n] = yv;
-                    }
-                }
-            } else {
-                if (r < BN) {
-                    for (int m = 0; m < p.M; ++m) {
-                        unsigned long long key = 0ull;
-                        if (valid) {
-                            const int32_t acc = whole ? sm.stg[r * MP + m] : atomicExch(&gacc[r * MP + m], 0);
-                            const float yv = __fmul_rn(__int2float_rn(acc), __fmul_rn(sm.sx[m], swn));
-                            key = ((unsigned long long)ordered_bits(yv) << 32) |
-                                  (unsigned long long)(0xFFFFFFFFu - (unsigned)n);
-                        }
-                        key = warp_max_u64(key);
-                        if (lane == 0) sm.red[warp * MP + m] = key;
-                    }
-                }
-                consumer_sync<CW>();
-                if (tid < p.M) {
-                    unsigned long long k = sm.red[tid];
-#pragma unroll
-                    for (int w = 1; w < BN / 32; ++w) {
-                        const unsigned long long o = sm.red[w * MP + tid];
-                        k = o > k ? o : k;
-                    }
-                    atomicMax(&p.keys[tid], k);
-                }
-                __threadfence();
-                consumer_sync<CW>();
-                if (tid == 0) {
-                    __threadfence();
-                    const unsigned prev = atomicAdd(p.done, 1u);
-                    *sm.flag = (prev + 1u == (unsigned)p.NT) ? 2 : 0;
-                }
-                consumer_sync<CW>();
-                if (*sm.flag == 2) {
-                    __threadfence();
-                    if (tid < p.M) {
-                        const unsigned long long k = atomicExch(&p.keys[tid], 0ull);
-                        p.tokens[tid] = (int32_t)(0xFFFFFFFFu - (unsigned)(k & 0xFFFFFFFFull));
-                        if (p.max_logit) p.max_logit[tid] = unordered_bits((unsigned)(k >> 32));
-                    }
-                    if (tid == 0) atomicExch(p.done, 0u);
-                }
-            }
-            if (!whole && tid == 0) atomicExch(&p.ws_cnt[nt], 0u);
-        }
-        consumer_sync<CW>();   // staging buffer and flags are reused by the next segment
+        stream_epilogue<MP, CW, EPI>(sm, p, nt, seg_end - seg_begin, tid);
     }
 }
 
@@ -568,7 +521,7 @@ bf16_stream_kernel(const __grid_constant__ CUtensorMap tmap_w,
 
     if (warp == CW) {
         if (lane == 0)
-            produce<Stages>(sm, &tmap_w, &tmap_x, a, b, p.KT, BKB / 2,
+            produce<Stages>(&g_stream_gemm_error, sm, &tmap_w, &tmap_x, a, b, p.KT, BKB / 2,
                             (unsigned)(kWTileBytes + C::XBytes));
         return;
     }
@@ -676,9 +629,9 @@ bf16_stream_kernel(const __grid_constant__ CUtensorMap tmap_w,
     }
 }
 
-template <class P, class... Args>
+template <class... Args, class... Params>
 cudaError_t launch_ex(void (*kern)(Args...), int grid, int threads, int smem, cudaStream_t s,
-                      const CUtensorMap& tw, const CUtensorMap& tx, const P& params) {
+                      const Params&... params) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -691,7 +644,7 @@ cudaError_t launch_ex(void (*kern)(Args...), int grid, int threads, int smem, cu
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, tw, tx, params);
+    return cudaLaunchKernelEx(&cfg, kern, params...);
 }
 
 // ---------------------------------------------------------------------------
@@ -800,22 +753,6 @@ __device__ __forceinline__ bool grid_wait(unsigned* sync, int flag, unsigned val
             return false;
         }
     }
-}
-
-// q = clamp(rne(fl32(x / s)), -127, 127), s != 0, decided from t = fl32(x * r)
-// with r = fl32(1 / s) when t is far from every half-integer, else from the
-// IEEE quotient. Error bound: r = (1/s)(1+d1), t = (x/s)(1+d1)(1+d2) and
-// fl32(x/s) = (x/s)(1+d3) with |di| <= 2^-24, so |t - fl32(x/s)| < 2^-22 |t|.
-// If the distance from t to the nearest half-integer exceeds 2^-20 |t|, both
-// lie strictly on the same side of it and round to the same integer.
-__device__ __forceinline__ int quant_code(float x, float s, float r) {
-    if (s == 0.f) return 0;
-    const float t = __fmul_rn(x, r);
-    float q = rintf(t);
-    const float margin = __fsub_rn(0.5f, fabsf(__fsub_rn(t, q)));
-    if (!(margin > __fmul_rn(fabsf(t), 0x1p-20f))) q = rintf(__fdiv_rn(x, s));
-    const int qi = __float2int_rn(q);
-    return qi > 127 ? 127 : (qi < -127 ? -127 : qi);
 }
 
 // The 8 bf16 or 4 fp32 elements of one 16-byte vector as binary32 (bf16 widened).
@@ -1323,8 +1260,8 @@ WsLayout ws_layout(int mp, int n, bool lm_head) {
     return L;
 }
 
-cudaError_t launch_w8a8_stream(const W8A8Launch& a, int num_sms, cudaStream_t s) {
-    const int NG = a.MP / 8;
+namespace {
+W8A8Params make_w8a8_params(const W8A8Launch& a, int num_sms, int* grid) {
     const bool lm = a.epi == Epi::LmHead;
     WsLayout L = ws_layout(a.MP, a.N, lm);
     W8A8Params p;
@@ -1339,16 +1276,32 @@ cudaError_t launch_w8a8_stream(const W8A8Launch& a, int num_sms, cudaStream_t s)
     p.ws_cnt = reinterpret_cast<unsigned*>(ws + L.counters);
     p.keys = reinterpret_cast<unsigned long long*>(ws + L.keys);
     p.done = reinterpret_cast<unsigned*>(ws + L.done);
-    const int grid = (int)(p.T < num_sms ? p.T : num_sms);
-#define QV_W8A8_CASE(NGV)                                                                    \
-    case NGV:                                                                                \
-        return lm ? launch_ex(w8a8_stream_kernel<NGV, (int)Epi::LmHead>, grid,               \
-                              (kW8A8Warps + 1) * 32, Cfg<NGV>::SmemBytes, s, a.tmap_w,       \
-                              a.tmap_x, p)                                                   \
-                  : launch_ex(w8a8_stream_kernel<NGV, (int)Epi::Linear>, grid,               \
-                              (kW8A8Warps + 1) * 32, Cfg<NGV>::SmemBytes, s, a.tmap_w,       \
-                              a.tmap_x, p);
-    switch (NG) {
+    *grid = (int)(p.T < num_sms ? p.T : num_sms);
+    return p;
+}
+
+// Code slots one CTA of the fused-quantization kernel needs: the K-tiles of
+// its stream-K range (at most ceil(T / grid) tiles), at most KT.
+int act_slots(long long T, int KT, int grid) {
+    const long long per = (T + grid - 1) / grid;
+    return (int)(per < KT ? per : KT);
+}
+}  // namespace
+
+cudaError_t launch_w8a8_stream(const W8A8Launch& a, int num_sms, cudaStream_t s) {
+    int grid;
+    const W8A8Params p = make_w8a8_params(a, num_sms, &grid);
+    const bool lm = a.epi == Epi::LmHead;
+    const ActParams q = {};
+#define QV_W8A8_CASE(NGV)                                                                      \
+    case NGV:                                                                                  \
+        return lm ? launch_ex(w8a8_stream_kernel<NGV, (int)Epi::LmHead, 0>, grid,              \
+                              (kW8A8Warps + 1) * 32, Cfg<NGV>::SmemBytes, s, a.tmap_w,         \
+                              a.tmap_x, p, q)                                                  \
+                  : launch_ex(w8a8_stream_kernel<NGV, (int)Epi::Linear, 0>, grid,              \
+                              (kW8A8Warps + 1) * 32, Cfg<NGV>::SmemBytes, s, a.tmap_w,         \
+                              a.tmap_x, p, q);
+    switch (a.MP / 8) {
         QV_W8A8_CASE(1)
         QV_W8A8_CASE(2)
         QV_W8A8_CASE(4)
@@ -1356,6 +1309,45 @@ cudaError_t launch_w8a8_stream(const W8A8Launch& a, int num_sms, cudaStream_t s)
         default: return cudaErrorInvalidValue;
     }
 #undef QV_W8A8_CASE
+}
+
+size_t w8a8_act_smem(int MP, int K, int N, int num_sms) {
+    const int KT = ceil_div(K, BKB), NT = ceil_div(N, BN);
+    const long long T = (long long)KT * NT;
+    const int grid = (int)(T < num_sms ? T : num_sms);
+    const size_t xc = (size_t)act_slots(T, KT, grid) * MP * BKB;
+    size_t base;
+    if (MP == 8) base = Cfg<1, false>::XcOffset;
+    else if (MP == 16) base = Cfg<2, false>::XcOffset;
+    else return 0;
+    const size_t total = 1024 + base + xc;
+    return total <= kMaxDynSmem ? total : 0;
+}
+
+cudaError_t launch_w8a8_act(const W8A8Launch& a, const void* x, bool x_bf16, const float* act_mul,
+                            int num_sms, cudaStream_t s) {
+    int grid;
+    const W8A8Params p = make_w8a8_params(a, num_sms, &grid);
+    const size_t smem = w8a8_act_smem(a.MP, a.K, a.N, num_sms);
+    if (smem == 0) return cudaErrorInvalidValue;
+    ActParams q;
+    q.x = x;
+    q.act_mul = act_mul;
+    q.xc_slots = act_slots(p.T, p.KT, grid);
+    const bool lm = a.epi == Epi::LmHead;
+    const int threads = (kW8A8Warps + 1) * 32;
+#define QV_ACT_CASE(NGV, XM)                                                                         \
+    return lm ? launch_ex(w8a8_stream_kernel<NGV, (int)Epi::LmHead, XM>, grid, threads, (int)smem, s, \
+                          a.tmap_w, a.tmap_w, p, q)                                                  \
+              : launch_ex(w8a8_stream_kernel<NGV, (int)Epi::Linear, XM>, grid, threads, (int)smem, s, \
+                          a.tmap_w, a.tmap_w, p, q);
+    if (a.MP == 8) {
+        if (x_bf16) { QV_ACT_CASE(1, 1) } else { QV_ACT_CASE(1, 2) }
+    } else if (a.MP == 16) {
+        if (x_bf16) { QV_ACT_CASE(2, 1) } else { QV_ACT_CASE(2, 2) }
+    }
+#undef QV_ACT_CASE
+    return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_bf16_stream(const Bf16Launch& a, int num_sms, cudaStream_t s) {

@@ -1,0 +1,372 @@
+// k_tc_gemm.cu -- the W8A8 weight-streaming GEMM on the fifth-generation
+// tensor cores (tcgen05): y = dequant(xq . wq^T) (qv_w8a8_linear) and the LM
+// head fused with the greedy argmax (qv_lm_head_argmax).
+//   Quasar, gist.science/ja summary, section 2.2 item 3 (INT8 GEMM with INT32
+//   accumulation, dequantization to high precision); gist.science/it summary,
+//   section 2 item 3 (logits kept precise for the acceptance test).
+//
+// sm_103a has no integer kind for tcgen05.mma, so the int8 codes are widened
+// exactly to binary16 and multiplied with kind::f16 into an f32 accumulator
+// in tensor memory. Every product is an integer of magnitude <= 2^14 and one
+// tile sums 128 of them (|sum| <= 2^21 < 2^24), so every partial sum is an
+// exact binary32 integer; each tile's accumulator is read back, converted to
+// int32 and added in registers, which makes the result the exact int32 dot
+// product whatever the order of the tensor core's additions.
+//
+// Work split: the same stream-K order as the mma.sync kernels (tiles of 128
+// output channels x 128 bytes of K, channel-tile major; each CTA one
+// contiguous equal range), the same TMA producer and ring, and the same
+// split-K / argmax epilogue. Per CTA (one per SM):
+//  - warp 9, one thread: TMA producer (weights before the grid-dependency
+//    wait, activation codes after it);
+//  - warps 0-7, "converters": thread (warp w, lane l) owns output channel
+//    32 * (w % 4) + l of the tile and half w / 4 of its 128 K bytes. It widens
+//    its 64 weight bytes to 32 f16x2 words and stores them in its TMEM lane
+//    (the MMA's A operand, channel = lane, K along the columns); together
+//    the converters widen the MP x 128 activation codes into a shared-memory
+//    f16 buffer in the 128-byte-swizzled K-major layout (the B operand);
+//  - warp 8, one thread: issues the tile's eight M=128 x N x K=16 MMAs into a
+//    TMEM accumulator and commits them to an mbarrier;
+//  - the converters read the accumulator back (thread = channel, its half of
+//    the token columns), convert to int32 and accumulate; at the end of a
+//    channel tile's K range they stage the sums in shared memory for the
+//    common epilogue.
+// A, B and the accumulator rotate through four slots, so widening of tile
+// i+1..i+3 overlaps the MMAs of tile i and the readout lags four tiles.
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "qv_internal.h"
+#include "qv_ptx.cuh"
+#include "stream_common.cuh"
+
+namespace qv {
+
+__device__ unsigned int g_tc_gemm_error;
+
+namespace {
+
+constexpr int kTcConv = 8;          // converter warps 0..7
+constexpr int kTcMmaWarp = 8;       // MMA issue and TMEM allocation
+constexpr int kTcProdWarp = 9;      // TMA producer
+constexpr int kTcThreads = 10 * 32;
+constexpr int kTcRing = 4;          // A / B / accumulator slots
+constexpr int kTcACols = 64;        // TMEM columns of one A slot (128 f16 of K per lane)
+
+template <int MP>
+struct TcCfg {
+    static constexpr int NM = MP < 16 ? 16 : MP;          // MMA N: tokens padded to 16
+    static constexpr int MPH = NM / 2;                    // accumulator columns per converter thread
+    static constexpr int XBytes = MP * BKB;
+    static constexpr int XSlot = ((XBytes + 1023) / 1024) * 1024;
+    static constexpr int StageBytes = kWTileBytes + XSlot;
+    static constexpr int BSlot = 2 * NM * 128;            // two 64-element K blocks of f16 rows
+    static constexpr int Stages = MP <= 16 ? 8 : MP == 32 ? 7 : 5;
+    static constexpr int StgWords = BN * MP;
+    static constexpr int DCol0 = kTcRing * kTcACols;      // first accumulator column
+    static constexpr int TmemCols = 512;
+    static constexpr int SmemBytes = 1024 + Stages * StageBytes + kTcRing * BSlot + StgWords * 4 +
+                                     (2 * Stages + 2 * kTcRing) * 8 + kMaxConsumerWarps * MP * 8 +
+                                     MP * 4 + 64;
+    static_assert(DCol0 + kTcRing * NM <= TmemCols, "TMEM budget");
+    static_assert(SmemBytes <= 232448, "shared memory budget");
+    static_assert(NM % 16 == 0 && NM <= 256, "MMA N");
+};
+
+template <int MP>
+struct TcSmem {
+    using C = TcCfg<MP>;
+    uint8_t* stages;           // Stages x (W tile | X tile), 1024-aligned
+    uint8_t* bring;            // kTcRing x BSlot f16 activation operands
+    int32_t* stg;              // BN x MP staged sums
+    uint64_t* full;
+    uint64_t* empty;
+    uint64_t* aready;          // converters -> MMA: A and B of a slot written
+    uint64_t* mdone;           // MMA -> converters: slot's MMAs complete
+    unsigned long long* red;   // kMaxConsumerWarps x MP (LM head)
+    float* sx;                 // MP
+    volatile int* abort;
+    volatile int* flag;
+    uint32_t* tmem_base;
+
+    __device__ __forceinline__ explicit TcSmem(uint8_t* raw) {
+        uintptr_t base = (reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023);
+        uint8_t* p = reinterpret_cast<uint8_t*>(base);
+        stages = p;
+        p += C::Stages * C::StageBytes;
+        bring = p;
+        p += kTcRing * C::BSlot;
+        stg = reinterpret_cast<int32_t*>(p);
+        p += C::StgWords * 4;
+        full = reinterpret_cast<uint64_t*>(p);
+        p += C::Stages * 8;
+        empty = reinterpret_cast<uint64_t*>(p);
+        p += C::Stages * 8;
+        aready = reinterpret_cast<uint64_t*>(p);
+        p += kTcRing * 8;
+        mdone = reinterpret_cast<uint64_t*>(p);
+        p += kTcRing * 8;
+        red = reinterpret_cast<unsigned long long*>(p);
+        p += kMaxConsumerWarps * MP * 8;
+        sx = reinterpret_cast<float*>(p);
+        p += MP * 4;
+        abort = reinterpret_cast<volatile int*>(p);
+        flag = reinterpret_cast<volatile int*>(p + 4);
+        tmem_base = reinterpret_cast<uint32_t*>(p + 8);
+    }
+    __device__ __forceinline__ uint8_t* w_tile(int s) { return stages + s * C::StageBytes; }
+    __device__ __forceinline__ uint8_t* x_tile(int s) { return stages + s * C::StageBytes + kWTileBytes; }
+    __device__ __forceinline__ uint8_t* b_slot(int j) { return bring + j * C::BSlot; }
+};
+
+// Wait for an mbarrier phase for at most kWaitLimitNs, whatever the abort
+// flag says (used before releasing tensor memory an MMA may still write).
+__device__ __forceinline__ bool mbar_wait_timed(uint64_t* bar, unsigned parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = global_timer_ns();
+    while (!mbar_try_wait(bar, parity))
+        if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+    return true;
+}
+
+template <int MP, int EPI>
+__global__ void __launch_bounds__(kTcThreads, 1)
+w8a8_tc_kernel(const __grid_constant__ CUtensorMap tmap_w,
+               const __grid_constant__ CUtensorMap tmap_x, const W8A8Params p) {
+    using C = TcCfg<MP>;
+    constexpr int NM = C::NM, MPH = C::MPH, Stages = C::Stages, R = kTcRing;
+    extern __shared__ uint8_t smem_raw[];
+    TcSmem<MP> sm(smem_raw);
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const long long G = gridDim.x;
+    const int a = (int)((long long)blockIdx.x * p.T / G);
+    const int b = (int)((long long)(blockIdx.x + 1) * p.T / G);
+    const int n = b - a;
+
+    if (tid == 0) {
+        for (int s = 0; s < Stages; ++s) {
+            mbar_init(&sm.full[s], 1);
+            mbar_init(&sm.empty[s], kTcConv);
+        }
+        for (int j = 0; j < R; ++j) {
+            mbar_init(&sm.aready[j], kTcConv);
+            mbar_init(&sm.mdone[j], 1);
+        }
+        *sm.abort = 0;
+        fence_barrier_init();
+    }
+    // Zero the activation operand slots once: rows MP..NM-1 (token padding of
+    // the MMA's N) are never written again and must hold finite values.
+    for (int e = tid; e < R * C::BSlot / 16; e += kTcThreads)
+        reinterpret_cast<uint4*>(sm.bring)[e] = make_uint4(0u, 0u, 0u, 0u);
+    fence_proxy_async_smem();
+    if (warp == kTcMmaWarp) {
+        tmem_alloc(sm.tmem_base, C::TmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *sm.tmem_base;
+    allow_dependent_launch();
+
+    if (warp == kTcProdWarp) {
+        if (lane == 0)
+            produce<Stages>(&g_tc_gemm_error, sm, &tmap_w, &tmap_x, a, b, p.KT, BKB,
+                            (unsigned)(kWTileBytes + C::XBytes));
+        return;
+    }
+
+    if (warp == kTcMmaWarp) {
+        // ---------------- MMA issue ----------------
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_f16_f32(128, NM);
+            for (int c = 0; c < n; ++c) {
+                const int j = c % R;
+                if (!mbar_wait_bounded(&sm.aready[j], (unsigned)(c / R) & 1u, sm.abort))
+                    atomicOr(&g_tc_gemm_error, kErrTcWait);
+                tc_fence_after();
+                const uint32_t a_t = tmem + (uint32_t)(j * kTcACols);
+                const uint32_t d_t = tmem + (uint32_t)(C::DCol0 + j * NM);
+                const uint32_t b_s = smem_u32(sm.b_slot(j));
+#pragma unroll
+                for (int t = 0; t < 8; ++t)
+                    umma_f16_ta(d_t, a_t + (uint32_t)(8 * t),
+                                sw128_kmajor_desc(b_s + (uint32_t)((t >> 2) * NM * 128 + 32 * (t & 3))),
+                                idesc, t > 0 ? 1u : 0u);
+                umma_commit(&sm.mdone[j]);
+            }
+            // Tensor memory stays allocated until the last MMA has completed.
+            if (n > 0 && !mbar_wait_timed(&sm.mdone[(n - 1) % R], (unsigned)((n - 1) / R) & 1u))
+                atomicOr(&g_tc_gemm_error, kErrTcWait);
+        }
+        __syncwarp();
+        named_bar_sync(2, (kTcConv + 1) * 32);
+        tc_fence_after();
+        tmem_dealloc(tmem, C::TmemCols);
+        return;
+    }
+
+    // ---------------- converters (warps 0..7) ----------------
+    const int qd = warp & 3;                 // TMEM lane quarter of this warp
+    const int h = warp >> 2;                 // K half (widening) and token half (readout)
+    const int row = 32 * qd + lane;          // output channel within the tile
+    const uint32_t lane_base = tmem + ((uint32_t)(32 * qd) << 16);
+    grid_dependency_wait();
+    if (tid < MP) sm.sx[tid] = tid < p.M ? p.sx[tid] : 0.f;
+    consumer_sync<kTcConv>();
+    const bool has_tokens = h * MPH < p.M;  // warp-uniform
+
+    int32_t acc[MPH];
+    int rd = 0;                              // next local tile whose accumulator is read
+    auto readout = [&](int r) {
+        const int jj = r % R;
+        if (!mbar_wait_bounded(&sm.mdone[jj], (unsigned)(r / R) & 1u, sm.abort))
+            atomicOr(&g_tc_gemm_error, kErrTcWait);
+        tc_fence_after();
+        if (has_tokens) {
+            uint32_t v[MPH];
+            tmem_ld<MPH>(lane_base + (uint32_t)(C::DCol0 + jj * NM + h * MPH), v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int m = 0; m < MPH; ++m) acc[m] += __float2int_rn(__uint_as_float(v[m]));
+        }
+    };
+
+    int i = a;
+    while (i < b) {
+        const int nt = i / p.KT;
+        const int seg_begin = i;
+        const int seg_end = min(b, (nt + 1) * p.KT);
+#pragma unroll
+        for (int m = 0; m < MPH; ++m) acc[m] = 0;
+
+        for (; i < seg_end; ++i) {
+            const int c = i - a;
+            const int s = c % Stages, j = c % R;
+            if (!mbar_wait_bounded(&sm.full[s], (unsigned)(c / Stages) & 1u, sm.abort))
+                atomicOr(&g_tc_gemm_error, kErrFullWait);
+            // Slot j is free once the MMAs of tile c - R have completed (their
+            // accumulator is read here too).
+            while (rd <= c - R) readout(rd++);
+
+            // A: this thread's 64 weight bytes -> 32 f16x2 words in its TMEM lane.
+            const uint8_t* wrow = sm.w_tile(s) + row * BKB;
+            uint32_t av[32];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const uint4 wv = *reinterpret_cast<const uint4*>(wrow + (((4 * h + u) ^ (row & 7)) << 4));
+                widen_i8x4_f16(wv.x, av[8 * u + 0], av[8 * u + 1]);
+                widen_i8x4_f16(wv.y, av[8 * u + 2], av[8 * u + 3]);
+                widen_i8x4_f16(wv.z, av[8 * u + 4], av[8 * u + 5]);
+                widen_i8x4_f16(wv.w, av[8 * u + 6], av[8 * u + 7]);
+            }
+            tmem_st_x32(lane_base + (uint32_t)(j * kTcACols + 32 * h), av);
+
+            // B: the MP x 128 activation codes -> f16, 128-byte swizzled K-major.
+            uint8_t* bs = sm.b_slot(j);
+            for (int e = tid; e < MP * 8; e += kTcConv * 32) {
+                const int xr = e >> 3, xc = e & 7;
+                const uint4 xv = *reinterpret_cast<const uint4*>(sm.x_tile(s) + xr * BKB + ((xc ^ (xr & 7)) << 4));
+                uint4 lo, hi;
+                widen_i8x4_f16(xv.x, lo.x, lo.y);
+                widen_i8x4_f16(xv.y, lo.z, lo.w);
+                widen_i8x4_f16(xv.z, hi.x, hi.y);
+                widen_i8x4_f16(xv.w, hi.z, hi.w);
+                uint8_t* brow = bs + (xc >> 2) * NM * 128 + xr * 128;
+                const int c0 = 2 * (xc & 3);
+                *reinterpret_cast<uint4*>(brow + ((c0 ^ (xr & 7)) << 4)) = lo;
+                *reinterpret_cast<uint4*>(brow + (((c0 + 1) ^ (xr & 7)) << 4)) = hi;
+            }
+            tmem_st_wait();
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&sm.empty[s]);
+                mbar_arrive(&sm.aready[j]);
+            }
+        }
+        // Segment end: read the remaining accumulators of this channel tile.
+        while (rd < i - a) readout(rd++);
+
+        if (has_tokens) {
+#pragma unroll
+            for (int m = 0; m < MPH; ++m) {
+                const int tok = h * MPH + m;
+                if (tok < MP) sm.stg[row * MP + tok] = acc[m];
+            }
+        }
+        consumer_sync<kTcConv>();
+        stream_epilogue<MP, kTcConv, EPI>(sm, p, nt, seg_end - seg_begin, tid);
+    }
+    tc_fence_before();
+    named_bar_sync(2, (kTcConv + 1) * 32);
+}
+
+template <class P, class... Args>
+cudaError_t launch_tc(void (*kern)(Args...), int grid, int smem, cudaStream_t s,
+                      const CUtensorMap& tw, const CUtensorMap& tx, const P& params) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kTcThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, tw, tx, params);
+}
+
+}  // namespace
+
+cudaError_t launch_w8a8_tc(const W8A8Launch& a, int num_sms, cudaStream_t s) {
+    const bool lm = a.epi == Epi::LmHead;
+    WsLayout L = ws_layout(a.MP, a.N, lm);
+    W8A8Params p;
+    p.M = a.M; p.N = a.N; p.K = a.K;
+    p.KT = ceil_div(a.K, BKB);
+    p.NT = ceil_div(a.N, BN);
+    p.T = (long long)p.KT * p.NT;
+    p.sx = a.sx; p.sw = a.sw; p.y = a.y; p.y_bf16 = a.y_bf16; p.acc_debug = a.acc_debug;
+    p.tokens = a.tokens; p.max_logit = a.max_logit;
+    uint8_t* ws = static_cast<uint8_t*>(a.ws);
+    p.ws_acc = reinterpret_cast<int32_t*>(ws + L.acc);
+    p.ws_cnt = reinterpret_cast<unsigned*>(ws + L.counters);
+    p.keys = reinterpret_cast<unsigned long long*>(ws + L.keys);
+    p.done = reinterpret_cast<unsigned*>(ws + L.done);
+    const int grid = (int)(p.T < num_sms ? p.T : num_sms);
+#define QV_TC_CASE(MPV)                                                                           \
+    case MPV:                                                                                     \
+        return lm ? launch_tc(w8a8_tc_kernel<MPV, (int)Epi::LmHead>, grid, TcCfg<MPV>::SmemBytes, \
+                              s, a.tmap_w, a.tmap_x, p)                                           \
+                  : launch_tc(w8a8_tc_kernel<MPV, (int)Epi::Linear>, grid, TcCfg<MPV>::SmemBytes, \
+                              s, a.tmap_w, a.tmap_x, p);
+    switch (a.MP) {
+        QV_TC_CASE(8)
+        QV_TC_CASE(16)
+        QV_TC_CASE(32)
+        QV_TC_CASE(64)
+        default: return cudaErrorInvalidValue;
+    }
+#undef QV_TC_CASE
+}
+
+cudaError_t read_and_clear_tc_gemm_error(unsigned* code) {
+    unsigned zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(code, g_tc_gemm_error, sizeof(unsigned));
+    if (e != cudaSuccess) return e;
+    return cudaMemcpyToSymbol(g_tc_gemm_error, &zero, sizeof(unsigned));
+}
+
+}  // namespace qv

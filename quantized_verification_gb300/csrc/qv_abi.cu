@@ -112,6 +112,18 @@ qv_status encode_2d(CUtensorMap* map, CUtensorMapDataType dt, size_t elem_bytes,
     return QV_OK;
 }
 
+// W8A8 streaming GEMM kernel by padded token count. Up to 16 tokens the
+// int8 mma.sync kernel keeps pace with HBM; from QV_TC_MIN_MP tokens the
+// tcgen05 kernel (exact f16 widening, TMEM accumulators) is used, whose
+// per-tile cost hardly grows with the token count (measured on GB300).
+#ifndef QV_TC_MIN_MP
+#define QV_TC_MIN_MP 32
+#endif
+cudaError_t launch_w8a8(const qv::W8A8Launch& L, int sms, cudaStream_t s) {
+    if (L.MP >= QV_TC_MIN_MP) return qv::launch_w8a8_tc(L, sms, s);
+    return qv::launch_w8a8_stream(L, sms, s);
+}
+
 // Padded token count of one streaming-GEMM launch for Mc rows: 8, 16, 32 or 64.
 int mp_for(int mc) {
     const int p = qv::pad_tokens(mc);
@@ -243,7 +255,7 @@ qv_status qv_w8a8_linear(const int8_t* xq, const float* sx, int M, int K, const 
         L.tokens = nullptr; L.max_logit = nullptr;
         L.ws = workspace;
         L.epi = qv::Epi::Linear;
-        e = qv::launch_w8a8_stream(L, sms, stream);
+        e = launch_w8a8(L, sms, stream);
         if (e != cudaSuccess) return cuda_fail(e, "qv_w8a8_linear launch");
     }
     return ok();
@@ -278,7 +290,7 @@ qv_status qv_lm_head_argmax(const int8_t* xq, const float* sx, int M, int K, con
         L.max_logit = max_logit ? max_logit + m0 : nullptr;
         L.ws = workspace;
         L.epi = qv::Epi::LmHead;
-        e = qv::launch_w8a8_stream(L, sms, stream);
+        e = launch_w8a8(L, sms, stream);
         if (e != cudaSuccess) return cuda_fail(e, "qv_lm_head_argmax launch");
     }
     return ok();
@@ -441,8 +453,11 @@ qv_status qv_device_error(unsigned int* code) {
     if (!code) return fail(QV_ERR_INVALID_ARG, "code is null");
     cudaError_t e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+    unsigned tc = 0;
     e = qv::read_and_clear_stream_gemm_error(code);
+    if (e == cudaSuccess) e = qv::read_and_clear_tc_gemm_error(&tc);
     if (e != cudaSuccess) return cuda_fail(e, "reading the device error word");
+    *code |= tc;
     return ok();
 }
 

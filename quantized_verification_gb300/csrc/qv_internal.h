@@ -91,6 +91,17 @@ size_t stack_ws_bytes(int mp, int M, int n_max, int kmax);
 size_t stack_xq_offset(int mp, int n_max);
 
 cudaError_t launch_w8a8_stream(const W8A8Launch& a, int num_sms, cudaStream_t s);
+cudaError_t launch_w8a8_tc(const W8A8Launch& a, int num_sms, cudaStream_t s);
+
+// Largest dynamic shared memory of one CTA on sm_103a (227 KB).
+constexpr size_t kMaxDynSmem = 232448;
+// W8A8 with the activation quantization fused in (x fp32 or bf16 [M][K] and
+// optional multipliers instead of codes; a.sx and a.tmap_x unused). Only for
+// MP <= 16; w8a8_act_smem returns the launch's shared memory, 0 when the
+// shape does not fit (the caller then quantizes separately).
+size_t w8a8_act_smem(int MP, int K, int N, int num_sms);
+cudaError_t launch_w8a8_act(const W8A8Launch& a, const void* x, bool x_bf16, const float* act_mul,
+                            int num_sms, cudaStream_t s);
 cudaError_t launch_verify_stack(const StackLaunch& a, int num_sms, cudaStream_t s);
 cudaError_t launch_bf16_stream(const Bf16Launch& a, int num_sms, cudaStream_t s);
 cudaError_t launch_quantize_rows(const void* x, bool bf16, int rows, int K,
@@ -99,5 +110,6 @@ cudaError_t launch_quantize_rows(const void* x, bool bf16, int rows, int K,
 cudaError_t launch_accept(const int32_t* t, const int32_t* d, int B, int gamma,
                           int32_t* len, int32_t* out, cudaStream_t s);
 cudaError_t read_and_clear_stream_gemm_error(unsigned* code);
+cudaError_t read_and_clear_tc_gemm_error(unsigned* code);
 
 }  // namespace qv

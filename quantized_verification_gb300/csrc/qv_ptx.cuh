@@ -1,6 +1,7 @@
 // qv_ptx.cuh -- inline-PTX building blocks for the sm_103a kernels of libqv:
-// mbarriers with bounded waits, 2-D TMA loads, ldmatrix, f16 mma.sync,
-// programmatic-dependent-launch controls and the exact int8 -> f16 widening.
+// mbarriers with bounded waits, 2-D TMA loads, ldmatrix, f16 mma.sync, the
+// tcgen05 tensor-memory and MMA instructions, programmatic-dependent-launch
+// controls and the exact int8 -> f16 widening.
 #pragma once
 
 #include <cstdint>
@@ -18,6 +19,7 @@ constexpr unsigned kErrFullWait = 1u;    // consumer waited too long for a stage
 constexpr unsigned kErrEmptyWait = 2u;   // producer waited too long for a slot
 constexpr unsigned kErrDrainWait = 4u;   // copies still in flight at exit
 constexpr unsigned kErrGridWait = 8u;    // a CTA waited too long at a grid barrier
+constexpr unsigned kErrTcWait = 16u;     // tensor-core pipeline wait (operands / MMA completion)
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -197,6 +199,143 @@ __device__ __forceinline__ void widen_i8x4_f16(uint32_t w, uint32_t& lo, uint32_
     hi = __byte_perm(u, 0x64646464u, 0x4342);
     asm("sub.f16x2 %0, %0, %1;" : "+r"(lo) : "r"(0x64806480u));
     asm("sub.f16x2 %0, %0, %1;" : "+r"(hi) : "r"(0x64806480u));
+}
+
+// ---------------------------------------------------------------- quantization
+// q = clamp(rne(fl32(x / s)), -127, 127) (0 when s == 0), decided from t = fl32(x * r)
+// with r = fl32(1 / s) when t is far from every half-integer, else from the
+// IEEE quotient. Error bound: r = (1/s)(1+d1), t = (x/s)(1+d1)(1+d2) and
+// fl32(x/s) = (x/s)(1+d3) with |di| <= 2^-24, so |t - fl32(x/s)| < 2^-22 |t|.
+// If the distance from t to the nearest half-integer exceeds 2^-20 |t|, both
+// lie strictly on the same side of it and round to the same integer.
+__device__ __forceinline__ int quant_code(float x, float s, float r) {
+    if (s == 0.f) return 0;
+    const float t = __fmul_rn(x, r);
+    float q = rintf(t);
+    const float margin = __fsub_rn(0.5f, fabsf(__fsub_rn(t, q)));
+    if (!(margin > __fmul_rn(fabsf(t), 0x1p-20f))) q = rintf(__fdiv_rn(x, s));
+    const int qi = __float2int_rn(q);
+    return qi > 127 ? 127 : (qi < -127 ? -127 : qi);
+}
+
+// ---------------------------------------------------------------- tcgen05
+// Tensor memory (TMEM): 128 lanes x 512 columns of 32-bit cells per SM. An
+// address is (lane << 16) | column; a warp reaches only the 32 lanes
+// 32 * (warp id % 4) .. +31.
+
+// Allocate `ncols` columns (a power of two >= 32); the whole warp executes it
+// and the base address is written to shared memory.
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                 :: "r"(smem_u32(dst)), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" :: "r"(taddr), "r"(ncols) : "memory");
+}
+// Order tcgen05 operations before / after a thread synchronisation.
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// Make this thread's generic shared-memory writes visible to the async proxy
+// (the tensor core reading an operand from shared memory).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor of a K-major operand stored as rows of 128
+// bytes with the 128-byte swizzle (16-byte chunk c of row r at position
+// c ^ (r % 8)), 8-row groups 1024 bytes apart; `saddr` is the group-aligned
+// start plus the byte offset of the K step inside the 128-byte row.
+__device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);      // start address / 16
+    d |= (uint64_t)1u << 16;                      // leading byte offset (unused with this swizzle)
+    d |= (uint64_t)(1024u >> 4) << 32;            // stride byte offset: 8 rows x 128 bytes
+    d |= (uint64_t)1u << 46;                      // descriptor version for tcgen05
+    d |= (uint64_t)2u << 61;                      // 128-byte swizzle
+    return d;
+}
+
+// Instruction descriptor of kind::f16 with f16 A and B (both K-major) and an
+// f32 accumulator, for an M x N tile.
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
+    return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// D[tmem] (+)= A[tmem] * B[smem]^T, one K = 16 step, issued by one thread.
+__device__ __forceinline__ void umma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+                 :: "r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
+}
+// Arrive once on `bar` when every tcgen05.mma issued so far by this thread has completed.
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                 :: "r"(smem_u32(bar)) : "memory");
+}
+
+// Store 32 consecutive columns of this thread's lane.
+__device__ __forceinline__ void tmem_st_x32(uint32_t taddr, const uint32_t (&v)[32]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+                 "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+                 "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};"
+                 :: "r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]),
+                    "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]),
+                    "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]),
+                    "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]),
+                    "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// Load NC consecutive columns of this thread's lane (NC = 8, 16 or 32).
+template <int NC>
+__device__ __forceinline__ void tmem_ld(uint32_t taddr, uint32_t (&v)[NC]);
+template <>
+__device__ __forceinline__ void tmem_ld<8>(uint32_t taddr, uint32_t (&v)[8]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]),
+                   "=r"(v[6]), "=r"(v[7])
+                 : "r"(taddr) : "memory");
+}
+template <>
+__device__ __forceinline__ void tmem_ld<16>(uint32_t taddr, uint32_t (&v)[16]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,"
+                 "%11,%12,%13,%14,%15}, [%16];"
+                 : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]),
+                   "=r"(v[6]), "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]),
+                   "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+                 : "r"(taddr) : "memory");
+}
+template <>
+__device__ __forceinline__ void tmem_ld<32>(uint32_t taddr, uint32_t (&v)[32]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,"
+                 "%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,"
+                 "%30,%31}, [%32];"
+                 : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]),
+                   "=r"(v[6]), "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]),
+                   "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]),
+                   "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]),
+                   "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]),
+                   "=r"(v[30]), "=r"(v[31])
+                 : "r"(taddr) : "memory");
+}
+__device__ __forceinline__ void tmem_ld_wait() {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Named barrier over `nthreads` threads (a multiple of 32).
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+    asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(nthreads) : "memory");
 }
 
 }  // namespace qv

@@ -112,21 +112,23 @@ def test_w8a8_linear(qv, oracle, M, K, N):
     assert np.array_equal(bf16_bits(yb), oracle.f32_to_bf16(y_ref))
 
 
+@pytest.mark.parametrize("M", [3, 40])
 @pytest.mark.parametrize("K,with_m128", [((133144 // 16) * 16, False), (4096, True)])
-def test_w8a8_extreme_magnitudes(qv, oracle, K, with_m128):
+def test_w8a8_extreme_magnitudes(qv, oracle, M, K, with_m128):
     """Codes at the ends of the range. The first case is the largest K that is
     a multiple of 16 and keeps every +-127 sum inside int32; -128 codes are
-    exercised at a K where their sums fit as well."""
-    M, N = 3, 130
+    exercised at a K where their sums fit as well. M = 3 runs the int8
+    mma.sync kernel, M = 40 the tcgen05 kernel (rows 3.. repeat rows 0..2)."""
+    N = 130
     xq = torch.full((M, K), 127, dtype=torch.int8)
-    xq[1] = -127
+    xq[1::3] = -127
     wq = torch.full((N, K), 127, dtype=torch.int8)
     wq[1::3] = -127
     if with_m128:
-        xq[2, ::2] = -128
+        xq[2::3, ::2] = -128
         wq[2::3, 1::2] = -128
     else:
-        xq[2, ::2] = -127
+        xq[2::3, ::2] = -127
         wq[2::3, 1::2] = -127
     sx = torch.full((M,), 1e-3)
     sw = torch.full((N,), 1e-4)
