@@ -278,31 +278,35 @@ def main():
     t_ver = stack.tokens.view(stack.B, stack.gamma + 1).cpu()
     stack.drafts.copy_(synth.geometric_drafts(t_ver, stack.V, 0.7, seed=99 + rank))
     per_op_graph = stack.capture()
+    two_call_graph = stack.capture_two_call()
     fused_graph = stack.capture_fused()
     log(f"setup {time.time() - t_setup:.1f} s; weight bytes/step {stack.weight_bytes() / 1e9:.3f} GB")
     stream = torch.cuda.current_stream()
 
-    # the per-op path (act quant + W8A8 linear per phase, LM head argmax, accept)
-    for _ in range(3):
-        per_op_graph.replay()
-    per_op_ms = time_graph(torch, per_op_graph, max(20, args.steps // 5), stream)
-    ref_tok, ref_len = stack.tokens.clone(), stack.accept_len.clone()
-    log(f"per-op path {per_op_ms:.4f} ms/step")
-    # the fused path: qv_verify_stack, one persistent launch per step
-    for _ in range(3):
-        fused_graph.replay()
-    torch.cuda.synchronize()
-    assert torch.equal(stack.tokens, ref_tok) and torch.equal(stack.accept_len, ref_len), \
-        "fused and per-op steps disagree"
-    fused_ms = time_graph(torch, fused_graph, max(20, args.steps // 5), stream)
-    log(f"fused path {fused_ms:.4f} ms/step")
-    if fused_ms <= per_op_ms:
-        step_graph, launches = fused_graph, stack.launches_per_step(fused=True)
-        path = "qv_verify_stack: one persistent cooperative launch per step"
-    else:
-        step_graph, launches = per_op_graph, stack.launches_per_step()
-        path = "per-op ABI calls (act quant + W8A8 linear per phase, LM head argmax, accept) in one CUDA graph"
-
+    # three public-API paths of the same step; all must give the same tokens
+    paths = [
+        ("per_op", per_op_graph, stack.launches_per_step(),
+         "per-op ABI calls (qv_w8a8_linear_act per projection, qv_lm_head_argmax_act, qv_accept) in one CUDA graph"),
+        ("two_call", two_call_graph, stack.launches_per_step_two_call(),
+         "per-op ABI calls (qv_quantize_act + qv_w8a8_linear per projection, qv_quantize_act + "
+         "qv_lm_head_argmax, qv_accept) in one CUDA graph"),
+        ("verify_stack", fused_graph, stack.launches_per_step(fused=True),
+         "qv_verify_stack: one persistent cooperative launch per step"),
+    ]
+    paths_ms = {}
+    ref_tok = ref_len = None
+    for name, g, _, _ in paths:
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        if ref_tok is None:
+            ref_tok, ref_len = stack.tokens.clone(), stack.accept_len.clone()
+        assert torch.equal(stack.tokens, ref_tok) and torch.equal(stack.accept_len, ref_len), \
+            f"{name} step disagrees with {paths[0][0]}"
+        paths_ms[name] = time_graph(torch, g, max(20, args.steps // 5), stream)
+        log(f"{name} path {paths_ms[name]:.4f} ms/step")
+    best = min(paths, key=lambda t: paths_ms[t[0]])
+    path_name, step_graph, launches, path = best
     for _ in range(max(args.warmup, 3)):
         step_graph.replay()
     torch.cuda.synchronize()
@@ -329,25 +333,31 @@ def main():
     assert qv.qv_device_error() == 0, "a kernel hit its wait limit"
     peak, peak_kind = read_peaks()
 
-    # ---- dominant kernel: qv_w8a8_linear on the step's 144 projections, back
-    # to back in one graph (PDL between launches), activations pre-quantized
+    # ---- dominant kernel: the W8A8 GEMM of the chosen per-op path on the
+    # step's 144 projections, back to back in one graph (PDL between launches)
     M = stack.M
-    lin_bytes = stack.linear_launch_bytes()
+    fused_act = path_name != "two_call"
+    lin_bytes = stack.linear_launch_bytes(fused_act=fused_act)
     xqs = []
-    for l in range(stack.layers):
-        for p, (name, K, N) in enumerate(stack.phases):
-            xq = torch.empty(M, K, dtype=torch.int8, device=dev)
-            sxp = torch.empty(M, device=dev)
-            qv.qv_quantize_act(stack.inputs[l][p], xq, sxp)
-            xqs.append((xq, sxp))
-    torch.cuda.synchronize()
+    if not fused_act:
+        for l in range(stack.layers):
+            for p, (name, K, N) in enumerate(stack.phases):
+                xq = torch.empty(M, K, dtype=torch.int8, device=dev)
+                sxp = torch.empty(M, device=dev)
+                qv.qv_quantize_act(stack.inputs[l][p], xq, sxp)
+                xqs.append((xq, sxp))
+        torch.cuda.synchronize()
 
     def lin_seq(s):
         j = 0
         for l in range(stack.layers):
             for p, (name, K, N) in enumerate(stack.phases):
                 wq, sw = stack.weights[l][p]
-                qv.qv_w8a8_linear(xqs[j][0], xqs[j][1], wq, sw, stack.y[: M * N].view(M, N), stack.ws, stream=s)
+                yv = stack.y[: M * N].view(M, N)
+                if fused_act:
+                    qv.qv_w8a8_linear_act(stack.inputs[l][p], wq, sw, yv, stack.ws_act, stream=s)
+                else:
+                    qv.qv_w8a8_linear(xqs[j][0], xqs[j][1], wq, sw, yv, stack.ws, stream=s)
                 j += 1
     gl = VerifyStack._capture(lin_seq, dev)
     lin_ms = time_graph(torch, gl, args.kernel_reps, stream)
@@ -355,7 +365,12 @@ def main():
     traffic = None
     if NCU_TRAFFIC["source_sha256"] == kernel_source_sha() and NCU_TRAFFIC["dram_bytes_per_algorithmic_byte"]:
         traffic = NCU_TRAFFIC["dram_bytes_per_algorithmic_byte"] * sum(lin_bytes) / len(lin_bytes)
-    linear_kernel = {"kernel": "w8a8_stream_kernel (qv_w8a8_linear)", "achieved": achieved,
+    if fused_act:
+        kname = ("w8a8_stream_kernel, activation quantization fused (qv_w8a8_linear_act)" if M <= 16
+                 else "quantize_rows_kernel + W8A8 GEMM (qv_w8a8_linear_act, codes materialised)")
+    else:
+        kname = "W8A8 GEMM on pre-quantized codes (qv_w8a8_linear)"
+    linear_kernel = {"kernel": kname, "achieved": achieved,
                      "frac": achieved / peak, "bytes_per_launch": sum(lin_bytes) / len(lin_bytes),
                      "launch_ms_mean": lin_ms / len(lin_bytes),
                      "timing": "144 launches of the step's projections back to back in one CUDA graph"}
@@ -371,7 +386,7 @@ def main():
                     "peak_source": f"{peak_kind} hbm_gbs (copy, burst)"}
     else:
         roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                    "traffic": traffic, "kernel": "w8a8_stream_kernel (qv_w8a8_linear)",
+                    "traffic": traffic, "kernel": kname,
                     "bytes_per_launch": sum(lin_bytes) / len(lin_bytes),
                     "launch_ms_mean": lin_ms / len(lin_bytes),
                     "timing": "144 launches of the step's projections back to back in one CUDA graph, "
@@ -440,7 +455,7 @@ def main():
             "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"],
                        "samples": clk["samples"]},
             "comparator": comparator,
-            "paths_ms_per_step": {"per_op": per_op_ms, "verify_stack": fused_ms},
+            "paths_ms_per_step": paths_ms,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

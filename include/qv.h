@@ -69,7 +69,9 @@ typedef enum {
     QV_OP_LINEAR = 0,         /* qv_w8a8_linear                            */
     QV_OP_LM_HEAD = 1,        /* qv_lm_head_argmax (N = vocabulary size V) */
     QV_OP_BF16_LINEAR = 2,    /* qv_bf16_linear                            */
-    QV_OP_VERIFY_STACK = 3    /* qv_verify_stack (K, N = largest K, N / V) */
+    QV_OP_VERIFY_STACK = 3,   /* qv_verify_stack (K, N = largest K, N / V) */
+    QV_OP_LINEAR_ACT = 4,     /* qv_w8a8_linear_act                        */
+    QV_OP_LM_HEAD_ACT = 5     /* qv_lm_head_argmax_act (N = V)             */
 } qv_op;
 
 /* floor((2^31 - 1) / 127^2): the int32 accumulation stays exact up to here. */
@@ -162,6 +164,45 @@ QV_API qv_status qv_lm_head_argmax(const int8_t* xq, const float* sx, int M, int
                             int32_t* tokens, float* max_logit,
                             void* workspace, size_t workspace_bytes,
                             cudaStream_t stream);
+
+/*
+ * qv_w8a8_linear_act -- a1 + a2 in one call: per-token quantization of the
+ * activations (qv_quantize_act) followed by the W8A8 linear (qv_w8a8_linear),
+ * with the same arithmetic, so y is bit-identical to the two calls.
+ *
+ *   Quasar, gist.science/ja summary, section 2.2 items 2-3: BF16
+ *   activations scaled by the smoothing factor, converted to INT8 online,
+ *   INT8 GEMM with INT32 accumulation, dequantized to high precision.
+ *
+ *   x [M*K] fp32 or bf16 (x_dtype), 16-byte aligned; act_mul [K] fp32 or
+ *   NULL, 16-byte aligned; wq, sw, y, y_dtype as qv_w8a8_linear.
+ *   workspace: qv_workspace_bytes(QV_OP_LINEAR_ACT, M, K, N) bytes,
+ *   16-byte aligned, ZERO-FILLED before its first use, with the same
+ *   reuse contract as qv_w8a8_linear (its first part is that call's
+ *   workspace; the rest holds the codes when they are materialised).
+ *   1 <= M <= QV_MAX_M, N >= 1. With M <= 16 and a K range per CTA whose
+ *   codes fit in shared memory, one kernel does both steps: every CTA
+ *   computes the per-token scales and quantizes only the slice of x its
+ *   weight tiles need, so the codes never reach HBM. Otherwise the codes are
+ *   written to the workspace by qv_quantize_act's kernel first.
+ */
+QV_API qv_status qv_w8a8_linear_act(const void* x, qv_dtype x_dtype, const float* act_mul,
+                                    int M, int K, const int8_t* wq, const float* sw, int N,
+                                    void* y, qv_dtype y_dtype,
+                                    void* workspace, size_t workspace_bytes,
+                                    cudaStream_t stream);
+
+/*
+ * qv_lm_head_argmax_act -- a1 + a3 in one call: qv_quantize_act of the
+ * final hidden state followed by qv_lm_head_argmax, bit-identical to the two
+ * calls (same fusion rule and workspace contract as qv_w8a8_linear_act,
+ * workspace qv_workspace_bytes(QV_OP_LM_HEAD_ACT, M, K, V)).
+ */
+QV_API qv_status qv_lm_head_argmax_act(const void* x, qv_dtype x_dtype, const float* act_mul,
+                                       int M, int K, const int8_t* wq, const float* sw, int V,
+                                       int32_t* tokens, float* max_logit,
+                                       void* workspace, size_t workspace_bytes,
+                                       cudaStream_t stream);
 
 /*
  * qv_accept -- a4: greedy acceptance of the longest matching draft prefix

@@ -94,7 +94,10 @@ struct Cfg {
     // the codes live in a per-CTA buffer after the carve-up below.
     static constexpr int XSlot = TMAX ? ((XBytes + 1023) / 1024) * 1024 : 0;
     static constexpr int StageBytes = kWTileBytes + XSlot;
-    static constexpr int Stages = !TMAX ? 6 : NG == 1 ? 6 : NG == 2 ? 6 : NG == 4 ? 5 : 4;
+    // Seven stages for up to 16 tokens also make a CTA need more than half of
+    // an SM's shared memory, so no SM ever holds two CTAs of one launch (two
+    // would share the SM's bandwidth and finish last).
+    static constexpr int Stages = !TMAX ? 6 : NG == 1 ? 7 : NG == 2 ? 7 : NG == 4 ? 5 : 4;
     static constexpr int StgWords = BN * MP;                 // epilogue staging
     static constexpr int SmemBytes =
         1024 /*alignment slack*/ + Stages * StageBytes + StgWords * 4 +
@@ -278,73 +281,164 @@ struct ActParams {
     int xc_slots;             // K-tiles of codes the shared buffer holds (>= min(tiles per CTA, KT))
 };
 
-// 16 elements of row `row` from column k0 as binary32, times the multipliers.
+// Raw 16-byte vectors of the 16 elements of row `row` from column k0 (2 for
+// bf16, 4 for fp32) and the 4 float4 of their multipliers.
 template <bool BF16>
-__device__ __forceinline__ void load16_scaled(const void* x, const float* mul, int K, int row, int k0,
-                                              float (&e)[16]) {
-    if (BF16) {
-        const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(x) + (size_t)row * K + k0);
-        const uint4 v0 = __ldg(src), v1 = __ldg(src + 1);
-        const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+__device__ __forceinline__ void load_chunk16(const void* x, int K, int row, int k0, uint4 (&r)[BF16 ? 2 : 4]) {
+    const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(x) +
+                                                      ((size_t)row * K + k0) * (BF16 ? 2 : 4));
+#pragma unroll
+    for (int j = 0; j < (BF16 ? 2 : 4); ++j) r[j] = __ldg(src + j);
+}
+template <bool BF16>
+__device__ __forceinline__ void unpack_chunk16(const uint4 (&r)[BF16 ? 2 : 4], float (&e)[16]) {
+    if constexpr (BF16) {
+        const uint32_t w[8] = {r[0].x, r[0].y, r[0].z, r[0].w, r[1].x, r[1].y, r[1].z, r[1].w};
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             e[2 * j] = __uint_as_float(w[j] << 16);
             e[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
         }
     } else {
-        const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(x) + (size_t)row * K + k0);
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            const float4 v = __ldg(src + j);
-            e[4 * j] = v.x; e[4 * j + 1] = v.y; e[4 * j + 2] = v.z; e[4 * j + 3] = v.w;
+            e[4 * j] = __uint_as_float(r[j].x); e[4 * j + 1] = __uint_as_float(r[j].y);
+            e[4 * j + 2] = __uint_as_float(r[j].z); e[4 * j + 3] = __uint_as_float(r[j].w);
         }
     }
-    if (mul) {
-        const float4* m4 = reinterpret_cast<const float4*>(mul + k0);
+}
+__device__ __forceinline__ void scale_chunk16(float (&e)[16], const float4 (&c)[4]) {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const float4 c = __ldg(m4 + j);
-            e[4 * j] = __fmul_rn(e[4 * j], c.x);
-            e[4 * j + 1] = __fmul_rn(e[4 * j + 1], c.y);
-            e[4 * j + 2] = __fmul_rn(e[4 * j + 2], c.z);
-            e[4 * j + 3] = __fmul_rn(e[4 * j + 3], c.w);
+    for (int j = 0; j < 4; ++j) {
+        e[4 * j] = __fmul_rn(e[4 * j], c[j].x);
+        e[4 * j + 1] = __fmul_rn(e[4 * j + 1], c[j].y);
+        e[4 * j + 2] = __fmul_rn(e[4 * j + 2], c[j].z);
+        e[4 * j + 3] = __fmul_rn(e[4 * j + 3], c[j].w);
+    }
+}
+
+// Per-token amax of x' over chunks [c0 + u * CT] (u < U) into the per-thread
+// running maxima amax[MP]; all U chunks' loads are issued before any is used.
+template <int MP, int CT, bool BF16, int U, bool MUL>
+__device__ __forceinline__ void amax_batch(const W8A8Params& p, const ActParams& q, int c0, int cpr,
+                                           int total, float (&amax)[MP]) {
+    constexpr int V = BF16 ? 2 : 4;
+    uint4 r[U][V];
+    float4 c[MUL ? U : 1][4];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        const int ci = c0 + u * CT;
+        if (ci < total) {
+            const int row = ci / cpr, k0 = (ci - row * cpr) * 16;
+            load_chunk16<BF16>(q.x, p.K, row, k0, r[u]);
+            if (MUL) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) c[MUL ? u : 0][j] = __ldg(reinterpret_cast<const float4*>(q.act_mul + k0) + j);
+            }
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        const int ci = c0 + u * CT;
+        if (ci < total) {
+            const int row = ci / cpr;
+            float e[16];
+            unpack_chunk16<BF16>(r[u], e);
+            if (MUL) scale_chunk16(e, c[MUL ? u : 0]);
+            float mx = 0.f;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) mx = fmaxf(mx, fabsf(e[j]));
+#pragma unroll
+            for (int m = 0; m < MP; ++m) amax[m] = row == m ? fmaxf(amax[m], mx) : amax[m];
+        }
+    }
+}
+
+// Codes of items [i0 + u * CT] (u < U); item = (slot j, row m < M, 16-byte
+// chunk ch) of the CTA's K-tiles kt0, kt0+1, ... (mod KT).
+template <int MP, int CT, bool BF16, int U, bool MUL>
+__device__ __forceinline__ void codes_batch(const W8A8Params& p, const ActParams& q, const float* sxs,
+                                            const float* rcp, uint8_t* xc, int kt0, int i0, int items) {
+    constexpr int V = BF16 ? 2 : 4;
+    const int per_slot = p.M * 8;
+    uint4 r[U][V];
+    float4 c[MUL ? U : 1][4];
+    int kk[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        const int it = i0 + u * CT;
+        kk[u] = -1;
+        if (it < items) {
+            const int j = it / per_slot, rem = it - j * per_slot;
+            const int row = rem >> 3, ch = rem & 7;
+            int kt = kt0 + j;
+            if (kt >= p.KT) kt -= p.KT;
+            const int k0 = kt * BKB + ch * 16;
+            if (k0 < p.K) {
+                kk[u] = k0;
+                load_chunk16<BF16>(q.x, p.K, row, k0, r[u]);
+                if (MUL) {
+#pragma unroll
+                    for (int t = 0; t < 4; ++t) c[MUL ? u : 0][t] = __ldg(reinterpret_cast<const float4*>(q.act_mul + k0) + t);
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        const int it = i0 + u * CT;
+        if (it < items && kk[u] >= 0) {
+            const int j = it / per_slot, rem = it - j * per_slot;
+            const int row = rem >> 3, ch = rem & 7;
+            float e[16];
+            unpack_chunk16<BF16>(r[u], e);
+            if (MUL) scale_chunk16(e, c[MUL ? u : 0]);
+            const float sc = sxs[row], rc = rcp[row];
+            uint32_t w[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+            for (int t = 0; t < 16; ++t)
+                w[t >> 2] |= (uint32_t)(uint8_t)(int8_t)quant_code(e[t], sc, rc) << (8 * (t & 3));
+            *reinterpret_cast<uint4*>(xc + (size_t)j * MP * BKB + row * BKB + ((ch ^ (row & 7)) << 4)) =
+                make_uint4(w[0], w[1], w[2], w[3]);
         }
     }
 }
 
 // Consumers of an XMODE 1/2 launch: per-token scales into sm_sx (and
 // reciprocals into s_rcp), then the codes of K-tiles kt0, kt0+1, ... (mod KT),
-// nslot of them, into xc (slot j = MP rows x 128 bytes, 128-byte swizzle).
+// nslot of them, into xc (slot j = MP rows x 128 bytes, 128-byte swizzle;
+// padding rows and a ragged K tail are zero). Loads are issued in batches of
+// 4-16 chunks per thread so that each pass costs about one memory round trip.
 template <int MP, int CW, bool BF16>
 __device__ __forceinline__ void act_prologue(const W8A8Params& p, const ActParams& q, float* sm_sx,
                                              unsigned* s_amax, float* s_rcp, uint8_t* xc, int kt0,
                                              int nslot, int tid) {
     constexpr int CT = CW * 32;
+    constexpr int UA = BF16 ? 8 : 4;       // chunks per thread per amax batch
+    constexpr int UC = BF16 ? 8 : 4;       // items per thread per code batch
     if (tid < MP) s_amax[tid] = 0u;
+    for (int e = tid; e < nslot * MP * 8; e += CT)
+        reinterpret_cast<uint4*>(xc)[e] = make_uint4(0u, 0u, 0u, 0u);
     consumer_sync<CW>();
-    // amax over 16-element chunks: chunk c of the row-major M x K matrix
     const int cpr = p.K / 16;
     const int total = p.M * cpr;
-    for (int base = tid; base < total; base += 4 * CT) {
-        float mx[4];
-        int rows[4];
+    float amax[MP];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int c = base + u * CT;
-            mx[u] = 0.f;
-            rows[u] = -1;
-            if (c < total) {
-                const int row = c / cpr;
-                float e[16];
-                load16_scaled<BF16>(q.x, q.act_mul, p.K, row, (c - row * cpr) * 16, e);
+    for (int m = 0; m < MP; ++m) amax[m] = 0.f;
+    if (q.act_mul) {
+        for (int c0 = tid; c0 < total; c0 += (UA / 2) * CT)
+            amax_batch<MP, CT, BF16, UA / 2, true>(p, q, c0, cpr, total, amax);
+    } else {
+        for (int c0 = tid; c0 < total; c0 += UA * CT)
+            amax_batch<MP, CT, BF16, UA, false>(p, q, c0, cpr, total, amax);
+    }
+    const int lane = tid & 31;
 #pragma unroll
-                for (int j = 0; j < 16; ++j) mx[u] = fmaxf(mx[u], fabsf(e[j]));
-                rows[u] = row;
-            }
-        }
+    for (int m = 0; m < MP; ++m) {
+        float v = amax[m];
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
-            if (rows[u] >= 0) atomicMax(&s_amax[rows[u]], __float_as_uint(mx[u]));
+        for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
+        if (lane == 0 && m < p.M) atomicMax(&s_amax[m], __float_as_uint(v));
     }
     consumer_sync<CW>();
     if (tid < MP) {
@@ -353,25 +447,13 @@ __device__ __forceinline__ void act_prologue(const W8A8Params& p, const ActParam
         s_rcp[tid] = __frcp_rn(sc);
     }
     consumer_sync<CW>();
-    const int items = nslot * MP * 8;
-    for (int it = tid; it < items; it += CT) {
-        const int j = it / (MP * 8);
-        const int rem = it - j * (MP * 8);
-        const int row = rem >> 3, ch = rem & 7;
-        int kt = kt0 + j;
-        if (kt >= p.KT) kt -= p.KT;
-        const int k0 = kt * BKB + ch * 16;
-        uint32_t w[4] = {0u, 0u, 0u, 0u};
-        if (row < p.M && k0 < p.K) {
-            float e[16];
-            load16_scaled<BF16>(q.x, q.act_mul, p.K, row, k0, e);
-            const float sc = sm_sx[row], rc = s_rcp[row];
-#pragma unroll
-            for (int jj = 0; jj < 16; ++jj)
-                w[jj >> 2] |= (uint32_t)(uint8_t)(int8_t)quant_code(e[jj], sc, rc) << (8 * (jj & 3));
-        }
-        *reinterpret_cast<uint4*>(xc + (size_t)j * MP * BKB + row * BKB + ((ch ^ (row & 7)) << 4)) =
-            make_uint4(w[0], w[1], w[2], w[3]);
+    const int items = nslot * p.M * 8;
+    if (q.act_mul) {
+        for (int i0 = tid; i0 < items; i0 += (UC / 2) * CT)
+            codes_batch<MP, CT, BF16, UC / 2, true>(p, q, sm_sx, s_rcp, xc, kt0, i0, items);
+    } else {
+        for (int i0 = tid; i0 < items; i0 += UC * CT)
+            codes_batch<MP, CT, BF16, UC, false>(p, q, sm_sx, s_rcp, xc, kt0, i0, items);
     }
     consumer_sync<CW>();
 }
@@ -433,6 +515,7 @@ w8a8_stream_kernel(const __grid_constant__ CUtensorMap tmap_w,
     const TileLanes<BPW> L(RW * warp, lane);
 
     int32_t acci[BPW][NG][4];
+    EpiState est;
     int s = 0, phase = 0;
     int slot = 0;                        // code slot of tile i (XMODE 1/2): (i - a) mod KT
     int i = a;
@@ -471,8 +554,9 @@ w8a8_stream_kernel(const __grid_constant__ CUtensorMap tmap_w,
         }
         consumer_sync<CW>();
 
-        stream_epilogue<MP, CW, EPI>(sm, p, nt, seg_end - seg_begin, tid);
+        segment_end<MP, CW, EPI>(sm, p, nt, seg_end - seg_begin, i >= b, tid, est);
     }
+    range_end<MP, CW, EPI>(sm, p, tid, est);
 }
 
 // ---------------------------------------------------------------------------
@@ -1320,7 +1404,9 @@ size_t w8a8_act_smem(int MP, int K, int N, int num_sms) {
     if (MP == 8) base = Cfg<1, false>::XcOffset;
     else if (MP == 16) base = Cfg<2, false>::XcOffset;
     else return 0;
-    const size_t total = 1024 + base + xc;
+    size_t total = 1024 + base + xc;
+    // at least half of an SM's shared memory plus one byte: one CTA per SM
+    if (total < kMinSmemOneCtaPerSm) total = kMinSmemOneCtaPerSm;
     return total <= kMaxDynSmem ? total : 0;
 }
 

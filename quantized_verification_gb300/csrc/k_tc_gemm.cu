@@ -224,6 +224,7 @@ w8a8_tc_kernel(const __grid_constant__ CUtensorMap tmap_w,
     const bool has_tokens = h * MPH < p.M;  // warp-uniform
 
     int32_t acc[MPH];
+    EpiState est;
     int rd = 0;                              // next local tile whose accumulator is read
     auto readout = [&](int r) {
         const int jj = r % R;
@@ -304,8 +305,9 @@ w8a8_tc_kernel(const __grid_constant__ CUtensorMap tmap_w,
             }
         }
         consumer_sync<kTcConv>();
-        stream_epilogue<MP, kTcConv, EPI>(sm, p, nt, seg_end - seg_begin, tid);
+        segment_end<MP, kTcConv, EPI>(sm, p, nt, seg_end - seg_begin, i >= b, tid, est);
     }
+    range_end<MP, kTcConv, EPI>(sm, p, tid, est);
     tc_fence_before();
     named_bar_sync(2, (kTcConv + 1) * 32);
 }

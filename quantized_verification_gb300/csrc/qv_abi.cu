@@ -157,6 +157,15 @@ qv_status check_gemm_common(const void* xq, const void* sx, int M, int K, const 
     return QV_OK;
 }
 
+size_t al16(size_t v) { return (v + 15) & ~size_t(15); }
+
+// Offset of the materialised codes in a *_ACT workspace: after the
+// streaming-GEMM part, 256-byte aligned.
+size_t act_codes_offset(bool lm, int M, int K, int N) {
+    const int mp = mp_for(M < qv::kMaxMPerLaunch ? M : qv::kMaxMPerLaunch);
+    return (qv::ws_layout(mp, N, lm).total + 255) & ~size_t(255);
+}
+
 }  // namespace
 
 namespace qv {
@@ -184,6 +193,11 @@ size_t qv_workspace_bytes(qv_op op, int M, int K, int N) {
         case QV_OP_VERIFY_STACK:
             if (M > qv::kMaxStackM) return 0;
             return qv::stack_ws_bytes(mp, M, N, K);
+        case QV_OP_LINEAR_ACT:
+        case QV_OP_LM_HEAD_ACT: {
+            const size_t off = act_codes_offset(op == QV_OP_LM_HEAD_ACT, M, K, N);
+            return off + al16((size_t)M * K) + al16((size_t)M * 4);
+        }
     }
     return 0;
 }
@@ -294,6 +308,91 @@ qv_status qv_lm_head_argmax(const int8_t* xq, const float* sx, int M, int K, con
         if (e != cudaSuccess) return cuda_fail(e, "qv_lm_head_argmax launch");
     }
     return ok();
+}
+
+namespace {
+// Shared body of qv_w8a8_linear_act / qv_lm_head_argmax_act.
+qv_status linear_act(bool lm, const void* x, qv_dtype x_dtype, const float* act_mul, int M, int K,
+                     const int8_t* wq, const float* sw, int N, void* y, qv_dtype y_dtype,
+                     int32_t* tokens, float* max_logit, void* workspace, size_t workspace_bytes,
+                     cudaStream_t stream) {
+    if (!x || !wq || !sw) return fail(QV_ERR_INVALID_ARG, "null input pointer");
+    if (x_dtype != QV_F32 && x_dtype != QV_BF16) return fail(QV_ERR_INVALID_ARG, "x_dtype must be QV_F32 or QV_BF16");
+    if (M < 1 || M > QV_MAX_M) return fail(QV_ERR_INVALID_ARG, "M=%d outside [1, %d]", M, QV_MAX_M);
+    if (N < 1) return fail(QV_ERR_INVALID_ARG, "N=%d must be >= 1", N);
+    qv_status st = check_k(K);
+    if (st != QV_OK) return st;
+    if (!aligned(x, 16) || !aligned(wq, 16) || (act_mul && !aligned(act_mul, 16)))
+        return fail(QV_ERR_INVALID_ARG, "x, wq and act_mul must be 16-byte aligned");
+    if (!aligned(sw, 4)) return fail(QV_ERR_INVALID_ARG, "sw must be 4-byte aligned");
+    if (lm) {
+        if (!tokens) return fail(QV_ERR_INVALID_ARG, "tokens is null");
+        if (!aligned(tokens, 4) || (max_logit && !aligned(max_logit, 4)))
+            return fail(QV_ERR_INVALID_ARG, "tokens/max_logit misaligned");
+    } else {
+        if (!y) return fail(QV_ERR_INVALID_ARG, "y is null");
+        if (y_dtype != QV_F32 && y_dtype != QV_BF16) return fail(QV_ERR_INVALID_ARG, "y_dtype must be QV_F32 or QV_BF16");
+        if (!aligned(y, y_dtype == QV_F32 ? 4 : 2)) return fail(QV_ERR_INVALID_ARG, "y misaligned");
+    }
+    const qv_op op = lm ? QV_OP_LM_HEAD_ACT : QV_OP_LINEAR_ACT;
+    const size_t need = qv_workspace_bytes(op, M, K, N);
+    if (!workspace) return fail(QV_ERR_WORKSPACE, "workspace is null (%zu bytes needed)", need);
+    if (!aligned(workspace, 16)) return fail(QV_ERR_WORKSPACE, "workspace must be 16-byte aligned");
+    if (workspace_bytes < need) return fail(QV_ERR_WORKSPACE, "workspace has %zu bytes, %zu needed", workspace_bytes, need);
+    QV_CHECK_DEV(x);
+    QV_CHECK_DEV(act_mul);
+    QV_CHECK_DEV(wq);
+    QV_CHECK_DEV(sw);
+    QV_CHECK_DEV(workspace);
+    QV_CHECK_DEV(y);
+    QV_CHECK_DEV(tokens);
+    QV_CHECK_DEV(max_logit);
+    cudaError_t e;
+    const int sms = sms_of_current_device(&e);
+    if (e != cudaSuccess) return cuda_fail(e, "device query");
+
+    const int mp = mp_for(M);
+    if (M <= 16 && qv::w8a8_act_smem(mp, K, N, sms) != 0) {
+        qv::W8A8Launch L = {};
+        if ((st = encode_2d(&L.tmap_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, wq, (uint64_t)K, (uint64_t)N,
+                            qv::kTileKBytes, qv::kTileN)) != QV_OK)
+            return st;
+        L.M = M; L.N = N; L.K = K; L.MP = mp;
+        L.sx = nullptr; L.sw = sw;
+        L.y = y; L.y_bf16 = !lm && y_dtype == QV_BF16; L.acc_debug = nullptr;
+        L.tokens = tokens; L.max_logit = max_logit;
+        L.ws = workspace;
+        L.epi = lm ? qv::Epi::LmHead : qv::Epi::Linear;
+        e = qv::launch_w8a8_act(L, x, x_dtype == QV_BF16, act_mul, sms, stream);
+        if (e != cudaSuccess) return cuda_fail(e, lm ? "qv_lm_head_argmax_act launch" : "qv_w8a8_linear_act launch");
+        return ok();
+    }
+    // Materialise the codes and scales in the workspace, then run the GEMM.
+    uint8_t* wsb = static_cast<uint8_t*>(workspace);
+    const size_t off = act_codes_offset(lm, M, K, N);
+    int8_t* xq = reinterpret_cast<int8_t*>(wsb + off);
+    float* sx = reinterpret_cast<float*>(wsb + off + al16((size_t)M * K));
+    e = qv::launch_quantize_rows(x, x_dtype == QV_BF16, M, K, act_mul, xq, sx, true, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "activation quantization launch");
+    if (lm)
+        return qv_lm_head_argmax(xq, sx, M, K, wq, sw, N, tokens, max_logit, workspace, off, stream);
+    return qv_w8a8_linear(xq, sx, M, K, wq, sw, N, y, y_dtype, nullptr, workspace, off, stream);
+}
+}  // namespace
+
+qv_status qv_w8a8_linear_act(const void* x, qv_dtype x_dtype, const float* act_mul, int M, int K,
+                             const int8_t* wq, const float* sw, int N, void* y, qv_dtype y_dtype,
+                             void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    return linear_act(false, x, x_dtype, act_mul, M, K, wq, sw, N, y, y_dtype, nullptr, nullptr,
+                      workspace, workspace_bytes, stream);
+}
+
+qv_status qv_lm_head_argmax_act(const void* x, qv_dtype x_dtype, const float* act_mul, int M, int K,
+                                const int8_t* wq, const float* sw, int V, int32_t* tokens,
+                                float* max_logit, void* workspace, size_t workspace_bytes,
+                                cudaStream_t stream) {
+    return linear_act(true, x, x_dtype, act_mul, M, K, wq, sw, V, nullptr, QV_F32, tokens, max_logit,
+                      workspace, workspace_bytes, stream);
 }
 
 qv_status qv_accept(const int32_t* verify_tokens, const int32_t* draft, int B, int gamma,

@@ -95,6 +95,9 @@ cudaError_t launch_w8a8_tc(const W8A8Launch& a, int num_sms, cudaStream_t s);
 
 // Largest dynamic shared memory of one CTA on sm_103a (227 KB).
 constexpr size_t kMaxDynSmem = 232448;
+// Dynamic shared memory that keeps a second CTA of the same kernel off an SM
+// (an SM has 228 KB, each CTA also takes 1 KB of reserved shared memory).
+constexpr size_t kMinSmemOneCtaPerSm = 118 * 1024;
 // W8A8 with the activation quantization fused in (x fp32 or bf16 [M][K] and
 // optional multipliers instead of codes; a.sx and a.tmap_x unused). Only for
 // MP <= 16; w8a8_act_smem returns the launch's shared memory, 0 when the

@@ -208,12 +208,18 @@ __device__ __forceinline__ void widen_i8x4_f16(uint32_t w, uint32_t& lo, uint32_
 // fl32(x/s) = (x/s)(1+d3) with |di| <= 2^-24, so |t - fl32(x/s)| < 2^-22 |t|.
 // If the distance from t to the nearest half-integer exceeds 2^-20 |t|, both
 // lie strictly on the same side of it and round to the same integer.
+// The IEEE-quotient decision, kept out of line so that the compiler branches
+// to it (rarely) instead of evaluating the division for every element.
+static __device__ __noinline__ int quant_code_div(float x, float s) {
+    const int qi = __float2int_rn(rintf(__fdiv_rn(x, s)));
+    return qi > 127 ? 127 : (qi < -127 ? -127 : qi);
+}
 __device__ __forceinline__ int quant_code(float x, float s, float r) {
     if (s == 0.f) return 0;
     const float t = __fmul_rn(x, r);
-    float q = rintf(t);
+    const float q = rintf(t);
     const float margin = __fsub_rn(0.5f, fabsf(__fsub_rn(t, q)));
-    if (!(margin > __fmul_rn(fabsf(t), 0x1p-20f))) q = rintf(__fdiv_rn(x, s));
+    if (!(margin > __fmul_rn(fabsf(t), 0x1p-20f))) return quant_code_div(x, s);
     const int qi = __float2int_rn(q);
     return qi > 127 ? 127 : (qi < -127 ? -127 : qi);
 }

@@ -119,65 +119,83 @@ struct W8A8Params {
     unsigned* done;
 };
 
-// Segment epilogue of the W8A8 streaming kernels, run by the CW consumer warps
-// (thread index tid in [0, 32*CW)) once the int32 sums of output-channel tile
-// nt over seg_len of its KT K-tiles are staged in sm.stg[row * MP + token] and
-// the consumers have synchronised. A tile whose K range is split over CTAs is
-// combined with int32 atomic adds into the workspace (exact, so order does not
-// matter); the CTA whose contribution completes the tile runs the finishing
-// step, reading and zeroing the sums in one atomic exchange, so the workspace
-// is left zeroed. Linear: y = fl(fl(acc) * fl(sx * sw)) per element. LM head:
-// one 64-bit key per token, (order-preserving bits of y) << 32 | (0xFFFFFFFF -
-// v), combined with atomicMax; the last channel tile to finish decodes the
-// keys into tokens (the lowest index wins ties) and leaves the keys zeroed.
+// ---------------------------------------------------------------------------
+// Epilogue of the W8A8 streaming kernels, run by the CW consumer warps
+// (thread index tid in [0, 32*CW)).
+//
+// A channel tile whose K range is split over CTAs is combined with int32
+// atomic adds into the workspace (exact, so order does not matter); the CTA
+// whose contribution completes the tile (the one that brings the tile's
+// counter to KT) finishes it, reading the sums and zeroing them, so the
+// workspace is left zeroed. Only thread 0 fences, after the CTA barrier that
+// orders the other threads' adds before it (and, on the finishing side,
+// before the barrier that releases the reads).
+//
+// A CTA's stream-K range starts with at most one partial segment that is not
+// its last; that segment's counter result is not needed until the range
+// ends, so the CTA keeps streaming and finishes the tile (if its add was the
+// last) after its final segment. The LM head finishes a tile by folding
+// each token's best (logit, index) key into a global atomicMax word and
+// counts finished tiles per CTA; one counter add per CTA at the end decides
+// which CTA decodes the keys (the last one), then zeroes them.
+//
+// Linear: y = fl(fl(acc) * fl(sx * sw)) per element. LM head key:
+// (order-preserving bits of y) << 32 | (0xFFFFFFFF - v), so the largest key
+// is the largest logit and, among equal logits, the lowest index.
+// ---------------------------------------------------------------------------
+struct EpiState {
+    int def_nt = -1;          // channel tile of the deferred partial contribution
+    int def_len = 0;
+    unsigned def_prev = 0;    // thread 0: tile counter before that contribution
+    unsigned tiles_done = 0;  // LM head: channel tiles this CTA finished
+};
+
+// Finish channel tile nt from sm.stg (from_ws = false) or from the workspace.
 template <int MP, int CW, int EPI, class SM>
-__device__ __forceinline__ void stream_epilogue(SM& sm, const W8A8Params& p, int nt, int seg_len,
-                                                int tid) {
-    constexpr int CT = CW * 32;
+__device__ __forceinline__ void finish_tile(SM& sm, const W8A8Params& p, int nt, bool from_ws, int tid,
+                                            EpiState& st) {
     const int warp = tid >> 5, lane = tid & 31;
-        const bool whole = seg_len == p.KT;
     int32_t* gacc = p.ws_acc + (size_t)nt * BN * MP;
-    if (!whole) {
-        for (int e = tid; e < BN * MP; e += CT) {
-            const int r = e / MP, m = e - (e / MP) * MP;
-            if (m < p.M && nt * BN + r < p.N) atomicAdd(&gacc[e], sm.stg[e]);
+    // the first BN consumer threads (warps 0..3) own one output channel each
+    const int r = tid;
+    const int n = nt * BN + r;
+    const bool valid = r < BN && n < p.N;
+    int32_t acc[MP];
+#pragma unroll
+    for (int m = 0; m < MP; ++m) acc[m] = 0;
+    if (valid) {
+#pragma unroll
+        for (int m = 0; m < MP; ++m)
+            if (m < p.M) acc[m] = from_ws ? __ldcg(&gacc[r * MP + m]) : sm.stg[r * MP + m];
+        if (from_ws) {
+#pragma unroll
+            for (int m = 0; m < MP; ++m)
+                if (m < p.M) __stcg(&gacc[r * MP + m], 0);
         }
-        __threadfence();
-        consumer_sync<CW>();
-        if (tid == 0) {
-            __threadfence();
-            const unsigned prev = atomicAdd(&p.ws_cnt[nt], (unsigned)seg_len);
-            *sm.flag = (prev + (unsigned)seg_len == (unsigned)p.KT) ? 1 : 0;
-        }
-        consumer_sync<CW>();
     }
-    const bool finisher = whole || *sm.flag;
-    if (finisher) {
-        if (!whole) __threadfence();
-        // the first BN consumer threads (warps 0..3) own one output channel each
-        const int r = tid;
-        const int n = nt * BN + r;
-        const bool valid = r < BN && n < p.N;
-        const float swn = valid ? p.sw[n] : 0.f;
-        if (EPI == (int)Epi::Linear) {
-            if (valid) {
-                for (int m = 0; m < p.M; ++m) {
-                    const int32_t acc = whole ? sm.stg[r * MP + m] : atomicExch(&gacc[r * MP + m], 0);
-                    if (p.acc_debug) p.acc_debug[(size_t)m * p.N + n] = acc;
-                    const float yv = __fmul_rn(__int2float_rn(acc), __fmul_rn(sm.sx[m], swn));
+    const float swn = valid ? p.sw[n] : 0.f;
+    if (EPI == (int)Epi::Linear) {
+        if (valid) {
+#pragma unroll
+            for (int m = 0; m < MP; ++m) {
+                if (m < p.M) {
+                    if (p.acc_debug) p.acc_debug[(size_t)m * p.N + n] = acc[m];
+                    const float yv = __fmul_rn(__int2float_rn(acc[m]), __fmul_rn(sm.sx[m], swn));
                     if (p.y_bf16)
                         reinterpret_cast<__nv_bfloat16*>(p.y)[(size_t)m * p.N + n] = __float2bfloat16_rn(yv);
                     else
                         reinterpret_cast<float*>(p.y)[(size_t)m * p.N + n] = yv;
                 }
             }
-        } else {
-            if (r < BN) {
-                for (int m = 0; m < p.M; ++m) {
+        }
+    } else {
+        if (r < BN) {
+#pragma unroll
+            for (int m = 0; m < MP; ++m) {
+                if (m < p.M) {
                     unsigned long long key = 0ull;
                     if (valid) {
-                        const int32_t acc = whole ? sm.stg[r * MP + m] : atomicExch(&gacc[r * MP + m], 0);
-                        const float yv = __fmul_rn(__int2float_rn(acc), __fmul_rn(sm.sx[m], swn));
+                        const float yv = __fmul_rn(__int2float_rn(acc[m]), __fmul_rn(sm.sx[m], swn));
                         key = ((unsigned long long)ordered_bits(yv) << 32) |
                               (unsigned long long)(0xFFFFFFFFu - (unsigned)n);
                     }
@@ -185,37 +203,93 @@ __device__ __forceinline__ void stream_epilogue(SM& sm, const W8A8Params& p, int
                     if (lane == 0) sm.red[warp * MP + m] = key;
                 }
             }
-            consumer_sync<CW>();
-            if (tid < p.M) {
-                unsigned long long k = sm.red[tid];
-#pragma unroll
-                for (int w = 1; w < BN / 32; ++w) {
-                    const unsigned long long o = sm.red[w * MP + tid];
-                    k = o > k ? o : k;
-                }
-                atomicMax(&p.keys[tid], k);
-            }
-            __threadfence();
-            consumer_sync<CW>();
-            if (tid == 0) {
-                __threadfence();
-                const unsigned prev = atomicAdd(p.done, 1u);
-                *sm.flag = (prev + 1u == (unsigned)p.NT) ? 2 : 0;
-            }
-            consumer_sync<CW>();
-            if (*sm.flag == 2) {
-                __threadfence();
-                if (tid < p.M) {
-                    const unsigned long long k = atomicExch(&p.keys[tid], 0ull);
-                    p.tokens[tid] = (int32_t)(0xFFFFFFFFu - (unsigned)(k & 0xFFFFFFFFull));
-                    if (p.max_logit) p.max_logit[tid] = unordered_bits((unsigned)(k >> 32));
-                }
-                if (tid == 0) atomicExch(p.done, 0u);
-            }
         }
-        if (!whole && tid == 0) atomicExch(&p.ws_cnt[nt], 0u);
+        consumer_sync<CW>();
+        if (tid < p.M) {
+            unsigned long long k = sm.red[tid];
+#pragma unroll
+            for (int w = 1; w < BN / 32; ++w) {
+                const unsigned long long o = sm.red[w * MP + tid];
+                k = o > k ? o : k;
+            }
+            atomicMax(&p.keys[tid], k);
+        }
+        ++st.tiles_done;
     }
-    consumer_sync<CW>();   // staging buffer and flags are reused by the next segment
+    if (from_ws && tid == 0) __stcg(&p.ws_cnt[nt], 0u);
+}
+
+// End of a segment (the channel tile nt's sums over seg_len of its K-tiles
+// are staged in sm.stg[row * MP + token] and the consumers have synchronised);
+// last_seg: this is the CTA's final segment.
+template <int MP, int CW, int EPI, class SM>
+__device__ __forceinline__ void segment_end(SM& sm, const W8A8Params& p, int nt, int seg_len,
+                                            bool last_seg, int tid, EpiState& st) {
+    constexpr int CT = CW * 32;
+    if (seg_len == p.KT) {
+        finish_tile<MP, CW, EPI>(sm, p, nt, false, tid, st);
+        consumer_sync<CW>();   // staging buffer and reduction slots are reused
+        return;
+    }
+    int32_t* gacc = p.ws_acc + (size_t)nt * BN * MP;
+    for (int e = tid; e < BN * MP; e += CT) {
+        const int r = e / MP, m = e - (e / MP) * MP;
+        if (m < p.M && nt * BN + r < p.N) atomicAdd(&gacc[e], sm.stg[e]);
+    }
+    consumer_sync<CW>();
+    unsigned prev = 0;
+    if (tid == 0) {
+        __threadfence();
+        prev = atomicAdd(&p.ws_cnt[nt], (unsigned)seg_len);
+    }
+    if (!last_seg) {
+        st.def_nt = nt;
+        st.def_len = seg_len;
+        if (tid == 0) st.def_prev = prev;   // read only when the range ends
+        return;
+    }
+    if (tid == 0) {
+        const bool fin = prev + (unsigned)seg_len == (unsigned)p.KT;
+        if (fin) __threadfence();
+        *sm.flag = fin ? 1 : 0;
+    }
+    consumer_sync<CW>();
+    if (*sm.flag) finish_tile<MP, CW, EPI>(sm, p, nt, true, tid, st);
+    consumer_sync<CW>();
+}
+
+// After the CTA's last segment: the deferred tile, then the LM head's decode.
+template <int MP, int CW, int EPI, class SM>
+__device__ __forceinline__ void range_end(SM& sm, const W8A8Params& p, int tid, EpiState& st) {
+    if (st.def_nt >= 0) {
+        if (tid == 0) {
+            const bool fin = st.def_prev + (unsigned)st.def_len == (unsigned)p.KT;
+            if (fin) __threadfence();
+            *sm.flag = fin ? 1 : 0;
+        }
+        consumer_sync<CW>();
+        if (*sm.flag) finish_tile<MP, CW, EPI>(sm, p, st.def_nt, true, tid, st);
+        consumer_sync<CW>();
+    }
+    if (EPI == (int)Epi::LmHead && st.tiles_done > 0) {
+        if (tid == 0) {
+            __threadfence();
+            const unsigned prev = atomicAdd(p.done, st.tiles_done);
+            const bool last = prev + st.tiles_done == (unsigned)p.NT;
+            if (last) __threadfence();
+            *sm.flag = last ? 2 : 0;
+        }
+        consumer_sync<CW>();
+        if (*sm.flag == 2) {
+            if (tid < p.M) {
+                const unsigned long long k = __ldcg(&p.keys[tid]);
+                __stcg(&p.keys[tid], 0ull);
+                p.tokens[tid] = (int32_t)(0xFFFFFFFFu - (unsigned)(k & 0xFFFFFFFFull));
+                if (p.max_logit) p.max_logit[tid] = unordered_bits((unsigned)(k >> 32));
+            }
+            if (tid == 0) __stcg(p.done, 0u);
+        }
+    }
 }
 
 }  // namespace

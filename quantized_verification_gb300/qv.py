@@ -18,6 +18,7 @@ LIB_PATH = os.path.join(_PKG, "libqv.so")
 QV_OK, QV_ERR_INVALID_ARG, QV_ERR_UNSUPPORTED, QV_ERR_WORKSPACE, QV_ERR_CUDA = range(5)
 QV_F32, QV_BF16 = 0, 1
 QV_OP_LINEAR, QV_OP_LM_HEAD, QV_OP_BF16_LINEAR, QV_OP_VERIFY_STACK = 0, 1, 2, 3
+QV_OP_LINEAR_ACT, QV_OP_LM_HEAD_ACT = 4, 5
 QV_MAX_K = 133144
 QV_MAX_M = 256
 
@@ -25,7 +26,7 @@ QV_MAX_M = 256
 EXPORTS = ("qv_quantize_act", "qv_w8a8_linear", "qv_lm_head_argmax", "qv_accept",
            "qv_quantize_weight", "qv_bf16_linear", "qv_workspace_bytes",
            "qv_last_error", "qv_device_error", "qv_num_sms", "qv_w8a8_linear_noalloc",
-           "qv_verify_stack")
+           "qv_verify_stack", "qv_w8a8_linear_act", "qv_lm_head_argmax_act")
 MAX_STACK_M = 16
 
 
@@ -68,6 +69,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         L.qv_w8a8_linear_noalloc.argtypes = [P, P, I, I, P, P, I, P, I, P, P]
         L.qv_verify_stack.argtypes = [ctypes.POINTER(LinearDesc), I, ctypes.POINTER(LinearDesc), I, I,
                                       P, I, I, P, P, P, P, P, S, P]
+        L.qv_w8a8_linear_act.argtypes = [P, I, P, I, I, P, P, I, P, I, P, S, P]
+        L.qv_lm_head_argmax_act.argtypes = [P, I, P, I, I, P, P, I, P, P, P, S, P]
         L.qv_workspace_bytes.argtypes = [I, I, I, I]
         L.qv_workspace_bytes.restype = S
         L.qv_last_error.argtypes = []
@@ -77,7 +80,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         L.qv_num_sms.restype = I
         for name in ("qv_quantize_act", "qv_w8a8_linear", "qv_lm_head_argmax", "qv_accept",
                      "qv_quantize_weight", "qv_bf16_linear", "qv_device_error",
-                     "qv_w8a8_linear_noalloc", "qv_verify_stack"):
+                     "qv_w8a8_linear_noalloc", "qv_verify_stack", "qv_w8a8_linear_act",
+                     "qv_lm_head_argmax_act"):
             getattr(L, name).restype = st
         _lib = L
         return L
@@ -183,6 +187,37 @@ def qv_lm_head_argmax(xq, sx, wq, sw, tokens, workspace, max_logit=None, stream=
     _check(load().qv_lm_head_argmax(_ptr(xq), _ptr(sx), M, K, _ptr(wq), _ptr(sw), V, _ptr(tokens),
                                     _ptr(max_logit), _ptr(workspace), workspace.numel(),
                                     ctypes.c_void_p(_stream(stream))))
+
+
+
+def qv_w8a8_linear_act(x, wq, sw, y, workspace, act_mul=None, stream=None):
+    """y [M, N] (fp32 or bf16) = dequant(quant(x * act_mul) wq^T) in one call."""
+    M, K = x.shape
+    N = wq.shape[0]
+    _need(wq.shape == (N, K) and wq.dtype == torch.int8, "wq must be int8 [N, K]")
+    _need(sw.shape == (N,) and sw.dtype == torch.float32, "sw must be float32 [N]")
+    _need(y.shape == (M, N), "y must be [M, N]")
+    if act_mul is not None:
+        _need(act_mul.shape == (K,) and act_mul.dtype == torch.float32, "act_mul must be float32 [K]")
+    _check(load().qv_w8a8_linear_act(_ptr(x), _dtype(x), _ptr(act_mul), M, K, _ptr(wq), _ptr(sw), N,
+                                     _ptr(y), _dtype(y), _ptr(workspace), workspace.numel(),
+                                     ctypes.c_void_p(_stream(stream))))
+
+
+def qv_lm_head_argmax_act(x, wq, sw, tokens, workspace, act_mul=None, max_logit=None, stream=None):
+    """tokens [M] int32 = greedy argmax over the W8A8 LM-head logits of quant(x * act_mul)."""
+    M, K = x.shape
+    V = wq.shape[0]
+    _need(wq.shape == (V, K) and wq.dtype == torch.int8, "wq must be int8 [V, K]")
+    _need(sw.shape == (V,) and sw.dtype == torch.float32, "sw must be float32 [V]")
+    _need(tokens.shape == (M,) and tokens.dtype == torch.int32, "tokens must be int32 [M]")
+    if act_mul is not None:
+        _need(act_mul.shape == (K,) and act_mul.dtype == torch.float32, "act_mul must be float32 [K]")
+    if max_logit is not None:
+        _need(max_logit.shape == (M,) and max_logit.dtype == torch.float32, "max_logit must be float32 [M]")
+    _check(load().qv_lm_head_argmax_act(_ptr(x), _dtype(x), _ptr(act_mul), M, K, _ptr(wq), _ptr(sw), V,
+                                        _ptr(tokens), _ptr(max_logit), _ptr(workspace), workspace.numel(),
+                                        ctypes.c_void_p(_stream(stream))))
 
 
 def qv_accept(verify_tokens, draft, accept_len, out_tokens, stream=None):

@@ -93,6 +93,9 @@ class VerifyStack:
         ws_bytes = max([qv.qv_workspace_bytes(qv.QV_OP_LINEAR, self.M, K, N) for (_, K, N) in self.phases]
                        + [qv.qv_workspace_bytes(qv.QV_OP_LM_HEAD, self.M, h, self.V)])
         self.ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
+        act_bytes = max([qv.qv_workspace_bytes(qv.QV_OP_LINEAR_ACT, self.M, K, N) for (_, K, N) in self.phases]
+                        + [qv.qv_workspace_bytes(qv.QV_OP_LM_HEAD_ACT, self.M, h, self.V)])
+        self.ws_act = torch.zeros(act_bytes, dtype=torch.uint8, device=dev)
         self.graph = None
         torch.cuda.synchronize(dev)
 
@@ -103,28 +106,30 @@ class VerifyStack:
         return per_layer * self.layers + self.V * self.model["hidden"]
 
     def algorithmic_bytes(self) -> int:
-        """All bytes one step must move at least: int8 weights and fp32 scales,
-        the activations read (bf16) and their int8 codes written and read back,
-        token scales, fp32/bf16 outputs, LM-head and acceptance I/O."""
+        """All bytes one step must move at least: int8 weights and fp32
+        channel scales, the bf16 activations read once, the fp32/bf16
+        outputs written, LM-head and acceptance I/O. (The int8 codes and
+        token scales need not reach HBM: the fused kernels keep them on chip.)"""
         M = self.M
         yb = 4 if self.y_dtype == torch.float32 else 2
         total = 0
         for (_, K, N) in self.phases:
-            total += N * K + 4 * N                     # weights + channel scales
-            total += M * K * 2 + M * K + 4 * M         # act quant: read bf16, write int8 + scale
-            total += M * K + 4 * M + M * N * yb        # GEMM: read codes + scales, write y
+            total += N * K + 4 * N + M * K * 2 + M * N * yb
         total *= self.layers
         h = self.model["hidden"]
-        total += M * h * 2 + M * h + 4 * M             # final act quant
-        total += self.V * h + 4 * self.V + M * h + 4 * M + 4 * M   # LM head + tokens
-        total += 4 * M + 4 * self.B * self.gamma + 4 * self.B + 4 * M  # accept I/O
+        total += self.V * h + 4 * self.V + M * h * 2 + 4 * M + 4 * M   # LM head: weights, x, tokens, max
+        total += 4 * M + 4 * self.B * self.gamma + 4 * self.B + 4 * self.B * (self.gamma + 1)  # accept I/O
         return total
 
-    def linear_launch_bytes(self):
-        """Algorithmic bytes of each qv_w8a8_linear launch of a step, in order."""
+    def linear_launch_bytes(self, fused_act: bool = True):
+        """Algorithmic bytes of each projection GEMM launch of a step, in
+        order: weights, channel scales and outputs, plus the bf16 activations
+        (qv_w8a8_linear_act) or their int8 codes and token scales
+        (qv_w8a8_linear)."""
         M = self.M
         yb = 4 if self.y_dtype == torch.float32 else 2
-        one = [N * K + 4 * N + M * K + 4 * M + M * N * yb for (_, K, N) in self.phases]
+        xb = (lambda K: M * K * 2) if fused_act else (lambda K: M * K + 4 * M)
+        one = [N * K + 4 * N + xb(K) + M * N * yb for (_, K, N) in self.phases]
         return one * self.layers
 
     def _xq(self, K):
@@ -132,7 +137,25 @@ class VerifyStack:
 
     # ------------------------------------------------------------------ step
     def enqueue(self, stream=None):
-        """Enqueue one verify step on `stream` (current stream if None)."""
+        """Enqueue one verify step on `stream` (current stream if None): one
+        qv_w8a8_linear_act per projection (activation quantization fused into
+        the GEMM), qv_lm_head_argmax_act, qv_accept."""
+        M = self.M
+        ws = self.ws_act
+        for l in range(self.layers):
+            for p, (name, K, N) in enumerate(self.phases):
+                wq, sw = self.weights[l][p]
+                qv.qv_w8a8_linear_act(self.inputs[l][p], wq, sw, self.y[: M * N].view(M, N), ws,
+                                      stream=stream)
+        qv.qv_lm_head_argmax_act(self.h_final, self.lm_wq, self.lm_sw, self.tokens, ws,
+                                 max_logit=self.max_logit, stream=stream)
+        qv.qv_accept(self.tokens.view(self.B, self.gamma + 1), self.drafts if self.gamma > 0 else None,
+                     self.accept_len, self.out_tokens, stream=stream)
+
+    def enqueue_two_call(self, stream=None):
+        """The same step with separate calls: qv_quantize_act then
+        qv_w8a8_linear per projection, qv_quantize_act then
+        qv_lm_head_argmax, qv_accept (bit-identical results)."""
         M = self.M
         ws = self.ws
         for l in range(self.layers):
@@ -149,9 +172,20 @@ class VerifyStack:
                      self.accept_len, self.out_tokens, stream=stream)
 
     def launches_per_step(self, fused: bool = False) -> int:
+        """Kernels one step launches. fused: the persistent qv_verify_stack
+        path. Otherwise the per-op path: per projection and for the LM head,
+        one fused kernel when M <= 16 (every shape of the Qwen3 models fits its
+        shared-memory code buffer), else an activation-quantization kernel and
+        one GEMM launch per 64 tokens; plus qv_accept."""
         if fused:
             return (self.layers * len(self.phases) + 1 + 149) // 150
-        return self.layers * len(self.phases) * 2 + 3
+        per_gemm = 1 if self.M <= 16 else 1 + (self.M + 63) // 64
+        return (self.layers * len(self.phases) + 1) * per_gemm + 1
+
+    def launches_per_step_two_call(self) -> int:
+        """Kernels of enqueue_two_call: a quantization kernel and one GEMM
+        launch per 64 tokens per projection and for the LM head; qv_accept."""
+        return (self.layers * len(self.phases) + 1) * (1 + (self.M + 63) // 64) + 1
 
     # ------------------------------------------------------------------ fused step
     def _fused_descs(self):
@@ -199,6 +233,10 @@ class VerifyStack:
         """Capture one step into a CUDA graph (after one eager warm-up step)."""
         self.graph = self._capture(self.enqueue, self.device)
         return self.graph
+
+    def capture_two_call(self):
+        self.graph_two_call = self._capture(self.enqueue_two_call, self.device)
+        return self.graph_two_call
 
     def replay(self):
         if self.graph is None:

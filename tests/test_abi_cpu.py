@@ -46,6 +46,13 @@ def test_workspace_sizes(lib):
     assert qv.qv_workspace_bytes(qv.QV_OP_LINEAR, 5, 100, 16) == 0     # K % 16
     assert qv.qv_workspace_bytes(qv.QV_OP_LINEAR, 257, 4096, 16) == 0  # M > QV_MAX_M
     assert qv.qv_workspace_bytes(qv.QV_OP_LINEAR, 5, 133152, 16) == 0  # K > QV_MAX_K
+    # *_ACT: the GEMM workspace, 256-byte aligned, then M*K codes and M scales
+    for op, base in ((qv.QV_OP_LINEAR_ACT, qv.QV_OP_LINEAR), (qv.QV_OP_LM_HEAD_ACT, qv.QV_OP_LM_HEAD)):
+        for (M, K, N) in ((5, 4096, 4096), (17, 272, 1000), (1, 16, 1)):
+            g = qv.qv_workspace_bytes(base, M, K, N)
+            off = (g + 255) // 256 * 256
+            assert qv.qv_workspace_bytes(op, M, K, N) == off + (M * K + 15) // 16 * 16 + (4 * M + 15) // 16 * 16
+        assert qv.qv_workspace_bytes(op, 5, 100, 16) == 0
 
 
 def test_host_validation_without_gpu(lib):
@@ -68,6 +75,17 @@ def test_host_validation_without_gpu(lib):
     assert lib.qv_accept(fake, fake, 0, 3, fake, fake, None) == qv.QV_ERR_INVALID_ARG
     assert lib.qv_accept(fake, fake, 2, -1, fake, fake, None) == qv.QV_ERR_INVALID_ARG
     assert lib.qv_bf16_linear(fake, 300, 256, fake, 8, fake, fake, 1 << 20, None) == qv.QV_ERR_INVALID_ARG
+    # fused act-quant calls: arguments checked before any CUDA call
+    assert lib.qv_w8a8_linear_act(None, 1, None, 5, 256, fake, fake, 8, fake, 0, fake, 1 << 20, None) == qv.QV_ERR_INVALID_ARG
+    assert lib.qv_w8a8_linear_act(fake, 3, None, 5, 256, fake, fake, 8, fake, 0, fake, 1 << 20, None) == qv.QV_ERR_INVALID_ARG
+    assert lib.qv_w8a8_linear_act(fake, 1, P(0x1004), 5, 256, fake, fake, 8, fake, 0, fake, 1 << 20, None) == qv.QV_ERR_INVALID_ARG
+    assert b"aligned" in lib.qv_last_error()
+    assert lib.qv_w8a8_linear_act(fake, 1, None, 257, 256, fake, fake, 8, fake, 0, fake, 1 << 20, None) == qv.QV_ERR_INVALID_ARG
+    assert lib.qv_w8a8_linear_act(fake, 1, None, 5, 256, fake, fake, 8, None, 0, fake, 1 << 20, None) == qv.QV_ERR_INVALID_ARG
+    assert lib.qv_w8a8_linear_act(fake, 1, None, 5, 256, fake, fake, 8, fake, 0, fake, 64, None) == qv.QV_ERR_WORKSPACE
+    assert lib.qv_lm_head_argmax_act(fake, 1, None, 5, 256, fake, fake, 8, None, None, fake, 1 << 20, None) == qv.QV_ERR_INVALID_ARG
+    assert b"tokens" in lib.qv_last_error()
+    assert lib.qv_lm_head_argmax_act(fake, 1, None, 5, 250, fake, fake, 8, fake, None, fake, 1 << 20, None) == qv.QV_ERR_INVALID_ARG
 
 
 def test_binding_rejects_host_tensors(lib):

@@ -1,0 +1,144 @@
+"""qv_w8a8_linear_act / qv_lm_head_argmax_act (activation quantization fused
+into the streaming GEMM) against the oracle chain quantize_rows -> w8a8_linear
+/ lm_head_argmax, bit for bit, and against the two-call GPU path. Covers both
+the fused kernel (M <= 16) and the materialised-codes route (M > 16, or a
+per-CTA code buffer larger than shared memory)."""
+import numpy as np
+import pytest
+import torch
+
+from gpu_util import bf16_bits, np_, rand_codes, rand_scales, require_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def qv():
+    require_gpu()
+    from quantized_verification_gb300 import qv as _qv
+    return _qv
+
+
+def _inputs(M, K, N, dtype, smooth, seed):
+    from quantized_verification_gb300 import synth
+    x = synth.activations(M, K, seed=seed, dtype=dtype)
+    if M >= 3:
+        x[1] = 0                        # scale 0, codes 0
+    if M >= 4:
+        x[2] = x[2] * 1e-30             # tiny row
+    mul = None
+    if smooth:
+        g = torch.Generator().manual_seed(K + seed)
+        mul = (torch.rand(K, generator=g) * 3.5 + 0.25).to(torch.float32)
+    wq = rand_codes((N, K), seed=seed + 1)
+    sw = rand_scales(N, seed=seed + 2)
+    return x, mul, wq, sw
+
+
+def _oracle_codes(oracle, x, mul):
+    m = None if mul is None else np_(mul)
+    if x.dtype == torch.bfloat16:
+        return oracle.quantize_rows(bf16_bits(x), m, bf16=True)
+    return oracle.quantize_rows(np_(x), m)
+
+
+def _gemm_part_zero(qv, ws, op_base, M, K, N):
+    n = qv.qv_workspace_bytes(op_base, M, K, N)
+    return int(ws[:n].count_nonzero()) == 0
+
+
+LINEAR_ACT_CASES = [
+    (5, 4096, 1024, torch.bfloat16, True),
+    (5, 4096, 1024, torch.float32, False),
+    (1, 16, 7, torch.bfloat16, False),
+    (8, 272, 300, torch.float32, True),
+    (9, 512, 384, torch.bfloat16, True),
+    (16, 12288, 512, torch.bfloat16, True),
+    (5, 12288, 4096, torch.bfloat16, True),
+    (17, 256, 200, torch.bfloat16, True),     # codes materialised (M > 16)
+    (64, 1024, 256, torch.float32, True),     # materialised, tcgen05 GEMM
+]
+
+
+@pytest.mark.parametrize("M,K,N,dtype,smooth", LINEAR_ACT_CASES)
+def test_w8a8_linear_act(qv, oracle, M, K, N, dtype, smooth):
+    x, mul, wq, sw = _inputs(M, K, N, dtype, smooth, seed=M * 1009 + K + N)
+    q_ref, s_ref = _oracle_codes(oracle, x, mul)
+    y_ref, _ = oracle.w8a8_linear(q_ref, s_ref, np_(wq), np_(sw))
+    xd, md, wd, sd = x.cuda(), (mul.cuda() if mul is not None else None), wq.cuda(), sw.cuda()
+    ws = qv.workspace(qv.QV_OP_LINEAR_ACT, M, K, N)
+    for y_dtype in (torch.float32, torch.bfloat16):
+        y = torch.full((M, N), float("nan"), dtype=y_dtype, device="cuda")
+        for _ in range(2):                        # the workspace is reusable
+            qv.qv_w8a8_linear_act(xd, wd, sd, y, ws, act_mul=md)
+            torch.cuda.synchronize()
+            assert _gemm_part_zero(qv, ws, qv.QV_OP_LINEAR, M, K, N), "GEMM workspace not left zero-filled"
+            if y_dtype == torch.float32:
+                assert np.array_equal(np_(y).view(np.uint32), y_ref.view(np.uint32))
+            else:
+                assert np.array_equal(bf16_bits(y), oracle.f32_to_bf16(y_ref))
+    # the two-call path gives the same bits
+    xq = torch.empty(M, K, dtype=torch.int8, device="cuda")
+    sx = torch.empty(M, device="cuda")
+    qv.qv_quantize_act(xd, xq, sx, act_mul=md)
+    y2 = torch.empty(M, N, device="cuda")
+    qv.qv_w8a8_linear(xq, sx, wd, sd, y2, qv.workspace(qv.QV_OP_LINEAR, M, K, N))
+    torch.cuda.synchronize()
+    assert np.array_equal(np_(y2).view(np.uint32), y_ref.view(np.uint32))
+
+
+def test_w8a8_linear_act_code_buffer_limit(qv, oracle):
+    """M = 16 with 60 K-tiles per CTA: the per-CTA code buffer no longer fits
+    beside the weight ring, so the call takes the materialised route; 59
+    tiles per CTA still run fused. Both must match the oracle."""
+    M, K = 16, 8192
+    for N in (128 * 140, 128 * 141):
+        x, mul, wq, sw = _inputs(M, K, N, torch.bfloat16, True, seed=N)
+        q_ref, s_ref = _oracle_codes(oracle, x, mul)
+        y_ref, _ = oracle.w8a8_linear(q_ref, s_ref, np_(wq), np_(sw))
+        ws = qv.workspace(qv.QV_OP_LINEAR_ACT, M, K, N)
+        y = torch.empty(M, N, device="cuda")
+        qv.qv_w8a8_linear_act(x.cuda(), wq.cuda(), sw.cuda(), y, ws, act_mul=mul.cuda())
+        torch.cuda.synchronize()
+        assert np.array_equal(np_(y).view(np.uint32), y_ref.view(np.uint32))
+        assert _gemm_part_zero(qv, ws, qv.QV_OP_LINEAR, M, K, N)
+
+
+LM_ACT_CASES = [(5, 4096, 3000, True), (1, 128, 130, False), (16, 256, 1000, True),
+                (20, 256, 777, True), (5, 512, 128 * 160 + 3, False)]
+
+
+@pytest.mark.parametrize("M,K,V,smooth", LM_ACT_CASES)
+def test_lm_head_argmax_act(qv, oracle, M, K, V, smooth):
+    x, mul, wq, sw = _inputs(M, K, V, torch.bfloat16, smooth, seed=M * 77 + K + V)
+    q_ref, s_ref = _oracle_codes(oracle, x, mul)
+    t_ref, m_ref = oracle.lm_head_argmax(q_ref, s_ref, np_(wq), np_(sw))
+    ws = qv.workspace(qv.QV_OP_LM_HEAD_ACT, M, K, V)
+    tok = torch.full((M,), -7, dtype=torch.int32, device="cuda")
+    mx = torch.full((M,), float("nan"), device="cuda")
+    for _ in range(2):
+        qv.qv_lm_head_argmax_act(x.cuda(), wq.cuda(), sw.cuda(), tok, ws,
+                                 act_mul=mul.cuda() if mul is not None else None, max_logit=mx)
+        torch.cuda.synchronize()
+        assert np.array_equal(np_(tok), t_ref)
+        assert np.array_equal(np_(mx).view(np.uint32), m_ref.view(np.uint32))
+        assert _gemm_part_zero(qv, ws, qv.QV_OP_LM_HEAD, M, K, V)
+
+
+def test_lm_head_argmax_act_ties(qv, oracle):
+    """Rows 400, 1700 and 1999 identical and maximal for token 0 (the codes
+    of x do not depend on the weights): the lowest index must win."""
+    M, K, V = 5, 256, 2000
+    x, mul, wq, sw = _inputs(M, K, V, torch.bfloat16, False, seed=3)
+    sw[:] = 0.003
+    q_ref, s_ref = _oracle_codes(oracle, x, mul)
+    best = torch.from_numpy((np.sign(q_ref[0]) * 127).astype(np.int8))
+    for r in (400, 1700, 1999):
+        wq[r] = best
+    t_ref, m_ref = oracle.lm_head_argmax(q_ref, s_ref, np_(wq), np_(sw))
+    assert t_ref[0] == 400
+    ws = qv.workspace(qv.QV_OP_LM_HEAD_ACT, M, K, V)
+    tok = torch.empty(M, dtype=torch.int32, device="cuda")
+    qv.qv_lm_head_argmax_act(x.cuda(), wq.cuda(), sw.cuda(), tok, ws)
+    torch.cuda.synchronize()
+    assert np.array_equal(np_(tok), t_ref)
