@@ -287,7 +287,7 @@ def main():
     paths = [
         ("per_op", per_op_graph, stack.launches_per_step(),
          "per-op ABI calls (qv_w8a8_linear_act per projection, qv_lm_head_argmax_act, qv_accept) in one CUDA graph"),
-        ("two_call", two_call_graph, stack.launches_per_step_two_call(),
+        ("two_call", two_call_graph, stack.launches_per_step(),
          "per-op ABI calls (qv_quantize_act + qv_w8a8_linear per projection, qv_quantize_act + "
          "qv_lm_head_argmax, qv_accept) in one CUDA graph"),
         ("verify_stack", fused_graph, stack.launches_per_step(fused=True),
@@ -333,31 +333,25 @@ def main():
     assert qv.qv_device_error() == 0, "a kernel hit its wait limit"
     peak, peak_kind = read_peaks()
 
-    # ---- dominant kernel: the W8A8 GEMM of the chosen per-op path on the
-    # step's 144 projections, back to back in one graph (PDL between launches)
+    # ---- dominant kernel: the W8A8 streaming GEMM on the step's 144
+    # projections (codes quantized beforehand), back to back in one graph
     M = stack.M
-    fused_act = path_name != "two_call"
-    lin_bytes = stack.linear_launch_bytes(fused_act=fused_act)
+    lin_bytes = stack.linear_launch_bytes(fused_act=False)
     xqs = []
-    if not fused_act:
-        for l in range(stack.layers):
-            for p, (name, K, N) in enumerate(stack.phases):
-                xq = torch.empty(M, K, dtype=torch.int8, device=dev)
-                sxp = torch.empty(M, device=dev)
-                qv.qv_quantize_act(stack.inputs[l][p], xq, sxp)
-                xqs.append((xq, sxp))
-        torch.cuda.synchronize()
+    for l in range(stack.layers):
+        for p, (name, K, N) in enumerate(stack.phases):
+            xq = torch.empty(M, K, dtype=torch.int8, device=dev)
+            sxp = torch.empty(M, device=dev)
+            qv.qv_quantize_act(stack.inputs[l][p], xq, sxp)
+            xqs.append((xq, sxp))
+    torch.cuda.synchronize()
 
     def lin_seq(s):
         j = 0
         for l in range(stack.layers):
             for p, (name, K, N) in enumerate(stack.phases):
                 wq, sw = stack.weights[l][p]
-                yv = stack.y[: M * N].view(M, N)
-                if fused_act:
-                    qv.qv_w8a8_linear_act(stack.inputs[l][p], wq, sw, yv, stack.ws_act, stream=s)
-                else:
-                    qv.qv_w8a8_linear(xqs[j][0], xqs[j][1], wq, sw, yv, stack.ws, stream=s)
+                qv.qv_w8a8_linear(xqs[j][0], xqs[j][1], wq, sw, stack.y[: M * N].view(M, N), stack.ws, stream=s)
                 j += 1
     gl = VerifyStack._capture(lin_seq, dev)
     lin_ms = time_graph(torch, gl, args.kernel_reps, stream)
@@ -365,11 +359,8 @@ def main():
     traffic = None
     if NCU_TRAFFIC["source_sha256"] == kernel_source_sha() and NCU_TRAFFIC["dram_bytes_per_algorithmic_byte"]:
         traffic = NCU_TRAFFIC["dram_bytes_per_algorithmic_byte"] * sum(lin_bytes) / len(lin_bytes)
-    if fused_act:
-        kname = ("w8a8_stream_kernel, activation quantization fused (qv_w8a8_linear_act)" if M <= 16
-                 else "quantize_rows_kernel + W8A8 GEMM (qv_w8a8_linear_act, codes materialised)")
-    else:
-        kname = "W8A8 GEMM on pre-quantized codes (qv_w8a8_linear)"
+    kname = ("w8a8_stream_kernel (int8 mma.sync, qv_w8a8_linear)" if M <= 16
+             else "w8a8_tc_kernel (tcgen05, qv_w8a8_linear)")
     linear_kernel = {"kernel": kname, "achieved": achieved,
                      "frac": achieved / peak, "bytes_per_launch": sum(lin_bytes) / len(lin_bytes),
                      "launch_ms_mean": lin_ms / len(lin_bytes),

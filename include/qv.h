@@ -168,7 +168,7 @@ QV_API qv_status qv_lm_head_argmax(const int8_t* xq, const float* sx, int M, int
 /*
  * qv_w8a8_linear_act -- a1 + a2 in one call: per-token quantization of the
  * activations (qv_quantize_act) followed by the W8A8 linear (qv_w8a8_linear),
- * with the same arithmetic, so y is bit-identical to the two calls.
+ * with the same kernels, so y is bit-identical to the two calls.
  *
  *   Quasar, gist.science/ja summary, section 2.2 items 2-3: BF16
  *   activations scaled by the smoothing factor, converted to INT8 online,
@@ -176,15 +176,18 @@ QV_API qv_status qv_lm_head_argmax(const int8_t* xq, const float* sx, int M, int
  *
  *   x [M*K] fp32 or bf16 (x_dtype), 16-byte aligned; act_mul [K] fp32 or
  *   NULL, 16-byte aligned; wq, sw, y, y_dtype as qv_w8a8_linear.
- *   workspace: qv_workspace_bytes(QV_OP_LINEAR_ACT, M, K, N) bytes,
- *   16-byte aligned, ZERO-FILLED before its first use, with the same
- *   reuse contract as qv_w8a8_linear (its first part is that call's
- *   workspace; the rest holds the codes when they are materialised).
- *   1 <= M <= QV_MAX_M, N >= 1. With M <= 16 and a K range per CTA whose
- *   codes fit in shared memory, one kernel does both steps: every CTA
- *   computes the per-token scales and quantizes only the slice of x its
- *   weight tiles need, so the codes never reach HBM. Otherwise the codes are
- *   written to the workspace by qv_quantize_act's kernel first.
+ *   workspace: at least qv_workspace_bytes(QV_OP_LINEAR_ACT, M, K, N)
+ *   bytes, 16-byte aligned, ZERO-FILLED before its first use. Its start is
+ *   the qv_w8a8_linear workspace (left zero-filled, as there); the int8 codes
+ *   and token scales are written to its last M*K + 4*M bytes (each rounded
+ *   up to 16, placed at a 256-byte boundary). A buffer shared by several
+ *   stream-ordered *_ACT calls of different shapes must therefore hold the
+ *   largest GEMM part (qv_workspace_bytes of QV_OP_LINEAR / QV_OP_LM_HEAD,
+ *   rounded up to 256) plus the largest code part.
+ *   1 <= M <= QV_MAX_M, N >= 1. Two kernels are enqueued (quantization,
+ *   then the streaming GEMM, which starts loading weights while the first
+ *   one runs). A single kernel doing both was measured slower on GB300:
+ *   every CTA needs the whole-row scales, so it would repeat the amax pass.
  */
 QV_API qv_status qv_w8a8_linear_act(const void* x, qv_dtype x_dtype, const float* act_mul,
                                     int M, int K, const int8_t* wq, const float* sw, int N,

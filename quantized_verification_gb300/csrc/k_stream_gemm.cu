@@ -86,23 +86,21 @@ __host__ __device__ constexpr int s8_pairs() { return NG == 1 ? QV_S8_PAIRS_NARR
 static_assert(kW8A8Warps == 4 || kW8A8Warps == 8, "4 or 8 consumer warps");
 static_assert(kBf16Warps == 4 || kBf16Warps == 8, "4 or 8 consumer warps");
 
-template <int NG, bool TMAX = true>
+template <int NG>
 struct Cfg {
     static constexpr int MP = 8 * NG;                        // padded tokens
     static constexpr int XBytes = MP * BKB;                  // activation slice
-    // TMAX: the activation slice travels with each weight tile; otherwise
-    // the codes live in a per-CTA buffer after the carve-up below.
-    static constexpr int XSlot = TMAX ? ((XBytes + 1023) / 1024) * 1024 : 0;
+    static constexpr int XSlot = ((XBytes + 1023) / 1024) * 1024;
     static constexpr int StageBytes = kWTileBytes + XSlot;
     // Seven stages for up to 16 tokens also make a CTA need more than half of
     // an SM's shared memory, so no SM ever holds two CTAs of one launch (two
     // would share the SM's bandwidth and finish last).
-    static constexpr int Stages = !TMAX ? 6 : NG == 1 ? 7 : NG == 2 ? 7 : NG == 4 ? 5 : 4;
+    static constexpr int Stages = NG == 1 ? 7 : NG == 2 ? 7 : NG == 4 ? 5 : 4;
     static constexpr int StgWords = BN * MP;                 // epilogue staging
     static constexpr int SmemBytes =
         1024 /*alignment slack*/ + Stages * StageBytes + StgWords * 4 +
         2 * Stages * 8 + kMaxConsumerWarps * MP * 8 + MP * 4 + 64;
-    static constexpr int XcOffset = ((SmemBytes + 1023) / 1024) * 1024;   // from the aligned base
+    static_assert(SmemBytes > (int)kMinSmemOneCtaPerSm, "one CTA per SM");
 };
 
 
@@ -264,206 +262,12 @@ __device__ __forceinline__ void w8a8_tile_mma(uint32_t wb, uint32_t xb, const Ti
 
 // ---------------------------------------------------------------------------
 // W8A8 kernel
-//
-// XMODE 0: the int8 activation codes (qv_quantize_act's output) travel with
-// each weight tile by TMA. XMODE 1 / 2: the kernel quantizes the bf16 / fp32
-// activations itself (qv_w8a8_linear_act): after the grid-dependency wait
-// every CTA computes the per-token amax of x' = fl(x * c) over the whole row
-// (the same bits in every CTA), then quantizes only the K-tiles its own
-// stream-K range touches into a shared-memory buffer with the layout of the
-// TMA tile (128-byte rows, 128-byte swizzle), while the producer keeps
-// streaming weights. Codes and scales are those of qv_quantize_act, bit for
-// bit: s = fl(amax / 127), q = quant_code(x', s, fl(1 / s)).
 // ---------------------------------------------------------------------------
-struct ActParams {
-    const void* x;            // [M][K] fp32 or bf16
-    const float* act_mul;     // [K] smoothing multipliers (16-byte aligned) or null
-    int xc_slots;             // K-tiles of codes the shared buffer holds (>= min(tiles per CTA, KT))
-};
-
-// Raw 16-byte vectors of the 16 elements of row `row` from column k0 (2 for
-// bf16, 4 for fp32) and the 4 float4 of their multipliers.
-template <bool BF16>
-__device__ __forceinline__ void load_chunk16(const void* x, int K, int row, int k0, uint4 (&r)[BF16 ? 2 : 4]) {
-    const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(x) +
-                                                      ((size_t)row * K + k0) * (BF16 ? 2 : 4));
-#pragma unroll
-    for (int j = 0; j < (BF16 ? 2 : 4); ++j) r[j] = __ldg(src + j);
-}
-template <bool BF16>
-__device__ __forceinline__ void unpack_chunk16(const uint4 (&r)[BF16 ? 2 : 4], float (&e)[16]) {
-    if constexpr (BF16) {
-        const uint32_t w[8] = {r[0].x, r[0].y, r[0].z, r[0].w, r[1].x, r[1].y, r[1].z, r[1].w};
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            e[2 * j] = __uint_as_float(w[j] << 16);
-            e[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
-        }
-    } else {
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            e[4 * j] = __uint_as_float(r[j].x); e[4 * j + 1] = __uint_as_float(r[j].y);
-            e[4 * j + 2] = __uint_as_float(r[j].z); e[4 * j + 3] = __uint_as_float(r[j].w);
-        }
-    }
-}
-__device__ __forceinline__ void scale_chunk16(float (&e)[16], const float4 (&c)[4]) {
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        e[4 * j] = __fmul_rn(e[4 * j], c[j].x);
-        e[4 * j + 1] = __fmul_rn(e[4 * j + 1], c[j].y);
-        e[4 * j + 2] = __fmul_rn(e[4 * j + 2], c[j].z);
-        e[4 * j + 3] = __fmul_rn(e[4 * j + 3], c[j].w);
-    }
-}
-
-// Per-token amax of x' over chunks [c0 + u * CT] (u < U) into the per-thread
-// running maxima amax[MP]; all U chunks' loads are issued before any is used.
-template <int MP, int CT, bool BF16, int U, bool MUL>
-__device__ __forceinline__ void amax_batch(const W8A8Params& p, const ActParams& q, int c0, int cpr,
-                                           int total, float (&amax)[MP]) {
-    constexpr int V = BF16 ? 2 : 4;
-    uint4 r[U][V];
-    float4 c[MUL ? U : 1][4];
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-        const int ci = c0 + u * CT;
-        if (ci < total) {
-            const int row = ci / cpr, k0 = (ci - row * cpr) * 16;
-            load_chunk16<BF16>(q.x, p.K, row, k0, r[u]);
-            if (MUL) {
-#pragma unroll
-                for (int j = 0; j < 4; ++j) c[MUL ? u : 0][j] = __ldg(reinterpret_cast<const float4*>(q.act_mul + k0) + j);
-            }
-        }
-    }
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-        const int ci = c0 + u * CT;
-        if (ci < total) {
-            const int row = ci / cpr;
-            float e[16];
-            unpack_chunk16<BF16>(r[u], e);
-            if (MUL) scale_chunk16(e, c[MUL ? u : 0]);
-            float mx = 0.f;
-#pragma unroll
-            for (int j = 0; j < 16; ++j) mx = fmaxf(mx, fabsf(e[j]));
-#pragma unroll
-            for (int m = 0; m < MP; ++m) amax[m] = row == m ? fmaxf(amax[m], mx) : amax[m];
-        }
-    }
-}
-
-// Codes of items [i0 + u * CT] (u < U); item = (slot j, row m < M, 16-byte
-// chunk ch) of the CTA's K-tiles kt0, kt0+1, ... (mod KT).
-template <int MP, int CT, bool BF16, int U, bool MUL>
-__device__ __forceinline__ void codes_batch(const W8A8Params& p, const ActParams& q, const float* sxs,
-                                            const float* rcp, uint8_t* xc, int kt0, int i0, int items) {
-    constexpr int V = BF16 ? 2 : 4;
-    const int per_slot = p.M * 8;
-    uint4 r[U][V];
-    float4 c[MUL ? U : 1][4];
-    int kk[U];
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-        const int it = i0 + u * CT;
-        kk[u] = -1;
-        if (it < items) {
-            const int j = it / per_slot, rem = it - j * per_slot;
-            const int row = rem >> 3, ch = rem & 7;
-            int kt = kt0 + j;
-            if (kt >= p.KT) kt -= p.KT;
-            const int k0 = kt * BKB + ch * 16;
-            if (k0 < p.K) {
-                kk[u] = k0;
-                load_chunk16<BF16>(q.x, p.K, row, k0, r[u]);
-                if (MUL) {
-#pragma unroll
-                    for (int t = 0; t < 4; ++t) c[MUL ? u : 0][t] = __ldg(reinterpret_cast<const float4*>(q.act_mul + k0) + t);
-                }
-            }
-        }
-    }
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-        const int it = i0 + u * CT;
-        if (it < items && kk[u] >= 0) {
-            const int j = it / per_slot, rem = it - j * per_slot;
-            const int row = rem >> 3, ch = rem & 7;
-            float e[16];
-            unpack_chunk16<BF16>(r[u], e);
-            if (MUL) scale_chunk16(e, c[MUL ? u : 0]);
-            const float sc = sxs[row], rc = rcp[row];
-            uint32_t w[4] = {0u, 0u, 0u, 0u};
-#pragma unroll
-            for (int t = 0; t < 16; ++t)
-                w[t >> 2] |= (uint32_t)(uint8_t)(int8_t)quant_code(e[t], sc, rc) << (8 * (t & 3));
-            *reinterpret_cast<uint4*>(xc + (size_t)j * MP * BKB + row * BKB + ((ch ^ (row & 7)) << 4)) =
-                make_uint4(w[0], w[1], w[2], w[3]);
-        }
-    }
-}
-
-// Consumers of an XMODE 1/2 launch: per-token scales into sm_sx (and
-// reciprocals into s_rcp), then the codes of K-tiles kt0, kt0+1, ... (mod KT),
-// nslot of them, into xc (slot j = MP rows x 128 bytes, 128-byte swizzle;
-// padding rows and a ragged K tail are zero). Loads are issued in batches of
-// 4-16 chunks per thread so that each pass costs about one memory round trip.
-template <int MP, int CW, bool BF16>
-__device__ __forceinline__ void act_prologue(const W8A8Params& p, const ActParams& q, float* sm_sx,
-                                             unsigned* s_amax, float* s_rcp, uint8_t* xc, int kt0,
-                                             int nslot, int tid) {
-    constexpr int CT = CW * 32;
-    constexpr int UA = BF16 ? 8 : 4;       // chunks per thread per amax batch
-    constexpr int UC = BF16 ? 8 : 4;       // items per thread per code batch
-    if (tid < MP) s_amax[tid] = 0u;
-    for (int e = tid; e < nslot * MP * 8; e += CT)
-        reinterpret_cast<uint4*>(xc)[e] = make_uint4(0u, 0u, 0u, 0u);
-    consumer_sync<CW>();
-    const int cpr = p.K / 16;
-    const int total = p.M * cpr;
-    float amax[MP];
-#pragma unroll
-    for (int m = 0; m < MP; ++m) amax[m] = 0.f;
-    if (q.act_mul) {
-        for (int c0 = tid; c0 < total; c0 += (UA / 2) * CT)
-            amax_batch<MP, CT, BF16, UA / 2, true>(p, q, c0, cpr, total, amax);
-    } else {
-        for (int c0 = tid; c0 < total; c0 += UA * CT)
-            amax_batch<MP, CT, BF16, UA, false>(p, q, c0, cpr, total, amax);
-    }
-    const int lane = tid & 31;
-#pragma unroll
-    for (int m = 0; m < MP; ++m) {
-        float v = amax[m];
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
-        if (lane == 0 && m < p.M) atomicMax(&s_amax[m], __float_as_uint(v));
-    }
-    consumer_sync<CW>();
-    if (tid < MP) {
-        const float sc = tid < p.M ? __fdiv_rn(__uint_as_float(s_amax[tid]), 127.0f) : 0.f;
-        sm_sx[tid] = sc;
-        s_rcp[tid] = __frcp_rn(sc);
-    }
-    consumer_sync<CW>();
-    const int items = nslot * p.M * 8;
-    if (q.act_mul) {
-        for (int i0 = tid; i0 < items; i0 += (UC / 2) * CT)
-            codes_batch<MP, CT, BF16, UC / 2, true>(p, q, sm_sx, s_rcp, xc, kt0, i0, items);
-    } else {
-        for (int i0 = tid; i0 < items; i0 += UC * CT)
-            codes_batch<MP, CT, BF16, UC, false>(p, q, sm_sx, s_rcp, xc, kt0, i0, items);
-    }
-    consumer_sync<CW>();
-}
-
-template <int NG, int EPI, int XMODE>
+template <int NG, int EPI>
 __global__ void __launch_bounds__((kW8A8Warps + 1) * 32, 1)
 w8a8_stream_kernel(const __grid_constant__ CUtensorMap tmap_w,
-                   const __grid_constant__ CUtensorMap tmap_x, const W8A8Params p, const ActParams q) {
-    constexpr bool TMAX = XMODE == 0;
-    using C = Cfg<NG, TMAX>;
+                   const __grid_constant__ CUtensorMap tmap_x, const W8A8Params p) {
+    using C = Cfg<NG>;
     constexpr int MP = C::MP;
     constexpr int Stages = C::Stages;
     constexpr int CW = kW8A8Warps;
@@ -472,9 +276,6 @@ w8a8_stream_kernel(const __grid_constant__ CUtensorMap tmap_w,
     constexpr int S8P = s8_pairs<NG>();
     extern __shared__ uint8_t smem_raw[];
     Smem<Stages, C::StageBytes, C::StgWords, MP> sm(smem_raw);
-    uint8_t* xc = sm.stages + (C::XcOffset - 0);   // the carve-up starts at the aligned base
-    __shared__ unsigned s_amax[MP];
-    __shared__ float s_rcp[MP];
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
@@ -495,21 +296,15 @@ w8a8_stream_kernel(const __grid_constant__ CUtensorMap tmap_w,
 
     if (warp == CW) {
         if (lane == 0)
-            produce<Stages>(&g_stream_gemm_error, sm, &tmap_w, TMAX ? &tmap_x : nullptr, a, b, p.KT,
-                            BKB, (unsigned)(kWTileBytes + (TMAX ? C::XBytes : 0)));
+            produce<Stages>(&g_stream_gemm_error, sm, &tmap_w, &tmap_x, a, b, p.KT, BKB,
+                            (unsigned)(kWTileBytes + C::XBytes));
         return;
     }
 
     // ---------------- consumers ----------------
     grid_dependency_wait();
-    const int kt0 = a % p.KT;
-    if (TMAX) {
-        if (tid < MP) sm.sx[tid] = tid < p.M ? p.sx[tid] : 0.f;
-        consumer_sync<CW>();
-    } else {
-        const int nslot = min(min(b - a, p.KT), q.xc_slots);   // the host sizes xc_slots to cover it
-        act_prologue<MP, CW, XMODE == 1>(p, q, sm.sx, s_amax, s_rcp, xc, kt0, nslot, tid);
-    }
+    if (tid < MP) sm.sx[tid] = tid < p.M ? p.sx[tid] : 0.f;
+    consumer_sync<CW>();
 
     const int g = lane >> 2, t4 = lane & 3;
     const TileLanes<BPW> L(RW * warp, lane);
@@ -517,7 +312,6 @@ w8a8_stream_kernel(const __grid_constant__ CUtensorMap tmap_w,
     int32_t acci[BPW][NG][4];
     EpiState est;
     int s = 0, phase = 0;
-    int slot = 0;                        // code slot of tile i (XMODE 1/2): (i - a) mod KT
     int i = a;
     while (i < b) {
         const int nt = i / p.KT;
@@ -533,12 +327,10 @@ w8a8_stream_kernel(const __grid_constant__ CUtensorMap tmap_w,
         for (; i < seg_end; ++i) {
             if (!mbar_wait_bounded(&sm.full[s], phase, sm.abort))
                 atomicOr(&g_stream_gemm_error, kErrFullWait);
-            const uint32_t xb = TMAX ? smem_u32(sm.x_tile(s)) : smem_u32(xc + slot * (MP * BKB));
-            w8a8_tile_mma<NG, BPW, S8P>(smem_u32(sm.w_tile(s)), xb, L, acci);
+            w8a8_tile_mma<NG, BPW, S8P>(smem_u32(sm.w_tile(s)), smem_u32(sm.x_tile(s)), L, acci);
             __syncwarp();
             if (lane == 0) mbar_arrive(&sm.empty[s]);
             if (++s == Stages) { s = 0; phase ^= 1; }
-            if (++slot == p.KT) slot = 0;
         }
 
         // -------- segment end: stage the int32 sums [row][token] --------
@@ -1344,8 +1136,7 @@ WsLayout ws_layout(int mp, int n, bool lm_head) {
     return L;
 }
 
-namespace {
-W8A8Params make_w8a8_params(const W8A8Launch& a, int num_sms, int* grid) {
+cudaError_t launch_w8a8_stream(const W8A8Launch& a, int num_sms, cudaStream_t s) {
     const bool lm = a.epi == Epi::LmHead;
     WsLayout L = ws_layout(a.MP, a.N, lm);
     W8A8Params p;
@@ -1360,31 +1151,15 @@ W8A8Params make_w8a8_params(const W8A8Launch& a, int num_sms, int* grid) {
     p.ws_cnt = reinterpret_cast<unsigned*>(ws + L.counters);
     p.keys = reinterpret_cast<unsigned long long*>(ws + L.keys);
     p.done = reinterpret_cast<unsigned*>(ws + L.done);
-    *grid = (int)(p.T < num_sms ? p.T : num_sms);
-    return p;
-}
-
-// Code slots one CTA of the fused-quantization kernel needs: the K-tiles of
-// its stream-K range (at most ceil(T / grid) tiles), at most KT.
-int act_slots(long long T, int KT, int grid) {
-    const long long per = (T + grid - 1) / grid;
-    return (int)(per < KT ? per : KT);
-}
-}  // namespace
-
-cudaError_t launch_w8a8_stream(const W8A8Launch& a, int num_sms, cudaStream_t s) {
-    int grid;
-    const W8A8Params p = make_w8a8_params(a, num_sms, &grid);
-    const bool lm = a.epi == Epi::LmHead;
-    const ActParams q = {};
-#define QV_W8A8_CASE(NGV)                                                                      \
-    case NGV:                                                                                  \
-        return lm ? launch_ex(w8a8_stream_kernel<NGV, (int)Epi::LmHead, 0>, grid,              \
-                              (kW8A8Warps + 1) * 32, Cfg<NGV>::SmemBytes, s, a.tmap_w,         \
-                              a.tmap_x, p, q)                                                  \
-                  : launch_ex(w8a8_stream_kernel<NGV, (int)Epi::Linear, 0>, grid,              \
-                              (kW8A8Warps + 1) * 32, Cfg<NGV>::SmemBytes, s, a.tmap_w,         \
-                              a.tmap_x, p, q);
+    const int grid = (int)(p.T < num_sms ? p.T : num_sms);
+#define QV_W8A8_CASE(NGV)                                                                    \
+    case NGV:                                                                                \
+        return lm ? launch_ex(w8a8_stream_kernel<NGV, (int)Epi::LmHead>, grid,               \
+                              (kW8A8Warps + 1) * 32, Cfg<NGV>::SmemBytes, s, a.tmap_w,       \
+                              a.tmap_x, p)                                                   \
+                  : launch_ex(w8a8_stream_kernel<NGV, (int)Epi::Linear>, grid,               \
+                              (kW8A8Warps + 1) * 32, Cfg<NGV>::SmemBytes, s, a.tmap_w,       \
+                              a.tmap_x, p);
     switch (a.MP / 8) {
         QV_W8A8_CASE(1)
         QV_W8A8_CASE(2)
@@ -1393,47 +1168,6 @@ cudaError_t launch_w8a8_stream(const W8A8Launch& a, int num_sms, cudaStream_t s)
         default: return cudaErrorInvalidValue;
     }
 #undef QV_W8A8_CASE
-}
-
-size_t w8a8_act_smem(int MP, int K, int N, int num_sms) {
-    const int KT = ceil_div(K, BKB), NT = ceil_div(N, BN);
-    const long long T = (long long)KT * NT;
-    const int grid = (int)(T < num_sms ? T : num_sms);
-    const size_t xc = (size_t)act_slots(T, KT, grid) * MP * BKB;
-    size_t base;
-    if (MP == 8) base = Cfg<1, false>::XcOffset;
-    else if (MP == 16) base = Cfg<2, false>::XcOffset;
-    else return 0;
-    size_t total = 1024 + base + xc;
-    // at least half of an SM's shared memory plus one byte: one CTA per SM
-    if (total < kMinSmemOneCtaPerSm) total = kMinSmemOneCtaPerSm;
-    return total <= kMaxDynSmem ? total : 0;
-}
-
-cudaError_t launch_w8a8_act(const W8A8Launch& a, const void* x, bool x_bf16, const float* act_mul,
-                            int num_sms, cudaStream_t s) {
-    int grid;
-    const W8A8Params p = make_w8a8_params(a, num_sms, &grid);
-    const size_t smem = w8a8_act_smem(a.MP, a.K, a.N, num_sms);
-    if (smem == 0) return cudaErrorInvalidValue;
-    ActParams q;
-    q.x = x;
-    q.act_mul = act_mul;
-    q.xc_slots = act_slots(p.T, p.KT, grid);
-    const bool lm = a.epi == Epi::LmHead;
-    const int threads = (kW8A8Warps + 1) * 32;
-#define QV_ACT_CASE(NGV, XM)                                                                         \
-    return lm ? launch_ex(w8a8_stream_kernel<NGV, (int)Epi::LmHead, XM>, grid, threads, (int)smem, s, \
-                          a.tmap_w, a.tmap_w, p, q)                                                  \
-              : launch_ex(w8a8_stream_kernel<NGV, (int)Epi::Linear, XM>, grid, threads, (int)smem, s, \
-                          a.tmap_w, a.tmap_w, p, q);
-    if (a.MP == 8) {
-        if (x_bf16) { QV_ACT_CASE(1, 1) } else { QV_ACT_CASE(1, 2) }
-    } else if (a.MP == 16) {
-        if (x_bf16) { QV_ACT_CASE(2, 1) } else { QV_ACT_CASE(2, 2) }
-    }
-#undef QV_ACT_CASE
-    return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_bf16_stream(const Bf16Launch& a, int num_sms, cudaStream_t s) {

@@ -347,29 +347,15 @@ qv_status linear_act(bool lm, const void* x, qv_dtype x_dtype, const float* act_
     QV_CHECK_DEV(y);
     QV_CHECK_DEV(tokens);
     QV_CHECK_DEV(max_logit);
+    // The codes and token scales go to the workspace (qv_quantize_act's
+    // kernel), then the GEMM streams the weights against them.
     cudaError_t e;
-    const int sms = sms_of_current_device(&e);
-    if (e != cudaSuccess) return cuda_fail(e, "device query");
-
-    const int mp = mp_for(M);
-    if (M <= 16 && qv::w8a8_act_smem(mp, K, N, sms) != 0) {
-        qv::W8A8Launch L = {};
-        if ((st = encode_2d(&L.tmap_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, wq, (uint64_t)K, (uint64_t)N,
-                            qv::kTileKBytes, qv::kTileN)) != QV_OK)
-            return st;
-        L.M = M; L.N = N; L.K = K; L.MP = mp;
-        L.sx = nullptr; L.sw = sw;
-        L.y = y; L.y_bf16 = !lm && y_dtype == QV_BF16; L.acc_debug = nullptr;
-        L.tokens = tokens; L.max_logit = max_logit;
-        L.ws = workspace;
-        L.epi = lm ? qv::Epi::LmHead : qv::Epi::Linear;
-        e = qv::launch_w8a8_act(L, x, x_dtype == QV_BF16, act_mul, sms, stream);
-        if (e != cudaSuccess) return cuda_fail(e, lm ? "qv_lm_head_argmax_act launch" : "qv_w8a8_linear_act launch");
-        return ok();
-    }
-    // Materialise the codes and scales in the workspace, then run the GEMM.
+    // The codes sit at the end of the caller's buffer, 256-byte aligned, so a
+    // buffer shared by calls of different shapes keeps every call's GEMM part
+    // (which must stay zero-filled) clear of any call's codes.
     uint8_t* wsb = static_cast<uint8_t*>(workspace);
-    const size_t off = act_codes_offset(lm, M, K, N);
+    const size_t codes = al16((size_t)M * K) + al16((size_t)M * 4);
+    const size_t off = (workspace_bytes - codes) & ~size_t(255);
     int8_t* xq = reinterpret_cast<int8_t*>(wsb + off);
     float* sx = reinterpret_cast<float*>(wsb + off + al16((size_t)M * K));
     e = qv::launch_quantize_rows(x, x_dtype == QV_BF16, M, K, act_mul, xq, sx, true, stream);

@@ -98,13 +98,6 @@ constexpr size_t kMaxDynSmem = 232448;
 // Dynamic shared memory that keeps a second CTA of the same kernel off an SM
 // (an SM has 228 KB, each CTA also takes 1 KB of reserved shared memory).
 constexpr size_t kMinSmemOneCtaPerSm = 118 * 1024;
-// W8A8 with the activation quantization fused in (x fp32 or bf16 [M][K] and
-// optional multipliers instead of codes; a.sx and a.tmap_x unused). Only for
-// MP <= 16; w8a8_act_smem returns the launch's shared memory, 0 when the
-// shape does not fit (the caller then quantizes separately).
-size_t w8a8_act_smem(int MP, int K, int N, int num_sms);
-cudaError_t launch_w8a8_act(const W8A8Launch& a, const void* x, bool x_bf16, const float* act_mul,
-                            int num_sms, cudaStream_t s);
 cudaError_t launch_verify_stack(const StackLaunch& a, int num_sms, cudaStream_t s);
 cudaError_t launch_bf16_stream(const Bf16Launch& a, int num_sms, cudaStream_t s);
 cudaError_t launch_quantize_rows(const void* x, bool bf16, int rows, int K,

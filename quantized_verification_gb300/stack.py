@@ -93,9 +93,13 @@ class VerifyStack:
         ws_bytes = max([qv.qv_workspace_bytes(qv.QV_OP_LINEAR, self.M, K, N) for (_, K, N) in self.phases]
                        + [qv.qv_workspace_bytes(qv.QV_OP_LM_HEAD, self.M, h, self.V)])
         self.ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
-        act_bytes = max([qv.qv_workspace_bytes(qv.QV_OP_LINEAR_ACT, self.M, K, N) for (_, K, N) in self.phases]
-                        + [qv.qv_workspace_bytes(qv.QV_OP_LM_HEAD_ACT, self.M, h, self.V)])
-        self.ws_act = torch.zeros(act_bytes, dtype=torch.uint8, device=dev)
+        # shared by every *_act call of a step: the largest GEMM part plus the
+        # largest code part (the codes go to the end of the buffer)
+        al = lambda v, a: (v + a - 1) // a * a
+        gemm = max([qv.qv_workspace_bytes(qv.QV_OP_LINEAR, self.M, K, N) for (_, K, N) in self.phases]
+                   + [qv.qv_workspace_bytes(qv.QV_OP_LM_HEAD, self.M, h, self.V)])
+        codes = max(al(self.M * K, 16) + al(4 * self.M, 16) for K in [K for (_, K, _) in self.phases] + [h])
+        self.ws_act = torch.zeros(al(gemm, 256) + al(codes, 256), dtype=torch.uint8, device=dev)
         self.graph = None
         torch.cuda.synchronize(dev)
 
@@ -138,8 +142,8 @@ class VerifyStack:
     # ------------------------------------------------------------------ step
     def enqueue(self, stream=None):
         """Enqueue one verify step on `stream` (current stream if None): one
-        qv_w8a8_linear_act per projection (activation quantization fused into
-        the GEMM), qv_lm_head_argmax_act, qv_accept."""
+        qv_w8a8_linear_act per projection (quantization kernel + streaming
+        GEMM), qv_lm_head_argmax_act, qv_accept."""
         M = self.M
         ws = self.ws_act
         for l in range(self.layers):
@@ -173,18 +177,11 @@ class VerifyStack:
 
     def launches_per_step(self, fused: bool = False) -> int:
         """Kernels one step launches. fused: the persistent qv_verify_stack
-        path. Otherwise the per-op path: per projection and for the LM head,
-        one fused kernel when M <= 16 (every shape of the Qwen3 models fits its
-        shared-memory code buffer), else an activation-quantization kernel and
-        one GEMM launch per 64 tokens; plus qv_accept."""
+        path. Otherwise the per-op path: per projection and for the LM head a
+        quantization kernel and one GEMM launch per 64 tokens; plus qv_accept
+        (the same count for enqueue and enqueue_two_call)."""
         if fused:
             return (self.layers * len(self.phases) + 1 + 149) // 150
-        per_gemm = 1 if self.M <= 16 else 1 + (self.M + 63) // 64
-        return (self.layers * len(self.phases) + 1) * per_gemm + 1
-
-    def launches_per_step_two_call(self) -> int:
-        """Kernels of enqueue_two_call: a quantization kernel and one GEMM
-        launch per 64 tokens per projection and for the LM head; qv_accept."""
         return (self.layers * len(self.phases) + 1) * (1 + (self.M + 63) // 64) + 1
 
     # ------------------------------------------------------------------ fused step

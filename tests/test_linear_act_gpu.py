@@ -142,3 +142,27 @@ def test_lm_head_argmax_act_ties(qv, oracle):
     qv.qv_lm_head_argmax_act(x.cuda(), wq.cuda(), sw.cuda(), tok, ws)
     torch.cuda.synchronize()
     assert np.array_equal(np_(tok), t_ref)
+
+
+def test_shared_workspace_across_shapes(qv, oracle):
+    """One buffer for *_act calls of different shapes, sized by the rule in
+    the header (largest GEMM part + largest code part): alternating calls
+    stay exact and leave every GEMM part zero-filled."""
+    al = lambda v, a: (v + a - 1) // a * a
+    shapes = [(5, 12288, 512), (5, 256, 4096), (16, 1024, 1000)]
+    gemm = max(qv.qv_workspace_bytes(qv.QV_OP_LINEAR, M, K, N) for (M, K, N) in shapes)
+    codes = max(al(M * K, 16) + al(4 * M, 16) for (M, K, N) in shapes)
+    ws = torch.zeros(al(gemm, 256) + al(codes, 256), dtype=torch.uint8, device="cuda")
+    cases = []
+    for (M, K, N) in shapes:
+        x, mul, wq, sw = _inputs(M, K, N, torch.bfloat16, True, seed=K + N)
+        q_ref, s_ref = _oracle_codes(oracle, x, mul)
+        y_ref, _ = oracle.w8a8_linear(q_ref, s_ref, np_(wq), np_(sw))
+        cases.append((x.cuda(), mul.cuda(), wq.cuda(), sw.cuda(), y_ref, M, K, N))
+    for rep in range(2):
+        for (xd, md, wd, sd, y_ref, M, K, N) in cases:
+            y = torch.empty(M, N, device="cuda")
+            qv.qv_w8a8_linear_act(xd, wd, sd, y, ws, act_mul=md)
+            torch.cuda.synchronize()
+            assert np.array_equal(np_(y).view(np.uint32), y_ref.view(np.uint32)), (rep, M, K, N)
+            assert int(ws[:gemm].count_nonzero()) == 0
