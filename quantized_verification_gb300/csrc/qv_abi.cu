@@ -113,14 +113,11 @@ qv_status encode_2d(CUtensorMap* map, CUtensorMapDataType dt, size_t elem_bytes,
 }
 
 // W8A8 streaming GEMM kernel by padded token count. Up to 16 tokens the
-// int8 mma.sync kernel keeps pace with HBM; from QV_TC_MIN_MP tokens the
-// tcgen05 kernel (exact f16 widening, TMEM accumulators) is used, whose
-// per-tile cost hardly grows with the token count (measured on GB300).
-#ifndef QV_TC_MIN_MP
-#define QV_TC_MIN_MP 32
-#endif
+// int8 mma.sync kernel keeps pace with HBM; from 32 tokens the tcgen05
+// kernel (exact f16 widening, TMEM accumulators) is used, whose per-tile cost
+// hardly grows with the token count (measured on GB300).
 cudaError_t launch_w8a8(const qv::W8A8Launch& L, int sms, cudaStream_t s) {
-    if (L.MP >= QV_TC_MIN_MP) return qv::launch_w8a8_tc(L, sms, s);
+    if (L.MP >= 32) return qv::launch_w8a8_tc(L, sms, s);
     return qv::launch_w8a8_stream(L, sms, s);
 }
 
