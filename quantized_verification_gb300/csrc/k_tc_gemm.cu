@@ -27,12 +27,15 @@
 //    f16 buffer in the 128-byte-swizzled K-major layout (the B operand);
 //  - warp 8, one thread: issues the tile's eight M=128 x N x K=16 MMAs into a
 //    TMEM accumulator and commits them to an mbarrier;
-//  - the converters read the accumulator back (thread = channel, its half of
-//    the token columns), convert to int32 and accumulate; at the end of a
-//    channel tile's K range they stage the sums in shared memory for the
-//    common epilogue.
-// A, B and the accumulator rotate through four slots, so widening of tile
-// i+1..i+3 overlaps the MMAs of tile i and the readout lags four tiles.
+//  - the MMAs of up to four consecutive tiles of a channel tile (K = 512:
+//    |sum| <= 512 * 128^2 = 2^23, still exact in fp32) accumulate into one of
+//    two TMEM accumulators; the converters read a group's accumulator back
+//    (thread = channel, its half of the token columns) while they widen the
+//    next group, convert to int32 and accumulate; at the end of a channel
+//    tile's K range they stage the sums in shared memory for the common
+//    epilogue.
+// A and B rotate through four slots, so widening of tiles i+1..i+3 overlaps
+// the MMAs of tile i.
 
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -54,8 +57,9 @@ constexpr int kTcConv = 8;          // converter warps 0..7
 constexpr int kTcMmaWarp = 8;       // MMA issue and TMEM allocation
 constexpr int kTcProdWarp = 9;      // TMA producer
 constexpr int kTcThreads = 10 * 32;
-constexpr int kTcRing = 4;          // A / B / accumulator slots
+constexpr int kTcRing = 4;          // A / B slots
 constexpr int kTcACols = 64;        // TMEM columns of one A slot (128 f16 of K per lane)
+constexpr int kTcGroup = 4;         // tiles accumulated in TMEM before a readout
 
 template <int MP>
 struct TcCfg {
@@ -70,9 +74,9 @@ struct TcCfg {
     static constexpr int DCol0 = kTcRing * kTcACols;      // first accumulator column
     static constexpr int TmemCols = 512;
     static constexpr int SmemBytes = 1024 + Stages * StageBytes + kTcRing * BSlot + StgWords * 4 +
-                                     (2 * Stages + 2 * kTcRing) * 8 + kMaxConsumerWarps * MP * 8 +
+                                     (2 * Stages + 2 * kTcRing + 2) * 8 + kMaxConsumerWarps * MP * 8 +
                                      MP * 4 + 64;
-    static_assert(DCol0 + kTcRing * NM <= TmemCols, "TMEM budget");
+    static_assert(DCol0 + 2 * NM <= TmemCols, "TMEM budget");
     static_assert(SmemBytes <= 232448, "shared memory budget");
     static_assert(NM % 16 == 0 && NM <= 256, "MMA N");
 };
@@ -86,7 +90,8 @@ struct TcSmem {
     uint64_t* full;
     uint64_t* empty;
     uint64_t* aready;          // converters -> MMA: A and B of a slot written
-    uint64_t* mdone;           // MMA -> converters: slot's MMAs complete
+    uint64_t* mdone;           // MMA -> converters: slot's MMAs complete (A, B reusable)
+    uint64_t* dfull;           // MMA -> converters: a group's accumulator complete (2)
     unsigned long long* red;   // kMaxConsumerWarps x MP (LM head)
     float* sx;                 // MP
     volatile int* abort;
@@ -110,6 +115,8 @@ struct TcSmem {
         p += kTcRing * 8;
         mdone = reinterpret_cast<uint64_t*>(p);
         p += kTcRing * 8;
+        dfull = reinterpret_cast<uint64_t*>(p);
+        p += 2 * 8;
         red = reinterpret_cast<unsigned long long*>(p);
         p += kMaxConsumerWarps * MP * 8;
         sx = reinterpret_cast<float*>(p);
@@ -122,6 +129,28 @@ struct TcSmem {
     __device__ __forceinline__ uint8_t* x_tile(int s) { return stages + s * C::StageBytes + kWTileBytes; }
     __device__ __forceinline__ uint8_t* b_slot(int j) { return bring + j * C::BSlot; }
 };
+
+// Hot-loop waits of this kernel. With QV_TC_SPIN the waiting thread polls with
+// the non-suspending test_wait instead of try_wait.
+#ifndef QV_TC_SPIN
+#define QV_TC_SPIN 0
+#endif
+__device__ __forceinline__ bool tc_wait(uint64_t* bar, unsigned parity, volatile int* abort) {
+#if QV_TC_SPIN
+    if (mbar_test_wait(bar, parity)) return true;
+    const unsigned long long t0 = global_timer_ns();
+    while (true) {
+        if (mbar_test_wait(bar, parity)) return true;
+        if (*abort) return false;
+        if (global_timer_ns() - t0 > kWaitLimitNs) {
+            *abort = 1;
+            return false;
+        }
+    }
+#else
+    return mbar_wait_bounded(bar, parity, abort);
+#endif
+}
 
 // Wait for an mbarrier phase for at most kWaitLimitNs, whatever the abort
 // flag says (used before releasing tensor memory an MMA may still write).
@@ -158,6 +187,8 @@ w8a8_tc_kernel(const __grid_constant__ CUtensorMap tmap_w,
             mbar_init(&sm.aready[j], kTcConv);
             mbar_init(&sm.mdone[j], 1);
         }
+        mbar_init(&sm.dfull[0], 1);
+        mbar_init(&sm.dfull[1], 1);
         *sm.abort = 0;
         fence_barrier_init();
     }
@@ -187,20 +218,25 @@ w8a8_tc_kernel(const __grid_constant__ CUtensorMap tmap_w,
         // ---------------- MMA issue ----------------
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_f16_f32(128, NM);
+            int gq = -1, pos = kTcGroup;
             for (int c = 0; c < n; ++c) {
                 const int j = c % R;
-                if (!mbar_wait_bounded(&sm.aready[j], (unsigned)(c / R) & 1u, sm.abort))
+                const int i = a + c;
+                if (c == 0 || i % p.KT == 0 || pos == kTcGroup) { ++gq; pos = 0; }
+                if (!mbar_wait_bounded_sleep(&sm.aready[j], (unsigned)(c / R) & 1u, sm.abort, 32))
                     atomicOr(&g_tc_gemm_error, kErrTcWait);
                 tc_fence_after();
                 const uint32_t a_t = tmem + (uint32_t)(j * kTcACols);
-                const uint32_t d_t = tmem + (uint32_t)(C::DCol0 + j * NM);
+                const uint32_t d_t = tmem + (uint32_t)(C::DCol0 + (gq & 1) * NM);
                 const uint32_t b_s = smem_u32(sm.b_slot(j));
 #pragma unroll
                 for (int t = 0; t < 8; ++t)
                     umma_f16_ta(d_t, a_t + (uint32_t)(8 * t),
                                 sw128_kmajor_desc(b_s + (uint32_t)((t >> 2) * NM * 128 + 32 * (t & 3))),
-                                idesc, t > 0 ? 1u : 0u);
+                                idesc, (pos > 0 || t > 0) ? 1u : 0u);
                 umma_commit(&sm.mdone[j]);
+                ++pos;
+                if (c + 1 == n || (i + 1) % p.KT == 0 || pos == kTcGroup) umma_commit(&sm.dfull[gq & 1]);
             }
             // Tensor memory stays allocated until the last MMA has completed.
             if (n > 0 && !mbar_wait_timed(&sm.mdone[(n - 1) % R], (unsigned)((n - 1) / R) & 1u))
@@ -225,20 +261,22 @@ w8a8_tc_kernel(const __grid_constant__ CUtensorMap tmap_w,
 
     int32_t acc[MPH];
     EpiState est;
-    int rd = 0;                              // next local tile whose accumulator is read
-    auto readout = [&](int r) {
-        const int jj = r % R;
-        if (!mbar_wait_bounded(&sm.mdone[jj], (unsigned)(r / R) & 1u, sm.abort))
+    // Group g's accumulator (buffer g & 1) completes on dfull[g & 1], the
+    // (g >> 1)-th phase of that barrier.
+    auto read_group = [&](int g) {
+        if (!tc_wait(&sm.dfull[g & 1], (unsigned)(g >> 1) & 1u, sm.abort))
             atomicOr(&g_tc_gemm_error, kErrTcWait);
         tc_fence_after();
         if (has_tokens) {
             uint32_t v[MPH];
-            tmem_ld<MPH>(lane_base + (uint32_t)(C::DCol0 + jj * NM + h * MPH), v);
+            tmem_ld<MPH>(lane_base + (uint32_t)(C::DCol0 + (g & 1) * NM + h * MPH), v);
             tmem_ld_wait();
 #pragma unroll
             for (int m = 0; m < MPH; ++m) acc[m] += __float2int_rn(__uint_as_float(v[m]));
         }
     };
+    int gq = -1, pos = kTcGroup;             // group of the current tile, position in it
+    int rq = 0;                              // next group to read out
 
     int i = a;
     while (i < b) {
@@ -251,39 +289,66 @@ w8a8_tc_kernel(const __grid_constant__ CUtensorMap tmap_w,
         for (; i < seg_end; ++i) {
             const int c = i - a;
             const int s = c % Stages, j = c % R;
-            if (!mbar_wait_bounded(&sm.full[s], (unsigned)(c / Stages) & 1u, sm.abort))
+            if (c == 0 || i % p.KT == 0 || pos == kTcGroup) { ++gq; pos = 0; }
+            if (!tc_wait(&sm.full[s], (unsigned)(c / Stages) & 1u, sm.abort))
                 atomicOr(&g_tc_gemm_error, kErrFullWait);
-            // Slot j is free once the MMAs of tile c - R have completed (their
-            // accumulator is read here too).
-            while (rd <= c - R) readout(rd++);
+            // Slot j is free once the MMAs of tile c - R have completed.
+            if (c >= R && !tc_wait(&sm.mdone[j], (unsigned)((c - R) / R) & 1u, sm.abort))
+                atomicOr(&g_tc_gemm_error, kErrTcWait);
+            // The previous group of this channel tile is read at the third
+            // tile of the current group (two tiles after its last MMAs were
+            // released, so they are normally complete); its buffer is written
+            // again by the next group, so a group start reads anything older.
+            if (pos == 0)
+                while (rq < gq - 1) read_group(rq++);
+            else if (pos == 2)
+                while (rq < gq) read_group(rq++);
+            ++pos;
 
-            // A: this thread's 64 weight bytes -> 32 f16x2 words in its TMEM lane.
+            // All shared-memory loads of the tile first (this thread's 64 weight
+            // bytes, its share of the activation codes), then the widening.
             const uint8_t* wrow = sm.w_tile(s) + row * BKB;
+            uint4 wv[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                wv[u] = *reinterpret_cast<const uint4*>(wrow + (((4 * h + u) ^ (row & 7)) << 4));
+            constexpr int XI = (MP * 8 + kTcConv * 32 - 1) / (kTcConv * 32);   // items per thread
+            uint4 xv[XI];
+#pragma unroll
+            for (int q = 0; q < XI; ++q) {
+                const int e = tid + q * kTcConv * 32;
+                const int xr = e >> 3, xc = e & 7;
+                xv[q] = e < MP * 8 ? *reinterpret_cast<const uint4*>(sm.x_tile(s) + xr * BKB + ((xc ^ (xr & 7)) << 4))
+                                   : make_uint4(0u, 0u, 0u, 0u);
+            }
+            // A: 32 f16x2 words into this thread's TMEM lane.
             uint32_t av[32];
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-                const uint4 wv = *reinterpret_cast<const uint4*>(wrow + (((4 * h + u) ^ (row & 7)) << 4));
-                widen_i8x4_f16(wv.x, av[8 * u + 0], av[8 * u + 1]);
-                widen_i8x4_f16(wv.y, av[8 * u + 2], av[8 * u + 3]);
-                widen_i8x4_f16(wv.z, av[8 * u + 4], av[8 * u + 5]);
-                widen_i8x4_f16(wv.w, av[8 * u + 6], av[8 * u + 7]);
+                widen_i8x4_f16(wv[u].x, av[8 * u + 0], av[8 * u + 1]);
+                widen_i8x4_f16(wv[u].y, av[8 * u + 2], av[8 * u + 3]);
+                widen_i8x4_f16(wv[u].z, av[8 * u + 4], av[8 * u + 5]);
+                widen_i8x4_f16(wv[u].w, av[8 * u + 6], av[8 * u + 7]);
             }
             tmem_st_x32(lane_base + (uint32_t)(j * kTcACols + 32 * h), av);
 
             // B: the MP x 128 activation codes -> f16, 128-byte swizzled K-major.
             uint8_t* bs = sm.b_slot(j);
-            for (int e = tid; e < MP * 8; e += kTcConv * 32) {
-                const int xr = e >> 3, xc = e & 7;
-                const uint4 xv = *reinterpret_cast<const uint4*>(sm.x_tile(s) + xr * BKB + ((xc ^ (xr & 7)) << 4));
-                uint4 lo, hi;
-                widen_i8x4_f16(xv.x, lo.x, lo.y);
-                widen_i8x4_f16(xv.y, lo.z, lo.w);
-                widen_i8x4_f16(xv.z, hi.x, hi.y);
-                widen_i8x4_f16(xv.w, hi.z, hi.w);
-                uint8_t* brow = bs + (xc >> 2) * NM * 128 + xr * 128;
-                const int c0 = 2 * (xc & 3);
-                *reinterpret_cast<uint4*>(brow + ((c0 ^ (xr & 7)) << 4)) = lo;
-                *reinterpret_cast<uint4*>(brow + (((c0 + 1) ^ (xr & 7)) << 4)) = hi;
+#pragma unroll
+            for (int q = 0; q < XI; ++q) {
+                const int e = tid + q * kTcConv * 32;
+                if (e < MP * 8) {
+                    const int xr = e >> 3, xc = e & 7;
+                    uint4 lo, hi;
+                    widen_i8x4_f16(xv[q].x, lo.x, lo.y);
+                    widen_i8x4_f16(xv[q].y, lo.z, lo.w);
+                    widen_i8x4_f16(xv[q].z, hi.x, hi.y);
+                    widen_i8x4_f16(xv[q].w, hi.z, hi.w);
+                    uint8_t* brow = bs + (xc >> 2) * NM * 128 + xr * 128;
+                    const int c0 = 2 * (xc & 3);
+                    *reinterpret_cast<uint4*>(brow + ((c0 ^ (xr & 7)) << 4)) = lo;
+                    *reinterpret_cast<uint4*>(brow + (((c0 + 1) ^ (xr & 7)) << 4)) = hi;
+                }
             }
             tmem_st_wait();
             fence_proxy_async_smem();
@@ -295,7 +360,7 @@ w8a8_tc_kernel(const __grid_constant__ CUtensorMap tmap_w,
             }
         }
         // Segment end: read the remaining accumulators of this channel tile.
-        while (rd < i - a) readout(rd++);
+        while (rq <= gq) read_group(rq++);
 
         if (has_tokens) {
 #pragma unroll

@@ -95,6 +95,24 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, unsigned parity
     }
 }
 
+// mbar_wait_bounded for a single thread that shares its SM sub-partition with
+// compute warps (a producer or an MMA issuer): between probes it sleeps for
+// about sleep_ns, so that its polling does not take their issue slots.
+__device__ __forceinline__ bool mbar_wait_bounded_sleep(uint64_t* bar, unsigned parity,
+                                                        volatile int* abort, unsigned sleep_ns) {
+    if (mbar_test_wait(bar, parity)) return true;
+    unsigned long long t0 = global_timer_ns();
+    while (true) {
+        __nanosleep(sleep_ns);
+        if (mbar_test_wait(bar, parity)) return true;
+        if (*abort) return false;
+        if (global_timer_ns() - t0 > kWaitLimitNs) {
+            *abort = 1;
+            return false;
+        }
+    }
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];"

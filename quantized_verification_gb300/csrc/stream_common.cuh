@@ -77,7 +77,7 @@ __device__ __forceinline__ void produce(unsigned* err, SM& sm, const CUtensorMap
     int s = pre % Stages;
     int round = pre / Stages;
     for (int j = pre; j < n; ++j) {
-        if (!mbar_wait_bounded(&sm.empty[s], (round - 1) & 1, sm.abort)) {
+        if (!mbar_wait_bounded_sleep(&sm.empty[s], (round - 1) & 1, sm.abort, 64)) {
             atomicOr(err, kErrEmptyWait);
             break;
         }

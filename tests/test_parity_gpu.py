@@ -347,3 +347,23 @@ def test_cuda_graph_replay_matches(qv, oracle):
 
 def test_device_error_word_clear(qv):
     assert qv.qv_device_error() == 0
+
+
+# More stream-K splits at up to 8 tokens: channel tiles split over 1, 2 and
+# many CTAs, whole tiles per CTA, ragged K blocks and ragged N.
+SPLIT_CASES = [
+    (5, 4096, 100), (5, 1040, 2432), (5, 4096, 4096), (8, 4096, 6144), (3, 2064, 24576 + 16),
+    (5, 12288, 4096), (1, 16, 33), (7, 12288, 3000),
+]
+
+
+@pytest.mark.parametrize("M,K,N", SPLIT_CASES)
+def test_w8a8_linear_split_schedules(qv, oracle, M, K, N):
+    xq = rand_codes((M, K), seed=M * 31 + K)
+    wq = rand_codes((N, K), seed=N * 7 + K)
+    sx = rand_scales(M, seed=M + 50, lo=1e-3, hi=0.2)
+    sw = rand_scales(N, seed=N + 60)
+    y, acc = _run_linear(qv, xq, sx, wq, sw)
+    y_ref, acc_ref = oracle.w8a8_linear(np_(xq), np_(sx), np_(wq), np_(sw))
+    assert np.array_equal(np_(acc), acc_ref)
+    assert np.array_equal(np_(y).view(np.uint32), y_ref.view(np.uint32))
