@@ -25,6 +25,7 @@ import torch
 
 QWEN3_8B = {"hidden": 4096, "kv": 1024, "ffn": 12288, "layers": 36, "vocab": 151936}
 QWEN3_32B = {"hidden": 5120, "q": 8192, "kv": 1024, "ffn": 25600, "layers": 64, "vocab": 151936}
+MODELS = {"qwen3-8b": QWEN3_8B, "qwen3-32b": QWEN3_32B}
 
 
 def layer_projections(model: dict) -> list[tuple[str, int, int]]:
@@ -102,5 +103,5 @@ def expected_accept_len(p: float, gamma: int) -> float:
     return 1.0 + sum(p ** i for i in range(1, gamma + 1))
 
 
-__all__ = ["QWEN3_8B", "QWEN3_32B", "layer_projections", "subseed", "activations", "weights",
+__all__ = ["QWEN3_8B", "QWEN3_32B", "MODELS", "layer_projections", "subseed", "activations", "weights",
            "uniform_tokens", "geometric_drafts", "expected_accept_len"]
