@@ -266,7 +266,7 @@ def main():
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
 
-    from quantized_verification_gb300 import build, qv, synth
+    from quantized_verification_gb300 import build, qv, replicas, synth
     from quantized_verification_gb300.stack import VerifyStack
     build.build()
 
@@ -313,20 +313,14 @@ def main():
     cvd = os.environ.get("CUDA_VISIBLE_DEVICES")
     clocks = ClockSampler(cvd.split(",")[local].strip() if cvd else str(local))
     clocks.start()
-    if world > 1:
-        dist.barrier()
+    replicas.barrier()
     torch.cuda.synchronize()
     w0 = time.time()
     ms = time_graph(torch, step_graph, args.steps, stream)
     w1 = time.time()
-    if world > 1:
-        dist.barrier()
+    replicas.barrier()
     clocks.stop()
-    ms_t = torch.tensor([ms], device=dev)
-    if world > 1:
-        dist.all_reduce(ms_t, op=dist.ReduceOp.MAX)
-    ms_max = float(ms_t.item())
-    value = world * stack.M / (ms_max / 1e3)
+    ms_max, value = replicas.job_step_time_and_rate(ms, stack.M, dev)
     clk = clocks.summary(w0, w1)
     alg_bytes = stack.algorithmic_bytes()
     log(f"step {ms:.4f} ms ({alg_bytes / (ms * 1e-3) / 1e9:.1f} GB/s algorithmic), clocks {clk}")

@@ -59,14 +59,16 @@ def main(argv=None):
     ap.add_argument("--model", default="qwen3-32b", choices=sorted(synth.MODELS))
     ap.add_argument("--m", default="1,2,4,8,16,32,64,128,256")
     ap.add_argument("--reps", type=int, default=24)
+    ap.add_argument("--shapes", default="qkv,o,gate_up,down,lm_head", help="projections to time")
     args = ap.parse_args(argv)
     build.build()
     model = synth.MODELS[args.model]
     ms = [int(v) for v in args.m.split(",")]
     dev = torch.device("cuda")
-    print(f"| shape (K -> N) | M | W8A8 us | W8A8 GB/s | BF16 us | BF16 GB/s | speed-up |")
-    print(f"|---|---|---|---|---|---|---|")
-    for name, K, N in shapes(model):
+    print("| shape (K -> N) | M | W8A8 us | W8A8 GB/s | BF16 us | BF16 GB/s | speed-up |")
+    print("|---|---|---|---|---|---|---|")
+    wanted = set(args.shapes.split(","))
+    for name, K, N in [t for t in shapes(model) if t[0] in wanted]:
         copies = max(2, -(-2 * L2_BYTES // (2 * N * K)))        # bf16 copies exceed 2 x L2
         wb = [synth.weights(N, K, synth.subseed(11, "msweep", name, c), device=dev) for c in range(copies)]
         wq = [torch.empty(N, K, dtype=torch.int8, device=dev) for _ in range(copies)]
