@@ -88,13 +88,25 @@ quantize_rows_kernel(const uint8_t* __restrict__ x, int K, const float* __restri
     using V = Vec<BF16>;
     constexpr int E = V::E;
     if (early_dependents) allow_dependent_launch();
-    grid_dependency_wait();
 
     const int row = blockIdx.x;
     const int tid = threadIdx.x;
     const int nvec = K / E;
     const bool in_regs = nvec <= kQuantThreads * kQuantRegVecs;
     const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)row * K * (BF16 ? 2 : 4));
+    // Bring the row (and the multipliers) into L2 while the preceding kernel
+    // finishes. A prefetch returns nothing to the SM, and L2 is the point of
+    // coherence, so it cannot observe data older than the dependency wait.
+    if (in_regs) {
+        for (int v = tid * 8; v < nvec; v += kQuantThreads * 8) {   // one 128-byte line per 8 vectors
+            asm volatile("prefetch.global.L2 [%0];" :: "l"(xr + v));
+            if (mul) {   // 8 vectors of multipliers span 8 * E * 4 bytes: one or two lines
+                asm volatile("prefetch.global.L2 [%0];" :: "l"(mul + (size_t)v * E));
+                if (E == 8) asm volatile("prefetch.global.L2 [%0];" :: "l"(mul + (size_t)v * E + 32));
+            }
+        }
+    }
+    grid_dependency_wait();
 
     uint4 rv[kQuantRegVecs];
     float amax = 0.f;
