@@ -39,7 +39,11 @@ FALLBACK_HBM_GBS = 6800.0
 # DRAM bytes per algorithmic byte of the dominant kernel from one ncu capture,
 # valid only for the kernel source it was taken on (sha256 of
 # csrc/k_stream_gemm.cu); traffic is reported as null otherwise.
-NCU_TRAFFIC = {"source_sha256": None, "dram_bytes_per_algorithmic_byte": None}
+# DRAM bytes per algorithmic byte of one projection launch of the streaming
+# W8A8 kernel, from an ncu capture of the gate+up launch (see
+# profiles/launches_qwen3_8b_1layer_m5.md), valid for these kernel sources.
+NCU_TRAFFIC = {"source_sha256": "6e9a6f871dde15dff7ab3d81160137a019c5be2b252e58d73649bbc6a2232cd2",
+               "dram_bytes_per_algorithmic_byte": (102247168 + 2811648) / 101273620}
 
 
 def log(*a):
@@ -224,8 +228,12 @@ def read_peaks():
 
 
 def kernel_source_sha():
-    with open(os.path.join(ROOT, "quantized_verification_gb300", "csrc", "k_stream_gemm.cu"), "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()
+    """Hash of the sources the streaming W8A8 kernel is compiled from."""
+    h = hashlib.sha256()
+    for name in ("k_stream_gemm.cu", "stream_common.cuh", "qv_ptx.cuh", "qv_internal.h"):
+        with open(os.path.join(ROOT, "quantized_verification_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
 
 
 def time_graph(torch, graph, n, stream):
