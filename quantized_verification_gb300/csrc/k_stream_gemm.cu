@@ -1160,9 +1160,10 @@ cudaError_t launch_w8a8_stream(const W8A8Launch& a, int num_sms, cudaStream_t s)
                   : launch_ex(w8a8_stream_kernel<NGV, (int)Epi::Linear>, grid,               \
                               (kW8A8Warps + 1) * 32, Cfg<NGV>::SmemBytes, s, a.tmap_w,       \
                               a.tmap_x, p);
-    switch (a.MP / 8) {   // up to 16 tokens; more go to the tcgen05 kernel
+    switch (a.MP / 8) {   // up to 32 tokens; more go to the tcgen05 kernel
         QV_W8A8_CASE(1)
         QV_W8A8_CASE(2)
+        QV_W8A8_CASE(4)
         default: return cudaErrorInvalidValue;
     }
 #undef QV_W8A8_CASE

@@ -419,10 +419,7 @@ cudaError_t launch_w8a8_tc(const W8A8Launch& a, int num_sms, cudaStream_t s) {
                               s, a.tmap_w, a.tmap_x, p)                                           \
                   : launch_tc(w8a8_tc_kernel<MPV, (int)Epi::Linear>, grid, TcCfg<MPV>::SmemBytes, \
                               s, a.tmap_w, a.tmap_x, p);
-    switch (a.MP) {
-        QV_TC_CASE(8)
-        QV_TC_CASE(16)
-        QV_TC_CASE(32)
+    switch (a.MP) {   // fewer tokens go to the mma.sync streaming kernel
         QV_TC_CASE(64)
         default: return cudaErrorInvalidValue;
     }

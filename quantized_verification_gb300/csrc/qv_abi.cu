@@ -112,16 +112,17 @@ qv_status encode_2d(CUtensorMap* map, CUtensorMapDataType dt, size_t elem_bytes,
     return QV_OK;
 }
 
-// W8A8 streaming GEMM kernel by padded token count. Up to 16 tokens the
-// int8 mma.sync kernel keeps pace with HBM; from 32 tokens the tcgen05
-// kernel (exact f16 widening, TMEM accumulators) is used, whose per-tile cost
-// hardly grows with the token count (measured on GB300).
+// W8A8 streaming GEMM kernel by padded token count. Up to 32 tokens the
+// int8 mma.sync kernel keeps pace with HBM (at 32 tokens it is still 10-15 %
+// faster than the tcgen05 kernel on every Qwen3-8B projection); at 64 tokens
+// mma.sync is compute-bound and the tcgen05 kernel (exact f16 widening, TMEM
+// accumulators), whose per-tile cost hardly grows with the token count, takes
+// over (measured on GB300).
 cudaError_t launch_w8a8(const qv::W8A8Launch& L, int sms, cudaStream_t s) {
-    if (L.MP >= 32) return qv::launch_w8a8_tc(L, sms, s);
+    if (L.MP >= 64) return qv::launch_w8a8_tc(L, sms, s);
     return qv::launch_w8a8_stream(L, sms, s);
 }
 
-// Padded token count of one streaming-GEMM launch for Mc rows: 8, 16, 32 or 64.
 int mp_for(int mc) {
     const int p = qv::pad_tokens(mc);
     return p <= 8 ? 8 : p <= 16 ? 16 : p <= 32 ? 32 : 64;

@@ -1,8 +1,7 @@
-"""qv_w8a8_linear_act / qv_lm_head_argmax_act (activation quantization fused
-into the streaming GEMM) against the oracle chain quantize_rows -> w8a8_linear
-/ lm_head_argmax, bit for bit, and against the two-call GPU path. Covers both
-the fused kernel (M <= 16) and the materialised-codes route (M > 16, or a
-per-CTA code buffer larger than shared memory)."""
+"""qv_w8a8_linear_act / qv_lm_head_argmax_act (activation quantization kernel,
+then the streaming GEMM, in one call) against the oracle chain quantize_rows -> w8a8_linear
+/ lm_head_argmax, bit for bit, and against the two-call GPU path. Covers the
+int8 mma.sync GEMM (up to 32 padded tokens) and the tcgen05 GEMM (64)."""
 import numpy as np
 import pytest
 import torch
@@ -55,8 +54,8 @@ LINEAR_ACT_CASES = [
     (9, 512, 384, torch.bfloat16, True),
     (16, 12288, 512, torch.bfloat16, True),
     (5, 12288, 4096, torch.bfloat16, True),
-    (17, 256, 200, torch.bfloat16, True),     # codes materialised (M > 16)
-    (64, 1024, 256, torch.float32, True),     # materialised, tcgen05 GEMM
+    (17, 256, 200, torch.bfloat16, True),     # 32 padded tokens, mma.sync GEMM
+    (64, 1024, 256, torch.float32, True),     # tcgen05 GEMM
 ]
 
 
@@ -87,10 +86,10 @@ def test_w8a8_linear_act(qv, oracle, M, K, N, dtype, smooth):
     assert np.array_equal(np_(y2).view(np.uint32), y_ref.view(np.uint32))
 
 
-def test_w8a8_linear_act_code_buffer_limit(qv, oracle):
-    """M = 16 with 60 K-tiles per CTA: the per-CTA code buffer no longer fits
-    beside the weight ring, so the call takes the materialised route; 59
-    tiles per CTA still run fused. Both must match the oracle."""
+def test_w8a8_linear_act_long_ranges(qv, oracle):
+    """M = 16, K = 8192 at 140 and 141 channel tiles: each CTA's stream-K
+    range spans about 59 or 60 K-tiles and crosses channel-tile boundaries
+    part-way through K. Both must match the oracle."""
     M, K = 16, 8192
     for N in (128 * 140, 128 * 141):
         x, mul, wq, sw = _inputs(M, K, N, torch.bfloat16, True, seed=N)

@@ -80,6 +80,7 @@ LINEAR_CASES = [
     (4, 256, 512), (1, 128, 128), (5, 4096, 1024), (5, 272, 1000), (8, 1024, 130),
     (9, 512, 384), (16, 384, 256), (17, 256, 200), (32, 640, 256), (33, 256, 129),
     (64, 512, 256), (65, 256, 128), (80, 512, 300), (256, 256, 136), (5, 16, 7),
+    (24, 4096, 4096), (32, 12288, 3000),
 ]
 
 
@@ -112,13 +113,14 @@ def test_w8a8_linear(qv, oracle, M, K, N):
     assert np.array_equal(bf16_bits(yb), oracle.f32_to_bf16(y_ref))
 
 
-@pytest.mark.parametrize("M", [3, 40])
+@pytest.mark.parametrize("M", [3, 24, 40])
 @pytest.mark.parametrize("K,with_m128", [((133144 // 16) * 16, False), (4096, True)])
 def test_w8a8_extreme_magnitudes(qv, oracle, M, K, with_m128):
     """Codes at the ends of the range. The first case is the largest K that is
     a multiple of 16 and keeps every +-127 sum inside int32; -128 codes are
-    exercised at a K where their sums fit as well. M = 3 runs the int8
-    mma.sync kernel, M = 40 the tcgen05 kernel (rows 3.. repeat rows 0..2)."""
+    exercised at a K where their sums fit as well. M = 3 and M = 24 run the
+    int8 mma.sync kernel (8 and 32 padded tokens), M = 40 the tcgen05 kernel
+    (rows 3.. repeat rows 0..2)."""
     N = 130
     xq = torch.full((M, K), 127, dtype=torch.int8)
     xq[1::3] = -127
@@ -166,7 +168,7 @@ def test_w8a8_quantize_chain(qv, oracle):
 # a3 LM head + argmax
 # ---------------------------------------------------------------------------
 LM_CASES = [(4, 256, 1024), (5, 4096, 3000), (1, 128, 130), (9, 256, 1000), (64, 256, 513),
-            (80, 128, 777), (5, 512, 128 * 160 + 3)]
+            (80, 128, 777), (5, 512, 128 * 160 + 3), (32, 4096, 3000), (24, 512, 128 * 160 + 3)]
 
 
 def _run_lm(qv, xq, sx, wq, sw):
