@@ -254,9 +254,10 @@ QV_API qv_status qv_quantize_weight(const void* w, qv_dtype w_dtype, int N, int 
  *   M*1B/BW).
  *   x [M*K] bf16, w [N*K] bf16, y [M*N] fp32 out.
  *   workspace: qv_workspace_bytes(QV_OP_BF16_LINEAR, M, K, N) bytes, same
- *   zero-fill contract as qv_w8a8_linear. Partial sums of one output are
- *   added in an order that may change from call to call, so results may
- *   differ in the last bits between calls.
+ *   zero-fill contract as qv_w8a8_linear. The fp32 partial sums of one
+ *   output (one per CTA its K range is split over) are added in K order; the
+ *   split depends only on the shape and the SM count, so repeated calls on
+ *   one GPU give identical results.
  *   1 <= M <= QV_MAX_M.
  */
 QV_API qv_status qv_bf16_linear(const uint16_t* x, int M, int K, const uint16_t* w,
@@ -338,7 +339,7 @@ QV_API qv_status qv_device_error(unsigned int* code);
 QV_API int qv_num_sms(void);
 
 /* Bytes of the library's built-in scratch buffer (see qv_w8a8_linear_noalloc). */
-#define QV_NOALLOC_SCRATCH_BYTES (4u << 20)
+#define QV_NOALLOC_SCRATCH_BYTES (16u << 20)
 
 /*
  * qv_w8a8_linear_noalloc -- qv_w8a8_linear for callers that cannot allocate
@@ -358,8 +359,9 @@ QV_API int qv_num_sms(void);
  *   - The first call on a device looks up the buffer's device address for
  *     that device (once); make that first call before any stream capture.
  *   - Shapes whose workspace, qv_workspace_bytes(QV_OP_LINEAR, M, K, N), is
- *     larger than the buffer are rejected with QV_ERR_UNSUPPORTED (about
- *     N <= 131000 at M <= 8, N <= 16000 at M = 64).
+ *     larger than the buffer are rejected with QV_ERR_UNSUPPORTED. With the
+ *     present workspace layout (split-K slots of at most 10.5 MB, at M > 32)
+ *     every shape that qv_w8a8_linear accepts fits.
  *   - Each call clears the part of the buffer it uses (cudaMemsetAsync on
  *     `stream`) before its kernel runs. All calls on a device share the one
  *     buffer: calls whose GPU work overlaps (different streams, no ordering

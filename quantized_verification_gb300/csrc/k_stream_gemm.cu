@@ -346,7 +346,7 @@ w8a8_stream_kernel(const __grid_constant__ CUtensorMap tmap_w,
         }
         consumer_sync<CW>();
 
-        segment_end<MP, CW, EPI>(sm, p, nt, seg_end - seg_begin, i >= b, tid, est);
+        segment_end<MP, CW, EPI>(sm, p, nt, seg_begin, seg_end - seg_begin, tid, est, &g_stream_gemm_error);
     }
     range_end<MP, CW, EPI>(sm, p, tid, est);
 }
@@ -359,8 +359,7 @@ struct Bf16Params {
     int M, N, K, KT, NT;
     long long T;
     float* y;
-    float* ws_acc;
-    unsigned* ws_cnt;
+    unsigned long long* slots;   // split-K partials (fp32 bits), one slot per CTA
 };
 
 template <int NG>
@@ -472,34 +471,21 @@ bf16_stream_kernel(const __grid_constant__ CUtensorMap tmap_w,
             }
         }
         consumer_sync<CW>();
-        const int seg_len = seg_end - seg_begin;
-        const bool whole = seg_len == p.KT;
-        float* gacc = p.ws_acc + (size_t)nt * BN * MP;
-        if (!whole) {
-            for (int e = tid; e < BN * MP; e += CT) {
-                const int r = e / MP, m = e - (e / MP) * MP;
-                if (m < p.M && nt * BN + r < p.N) atomicAdd(&gacc[e], stgf[e]);
+        // split tiles combine through per-CTA slots, as in the W8A8 kernels;
+        // the head's CTA sums the partials in K order
+        if (seg_end - seg_begin != p.KT) {
+            if (seg_begin != nt * p.KT) {
+                publish_partial<MP, CW>(sm, p.slots, p.M, tid);
+                consumer_sync<CW>();
+                continue;
             }
-            __threadfence();
-            consumer_sync<CW>();
-            if (tid == 0) {
-                __threadfence();
-                const unsigned prev = atomicAdd(&p.ws_cnt[nt], (unsigned)seg_len);
-                *sm.flag = (prev + (unsigned)seg_len == (unsigned)p.KT) ? 1 : 0;
-            }
+            gather_partials<MP, CW, true>(sm, p.slots, p.M, p.T, p.KT, nt, tid, &g_stream_gemm_error);
             consumer_sync<CW>();
         }
-        if (whole || *sm.flag) {
-            if (!whole) __threadfence();
-            const int r = tid;
-            const int n = nt * BN + r;
-            if (r < BN && n < p.N) {
-                for (int m = 0; m < p.M; ++m) {
-                    const float v = whole ? stgf[r * MP + m] : atomicExch(&gacc[r * MP + m], 0.f);
-                    p.y[(size_t)m * p.N + n] = v;
-                }
-            }
-            if (!whole && tid == 0) atomicExch(&p.ws_cnt[nt], 0u);
+        const int r = tid;
+        const int n = nt * BN + r;
+        if (r < BN && n < p.N) {
+            for (int m = 0; m < p.M; ++m) p.y[(size_t)m * p.N + n] = stgf[r * MP + m];
         }
         consumer_sync<CW>();
     }
@@ -1120,14 +1106,17 @@ verify_stack_kernel(const __grid_constant__ StackParams sp) {
 
 }  // namespace
 
-WsLayout ws_layout(int mp, int n, bool lm_head) {
+WsLayout ws_layout(int mp, int n, bool lm_head, bool stack) {
     WsLayout L;
     const int nt = ceil_div(n, BN);
     auto al16 = [](size_t v) { return (v + 15) & ~size_t(15); };
-    L.acc = 0;
-    size_t off = al16((size_t)nt * BN * mp * 4);
+    size_t off = 0;
+    L.slots = off;
+    if (!stack) off = al16(off + (size_t)kMaxStreamCtas * BN * mp * 8);
+    L.acc = off;
+    if (stack) off = al16(off + (size_t)nt * BN * mp * 4);
     L.counters = off;
-    off = al16(off + (size_t)nt * 4);
+    if (stack) off = al16(off + (size_t)nt * 4);
     L.keys = off;
     if (lm_head) off = al16(off + (size_t)mp * 8);
     L.done = off;
@@ -1147,11 +1136,10 @@ cudaError_t launch_w8a8_stream(const W8A8Launch& a, int num_sms, cudaStream_t s)
     p.sx = a.sx; p.sw = a.sw; p.y = a.y; p.y_bf16 = a.y_bf16; p.acc_debug = a.acc_debug;
     p.tokens = a.tokens; p.max_logit = a.max_logit;
     uint8_t* ws = static_cast<uint8_t*>(a.ws);
-    p.ws_acc = reinterpret_cast<int32_t*>(ws + L.acc);
-    p.ws_cnt = reinterpret_cast<unsigned*>(ws + L.counters);
+    p.slots = reinterpret_cast<unsigned long long*>(ws + L.slots);
     p.keys = reinterpret_cast<unsigned long long*>(ws + L.keys);
     p.done = reinterpret_cast<unsigned*>(ws + L.done);
-    const int grid = (int)(p.T < num_sms ? p.T : num_sms);
+    const int grid = stream_grid(p.T, num_sms);
 #define QV_W8A8_CASE(NGV)                                                                    \
     case NGV:                                                                                \
         return lm ? launch_ex(w8a8_stream_kernel<NGV, (int)Epi::LmHead>, grid,               \
@@ -1179,9 +1167,8 @@ cudaError_t launch_bf16_stream(const Bf16Launch& a, int num_sms, cudaStream_t s)
     p.T = (long long)p.KT * p.NT;
     p.y = a.y;
     uint8_t* ws = static_cast<uint8_t*>(a.ws);
-    p.ws_acc = reinterpret_cast<float*>(ws + L.acc);
-    p.ws_cnt = reinterpret_cast<unsigned*>(ws + L.counters);
-    const int grid = (int)(p.T < num_sms ? p.T : num_sms);
+    p.slots = reinterpret_cast<unsigned long long*>(ws + L.slots);
+    const int grid = stream_grid(p.T, num_sms);
 #define QV_BF16_CASE(NGV) \
     case NGV: return launch_ex(bf16_stream_kernel<NGV>, grid, (kBf16Warps + 1) * 32, Cfg<NGV>::SmemBytes, s, a.tmap_w, a.tmap_x, p);
     switch (NG) {
@@ -1213,7 +1200,7 @@ cudaError_t launch_verify_stack(const StackLaunch& a, int num_sms, cudaStream_t 
     sp.B = a.B; sp.gamma = a.gamma; sp.draft = a.draft;
     sp.tokens = a.tokens; sp.max_logit = a.max_logit;
     sp.accept_len = a.accept_len; sp.out_tokens = a.out_tokens;
-    WsLayout L = ws_layout(a.MP, a.n_max, true);
+    WsLayout L = ws_layout(a.MP, a.n_max, true, true);
     uint8_t* ws = static_cast<uint8_t*>(a.ws);
     sp.ws_acc = reinterpret_cast<int32_t*>(ws + L.acc);
     sp.ws_cnt = reinterpret_cast<unsigned*>(ws + L.counters);
@@ -1251,7 +1238,7 @@ cudaError_t launch_verify_stack(const StackLaunch& a, int num_sms, cudaStream_t 
 }
 
 size_t stack_xq_offset(int mp, int n_max) {
-    return (ws_layout(mp, n_max, true).total + 255) & ~size_t(255);
+    return (ws_layout(mp, n_max, true, true).total + 255) & ~size_t(255);
 }
 
 size_t stack_ws_bytes(int mp, int M, int n_max, int kmax) {

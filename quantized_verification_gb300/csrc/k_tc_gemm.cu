@@ -370,7 +370,7 @@ w8a8_tc_kernel(const __grid_constant__ CUtensorMap tmap_w,
             }
         }
         consumer_sync<kTcConv>();
-        segment_end<MP, kTcConv, EPI>(sm, p, nt, seg_end - seg_begin, i >= b, tid, est);
+        segment_end<MP, kTcConv, EPI>(sm, p, nt, seg_begin, seg_end - seg_begin, tid, est, &g_tc_gemm_error);
     }
     range_end<MP, kTcConv, EPI>(sm, p, tid, est);
     tc_fence_before();
@@ -408,11 +408,10 @@ cudaError_t launch_w8a8_tc(const W8A8Launch& a, int num_sms, cudaStream_t s) {
     p.sx = a.sx; p.sw = a.sw; p.y = a.y; p.y_bf16 = a.y_bf16; p.acc_debug = a.acc_debug;
     p.tokens = a.tokens; p.max_logit = a.max_logit;
     uint8_t* ws = static_cast<uint8_t*>(a.ws);
-    p.ws_acc = reinterpret_cast<int32_t*>(ws + L.acc);
-    p.ws_cnt = reinterpret_cast<unsigned*>(ws + L.counters);
+    p.slots = reinterpret_cast<unsigned long long*>(ws + L.slots);
     p.keys = reinterpret_cast<unsigned long long*>(ws + L.keys);
     p.done = reinterpret_cast<unsigned*>(ws + L.done);
-    const int grid = (int)(p.T < num_sms ? p.T : num_sms);
+    const int grid = stream_grid(p.T, num_sms);
 #define QV_TC_CASE(MPV)                                                                           \
     case MPV:                                                                                     \
         return lm ? launch_tc(w8a8_tc_kernel<MPV, (int)Epi::LmHead>, grid, TcCfg<MPV>::SmemBytes, \

@@ -20,13 +20,23 @@ constexpr int kMaxMPerLaunch = 64;
 inline int ceil_div(long long a, long long b) { return (int)((a + b - 1) / b); }
 inline int pad_tokens(int m) { return ((m + 7) / 8) * 8; }
 
-// Workspace layout of one streaming-GEMM call (all offsets in bytes, 16-byte
-// aligned): [acc: Npad*MP 4-byte words][tile counters: NT words][keys: MP
-// 8-byte words][done counter].
+// Most CTAs of one streaming-GEMM launch (one per SM, at most this many);
+// the workspace holds one split-K slot per CTA.
+constexpr int kMaxStreamCtas = 160;
+inline int stream_grid(long long tiles, int num_sms) {
+    long long g = tiles < num_sms ? tiles : num_sms;
+    return (int)(g < kMaxStreamCtas ? g : kMaxStreamCtas);
+}
+
+// Workspace layout of one GEMM call (all offsets in bytes, 16-byte aligned).
+// Streaming kernels (stack = false): [slots: kMaxStreamCtas x 128 x MP
+// 8-byte words][keys: MP 8-byte words][done counter]. Persistent stack
+// (stack = true): [acc: Npad*MP 4-byte words][tile counters: NT words]
+// [keys][done].
 struct WsLayout {
-    size_t acc = 0, counters = 0, keys = 0, done = 0, total = 0;
+    size_t slots = 0, acc = 0, counters = 0, keys = 0, done = 0, total = 0;
 };
-WsLayout ws_layout(int mp, int n, bool lm_head);
+WsLayout ws_layout(int mp, int n, bool lm_head, bool stack = false);
 
 enum class Epi : int { Linear = 0, LmHead = 1 };
 

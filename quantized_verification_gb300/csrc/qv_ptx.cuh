@@ -20,6 +20,7 @@ constexpr unsigned kErrEmptyWait = 2u;   // producer waited too long for a slot
 constexpr unsigned kErrDrainWait = 4u;   // copies still in flight at exit
 constexpr unsigned kErrGridWait = 8u;    // a CTA waited too long at a grid barrier
 constexpr unsigned kErrTcWait = 16u;     // tensor-core pipeline wait (operands / MMA completion)
+constexpr unsigned kErrSlotWait = 32u;   // split-K head waited too long for a partial sum
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));

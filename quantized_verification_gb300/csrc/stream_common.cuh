@@ -113,49 +113,163 @@ struct W8A8Params {
     int32_t* acc_debug;
     int32_t* tokens;
     float* max_logit;
-    int32_t* ws_acc;
-    unsigned* ws_cnt;
+    unsigned long long* slots;   // split-K partials: one BN x MP slot per CTA
     unsigned long long* keys;
     unsigned* done;
 };
 
 // ---------------------------------------------------------------------------
+// Split-K combination through per-CTA slots of tagged words.
+//
+// A channel tile whose K range is split over CTAs has exactly one segment
+// that starts at K-tile 0: the head, which is the last segment of the CTA
+// that holds it (that CTA's range ends inside the tile). Every other segment
+// of the tile is the first segment of a later CTA. Those CTAs publish their
+// partial sums into their own slot as 64-bit words (1 << 32 | 32-bit value):
+// an aligned 64-bit access is single-copy atomic, so a reader that sees the
+// tag also sees the value, and publishing needs no fence and no counter. The
+// head's CTA adds the slots of the CTAs after it whose ranges start inside
+// the tile (read with relaxed loads, waiting with a time limit for a tag
+// still missing), zeroes them and finishes the tile. The wait is one-way
+// (a CTA waits only on CTAs with a higher index, which publish before they
+// wait on anything) and every CTA of the grid is resident before a later
+// kernel can take an SM (each CTA allows dependent launches only once it
+// runs), so it always ends.
+//
+// Slot layout: slot c = slots + c * BN * MP words, word [token m][row r].
+// ---------------------------------------------------------------------------
+constexpr unsigned long long kSlotTag = 1ull << 32;
+
+__device__ __forceinline__ void st_relaxed_v2_u64(unsigned long long* p, unsigned long long a,
+                                                  unsigned long long b) {
+    asm volatile("st.relaxed.gpu.global.v2.u64 [%0], {%1, %2};" :: "l"(p), "l"(a), "l"(b) : "memory");
+}
+__device__ __forceinline__ void ld_relaxed_v2_u64(const unsigned long long* p, unsigned long long& a,
+                                                  unsigned long long& b) {
+    asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "l"(p) : "memory");
+}
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long* p) {
+    unsigned long long v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// A tagged word not yet published when first read: poll it (rarely taken,
+// kept out of line). After the time limit the error bit is set and 0 is used.
+static __device__ __noinline__ unsigned long long wait_tagged(const unsigned long long* p, unsigned* err) {
+    const unsigned long long t0 = global_timer_ns();
+    while (true) {
+        __nanosleep(32);
+        const unsigned long long w = ld_relaxed_u64(p);
+        if (w >> 32) return w;
+        if (global_timer_ns() - t0 > kWaitLimitNs) {
+            atomicOr(err, kErrSlotWait);
+            return kSlotTag;
+        }
+    }
+}
+
+// Publish this CTA's staged partial sums (stg[row * MP + token], 32-bit
+// words) into its slot. The caller synchronises the consumers afterwards
+// before stg is written again.
+template <int MP, int CW, class SM>
+__device__ __forceinline__ void publish_partial(SM& sm, unsigned long long* slots, int M, int tid) {
+    constexpr int CT = CW * 32;
+    unsigned long long* slot = slots + (size_t)blockIdx.x * (BN * MP);
+    const uint32_t* stg = reinterpret_cast<const uint32_t*>(sm.stg);
+    for (int q = tid; q < M * (BN / 2); q += CT) {
+        const int m = q / (BN / 2), r = 2 * (q - m * (BN / 2));
+        st_relaxed_v2_u64(slot + m * BN + r, kSlotTag | stg[r * MP + m], kSlotTag | stg[(r + 1) * MP + m]);
+    }
+}
+
+// Head segment of a split tile nt: add the partials of the CTAs after this
+// one whose ranges start inside the tile (in CTA order, i.e. in K order)
+// onto stg, zeroing their slots. Integer sums (FLOAT = false) or fp32 sums.
+// The caller synchronises the consumers before and after.
+template <int MP, int CW, bool FLOAT, class SM>
+__device__ __forceinline__ void gather_partials(SM& sm, unsigned long long* slots, int M, long long T,
+                                                int KT, int nt, int tid, unsigned* err) {
+    constexpr int CT = CW * 32;
+    constexpr int QP = 2;         // pairs of words per thread in flight
+    constexpr int CB = 8;         // contributor slots per batch
+    const int G = gridDim.x;
+    const long long tile_end = (long long)(nt + 1) * KT;
+    const int c1 = blockIdx.x + 1;
+    int c2 = c1;
+    while (c2 < G && (long long)c2 * T / G < tile_end) ++c2;
+    uint32_t* stg = reinterpret_cast<uint32_t*>(sm.stg);
+    const int pairs = M * (BN / 2);
+    for (int q0 = tid; q0 < pairs; q0 += QP * CT) {
+        int off[QP];
+        uint32_t s[QP][2];
+#pragma unroll
+        for (int u = 0; u < QP; ++u) {
+            const int q = q0 + u * CT;
+            const int m = q / (BN / 2), r = 2 * (q - m * (BN / 2));
+            off[u] = m * BN + r;
+            if (q < pairs) {
+                s[u][0] = stg[r * MP + m];
+                s[u][1] = stg[(r + 1) * MP + m];
+            }
+        }
+        for (int c = c1; c < c2; c += CB) {
+            unsigned long long w[CB][QP][2];
+#pragma unroll
+            for (int j = 0; j < CB; ++j)
+#pragma unroll
+                for (int u = 0; u < QP; ++u)
+                    if (c + j < c2 && q0 + u * CT < pairs)
+                        ld_relaxed_v2_u64(slots + (size_t)(c + j) * (BN * MP) + off[u], w[j][u][0], w[j][u][1]);
+#pragma unroll
+            for (int j = 0; j < CB; ++j)
+#pragma unroll
+                for (int u = 0; u < QP; ++u)
+                    if (c + j < c2 && q0 + u * CT < pairs) {
+                        unsigned long long* a = slots + (size_t)(c + j) * (BN * MP) + off[u];
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            if (!(w[j][u][h] >> 32)) w[j][u][h] = wait_tagged(a + h, err);
+                            const uint32_t v = (uint32_t)w[j][u][h];
+                            s[u][h] = FLOAT ? __float_as_uint(__uint_as_float(s[u][h]) + __uint_as_float(v))
+                                            : s[u][h] + v;
+                        }
+                        st_relaxed_v2_u64(a, 0ull, 0ull);
+                    }
+        }
+#pragma unroll
+        for (int u = 0; u < QP; ++u) {
+            const int q = q0 + u * CT;
+            if (q < pairs) {
+                const int m = q / (BN / 2), r = 2 * (q - m * (BN / 2));
+                stg[r * MP + m] = s[u][0];
+                stg[(r + 1) * MP + m] = s[u][1];
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
 // Epilogue of the W8A8 streaming kernels, run by the CW consumer warps
 // (thread index tid in [0, 32*CW)).
 //
-// A channel tile whose K range is split over CTAs is combined with int32
-// atomic adds into the workspace (exact, so order does not matter); the CTA
-// whose contribution completes the tile (the one that brings the tile's
-// counter to KT) finishes it, reading the sums and zeroing them, so the
-// workspace is left zeroed. Only thread 0 fences, after the CTA barrier that
-// orders the other threads' adds before it (and, on the finishing side,
-// before the barrier that releases the reads).
-//
-// A CTA's stream-K range starts with at most one partial segment that is not
-// its last; that segment's counter result is not needed until the range
-// ends, so the CTA keeps streaming and finishes the tile (if its add was the
-// last) after its final segment. The LM head finishes a tile by folding
-// each token's best (logit, index) key into a global atomicMax word and
-// counts finished tiles per CTA; one counter add per CTA at the end decides
-// which CTA decodes the keys (the last one), then zeroes them.
+// The LM head finishes a tile by folding each token's best (logit, index)
+// key into a global atomicMax word and counts finished tiles per CTA; one
+// counter add per CTA at the end decides which CTA decodes the keys (the
+// last one), then zeroes them.
 //
 // Linear: y = fl(fl(acc) * fl(sx * sw)) per element. LM head key:
 // (order-preserving bits of y) << 32 | (0xFFFFFFFF - v), so the largest key
 // is the largest logit and, among equal logits, the lowest index.
 // ---------------------------------------------------------------------------
 struct EpiState {
-    int def_nt = -1;          // channel tile of the deferred partial contribution
-    int def_len = 0;
-    unsigned def_prev = 0;    // thread 0: tile counter before that contribution
     unsigned tiles_done = 0;  // LM head: channel tiles this CTA finished
 };
 
-// Finish channel tile nt from sm.stg (from_ws = false) or from the workspace.
+// Finish channel tile nt from its complete int32 sums in sm.stg.
 template <int MP, int CW, int EPI, class SM>
-__device__ __forceinline__ void finish_tile(SM& sm, const W8A8Params& p, int nt, bool from_ws, int tid,
-                                            EpiState& st) {
+__device__ __forceinline__ void finish_tile(SM& sm, const W8A8Params& p, int nt, int tid, EpiState& st) {
     const int warp = tid >> 5, lane = tid & 31;
-    int32_t* gacc = p.ws_acc + (size_t)nt * BN * MP;
     // the first BN consumer threads (warps 0..3) own one output channel each
     const int r = tid;
     const int n = nt * BN + r;
@@ -166,12 +280,7 @@ __device__ __forceinline__ void finish_tile(SM& sm, const W8A8Params& p, int nt,
     if (valid) {
 #pragma unroll
         for (int m = 0; m < MP; ++m)
-            if (m < p.M) acc[m] = from_ws ? __ldcg(&gacc[r * MP + m]) : sm.stg[r * MP + m];
-        if (from_ws) {
-#pragma unroll
-            for (int m = 0; m < MP; ++m)
-                if (m < p.M) __stcg(&gacc[r * MP + m], 0);
-        }
+            if (m < p.M) acc[m] = sm.stg[r * MP + m];
     }
     const float swn = valid ? p.sw[n] : 0.f;
     if (EPI == (int)Epi::Linear) {
@@ -216,61 +325,30 @@ __device__ __forceinline__ void finish_tile(SM& sm, const W8A8Params& p, int nt,
         }
         ++st.tiles_done;
     }
-    if (from_ws && tid == 0) __stcg(&p.ws_cnt[nt], 0u);
 }
 
-// End of a segment (the channel tile nt's sums over seg_len of its K-tiles
-// are staged in sm.stg[row * MP + token] and the consumers have synchronised);
-// last_seg: this is the CTA's final segment.
+// End of a segment: the channel tile nt's sums over K-tiles [seg_begin,
+// seg_begin + seg_len) (tile indices) are staged in sm.stg[row * MP + token]
+// and the consumers have synchronised.
 template <int MP, int CW, int EPI, class SM>
-__device__ __forceinline__ void segment_end(SM& sm, const W8A8Params& p, int nt, int seg_len,
-                                            bool last_seg, int tid, EpiState& st) {
-    constexpr int CT = CW * 32;
-    if (seg_len == p.KT) {
-        finish_tile<MP, CW, EPI>(sm, p, nt, false, tid, st);
-        consumer_sync<CW>();   // staging buffer and reduction slots are reused
-        return;
+__device__ __forceinline__ void segment_end(SM& sm, const W8A8Params& p, int nt, int seg_begin, int seg_len,
+                                            int tid, EpiState& st, unsigned* err) {
+    if (seg_len != p.KT) {
+        if (seg_begin != nt * p.KT) {                 // not the head: publish
+            publish_partial<MP, CW>(sm, p.slots, p.M, tid);
+            consumer_sync<CW>();
+            return;
+        }
+        gather_partials<MP, CW, false>(sm, p.slots, p.M, p.T, p.KT, nt, tid, err);
+        consumer_sync<CW>();
     }
-    int32_t* gacc = p.ws_acc + (size_t)nt * BN * MP;
-    for (int e = tid; e < BN * MP; e += CT) {
-        const int r = e / MP, m = e - (e / MP) * MP;
-        if (m < p.M && nt * BN + r < p.N) atomicAdd(&gacc[e], sm.stg[e]);
-    }
-    consumer_sync<CW>();
-    unsigned prev = 0;
-    if (tid == 0) {
-        __threadfence();
-        prev = atomicAdd(&p.ws_cnt[nt], (unsigned)seg_len);
-    }
-    if (!last_seg) {
-        st.def_nt = nt;
-        st.def_len = seg_len;
-        if (tid == 0) st.def_prev = prev;   // read only when the range ends
-        return;
-    }
-    if (tid == 0) {
-        const bool fin = prev + (unsigned)seg_len == (unsigned)p.KT;
-        if (fin) __threadfence();
-        *sm.flag = fin ? 1 : 0;
-    }
-    consumer_sync<CW>();
-    if (*sm.flag) finish_tile<MP, CW, EPI>(sm, p, nt, true, tid, st);
-    consumer_sync<CW>();
+    finish_tile<MP, CW, EPI>(sm, p, nt, tid, st);
+    consumer_sync<CW>();   // staging buffer and reduction slots are reused
 }
 
-// After the CTA's last segment: the deferred tile, then the LM head's decode.
+// After the CTA's last segment: the LM head's decode.
 template <int MP, int CW, int EPI, class SM>
 __device__ __forceinline__ void range_end(SM& sm, const W8A8Params& p, int tid, EpiState& st) {
-    if (st.def_nt >= 0) {
-        if (tid == 0) {
-            const bool fin = st.def_prev + (unsigned)st.def_len == (unsigned)p.KT;
-            if (fin) __threadfence();
-            *sm.flag = fin ? 1 : 0;
-        }
-        consumer_sync<CW>();
-        if (*sm.flag) finish_tile<MP, CW, EPI>(sm, p, st.def_nt, true, tid, st);
-        consumer_sync<CW>();
-    }
     if (EPI == (int)Epi::LmHead && st.tiles_done > 0) {
         if (tid == 0) {
             __threadfence();

@@ -34,7 +34,7 @@ class LinearDesc(ctypes.Structure):
     """qv_linear_desc of include/qv.h."""
     _fields_ = [("x", ctypes.c_void_p), ("act_mul", ctypes.c_void_p), ("wq", ctypes.c_void_p),
                 ("sw", ctypes.c_void_p), ("y", ctypes.c_void_p), ("K", ctypes.c_int), ("N", ctypes.c_int)]
-QV_NOALLOC_SCRATCH_BYTES = 4 << 20
+QV_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
 class QVError(RuntimeError):

@@ -38,10 +38,16 @@ def test_exports_every_declared_symbol(lib):
 
 def test_workspace_sizes(lib):
     from quantized_verification_gb300 import qv
-    # linear: Npad*MP int32 + counters; M=5 -> MP=8
-    assert qv.qv_workspace_bytes(qv.QV_OP_LINEAR, 5, 4096, 4096) == 4096 * 8 * 4 + 32 * 4
-    assert qv.qv_workspace_bytes(qv.QV_OP_LINEAR, 5, 4096, 1000) == 1024 * 8 * 4 + 8 * 4
-    assert qv.qv_workspace_bytes(qv.QV_OP_LM_HEAD, 5, 4096, 151936) > 151936 * 8 * 4
+    # linear: one split-K slot of 128 x MP 8-byte words per CTA (at most 160
+    # CTAs), whatever N; M=5 -> MP=8
+    slots8 = 160 * 128 * 8 * 8
+    assert qv.qv_workspace_bytes(qv.QV_OP_LINEAR, 5, 4096, 4096) == slots8
+    assert qv.qv_workspace_bytes(qv.QV_OP_LINEAR, 5, 4096, 1000) == slots8
+    assert qv.qv_workspace_bytes(qv.QV_OP_BF16_LINEAR, 5, 4096, 1000) == slots8
+    assert qv.qv_workspace_bytes(qv.QV_OP_LINEAR, 17, 4096, 1000) == 4 * slots8       # MP = 32
+    assert qv.qv_workspace_bytes(qv.QV_OP_LINEAR, 200, 4096, 1000) == 8 * slots8      # 64-row slices
+    # LM head: slots + per-token keys + the done counter on its own lines
+    assert qv.qv_workspace_bytes(qv.QV_OP_LM_HEAD, 5, 4096, 151936) == slots8 + 8 * 8 + 5 * 128
     assert qv.qv_workspace_bytes(qv.QV_OP_LINEAR, 0, 4096, 16) == 0
     assert qv.qv_workspace_bytes(qv.QV_OP_LINEAR, 5, 100, 16) == 0     # K % 16
     assert qv.qv_workspace_bytes(qv.QV_OP_LINEAR, 257, 4096, 16) == 0  # M > QV_MAX_M
