@@ -302,6 +302,8 @@ w8a8_stream_kernel(const __grid_constant__ CUtensorMap tmap_w,
     }
 
     // ---------------- consumers ----------------
+    EpiState est;
+    est.c2 = split_contributors_end(p.T, p.KT, b);
     grid_dependency_wait();
     if (tid < MP) sm.sx[tid] = tid < p.M ? p.sx[tid] : 0.f;
     consumer_sync<CW>();
@@ -310,13 +312,13 @@ w8a8_stream_kernel(const __grid_constant__ CUtensorMap tmap_w,
     const TileLanes<BPW> L(RW * warp, lane);
 
     int32_t acci[BPW][NG][4];
-    EpiState est;
     int s = 0, phase = 0;
     int i = a;
     while (i < b) {
         const int nt = i / p.KT;
         const int seg_begin = i;
         const int seg_end = min(b, (nt + 1) * p.KT);
+        segment_start(est, p, nt, tid);
 #pragma unroll
         for (int blk = 0; blk < BPW; ++blk)
 #pragma unroll
@@ -400,6 +402,7 @@ bf16_stream_kernel(const __grid_constant__ CUtensorMap tmap_w,
                             (unsigned)(kWTileBytes + C::XBytes));
         return;
     }
+    const int c2 = split_contributors_end(p.T, p.KT, b);
     grid_dependency_wait();
 
     const int li = lane & 7, lj = lane >> 3;
@@ -479,7 +482,7 @@ bf16_stream_kernel(const __grid_constant__ CUtensorMap tmap_w,
                 consumer_sync<CW>();
                 continue;
             }
-            gather_partials<MP, CW, true>(sm, p.slots, p.M, p.T, p.KT, nt, tid, &g_stream_gemm_error);
+            gather_partials<MP, CW, true>(sm, p.slots, p.M, c2, tid, &g_stream_gemm_error);
             consumer_sync<CW>();
         }
         const int r = tid;

@@ -254,13 +254,14 @@ w8a8_tc_kernel(const __grid_constant__ CUtensorMap tmap_w,
     const int h = warp >> 2;                 // K half (widening) and token half (readout)
     const int row = 32 * qd + lane;          // output channel within the tile
     const uint32_t lane_base = tmem + ((uint32_t)(32 * qd) << 16);
+    EpiState est;
+    est.c2 = split_contributors_end(p.T, p.KT, b);
     grid_dependency_wait();
     if (tid < MP) sm.sx[tid] = tid < p.M ? p.sx[tid] : 0.f;
     consumer_sync<kTcConv>();
     const bool has_tokens = h * MPH < p.M;  // warp-uniform
 
     int32_t acc[MPH];
-    EpiState est;
     // Group g's accumulator (buffer g & 1) completes on dfull[g & 1], the
     // (g >> 1)-th phase of that barrier.
     auto read_group = [&](int g) {
@@ -283,6 +284,7 @@ w8a8_tc_kernel(const __grid_constant__ CUtensorMap tmap_w,
         const int nt = i / p.KT;
         const int seg_begin = i;
         const int seg_end = min(b, (nt + 1) * p.KT);
+        segment_start(est, p, nt, tid);
 #pragma unroll
         for (int m = 0; m < MPH; ++m) acc[m] = 0;
 

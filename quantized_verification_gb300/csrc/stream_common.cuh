@@ -129,8 +129,9 @@ struct W8A8Params {
 // an aligned 64-bit access is single-copy atomic, so a reader that sees the
 // tag also sees the value, and publishing needs no fence and no counter. The
 // head's CTA adds the slots of the CTAs after it whose ranges start inside
-// the tile (read with relaxed loads, waiting with a time limit for a tag
-// still missing), zeroes them and finishes the tile. The wait is one-way
+// the tile (read with relaxed loads; words still untagged are re-read
+// together until they are tagged, with a time limit), zeroes them and
+// finishes the tile. The wait is one-way
 // (a CTA waits only on CTAs with a higher index, which publish before they
 // wait on anything) and every CTA of the grid is resident before a later
 // kernel can take an SM (each CTA allows dependent launches only once it
@@ -154,21 +155,6 @@ __device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long
     return v;
 }
 
-// A tagged word not yet published when first read: poll it (rarely taken,
-// kept out of line). After the time limit the error bit is set and 0 is used.
-static __device__ __noinline__ unsigned long long wait_tagged(const unsigned long long* p, unsigned* err) {
-    const unsigned long long t0 = global_timer_ns();
-    while (true) {
-        __nanosleep(32);
-        const unsigned long long w = ld_relaxed_u64(p);
-        if (w >> 32) return w;
-        if (global_timer_ns() - t0 > kWaitLimitNs) {
-            atomicOr(err, kErrSlotWait);
-            return kSlotTag;
-        }
-    }
-}
-
 // Publish this CTA's staged partial sums (stg[row * MP + token], 32-bit
 // words) into its slot. The caller synchronises the consumers afterwards
 // before stg is written again.
@@ -183,21 +169,29 @@ __device__ __forceinline__ void publish_partial(SM& sm, unsigned long long* slot
     }
 }
 
-// Head segment of a split tile nt: add the partials of the CTAs after this
-// one whose ranges start inside the tile (in CTA order, i.e. in K order)
+// With this CTA's stream-K range ending at tile index b (exclusive), one
+// past the last CTA whose range starts inside the channel tile of tile b-1:
+// CTA c starts at floor(c*T/G), so that is the first c with c*T >= E*G,
+// E = the end of that channel tile. Computed once, before the grid
+// dependency wait.
+__device__ __forceinline__ int split_contributors_end(long long T, int KT, int b) {
+    const long long G = gridDim.x;
+    const long long E = (long long)((b - 1) / KT + 1) * KT;
+    const long long c2 = (E * G + T - 1) / T;
+    return (int)(c2 < G ? c2 : G);
+}
+
+// Head segment of a split tile: add the partials of CTAs blockIdx.x+1 ..
+// c2-1 (whose ranges start inside the tile; in CTA order, i.e. in K order)
 // onto stg, zeroing their slots. Integer sums (FLOAT = false) or fp32 sums.
 // The caller synchronises the consumers before and after.
 template <int MP, int CW, bool FLOAT, class SM>
-__device__ __forceinline__ void gather_partials(SM& sm, unsigned long long* slots, int M, long long T,
-                                                int KT, int nt, int tid, unsigned* err) {
+__device__ __forceinline__ void gather_partials(SM& sm, unsigned long long* slots, int M, int c2, int tid,
+                                                unsigned* err) {
     constexpr int CT = CW * 32;
     constexpr int QP = 2;         // pairs of words per thread in flight
     constexpr int CB = 8;         // contributor slots per batch
-    const int G = gridDim.x;
-    const long long tile_end = (long long)(nt + 1) * KT;
     const int c1 = blockIdx.x + 1;
-    int c2 = c1;
-    while (c2 < G && (long long)c2 * T / G < tile_end) ++c2;
     uint32_t* stg = reinterpret_cast<uint32_t*>(sm.stg);
     const int pairs = M * (BN / 2);
     for (int q0 = tid; q0 < pairs; q0 += QP * CT) {
@@ -221,20 +215,45 @@ __device__ __forceinline__ void gather_partials(SM& sm, unsigned long long* slot
                 for (int u = 0; u < QP; ++u)
                     if (c + j < c2 && q0 + u * CT < pairs)
                         ld_relaxed_v2_u64(slots + (size_t)(c + j) * (BN * MP) + off[u], w[j][u][0], w[j][u][1]);
+            // Words still untagged: re-read all of them together (one round
+            // trip per polling round), up to the time limit.
+            unsigned long long t0 = 0;
+            while (true) {
+                bool pending = false;
+#pragma unroll
+                for (int j = 0; j < CB; ++j)
+#pragma unroll
+                    for (int u = 0; u < QP; ++u)
+                        if (c + j < c2 && q0 + u * CT < pairs && !((w[j][u][0] & w[j][u][1]) >> 32))
+                            pending = true;
+                if (!pending) break;
+                if (t0 == 0) {
+                    t0 = global_timer_ns();
+                } else if (global_timer_ns() - t0 > kWaitLimitNs) {
+                    atomicOr(err, kErrSlotWait);
+                    break;
+                }
+                __nanosleep(20);
+#pragma unroll
+                for (int j = 0; j < CB; ++j)
+#pragma unroll
+                    for (int u = 0; u < QP; ++u)
+                        if (c + j < c2 && q0 + u * CT < pairs && !((w[j][u][0] & w[j][u][1]) >> 32))
+                            ld_relaxed_v2_u64(slots + (size_t)(c + j) * (BN * MP) + off[u], w[j][u][0],
+                                              w[j][u][1]);
+            }
 #pragma unroll
             for (int j = 0; j < CB; ++j)
 #pragma unroll
                 for (int u = 0; u < QP; ++u)
                     if (c + j < c2 && q0 + u * CT < pairs) {
-                        unsigned long long* a = slots + (size_t)(c + j) * (BN * MP) + off[u];
 #pragma unroll
                         for (int h = 0; h < 2; ++h) {
-                            if (!(w[j][u][h] >> 32)) w[j][u][h] = wait_tagged(a + h, err);
                             const uint32_t v = (uint32_t)w[j][u][h];
                             s[u][h] = FLOAT ? __float_as_uint(__uint_as_float(s[u][h]) + __uint_as_float(v))
                                             : s[u][h] + v;
                         }
-                        st_relaxed_v2_u64(a, 0ull, 0ull);
+                        st_relaxed_v2_u64(slots + (size_t)(c + j) * (BN * MP) + off[u], 0ull, 0ull);
                     }
         }
 #pragma unroll
@@ -263,8 +282,17 @@ __device__ __forceinline__ void gather_partials(SM& sm, unsigned long long* slot
 // is the largest logit and, among equal logits, the lowest index.
 // ---------------------------------------------------------------------------
 struct EpiState {
+    int c2 = 0;               // split_contributors_end of the CTA's range
+    float swn = 0.f;          // channel scale of this thread's row in the current tile
     unsigned tiles_done = 0;  // LM head: channel tiles this CTA finished
 };
+
+// At the start of a segment of channel tile nt: load the channel scale the
+// finish needs, so that its latency hides behind the segment's MMAs.
+__device__ __forceinline__ void segment_start(EpiState& st, const W8A8Params& p, int nt, int tid) {
+    const int n = nt * BN + tid;
+    st.swn = (tid < BN && n < p.N) ? __ldg(&p.sw[n]) : 0.f;
+}
 
 // Finish channel tile nt from its complete int32 sums in sm.stg.
 template <int MP, int CW, int EPI, class SM>
@@ -282,7 +310,7 @@ __device__ __forceinline__ void finish_tile(SM& sm, const W8A8Params& p, int nt,
         for (int m = 0; m < MP; ++m)
             if (m < p.M) acc[m] = sm.stg[r * MP + m];
     }
-    const float swn = valid ? p.sw[n] : 0.f;
+    const float swn = st.swn;
     if (EPI == (int)Epi::Linear) {
         if (valid) {
 #pragma unroll
@@ -339,7 +367,7 @@ __device__ __forceinline__ void segment_end(SM& sm, const W8A8Params& p, int nt,
             consumer_sync<CW>();
             return;
         }
-        gather_partials<MP, CW, false>(sm, p.slots, p.M, p.T, p.KT, nt, tid, err);
+        gather_partials<MP, CW, false>(sm, p.slots, p.M, st.c2, tid, err);
         consumer_sync<CW>();
     }
     finish_tile<MP, CW, EPI>(sm, p, nt, tid, st);
