@@ -55,7 +55,11 @@ LINEAR_ACT_CASES = [
     (16, 12288, 512, torch.bfloat16, True),
     (5, 12288, 4096, torch.bfloat16, True),
     (17, 256, 200, torch.bfloat16, True),     # 32 padded tokens, mma.sync GEMM
-    (64, 1024, 256, torch.float32, True),     # tcgen05 GEMM
+    (64, 1024, 256, torch.float32, True),     # tcgen05 GEMM (separate quantization kernel)
+    (3, 12288, 300, torch.float32, True),     # fp32 rows longer than the quantizer keeps in registers
+    (20, 16, 7, torch.bfloat16, True),        # a single GEMM tile
+    (9, 128, 130, torch.float32, False),      # two GEMM CTAs
+    (32, 4096, 1024, torch.bfloat16, True),   # 32 tokens, the most the mma.sync kernel takes
 ]
 
 
