@@ -361,7 +361,7 @@ def main():
     traffic = None
     if NCU_TRAFFIC["source_sha256"] == kernel_source_sha() and NCU_TRAFFIC["dram_bytes_per_algorithmic_byte"]:
         traffic = NCU_TRAFFIC["dram_bytes_per_algorithmic_byte"] * sum(lin_bytes) / len(lin_bytes)
-    kname = ("w8a8_stream_kernel (int8 mma.sync, qv_w8a8_linear)" if M <= 16
+    kname = ("w8a8_stream_kernel (int8 mma.sync, qv_w8a8_linear)" if M <= 32
              else "w8a8_tc_kernel (tcgen05, qv_w8a8_linear)")
     linear_kernel = {"kernel": kname, "achieved": achieved,
                      "frac": achieved / peak, "bytes_per_launch": sum(lin_bytes) / len(lin_bytes),

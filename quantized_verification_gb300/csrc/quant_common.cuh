@@ -1,7 +1,6 @@
-// quant_common.cuh -- per-row symmetric int8 quantization of one row by the
-// threads of a CTA, shared by the activation-quantization kernel and the
-// streaming GEMM's fused activation quantization (same code, so the same
-// codes and scales bit for bit).
+// quant_common.cuh -- symmetric int8 quantization of one row by the threads
+// of a CTA (the activation- and weight-quantization kernel's body), written
+// against a caller-supplied barrier so that any group of threads can run it.
 //
 //   Quasar, gist.science/ja summary, section 2.2 "Enhanced SmoothQuant",
 //   items 2-3: BF16 activations scaled by the smoothing factor and converted
