@@ -36,14 +36,13 @@ WORKLOAD = ("qwen3-8b-shaped W8A8 verify step, M=5 (B=1, gamma=4): 36 layers x (
             "o 4096->4096, gate|up 4096->24576, down 12288->4096) + LM head 4096->151936 argmax + accept")
 FALLBACK_HBM_GBS = 6800.0
 
-# DRAM bytes per algorithmic byte of the dominant kernel from one ncu capture,
-# valid only for the kernel source it was taken on (sha256 of
-# csrc/k_stream_gemm.cu); traffic is reported as null otherwise.
 # DRAM bytes per algorithmic byte of one projection launch of the streaming
-# W8A8 kernel, from an ncu capture of the gate+up launch (see
-# profiles/launches_qwen3_8b_1layer_m5.md), valid for these kernel sources.
-NCU_TRAFFIC = {"source_sha256": "6e9a6f871dde15dff7ab3d81160137a019c5be2b252e58d73649bbc6a2232cd2",
-               "dram_bytes_per_algorithmic_byte": (102247168 + 2811648) / 101273620}
+# W8A8 kernel: ncu dram__bytes_read.sum + dram__bytes_write.sum of the gate+up
+# launch (4096 -> 24576, M = 5) over its algorithmic bytes. Valid only for the
+# kernel sources whose sha256 is recorded (kernel_source_sha); roofline.traffic
+# is null otherwise.
+NCU_TRAFFIC = {"source_sha256": "d81d0f3a410976abb9e18225716717ddc48fca693a89fbee94b1c5f5569a07f8",
+               "dram_bytes_per_algorithmic_byte": (101698304 + 2669568) / 101273620}
 
 
 def log(*a):
