@@ -79,6 +79,24 @@ class VerifyStack:
         self.lm_bf16 = wl if keep_bf16 else None
         del wl
         self.h_final = synth.activations(self.M, h, synth.subseed(seed, "x", "final"), device=dev)
+        # Every per-step activation input becomes a view into one contiguous
+        # buffer (each [M, K] bf16 slice starts 16-byte aligned because K is a
+        # multiple of 16), so a step from host memory is one copy.
+        flat = [x for li in self.inputs for x in li] + [self.h_final]
+        self.in_buf = torch.empty(sum(x.numel() for x in flat), dtype=flat[0].dtype, device=dev)
+        views, off = [], 0
+        for x in flat:
+            v = self.in_buf[off: off + x.numel()].view(x.shape)
+            v.copy_(x)
+            views.append(v)
+            off += x.numel()
+        k = 0
+        for li in self.inputs:
+            for p in range(len(li)):
+                li[p] = views[k]
+                k += 1
+        self.h_final = views[k]
+        del flat
         self.drafts = torch.zeros(B, max(gamma, 0), dtype=torch.int32, device=dev)
 
         kmax = max(K for (_, K, _) in self.phases)
@@ -241,29 +259,23 @@ class VerifyStack:
         self.graph.replay()
 
     # ------------------------------------------------------------------ host API
-    def _step_inputs(self):
-        return [x for li in self.inputs for x in li] + [self.h_final]
-
     def pinned_host_inputs(self):
-        """Pinned host copies of every per-step input (activations, drafts)."""
-        flat = self._step_inputs()
-        host = [torch.empty_like(x, device="cpu").pin_memory() for x in flat]
-        for hsrc, d in zip(host, flat):
-            hsrc.copy_(d)
+        """Pinned host copies of the per-step inputs: every activation input in
+        one buffer (laid out like the device buffer), and the drafts."""
+        host = torch.empty_like(self.in_buf, device="cpu").pin_memory()
+        host.copy_(self.in_buf)
         drafts = torch.empty_like(self.drafts, device="cpu").pin_memory()
         drafts.copy_(self.drafts)
         return host, drafts
 
     def step_from_host(self, host_inputs, host_drafts, out_len, out_tokens, graph=None):
         """One verify step from host buffers: copy the step's inputs to the
-        device, run the captured step, copy the accepted lengths and tokens
-        back (into pinned host tensors). Returns bytes copied (h2d, d2h)."""
-        h2d = 0
-        for d, hsrc in zip(self._step_inputs(), host_inputs):
-            d.copy_(hsrc, non_blocking=True)
-            h2d += hsrc.numel() * hsrc.element_size()
+        device (one copy for all activations, one for the drafts), run the
+        captured step, copy the accepted lengths and tokens back (into pinned
+        host tensors). Returns bytes copied (h2d, d2h)."""
+        self.in_buf.copy_(host_inputs, non_blocking=True)
         self.drafts.copy_(host_drafts, non_blocking=True)
-        h2d += host_drafts.numel() * host_drafts.element_size()
+        h2d = host_inputs.numel() * host_inputs.element_size() + host_drafts.numel() * host_drafts.element_size()
         (graph or self.graph).replay()
         out_len.copy_(self.accept_len, non_blocking=True)
         out_tokens.copy_(self.out_tokens, non_blocking=True)

@@ -183,6 +183,31 @@ def test_verify_stack_equals_per_op_calls(qv):
     assert torch.equal(st.tokens, t1)
 
 
+def test_step_from_host_buffers(qv):
+    """The end-to-end step: the packed host inputs, copied in one transfer and
+    run through the captured graph, give the same tokens as the device-resident
+    step, and the result lands in the pinned host tensors."""
+    from quantized_verification_gb300 import synth
+    from quantized_verification_gb300.stack import VerifyStack
+    model = {"hidden": 256, "kv": 128, "ffn": 512, "layers": 2, "vocab": 1000}
+    st = VerifyStack(model=model, B=1, gamma=4, seed=11)
+    st.drafts.copy_(synth.uniform_tokens((1, 4), 1000, seed=2).cuda())
+    g = st.capture()
+    g.replay()
+    torch.cuda.synchronize()
+    l1, o1 = st.accept_len.clone(), st.out_tokens.clone()
+    host_in, host_d = st.pinned_host_inputs()
+    assert host_in.numel() == sum(x.numel() for li in st.inputs for x in li) + st.h_final.numel()
+    st.in_buf.zero_()
+    st.drafts.zero_()
+    out_len = torch.empty(1, dtype=torch.int32).pin_memory()
+    out_tok = torch.empty(1, 5, dtype=torch.int32).pin_memory()
+    h2d, d2h = st.step_from_host(host_in, host_d, out_len, out_tok, graph=g)
+    torch.cuda.synchronize()
+    assert h2d == host_in.numel() * 2 + host_d.numel() * 4 and d2h == 4 + 20
+    assert torch.equal(out_len, l1.cpu()) and torch.equal(out_tok, o1.cpu())
+
+
 def test_verify_stack_rejects_large_m(qv):
     M, K, N = 17, 128, 128
     dev = "cuda"
