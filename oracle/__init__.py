@@ -73,6 +73,12 @@ class Oracle:
         L.qvo_lm_head_argmax.argtypes = [_P, _P, _P, _P, _I, _I, _I, _P, _P]
         L.qvo_accept.argtypes = [_P, _P, _I, _I, _P, _P]
         L.qvo_linear_f64.argtypes = [_P, _P, _I, _I, _I, _P]
+        L.qvo_exp.restype = ctypes.c_float
+        L.qvo_exp.argtypes = [ctypes.c_float]
+        L.qvo_silu.restype = ctypes.c_float
+        L.qvo_silu.argtypes = [ctypes.c_float]
+        L.qvo_swiglu_quant.argtypes = [_P, _I, _I, _P, _P]
+        L.qvo_residual_rmsnorm_quant.argtypes = [_P, _P, _P, ctypes.c_float, _P, _I, _I, _P, _P, _P]
 
     # -- bf16 ------------------------------------------------------------
     def bf16_to_f32(self, h: np.ndarray) -> np.ndarray:
@@ -198,9 +204,50 @@ class Oracle:
         return y
 
 
+    # -- f1: non-linear steps between the linears of a layer -------------
+    def exp(self, x: float) -> float:
+        """The layer's exp: Cody-Waite reduction + degree-7 Taylor, binary32."""
+        return float(self._L.qvo_exp(float(x)))
+
+    def silu(self, x: float) -> float:
+        """silu(v) = v * 1 / (1 + exp(-v)), binary32, with the layer's exp."""
+        return float(self._L.qvo_silu(float(x)))
+
+    def swiglu_quant(self, gu: np.ndarray):
+        """gu [M, 2F] fp32 (gate | up) -> codes [M, F] int8, scales [M]:
+        a = silu(gate) * up, then the per-token quantization
+        (gist.science/ja summary, section 2.2 item 3: non-linear layers in
+        high precision, then INT8 for the next linear)."""
+        gu = np.ascontiguousarray(gu, dtype=np.float32)
+        M, F2 = gu.shape
+        F = F2 // 2
+        q = np.empty((M, F), dtype=np.int8)
+        s = np.empty(M, dtype=np.float32)
+        self._L.qvo_swiglu_quant(_ptr(gu), M, F, _ptr(q), _ptr(s))
+        return q, s
+
+    def residual_rmsnorm_quant(self, h: np.ndarray, d: np.ndarray | None, g: np.ndarray, eps: float,
+                               mul: np.ndarray | None = None):
+        """h [M, H] bf16 bits (uint16); d the bf16 delta or None; g [H] bf16
+        bits. Returns (h', codes [M, H], scales [M], x [M, H] bf16 bits):
+        h' = rne_bf16(h + d), x = RMSNorm(h') * g in bf16, then the
+        per-token quantization of x."""
+        h = np.array(h, dtype=np.uint16, copy=True, order="C")
+        M, H = h.shape
+        d_ = None if d is None else np.ascontiguousarray(d, dtype=np.uint16)
+        g = np.ascontiguousarray(g, dtype=np.uint16)
+        mul_ = None if mul is None else np.ascontiguousarray(mul, dtype=np.float32)
+        q = np.empty((M, H), dtype=np.int8)
+        s = np.empty(M, dtype=np.float32)
+        x = np.empty((M, H), dtype=np.uint16)
+        self._L.qvo_residual_rmsnorm_quant(_ptr(h), None if d_ is None else _ptr(d_), _ptr(g),
+                                           ctypes.c_float(eps), None if mul_ is None else _ptr(mul_),
+                                           M, H, _ptr(q), _ptr(s), _ptr(x))
+        return h, q, s, x
+
+
 _default: Oracle | None = None
 _lock = threading.Lock()
-
 
 def get() -> Oracle:
     """The oracle built from ``qv_oracle.c`` (compiled on first use)."""

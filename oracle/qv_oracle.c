@@ -31,6 +31,13 @@
  *       -- gist.science/it summary, section 2 item 3 ("Campionamento di
  *          Rifiuto Lossless"); greedy setting, gist.science/ja summary,
  *          section 4 "main results".
+ *   f1  the non-linear steps between the quantized linears of one decoder
+ *       layer, run in high precision after dequantization (residual add,
+ *       RMSNorm, SiLU(gate) * up), each followed by the a1 quantization of
+ *       the next linear's input
+ *       -- gist.science/ja summary, section 2.2 item 3 (dequantize back to
+ *          high precision before the non-linear layers);
+ *          gist.science/fr summary, section 2 "Pipeline Technique".
  *   a4  acceptance: the longest draft prefix equal to the verifier's tokens,
  *       plus one token from the verifier (so at least one token per step)
  *       -- gist.science/fr summary, lay explanation (a wrong guess is
@@ -49,6 +56,20 @@
  *   - dequant: y = fl32( fl32((float)acc) * fl32(sx * sw) ), every operation
  *     rounded to nearest-even, no fused multiply-add.
  *   - argmax ties go to the lowest index; -0 compares equal to +0.
+ *   - f1 (the layer is not spelled out by the summaries; the readings follow
+ *     the Qwen3-shaped decoder layer of the workloads, with a bf16 residual
+ *     stream):
+ *       residual add  h = rne_bf16(h + d), d the bf16 output of a linear;
+ *       RMSNorm       ss = sum of h_k^2 in binary64 (every bf16 square is
+ *                     exact there), var = fl32(ss / H),
+ *                     rstd = fl32(1 / fl32(sqrt(fl32(var + eps)))),
+ *                     x_k = rne_bf16(g_k * rne_bf16(fl32(h_k * rstd)));
+ *       SwiGLU        a_k = fl32(fl32(gate_k * sigma(gate_k)) * up_k) on the
+ *                     fp32 gate|up outputs, sigma(v) = fl32(1 / fl32(1 + E(-v)))
+ *                     with E the exp defined at qvo_exp (Cody-Waite reduction
+ *                     and a Taylor polynomial, written out so that the GPU side
+ *                     can evaluate the identical binary32 operations);
+ *     then the a1 quantization of x (bf16) or a (fp32).
  *   - acceptance: row j of sequence b holds the verifier token t[b][j] that
  *     follows prefix position j; draft d[b][j] is accepted iff it equals
  *     t[b][j] and all earlier drafts were accepted; the verifier token at the
@@ -63,6 +84,7 @@
  */
 #include <stdint.h>
 #include <stddef.h>
+#include <stdlib.h>
 #include <string.h>
 #include <math.h>
 
@@ -302,4 +324,112 @@ void qvo_linear_f64(const float* x, const float* w, int64_t M, int64_t N,
                 sum += (double)x[m * K + k] * (double)w[n * K + k];
             y[m * N + n] = sum;
         }
+}
+
+/* ------------------------------------------------------------------ */
+/* f1: the non-linear steps between the quantized linears of a layer    */
+/* ------------------------------------------------------------------ */
+
+/*
+ * exp(x) in binary32 by Cody and Waite's additive range reduction and a
+ * Taylor polynomial (W. J. Cody, W. Waite, "Software Manual for the
+ * Elementary Functions", 1980), each step one binary32 operation in
+ * round-to-nearest-even:
+ *   x > 88        -> +inf;   x < -87 -> 0
+ *   k = rne(fl(x * LOG2E))                     (an integer, |k| <= 127)
+ *   r = fl(fl(x - fl(k * LN2_HI)) - fl(k * LN2_LO)),   |r| <= ~0.347
+ *   p = 1 + r(1 + r(c2 + r(c3 + r(c4 + r(c5 + r(c6 + r c7))))))  (Horner,
+ *       c_n = fl(1 / n!), one multiply and one add per step)
+ *   E = fl(p * 2^k)                            (2^k built from its exponent bits)
+ * LN2_HI = 0.693145751953125 has 16 significant bits, so k * LN2_HI is exact;
+ * LN2_LO = fl(ln 2 - LN2_HI). The degree-7 truncation is below 6e-9 relative
+ * on |r| <= ln 2 / 2.
+ */
+static const float QVO_LOG2E = 1.44269504088896341f;
+static const float QVO_LN2_HI = 0.693145751953125f;
+static const float QVO_LN2_LO = 1.42860682030941723212e-6f;
+
+float qvo_exp(float x)
+{
+    if (x > 88.0f) return INFINITY;
+    if (x < -87.0f) return 0.0f;
+    float k = round_half_even(x * QVO_LOG2E);
+    float r = x - k * QVO_LN2_HI;
+    r = r - k * QVO_LN2_LO;
+    const float c[8] = {1.0f, 1.0f, 0.5f, 1.0f / 6.0f, 1.0f / 24.0f, 1.0f / 120.0f,
+                        1.0f / 720.0f, 1.0f / 5040.0f};
+    float p = c[7];
+    for (int n = 6; n >= 0; --n) {
+        p = p * r;
+        p = p + c[n];
+    }
+    union { uint32_t u; float f; } two_k;
+    two_k.u = (uint32_t)((int32_t)k + 127) << 23;
+    return p * two_k.f;
+}
+
+/* sigma(v) = fl32(1 / fl32(1 + E(-v))), silu(v) = fl32(v * sigma(v)). */
+float qvo_silu(float v)
+{
+    float e = qvo_exp(-v);
+    float den = 1.0f + e;
+    float sig = 1.0f / den;
+    return v * sig;
+}
+
+/*
+ * SwiGLU then a1: gu is M rows of 2F fp32 values, gate in columns [0, F),
+ * up in [F, 2F) (the concatenated gate|up linear's output).
+ *   a_k = fl32(silu(gate_k) * up_k); q, s = the per-row quantization of a.
+ */
+void qvo_swiglu_quant(const float* gu, int64_t M, int64_t F, int8_t* q, float* s)
+{
+    float* a = (float*)malloc((size_t)F * sizeof(float));
+    for (int64_t m = 0; m < M; ++m) {
+        const float* row = gu + m * 2 * F;
+        for (int64_t k = 0; k < F; ++k) a[k] = qvo_silu(row[k]) * row[F + k];
+        qvo_quantize_rows_f32(a, 1, F, NULL, q + m * F, s + m);
+    }
+    free(a);
+}
+
+/*
+ * Residual add, RMSNorm, then a1. h: M rows of H bf16 values, updated in
+ * place when d (M x H bf16, the delta) is given; g: H bf16 norm weights;
+ * mul: the a1 smoothing multipliers or NULL.
+ *   h_k   = rne_bf16(fl32(h_k + d_k))
+ *   ss    = sum_k h_k^2 in binary64, var = fl32(ss / H)
+ *   rstd  = fl32(1 / fl32(sqrt(fl32(var + eps))))
+ *   x_k   = rne_bf16(fl32(g_k * rne_bf16(fl32(h_k * rstd))))
+ *   q, s  = the per-row quantization of x (bf16), after mul.
+ * x_out (M x H bf16) receives x when not NULL.
+ */
+void qvo_residual_rmsnorm_quant(uint16_t* h, const uint16_t* d, const uint16_t* g, float eps,
+                                const float* mul, int64_t M, int64_t H, int8_t* q, float* s,
+                                uint16_t* x_out)
+{
+    uint16_t* x = (uint16_t*)malloc((size_t)H * sizeof(uint16_t));
+    for (int64_t m = 0; m < M; ++m) {
+        uint16_t* hr = h + m * H;
+        if (d) {
+            for (int64_t k = 0; k < H; ++k)
+                hr[k] = qvo_f32_to_bf16_rne(qvo_bf16_to_f32(hr[k]) + qvo_bf16_to_f32(d[m * H + k]));
+        }
+        double ss = 0.0;
+        for (int64_t k = 0; k < H; ++k) {
+            double v = (double)qvo_bf16_to_f32(hr[k]);
+            ss += v * v;
+        }
+        float var = (float)(ss / (double)H);
+        float t = var + eps;
+        float sq = sqrtf(t);
+        float rstd = 1.0f / sq;
+        for (int64_t k = 0; k < H; ++k) {
+            float u = qvo_bf16_to_f32(qvo_f32_to_bf16_rne(qvo_bf16_to_f32(hr[k]) * rstd));
+            x[k] = qvo_f32_to_bf16_rne(qvo_bf16_to_f32(g[k]) * u);
+        }
+        if (x_out) memcpy(x_out + m * H, x, (size_t)H * sizeof(uint16_t));
+        qvo_quantize_rows_bf16(x, 1, H, mul, q + m * H, s + m);
+    }
+    free(x);
 }

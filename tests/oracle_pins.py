@@ -331,6 +331,118 @@ def pin_linear_f64(o):
     assert np.allclose(y, ynp, rtol=1e-12, atol=1e-15)
 
 
+
+# ---------------------------------------------------------------------------
+# f1: the non-linear steps between the linears of a layer (residual add,
+# RMSNorm, SiLU(gate) * up), each followed by the a1 quantization.
+# ---------------------------------------------------------------------------
+def _ulp32(v: float) -> float:
+    return float(np.spacing(np.float32(abs(v))))
+
+
+def pin_layer_exp(o):
+    """The layer's exp is the mathematical e^x to 2 ulp over its range, exact
+    at 0, +inf above 88, 0 below -87, and non-decreasing."""
+    import math
+    xs = np.concatenate([np.linspace(-87.0, 88.0, 4001, dtype=np.float32),
+                         np.float32([-1e-7, 1e-7, 0.5, -0.5, 0.34657359, -0.34657359, 1.0, -1.0])])
+    for x in xs:
+        e = o.exp(float(x))
+        t = math.exp(float(x))
+        assert abs(e - t) <= 2 * _ulp32(t), (float(x), e, t)
+    assert o.exp(0.0) == 1.0
+    assert o.exp(88.5) == float("inf") and o.exp(-90.0) == 0.0
+    grid = np.sort(xs)
+    vals = [o.exp(float(x)) for x in grid]
+    assert all(b >= a for a, b in zip(vals, vals[1:]))
+
+
+def pin_silu(o):
+    """silu(v) = v / (1 + e^-v): against the binary64 formula to 4 ulp on
+    [-20, 20]; exactly 0 at 0, v for large v, -0 for very negative v."""
+    import math
+    for v in np.linspace(-20.0, 20.0, 801, dtype=np.float32):
+        ref = float(v) / (1.0 + math.exp(-float(v)))
+        got = o.silu(float(v))
+        assert abs(got - ref) <= 4 * _ulp32(ref) + 1e-30, (float(v), got, ref)
+    assert o.silu(0.0) == 0.0
+    assert o.silu(100.0) == 100.0
+    assert o.silu(-100.0) == 0.0
+
+
+def pin_swiglu_quant(o):
+    """a = silu(gate) * up, then a1. (1) Random rows: every code within one of
+    the binary64 reference's round(a / s) and the scale within 4 ulp of
+    max|a| / 127. (2) Saturated gate (silu(100) = 100 exactly): the codes are
+    the exact-rational a1 quantization of fl(100 * up) (swapping gate and up
+    breaks it). (3) up = 0: all codes and the scale are 0."""
+    import math
+    rng = np.random.default_rng(31)
+    M, F = 3, 64
+    gu = rng.normal(0.0, 2.0, (M, 2 * F)).astype(np.float32)
+    q, s = o.swiglu_quant(gu)
+    for m in range(M):
+        a = [float(g) / (1.0 + math.exp(-float(g))) * float(u) for g, u in zip(gu[m, :F], gu[m, F:])]
+        amax = max(abs(v) for v in a)
+        assert abs(float(s[m]) - amax / 127.0) <= 4 * _ulp32(amax / 127.0)
+        ref = np.array([round(v / (amax / 127.0)) for v in a])
+        assert np.max(np.abs(q[m].astype(np.int64) - ref)) <= 1
+        assert np.mean(q[m].astype(np.int64) == ref) > 0.9
+    up = rng.normal(0.0, 1.0, (2, F)).astype(np.float32)
+    gu2 = np.concatenate([np.full((2, F), 100.0, dtype=np.float32), up], axis=1)
+    q2, s2 = o.swiglu_quant(gu2)
+    for m in range(2):
+        qe, se = quantize_row_exact((np.float32(100.0) * up[m]).astype(np.float32))
+        assert list(q2[m]) == list(qe) and np.float32(s2[m]) == se
+    gu3 = np.concatenate([rng.normal(0.0, 1.0, (1, F)).astype(np.float32), np.zeros((1, F), np.float32)], axis=1)
+    q3, s3 = o.swiglu_quant(gu3)
+    assert not q3.any() and s3[0] == 0.0
+
+
+def pin_rmsnorm_quant(o):
+    """Residual add + RMSNorm + a1.
+    (1) Constant rows c (a power of two) with g = 1, eps = 0: x = sign(c),
+        so every code is +-127 and the scale is fl(1/127).
+    (2) d = -h: the sum is 0, so codes and scale are 0.
+    (3) The residual sum equals torch's bf16 addition (fp32 sum, rne to bf16).
+    (4) Scaling h by 2 (exact in bf16) with eps = 0 leaves x and the codes.
+    (5) x is within two bf16 roundings of the binary64 g * h / sqrt(mean(h^2) + eps).
+    (6) The codes are the exact-rational a1 quantization of x."""
+    import torch
+    H = 96
+    one = np.full(H, 0x3F80, dtype=np.uint16)                      # bf16 1.0
+    hc = np.stack([np.full(H, 0x4000, np.uint16), np.full(H, 0xBE80, np.uint16)])   # 2.0, -0.25
+    _, q, s, x = o.residual_rmsnorm_quant(hc, None, one, 0.0)
+    assert (q[0] == 127).all() and (q[1] == -127).all()
+    assert s[0] == np.float32(1.0) / np.float32(127.0) and s[1] == s[0]
+    rng = np.random.default_rng(41)
+    hf = rng.normal(0.0, 1.0, (3, H)).astype(np.float32)
+    hb = torch.from_numpy(hf).to(torch.bfloat16)
+    h_bits = hb.view(torch.int16).numpy().view(np.uint16)
+    neg_bits = (-hb).view(torch.int16).numpy().view(np.uint16)
+    h0, q0, s0, _ = o.residual_rmsnorm_quant(h_bits, neg_bits, one, 1e-6)
+    assert not q0.any() and not s0.any() and not (h0 & 0x7FFF).any()
+    db = torch.from_numpy(rng.normal(0.0, 0.5, (3, H)).astype(np.float32)).to(torch.bfloat16)
+    d_bits = db.view(torch.int16).numpy().view(np.uint16)
+    g_f = rng.uniform(0.5, 1.5, H).astype(np.float32)
+    g_bits = torch.from_numpy(g_f).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    h1, q1, s1, x1 = o.residual_rmsnorm_quant(h_bits, d_bits, g_bits, 1e-6)
+    ref_sum = (hb.float() + db.float()).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(h1, ref_sum)
+    h2x = (torch.from_numpy(hf).to(torch.bfloat16) * 2).view(torch.int16).numpy().view(np.uint16)
+    _, qa, _, xa = o.residual_rmsnorm_quant(h_bits, None, g_bits, 0.0)
+    _, qb, _, xb = o.residual_rmsnorm_quant(h2x, None, g_bits, 0.0)
+    assert np.array_equal(xa, xb) and np.array_equal(qa, qb)
+    hv = torch.from_numpy(h1.view(np.int16)).view(torch.bfloat16).double().numpy()
+    gv = torch.from_numpy(g_bits.view(np.int16)).view(torch.bfloat16).double().numpy()
+    xv = torch.from_numpy(x1.view(np.int16)).view(torch.bfloat16).double().numpy()
+    for m in range(3):
+        ref = gv * hv[m] / np.sqrt(np.mean(hv[m] ** 2) + 1e-6)
+        assert np.all(np.abs(xv[m] - ref) <= 2.0 ** -7 * np.abs(ref) + 1e-30)
+        xf = torch.from_numpy(x1[m].view(np.int16)).view(torch.bfloat16).float().numpy()
+        qe, se = quantize_row_exact(xf)
+        assert list(q1[m]) == list(qe) and np.float32(s1[m]) == se
+
 ALL_PINS = [
     pin_worked_example,
     pin_quantize_exact_rational,
@@ -344,4 +456,8 @@ ALL_PINS = [
     pin_accept_enumeration,
     pin_bf16,
     pin_linear_f64,
+    pin_layer_exp,
+    pin_silu,
+    pin_swiglu_quant,
+    pin_rmsnorm_quant,
 ]

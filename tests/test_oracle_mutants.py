@@ -37,6 +37,18 @@ MUTANTS = [
      "float v = mul ? xr[k] * mul[k] : xr[k];\n            float a = fabsf(v);",
      "float v = xr[k];\n            float a = fabsf(v);"),
     ("linear_f64_in_float", "double sum = 0.0;", "float sum = 0.0f;"),
+    ("exp_taylor_short", "for (int n = 6; n >= 0; --n) {", "for (int n = 6; n >= 2; --n) {"),
+    ("exp_drops_ln2_lo", "r = r - k * QVO_LN2_LO;", "r = r;"),
+    ("silu_sigmoid_sign", "float e = qvo_exp(-v);", "float e = qvo_exp(v);"),
+    ("swiglu_gate_up_swapped", "a[k] = qvo_silu(row[k]) * row[F + k];",
+     "a[k] = qvo_silu(row[F + k]) * row[k];"),
+    ("rmsnorm_sum_not_mean", "float var = (float)(ss / (double)H);", "float var = (float)ss;"),
+    ("rmsnorm_no_sqrt", "float sq = sqrtf(t);", "float sq = t;"),
+    ("rmsnorm_ignores_weight", "x[k] = qvo_f32_to_bf16_rne(qvo_bf16_to_f32(g[k]) * u);",
+     "x[k] = qvo_f32_to_bf16_rne(u);"),
+    ("residual_not_added",
+     "hr[k] = qvo_f32_to_bf16_rne(qvo_bf16_to_f32(hr[k]) + qvo_bf16_to_f32(d[m * H + k]));",
+     "hr[k] = hr[k];"),
 ]
 
 
