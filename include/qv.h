@@ -208,6 +208,54 @@ QV_API qv_status qv_lm_head_argmax_act(const void* x, qv_dtype x_dtype, const fl
                                        cudaStream_t stream);
 
 /*
+ * qv_rmsnorm_quant -- the residual add and RMSNorm in front of a layer's
+ * linears, fused with the a1 quantization of their input (one row per token).
+ *
+ *   gist.science/ja summary, section 2.2 item 3: the GEMM's result returns to
+ *   high precision before the non-linear layers, and the next linear's BF16
+ *   input is converted to INT8 online. The layer itself (a Qwen3-shaped
+ *   decoder with a bf16 residual stream) is this library's reading; the
+ *   summaries do not spell it out.
+ *
+ *   if delta:  h[m][k] = rne_bf16(fl32(h[m][k] + delta[m][k]))   (written back)
+ *   ss   = sum_k h[m][k]^2 in binary64;  var = fl32(ss / H)
+ *   rstd = fl32(1 / fl32(sqrt(fl32(var + eps))))
+ *   x[m][k] = rne_bf16(fl32(gamma[k] * rne_bf16(fl32(h[m][k] * rstd))))
+ *   xq, sx = the qv_quantize_act codes and scale of x (times act_mul if given)
+ *
+ *   h      [M*H] bf16, in/out (updated only when delta is given), 16-byte aligned
+ *   delta  [M*H] bf16 (a linear's bf16 output) or NULL, 16-byte aligned
+ *   gamma  [H] bf16 norm weights, 16-byte aligned; act_mul [H] fp32 or NULL
+ *   xq     [M*H] int8 out, sx [M] fp32 out; x_out [M*H] bf16 out or NULL (x)
+ *   1 <= M <= 65535, 16 <= H <= 16384, H % 16 == 0, eps >= 0 finite.
+ * The binary64 sum may be taken in any order; only its last bits depend on
+ * it. Non-finite inputs are outside the contract.
+ */
+QV_API qv_status qv_rmsnorm_quant(uint16_t* h, const uint16_t* delta, const uint16_t* gamma,
+                                  float eps, const float* act_mul, int M, int H,
+                                  int8_t* xq, float* sx, uint16_t* x_out, cudaStream_t stream);
+
+/*
+ * qv_swiglu_quant -- SiLU(gate) * up on the gate|up linear's output, fused
+ * with the a1 quantization of the down projection's input.
+ *
+ *   gist.science/ja summary, section 2.2 item 3 (non-linear layers in high
+ *   precision after dequantization, INT8 input for the next linear).
+ *
+ *   gate_up [M][2F] fp32: gate in columns [0, F), up in [F, 2F)
+ *   a[m][k] = fl32(fl32(g * sigma(g)) * up[m][k]), g = gate[m][k],
+ *   sigma(v) = fl32(1 / fl32(1 + E(-v))), E the library's binary32 exp:
+ *     v > 88 -> +inf, v < -87 -> 0, else k = rne(fl(v * 1.44269504)),
+ *     r = fl(fl(v - fl(k * 0.693145751953125)) - fl(k * 1.4286068e-6)),
+ *     E = fl(p(r) * 2^k) with p the degree-7 Taylor polynomial of e^r by
+ *     Horner (coefficients fl(1/n!)); within 2 ulp of e^v.
+ *   xq [M*F] int8, sx [M] fp32 = the per-token quantization of a.
+ *   gate_up 16-byte aligned; 1 <= M <= 65535, 16 <= F <= 32768, F % 16 == 0.
+ */
+QV_API qv_status qv_swiglu_quant(const float* gate_up, int M, int F, int8_t* xq, float* sx,
+                                 cudaStream_t stream);
+
+/*
  * qv_accept -- a4: greedy acceptance of the longest matching draft prefix
  * plus one verifier token.
  *

@@ -1,0 +1,274 @@
+// k_layer.cu -- the non-linear steps between the quantized linears of one
+// decoder layer, each fused with the per-token int8 quantization of the next
+// linear's input.
+//
+//   Quasar, gist.science/ja summary, section 2.2 item 3: the INT8 GEMM's
+//   result is dequantized back to high precision before the non-linear
+//   layers, and the next linear's BF16 input is quantized online;
+//   gist.science/fr summary, section 2 "Pipeline Technique".
+//
+// The layer follows the Qwen3-shaped decoder of the workloads with a bf16
+// residual stream (the summaries do not spell it out):
+//   residual_rmsnorm_quant  h = rne_bf16(h + d) (d: a linear's bf16 output),
+//                           ss = sum h_k^2 in binary64, var = fl32(ss / H),
+//                           rstd = fl32(1 / fl32(sqrt(fl32(var + eps)))),
+//                           x_k = rne_bf16(g_k * rne_bf16(fl32(h_k * rstd))),
+//                           then codes and the token scale of x (times the
+//                           optional smoothing multipliers);
+//   swiglu_quant            a_k = fl32(fl32(gate_k * sigma(gate_k)) * up_k) on
+//                           the fp32 gate|up output, sigma(v) =
+//                           fl32(1 / fl32(1 + E(-v))), then codes and scale.
+// E is exp by Cody and Waite's range reduction and a degree-7 Taylor
+// polynomial (layer_exp); every step is one binary32 operation in
+// round-to-nearest-even (explicit _rn intrinsics, never contracted), so the
+// results are determined by the definition alone. The only freedom is the
+// order of the binary64 sum of squares, which changes its last bits only.
+//
+// One CTA of 512 threads per row; the row is held in registers (H up to
+// 16384, F up to 32768).
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "qv_internal.h"
+#include "qv_ptx.cuh"
+
+namespace qv {
+namespace {
+
+constexpr int kLayerThreads = 512;
+constexpr int kNormVecs = 4;     // 8-bf16 vectors per thread: H <= 16384
+constexpr int kGluVecs = 16;     // 4-float vectors per thread: F <= 32768
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+__device__ __forceinline__ uint32_t bf16_bits(float f) {
+    return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(f));
+}
+__device__ __forceinline__ float round_bf16(float f) { return __uint_as_float(bf16_bits(f) << 16); }
+
+// exp(x): x > 88 -> +inf, x < -87 -> 0; otherwise k = rne(fl(x * log2 e)),
+// r = fl(fl(x - fl(k * LN2_HI)) - fl(k * LN2_LO)), p = the degree-7 Taylor
+// polynomial of e^r by Horner (coefficients fl(1/n!)), E = fl(p * 2^k).
+// LN2_HI has 16 significant bits, so k * LN2_HI is exact for |k| <= 127.
+__device__ __forceinline__ float layer_exp(float x) {
+    if (x > 88.0f) return __uint_as_float(0x7F800000u);
+    if (x < -87.0f) return 0.0f;
+    const float k = rintf(__fmul_rn(x, 1.44269504088896341f));
+    float r = __fsub_rn(x, __fmul_rn(k, 0.693145751953125f));
+    r = __fsub_rn(r, __fmul_rn(k, 1.42860682030941723212e-6f));
+    float p = 1.0f / 5040.0f;
+    p = __fadd_rn(__fmul_rn(p, r), 1.0f / 720.0f);
+    p = __fadd_rn(__fmul_rn(p, r), 1.0f / 120.0f);
+    p = __fadd_rn(__fmul_rn(p, r), 1.0f / 24.0f);
+    p = __fadd_rn(__fmul_rn(p, r), 1.0f / 6.0f);
+    p = __fadd_rn(__fmul_rn(p, r), 0.5f);
+    p = __fadd_rn(__fmul_rn(p, r), 1.0f);
+    p = __fadd_rn(__fmul_rn(p, r), 1.0f);
+    const float two_k = __uint_as_float((uint32_t)((int)k + 127) << 23);
+    return __fmul_rn(p, two_k);
+}
+
+__device__ __forceinline__ float silu(float v) {
+    const float den = __fadd_rn(1.0f, layer_exp(-v));
+    return __fmul_rn(v, __fdiv_rn(1.0f, den));
+}
+
+// Block-wide max of non-negative floats (all kLayerThreads threads call it).
+__device__ __forceinline__ float block_max(float v, float* red) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+    __syncthreads();
+    float m = red[0];
+#pragma unroll
+    for (int w = 1; w < kLayerThreads / 32; ++w) m = fmaxf(m, red[w]);
+    __syncthreads();   // red is reused
+    return m;
+}
+
+__device__ __forceinline__ double block_sum_f64(double v, double* red) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+    __syncthreads();
+    double s = 0.0;
+#pragma unroll
+    for (int w = 0; w < kLayerThreads / 32; ++w) s += red[w];
+    __syncthreads();
+    return s;
+}
+
+__device__ __forceinline__ uint32_t pack_codes4(float a, float b, float c, float d, float s, float r) {
+    return (uint32_t)(uint8_t)(int8_t)quant_code(a, s, r) |
+           ((uint32_t)(uint8_t)(int8_t)quant_code(b, s, r) << 8) |
+           ((uint32_t)(uint8_t)(int8_t)quant_code(c, s, r) << 16) |
+           ((uint32_t)(uint8_t)(int8_t)quant_code(d, s, r) << 24);
+}
+
+__global__ void __launch_bounds__(kLayerThreads)
+residual_rmsnorm_quant_kernel(uint16_t* __restrict__ h, const uint16_t* __restrict__ delta,
+                              const uint16_t* __restrict__ gamma, float eps, const float* __restrict__ mul,
+                              int H, int8_t* __restrict__ xq, float* __restrict__ sx,
+                              uint16_t* __restrict__ x_out) {
+    allow_dependent_launch();
+    const int row = blockIdx.x, tid = threadIdx.x;
+    const int nvec = H / 8;
+    uint4* hr = reinterpret_cast<uint4*>(h + (size_t)row * H);
+    const uint4* dr = delta ? reinterpret_cast<const uint4*>(delta + (size_t)row * H) : nullptr;
+    for (int v = tid * 8; v < nvec; v += kLayerThreads * 8) {     // one 128-byte line per 8 vectors
+        asm volatile("prefetch.global.L2 [%0];" :: "l"(hr + v));
+        if (dr) asm volatile("prefetch.global.L2 [%0];" :: "l"(dr + v));
+    }
+    grid_dependency_wait();
+    __shared__ double red_d[kLayerThreads / 32];
+    __shared__ float red_f[kLayerThreads / 32];
+
+    uint4 hv[kNormVecs];
+    double ss = 0.0;
+#pragma unroll
+    for (int u = 0; u < kNormVecs; ++u) {
+        const int v = tid + u * kLayerThreads;
+        hv[u] = make_uint4(0u, 0u, 0u, 0u);
+        if (v < nvec) {
+            hv[u] = hr[v];
+            if (dr) {
+                const uint4 dv = dr[v];
+                uint32_t* w = reinterpret_cast<uint32_t*>(&hv[u]);
+                const uint32_t* dw = reinterpret_cast<const uint32_t*>(&dv);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const uint32_t lo = bf16_bits(__fadd_rn(bf16_lo(w[j]), bf16_lo(dw[j])));
+                    const uint32_t hi = bf16_bits(__fadd_rn(bf16_hi(w[j]), bf16_hi(dw[j])));
+                    w[j] = lo | (hi << 16);
+                }
+                hr[v] = hv[u];
+            }
+            const uint32_t* w = reinterpret_cast<const uint32_t*>(&hv[u]);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const double a = (double)bf16_lo(w[j]), b = (double)bf16_hi(w[j]);
+                ss = __dadd_rn(ss, __dmul_rn(a, a));
+                ss = __dadd_rn(ss, __dmul_rn(b, b));
+            }
+        }
+    }
+    ss = block_sum_f64(ss, red_d);
+    const float var = __double2float_rn(__ddiv_rn(ss, (double)H));
+    const float rstd = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(var, eps)));
+
+    // x = rne_bf16(g * rne_bf16(h * rstd)), then the optional multipliers
+    float xv[kNormVecs][8];
+    float amax = 0.0f;
+#pragma unroll
+    for (int u = 0; u < kNormVecs; ++u) {
+        const int v = tid + u * kLayerThreads;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) xv[u][j] = 0.0f;
+        if (v < nvec) {
+            const uint4 gv = reinterpret_cast<const uint4*>(gamma)[v];
+            const uint32_t* w = reinterpret_cast<const uint32_t*>(&hv[u]);
+            const uint32_t* gw = reinterpret_cast<const uint32_t*>(&gv);
+            uint32_t xb[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float lo = round_bf16(__fmul_rn(bf16_lo(gw[j]), round_bf16(__fmul_rn(bf16_lo(w[j]), rstd))));
+                const float hi = round_bf16(__fmul_rn(bf16_hi(gw[j]), round_bf16(__fmul_rn(bf16_hi(w[j]), rstd))));
+                xb[j] = (__float_as_uint(lo) >> 16) | (__float_as_uint(hi) & 0xFFFF0000u);
+                xv[u][2 * j] = lo;
+                xv[u][2 * j + 1] = hi;
+            }
+            if (x_out) reinterpret_cast<uint4*>(x_out + (size_t)row * H)[v] = make_uint4(xb[0], xb[1], xb[2], xb[3]);
+            if (mul) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) xv[u][j] = __fmul_rn(xv[u][j], __ldg(mul + v * 8 + j));
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(xv[u][j]));
+        }
+    }
+    amax = block_max(amax, red_f);
+    const float s = __fdiv_rn(amax, 127.0f);
+    const float r = __frcp_rn(s);
+    if (tid == 0) sx[row] = s;
+    int8_t* qr = xq + (size_t)row * H;
+#pragma unroll
+    for (int u = 0; u < kNormVecs; ++u) {
+        const int v = tid + u * kLayerThreads;
+        if (v < nvec)
+            *reinterpret_cast<uint2*>(qr + v * 8) =
+                make_uint2(pack_codes4(xv[u][0], xv[u][1], xv[u][2], xv[u][3], s, r),
+                           pack_codes4(xv[u][4], xv[u][5], xv[u][6], xv[u][7], s, r));
+    }
+}
+
+__global__ void __launch_bounds__(kLayerThreads)
+swiglu_quant_kernel(const float* __restrict__ gate_up, int F, int8_t* __restrict__ xq, float* __restrict__ sx) {
+    allow_dependent_launch();
+    const int row = blockIdx.x, tid = threadIdx.x;
+    const int nvec = F / 4;
+    const float4* gr = reinterpret_cast<const float4*>(gate_up + (size_t)row * 2 * F);
+    const float4* ur = gr + nvec;
+    for (int v = tid * 8; v < nvec; v += kLayerThreads * 8) {     // one 128-byte line per 8 vectors
+        asm volatile("prefetch.global.L2 [%0];" :: "l"(gr + v));
+        asm volatile("prefetch.global.L2 [%0];" :: "l"(ur + v));
+    }
+    grid_dependency_wait();
+    __shared__ float red_f[kLayerThreads / 32];
+
+    float4 av[kGluVecs];
+    float amax = 0.0f;
+#pragma unroll
+    for (int u = 0; u < kGluVecs; ++u) {
+        const int v = tid + u * kLayerThreads;
+        av[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (v < nvec) {
+            const float4 g = gr[v], up = ur[v];
+            av[u] = make_float4(__fmul_rn(silu(g.x), up.x), __fmul_rn(silu(g.y), up.y),
+                                __fmul_rn(silu(g.z), up.z), __fmul_rn(silu(g.w), up.w));
+            amax = fmaxf(amax, fmaxf(fmaxf(fabsf(av[u].x), fabsf(av[u].y)), fmaxf(fabsf(av[u].z), fabsf(av[u].w))));
+        }
+    }
+    amax = block_max(amax, red_f);
+    const float s = __fdiv_rn(amax, 127.0f);
+    const float r = __frcp_rn(s);
+    if (tid == 0) sx[row] = s;
+    int8_t* qr = xq + (size_t)row * F;
+#pragma unroll
+    for (int u = 0; u < kGluVecs; ++u) {
+        const int v = tid + u * kLayerThreads;
+        if (v < nvec)
+            *reinterpret_cast<uint32_t*>(qr + v * 4) = pack_codes4(av[u].x, av[u].y, av[u].z, av[u].w, s, r);
+    }
+}
+
+cudaError_t launch_pdl(const void* kernel, int rows, void** args, cudaStream_t s) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(rows);
+    cfg.blockDim = dim3(kLayerThreads);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelExC(&cfg, kernel, args);
+}
+
+}  // namespace
+
+cudaError_t launch_residual_rmsnorm_quant(uint16_t* h, const uint16_t* delta, const uint16_t* gamma, float eps,
+                                          const float* mul, int M, int H, int8_t* xq, float* sx,
+                                          uint16_t* x_out, cudaStream_t s) {
+    void* args[] = {&h, &delta, &gamma, &eps, &mul, &H, &xq, &sx, &x_out};
+    return launch_pdl(reinterpret_cast<const void*>(residual_rmsnorm_quant_kernel), M, args, s);
+}
+
+cudaError_t launch_swiglu_quant(const float* gate_up, int M, int F, int8_t* xq, float* sx, cudaStream_t s) {
+    void* args[] = {&gate_up, &F, &xq, &sx};
+    return launch_pdl(reinterpret_cast<const void*>(swiglu_quant_kernel), M, args, s);
+}
+
+}  // namespace qv

@@ -379,6 +379,44 @@ qv_status qv_lm_head_argmax_act(const void* x, qv_dtype x_dtype, const float* ac
                       workspace, workspace_bytes, stream);
 }
 
+qv_status qv_rmsnorm_quant(uint16_t* h, const uint16_t* delta, const uint16_t* gamma, float eps,
+                           const float* act_mul, int M, int H, int8_t* xq, float* sx, uint16_t* x_out,
+                           cudaStream_t stream) {
+    if (!h || !gamma || !xq || !sx) return fail(QV_ERR_INVALID_ARG, "null pointer");
+    if (M < 1 || M > 65535) return fail(QV_ERR_INVALID_ARG, "M=%d outside [1, 65535]", M);
+    if (H < 16 || H > 16384 || H % 16 != 0)
+        return fail(QV_ERR_INVALID_ARG, "H=%d must be a multiple of 16 in [16, 16384]", H);
+    if (!(eps >= 0.0f) || eps > 3.0e38f) return fail(QV_ERR_INVALID_ARG, "eps must be finite and >= 0");
+    if (!aligned(h, 16) || (delta && !aligned(delta, 16)) || !aligned(gamma, 16) || !aligned(xq, 16) ||
+        (act_mul && !aligned(act_mul, 16)) || (x_out && !aligned(x_out, 16)) || !aligned(sx, 4))
+        return fail(QV_ERR_INVALID_ARG, "h, delta, gamma, xq, act_mul, x_out must be 16-byte aligned");
+    QV_CHECK_DEV(h);
+    QV_CHECK_DEV(delta);
+    QV_CHECK_DEV(gamma);
+    QV_CHECK_DEV(act_mul);
+    QV_CHECK_DEV(xq);
+    QV_CHECK_DEV(sx);
+    QV_CHECK_DEV(x_out);
+    cudaError_t e = qv::launch_residual_rmsnorm_quant(h, delta, gamma, eps, act_mul, M, H, xq, sx, x_out, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "qv_rmsnorm_quant launch");
+    return ok();
+}
+
+qv_status qv_swiglu_quant(const float* gate_up, int M, int F, int8_t* xq, float* sx, cudaStream_t stream) {
+    if (!gate_up || !xq || !sx) return fail(QV_ERR_INVALID_ARG, "null pointer");
+    if (M < 1 || M > 65535) return fail(QV_ERR_INVALID_ARG, "M=%d outside [1, 65535]", M);
+    if (F < 16 || F > 32768 || F % 16 != 0)
+        return fail(QV_ERR_INVALID_ARG, "F=%d must be a multiple of 16 in [16, 32768]", F);
+    if (!aligned(gate_up, 16) || !aligned(xq, 16) || !aligned(sx, 4))
+        return fail(QV_ERR_INVALID_ARG, "gate_up and xq must be 16-byte aligned");
+    QV_CHECK_DEV(gate_up);
+    QV_CHECK_DEV(xq);
+    QV_CHECK_DEV(sx);
+    cudaError_t e = qv::launch_swiglu_quant(gate_up, M, F, xq, sx, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "qv_swiglu_quant launch");
+    return ok();
+}
+
 qv_status qv_accept(const int32_t* verify_tokens, const int32_t* draft, int B, int gamma,
                     int32_t* accept_len, int32_t* out_tokens, cudaStream_t stream) {
     if (!verify_tokens || !accept_len || !out_tokens) return fail(QV_ERR_INVALID_ARG, "null pointer");

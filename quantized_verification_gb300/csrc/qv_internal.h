@@ -110,6 +110,12 @@ constexpr size_t kMaxDynSmem = 232448;
 constexpr size_t kMinSmemOneCtaPerSm = 118 * 1024;
 cudaError_t launch_verify_stack(const StackLaunch& a, int num_sms, cudaStream_t s);
 cudaError_t launch_bf16_stream(const Bf16Launch& a, int num_sms, cudaStream_t s);
+// The layer's fused non-linear steps (k_layer.cu).
+cudaError_t launch_residual_rmsnorm_quant(uint16_t* h, const uint16_t* delta, const uint16_t* gamma, float eps,
+                                          const float* mul, int M, int H, int8_t* xq, float* sx,
+                                          uint16_t* x_out, cudaStream_t s);
+cudaError_t launch_swiglu_quant(const float* gate_up, int M, int F, int8_t* xq, float* sx, cudaStream_t s);
+
 cudaError_t launch_quantize_rows(const void* x, bool bf16, int rows, int K,
                                  const float* mul, int8_t* q, float* scale,
                                  bool early_dependents, cudaStream_t s);

@@ -26,7 +26,8 @@ QV_MAX_M = 256
 EXPORTS = ("qv_quantize_act", "qv_w8a8_linear", "qv_lm_head_argmax", "qv_accept",
            "qv_quantize_weight", "qv_bf16_linear", "qv_workspace_bytes",
            "qv_last_error", "qv_device_error", "qv_num_sms", "qv_w8a8_linear_noalloc",
-           "qv_verify_stack", "qv_w8a8_linear_act", "qv_lm_head_argmax_act")
+           "qv_verify_stack", "qv_w8a8_linear_act", "qv_lm_head_argmax_act",
+           "qv_rmsnorm_quant", "qv_swiglu_quant")
 MAX_STACK_M = 16
 
 
@@ -71,6 +72,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
                                       P, I, I, P, P, P, P, P, S, P]
         L.qv_w8a8_linear_act.argtypes = [P, I, P, I, I, P, P, I, P, I, P, S, P]
         L.qv_lm_head_argmax_act.argtypes = [P, I, P, I, I, P, P, I, P, P, P, S, P]
+        L.qv_rmsnorm_quant.argtypes = [P, P, P, ctypes.c_float, P, I, I, P, P, P, P]
+        L.qv_swiglu_quant.argtypes = [P, I, I, P, P, P]
         L.qv_workspace_bytes.argtypes = [I, I, I, I]
         L.qv_workspace_bytes.restype = S
         L.qv_last_error.argtypes = []
@@ -135,6 +138,35 @@ def qv_quantize_act(x, xq, sx, act_mul=None, stream=None):
         _need(act_mul.shape == (K,) and act_mul.dtype == torch.float32, "act_mul must be float32 [K]")
     _check(load().qv_quantize_act(_ptr(x), _dtype(x), M, K, _ptr(act_mul), _ptr(xq), _ptr(sx),
                                   ctypes.c_void_p(_stream(stream))))
+
+
+def qv_rmsnorm_quant(h, gamma, xq, sx, delta=None, eps=1e-6, act_mul=None, x_out=None, stream=None):
+    """h [M, H] bf16 (updated in place when delta is given: h += delta in
+    bf16); xq [M, H] int8, sx [M] = per-token codes of RMSNorm(h) * gamma."""
+    M, H = h.shape
+    _need(h.dtype == torch.bfloat16, "h must be bf16 [M, H]")
+    _need(gamma.shape == (H,) and gamma.dtype == torch.bfloat16, "gamma must be bf16 [H]")
+    _need(xq.shape == (M, H) and xq.dtype == torch.int8, "xq must be int8 [M, H]")
+    _need(sx.shape == (M,) and sx.dtype == torch.float32, "sx must be float32 [M]")
+    if delta is not None:
+        _need(delta.shape == (M, H) and delta.dtype == torch.bfloat16, "delta must be bf16 [M, H]")
+    if act_mul is not None:
+        _need(act_mul.shape == (H,) and act_mul.dtype == torch.float32, "act_mul must be float32 [H]")
+    if x_out is not None:
+        _need(x_out.shape == (M, H) and x_out.dtype == torch.bfloat16, "x_out must be bf16 [M, H]")
+    _check(load().qv_rmsnorm_quant(_ptr(h), _ptr(delta), _ptr(gamma), ctypes.c_float(eps), _ptr(act_mul),
+                                   M, H, _ptr(xq), _ptr(sx), _ptr(x_out), ctypes.c_void_p(_stream(stream))))
+
+
+def qv_swiglu_quant(gate_up, xq, sx, stream=None):
+    """gate_up [M, 2F] fp32 (gate | up) -> xq [M, F] int8, sx [M]: per-token
+    codes of SiLU(gate) * up."""
+    M, F2 = gate_up.shape
+    F = F2 // 2
+    _need(gate_up.dtype == torch.float32 and F2 == 2 * F, "gate_up must be float32 [M, 2F]")
+    _need(xq.shape == (M, F) and xq.dtype == torch.int8, "xq must be int8 [M, F]")
+    _need(sx.shape == (M,) and sx.dtype == torch.float32, "sx must be float32 [M]")
+    _check(load().qv_swiglu_quant(_ptr(gate_up), M, F, _ptr(xq), _ptr(sx), ctypes.c_void_p(_stream(stream))))
 
 
 def qv_quantize_weight(w, wq, sw, stream=None):

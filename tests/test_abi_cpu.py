@@ -92,6 +92,21 @@ def test_host_validation_without_gpu(lib):
     assert lib.qv_lm_head_argmax_act(fake, 1, None, 5, 256, fake, fake, 8, None, None, fake, 1 << 20, None) == qv.QV_ERR_INVALID_ARG
     assert b"tokens" in lib.qv_last_error()
     assert lib.qv_lm_head_argmax_act(fake, 1, None, 5, 250, fake, fake, 8, fake, None, fake, 1 << 20, None) == qv.QV_ERR_INVALID_ARG
+    # the layer's fused non-linear steps
+    F32 = ctypes.c_float
+    assert lib.qv_rmsnorm_quant(None, None, fake, F32(1e-6), None, 5, 256, fake, fake, None, None) == qv.QV_ERR_INVALID_ARG
+    assert lib.qv_rmsnorm_quant(fake, None, fake, F32(1e-6), None, 5, 264, fake, fake, None, None) == qv.QV_ERR_INVALID_ARG
+    assert b"multiple of 16" in lib.qv_last_error()
+    assert lib.qv_rmsnorm_quant(fake, None, fake, F32(1e-6), None, 5, 16400, fake, fake, None, None) == qv.QV_ERR_INVALID_ARG
+    assert lib.qv_rmsnorm_quant(fake, None, fake, F32(-1.0), None, 5, 256, fake, fake, None, None) == qv.QV_ERR_INVALID_ARG
+    assert lib.qv_rmsnorm_quant(fake, P(0x1008), fake, F32(1e-6), None, 5, 256, fake, fake, None, None) == qv.QV_ERR_INVALID_ARG
+    assert b"aligned" in lib.qv_last_error()
+    assert lib.qv_rmsnorm_quant(fake, None, fake, F32(1e-6), None, 0, 256, fake, fake, None, None) == qv.QV_ERR_INVALID_ARG
+    assert lib.qv_swiglu_quant(None, 5, 256, fake, fake, None) == qv.QV_ERR_INVALID_ARG
+    assert lib.qv_swiglu_quant(fake, 5, 8, fake, fake, None) == qv.QV_ERR_INVALID_ARG
+    assert lib.qv_swiglu_quant(fake, 5, 32784, fake, fake, None) == qv.QV_ERR_INVALID_ARG
+    assert lib.qv_swiglu_quant(P(0x1004), 5, 256, fake, fake, None) == qv.QV_ERR_INVALID_ARG
+    assert b"aligned" in lib.qv_last_error()
 
 
 def test_binding_rejects_host_tensors(lib):
