@@ -422,6 +422,26 @@ def main():
            "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3}
 
     cpu = None
+    # ---- chained decoder layers (residual stream, RMSNorm, SwiGLU between
+    # the linears): the same weights and launch count, a real layer chain
+    layer_chain = None
+    if rank == 0:
+        stack.prepare_chain()
+        chain_graph = stack.capture_chain()
+        for _ in range(3):
+            chain_graph.replay()
+        torch.cuda.synchronize()
+        chain_ms = time_graph(torch, chain_graph, max(20, args.steps // 5), stream)
+        log(f"layer chain {chain_ms:.4f} ms/step")
+        layer_chain = {"ms_per_step": chain_ms, "tokens_per_s": stack.M / (chain_ms * 1e-3),
+                       "weight_stream_gbs": stack.weight_bytes() / (chain_ms * 1e-3) / 1e9,
+                       "launches_per_step": 8 * stack.layers + 3,
+                       "path": "per layer: qv_rmsnorm_quant (residual add + RMSNorm + quant) -> qkv, "
+                               "qv_quantize_act (seeded attention output) -> o, qv_rmsnorm_quant -> qv_w8a8_swiglu "
+                               "(gate|up with SiLU(gate)*up in the epilogue) -> qv_quantize_act -> down (bf16); "
+                               "final qv_rmsnorm_quant -> LM head "
+                               "argmax -> accept; one CUDA graph"}
+
     if rank == 0 and world == 1 and not args.no_cpu:
         cpu = cpu_baseline(args.cpu_seconds)
 
@@ -448,6 +468,7 @@ def main():
                        "samples": clk["samples"]},
             "comparator": comparator,
             "paths_ms_per_step": paths_ms,
+            "layer_chain": layer_chain,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -208,6 +208,28 @@ QV_API qv_status qv_lm_head_argmax_act(const void* x, qv_dtype x_dtype, const fl
                                        cudaStream_t stream);
 
 /*
+ * qv_w8a8_swiglu -- the gate|up projection of a layer's MLP with SiLU(gate) *
+ * up fused into its epilogue (a2 with a SwiGLU epilogue).
+ *
+ *   gist.science/ja summary, section 2.2 item 3 (INT8 GEMM, INT32
+ *   accumulation, dequantization to high precision before the non-linear
+ *   layer, here applied in the same kernel).
+ *
+ *   wq_gu [2F][K] int8, sw_gu [2F]: the gate and up weight rows interleaved
+ *     by 64: rows 128t .. 128t+63 are gate rows 64t .. 64t+63 and rows
+ *     128t+64 .. 128t+127 the up rows 64t .. 64t+63 (so one 128-channel tile
+ *     holds both operands of 64 features). F % 64 == 0.
+ *   y_g, y_u = the qv_w8a8_linear outputs (fp32) of the gate and up rows
+ *   a [M][F] fp32 out: a[m][f] = fl32(silu(y_g[m][f]) * y_u[m][f]), silu as
+ *     in qv_swiglu_quant.
+ *   xq, sx, M, K, workspace: as qv_w8a8_linear (workspace:
+ *     qv_workspace_bytes(QV_OP_LINEAR, M, K, 2F)).
+ */
+QV_API qv_status qv_w8a8_swiglu(const int8_t* xq, const float* sx, int M, int K,
+                                const int8_t* wq_gu, const float* sw_gu, int F, float* a,
+                                void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * qv_rmsnorm_quant -- the residual add and RMSNorm in front of a layer's
  * linears, fused with the a1 quantization of their input (one row per token).
  *
@@ -228,8 +250,10 @@ QV_API qv_status qv_lm_head_argmax_act(const void* x, qv_dtype x_dtype, const fl
  *   gamma  [H] bf16 norm weights, 16-byte aligned; act_mul [H] fp32 or NULL
  *   xq     [M*H] int8 out, sx [M] fp32 out; x_out [M*H] bf16 out or NULL (x)
  *   1 <= M <= 65535, 16 <= H <= 16384, H % 16 == 0, eps >= 0 finite.
- * The binary64 sum may be taken in any order; only its last bits depend on
- * it. Non-finite inputs are outside the contract.
+ * The kernel adds the exact binary32 squares in float-float (about 48 bits),
+ * which matches the binary64 sum to about 2^-47 relative: var is the same
+ * unless ss / H lies that close to a binary32 rounding boundary. Non-finite
+ * inputs are outside the contract.
  */
 QV_API qv_status qv_rmsnorm_quant(uint16_t* h, const uint16_t* delta, const uint16_t* gamma,
                                   float eps, const float* act_mul, int M, int H,

@@ -21,8 +21,10 @@
 // E is exp by Cody and Waite's range reduction and a degree-7 Taylor
 // polynomial (layer_exp); every step is one binary32 operation in
 // round-to-nearest-even (explicit _rn intrinsics, never contracted), so the
-// results are determined by the definition alone. The only freedom is the
-// order of the binary64 sum of squares, which changes its last bits only.
+// results are determined by the definition alone, except for the sum of
+// squares: the kernel adds the (exact) binary32 squares in float-float, which
+// agrees with the definition's binary64 sum to about 2^-47 relative, far
+// below the binary32 rounding of var that follows.
 //
 // One CTA of 512 threads per row; the row is held in registers (H up to
 // 16384, F up to 32768).
@@ -49,33 +51,6 @@ __device__ __forceinline__ uint32_t bf16_bits(float f) {
 }
 __device__ __forceinline__ float round_bf16(float f) { return __uint_as_float(bf16_bits(f) << 16); }
 
-// exp(x): x > 88 -> +inf, x < -87 -> 0; otherwise k = rne(fl(x * log2 e)),
-// r = fl(fl(x - fl(k * LN2_HI)) - fl(k * LN2_LO)), p = the degree-7 Taylor
-// polynomial of e^r by Horner (coefficients fl(1/n!)), E = fl(p * 2^k).
-// LN2_HI has 16 significant bits, so k * LN2_HI is exact for |k| <= 127.
-__device__ __forceinline__ float layer_exp(float x) {
-    if (x > 88.0f) return __uint_as_float(0x7F800000u);
-    if (x < -87.0f) return 0.0f;
-    const float k = rintf(__fmul_rn(x, 1.44269504088896341f));
-    float r = __fsub_rn(x, __fmul_rn(k, 0.693145751953125f));
-    r = __fsub_rn(r, __fmul_rn(k, 1.42860682030941723212e-6f));
-    float p = 1.0f / 5040.0f;
-    p = __fadd_rn(__fmul_rn(p, r), 1.0f / 720.0f);
-    p = __fadd_rn(__fmul_rn(p, r), 1.0f / 120.0f);
-    p = __fadd_rn(__fmul_rn(p, r), 1.0f / 24.0f);
-    p = __fadd_rn(__fmul_rn(p, r), 1.0f / 6.0f);
-    p = __fadd_rn(__fmul_rn(p, r), 0.5f);
-    p = __fadd_rn(__fmul_rn(p, r), 1.0f);
-    p = __fadd_rn(__fmul_rn(p, r), 1.0f);
-    const float two_k = __uint_as_float((uint32_t)((int)k + 127) << 23);
-    return __fmul_rn(p, two_k);
-}
-
-__device__ __forceinline__ float silu(float v) {
-    const float den = __fadd_rn(1.0f, layer_exp(-v));
-    return __fmul_rn(v, __fdiv_rn(1.0f, den));
-}
-
 // Block-wide max of non-negative floats (all kLayerThreads threads call it).
 __device__ __forceinline__ float block_max(float v, float* red) {
 #pragma unroll
@@ -89,16 +64,51 @@ __device__ __forceinline__ float block_max(float v, float* red) {
     return m;
 }
 
-__device__ __forceinline__ double block_sum_f64(double v, double* red) {
+// Float-float (hi, lo) sums built from Knuth's error-free TwoSum: hi + lo
+// carries about 48 significant bits. Explicit _rn operations: a contracted
+// or reassociated step would lose the error term.
+struct FF {
+    float hi, lo;
+};
+__device__ __forceinline__ FF ff_add(FF a, float b) {
+    const float t = __fadd_rn(a.hi, b);
+    const float bv = __fsub_rn(t, a.hi);
+    const float err = __fadd_rn(__fsub_rn(a.hi, __fsub_rn(t, bv)), __fsub_rn(b, bv));
+    return FF{t, __fadd_rn(a.lo, err)};
+}
+__device__ __forceinline__ FF ff_add(FF a, FF b) {
+    FF r = ff_add(a, b.hi);
+    r.lo = __fadd_rn(r.lo, b.lo);
+    return r;
+}
+
+// sum_k h_k^2 of a row: every square of a bf16 value is exact in binary32;
+// the squares are added in float-float and the block's total returned, to
+// every thread, as the binary64 value hi + lo. It agrees with a binary64 sum
+// in any order to about 2^-47 relative.
+__device__ __forceinline__ double block_sum_squares(FF v, FF* red, double* total) {
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+    for (int off = 16; off > 0; off >>= 1) {
+        FF o;
+        o.hi = __shfl_xor_sync(0xffffffffu, v.hi, off);
+        o.lo = __shfl_xor_sync(0xffffffffu, v.lo, off);
+        v = ff_add(v, o);
+    }
     if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
     __syncthreads();
-    double s = 0.0;
+    if (threadIdx.x < 32) {
+        FF w = threadIdx.x < kLayerThreads / 32 ? red[threadIdx.x] : FF{0.0f, 0.0f};
 #pragma unroll
-    for (int w = 0; w < kLayerThreads / 32; ++w) s += red[w];
+        for (int off = 8; off > 0; off >>= 1) {
+            FF o;
+            o.hi = __shfl_xor_sync(0xffffffffu, w.hi, off);
+            o.lo = __shfl_xor_sync(0xffffffffu, w.lo, off);
+            w = ff_add(w, o);
+        }
+        if (threadIdx.x == 0) *total = __dadd_rn((double)w.hi, (double)w.lo);
+    }
     __syncthreads();
-    return s;
+    return *total;
 }
 
 __device__ __forceinline__ uint32_t pack_codes4(float a, float b, float c, float d, float s, float r) {
@@ -123,11 +133,13 @@ residual_rmsnorm_quant_kernel(uint16_t* __restrict__ h, const uint16_t* __restri
         if (dr) asm volatile("prefetch.global.L2 [%0];" :: "l"(dr + v));
     }
     grid_dependency_wait();
-    __shared__ double red_d[kLayerThreads / 32];
+    __shared__ FF red_ff[kLayerThreads / 32];
     __shared__ float red_f[kLayerThreads / 32];
+    __shared__ double ss_total;
+    __shared__ float rstd_s;
 
     uint4 hv[kNormVecs];
-    double ss = 0.0;
+    FF ss{0.0f, 0.0f};
 #pragma unroll
     for (int u = 0; u < kNormVecs; ++u) {
         const int v = tid + u * kLayerThreads;
@@ -149,15 +161,19 @@ residual_rmsnorm_quant_kernel(uint16_t* __restrict__ h, const uint16_t* __restri
             const uint32_t* w = reinterpret_cast<const uint32_t*>(&hv[u]);
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                const double a = (double)bf16_lo(w[j]), b = (double)bf16_hi(w[j]);
-                ss = __dadd_rn(ss, __dmul_rn(a, a));
-                ss = __dadd_rn(ss, __dmul_rn(b, b));
+                const float a = bf16_lo(w[j]), b = bf16_hi(w[j]);
+                ss = ff_add(ss, __fmul_rn(a, a));     // exact: 8-bit significands
+                ss = ff_add(ss, __fmul_rn(b, b));
             }
         }
     }
-    ss = block_sum_f64(ss, red_d);
-    const float var = __double2float_rn(__ddiv_rn(ss, (double)H));
-    const float rstd = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(var, eps)));
+    const double sum = block_sum_squares(ss, red_ff, &ss_total);
+    if (tid == 0) {
+        const float var = __double2float_rn(__ddiv_rn(sum, (double)H));
+        rstd_s = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(var, eps)));
+    }
+    __syncthreads();
+    const float rstd = rstd_s;
 
     // x = rne_bf16(g * rne_bf16(h * rstd)), then the optional multipliers
     float xv[kNormVecs][8];

@@ -318,7 +318,7 @@ w8a8_stream_kernel(const __grid_constant__ CUtensorMap tmap_w,
         const int nt = i / p.KT;
         const int seg_begin = i;
         const int seg_end = min(b, (nt + 1) * p.KT);
-        segment_start(est, p, nt, tid);
+        segment_start<EPI>(est, p, nt, tid);
 #pragma unroll
         for (int blk = 0; blk < BPW; ++blk)
 #pragma unroll
@@ -1143,14 +1143,14 @@ cudaError_t launch_w8a8_stream(const W8A8Launch& a, int num_sms, cudaStream_t s)
     p.keys = reinterpret_cast<unsigned long long*>(ws + L.keys);
     p.done = reinterpret_cast<unsigned*>(ws + L.done);
     const int grid = stream_grid(p.T, num_sms);
+#define QV_W8A8_LAUNCH(NGV, EPIV)                                                            \
+    launch_ex(w8a8_stream_kernel<NGV, (int)EPIV>, grid, (kW8A8Warps + 1) * 32,               \
+              Cfg<NGV>::SmemBytes, s, a.tmap_w, a.tmap_x, p)
 #define QV_W8A8_CASE(NGV)                                                                    \
     case NGV:                                                                                \
-        return lm ? launch_ex(w8a8_stream_kernel<NGV, (int)Epi::LmHead>, grid,               \
-                              (kW8A8Warps + 1) * 32, Cfg<NGV>::SmemBytes, s, a.tmap_w,       \
-                              a.tmap_x, p)                                                   \
-                  : launch_ex(w8a8_stream_kernel<NGV, (int)Epi::Linear>, grid,               \
-                              (kW8A8Warps + 1) * 32, Cfg<NGV>::SmemBytes, s, a.tmap_w,       \
-                              a.tmap_x, p);
+        return lm ? QV_W8A8_LAUNCH(NGV, Epi::LmHead)                                         \
+                  : a.epi == Epi::SwiGLU ? QV_W8A8_LAUNCH(NGV, Epi::SwiGLU)                  \
+                                         : QV_W8A8_LAUNCH(NGV, Epi::Linear);
     switch (a.MP / 8) {   // up to 32 tokens; more go to the tcgen05 kernel
         QV_W8A8_CASE(1)
         QV_W8A8_CASE(2)
@@ -1158,6 +1158,7 @@ cudaError_t launch_w8a8_stream(const W8A8Launch& a, int num_sms, cudaStream_t s)
         default: return cudaErrorInvalidValue;
     }
 #undef QV_W8A8_CASE
+#undef QV_W8A8_LAUNCH
 }
 
 cudaError_t launch_bf16_stream(const Bf16Launch& a, int num_sms, cudaStream_t s) {

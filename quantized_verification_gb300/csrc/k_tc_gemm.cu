@@ -284,7 +284,7 @@ w8a8_tc_kernel(const __grid_constant__ CUtensorMap tmap_w,
         const int nt = i / p.KT;
         const int seg_begin = i;
         const int seg_end = min(b, (nt + 1) * p.KT);
-        segment_start(est, p, nt, tid);
+        segment_start<EPI>(est, p, nt, tid);
 #pragma unroll
         for (int m = 0; m < MPH; ++m) acc[m] = 0;
 
@@ -414,17 +414,18 @@ cudaError_t launch_w8a8_tc(const W8A8Launch& a, int num_sms, cudaStream_t s) {
     p.keys = reinterpret_cast<unsigned long long*>(ws + L.keys);
     p.done = reinterpret_cast<unsigned*>(ws + L.done);
     const int grid = stream_grid(p.T, num_sms);
+#define QV_TC_LAUNCH(MPV, EPIV) \
+    launch_tc(w8a8_tc_kernel<MPV, (int)EPIV>, grid, TcCfg<MPV>::SmemBytes, s, a.tmap_w, a.tmap_x, p)
 #define QV_TC_CASE(MPV)                                                                           \
     case MPV:                                                                                     \
-        return lm ? launch_tc(w8a8_tc_kernel<MPV, (int)Epi::LmHead>, grid, TcCfg<MPV>::SmemBytes, \
-                              s, a.tmap_w, a.tmap_x, p)                                           \
-                  : launch_tc(w8a8_tc_kernel<MPV, (int)Epi::Linear>, grid, TcCfg<MPV>::SmemBytes, \
-                              s, a.tmap_w, a.tmap_x, p);
+        return lm ? QV_TC_LAUNCH(MPV, Epi::LmHead)                                                \
+                  : a.epi == Epi::SwiGLU ? QV_TC_LAUNCH(MPV, Epi::SwiGLU) : QV_TC_LAUNCH(MPV, Epi::Linear);
     switch (a.MP) {   // fewer tokens go to the mma.sync streaming kernel
         QV_TC_CASE(64)
         default: return cudaErrorInvalidValue;
     }
 #undef QV_TC_CASE
+#undef QV_TC_LAUNCH
 }
 
 cudaError_t read_and_clear_tc_gemm_error(unsigned* code) {

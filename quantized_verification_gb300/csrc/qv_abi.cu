@@ -273,6 +273,41 @@ qv_status qv_w8a8_linear(const int8_t* xq, const float* sx, int M, int K, const 
     return ok();
 }
 
+qv_status qv_w8a8_swiglu(const int8_t* xq, const float* sx, int M, int K, const int8_t* wq_gu,
+                         const float* sw_gu, int F, float* a, void* workspace, size_t workspace_bytes,
+                         cudaStream_t stream) {
+    if (F < 64 || F % 64 != 0) return fail(QV_ERR_INVALID_ARG, "F=%d must be a positive multiple of 64", F);
+    qv_status st = check_gemm_common(xq, sx, M, K, wq_gu, sw_gu, 2 * F, workspace, workspace_bytes, QV_OP_LINEAR);
+    if (st != QV_OK) return st;
+    if (!a) return fail(QV_ERR_INVALID_ARG, "a is null");
+    if (!aligned(a, 4)) return fail(QV_ERR_INVALID_ARG, "a misaligned");
+    QV_CHECK_DEV(a);
+    cudaError_t e;
+    const int sms = sms_of_current_device(&e);
+    if (e != cudaSuccess) return cuda_fail(e, "device query");
+    qv::W8A8Launch L = {};
+    if ((st = encode_2d(&L.tmap_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, wq_gu, (uint64_t)K, (uint64_t)(2 * F),
+                        qv::kTileKBytes, qv::kTileN)) != QV_OK)
+        return st;
+    for (int m0 = 0; m0 < M; m0 += qv::kMaxMPerLaunch) {
+        const int mc = M - m0 < qv::kMaxMPerLaunch ? M - m0 : qv::kMaxMPerLaunch;
+        L.M = mc; L.N = 2 * F; L.K = K; L.MP = mp_for(mc);
+        if ((st = encode_2d(&L.tmap_x, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, xq + (size_t)m0 * K,
+                            (uint64_t)K, (uint64_t)mc, qv::kTileKBytes, (uint32_t)L.MP)) != QV_OK)
+            return st;
+        L.sx = sx + m0; L.sw = sw_gu;
+        L.y = a + (size_t)m0 * F;
+        L.y_bf16 = 0;
+        L.acc_debug = nullptr;
+        L.tokens = nullptr; L.max_logit = nullptr;
+        L.ws = workspace;
+        L.epi = qv::Epi::SwiGLU;
+        e = launch_w8a8(L, sms, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "qv_w8a8_swiglu launch");
+    }
+    return ok();
+}
+
 qv_status qv_lm_head_argmax(const int8_t* xq, const float* sx, int M, int K, const int8_t* wq,
                             const float* sw, int V, int32_t* tokens, float* max_logit,
                             void* workspace, size_t workspace_bytes, cudaStream_t stream) {

@@ -38,7 +38,10 @@ struct WsLayout {
 };
 WsLayout ws_layout(int mp, int n, bool lm_head, bool stack = false);
 
-enum class Epi : int { Linear = 0, LmHead = 1 };
+// Linear: y = dequant(acc). LmHead: greedy argmax over y. SwiGLU: the
+// gate|up weight rows interleaved by 64 (tile t holds gate rows 64t..64t+63,
+// then up rows 64t..64t+63) and a = silu(y_gate) * y_up written as [M][N/2].
+enum class Epi : int { Linear = 0, LmHead = 1, SwiGLU = 2 };
 
 struct W8A8Launch {
     CUtensorMap tmap_w;       // int8 [N rows][K], box {128, 128}, 128B swizzle

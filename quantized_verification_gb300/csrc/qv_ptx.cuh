@@ -243,6 +243,36 @@ __device__ __forceinline__ int quant_code(float x, float s, float r) {
     return qi > 127 ? 127 : (qi < -127 ? -127 : qi);
 }
 
+// ---------------------------------------------------------------- SiLU
+// The decoder layer's SiLU, shared by the SwiGLU steps (the fused
+// quantization kernel and the gate|up GEMM epilogue).
+// exp(x): x > 88 -> +inf, x < -87 -> 0; otherwise k = rne(fl(x * log2 e)),
+// r = fl(fl(x - fl(k * LN2_HI)) - fl(k * LN2_LO)), p = the degree-7 Taylor
+// polynomial of e^r by Horner (coefficients fl(1/n!)), E = fl(p * 2^k).
+// LN2_HI has 16 significant bits, so k * LN2_HI is exact for |k| <= 127.
+__device__ __forceinline__ float layer_exp(float x) {
+    if (x > 88.0f) return __uint_as_float(0x7F800000u);
+    if (x < -87.0f) return 0.0f;
+    const float k = rintf(__fmul_rn(x, 1.44269504088896341f));
+    float r = __fsub_rn(x, __fmul_rn(k, 0.693145751953125f));
+    r = __fsub_rn(r, __fmul_rn(k, 1.42860682030941723212e-6f));
+    float p = 1.0f / 5040.0f;
+    p = __fadd_rn(__fmul_rn(p, r), 1.0f / 720.0f);
+    p = __fadd_rn(__fmul_rn(p, r), 1.0f / 120.0f);
+    p = __fadd_rn(__fmul_rn(p, r), 1.0f / 24.0f);
+    p = __fadd_rn(__fmul_rn(p, r), 1.0f / 6.0f);
+    p = __fadd_rn(__fmul_rn(p, r), 0.5f);
+    p = __fadd_rn(__fmul_rn(p, r), 1.0f);
+    p = __fadd_rn(__fmul_rn(p, r), 1.0f);
+    const float two_k = __uint_as_float((uint32_t)((int)k + 127) << 23);
+    return __fmul_rn(p, two_k);
+}
+
+__device__ __forceinline__ float silu(float v) {
+    const float den = __fadd_rn(1.0f, layer_exp(-v));
+    return __fmul_rn(v, __fdiv_rn(1.0f, den));
+}
+
 // ---------------------------------------------------------------- tcgen05
 // Tensor memory (TMEM): 128 lanes x 512 columns of 32-bit cells per SM. An
 // address is (lane << 16) | column; a warp reaches only the 32 lanes

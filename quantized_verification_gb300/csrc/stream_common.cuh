@@ -284,14 +284,17 @@ __device__ __forceinline__ void gather_partials(SM& sm, unsigned long long* slot
 struct EpiState {
     int c2 = 0;               // split_contributors_end of the CTA's range
     float swn = 0.f;          // channel scale of this thread's row in the current tile
+    float swn_up = 0.f;       // SwiGLU: the scale of row tid + 64 (the up feature of this gate row)
     unsigned tiles_done = 0;  // LM head: channel tiles this CTA finished
 };
 
 // At the start of a segment of channel tile nt: load the channel scale the
 // finish needs, so that its latency hides behind the segment's MMAs.
+template <int EPI>
 __device__ __forceinline__ void segment_start(EpiState& st, const W8A8Params& p, int nt, int tid) {
     const int n = nt * BN + tid;
     st.swn = (tid < BN && n < p.N) ? __ldg(&p.sw[n]) : 0.f;
+    if (EPI == (int)Epi::SwiGLU) st.swn_up = (tid < BN / 2 && n + BN / 2 < p.N) ? __ldg(&p.sw[n + BN / 2]) : 0.f;
 }
 
 // Finish channel tile nt from its complete int32 sums in sm.stg.
@@ -322,6 +325,23 @@ __device__ __forceinline__ void finish_tile(SM& sm, const W8A8Params& p, int nt,
                         reinterpret_cast<__nv_bfloat16*>(p.y)[(size_t)m * p.N + n] = __float2bfloat16_rn(yv);
                     else
                         reinterpret_cast<float*>(p.y)[(size_t)m * p.N + n] = yv;
+                }
+            }
+        }
+    } else if (EPI == (int)Epi::SwiGLU) {
+        // rows r and r + 64 of the tile: gate and up of feature f
+        const int f = nt * (BN / 2) + r;
+        if (r < BN / 2 && 2 * f < p.N) {
+            float* a = reinterpret_cast<float*>(p.y);
+            const int F = p.N / 2;
+#pragma unroll 8
+            for (int m = 0; m < MP; ++m) {
+                if (m < p.M) {
+                    const float sxm = sm.sx[m];
+                    const float yg = __fmul_rn(__int2float_rn(sm.stg[r * MP + m]), __fmul_rn(sxm, swn));
+                    const float yu = __fmul_rn(__int2float_rn(sm.stg[(r + BN / 2) * MP + m]),
+                                               __fmul_rn(sxm, st.swn_up));
+                    a[(size_t)m * F + f] = __fmul_rn(silu(yg), yu);
                 }
             }
         }

@@ -27,7 +27,7 @@ EXPORTS = ("qv_quantize_act", "qv_w8a8_linear", "qv_lm_head_argmax", "qv_accept"
            "qv_quantize_weight", "qv_bf16_linear", "qv_workspace_bytes",
            "qv_last_error", "qv_device_error", "qv_num_sms", "qv_w8a8_linear_noalloc",
            "qv_verify_stack", "qv_w8a8_linear_act", "qv_lm_head_argmax_act",
-           "qv_rmsnorm_quant", "qv_swiglu_quant")
+           "qv_rmsnorm_quant", "qv_swiglu_quant", "qv_w8a8_swiglu")
 MAX_STACK_M = 16
 
 
@@ -74,6 +74,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         L.qv_lm_head_argmax_act.argtypes = [P, I, P, I, I, P, P, I, P, P, P, S, P]
         L.qv_rmsnorm_quant.argtypes = [P, P, P, ctypes.c_float, P, I, I, P, P, P, P]
         L.qv_swiglu_quant.argtypes = [P, I, I, P, P, P]
+        L.qv_w8a8_swiglu.argtypes = [P, P, I, I, P, P, I, P, P, S, P]
         L.qv_workspace_bytes.argtypes = [I, I, I, I]
         L.qv_workspace_bytes.restype = S
         L.qv_last_error.argtypes = []
@@ -156,6 +157,28 @@ def qv_rmsnorm_quant(h, gamma, xq, sx, delta=None, eps=1e-6, act_mul=None, x_out
         _need(x_out.shape == (M, H) and x_out.dtype == torch.bfloat16, "x_out must be bf16 [M, H]")
     _check(load().qv_rmsnorm_quant(_ptr(h), _ptr(delta), _ptr(gamma), ctypes.c_float(eps), _ptr(act_mul),
                                    M, H, _ptr(xq), _ptr(sx), _ptr(x_out), ctypes.c_void_p(_stream(stream))))
+
+
+def interleave_gate_up(w: torch.Tensor) -> torch.Tensor:
+    """[2F, ...] rows gate (0..F-1) then up (F..2F-1) -> the layout of
+    qv_w8a8_swiglu: per 128 rows, 64 gate rows then the same 64 up rows."""
+    F = w.shape[0] // 2
+    _need(F % 64 == 0 and w.shape[0] == 2 * F, "gate|up rows must be 2F with F a multiple of 64")
+    rest = tuple(w.shape[1:])
+    return torch.stack([w[:F].reshape(F // 64, 64, *rest), w[F:].reshape(F // 64, 64, *rest)], dim=1).reshape(2 * F, *rest)
+
+
+def qv_w8a8_swiglu(xq, sx, wq_gu, sw_gu, a, workspace, stream=None):
+    """a [M, F] fp32 = silu(y_gate) * y_up of the interleaved gate|up linear."""
+    M, K = xq.shape
+    F2 = wq_gu.shape[0]
+    F = F2 // 2
+    _need(wq_gu.shape == (F2, K) and wq_gu.dtype == torch.int8 and xq.dtype == torch.int8, "int8 xq, wq_gu")
+    _need(sx.shape == (M,) and sw_gu.shape == (F2,), "sx [M], sw_gu [2F]")
+    _need(a.shape == (M, F) and a.dtype == torch.float32, "a must be float32 [M, F]")
+    _need(workspace.dtype == torch.uint8, "workspace must be a uint8 tensor")
+    _check(load().qv_w8a8_swiglu(_ptr(xq), _ptr(sx), M, K, _ptr(wq_gu), _ptr(sw_gu), F, _ptr(a),
+                                 _ptr(workspace), workspace.numel(), ctypes.c_void_p(_stream(stream))))
 
 
 def qv_swiglu_quant(gate_up, xq, sx, stream=None):

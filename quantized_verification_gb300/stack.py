@@ -59,6 +59,10 @@ class VerifyStack:
             lw, lb, li = [], [], []
             for (name, K, N) in self.phases:
                 w = synth.weights(N, K, synth.subseed(seed, "w", l, name), device=dev)
+                if name == "gate_up" and (N // 2) % 64 == 0:
+                    # gate and up rows interleaved by 64 (qv_w8a8_swiglu's layout);
+                    # the other paths only need some row order
+                    w = qv.interleave_gate_up(w)
                 wq = torch.empty(N, K, dtype=torch.int8, device=dev)
                 sw = torch.empty(N, dtype=torch.float32, device=dev)
                 qv.qv_quantize_weight(w, wq, sw)
@@ -192,6 +196,73 @@ class VerifyStack:
                              max_logit=self.max_logit, stream=stream)
         qv.qv_accept(self.tokens.view(self.B, self.gamma + 1), self.drafts if self.gamma > 0 else None,
                      self.accept_len, self.out_tokens, stream=stream)
+
+    # ------------------------------------------------------------------ chained layers
+    def prepare_chain(self, eps: float = 1e-6):
+        """Norm weights, the step's input residual stream and the output
+        buffers of the chained step (enqueue_chain)."""
+        h, M, F = self.model["hidden"], self.M, self.model["ffn"]
+        dev = self.device
+        self.eps = eps
+        self.norm_w = [(synth.norm_weights(h, synth.subseed(self.seed, "g", l, "attn"), device=dev),
+                        synth.norm_weights(h, synth.subseed(self.seed, "g", l, "mlp"), device=dev))
+                       for l in range(self.layers)]
+        self.norm_final = synth.norm_weights(h, synth.subseed(self.seed, "g", "final"), device=dev)
+        self.h0 = synth.activations(M, h, synth.subseed(self.seed, "x", "embed"), device=dev)
+        self.h_res = torch.empty_like(self.h0)
+        self.y_qkv = torch.empty(M, self.phases[0][2], dtype=torch.bfloat16, device=dev)
+        self.y_o = torch.empty(M, h, dtype=torch.bfloat16, device=dev)
+        self.a_glu = torch.empty(M, F, dtype=torch.float32, device=dev)
+        self.y_down = torch.empty(M, h, dtype=torch.bfloat16, device=dev)
+
+    def enqueue_chain(self, stream=None):
+        """One verify step through chained decoder layers: the bf16 residual
+        stream h runs through every layer, with the non-linear steps between
+        the quantized linears fused with the next linear's quantization
+        (gist.science/ja summary, section 2.2 item 3):
+          attention block: x = RMSNorm(h += down_prev) -> qkv; the attention
+            core itself is not modelled: the o projection takes the seeded
+            attention output of the layer; h += o's bf16 output, next block;
+          MLP block: x = RMSNorm(h) -> gate|up with SiLU(gate)*up in its
+            epilogue (fp32) -> per-token quantization -> down (bf16 output,
+            added to h by the next RMSNorm);
+          head: x = RMSNorm(h += down_last) -> LM head argmax -> acceptance.
+        Eight launches per layer (as in enqueue), plus the final three."""
+        M, h, F = self.M, self.model["hidden"], self.model["ffn"]
+        ws = self.ws
+        cur = torch.cuda.current_stream() if stream is None else stream
+        with torch.cuda.stream(cur):
+            self.h_res.copy_(self.h0)
+        for l in range(self.layers):
+            g1, g2 = self.norm_w[l]
+            xq = self._xq(h)
+            qv.qv_rmsnorm_quant(self.h_res, g1, xq, self.sx, delta=None if l == 0 else self.y_down,
+                                eps=self.eps, stream=stream)
+            wq, sw = self.weights[l][0]
+            qv.qv_w8a8_linear(xq, self.sx, wq, sw, self.y_qkv, ws, stream=stream)
+            xq = self._xq(self.phases[1][1])
+            qv.qv_quantize_act(self.inputs[l][1], xq, self.sx, stream=stream)
+            wq, sw = self.weights[l][1]
+            qv.qv_w8a8_linear(xq, self.sx, wq, sw, self.y_o, ws, stream=stream)
+            xq = self._xq(h)
+            qv.qv_rmsnorm_quant(self.h_res, g2, xq, self.sx, delta=self.y_o, eps=self.eps, stream=stream)
+            wq, sw = self.weights[l][2]
+            qv.qv_w8a8_swiglu(xq, self.sx, wq, sw, self.a_glu, ws, stream=stream)
+            xq = self._xq(F)
+            qv.qv_quantize_act(self.a_glu, xq, self.sx, stream=stream)
+            wq, sw = self.weights[l][3]
+            qv.qv_w8a8_linear(xq, self.sx, wq, sw, self.y_down, ws, stream=stream)
+        xq = self._xq(h)
+        qv.qv_rmsnorm_quant(self.h_res, self.norm_final, xq, self.sx, delta=self.y_down, eps=self.eps,
+                            stream=stream)
+        qv.qv_lm_head_argmax(xq, self.sx, self.lm_wq, self.lm_sw, self.tokens, ws,
+                             max_logit=self.max_logit, stream=stream)
+        qv.qv_accept(self.tokens.view(self.B, self.gamma + 1), self.drafts if self.gamma > 0 else None,
+                     self.accept_len, self.out_tokens, stream=stream)
+
+    def capture_chain(self):
+        self.graph_chain = self._capture(self.enqueue_chain, self.device)
+        return self.graph_chain
 
     def launches_per_step(self, fused: bool = False) -> int:
         """Kernels one step launches. fused: the persistent qv_verify_stack

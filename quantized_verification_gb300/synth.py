@@ -69,6 +69,13 @@ def weights(N: int, K: int, seed: int, dtype=torch.bfloat16, device="cpu",
     return w.to(dtype)
 
 
+def norm_weights(H: int, seed: int, dtype=torch.bfloat16, device="cpu", std: float = 0.1) -> torch.Tensor:
+    """[H] RMSNorm weights 1 + N(0, std)."""
+    g = _gen(seed, device)
+    w = 1.0 + std * torch.randn(H, generator=g, device=device, dtype=torch.float32)
+    return w.to(dtype)
+
+
 def uniform_tokens(shape, V: int, seed: int, device="cpu") -> torch.Tensor:
     g = _gen(seed, device)
     return torch.randint(0, V, shape, generator=g, device=device, dtype=torch.int32)
@@ -104,4 +111,5 @@ def expected_accept_len(p: float, gamma: int) -> float:
 
 
 __all__ = ["QWEN3_8B", "QWEN3_32B", "MODELS", "layer_projections", "subseed", "activations", "weights",
+           "norm_weights",
            "uniform_tokens", "geometric_drafts", "expected_accept_len"]

@@ -1,6 +1,7 @@
-"""The layer's fused non-linear steps (qv_rmsnorm_quant, qv_swiglu_quant)
-against the oracle, bit for bit: the updated residual stream, the normalized
-bf16 activations, the int8 codes and the fp32 token scales."""
+"""The layer's fused non-linear steps (qv_rmsnorm_quant, qv_swiglu_quant,
+qv_w8a8_swiglu) and the chained layers against the oracle, bit for bit: the
+updated residual stream, the normalized bf16 activations, the SwiGLU output,
+the int8 codes, the fp32 token scales, the tokens and accepted lengths."""
 import numpy as np
 import pytest
 import torch
@@ -117,3 +118,85 @@ def test_swiglu_exp_grid(qv, oracle):
     torch.cuda.synchronize()
     assert np.array_equal(np_(xq), q_ref)
     assert np.array_equal(np_(sx).view(np.uint32), s_ref.view(np.uint32))
+
+
+def test_chained_layers_match_oracle(qv, oracle):
+    """Two chained decoder layers (residual stream, RMSNorm, SwiGLU between
+    the W8A8 linears), the final RMSNorm, the LM head and the acceptance:
+    the residual stream, every linear's output that feeds the chain, the
+    tokens and the accepted lengths equal the oracle's chain bit for bit."""
+    from quantized_verification_gb300 import synth
+    from quantized_verification_gb300.stack import VerifyStack
+    model = {"hidden": 256, "kv": 64, "ffn": 512, "layers": 2, "vocab": 1000}
+    st = VerifyStack(model=model, B=2, gamma=3, seed=5)
+    st.prepare_chain(eps=1e-6)
+    st.drafts.copy_(synth.uniform_tokens((2, 3), 1000, seed=3).cuda())
+    st.enqueue_chain()
+    torch.cuda.synchronize()
+
+    cpu = lambda t: t.cpu().numpy()
+    h = _bits(st.h0)
+    yd = None
+    for l in range(model["layers"]):
+        g1, g2 = st.norm_w[l]
+        h, q, s, _ = oracle.residual_rmsnorm_quant(h, yd, _bits(g1), 1e-6)
+        wq, sw = st.weights[l][1]
+        qo, so = oracle.quantize_rows(_bits(st.inputs[l][1]), bf16=True)
+        y_o = oracle.f32_to_bf16(oracle.w8a8_linear(qo, so, cpu(wq), cpu(sw))[0])
+        h, q2, s2, _ = oracle.residual_rmsnorm_quant(h, y_o, _bits(g2), 1e-6)
+        wq, sw = st.weights[l][2]
+        y_il, _ = oracle.w8a8_linear(q2, s2, cpu(wq), cpu(sw))     # gate|up rows interleaved by 64
+        F = y_il.shape[1] // 2
+        blocks = y_il.reshape(-1, F // 64, 2, 64)
+        y_gu = np.concatenate([blocks[:, :, 0, :].reshape(-1, F), blocks[:, :, 1, :].reshape(-1, F)], axis=1)
+        q3, s3 = oracle.swiglu_quant(y_gu)
+        wq, sw = st.weights[l][3]
+        yd = oracle.f32_to_bf16(oracle.w8a8_linear(q3, s3, cpu(wq), cpu(sw))[0])
+        if l == model["layers"] - 1:
+            wq, sw = st.weights[l][0]
+            y_qkv = oracle.f32_to_bf16(oracle.w8a8_linear(q, s, cpu(wq), cpu(sw))[0])
+            assert np.array_equal(_bits(st.y_qkv), y_qkv)
+            assert np.array_equal(_bits(st.y_o), y_o)
+            a_ref = _silu_times(oracle, y_gu[:, :F], y_gu[:, F:])
+            assert np.array_equal(np_(st.a_glu).view(np.uint32), a_ref.view(np.uint32))
+            assert np.array_equal(_bits(st.y_down), yd)
+    h, qf, sf, _ = oracle.residual_rmsnorm_quant(h, yd, _bits(st.norm_final), 1e-6)
+    assert np.array_equal(_bits(st.h_res), h)
+    tok, _ = oracle.lm_head_argmax(qf, sf, cpu(st.lm_wq), cpu(st.lm_sw))
+    assert np.array_equal(np_(st.tokens), tok)
+    ln, out = oracle.accept(tok, cpu(st.drafts), 2, 3)
+    assert np.array_equal(np_(st.accept_len), ln) and np.array_equal(np_(st.out_tokens), out)
+    # the captured step gives the same result again (the residual stream is reset per step)
+    g = st.capture_chain()
+    st.tokens.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert np.array_equal(np_(st.tokens), tok) and np.array_equal(_bits(st.h_res), h)
+
+
+def _silu_times(oracle, gate: np.ndarray, up: np.ndarray) -> np.ndarray:
+    """fl32(silu(g) * u) elementwise with the oracle's silu."""
+    sil = np.array([oracle.silu(float(g)) for g in gate.reshape(-1)], dtype=np.float32).reshape(gate.shape)
+    return (sil * up.astype(np.float32)).astype(np.float32)
+
+
+@pytest.mark.parametrize("M,K,F", [(5, 256, 64), (17, 512, 192), (5, 4096, 1024), (64, 256, 128), (80, 128, 256)])
+def test_w8a8_swiglu(qv, oracle, M, K, F):
+    """The gate|up linear with SiLU(gate) * up in its epilogue (interleaved
+    rows; mma.sync kernel up to 32 tokens, tcgen05 at 64, 64-row slices
+    beyond): a equals fl32(silu(y_gate) * y_up) of the oracle's linear."""
+    from gpu_util import rand_codes, rand_scales
+    xq = rand_codes((M, K), seed=M + 3 * K)
+    sx = rand_scales(M, seed=M + 1, lo=1e-3, hi=0.2)
+    wq = rand_codes((2 * F, K), seed=F + 7)
+    sw = rand_scales(2 * F, seed=F + 9)
+    y, _ = oracle.w8a8_linear(np_(xq), np_(sx), np_(wq), np_(sw))
+    a_ref = _silu_times(oracle, y[:, :F], y[:, F:])
+    wq_il = qv.interleave_gate_up(wq.cuda())
+    sw_il = qv.interleave_gate_up(sw.cuda())
+    a = torch.full((M, F), float("nan"), device="cuda")
+    ws = qv.workspace(qv.QV_OP_LINEAR, M, K, 2 * F)
+    qv.qv_w8a8_swiglu(xq.cuda(), sx.cuda(), wq_il, sw_il, a, ws)
+    torch.cuda.synchronize()
+    assert np.array_equal(np_(a).view(np.uint32), a_ref.view(np.uint32))
+    assert int(ws.count_nonzero()) == 0, "workspace not left zero-filled"
