@@ -79,6 +79,11 @@ class Oracle:
         L.qvo_silu.argtypes = [ctypes.c_float]
         L.qvo_swiglu_quant.argtypes = [_P, _I, _I, _P, _P]
         L.qvo_residual_rmsnorm_quant.argtypes = [_P, _P, _P, ctypes.c_float, _P, _I, _I, _P, _P, _P]
+        L.qvo_splitmix64.restype = ctypes.c_uint64
+        L.qvo_splitmix64.argtypes = [ctypes.c_uint64, ctypes.c_uint64]
+        L.qvo_spec_sample.argtypes = [_P, _P, _P, _I, _I, _I, ctypes.c_float, ctypes.c_uint64, _P, _P]
+        L.qvo_draw_index.restype = ctypes.c_int32
+        L.qvo_draw_index.argtypes = [_P, _I, ctypes.c_uint64, ctypes.c_uint32]
 
     # -- bf16 ------------------------------------------------------------
     def bf16_to_f32(self, h: np.ndarray) -> np.ndarray:
@@ -245,6 +250,33 @@ class Oracle:
                                            M, H, _ptr(q), _ptr(s), _ptr(x))
         return h, q, s, x
 
+
+    # -- f2: lossless rejection sampling at T > 0 -------------------------
+    def splitmix64(self, seed: int, n: int) -> int:
+        """Draw n of SplitMix64 seeded with ``seed`` (counter-based form)."""
+        return int(self._L.qvo_splitmix64(seed & (2 ** 64 - 1), n))
+
+    def draw_index(self, x, u24: int) -> int:
+        """The sampling draw: the smallest v whose prefix sum of the integer
+        weights x exceeds floor(u24 * sum(x) / 2^24)."""
+        x = np.ascontiguousarray(x, dtype=np.uint64)
+        return int(self._L.qvo_draw_index(_ptr(x), x.size, int(x.sum()), u24))
+
+    def spec_sample(self, z: np.ndarray, d: np.ndarray, q: np.ndarray, B: int, gamma: int,
+                    T: float, seed: int):
+        """Speculative sampling at temperature T (gist.science/it summary,
+        section 2 item 3): z [B*(gamma+1), V] fp32 logits, d [B, gamma] draft
+        tokens, q [B*gamma, V] draft probabilities. Returns (len [B],
+        out [B, gamma+1])."""
+        z = np.ascontiguousarray(z, dtype=np.float32)
+        V = z.shape[1]
+        d = np.ascontiguousarray(d, dtype=np.int32).reshape(max(B * gamma, 0))
+        q = np.ascontiguousarray(q, dtype=np.float32).reshape(max(B * gamma, 0), V)
+        ln = np.empty(B, dtype=np.int32)
+        out = np.empty(B * (gamma + 1), dtype=np.int32)
+        self._L.qvo_spec_sample(_ptr(z), _ptr(d) if d.size else None, _ptr(q) if q.size else None,
+                                B, gamma, V, ctypes.c_float(T), seed & (2 ** 64 - 1), _ptr(ln), _ptr(out))
+        return ln, out.reshape(B, gamma + 1)
 
 _default: Oracle | None = None
 _lock = threading.Lock()

@@ -38,6 +38,13 @@
  *       -- gist.science/ja summary, section 2.2 item 3 (dequantize back to
  *          high precision before the non-linear layers);
  *          gist.science/fr summary, section 2 "Pipeline Technique".
+ *   f2  lossless rejection sampling at temperature T > 0: draft token d_j is
+ *       kept with probability min(1, p_j(d_j) / q_j(d_j)); at the first
+ *       rejection a token is drawn from the normalized max(0, p_j - q_j); when
+ *       every draft is kept, the bonus token is drawn from p_gamma
+ *       -- gist.science/it summary, section 2 item 3 ("Campionamento di
+ *          Rifiuto Lossless": the verifier's logits stay precise so that
+ *          the target distribution is kept).
  *   a4  acceptance: the longest draft prefix equal to the verifier's tokens,
  *       plus one token from the verifier (so at least one token per step)
  *       -- gist.science/fr summary, lay explanation (a wrong guess is
@@ -70,6 +77,22 @@
  *                     and a Taylor polynomial, written out so that the GPU side
  *                     can evaluate the identical binary32 operations);
  *     then the a1 quantization of x (bf16) or a (fp32).
+ *   - f2 (the summaries name the rule, not its arithmetic): probabilities
+ *     become integer weights so that every sum over the vocabulary is exact:
+ *       p: m = max_v z_v, w_v = floor(E(fl32(fl32(z_v - m) / T)) * 2^24),
+ *          Z = sum w_v;     q: c_v = floor(fl32(clamp(q_v, 0, 1) * 2^24)),
+ *          Q = sum c_v;
+ *       keep d iff u * (w_d / Z) / (c_d / Q) ... i.e. u24 * Z * c_d <
+ *       w_d * Q * 2^24 (128-bit integers), u24 the top 24 bits of one draw;
+ *       the replacement at the first rejection k: weights
+ *       r_v = max(0, w_v * Q - c_v * Z) (128-bit), or w when R = sum r = 0;
+ *       the bonus (no rejection): weights w of row gamma; a draw from
+ *       weights x with total X is the smallest v whose prefix sum exceeds
+ *       floor(u24' * X / 2^24), u24' from a second draw.
+ *     Draws: SplitMix64 (G. Steele, D. Lea, C. Flood, "Fast splittable
+ *     pseudorandom number generators", 2014) used as a counter-based
+ *     generator: draw n of seed s is mix(s + (n + 1) * 0x9E3779B97F4A7C15);
+ *     n = 2 * row + purpose (0: keep test, 1: sample), row = b * (gamma + 1) + j.
  *   - acceptance: row j of sequence b holds the verifier token t[b][j] that
  *     follows prefix position j; draft d[b][j] is accepted iff it equals
  *     t[b][j] and all earlier drafts were accepted; the verifier token at the
@@ -432,4 +455,131 @@ void qvo_residual_rmsnorm_quant(uint16_t* h, const uint16_t* d, const uint16_t* 
         qvo_quantize_rows_bf16(x, 1, H, mul, q + m * H, s + m);
     }
     free(x);
+}
+
+/* ------------------------------------------------------------------ */
+/* f2: lossless rejection sampling at T > 0                             */
+/* ------------------------------------------------------------------ */
+
+typedef unsigned __int128 u128;
+
+/* SplitMix64 output n of the sequence seeded with s (counter-based form). */
+uint64_t qvo_splitmix64(uint64_t s, uint64_t n)
+{
+    uint64_t z = s + (n + 1) * 0x9E3779B97F4A7C15ull;
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+    return z ^ (z >> 31);
+}
+
+/* Integer weight floor(x * 2^24) of a value x in [0, 1] (clamped). */
+static uint32_t weight24(float x)
+{
+    if (!(x > 0.0f)) return 0u;
+    if (x >= 1.0f) return 1u << 24;
+    return (uint32_t)(x * 16777216.0f);     /* exact product, truncated */
+}
+
+/* p weights of one logits row: w_v = floor(E((z_v - m) / T) * 2^24). */
+static uint64_t p_weights(const float* z, int64_t V, float T, uint32_t* w)
+{
+    float m = z[0];
+    for (int64_t v = 1; v < V; ++v)
+        if (z[v] > m) m = z[v];
+    uint64_t Z = 0;
+    for (int64_t v = 0; v < V; ++v) {
+        float t = (z[v] - m) / T;
+        w[v] = weight24(qvo_exp(t));
+        Z += w[v];
+    }
+    return Z;
+}
+
+/* Smallest v whose prefix sum of x exceeds floor(u24 * X / 2^24). */
+static int32_t draw_u64(const uint64_t* x, int64_t V, uint64_t X, uint32_t u24)
+{
+    u128 target = ((u128)u24 * (u128)X) >> 24;
+    u128 acc = 0;
+    for (int64_t v = 0; v < V; ++v) {
+        acc += x[v];
+        if (acc > target) return (int32_t)v;
+    }
+    return (int32_t)(V - 1);
+}
+static int32_t draw_u128(const u128* x, int64_t V, u128 X, uint32_t u24)
+{
+    /* floor(u24 * X / 2^24) without overflow: X < 2^106 here */
+    u128 target = (X >> 24) * u24 + (((X & 0xFFFFFFull) * u24) >> 24);
+    u128 acc = 0;
+    for (int64_t v = 0; v < V; ++v) {
+        acc += x[v];
+        if (acc > target) return (int32_t)v;
+    }
+    return (int32_t)(V - 1);
+}
+
+/* The draw of qvo_spec_sample from integer weights x (total X), exported
+ * for the tests. */
+int32_t qvo_draw_index(const uint64_t* x, int64_t V, uint64_t X, uint32_t u24)
+{
+    return draw_u64(x, V, X, u24);
+}
+
+/*
+ * Speculative sampling for B sequences of gamma drafts.
+ *   z   : M = B*(gamma+1) rows of V fp32 verifier logits (row b*(gamma+1)+j
+ *         follows prefix position j)
+ *   d   : B*gamma draft tokens; q: B*gamma rows of V draft probabilities
+ *   len : B accepted lengths (kept drafts + 1); out: B*(gamma+1) tokens,
+ *         the kept drafts, then the replacement or bonus token, then -1
+ */
+void qvo_spec_sample(const float* z, const int32_t* d, const float* q, int64_t B, int64_t gamma,
+                     int64_t V, float T, uint64_t seed, int32_t* len, int32_t* out)
+{
+    int64_t G = gamma + 1;
+    uint32_t* w = (uint32_t*)malloc((size_t)V * sizeof(uint32_t));
+    uint32_t* c = (uint32_t*)malloc((size_t)V * sizeof(uint32_t));
+    uint64_t* x64 = (uint64_t*)malloc((size_t)V * sizeof(uint64_t));
+    u128* x128 = (u128*)malloc((size_t)V * sizeof(u128));
+    for (int64_t b = 0; b < B; ++b) {
+        int64_t k = 0;
+        int32_t tok = -1;
+        for (; k < gamma; ++k) {
+            int64_t row = b * G + k;
+            uint64_t Z = p_weights(z + row * V, V, T, w);
+            uint64_t Q = 0;
+            for (int64_t v = 0; v < V; ++v) { c[v] = weight24(q[(b * gamma + k) * V + v]); Q += c[v]; }
+            int32_t dk = d[b * gamma + k];
+            uint32_t u24 = (uint32_t)(qvo_splitmix64(seed, (uint64_t)(2 * row)) >> 40);
+            u128 lhs = (u128)u24 * (u128)Z * (u128)c[dk];
+            u128 rhs = ((u128)w[dk] * (u128)Q) << 24;
+            if (lhs < rhs) continue;                         /* kept */
+            /* rejected: draw from max(0, w*Q - c*Z), or from w if that is all 0 */
+            u128 R = 0;
+            for (int64_t v = 0; v < V; ++v) {
+                u128 a1 = (u128)w[v] * Q, a2 = (u128)c[v] * Z;
+                x128[v] = a1 > a2 ? a1 - a2 : 0;
+                R += x128[v];
+            }
+            uint32_t u2 = (uint32_t)(qvo_splitmix64(seed, (uint64_t)(2 * row + 1)) >> 40);
+            if (R > 0) {
+                tok = draw_u128(x128, V, R, u2);
+            } else {
+                for (int64_t v = 0; v < V; ++v) x64[v] = w[v];
+                tok = draw_u64(x64, V, Z, u2);
+            }
+            break;
+        }
+        if (k == gamma) {                                    /* every draft kept: the bonus */
+            int64_t row = b * G + gamma;
+            uint64_t Z = p_weights(z + row * V, V, T, w);
+            for (int64_t v = 0; v < V; ++v) x64[v] = w[v];
+            uint32_t u2 = (uint32_t)(qvo_splitmix64(seed, (uint64_t)(2 * row + 1)) >> 40);
+            tok = draw_u64(x64, V, Z, u2);
+        }
+        len[b] = (int32_t)(k + 1);
+        for (int64_t j = 0; j < G; ++j)
+            out[b * G + j] = j < k ? d[b * gamma + j] : (j == k ? tok : -1);
+    }
+    free(w); free(c); free(x64); free(x128);
 }

@@ -443,6 +443,109 @@ def pin_rmsnorm_quant(o):
         qe, se = quantize_row_exact(xf)
         assert list(q1[m]) == list(qe) and np.float32(s1[m]) == se
 
+
+# ---------------------------------------------------------------------------
+# f2: lossless rejection sampling at T > 0
+# ---------------------------------------------------------------------------
+def pin_splitmix64_kat(o):
+    """SplitMix64 seeded with 0: its published first outputs."""
+    assert [o.splitmix64(0, n) for n in range(3)] == [0xE220A8397B1DCDAF, 0x6E789E6AA1B965F4,
+                                                      0x06C45D188009454F]
+
+
+def _softmax64(z, T):
+    z = np.asarray(z, dtype=np.float64) / T
+    e = np.exp(z - z.max())
+    return e / e.sum()
+
+
+def _chi2_ok(counts, probs, n):
+    """Pearson chi-square of counts against probs, far from rejection
+    (the 1e-4 upper quantile of chi2 with df <= 9 is below 40)."""
+    exp = np.asarray(probs) * n
+    mask = exp > 0
+    stat = float(np.sum((np.asarray(counts)[mask] - exp[mask]) ** 2 / exp[mask]))
+    return stat < 40.0 and np.all(np.asarray(counts)[~mask] == 0)
+
+
+def pin_spec_lossless(o):
+    """The defining property of speculative sampling: with drafts drawn from
+    any draft distribution q, the emitted tokens are distributed as the
+    verifier's p. Over 20000 seeds (drafts drawn from q by an independent
+    generator): the first token follows p_0, the second one, given that the
+    first draft was kept, follows p_1, and the bonus after two kept drafts
+    follows p_2 (chi-square)."""
+    V, gamma, T = 6, 2, 0.8
+    z = np.float32([[1.0, 0.2, -0.5, 2.0, 0.0, -1.0], [0.5, -0.3, 1.5, 0.1, -2.0, 0.7],
+                    [-1.0, 0.5, 2.0, 0.0, 1.0, -0.5]])
+    q = np.float32([[0.05, 0.3, 0.1, 0.15, 0.25, 0.15], [0.2, 0.2, 0.1, 0.1, 0.3, 0.1]])
+    qn = q.astype(np.float64) / q.astype(np.float64).sum(axis=1, keepdims=True)
+    drafter = np.random.default_rng(2024)
+    n = 20000
+    first = np.zeros(V)
+    second = np.zeros(V)
+    n2 = 0
+    third = np.zeros(V)
+    n3 = 0
+    for seed in range(n):
+        d = np.int32([[drafter.choice(V, p=qn[0]), drafter.choice(V, p=qn[1])]])
+        ln, out = o.spec_sample(z, d, q, 1, gamma, T, seed * 7919 + 13)
+        first[out[0, 0]] += 1
+        if ln[0] >= 2:
+            second[out[0, 1]] += 1
+            n2 += 1
+        if ln[0] == 3:
+            third[out[0, 2]] += 1
+            n3 += 1
+    assert _chi2_ok(first, _softmax64(z[0], T), n)
+    assert n2 > 1000 and _chi2_ok(second, _softmax64(z[1], T), n2)
+    assert n3 > 500 and _chi2_ok(third, _softmax64(z[2], T), n3)
+
+
+def pin_draw_index(o):
+    """Inverse-CDF draw on integer weights, worked by hand: weights
+    [0, 3, 0, 5] (total 8) split [0, 2^24) into u24 < 3 * 2^21 -> token 1 and
+    the rest -> token 3; a zero weight is never drawn."""
+    w = [0, 3, 0, 5]
+    assert o.draw_index(w, 0) == 1
+    assert o.draw_index(w, 3 * 2 ** 21 - 1) == 1
+    assert o.draw_index(w, 3 * 2 ** 21) == 3
+    assert o.draw_index(w, 2 ** 24 - 1) == 3
+    for u in range(0, 2 ** 24, 2 ** 18):
+        assert o.draw_index(w, u) in (1, 3)
+    assert o.draw_index([7], 12345) == 0
+
+
+def pin_spec_special_cases(o):
+    """(1) q equal to p (flat logits, flat draft): every draft is kept.
+    (2) p(d) = 0: the draft is never kept and never drawn as the replacement.
+    (3) Logits and T both scaled by 2 (exact in binary32): the same outputs.
+    (4) Invariants: len in [1, gamma+1], the kept drafts are emitted in order."""
+    V, gamma, B = 8, 3, 4
+    z = np.zeros((B * (gamma + 1), V), np.float32)
+    q = np.ones((B * gamma, V), np.float32)
+    d = np.random.default_rng(3).integers(0, V, (B, gamma)).astype(np.int32)
+    for seed in range(50):
+        ln, _ = o.spec_sample(z, d, q, B, gamma, 1.0, seed)
+        assert (ln == gamma + 1).all()
+    rng = np.random.default_rng(5)
+    z2 = rng.normal(0, 1, (B * (gamma + 1), V)).astype(np.float32)
+    for b in range(B):
+        z2[b * (gamma + 1), d[b, 0]] = -1000.0
+    q2 = rng.uniform(0.01, 1.0, (B * gamma, V)).astype(np.float32)
+    for seed in range(50):
+        ln, out = o.spec_sample(z2, d, q2, B, gamma, 1.0, seed)
+        assert (ln == 1).all() and all(out[b, 0] != d[b, 0] for b in range(B))
+        ln2, out2 = o.spec_sample(z2 * np.float32(2), d, q2, B, gamma, 2.0, seed)
+        assert np.array_equal(ln, ln2) and np.array_equal(out, out2)
+    z3 = rng.normal(0, 2, (B * (gamma + 1), V)).astype(np.float32)
+    for seed in range(50):
+        ln, out = o.spec_sample(z3, d, q2, B, gamma, 0.7, seed)
+        for b in range(B):
+            assert 1 <= ln[b] <= gamma + 1
+            assert list(out[b, : ln[b] - 1]) == list(d[b, : ln[b] - 1])
+            assert 0 <= out[b, ln[b] - 1] < V and (out[b, ln[b]:] == -1).all()
+
 ALL_PINS = [
     pin_worked_example,
     pin_quantize_exact_rational,
@@ -460,4 +563,8 @@ ALL_PINS = [
     pin_silu,
     pin_swiglu_quant,
     pin_rmsnorm_quant,
+    pin_splitmix64_kat,
+    pin_spec_lossless,
+    pin_draw_index,
+    pin_spec_special_cases,
 ]

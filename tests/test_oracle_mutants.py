@@ -46,6 +46,14 @@ MUTANTS = [
     ("rmsnorm_no_sqrt", "float sq = sqrtf(t);", "float sq = t;"),
     ("rmsnorm_ignores_weight", "x[k] = qvo_f32_to_bf16_rne(qvo_bf16_to_f32(g[k]) * u);",
      "x[k] = qvo_f32_to_bf16_rne(u);"),
+    ("spec_keep_test_inverted", "if (lhs < rhs) continue;", "if (lhs > rhs) continue;"),
+    ("spec_residual_q_minus_p", "x128[v] = a1 > a2 ? a1 - a2 : 0;", "x128[v] = a2 > a1 ? a2 - a1 : 0;"),
+    ("spec_bonus_from_first_row", "int64_t row = b * G + gamma;", "int64_t row = b * G;"),
+    ("spec_draw_inclusive", "if (acc > target) return (int32_t)v;\n    }\n    return (int32_t)(V - 1);\n}\nstatic int32_t draw_u128",
+     "if (acc >= target) return (int32_t)v;\n    }\n    return (int32_t)(V - 1);\n}\nstatic int32_t draw_u128"),
+    ("spec_same_draw_for_both", "(uint64_t)(2 * row + 1)) >> 40);\n            if (R > 0)",
+     "(uint64_t)(2 * row)) >> 40);\n            if (R > 0)"),
+    ("splitmix_constant", "0xBF58476D1CE4E5B9ull", "0xBF58476D1CE4E5B8ull"),
     ("residual_not_added",
      "hr[k] = qvo_f32_to_bf16_rne(qvo_bf16_to_f32(hr[k]) + qvo_bf16_to_f32(d[m * H + k]));",
      "hr[k] = hr[k];"),
