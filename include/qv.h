@@ -71,7 +71,8 @@ typedef enum {
     QV_OP_BF16_LINEAR = 2,    /* qv_bf16_linear                            */
     QV_OP_VERIFY_STACK = 3,   /* qv_verify_stack (K, N = largest K, N / V) */
     QV_OP_LINEAR_ACT = 4,     /* qv_w8a8_linear_act                        */
-    QV_OP_LM_HEAD_ACT = 5     /* qv_lm_head_argmax_act (N = V)             */
+    QV_OP_LM_HEAD_ACT = 5,    /* qv_lm_head_argmax_act (N = V)             */
+    QV_OP_SPEC_SAMPLE = 6     /* qv_spec_sample (M = B*(gamma+1); K, N ignored) */
 } qv_op;
 
 /* floor((2^31 - 1) / 127^2): the int32 accumulation stays exact up to here. */
@@ -278,6 +279,45 @@ QV_API qv_status qv_rmsnorm_quant(uint16_t* h, const uint16_t* delta, const uint
  */
 QV_API qv_status qv_swiglu_quant(const float* gate_up, int M, int F, int8_t* xq, float* sx,
                                  cudaStream_t stream);
+
+/*
+ * qv_spec_sample -- acceptance at temperature T > 0: lossless rejection
+ * sampling (speculative sampling) over the verifier's logits.
+ *
+ *   gist.science/it summary, section 2 item 3 ("Campionamento di Rifiuto
+ *   Lossless"): the verifier's logits stay precise so that the target
+ *   distribution is kept. The rule is the textbook one: keep draft d_j with
+ *   probability min(1, p_j(d_j) / q_j(d_j)); at the first rejection draw from
+ *   the normalized max(0, p_j - q_j); with every draft kept, draw the bonus
+ *   token from p_gamma. Emitted tokens are distributed as sampling from p.
+ *
+ *   logits      [B*(gamma+1)][V] fp32 (e.g. qv_w8a8_linear of the LM head);
+ *               row b*(gamma+1)+j follows prefix position j
+ *   draft       [B*gamma] int32 drafted tokens (drawn from draft_probs)
+ *   draft_probs [B*gamma][V] fp32 draft probabilities q (values clamped to
+ *               [0, 1]; need not sum to 1)
+ *   temperature > 0; p_j = softmax(logits_j / temperature)
+ *   seed        selects the uniforms (same seed, same inputs: same outputs)
+ *   accept_len  [B] out, in [1, gamma+1]; out_tokens [B*(gamma+1)] out: the
+ *               kept drafts, the replacement or bonus token, then -1
+ *   workspace   qv_workspace_bytes(QV_OP_SPEC_SAMPLE, B*(gamma+1), 16, V)
+ *               bytes (row statistics, scratch; no zero-fill needed)
+ * Arithmetic (so that every decision is exact and reproducible): with E the
+ * library's binary32 exp (qv_swiglu_quant), m = max_v z_v,
+ * w_v = floor(E(fl32(fl32(z_v - m) / T)) * 2^24), Z = sum w_v,
+ * c_v = floor(fl32(q_v * 2^24)), Q = sum c_v; keep d iff
+ * u * Z * c_d < w_d * Q * 2^24 (128-bit integers); replacement weights
+ * max(0, w_v * Q - c_v * Z), or w when all are 0; a draw from weights x is
+ * the smallest v whose prefix sum exceeds floor(u' * sum(x) / 2^24). u, u'
+ * are the top 24 bits of SplitMix64 draws 2*row and 2*row + 1 of the seed
+ * (counter-based: mix(seed + (n+1) * 0x9E3779B97F4A7C15)).
+ * Draft tokens outside [0, V) are never kept. B >= 1, 0 <= gamma <= 1023,
+ * 1 <= V <= 16777216, logits and draft_probs 4-byte aligned.
+ */
+QV_API qv_status qv_spec_sample(const float* logits, const int32_t* draft, const float* draft_probs,
+                                int B, int gamma, int V, float temperature, uint64_t seed,
+                                int32_t* accept_len, int32_t* out_tokens,
+                                void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
  * qv_accept -- a4: greedy acceptance of the longest matching draft prefix

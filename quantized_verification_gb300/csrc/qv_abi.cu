@@ -182,6 +182,7 @@ int qv_num_sms(void) {
 }
 
 size_t qv_workspace_bytes(qv_op op, int M, int K, int N) {
+    if (op == QV_OP_SPEC_SAMPLE) return (M >= 1 && M <= 65535) ? (qv::spec_workspace_bytes(M) + 255) & ~size_t(255) : 0;
     if (M < 1 || M > QV_MAX_M || N < 1 || K < 16 || K % 16 != 0 || K > QV_MAX_K) return 0;
     const int mp = mp_for(M < qv::kMaxMPerLaunch ? M : qv::kMaxMPerLaunch);
     switch (op) {
@@ -191,6 +192,8 @@ size_t qv_workspace_bytes(qv_op op, int M, int K, int N) {
         case QV_OP_VERIFY_STACK:
             if (M > qv::kMaxStackM) return 0;
             return qv::stack_ws_bytes(mp, M, N, K);
+        case QV_OP_SPEC_SAMPLE:
+            return 0;   // handled above
         case QV_OP_LINEAR_ACT:
         case QV_OP_LM_HEAD_ACT: {
             const size_t off = act_codes_offset(op == QV_OP_LM_HEAD_ACT, M, K, N);
@@ -449,6 +452,38 @@ qv_status qv_swiglu_quant(const float* gate_up, int M, int F, int8_t* xq, float*
     QV_CHECK_DEV(sx);
     cudaError_t e = qv::launch_swiglu_quant(gate_up, M, F, xq, sx, stream);
     if (e != cudaSuccess) return cuda_fail(e, "qv_swiglu_quant launch");
+    return ok();
+}
+
+qv_status qv_spec_sample(const float* logits, const int32_t* draft, const float* draft_probs, int B,
+                         int gamma, int V, float temperature, uint64_t seed, int32_t* accept_len,
+                         int32_t* out_tokens, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    if (!logits || !accept_len || !out_tokens) return fail(QV_ERR_INVALID_ARG, "null pointer");
+    if (B < 1) return fail(QV_ERR_INVALID_ARG, "B=%d must be >= 1", B);
+    if (gamma < 0 || gamma > 1023) return fail(QV_ERR_INVALID_ARG, "gamma=%d outside [0, 1023]", gamma);
+    if (gamma > 0 && (!draft || !draft_probs)) return fail(QV_ERR_INVALID_ARG, "draft / draft_probs null with gamma > 0");
+    if (V < 1 || V > (1 << 24)) return fail(QV_ERR_INVALID_ARG, "V=%d outside [1, 2^24]", V);
+    if (!(temperature > 0.0f) || temperature > 3.0e38f)
+        return fail(QV_ERR_INVALID_ARG, "temperature must be finite and > 0");
+    if ((long long)B * (gamma + 1) > 65535) return fail(QV_ERR_INVALID_ARG, "B*(gamma+1) must be <= 65535");
+    if (!aligned(logits, 4) || (draft && !aligned(draft, 4)) || (draft_probs && !aligned(draft_probs, 4)) ||
+        !aligned(accept_len, 4) || !aligned(out_tokens, 4))
+        return fail(QV_ERR_INVALID_ARG, "buffers must be 4-byte aligned");
+    const int M = B * (gamma + 1);
+    const size_t need = qv_workspace_bytes(QV_OP_SPEC_SAMPLE, M, 16, V);
+    if (!workspace) return fail(QV_ERR_WORKSPACE, "workspace is null (%zu bytes needed)", need);
+    if (!aligned(workspace, 16)) return fail(QV_ERR_WORKSPACE, "workspace must be 16-byte aligned");
+    if (workspace_bytes < need) return fail(QV_ERR_WORKSPACE, "workspace has %zu bytes, %zu needed", workspace_bytes, need);
+    QV_CHECK_DEV(logits);
+    QV_CHECK_DEV(draft);
+    QV_CHECK_DEV(draft_probs);
+    QV_CHECK_DEV(accept_len);
+    QV_CHECK_DEV(out_tokens);
+    QV_CHECK_DEV(workspace);
+    cudaError_t e = qv::launch_spec_sample(logits, gamma > 0 ? draft : nullptr, gamma > 0 ? draft_probs : nullptr,
+                                           B, gamma, V, temperature, seed, accept_len, out_tokens, workspace,
+                                           stream);
+    if (e != cudaSuccess) return cuda_fail(e, "qv_spec_sample launch");
     return ok();
 }
 

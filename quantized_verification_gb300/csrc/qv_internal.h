@@ -113,6 +113,13 @@ constexpr size_t kMaxDynSmem = 232448;
 constexpr size_t kMinSmemOneCtaPerSm = 118 * 1024;
 cudaError_t launch_verify_stack(const StackLaunch& a, int num_sms, cudaStream_t s);
 cudaError_t launch_bf16_stream(const Bf16Launch& a, int num_sms, cudaStream_t s);
+// Speculative sampling at T > 0 (k_spec.cu): 32 bytes of row statistics per
+// verify row in the workspace.
+size_t spec_workspace_bytes(int M);
+cudaError_t launch_spec_sample(const float* logits, const int32_t* draft, const float* q, int B, int gamma,
+                               int V, float T, uint64_t seed, int32_t* accept_len, int32_t* out_tokens,
+                               void* ws, cudaStream_t s);
+
 // The layer's fused non-linear steps (k_layer.cu).
 cudaError_t launch_residual_rmsnorm_quant(uint16_t* h, const uint16_t* delta, const uint16_t* gamma, float eps,
                                           const float* mul, int M, int H, int8_t* xq, float* sx,

@@ -19,6 +19,7 @@ QV_OK, QV_ERR_INVALID_ARG, QV_ERR_UNSUPPORTED, QV_ERR_WORKSPACE, QV_ERR_CUDA = r
 QV_F32, QV_BF16 = 0, 1
 QV_OP_LINEAR, QV_OP_LM_HEAD, QV_OP_BF16_LINEAR, QV_OP_VERIFY_STACK = 0, 1, 2, 3
 QV_OP_LINEAR_ACT, QV_OP_LM_HEAD_ACT = 4, 5
+QV_OP_SPEC_SAMPLE = 6
 QV_MAX_K = 133144
 QV_MAX_M = 256
 
@@ -27,7 +28,7 @@ EXPORTS = ("qv_quantize_act", "qv_w8a8_linear", "qv_lm_head_argmax", "qv_accept"
            "qv_quantize_weight", "qv_bf16_linear", "qv_workspace_bytes",
            "qv_last_error", "qv_device_error", "qv_num_sms", "qv_w8a8_linear_noalloc",
            "qv_verify_stack", "qv_w8a8_linear_act", "qv_lm_head_argmax_act",
-           "qv_rmsnorm_quant", "qv_swiglu_quant", "qv_w8a8_swiglu")
+           "qv_rmsnorm_quant", "qv_swiglu_quant", "qv_w8a8_swiglu", "qv_spec_sample")
 MAX_STACK_M = 16
 
 
@@ -75,6 +76,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         L.qv_rmsnorm_quant.argtypes = [P, P, P, ctypes.c_float, P, I, I, P, P, P, P]
         L.qv_swiglu_quant.argtypes = [P, I, I, P, P, P]
         L.qv_w8a8_swiglu.argtypes = [P, P, I, I, P, P, I, P, P, S, P]
+        L.qv_spec_sample.argtypes = [P, P, P, I, I, I, ctypes.c_float, ctypes.c_uint64, P, P, P, S, P]
         L.qv_workspace_bytes.argtypes = [I, I, I, I]
         L.qv_workspace_bytes.restype = S
         L.qv_last_error.argtypes = []
@@ -179,6 +181,28 @@ def qv_w8a8_swiglu(xq, sx, wq_gu, sw_gu, a, workspace, stream=None):
     _need(workspace.dtype == torch.uint8, "workspace must be a uint8 tensor")
     _check(load().qv_w8a8_swiglu(_ptr(xq), _ptr(sx), M, K, _ptr(wq_gu), _ptr(sw_gu), F, _ptr(a),
                                  _ptr(workspace), workspace.numel(), ctypes.c_void_p(_stream(stream))))
+
+
+def qv_spec_sample(logits, draft, draft_probs, temperature, seed, accept_len, out_tokens, workspace,
+                   stream=None):
+    """Speculative sampling at temperature > 0: logits [B*(gamma+1), V]
+    fp32, draft [B, gamma] int32, draft_probs [B*gamma, V] fp32 ->
+    accept_len [B], out_tokens [B, gamma+1]."""
+    B, G = out_tokens.shape
+    gamma = G - 1
+    M, V = logits.shape
+    _need(logits.dtype == torch.float32 and M == B * G, "logits must be float32 [B*(gamma+1), V]")
+    _need(accept_len.shape == (B,) and accept_len.dtype == torch.int32, "accept_len int32 [B]")
+    _need(out_tokens.dtype == torch.int32, "out_tokens int32 [B, gamma+1]")
+    if gamma > 0:
+        _need(draft.shape == (B, gamma) and draft.dtype == torch.int32, "draft int32 [B, gamma]")
+        _need(draft_probs.shape == (B * gamma, V) and draft_probs.dtype == torch.float32,
+              "draft_probs float32 [B*gamma, V]")
+    _check(load().qv_spec_sample(_ptr(logits), _ptr(draft) if gamma > 0 else None,
+                                 _ptr(draft_probs) if gamma > 0 else None, B, gamma, V,
+                                 ctypes.c_float(temperature), ctypes.c_uint64(seed & (2 ** 64 - 1)),
+                                 _ptr(accept_len), _ptr(out_tokens), _ptr(workspace), workspace.numel(),
+                                 ctypes.c_void_p(_stream(stream))))
 
 
 def qv_swiglu_quant(gate_up, xq, sx, stream=None):

@@ -92,8 +92,18 @@ def test_host_validation_without_gpu(lib):
     assert lib.qv_lm_head_argmax_act(fake, 1, None, 5, 256, fake, fake, 8, None, None, fake, 1 << 20, None) == qv.QV_ERR_INVALID_ARG
     assert b"tokens" in lib.qv_last_error()
     assert lib.qv_lm_head_argmax_act(fake, 1, None, 5, 250, fake, fake, 8, fake, None, fake, 1 << 20, None) == qv.QV_ERR_INVALID_ARG
-    # the layer's fused non-linear steps
+    # speculative sampling at T > 0
     F32 = ctypes.c_float
+    U64 = ctypes.c_uint64
+    assert lib.qv_spec_sample(None, fake, fake, 1, 4, 1000, F32(1.0), U64(1), fake, fake, fake, 1 << 20, None) == qv.QV_ERR_INVALID_ARG
+    assert lib.qv_spec_sample(fake, None, fake, 1, 4, 1000, F32(1.0), U64(1), fake, fake, fake, 1 << 20, None) == qv.QV_ERR_INVALID_ARG
+    assert lib.qv_spec_sample(fake, fake, fake, 1, 4, 1000, F32(0.0), U64(1), fake, fake, fake, 1 << 20, None) == qv.QV_ERR_INVALID_ARG
+    assert b"temperature" in lib.qv_last_error()
+    assert lib.qv_spec_sample(fake, fake, fake, 1, 4, 0, F32(1.0), U64(1), fake, fake, fake, 1 << 20, None) == qv.QV_ERR_INVALID_ARG
+    assert lib.qv_spec_sample(fake, fake, fake, 1, 4, 1000, F32(1.0), U64(1), fake, fake, fake, 16, None) == qv.QV_ERR_WORKSPACE
+    assert qv.qv_workspace_bytes(qv.QV_OP_SPEC_SAMPLE, 5, 16, 151936) == 256
+    assert qv.qv_workspace_bytes(qv.QV_OP_SPEC_SAMPLE, 80, 16, 151936) == 2560
+    # the layer's fused non-linear steps
     assert lib.qv_rmsnorm_quant(None, None, fake, F32(1e-6), None, 5, 256, fake, fake, None, None) == qv.QV_ERR_INVALID_ARG
     assert lib.qv_rmsnorm_quant(fake, None, fake, F32(1e-6), None, 5, 264, fake, fake, None, None) == qv.QV_ERR_INVALID_ARG
     assert b"multiple of 16" in lib.qv_last_error()
