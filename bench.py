@@ -442,6 +442,23 @@ def main():
                                "final qv_rmsnorm_quant -> LM head "
                                "argmax -> accept; one CUDA graph"}
 
+    # ---- T > 0: LM-head logits and lossless rejection sampling
+    sampling = None
+    if rank == 0:
+        stack.prepare_sampling(temperature=0.8)
+        sg = stack.capture_sampled()
+        for _ in range(3):
+            sg.replay()
+        torch.cuda.synchronize()
+        s_ms = time_graph(torch, sg, max(20, args.steps // 5), stream)
+        log(f"T>0 sampling step {s_ms:.4f} ms/step (mean accepted length "
+            f"{float(stack.accept_len.float().mean()):.2f})")
+        sampling = {"ms_per_step": s_ms, "tokens_per_s": stack.M / (s_ms * 1e-3), "temperature": 0.8,
+                    "launches_per_step": stack.launches_per_step() + 1,
+                    "path": "per projection qv_quantize_act + qv_w8a8_linear; LM head qv_w8a8_linear "
+                            "(fp32 logits) + qv_spec_sample (lossless rejection sampling against seeded "
+                            "draft distributions); one CUDA graph"}
+
     if rank == 0 and world == 1 and not args.no_cpu:
         cpu = cpu_baseline(args.cpu_seconds)
 
@@ -469,6 +486,7 @@ def main():
             "comparator": comparator,
             "paths_ms_per_step": paths_ms,
             "layer_chain": layer_chain,
+            "sampling_t_gt_0": sampling,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -260,6 +260,46 @@ class VerifyStack:
         qv.qv_accept(self.tokens.view(self.B, self.gamma + 1), self.drafts if self.gamma > 0 else None,
                      self.accept_len, self.out_tokens, stream=stream)
 
+    # ------------------------------------------------------------------ T > 0
+    def prepare_sampling(self, temperature: float = 0.8, seed: int = 1234):
+        """Buffers of the T > 0 step (enqueue_sampled): fp32 logits, seeded
+        draft distributions q (softmax of N(0, 2) logits) and drafts drawn
+        from them, the qv_spec_sample workspace."""
+        B, g, V, M = self.B, self.gamma, self.V, self.M
+        dev = self.device
+        self.temperature, self.sample_seed = temperature, seed
+        self.logits = torch.empty(M, V, dtype=torch.float32, device=dev)
+        gen = torch.Generator(device="cpu").manual_seed(synth.subseed(self.seed, "q"))
+        zq = 2.0 * torch.randn(max(B * g, 1), V, generator=gen)
+        self.q = torch.softmax(zq, dim=1)[: B * g].contiguous().to(dev)
+        self.q_drafts = (torch.multinomial(self.q.cpu().double(), 1, generator=gen).view(B, g).to(torch.int32)
+                         .to(dev) if g > 0 else torch.zeros(B, 0, dtype=torch.int32, device=dev))
+        self.ws_spec = torch.empty(qv.qv_workspace_bytes(qv.QV_OP_SPEC_SAMPLE, M, 16, V), dtype=torch.uint8,
+                                   device=dev)
+
+    def enqueue_sampled(self, stream=None):
+        """The verify step at temperature T > 0: the same layers as
+        enqueue_two_call, then the LM head's fp32 logits (qv_w8a8_linear) and
+        lossless rejection sampling against the draft distributions
+        (qv_spec_sample)."""
+        M = self.M
+        ws = self.ws
+        for l in range(self.layers):
+            for p, (name, K, N) in enumerate(self.phases):
+                xq = self._xq(K)
+                qv.qv_quantize_act(self.inputs[l][p], xq, self.sx, stream=stream)
+                wq, sw = self.weights[l][p]
+                qv.qv_w8a8_linear(xq, self.sx, wq, sw, self.y[: M * N].view(M, N), ws, stream=stream)
+        xq = self._xq(self.model["hidden"])
+        qv.qv_quantize_act(self.h_final, xq, self.sx, stream=stream)
+        qv.qv_w8a8_linear(xq, self.sx, self.lm_wq, self.lm_sw, self.logits, ws, stream=stream)
+        qv.qv_spec_sample(self.logits, self.q_drafts, self.q, self.temperature, self.sample_seed,
+                          self.accept_len, self.out_tokens, self.ws_spec, stream=stream)
+
+    def capture_sampled(self):
+        self.graph_sampled = self._capture(self.enqueue_sampled, self.device)
+        return self.graph_sampled
+
     def capture_chain(self):
         self.graph_chain = self._capture(self.enqueue_chain, self.device)
         return self.graph_chain

@@ -99,3 +99,17 @@ def test_spec_sample_closed_cases(qv, oracle):
     d_bad[:, 0] = [V, -1, 1 << 30]
     ln, out = _run(qv, z, d_bad, q, B, gamma, 1.0, 5)
     assert (ln == 1).all() and ((out[:, 0] >= 0) & (out[:, 0] < V)).all()
+
+
+def test_sampled_step_matches_oracle(qv, oracle):
+    """A small stack's T > 0 step (layers, LM-head logits, qv_spec_sample in
+    one graph) equals the oracle's sampling on the same logits."""
+    from quantized_verification_gb300.stack import VerifyStack
+    model = {"hidden": 256, "kv": 64, "ffn": 512, "layers": 2, "vocab": 3000}
+    st = VerifyStack(model=model, B=2, gamma=3, seed=9)
+    st.prepare_sampling(temperature=0.9, seed=77)
+    g = st.capture_sampled()
+    g.replay()
+    torch.cuda.synchronize()
+    ln_ref, out_ref = oracle.spec_sample(np_(st.logits), np_(st.q_drafts), np_(st.q), 2, 3, 0.9, 77)
+    assert np.array_equal(np_(st.accept_len), ln_ref) and np.array_equal(np_(st.out_tokens), out_ref)
