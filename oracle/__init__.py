@@ -82,6 +82,7 @@ class Oracle:
         L.qvo_splitmix64.restype = ctypes.c_uint64
         L.qvo_splitmix64.argtypes = [ctypes.c_uint64, ctypes.c_uint64]
         L.qvo_spec_sample.argtypes = [_P, _P, _P, _I, _I, _I, ctypes.c_float, ctypes.c_uint64, _P, _P]
+        L.qvo_tree_accept.argtypes = [_P, _P, _P, _I, _I, _P, _P, _P]
         L.qvo_draw_index.restype = ctypes.c_int32
         L.qvo_draw_index.argtypes = [_P, _I, ctypes.c_uint64, ctypes.c_uint32]
 
@@ -277,6 +278,22 @@ class Oracle:
         self._L.qvo_spec_sample(_ptr(z), _ptr(d) if d.size else None, _ptr(q) if q.size else None,
                                 B, gamma, V, ctypes.c_float(T), seed & (2 ** 64 - 1), _ptr(ln), _ptr(out))
         return ln, out.reshape(B, gamma + 1)
+
+    # -- f3: tree verification at T = 0 ------------------------------------
+    def tree_accept(self, t: np.ndarray, d: np.ndarray, par: np.ndarray):
+        """Greedy tree verification: t, d, par [B, N] int32 (node 0 the root,
+        parents before children). Returns (len [B], out [B, N], node [B]): the
+        deepest fully matching root path (lowest index on ties), its drafted
+        tokens, then the verifier's token after it."""
+        t = np.ascontiguousarray(t, dtype=np.int32)
+        B, N = t.shape
+        d = np.ascontiguousarray(d, dtype=np.int32)
+        par = np.ascontiguousarray(par, dtype=np.int32)
+        ln = np.empty(B, dtype=np.int32)
+        out = np.empty((B, N), dtype=np.int32)
+        node = np.empty(B, dtype=np.int32)
+        self._L.qvo_tree_accept(_ptr(t), _ptr(d), _ptr(par), B, N, _ptr(ln), _ptr(out), _ptr(node))
+        return ln, out, node
 
 _default: Oracle | None = None
 _lock = threading.Lock()

@@ -45,6 +45,13 @@
  *       -- gist.science/it summary, section 2 item 3 ("Campionamento di
  *          Rifiuto Lossless": the verifier's logits stay precise so that
  *          the target distribution is kept).
+ *   f3  tree verification at T = 0: the drafts form a tree; the verifier's
+ *       greedy tokens are computed for every node at once, and the deepest
+ *       root path whose every drafted token equals the verifier's token after
+ *       its parent is accepted, plus the verifier's token after its last node
+ *       -- tree-structured verification named as an extension by the
+ *          summaries (gist.science/ja summary, section 4; shd-paper.top,
+ *          outlook); the acceptance rule is a4's applied along each path.
  *   a4  acceptance: the longest draft prefix equal to the verifier's tokens,
  *       plus one token from the verifier (so at least one token per step)
  *       -- gist.science/fr summary, lay explanation (a wrong guess is
@@ -582,4 +589,53 @@ void qvo_spec_sample(const float* z, const int32_t* d, const float* q, int64_t B
             out[b * G + j] = j < k ? d[b * gamma + j] : (j == k ? tok : -1);
     }
     free(w); free(c); free(x64); free(x128);
+}
+
+/* ------------------------------------------------------------------ */
+/* f3: tree verification at T = 0                                      */
+/* ------------------------------------------------------------------ */
+
+/*
+ * B trees of N nodes. Node 0 of tree b is its root (the last accepted
+ * position); node i >= 1 has parent par[b*N+i] (valid when in [0, i)) and
+ * drafted token d[b*N+i]; t[b*N+i] is the verifier's greedy token after the
+ * root path of node i.
+ *   accepted(0) = true; accepted(i) = par in [0, i) and accepted(par) and
+ *   d[i] == t[par]; depth(0) = 0, depth(i) = depth(par) + 1.
+ *   best = the accepted node of largest depth, the lowest index among them.
+ *   len[b] = depth(best) + 1; out[b][0 .. depth-1] = the drafted tokens on
+ *   the path root -> best (root excluded), out[b][depth] = t[best], then -1
+ *   (out has N entries per tree); node[b] = best.
+ */
+void qvo_tree_accept(const int32_t* t, const int32_t* d, const int32_t* par, int64_t B, int64_t N,
+                     int32_t* len, int32_t* out, int32_t* node)
+{
+    int32_t* depth = (int32_t*)malloc((size_t)N * sizeof(int32_t));
+    uint8_t* acc = (uint8_t*)malloc((size_t)N);
+    for (int64_t b = 0; b < B; ++b) {
+        const int32_t* tb = t + b * N;
+        const int32_t* db = d + b * N;
+        const int32_t* pb = par + b * N;
+        acc[0] = 1;
+        depth[0] = 0;
+        int64_t best = 0;
+        for (int64_t i = 1; i < N; ++i) {
+            int32_t p = pb[i];
+            acc[i] = (p >= 0 && p < i && acc[p] && db[i] == tb[p]) ? 1 : 0;
+            depth[i] = (p >= 0 && p < i) ? depth[p] + 1 : 0;
+            if (acc[i] && depth[i] > depth[best]) best = i;
+        }
+        int32_t D = depth[best];
+        len[b] = D + 1;
+        for (int64_t j = 0; j < N; ++j) out[b * N + j] = -1;
+        out[b * N + D] = tb[best];
+        int64_t i = best;
+        for (int32_t k = D - 1; k >= 0; --k) {
+            out[b * N + k] = db[i];
+            i = pb[i];
+        }
+        if (node) node[b] = (int32_t)best;
+    }
+    free(depth);
+    free(acc);
 }

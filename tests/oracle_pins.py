@@ -546,6 +546,66 @@ def pin_spec_special_cases(o):
             assert list(out[b, : ln[b] - 1]) == list(d[b, : ln[b] - 1])
             assert 0 <= out[b, ln[b] - 1] < V and (out[b, ln[b]:] == -1).all()
 
+
+# ---------------------------------------------------------------------------
+# f3: tree verification at T = 0
+# ---------------------------------------------------------------------------
+def _random_tree(rng, N, V):
+    par = np.full(N, -1, np.int32)
+    for i in range(1, N):
+        par[i] = rng.integers(0, i)
+    return par
+
+
+def pin_tree_chain_is_linear(o):
+    """A chain-shaped tree (parent of node i is i-1) is the linear rule:
+    the same lengths and tokens as a4 on the chain's drafts."""
+    rng = np.random.default_rng(17)
+    B, gamma, V = 64, 5, 3
+    t = rng.integers(0, V, (B, gamma + 1)).astype(np.int32)
+    dl = rng.integers(0, V, (B, gamma)).astype(np.int32)
+    par = np.tile(np.arange(-1, gamma, dtype=np.int32), (B, 1))
+    d = np.concatenate([np.zeros((B, 1), np.int32), dl], axis=1)
+    ln, out, node = o.tree_accept(t, d, par)
+    ln_ref, out_ref = o.accept(t, dl, B, gamma)
+    assert np.array_equal(ln, ln_ref) and np.array_equal(out, out_ref)
+    assert np.array_equal(node, ln - 1)
+
+
+def pin_tree_bruteforce(o):
+    """Random tiny trees: every root path checked on its own (walk up from
+    each node, all edges matching); the deepest matching node, lowest index
+    among the deepest, its path and bonus, against the oracle."""
+    rng = np.random.default_rng(23)
+    for _ in range(300):
+        N = int(rng.integers(1, 9))
+        V = int(rng.integers(1, 4))
+        par = _random_tree(rng, N, V)
+        t = rng.integers(0, V, N).astype(np.int32)
+        d = rng.integers(0, V, N).astype(np.int32)
+        best, best_depth = 0, 0
+        for i in range(N):
+            path, j, ok = [], i, True
+            while j != 0:
+                p = int(par[j])
+                ok = ok and d[j] == t[p]
+                path.append(j)
+                j = p
+            if ok and len(path) > best_depth:
+                best, best_depth = i, len(path)
+        exp_out = [int(d[j]) for j in reversed(_path(par, best))] + [int(t[best])]
+        exp_out += [-1] * (N - len(exp_out))
+        ln, out, node = o.tree_accept(t[None], d[None], par[None])
+        assert ln[0] == best_depth + 1 and node[0] == best and list(out[0]) == exp_out
+
+
+def _path(par, i):
+    out = []
+    while i != 0:
+        out.append(i)
+        i = int(par[i])
+    return out
+
 ALL_PINS = [
     pin_worked_example,
     pin_quantize_exact_rational,
@@ -567,4 +627,6 @@ ALL_PINS = [
     pin_spec_lossless,
     pin_draw_index,
     pin_spec_special_cases,
+    pin_tree_chain_is_linear,
+    pin_tree_bruteforce,
 ]

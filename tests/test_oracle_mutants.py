@@ -54,6 +54,13 @@ MUTANTS = [
     ("spec_same_draw_for_both", "(uint64_t)(2 * row + 1)) >> 40);\n            if (R > 0)",
      "(uint64_t)(2 * row)) >> 40);\n            if (R > 0)"),
     ("splitmix_constant", "0xBF58476D1CE4E5B9ull", "0xBF58476D1CE4E5B8ull"),
+    ("tree_own_token", "acc[i] = (p >= 0 && p < i && acc[p] && db[i] == tb[p]) ? 1 : 0;",
+     "acc[i] = (p >= 0 && p < i && acc[p] && db[i] == tb[i]) ? 1 : 0;"),
+    ("tree_ignores_ancestors", "acc[i] = (p >= 0 && p < i && acc[p] && db[i] == tb[p]) ? 1 : 0;",
+     "acc[i] = (p >= 0 && p < i && db[i] == tb[p]) ? 1 : 0;"),
+    ("tree_ties_last", "if (acc[i] && depth[i] > depth[best]) best = i;",
+     "if (acc[i] && depth[i] >= depth[best]) best = i;"),
+    ("tree_bonus_from_parent", "out[b * N + D] = tb[best];", "out[b * N + D] = tb[pb[best] >= 0 ? pb[best] : 0];"),
     ("residual_not_added",
      "hr[k] = qvo_f32_to_bf16_rne(qvo_bf16_to_f32(hr[k]) + qvo_bf16_to_f32(d[m * H + k]));",
      "hr[k] = hr[k];"),
