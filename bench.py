@@ -459,6 +459,35 @@ def main():
                             "(fp32 logits) + qv_spec_sample (lossless rejection sampling against seeded "
                             "draft distributions); one CUDA graph"}
 
+    # ---- a 16-node draft tree (root, 3 children, 2 grandchildren each, one
+    # great-grandchild each) verified in one step, greedy
+    tree = None
+    if rank == 0:
+        n_tree = 16
+        parent = torch.tensor([[-1, 0, 0, 0, 1, 1, 2, 2, 3, 3, 4, 5, 6, 7, 8, 9]], dtype=torch.int32)
+        tstack = VerifyStack(B=1, gamma=n_tree - 1, seed=7 + rank, layers=args.layers, device=str(dev))
+        tstack.prepare_tree(parent, torch.zeros(1, n_tree, dtype=torch.int32))
+        tstack.enqueue_tree()
+        torch.cuda.synchronize()
+        tv = tstack.tokens.cpu()
+        draft = torch.randint(0, tstack.V, (1, n_tree), generator=torch.Generator().manual_seed(5),
+                              dtype=torch.int32)
+        for node in (1, 4, 10):                 # the path 0 -> 1 -> 4 -> 10 matches the verifier
+            draft[0, node] = tv[int(parent[0, node])]
+        tstack.prepare_tree(parent, draft)
+        tg = tstack.capture_tree()
+        for _ in range(3):
+            tg.replay()
+        torch.cuda.synchronize()
+        t_ms = time_graph(torch, tg, max(20, args.steps // 5), stream)
+        log(f"16-node tree step {t_ms:.4f} ms/step, accepted length {int(tstack.tree_len[0])}")
+        tree = {"nodes": n_tree, "ms_per_step": t_ms, "accept_len": int(tstack.tree_len[0]),
+                "verified_nodes_per_s": n_tree / (t_ms * 1e-3),
+                "path": "layers over the 16 tree rows (qv_quantize_act + qv_w8a8_linear), LM-head argmax, "
+                        "qv_tree_accept; one CUDA graph"}
+        del tg, tstack
+        torch.cuda.empty_cache()
+
     if rank == 0 and world == 1 and not args.no_cpu:
         cpu = cpu_baseline(args.cpu_seconds)
 
@@ -487,6 +516,7 @@ def main():
             "paths_ms_per_step": paths_ms,
             "layer_chain": layer_chain,
             "sampling_t_gt_0": sampling,
+            "tree_verify": tree,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

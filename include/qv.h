@@ -281,6 +281,31 @@ QV_API qv_status qv_swiglu_quant(const float* gate_up, int M, int F, int8_t* xq,
                                  cudaStream_t stream);
 
 /*
+ * qv_tree_accept -- greedy (T = 0) verification of a draft tree.
+ *
+ *   Tree-structured verification is the extension the summaries name for
+ *   the drafts (gist.science/ja summary, section 4; shd-paper.top, outlook);
+ *   along each root path the rule is qv_accept's.
+ *
+ * Tree b has N nodes, stored at [b*N + i]: node 0 is the root (the last
+ * accepted position); node i >= 1 has parent[i] (valid when in [0, i)) and
+ * drafted token draft[i] (draft[0] and parent[0] are ignored);
+ * verify_tokens[i] is the verifier's greedy token after node i's root path
+ * (e.g. qv_lm_head_argmax over the M = B*N tree rows with a tree attention
+ * mask). Node i is accepted when every node j != 0 on its root path has a
+ * valid parent p and draft[j] == verify_tokens[p].
+ *   best = the accepted node of largest depth, the lowest index among them
+ *   accept_len[b] = depth(best) + 1                       (in [1, N])
+ *   out_tokens[b*N + 0 .. depth-1] = the drafted tokens on the root -> best
+ *   path, out_tokens[b*N + depth] = verify_tokens[best], then -1
+ *   best_node[b] = best (or NULL)
+ * Token ids are compared as raw int32. 1 <= B <= 65535, 1 <= N <= 1024.
+ */
+QV_API qv_status qv_tree_accept(const int32_t* verify_tokens, const int32_t* draft, const int32_t* parent,
+                                int B, int N, int32_t* accept_len, int32_t* out_tokens, int32_t* best_node,
+                                cudaStream_t stream);
+
+/*
  * qv_spec_sample -- acceptance at temperature T > 0: lossless rejection
  * sampling (speculative sampling) over the verifier's logits.
  *

@@ -455,6 +455,26 @@ qv_status qv_swiglu_quant(const float* gate_up, int M, int F, int8_t* xq, float*
     return ok();
 }
 
+qv_status qv_tree_accept(const int32_t* verify_tokens, const int32_t* draft, const int32_t* parent, int B, int N,
+                         int32_t* accept_len, int32_t* out_tokens, int32_t* best_node, cudaStream_t stream) {
+    if (!verify_tokens || !draft || !parent || !accept_len || !out_tokens) return fail(QV_ERR_INVALID_ARG, "null pointer");
+    if (B < 1 || B > 65535) return fail(QV_ERR_INVALID_ARG, "B=%d outside [1, 65535]", B);
+    if (N < 1 || N > 1024) return fail(QV_ERR_INVALID_ARG, "N=%d outside [1, 1024]", N);
+    if (!aligned(verify_tokens, 4) || !aligned(draft, 4) || !aligned(parent, 4) || !aligned(accept_len, 4) ||
+        !aligned(out_tokens, 4) || (best_node && !aligned(best_node, 4)))
+        return fail(QV_ERR_INVALID_ARG, "int32 buffers must be 4-byte aligned");
+    QV_CHECK_DEV(verify_tokens);
+    QV_CHECK_DEV(draft);
+    QV_CHECK_DEV(parent);
+    QV_CHECK_DEV(accept_len);
+    QV_CHECK_DEV(out_tokens);
+    QV_CHECK_DEV(best_node);
+    cudaError_t e = qv::launch_tree_accept(verify_tokens, draft, parent, B, N, accept_len, out_tokens, best_node,
+                                           stream);
+    if (e != cudaSuccess) return cuda_fail(e, "qv_tree_accept launch");
+    return ok();
+}
+
 qv_status qv_spec_sample(const float* logits, const int32_t* draft, const float* draft_probs, int B,
                          int gamma, int V, float temperature, uint64_t seed, int32_t* accept_len,
                          int32_t* out_tokens, void* workspace, size_t workspace_bytes, cudaStream_t stream) {

@@ -113,6 +113,10 @@ constexpr size_t kMaxDynSmem = 232448;
 constexpr size_t kMinSmemOneCtaPerSm = 118 * 1024;
 cudaError_t launch_verify_stack(const StackLaunch& a, int num_sms, cudaStream_t s);
 cudaError_t launch_bf16_stream(const Bf16Launch& a, int num_sms, cudaStream_t s);
+// Greedy tree verification (k_tree.cu), N <= 1024 nodes per tree.
+cudaError_t launch_tree_accept(const int32_t* t, const int32_t* d, const int32_t* par, int B, int N,
+                               int32_t* len, int32_t* out, int32_t* node, cudaStream_t s);
+
 // Speculative sampling at T > 0 (k_spec.cu): 32 bytes of row statistics per
 // verify row in the workspace.
 size_t spec_workspace_bytes(int M);

@@ -28,7 +28,8 @@ EXPORTS = ("qv_quantize_act", "qv_w8a8_linear", "qv_lm_head_argmax", "qv_accept"
            "qv_quantize_weight", "qv_bf16_linear", "qv_workspace_bytes",
            "qv_last_error", "qv_device_error", "qv_num_sms", "qv_w8a8_linear_noalloc",
            "qv_verify_stack", "qv_w8a8_linear_act", "qv_lm_head_argmax_act",
-           "qv_rmsnorm_quant", "qv_swiglu_quant", "qv_w8a8_swiglu", "qv_spec_sample")
+           "qv_rmsnorm_quant", "qv_swiglu_quant", "qv_w8a8_swiglu", "qv_spec_sample",
+           "qv_tree_accept")
 MAX_STACK_M = 16
 
 
@@ -77,6 +78,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         L.qv_swiglu_quant.argtypes = [P, I, I, P, P, P]
         L.qv_w8a8_swiglu.argtypes = [P, P, I, I, P, P, I, P, P, S, P]
         L.qv_spec_sample.argtypes = [P, P, P, I, I, I, ctypes.c_float, ctypes.c_uint64, P, P, P, S, P]
+        L.qv_tree_accept.argtypes = [P, P, P, I, I, P, P, P, P]
         L.qv_workspace_bytes.argtypes = [I, I, I, I]
         L.qv_workspace_bytes.restype = S
         L.qv_last_error.argtypes = []
@@ -181,6 +183,20 @@ def qv_w8a8_swiglu(xq, sx, wq_gu, sw_gu, a, workspace, stream=None):
     _need(workspace.dtype == torch.uint8, "workspace must be a uint8 tensor")
     _check(load().qv_w8a8_swiglu(_ptr(xq), _ptr(sx), M, K, _ptr(wq_gu), _ptr(sw_gu), F, _ptr(a),
                                  _ptr(workspace), workspace.numel(), ctypes.c_void_p(_stream(stream))))
+
+
+def qv_tree_accept(verify_tokens, draft, parent, accept_len, out_tokens, best_node=None, stream=None):
+    """Greedy tree verification: verify_tokens, draft, parent [B, N] int32 ->
+    accept_len [B], out_tokens [B, N], best_node [B] (optional)."""
+    B, N = verify_tokens.shape
+    for name, tsr in (("verify_tokens", verify_tokens), ("draft", draft), ("parent", parent),
+                      ("out_tokens", out_tokens)):
+        _need(tsr.shape == (B, N) and tsr.dtype == torch.int32, f"{name} must be int32 [B, N]")
+    _need(accept_len.shape == (B,) and accept_len.dtype == torch.int32, "accept_len int32 [B]")
+    if best_node is not None:
+        _need(best_node.shape == (B,) and best_node.dtype == torch.int32, "best_node int32 [B]")
+    _check(load().qv_tree_accept(_ptr(verify_tokens), _ptr(draft), _ptr(parent), B, N, _ptr(accept_len),
+                                 _ptr(out_tokens), _ptr(best_node), ctypes.c_void_p(_stream(stream))))
 
 
 def qv_spec_sample(logits, draft, draft_probs, temperature, seed, accept_len, out_tokens, workspace,

@@ -260,6 +260,40 @@ class VerifyStack:
         qv.qv_accept(self.tokens.view(self.B, self.gamma + 1), self.drafts if self.gamma > 0 else None,
                      self.accept_len, self.out_tokens, stream=stream)
 
+    # ------------------------------------------------------------------ draft tree
+    def prepare_tree(self, parent: torch.Tensor, draft: torch.Tensor):
+        """A draft tree over the step's M = N rows (B = 1): parent, draft [1, N]
+        int32 (node 0 the root); row i's verifier token follows node i."""
+        assert self.B == 1 and parent.shape == (1, self.M) and draft.shape == (1, self.M)
+        dev = self.device
+        self.tree_parent = parent.to(dev, torch.int32).contiguous()
+        self.tree_draft = draft.to(dev, torch.int32).contiguous()
+        self.tree_len = torch.empty(1, dtype=torch.int32, device=dev)
+        self.tree_out = torch.empty(1, self.M, dtype=torch.int32, device=dev)
+        self.tree_node = torch.empty(1, dtype=torch.int32, device=dev)
+
+    def enqueue_tree(self, stream=None):
+        """The verify step of a draft tree: the layers over all N tree rows
+        (as enqueue_two_call), the LM head's greedy tokens, then
+        qv_tree_accept (the deepest fully matching root path)."""
+        M = self.M
+        ws = self.ws
+        for l in range(self.layers):
+            for p, (name, K, N) in enumerate(self.phases):
+                xq = self._xq(K)
+                qv.qv_quantize_act(self.inputs[l][p], xq, self.sx, stream=stream)
+                wq, sw = self.weights[l][p]
+                qv.qv_w8a8_linear(xq, self.sx, wq, sw, self.y[: M * N].view(M, N), ws, stream=stream)
+        xq = self._xq(self.model["hidden"])
+        qv.qv_quantize_act(self.h_final, xq, self.sx, stream=stream)
+        qv.qv_lm_head_argmax(xq, self.sx, self.lm_wq, self.lm_sw, self.tokens, ws, stream=stream)
+        qv.qv_tree_accept(self.tokens.view(1, M), self.tree_draft, self.tree_parent, self.tree_len,
+                          self.tree_out, best_node=self.tree_node, stream=stream)
+
+    def capture_tree(self):
+        self.graph_tree = self._capture(self.enqueue_tree, self.device)
+        return self.graph_tree
+
     # ------------------------------------------------------------------ T > 0
     def prepare_sampling(self, temperature: float = 0.8, seed: int = 1234):
         """Buffers of the T > 0 step (enqueue_sampled): fp32 logits, seeded

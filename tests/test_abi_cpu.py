@@ -92,6 +92,11 @@ def test_host_validation_without_gpu(lib):
     assert lib.qv_lm_head_argmax_act(fake, 1, None, 5, 256, fake, fake, 8, None, None, fake, 1 << 20, None) == qv.QV_ERR_INVALID_ARG
     assert b"tokens" in lib.qv_last_error()
     assert lib.qv_lm_head_argmax_act(fake, 1, None, 5, 250, fake, fake, 8, fake, None, fake, 1 << 20, None) == qv.QV_ERR_INVALID_ARG
+    # greedy tree verification
+    assert lib.qv_tree_accept(None, fake, fake, 1, 16, fake, fake, None, None) == qv.QV_ERR_INVALID_ARG
+    assert lib.qv_tree_accept(fake, fake, fake, 1, 1025, fake, fake, None, None) == qv.QV_ERR_INVALID_ARG
+    assert lib.qv_tree_accept(fake, fake, fake, 0, 16, fake, fake, None, None) == qv.QV_ERR_INVALID_ARG
+    assert lib.qv_tree_accept(fake, P(0x1002), fake, 1, 16, fake, fake, None, None) == qv.QV_ERR_INVALID_ARG
     # speculative sampling at T > 0
     F32 = ctypes.c_float
     U64 = ctypes.c_uint64
