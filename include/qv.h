@@ -72,7 +72,7 @@ typedef enum {
     QV_OP_VERIFY_STACK = 3,   /* qv_verify_stack (K, N = largest K, N / V) */
     QV_OP_LINEAR_ACT = 4,     /* qv_w8a8_linear_act                        */
     QV_OP_LM_HEAD_ACT = 5,    /* qv_lm_head_argmax_act (N = V)             */
-    QV_OP_SPEC_SAMPLE = 6     /* qv_spec_sample (M = B*(gamma+1); K, N ignored) */
+    QV_OP_SPEC_SAMPLE = 6     /* qv_spec_sample (M = B*(gamma+1), N = V; K ignored) */
 } qv_op;
 
 /* floor((2^31 - 1) / 127^2): the int32 accumulation stays exact up to here. */
@@ -326,7 +326,8 @@ QV_API qv_status qv_tree_accept(const int32_t* verify_tokens, const int32_t* dra
  *   accept_len  [B] out, in [1, gamma+1]; out_tokens [B*(gamma+1)] out: the
  *               kept drafts, the replacement or bonus token, then -1
  *   workspace   qv_workspace_bytes(QV_OP_SPEC_SAMPLE, B*(gamma+1), 16, V)
- *               bytes (row statistics, scratch; no zero-fill needed)
+ *               bytes, 16-byte aligned (per-chunk maxima and sums, row
+ *               statistics; no zero-fill needed)
  * Arithmetic (so that every decision is exact and reproducible): with E the
  * library's binary32 exp (qv_swiglu_quant), m = max_v z_v,
  * w_v = floor(E(fl32(fl32(z_v - m) / T)) * 2^24), Z = sum w_v,

@@ -182,7 +182,8 @@ int qv_num_sms(void) {
 }
 
 size_t qv_workspace_bytes(qv_op op, int M, int K, int N) {
-    if (op == QV_OP_SPEC_SAMPLE) return (M >= 1 && M <= 65535) ? (qv::spec_workspace_bytes(M) + 255) & ~size_t(255) : 0;
+    if (op == QV_OP_SPEC_SAMPLE)
+        return (M >= 1 && M <= 65535 && N >= 1 && N <= (1 << 24)) ? qv::spec_workspace_bytes(M, N) : 0;
     if (M < 1 || M > QV_MAX_M || N < 1 || K < 16 || K % 16 != 0 || K > QV_MAX_K) return 0;
     const int mp = mp_for(M < qv::kMaxMPerLaunch ? M : qv::kMaxMPerLaunch);
     switch (op) {

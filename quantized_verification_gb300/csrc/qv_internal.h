@@ -117,9 +117,10 @@ cudaError_t launch_bf16_stream(const Bf16Launch& a, int num_sms, cudaStream_t s)
 cudaError_t launch_tree_accept(const int32_t* t, const int32_t* d, const int32_t* par, int B, int N,
                                int32_t* len, int32_t* out, int32_t* node, cudaStream_t s);
 
-// Speculative sampling at T > 0 (k_spec.cu): 32 bytes of row statistics per
-// verify row in the workspace.
-size_t spec_workspace_bytes(int M);
+// Speculative sampling at T > 0 (k_spec.cu): per-chunk maxima and sums, row
+// statistics and the decisions for M rows of V tokens (every call rewrites
+// all of it, so the workspace needs no initialisation).
+size_t spec_workspace_bytes(int M, int V);
 cudaError_t launch_spec_sample(const float* logits, const int32_t* draft, const float* q, int B, int gamma,
                                int V, float T, uint64_t seed, int32_t* accept_len, int32_t* out_tokens,
                                void* ws, cudaStream_t s);

@@ -106,8 +106,16 @@ def test_host_validation_without_gpu(lib):
     assert b"temperature" in lib.qv_last_error()
     assert lib.qv_spec_sample(fake, fake, fake, 1, 4, 0, F32(1.0), U64(1), fake, fake, fake, 1 << 20, None) == qv.QV_ERR_INVALID_ARG
     assert lib.qv_spec_sample(fake, fake, fake, 1, 4, 1000, F32(1.0), U64(1), fake, fake, fake, 16, None) == qv.QV_ERR_WORKSPACE
-    assert qv.qv_workspace_bytes(qv.QV_OP_SPEC_SAMPLE, 5, 16, 151936) == 256
-    assert qv.qv_workspace_bytes(qv.QV_OP_SPEC_SAMPLE, 80, 16, 151936) == 2560
+    # chunks of 2048 tokens: per (row, chunk) a float max, two u64 sums and a
+    # u128 draw sum; 32 bytes of statistics and an int decision per row;
+    # every region rounded up to 256 bytes
+    r256 = lambda v: (v + 255) // 256 * 256
+    for M, V in ((5, 151936), (80, 151936), (1, 1), (3, 2049)):
+        S = (V + 2047) // 2048
+        want = r256(M * S * 4) + 2 * r256(M * S * 8) + r256(M * 32) + r256(M * S * 16) + r256(M * 4)
+        assert qv.qv_workspace_bytes(qv.QV_OP_SPEC_SAMPLE, M, 16, V) == want
+    assert qv.qv_workspace_bytes(qv.QV_OP_SPEC_SAMPLE, 5, 16, 0) == 0
+    assert qv.qv_workspace_bytes(qv.QV_OP_SPEC_SAMPLE, 0, 16, 1000) == 0
     # the layer's fused non-linear steps
     assert lib.qv_rmsnorm_quant(None, None, fake, F32(1e-6), None, 5, 256, fake, fake, None, None) == qv.QV_ERR_INVALID_ARG
     assert lib.qv_rmsnorm_quant(fake, None, fake, F32(1e-6), None, 5, 264, fake, fake, None, None) == qv.QV_ERR_INVALID_ARG

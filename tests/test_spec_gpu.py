@@ -42,8 +42,10 @@ def _case(B, gamma, V, mode, seed):
 
 def _run(qv, z, d, q, B, gamma, T, seed):
     V = z.shape[1]
-    ws = torch.empty(qv.qv_workspace_bytes(qv.QV_OP_SPEC_SAMPLE, B * (gamma + 1), 16, V), dtype=torch.uint8,
-                     device="cuda")
+    # the workspace needs no initialisation: hand it over full of junk
+    g = torch.Generator(device="cuda").manual_seed(seed)
+    ws = torch.randint(0, 256, (qv.qv_workspace_bytes(qv.QV_OP_SPEC_SAMPLE, B * (gamma + 1), 16, V),),
+                       dtype=torch.uint8, device="cuda", generator=g)
     ln = torch.full((B,), -7, dtype=torch.int32, device="cuda")
     out = torch.full((B, gamma + 1), -7, dtype=torch.int32, device="cuda")
     qv.qv_spec_sample(torch.from_numpy(z).cuda(), torch.from_numpy(d).cuda(), torch.from_numpy(q).cuda(),
@@ -59,6 +61,8 @@ CASES = [  # B, gamma, V, T, draft distribution
     (4, 3, 64, 0.5, "close"),
     (8, 7, 3000, 1.0, "far"),
     (2, 3, 1, 1.0, "close"),
+    (2, 2, 6145, 0.9, "far"),        # three full 2048-token chunks and a 1-token tail
+    (1, 1, 2100000, 1.0, "close"),   # more chunks (1026) than draw-kernel threads
 ]
 
 
