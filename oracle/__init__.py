@@ -83,6 +83,9 @@ class Oracle:
         L.qvo_splitmix64.argtypes = [ctypes.c_uint64, ctypes.c_uint64]
         L.qvo_spec_sample.argtypes = [_P, _P, _P, _I, _I, _I, ctypes.c_float, ctypes.c_uint64, _P, _P]
         L.qvo_tree_accept.argtypes = [_P, _P, _P, _I, _I, _P, _P, _P]
+        L.qvo_quantize_rows_w4_f32.argtypes = [_P, _I, _I, _P, _P]
+        L.qvo_pack_w4.argtypes = [_P, _I, _I, _P]
+        L.qvo_unpack_w4.argtypes = [_P, _I, _I, _P]
         L.qvo_draw_index.restype = ctypes.c_int32
         L.qvo_draw_index.argtypes = [_P, _I, ctypes.c_uint64, ctypes.c_uint32]
 
@@ -294,6 +297,50 @@ class Oracle:
         node = np.empty(B, dtype=np.int32)
         self._L.qvo_tree_accept(_ptr(t), _ptr(d), _ptr(par), B, N, _ptr(ln), _ptr(out), _ptr(node))
         return ln, out, node
+
+    # -- f4: W4A8 ----------------------------------------------------------
+    def quantize_rows_w4(self, w: np.ndarray, bf16: bool = False):
+        """Per-output-channel symmetric int4 weights, the a0 rule with codes in
+        [-7, 7] (lower-bit verifiers: gist.science/it summary, conclusions;
+        INT4 among the widths tried, paper-digest summary, key design).
+        ``w`` float32 [N, K], or bf16 patterns with ``bf16=True`` (widened
+        exactly). Returns (q int8 [N, K] codes, s float32 [N])."""
+        if bf16:
+            w = self.bf16_to_f32(np.ascontiguousarray(w, dtype=np.uint16))
+        w = np.ascontiguousarray(w, dtype=np.float32)
+        N, K = w.shape
+        q = np.empty((N, K), dtype=np.int8)
+        s = np.empty(N, dtype=np.float32)
+        self._L.qvo_quantize_rows_w4_f32(_ptr(w), N, K, _ptr(q), _ptr(s))
+        return q, s
+
+    def pack_w4(self, q: np.ndarray) -> np.ndarray:
+        """Two int4 codes per byte, even k in the low nibble: uint8 [N, K/2]."""
+        q = np.ascontiguousarray(q, dtype=np.int8)
+        N, K = q.shape
+        assert K % 2 == 0
+        out = np.empty((N, K // 2), dtype=np.uint8)
+        self._L.qvo_pack_w4(_ptr(q), N, K, _ptr(out))
+        return out
+
+    def unpack_w4(self, packed: np.ndarray) -> np.ndarray:
+        """Inverse of pack_w4: int8 codes [N, 2 * bytes]."""
+        packed = np.ascontiguousarray(packed, dtype=np.uint8)
+        N, KB = packed.shape
+        q = np.empty((N, 2 * KB), dtype=np.int8)
+        self._L.qvo_unpack_w4(_ptr(packed), N, 2 * KB, _ptr(q))
+        return q
+
+    def w4a8_linear(self, xq, sx, wq4, sw):
+        """f4: y = dequant(sum_k xq[m, k] * w[n, k]) with the int4 codes
+        unpacked from ``wq4``; the sums and the dequantization are a2's.
+        Returns (y float32 [M, N], acc int32 [M, N])."""
+        return self.w8a8_linear(xq, sx, self.unpack_w4(wq4), sw)
+
+    def w4a8_lm_head_argmax(self, xq, sx, wq4, sw):
+        """f4 with the a3 greedy argmax (lowest index on ties)."""
+        return self.lm_head_argmax(xq, sx, self.unpack_w4(wq4), sw)
+
 
 _default: Oracle | None = None
 _lock = threading.Lock()

@@ -52,6 +52,12 @@
  *       -- tree-structured verification named as an extension by the
  *          summaries (gist.science/ja summary, section 4; shd-paper.top,
  *          outlook); the acceptance rule is a4's applied along each path.
+ *   f4  a lower-bit verifier, W4A8: int4 weights against the a1 int8
+ *       activations, accumulated exactly in integers and dequantized as in a2
+ *       -- lower bit widths (4-bit, 2-bit) named as the next step by the
+ *          summaries (gist.science/it summary, conclusions; gist.science/de
+ *          summary, outlook; shd-paper.top, future work), INT4 among the
+ *          bit widths the authors tried (paper-digest summary, key design).
  *   a4  acceptance: the longest draft prefix equal to the verifier's tokens,
  *       plus one token from the verifier (so at least one token per step)
  *       -- gist.science/fr summary, lay explanation (a wrong guess is
@@ -100,6 +106,12 @@
  *     pseudorandom number generators", 2014) used as a counter-based
  *     generator: draw n of seed s is mix(s + (n + 1) * 0x9E3779B97F4A7C15);
  *     n = 2 * row + purpose (0: keep test, 1: sample), row = b * (gamma + 1) + j.
+ *   - f4 (no int4 format is given): per-output-channel symmetric int4, the
+ *     a0 rule with 7 in place of 127: s = fl32(amax / 7),
+ *     q = clamp(rne(fl32(w / s)), -7, 7), q = 0 when s = 0; two codes per
+ *     byte, code k even in the low nibble and k + 1 in the high nibble, each
+ *     a 4-bit two's complement (so -8 is never produced); the integer sums
+ *     and the dequantization are a2's.
  *   - acceptance: row j of sequence b holds the verifier token t[b][j] that
  *     follows prefix position j; draft d[b][j] is accepted iff it equals
  *     t[b][j] and all earlier drafts were accepted; the verifier token at the
@@ -638,4 +650,59 @@ void qvo_tree_accept(const int32_t* t, const int32_t* d, const int32_t* par, int
     }
     free(depth);
     free(acc);
+}
+
+/* ------------------------------------------------------------------ */
+/* f4: W4A8, int4 weights                                               */
+/* ------------------------------------------------------------------ */
+
+/* Per-row symmetric int4 quantization of weights: the a0 rule with the
+ * code range [-7, 7]. x is rows*K binary32 values (bf16 callers widen
+ * first); q gets one code per int8. */
+void qvo_quantize_rows_w4_f32(const float* x, int64_t rows, int64_t K, int8_t* q, float* s)
+{
+    for (int64_t r = 0; r < rows; ++r) {
+        const float* xr = x + r * K;
+        float amax = 0.0f;
+        for (int64_t k = 0; k < K; ++k) {
+            float a = fabsf(xr[k]);
+            if (a > amax) amax = a;
+        }
+        float scale = amax / 7.0f;
+        s[r] = scale;
+        for (int64_t k = 0; k < K; ++k) {
+            if (scale == 0.0f) { q[r * K + k] = 0; continue; }
+            float t = round_half_even(xr[k] / scale);
+            if (t > 7.0f) t = 7.0f;
+            if (t < -7.0f) t = -7.0f;
+            q[r * K + k] = (int8_t)t;
+        }
+    }
+}
+
+/* Two codes per byte: byte j of a row holds code 2j in bits 0-3 and code
+ * 2j+1 in bits 4-7, each as 4-bit two's complement. K is even. */
+void qvo_pack_w4(const int8_t* q, int64_t rows, int64_t K, uint8_t* packed)
+{
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t j = 0; j < K / 2; ++j) {
+            unsigned lo = (unsigned)(uint8_t)q[r * K + 2 * j] & 0xFu;
+            unsigned hi = (unsigned)(uint8_t)q[r * K + 2 * j + 1] & 0xFu;
+            packed[r * (K / 2) + j] = (uint8_t)(lo | (hi << 4));
+        }
+}
+
+static int8_t nibble_value(unsigned n)
+{
+    return (int8_t)(n >= 8u ? (int)n - 16 : (int)n);
+}
+
+void qvo_unpack_w4(const uint8_t* packed, int64_t rows, int64_t K, int8_t* q)
+{
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t j = 0; j < K / 2; ++j) {
+            unsigned byte = packed[r * (K / 2) + j];
+            q[r * K + 2 * j] = nibble_value(byte & 0xFu);
+            q[r * K + 2 * j + 1] = nibble_value(byte >> 4);
+        }
 }

@@ -51,22 +51,23 @@ def f32(v) -> Fraction:
     return Fraction(float(np.float32(v)))
 
 
-def quantize_row_exact(row_f32, mul=None):
-    """Per-row symmetric int8 quantization done with exact rationals plus one
+def quantize_row_exact(row_f32, mul=None, qmax=127):
+    """Per-row symmetric quantization done with exact rationals plus one
     explicit binary32 rounding per operation of the definition:
-    x' = fl(x*c), s = fl(amax/127), q = clamp(rne(fl(x'/s)), -127, 127)."""
+    x' = fl(x*c), s = fl(amax/qmax), q = clamp(rne(fl(x'/s)), -qmax, qmax)
+    (qmax = 127 for int8 codes, 7 for int4 ones)."""
     xs = [f32(v) for v in row_f32]
     if mul is not None:
         xs = [f32(round_to_f32(x * f32(c))) for x, c in zip(xs, mul)]
     amax = max(abs(x) for x in xs)
-    s = round_to_f32(amax / 127)
+    s = round_to_f32(amax / qmax)
     if s == 0:
         return [0] * len(xs), np.float32(0.0)
     sF = f32(s)
     q = []
     for x in xs:
         v = rne_int(f32(round_to_f32(x / sF)))
-        q.append(max(-127, min(127, v)))
+        q.append(max(-qmax, min(qmax, v)))
     return q, s
 
 

@@ -606,6 +606,99 @@ def _path(par, i):
         i = int(par[i])
     return out
 
+# ---------------------------------------------------------------------------
+# f4: W4A8
+# ---------------------------------------------------------------------------
+
+def pin_w4_worked_example(o):
+    """The hand-worked W4A8 example: codes, scales, packed bytes, integer
+    sums, outputs and the token."""
+    g = _golden("w4a8_worked_2x1x6.json")
+    w = (np.array(g["w_num"], dtype=np.float64) / np.array(g["w_den"], dtype=np.float64)[:, None]).astype(np.float32)
+    for bf16 in (False, True):
+        q, s = o.quantize_rows_w4(_bf16_bits(w) if bf16 else w, bf16=bf16)
+        assert q.tolist() == g["q"], (bf16, q)
+        assert s.tolist() == g["s"]
+    packed = o.pack_w4(np.array(g["q"], dtype=np.int8))
+    assert packed.tolist() == g["packed"]
+    assert o.unpack_w4(np.array(g["packed"], dtype=np.uint8)).tolist() == g["q"]
+    xq = np.array(g["xq"], dtype=np.int8)
+    sx = np.array(g["sx"], dtype=np.float32)
+    sw = np.array(g["s"], dtype=np.float32)
+    y, acc = o.w4a8_linear(xq, sx, packed, sw)
+    assert acc.tolist() == g["acc"]
+    assert np.array_equal(y, np.array(g["y_num_over_512"], dtype=np.float64) / 512)
+    tok, _ = o.w4a8_lm_head_argmax(xq, sx, packed, sw)
+    assert tok.tolist() == g["token"]
+
+
+def pin_w4_quantize_exact_rational(o):
+    """int4 codes and scales against exact rational arithmetic with one
+    binary32 rounding per operation (s = fl(amax/7), q = rne(fl(w/s)))."""
+    rng = np.random.default_rng(4321)
+    K = 64
+    rows = [rng.standard_normal(K).astype(np.float32),
+            (rng.standard_normal(K) * 1e-3).astype(np.float32),
+            (rng.standard_normal(K) * 3e4).astype(np.float32),
+            (rng.standard_normal(K) * 1e-38).astype(np.float32)]
+    # quotients within an ulp of a half-integer: division by s and
+    # multiplication by 7/amax disagree there
+    for _ in range(4):
+        amax = np.float32(rng.uniform(0.5, 4.0))
+        s = np.float32(amax / np.float32(7))
+        cand = rng.uniform(-amax, amax, size=200000).astype(np.float32)
+        hard = cand[np.rint(cand / s) != np.rint(cand * np.float32(np.float32(7) / amax))]
+        row = np.concatenate([[amax], hard[: K - 1]]).astype(np.float32)
+        row = np.concatenate([row, rng.uniform(-amax, amax, K - row.size).astype(np.float32)])
+        rows.append(row)
+    x = np.stack(rows)
+    q, s = o.quantize_rows_w4(x)
+    for i in range(x.shape[0]):
+        q_ref, s_ref = quantize_row_exact(x[i], qmax=7)
+        assert np.float32(s[i]) == s_ref, (i, s[i], s_ref)
+        assert q[i].tolist() == q_ref, i
+    assert int(np.abs(q).max()) <= 7
+
+
+def pin_w4_pack_roundtrip(o):
+    """Every pair of codes in [-8, 7] survives packing, every byte survives
+    unpacking, and a code's nibble sits where the format puts it: a lone
+    code at an even index lands in the low nibble of its byte."""
+    pairs = np.array([[a, b] for a in range(-8, 8) for b in range(-8, 8)], dtype=np.int8)
+    q = pairs.reshape(1, -1)
+    assert np.array_equal(o.unpack_w4(o.pack_w4(q)), q)
+    allb = np.arange(256, dtype=np.uint8).reshape(1, -1)
+    assert np.array_equal(o.pack_w4(o.unpack_w4(allb)), allb)
+    one = np.zeros((1, 8), dtype=np.int8)
+    one[0, 2] = 1          # code 2 -> byte 1, bits 0-3
+    assert o.pack_w4(one).tolist() == [[0, 1, 0, 0]]
+    one[0, 2], one[0, 5] = 0, -1   # code 5 -> byte 2, bits 4-7 = 0xF
+    assert o.pack_w4(one).tolist() == [[0, 0, 0xF0, 0]]
+
+
+def pin_w4_linear_bruteforce(o):
+    """W4A8 sums by Python integers over nibbles read off the packed bytes,
+    for small random shapes."""
+    rng = np.random.default_rng(77)
+    for M, K, N in ((1, 2, 1), (3, 6, 4), (2, 32, 5)):
+        xq = rng.integers(-127, 128, (M, K)).astype(np.int8)
+        packed = rng.integers(0, 256, (N, K // 2)).astype(np.uint8)
+        sx = rng.uniform(1e-3, 1e-1, M).astype(np.float32)
+        sw = rng.uniform(1e-3, 1e-1, N).astype(np.float32)
+        y, acc = o.w4a8_linear(xq, sx, packed, sw)
+        for m in range(M):
+            for n in range(N):
+                tot = 0
+                for j in range(K // 2):
+                    byte = int(packed[n, j])
+                    lo, hi = byte % 16, byte // 16
+                    lo = lo - 16 if lo > 7 else lo
+                    hi = hi - 16 if hi > 7 else hi
+                    tot += int(xq[m, 2 * j]) * lo + int(xq[m, 2 * j + 1]) * hi
+                assert int(acc[m, n]) == tot
+                assert y[m, n] == dequant_exact(tot, sx[m], sw[n])
+
+
 ALL_PINS = [
     pin_worked_example,
     pin_quantize_exact_rational,
@@ -629,4 +722,8 @@ ALL_PINS = [
     pin_spec_special_cases,
     pin_tree_chain_is_linear,
     pin_tree_bruteforce,
+    pin_w4_worked_example,
+    pin_w4_quantize_exact_rational,
+    pin_w4_pack_roundtrip,
+    pin_w4_linear_bruteforce,
 ]

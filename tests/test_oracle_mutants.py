@@ -61,6 +61,13 @@ MUTANTS = [
     ("tree_ties_last", "if (acc[i] && depth[i] > depth[best]) best = i;",
      "if (acc[i] && depth[i] >= depth[best]) best = i;"),
     ("tree_bonus_from_parent", "out[b * N + D] = tb[best];", "out[b * N + D] = tb[pb[best] >= 0 ? pb[best] : 0];"),
+    ("w4_scale_127", "float scale = amax / 7.0f;", "float scale = amax / 127.0f;"),
+    ("w4_truncate", "float t = round_half_even(xr[k] / scale);", "float t = truncf(xr[k] / scale);"),
+    ("w4_nibbles_swapped", "packed[r * (K / 2) + j] = (uint8_t)(lo | (hi << 4));",
+     "packed[r * (K / 2) + j] = (uint8_t)(hi | (lo << 4));"),
+    ("w4_unpack_unsigned", "return (int8_t)(n >= 8u ? (int)n - 16 : (int)n);", "return (int8_t)n;"),
+    ("w4_unpack_high_first", "q[r * K + 2 * j] = nibble_value(byte & 0xFu);",
+     "q[r * K + 2 * j] = nibble_value(byte >> 4);"),
     ("residual_not_added",
      "hr[k] = qvo_f32_to_bf16_rne(qvo_bf16_to_f32(hr[k]) + qvo_bf16_to_f32(d[m * H + k]));",
      "hr[k] = hr[k];"),
