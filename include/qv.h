@@ -384,6 +384,49 @@ QV_API qv_status qv_quantize_weight(const void* w, qv_dtype w_dtype, int N, int 
                              int8_t* wq, float* sw, cudaStream_t stream);
 
 /*
+ * W4A8 -- the lower-bit verifier: int4 weights against the int8 activation
+ * codes of qv_quantize_act.
+ *   Lower bit widths (4-bit, 2-bit) for the verifier are the next step the
+ *   Quasar summaries name (gist.science/it summary, conclusions;
+ *   gist.science/de summary, outlook; shd-paper.top, future work); INT4 is
+ *   among the widths the authors tried (paper-digest summary, key design).
+ *   The pages give no int4 format; the one here keeps a2's exact integer
+ *   accumulation and dequantization unchanged.
+ *
+ * qv_quantize_weight_w4 (setup): per-output-channel symmetric int4,
+ *   sw[n] = fl32(amax_n / 7), q = clamp(rne(fl32(w[n][k] / sw[n])), -7, 7),
+ *   q = 0 for a row whose scale is 0. Packed two codes per byte:
+ *   wq4[n*K/2 + j] = (q[n][2j] & 0xF) | (q[n][2j+1] & 0xF) << 4 (4-bit two's
+ *   complement; -8 is never produced).
+ *   w [N*K] fp32 or bf16 (16-byte aligned), wq4 [N*K/2] bytes out (16-byte
+ *   aligned), sw [N] fp32 out; K a multiple of 32 in [32, QV_MAX_K].
+ *
+ * qv_w4a8_linear, qv_w4a8_swiglu, qv_w4a8_lm_head_argmax: qv_w8a8_linear,
+ *   qv_w8a8_swiglu and qv_lm_head_argmax with packed int4 weights in place
+ *   of int8 ones; every other argument, the results, the workspace (sized by
+ *   qv_workspace_bytes with QV_OP_LINEAR / QV_OP_LM_HEAD, left zero-filled)
+ *   and the errors are theirs. acc[m][n] = sum_k xq[m][k] * q[n][k] exactly
+ *   (|acc| <= 127 * 7 * K), y = fl32(fl32((float)acc) * fl32(sx[m]*sw[n])).
+ *   K must be a multiple of 32 (QV_ERR_INVALID_ARG otherwise). For
+ *   qv_w4a8_swiglu the 2F packed rows are interleaved like qv_w8a8_swiglu's.
+ *   Up to 32 token rows run per launch; more rows take several launches.
+ */
+QV_API qv_status qv_quantize_weight_w4(const void* w, qv_dtype w_dtype, int N, int K,
+                                       uint8_t* wq4, float* sw, cudaStream_t stream);
+QV_API qv_status qv_w4a8_linear(const int8_t* xq, const float* sx, int M, int K,
+                                const uint8_t* wq4, const float* sw, int N,
+                                void* y, qv_dtype y_dtype, int32_t* acc_debug,
+                                void* workspace, size_t workspace_bytes, cudaStream_t stream);
+QV_API qv_status qv_w4a8_swiglu(const int8_t* xq, const float* sx, int M, int K,
+                                const uint8_t* wq4_gu, const float* sw_gu, int F, float* a,
+                                void* workspace, size_t workspace_bytes, cudaStream_t stream);
+QV_API qv_status qv_w4a8_lm_head_argmax(const int8_t* xq, const float* sx, int M, int K,
+                                        const uint8_t* wq4, const float* sw, int V,
+                                        int32_t* tokens, float* max_logit,
+                                        void* workspace, size_t workspace_bytes,
+                                        cudaStream_t stream);
+
+/*
  * qv_bf16_linear -- the high-precision verifier being replaced, as a traffic
  * comparator: y = x w^T with bf16 operands and fp32 accumulation.
  *   The verify pass "in full precision (BF16)" whose weight traffic the

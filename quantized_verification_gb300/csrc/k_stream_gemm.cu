@@ -86,10 +86,10 @@ __host__ __device__ constexpr int s8_pairs() { return NG == 1 ? QV_S8_PAIRS_NARR
 static_assert(kW8A8Warps == 4 || kW8A8Warps == 8, "4 or 8 consumer warps");
 static_assert(kBf16Warps == 4 || kBf16Warps == 8, "4 or 8 consumer warps");
 
-template <int NG>
+template <int NG, int XB = 1>
 struct Cfg {
     static constexpr int MP = 8 * NG;                        // padded tokens
-    static constexpr int XBytes = MP * BKB;                  // activation slice
+    static constexpr int XBytes = MP * BKB * XB;             // activation slice (XB boxes)
     static constexpr int XSlot = ((XBytes + 1023) / 1024) * 1024;
     static constexpr int StageBytes = kWTileBytes + XSlot;
     // Seven stages for up to 16 tokens also make a CTA need more than half of
@@ -136,6 +136,8 @@ struct Smem {
     }
     __device__ __forceinline__ uint8_t* w_tile(int s) { return stages + s * StageBytes; }
     __device__ __forceinline__ uint8_t* x_tile(int s) { return stages + s * StageBytes + kWTileBytes; }
+    // box j of the activation slice: MP rows x 128 bytes, 1024-byte aligned
+    __device__ __forceinline__ uint8_t* x_box(int s, int j) { return x_tile(s) + j * MP * BKB; }
 };
 
 
@@ -261,13 +263,63 @@ __device__ __forceinline__ void w8a8_tile_mma(uint32_t wb, uint32_t xb, const Ti
 }
 
 // ---------------------------------------------------------------------------
-// W8A8 kernel
+// W4A8 tile: 128 channels x 128 bytes of packed int4 codes (256 codes of K per
+// channel; byte j holds code 2j in its low nibble and 2j+1 in its high one)
+// against the activation tile, two 128-byte swizzled boxes of MP tokens x
+// 128 codes. The nibbles become int8 operands of the int8 m16n8k32 MMA
+// without a table: masking the high nibble in place gives 16 * code(2j+1),
+// shifting the low nibble up gives 16 * code(2j), both exact int8 values
+// (16 * [-7, 7]). Each thread's ldmatrix word of a 16-byte chunk holds codes
+// 32c + 8t .. 32c + 8t + 7 (t = lane % 4), so the MMA's K slots carry even
+// codes in its first half and odd codes in its second; the activation
+// operand is fetched in the same order (one 8-byte load of codes 8t .. 8t+7
+// per token, split into even and odd bytes), which leaves every dot product
+// unchanged. The sums are 16 times the true ones; the caller shifts them
+// back exactly (|sum| <= 16 * 7 * 127 * K < 2^31 for K <= 150975).
 // ---------------------------------------------------------------------------
-template <int NG, int EPI>
+template <int NG, int BPW, int MP>
+__device__ __forceinline__ void w4a8_tile_mma(uint32_t wb, uint32_t xb, const TileLanes<BPW>& L,
+                                              const uint32_t (&x_off)[4], int32_t (&acci)[BPW][NG][4]) {
+#pragma unroll
+    for (int P = 0; P < 4; ++P) {                 // packed chunks 2P, 2P+1: codes 64P .. 64P+63
+        uint32_t be[2][NG], bo[2][NG];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int c = 2 * P + h;
+#pragma unroll
+            for (int gr = 0; gr < NG; ++gr) {
+                uint32_t lo, hi;
+                lds_v2_u32(xb + (uint32_t)((c >> 2) * MP * BKB + 8 * gr * BKB) + x_off[c & 3], lo, hi);
+                be[h][gr] = __byte_perm(lo, hi, 0x6420);   // codes 8t, 8t+2, 8t+4, 8t+6
+                bo[h][gr] = __byte_perm(lo, hi, 0x7531);   // codes 8t+1, 8t+3, 8t+5, 8t+7
+            }
+        }
+#pragma unroll
+        for (int blk = 0; blk < BPW; ++blk) {
+            uint32_t r0, r1, r2, r3;     // rows g, g+8 of chunk 2P; rows g, g+8 of chunk 2P+1
+            ldmatrix_x4(wb + L.w_row_off[blk] + L.w_chunk_off[P], r0, r1, r2, r3);
+            const uint32_t e0 = (r0 << 4) & 0xF0F0F0F0u, o0 = r0 & 0xF0F0F0F0u;
+            const uint32_t e1 = (r1 << 4) & 0xF0F0F0F0u, o1 = r1 & 0xF0F0F0F0u;
+            const uint32_t e2 = (r2 << 4) & 0xF0F0F0F0u, o2 = r2 & 0xF0F0F0F0u;
+            const uint32_t e3 = (r3 << 4) & 0xF0F0F0F0u, o3 = r3 & 0xF0F0F0F0u;
+#pragma unroll
+            for (int gr = 0; gr < NG; ++gr) {
+                mma_s8_16832(acci[blk][gr], e0, e1, o0, o1, be[0][gr], bo[0][gr]);
+                mma_s8_16832(acci[blk][gr], e2, e3, o2, o3, be[1][gr], bo[1][gr]);
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// W8A8 kernel (W4 = 1: the W4A8 kernel, packed int4 weights, same pipeline
+// and epilogue)
+// ---------------------------------------------------------------------------
+template <int NG, int EPI, int W4>
 __global__ void __launch_bounds__((kW8A8Warps + 1) * 32, 1)
 w8a8_stream_kernel(const __grid_constant__ CUtensorMap tmap_w,
                    const __grid_constant__ CUtensorMap tmap_x, const W8A8Params p) {
-    using C = Cfg<NG>;
+    using C = Cfg<NG, W4 ? 2 : 1>;
     constexpr int MP = C::MP;
     constexpr int Stages = C::Stages;
     constexpr int CW = kW8A8Warps;
@@ -296,8 +348,8 @@ w8a8_stream_kernel(const __grid_constant__ CUtensorMap tmap_w,
 
     if (warp == CW) {
         if (lane == 0)
-            produce<Stages>(&g_stream_gemm_error, sm, &tmap_w, &tmap_x, a, b, p.KT, BKB,
-                            (unsigned)(kWTileBytes + C::XBytes));
+            produce<Stages, W4 ? 2 : 1>(&g_stream_gemm_error, sm, &tmap_w, &tmap_x, a, b, p.KT, BKB,
+                                        (unsigned)(kWTileBytes + C::XBytes));
         return;
     }
 
@@ -310,6 +362,11 @@ w8a8_stream_kernel(const __grid_constant__ CUtensorMap tmap_w,
 
     const int g = lane >> 2, t4 = lane & 3;
     const TileLanes<BPW> L(RW * warp, lane);
+    // W4: this lane's 8-byte activation word of each 32-code chunk of a box
+    uint32_t x_off[4];
+#pragma unroll
+    for (int cc = 0; cc < 4; ++cc)
+        x_off[cc] = (uint32_t)(g * BKB + ((((2 * cc) + (t4 >> 1)) ^ g) << 4) + ((t4 & 1) << 3));
 
     int32_t acci[BPW][NG][4];
     int s = 0, phase = 0;
@@ -329,21 +386,29 @@ w8a8_stream_kernel(const __grid_constant__ CUtensorMap tmap_w,
         for (; i < seg_end; ++i) {
             if (!mbar_wait_bounded(&sm.full[s], phase, sm.abort))
                 atomicOr(&g_stream_gemm_error, kErrFullWait);
-            w8a8_tile_mma<NG, BPW, S8P>(smem_u32(sm.w_tile(s)), smem_u32(sm.x_tile(s)), L, acci);
+            if constexpr (W4)
+                w4a8_tile_mma<NG, BPW, MP>(smem_u32(sm.w_tile(s)), smem_u32(sm.x_tile(s)), L, x_off, acci);
+            else
+                w8a8_tile_mma<NG, BPW, S8P>(smem_u32(sm.w_tile(s)), smem_u32(sm.x_tile(s)), L, acci);
             __syncwarp();
             if (lane == 0) mbar_arrive(&sm.empty[s]);
             if (++s == Stages) { s = 0; phase ^= 1; }
         }
 
         // -------- segment end: stage the int32 sums [row][token] --------
+        // (W4: the sums are 16 times the true ones, multiples of 16, so the
+        // arithmetic shift is exact)
+        constexpr int SH = W4 ? 4 : 0;
 #pragma unroll
         for (int blk = 0; blk < BPW; ++blk) {
             const int r0 = RW * warp + 16 * blk + g;
 #pragma unroll
             for (int gr = 0; gr < NG; ++gr) {
                 const int col = 8 * gr + 2 * t4;
-                *reinterpret_cast<int2*>(&sm.stg[r0 * MP + col]) = make_int2(acci[blk][gr][0], acci[blk][gr][1]);
-                *reinterpret_cast<int2*>(&sm.stg[(r0 + 8) * MP + col]) = make_int2(acci[blk][gr][2], acci[blk][gr][3]);
+                *reinterpret_cast<int2*>(&sm.stg[r0 * MP + col]) =
+                    make_int2(acci[blk][gr][0] >> SH, acci[blk][gr][1] >> SH);
+                *reinterpret_cast<int2*>(&sm.stg[(r0 + 8) * MP + col]) =
+                    make_int2(acci[blk][gr][2] >> SH, acci[blk][gr][3] >> SH);
             }
         }
         consumer_sync<CW>();
@@ -1133,7 +1198,7 @@ cudaError_t launch_w8a8_stream(const W8A8Launch& a, int num_sms, cudaStream_t s)
     WsLayout L = ws_layout(a.MP, a.N, lm);
     W8A8Params p;
     p.M = a.M; p.N = a.N; p.K = a.K;
-    p.KT = ceil_div(a.K, BKB);
+    p.KT = ceil_div(a.w4 ? a.K / 2 : a.K, BKB);   // weight bytes of K per tile row
     p.NT = ceil_div(a.N, BN);
     p.T = (long long)p.KT * p.NT;
     p.sx = a.sx; p.sw = a.sw; p.y = a.y; p.y_bf16 = a.y_bf16; p.acc_debug = a.acc_debug;
@@ -1143,14 +1208,16 @@ cudaError_t launch_w8a8_stream(const W8A8Launch& a, int num_sms, cudaStream_t s)
     p.keys = reinterpret_cast<unsigned long long*>(ws + L.keys);
     p.done = reinterpret_cast<unsigned*>(ws + L.done);
     const int grid = stream_grid(p.T, num_sms);
-#define QV_W8A8_LAUNCH(NGV, EPIV)                                                            \
-    launch_ex(w8a8_stream_kernel<NGV, (int)EPIV>, grid, (kW8A8Warps + 1) * 32,               \
-              Cfg<NGV>::SmemBytes, s, a.tmap_w, a.tmap_x, p)
+#define QV_W8A8_LAUNCH(NGV, EPIV, W4V)                                                       \
+    launch_ex(w8a8_stream_kernel<NGV, (int)EPIV, W4V>, grid, (kW8A8Warps + 1) * 32,          \
+              Cfg<NGV, W4V ? 2 : 1>::SmemBytes, s, a.tmap_w, a.tmap_x, p)
+#define QV_W8A8_EPI(NGV, W4V)                                                                \
+        (lm ? QV_W8A8_LAUNCH(NGV, Epi::LmHead, W4V)                                          \
+            : a.epi == Epi::SwiGLU ? QV_W8A8_LAUNCH(NGV, Epi::SwiGLU, W4V)                   \
+                                   : QV_W8A8_LAUNCH(NGV, Epi::Linear, W4V))
 #define QV_W8A8_CASE(NGV)                                                                    \
     case NGV:                                                                                \
-        return lm ? QV_W8A8_LAUNCH(NGV, Epi::LmHead)                                         \
-                  : a.epi == Epi::SwiGLU ? QV_W8A8_LAUNCH(NGV, Epi::SwiGLU)                  \
-                                         : QV_W8A8_LAUNCH(NGV, Epi::Linear);
+        return a.w4 ? QV_W8A8_EPI(NGV, 1) : QV_W8A8_EPI(NGV, 0);
     switch (a.MP / 8) {   // up to 32 tokens; more go to the tcgen05 kernel
         QV_W8A8_CASE(1)
         QV_W8A8_CASE(2)
@@ -1158,6 +1225,7 @@ cudaError_t launch_w8a8_stream(const W8A8Launch& a, int num_sms, cudaStream_t s)
         default: return cudaErrorInvalidValue;
     }
 #undef QV_W8A8_CASE
+#undef QV_W8A8_EPI
 #undef QV_W8A8_LAUNCH
 }
 

@@ -127,6 +127,7 @@ struct TcSmem {
     }
     __device__ __forceinline__ uint8_t* w_tile(int s) { return stages + s * C::StageBytes; }
     __device__ __forceinline__ uint8_t* x_tile(int s) { return stages + s * C::StageBytes + kWTileBytes; }
+    __device__ __forceinline__ uint8_t* x_box(int s, int j) { return x_tile(s) + j * MP * BKB; }
     __device__ __forceinline__ uint8_t* b_slot(int j) { return bring + j * C::BSlot; }
 };
 

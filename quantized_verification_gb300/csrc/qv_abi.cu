@@ -119,6 +119,7 @@ qv_status encode_2d(CUtensorMap* map, CUtensorMapDataType dt, size_t elem_bytes,
 // accumulators), whose per-tile cost hardly grows with the token count, takes
 // over (measured on GB300).
 cudaError_t launch_w8a8(const qv::W8A8Launch& L, int sms, cudaStream_t s) {
+    if (L.w4 && L.MP > qv::kMaxMPerLaunchW4) return cudaErrorInvalidValue;
     if (L.MP >= 64) return qv::launch_w8a8_tc(L, sms, s);
     return qv::launch_w8a8_stream(L, sms, s);
 }
@@ -162,6 +163,66 @@ size_t al16(size_t v) { return (v + 15) & ~size_t(15); }
 size_t act_codes_offset(bool lm, int M, int K, int N) {
     const int mp = mp_for(M < qv::kMaxMPerLaunch ? M : qv::kMaxMPerLaunch);
     return (qv::ws_layout(mp, N, lm).total + 255) & ~size_t(255);
+}
+
+// One streaming GEMM call (W8A8 or W4A8) over all token rows: the weight
+// tensor map once, then one launch per slice of at most kMaxMPerLaunch rows
+// (kMaxMPerLaunchW4 for packed int4 weights).
+struct GemmCall {
+    bool w4;
+    qv::Epi epi;
+    const int8_t* xq;
+    const float* sx;
+    int M, K;
+    const void* wq;
+    const float* sw;
+    int N;
+    uint8_t* y;            // Linear / SwiGLU output, row pitch y_row_bytes
+    size_t y_row_bytes;
+    int y_bf16;
+    int32_t* acc_debug;
+    int32_t* tokens;       // LmHead
+    float* max_logit;
+    void* ws;
+};
+
+qv_status run_gemm(const GemmCall& c, const char* what, cudaStream_t stream) {
+    cudaError_t e;
+    const int sms = sms_of_current_device(&e);
+    if (e != cudaSuccess) return cuda_fail(e, "device query");
+    qv::W8A8Launch L = {};
+    qv_status st;
+    const uint64_t w_inner = c.w4 ? (uint64_t)c.K / 2 : (uint64_t)c.K;   // weight bytes per row
+    if ((st = encode_2d(&L.tmap_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, c.wq, w_inner, (uint64_t)c.N,
+                        qv::kTileKBytes, qv::kTileN)) != QV_OK)
+        return st;
+    const int step = c.w4 ? qv::kMaxMPerLaunchW4 : qv::kMaxMPerLaunch;
+    for (int m0 = 0; m0 < c.M; m0 += step) {
+        const int mc = c.M - m0 < step ? c.M - m0 : step;
+        L.M = mc; L.N = c.N; L.K = c.K; L.MP = mp_for(mc);
+        if ((st = encode_2d(&L.tmap_x, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, c.xq + (size_t)m0 * c.K,
+                            (uint64_t)c.K, (uint64_t)mc, qv::kTileKBytes, (uint32_t)L.MP)) != QV_OK)
+            return st;
+        L.sx = c.sx + m0; L.sw = c.sw;
+        L.y = c.y ? c.y + (size_t)m0 * c.y_row_bytes : nullptr;
+        L.y_bf16 = c.y_bf16;
+        L.acc_debug = c.acc_debug ? c.acc_debug + (size_t)m0 * c.N : nullptr;
+        L.tokens = c.tokens ? c.tokens + m0 : nullptr;
+        L.max_logit = c.max_logit ? c.max_logit + m0 : nullptr;
+        L.ws = c.ws;
+        L.epi = c.epi;
+        L.w4 = c.w4 ? 1 : 0;
+        e = launch_w8a8(L, sms, stream);
+        if (e != cudaSuccess) return cuda_fail(e, what);
+    }
+    return ok();
+}
+
+qv_status check_k_w4(int K) {
+    if (K < 32 || K % 32 != 0 || K > QV_MAX_K)
+        return fail(QV_ERR_INVALID_ARG, "K=%d must be a positive multiple of 32 and <= %d for int4 weights", K,
+                    QV_MAX_K);
+    return QV_OK;
 }
 
 }  // namespace
@@ -250,31 +311,10 @@ qv_status qv_w8a8_linear(const int8_t* xq, const float* sx, int M, int K, const 
         return fail(QV_ERR_INVALID_ARG, "y/acc_debug misaligned");
     QV_CHECK_DEV(y);
     QV_CHECK_DEV(acc_debug);
-    cudaError_t e;
-    const int sms = sms_of_current_device(&e);
-    if (e != cudaSuccess) return cuda_fail(e, "device query");
-    qv::W8A8Launch L = {};
-    if ((st = encode_2d(&L.tmap_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, wq, (uint64_t)K, (uint64_t)N,
-                        qv::kTileKBytes, qv::kTileN)) != QV_OK)
-        return st;
     const size_t ybytes = y_dtype == QV_F32 ? 4 : 2;
-    for (int m0 = 0; m0 < M; m0 += qv::kMaxMPerLaunch) {
-        const int mc = M - m0 < qv::kMaxMPerLaunch ? M - m0 : qv::kMaxMPerLaunch;
-        L.M = mc; L.N = N; L.K = K; L.MP = mp_for(mc);
-        if ((st = encode_2d(&L.tmap_x, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, xq + (size_t)m0 * K,
-                            (uint64_t)K, (uint64_t)mc, qv::kTileKBytes, (uint32_t)L.MP)) != QV_OK)
-            return st;
-        L.sx = sx + m0; L.sw = sw;
-        L.y = static_cast<uint8_t*>(y) + (size_t)m0 * N * ybytes;
-        L.y_bf16 = y_dtype == QV_BF16;
-        L.acc_debug = acc_debug ? acc_debug + (size_t)m0 * N : nullptr;
-        L.tokens = nullptr; L.max_logit = nullptr;
-        L.ws = workspace;
-        L.epi = qv::Epi::Linear;
-        e = launch_w8a8(L, sms, stream);
-        if (e != cudaSuccess) return cuda_fail(e, "qv_w8a8_linear launch");
-    }
-    return ok();
+    const GemmCall c = {false, qv::Epi::Linear, xq, sx, M, K, wq, sw, N, static_cast<uint8_t*>(y),
+                        (size_t)N * ybytes, y_dtype == QV_BF16, acc_debug, nullptr, nullptr, workspace};
+    return run_gemm(c, "qv_w8a8_linear launch", stream);
 }
 
 qv_status qv_w8a8_swiglu(const int8_t* xq, const float* sx, int M, int K, const int8_t* wq_gu,
@@ -286,30 +326,9 @@ qv_status qv_w8a8_swiglu(const int8_t* xq, const float* sx, int M, int K, const 
     if (!a) return fail(QV_ERR_INVALID_ARG, "a is null");
     if (!aligned(a, 4)) return fail(QV_ERR_INVALID_ARG, "a misaligned");
     QV_CHECK_DEV(a);
-    cudaError_t e;
-    const int sms = sms_of_current_device(&e);
-    if (e != cudaSuccess) return cuda_fail(e, "device query");
-    qv::W8A8Launch L = {};
-    if ((st = encode_2d(&L.tmap_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, wq_gu, (uint64_t)K, (uint64_t)(2 * F),
-                        qv::kTileKBytes, qv::kTileN)) != QV_OK)
-        return st;
-    for (int m0 = 0; m0 < M; m0 += qv::kMaxMPerLaunch) {
-        const int mc = M - m0 < qv::kMaxMPerLaunch ? M - m0 : qv::kMaxMPerLaunch;
-        L.M = mc; L.N = 2 * F; L.K = K; L.MP = mp_for(mc);
-        if ((st = encode_2d(&L.tmap_x, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, xq + (size_t)m0 * K,
-                            (uint64_t)K, (uint64_t)mc, qv::kTileKBytes, (uint32_t)L.MP)) != QV_OK)
-            return st;
-        L.sx = sx + m0; L.sw = sw_gu;
-        L.y = a + (size_t)m0 * F;
-        L.y_bf16 = 0;
-        L.acc_debug = nullptr;
-        L.tokens = nullptr; L.max_logit = nullptr;
-        L.ws = workspace;
-        L.epi = qv::Epi::SwiGLU;
-        e = launch_w8a8(L, sms, stream);
-        if (e != cudaSuccess) return cuda_fail(e, "qv_w8a8_swiglu launch");
-    }
-    return ok();
+    const GemmCall c = {false, qv::Epi::SwiGLU, xq, sx, M, K, wq_gu, sw_gu, 2 * F,
+                        reinterpret_cast<uint8_t*>(a), (size_t)F * 4, 0, nullptr, nullptr, nullptr, workspace};
+    return run_gemm(c, "qv_w8a8_swiglu launch", stream);
 }
 
 qv_status qv_lm_head_argmax(const int8_t* xq, const float* sx, int M, int K, const int8_t* wq,
@@ -322,29 +341,78 @@ qv_status qv_lm_head_argmax(const int8_t* xq, const float* sx, int M, int K, con
         return fail(QV_ERR_INVALID_ARG, "tokens/max_logit misaligned");
     QV_CHECK_DEV(tokens);
     QV_CHECK_DEV(max_logit);
-    cudaError_t e;
-    const int sms = sms_of_current_device(&e);
-    if (e != cudaSuccess) return cuda_fail(e, "device query");
-    qv::W8A8Launch L = {};
-    if ((st = encode_2d(&L.tmap_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, wq, (uint64_t)K, (uint64_t)V,
-                        qv::kTileKBytes, qv::kTileN)) != QV_OK)
-        return st;
-    for (int m0 = 0; m0 < M; m0 += qv::kMaxMPerLaunch) {
-        const int mc = M - m0 < qv::kMaxMPerLaunch ? M - m0 : qv::kMaxMPerLaunch;
-        L.M = mc; L.N = V; L.K = K; L.MP = mp_for(mc);
-        if ((st = encode_2d(&L.tmap_x, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, xq + (size_t)m0 * K,
-                            (uint64_t)K, (uint64_t)mc, qv::kTileKBytes, (uint32_t)L.MP)) != QV_OK)
-            return st;
-        L.sx = sx + m0; L.sw = sw;
-        L.y = nullptr; L.y_bf16 = 0; L.acc_debug = nullptr;
-        L.tokens = tokens + m0;
-        L.max_logit = max_logit ? max_logit + m0 : nullptr;
-        L.ws = workspace;
-        L.epi = qv::Epi::LmHead;
-        e = launch_w8a8(L, sms, stream);
-        if (e != cudaSuccess) return cuda_fail(e, "qv_lm_head_argmax launch");
-    }
+    const GemmCall c = {false, qv::Epi::LmHead, xq, sx, M, K, wq, sw, V, nullptr, 0, 0, nullptr,
+                        tokens, max_logit, workspace};
+    return run_gemm(c, "qv_lm_head_argmax launch", stream);
+}
+
+qv_status qv_quantize_weight_w4(const void* w, qv_dtype w_dtype, int N, int K, uint8_t* wq4, float* sw,
+                                cudaStream_t stream) {
+    if (!w || !wq4 || !sw) return fail(QV_ERR_INVALID_ARG, "null pointer");
+    if (w_dtype != QV_F32 && w_dtype != QV_BF16) return fail(QV_ERR_INVALID_ARG, "w_dtype must be QV_F32 or QV_BF16");
+    if (N < 1) return fail(QV_ERR_INVALID_ARG, "N=%d must be >= 1", N);
+    qv_status st = check_k_w4(K);
+    if (st != QV_OK) return st;
+    if (!aligned(w, 16) || !aligned(wq4, 16)) return fail(QV_ERR_INVALID_ARG, "w and wq4 must be 16-byte aligned");
+    if (!aligned(sw, 4)) return fail(QV_ERR_INVALID_ARG, "sw must be 4-byte aligned");
+    QV_CHECK_DEV(w);
+    QV_CHECK_DEV(wq4);
+    QV_CHECK_DEV(sw);
+    cudaError_t e = qv::launch_quantize_weight_w4(w, w_dtype == QV_BF16, N, K, wq4, sw, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "qv_quantize_weight_w4 launch");
     return ok();
+}
+
+qv_status qv_w4a8_linear(const int8_t* xq, const float* sx, int M, int K, const uint8_t* wq4,
+                         const float* sw, int N, void* y, qv_dtype y_dtype, int32_t* acc_debug,
+                         void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    qv_status st = check_k_w4(K);
+    if (st != QV_OK) return st;
+    if ((st = check_gemm_common(xq, sx, M, K, wq4, sw, N, workspace, workspace_bytes, QV_OP_LINEAR)) != QV_OK)
+        return st;
+    if (!y) return fail(QV_ERR_INVALID_ARG, "y is null");
+    if (y_dtype != QV_F32 && y_dtype != QV_BF16) return fail(QV_ERR_INVALID_ARG, "y_dtype must be QV_F32 or QV_BF16");
+    if (!aligned(y, y_dtype == QV_F32 ? 4 : 2) || (acc_debug && !aligned(acc_debug, 4)))
+        return fail(QV_ERR_INVALID_ARG, "y/acc_debug misaligned");
+    QV_CHECK_DEV(y);
+    QV_CHECK_DEV(acc_debug);
+    const size_t ybytes = y_dtype == QV_F32 ? 4 : 2;
+    const GemmCall c = {true, qv::Epi::Linear, xq, sx, M, K, wq4, sw, N, static_cast<uint8_t*>(y),
+                        (size_t)N * ybytes, y_dtype == QV_BF16, acc_debug, nullptr, nullptr, workspace};
+    return run_gemm(c, "qv_w4a8_linear launch", stream);
+}
+
+qv_status qv_w4a8_swiglu(const int8_t* xq, const float* sx, int M, int K, const uint8_t* wq4_gu,
+                         const float* sw_gu, int F, float* a, void* workspace, size_t workspace_bytes,
+                         cudaStream_t stream) {
+    if (F < 64 || F % 64 != 0) return fail(QV_ERR_INVALID_ARG, "F=%d must be a positive multiple of 64", F);
+    qv_status st = check_k_w4(K);
+    if (st != QV_OK) return st;
+    if ((st = check_gemm_common(xq, sx, M, K, wq4_gu, sw_gu, 2 * F, workspace, workspace_bytes, QV_OP_LINEAR)) != QV_OK)
+        return st;
+    if (!a) return fail(QV_ERR_INVALID_ARG, "a is null");
+    if (!aligned(a, 4)) return fail(QV_ERR_INVALID_ARG, "a misaligned");
+    QV_CHECK_DEV(a);
+    const GemmCall c = {true, qv::Epi::SwiGLU, xq, sx, M, K, wq4_gu, sw_gu, 2 * F,
+                        reinterpret_cast<uint8_t*>(a), (size_t)F * 4, 0, nullptr, nullptr, nullptr, workspace};
+    return run_gemm(c, "qv_w4a8_swiglu launch", stream);
+}
+
+qv_status qv_w4a8_lm_head_argmax(const int8_t* xq, const float* sx, int M, int K, const uint8_t* wq4,
+                                 const float* sw, int V, int32_t* tokens, float* max_logit,
+                                 void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    qv_status st = check_k_w4(K);
+    if (st != QV_OK) return st;
+    if ((st = check_gemm_common(xq, sx, M, K, wq4, sw, V, workspace, workspace_bytes, QV_OP_LM_HEAD)) != QV_OK)
+        return st;
+    if (!tokens) return fail(QV_ERR_INVALID_ARG, "tokens is null");
+    if (!aligned(tokens, 4) || (max_logit && !aligned(max_logit, 4)))
+        return fail(QV_ERR_INVALID_ARG, "tokens/max_logit misaligned");
+    QV_CHECK_DEV(tokens);
+    QV_CHECK_DEV(max_logit);
+    const GemmCall c = {true, qv::Epi::LmHead, xq, sx, M, K, wq4, sw, V, nullptr, 0, 0, nullptr,
+                        tokens, max_logit, workspace};
+    return run_gemm(c, "qv_w4a8_lm_head_argmax launch", stream);
 }
 
 namespace {

@@ -56,6 +56,7 @@ struct W8A8Launch {
     float* max_logit;         // LmHead: [M] or null
     void* ws;
     Epi epi;
+    int w4;                   // 1: packed int4 weights [N rows][K/2 bytes] (streaming kernel only)
 };
 
 struct Bf16Launch {
@@ -116,6 +117,14 @@ cudaError_t launch_bf16_stream(const Bf16Launch& a, int num_sms, cudaStream_t s)
 // Greedy tree verification (k_tree.cu), N <= 1024 nodes per tree.
 cudaError_t launch_tree_accept(const int32_t* t, const int32_t* d, const int32_t* par, int B, int N,
                                int32_t* len, int32_t* out, int32_t* node, cudaStream_t s);
+
+// int4 weight quantization for the W4A8 verifier (k_w4.cu): [N][K] fp32 or
+// bf16 -> packed [N][K/2] bytes + [N] scales.
+cudaError_t launch_quantize_weight_w4(const void* w, bool bf16, int N, int K, uint8_t* wq4, float* sw,
+                                      cudaStream_t s);
+// Packed int4 weights go through the streaming kernel only: at most 32 token
+// rows per launch.
+constexpr int kMaxMPerLaunchW4 = 32;
 
 // Speculative sampling at T > 0 (k_spec.cu): per-chunk maxima and sums, row
 // statistics and the decisions for M rows of V tokens (every call rewrites

@@ -166,6 +166,11 @@ __device__ __forceinline__ void allow_dependent_launch() {
 }
 
 // ---------------------------------------------------------------- warp MMA
+// Two consecutive 32-bit words of shared memory (8-byte aligned address).
+__device__ __forceinline__ void lds_v2_u32(uint32_t addr, uint32_t& r0, uint32_t& r1) {
+    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(addr));
+}
+
 __device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& r0, uint32_t& r1,
                                             uint32_t& r2, uint32_t& r3) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"

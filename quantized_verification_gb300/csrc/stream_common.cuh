@@ -51,7 +51,10 @@ __device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long v)
 // Producer: stream tiles [a, b) into the ring. Weight tiles of the first
 // ring fill are requested before the grid dependency wait. With tx == null
 // only weight tiles travel (tx_bytes must then count the weight tile alone).
-template <int Stages, class SM>
+// Each weight tile travels with XB activation boxes: box j of tile kt starts
+// at element (kt * XB + j) * kx_elems_per_tile of K (XB = 2 when a weight
+// tile's 128 bytes hold 256 int4 codes of K).
+template <int Stages, int XB = 1, class SM>
 __device__ __forceinline__ void produce(unsigned* err, SM& sm, const CUtensorMap* tw, const CUtensorMap* tx,
                                         int a, int b, int KT, int kx_elems_per_tile,
                                         unsigned tx_bytes) {
@@ -70,7 +73,9 @@ __device__ __forceinline__ void produce(unsigned* err, SM& sm, const CUtensorMap
     if (tx) {
         for (int j = 0; j < pre; ++j) {
             const int tile = a + j, kt = tile % KT;
-            tma_load_2d(sm.x_tile(j), tx, kt * kx_elems_per_tile, 0, &sm.full[j], pol_x);
+#pragma unroll
+            for (int xb = 0; xb < XB; ++xb)
+                tma_load_2d(sm.x_box(j, xb), tx, (kt * XB + xb) * kx_elems_per_tile, 0, &sm.full[j], pol_x);
         }
     }
     int issued = pre;
@@ -84,7 +89,11 @@ __device__ __forceinline__ void produce(unsigned* err, SM& sm, const CUtensorMap
         const int tile = a + j, nt = tile / KT, kt = tile - nt * KT;
         mbar_arrive_expect_tx(&sm.full[s], tx_bytes);
         tma_load_2d(sm.w_tile(s), tw, kt * kx_elems_per_tile, nt * BN, &sm.full[s], pol_w);
-        if (tx) tma_load_2d(sm.x_tile(s), tx, kt * kx_elems_per_tile, 0, &sm.full[s], pol_x);
+        if (tx) {
+#pragma unroll
+            for (int xb = 0; xb < XB; ++xb)
+                tma_load_2d(sm.x_box(s, xb), tx, (kt * XB + xb) * kx_elems_per_tile, 0, &sm.full[s], pol_x);
+        }
         ++issued;
         if (++s == Stages) { s = 0; ++round; }
     }

@@ -29,7 +29,8 @@ EXPORTS = ("qv_quantize_act", "qv_w8a8_linear", "qv_lm_head_argmax", "qv_accept"
            "qv_last_error", "qv_device_error", "qv_num_sms", "qv_w8a8_linear_noalloc",
            "qv_verify_stack", "qv_w8a8_linear_act", "qv_lm_head_argmax_act",
            "qv_rmsnorm_quant", "qv_swiglu_quant", "qv_w8a8_swiglu", "qv_spec_sample",
-           "qv_tree_accept")
+           "qv_tree_accept", "qv_quantize_weight_w4", "qv_w4a8_linear", "qv_w4a8_swiglu",
+           "qv_w4a8_lm_head_argmax")
 MAX_STACK_M = 16
 
 
@@ -79,6 +80,10 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         L.qv_w8a8_swiglu.argtypes = [P, P, I, I, P, P, I, P, P, S, P]
         L.qv_spec_sample.argtypes = [P, P, P, I, I, I, ctypes.c_float, ctypes.c_uint64, P, P, P, S, P]
         L.qv_tree_accept.argtypes = [P, P, P, I, I, P, P, P, P]
+        L.qv_quantize_weight_w4.argtypes = [P, I, I, I, P, P, P]
+        L.qv_w4a8_linear.argtypes = [P, P, I, I, P, P, I, P, I, P, P, S, P]
+        L.qv_w4a8_swiglu.argtypes = [P, P, I, I, P, P, I, P, P, S, P]
+        L.qv_w4a8_lm_head_argmax.argtypes = [P, P, I, I, P, P, I, P, P, P, S, P]
         L.qv_workspace_bytes.argtypes = [I, I, I, I]
         L.qv_workspace_bytes.restype = S
         L.qv_last_error.argtypes = []
@@ -283,6 +288,61 @@ def qv_lm_head_argmax(xq, sx, wq, sw, tokens, workspace, max_logit=None, stream=
                                     _ptr(max_logit), _ptr(workspace), workspace.numel(),
                                     ctypes.c_void_p(_stream(stream))))
 
+
+# --- W4A8: packed int4 weights [N, K/2] uint8 (even k in the low nibble) ---
+def qv_quantize_weight_w4(w, wq4, sw, stream=None):
+    """w [N, K] fp32/bf16 -> wq4 [N, K/2] uint8 (two int4 codes per byte), sw [N] fp32."""
+    N, K = w.shape
+    _need(K % 2 == 0 and wq4.shape == (N, K // 2) and wq4.dtype == torch.uint8, "wq4 must be uint8 [N, K/2]")
+    _need(sw.shape == (N,) and sw.dtype == torch.float32, "sw must be float32 [N]")
+    _check(load().qv_quantize_weight_w4(_ptr(w), _dtype(w), N, K, _ptr(wq4), _ptr(sw),
+                                        ctypes.c_void_p(_stream(stream))))
+
+
+def _w4_shapes(xq, wq4):
+    M, K = xq.shape
+    N = wq4.shape[0]
+    _need(xq.dtype == torch.int8, "xq must be int8 [M, K]")
+    _need(wq4.dtype == torch.uint8 and wq4.shape == (N, K // 2) and K % 2 == 0, "wq4 must be uint8 [N, K/2]")
+    return M, K, N
+
+
+def qv_w4a8_linear(xq, sx, wq4, sw, y, workspace, acc_debug=None, stream=None):
+    """y [M, N] (fp32 or bf16) = dequant(xq q^T), q the int4 codes of wq4."""
+    M, K, N = _w4_shapes(xq, wq4)
+    _need(sx.shape == (M,) and sw.shape == (N,), "sx [M], sw [N]")
+    _need(sx.dtype == torch.float32 and sw.dtype == torch.float32, "scales must be float32")
+    _need(y.shape == (M, N), "y must be [M, N]")
+    if acc_debug is not None:
+        _need(acc_debug.shape == (M, N) and acc_debug.dtype == torch.int32, "acc_debug int32 [M, N]")
+    _need(workspace.dtype == torch.uint8, "workspace must be a uint8 tensor")
+    _check(load().qv_w4a8_linear(_ptr(xq), _ptr(sx), M, K, _ptr(wq4), _ptr(sw), N, _ptr(y),
+                                 _dtype(y), _ptr(acc_debug), _ptr(workspace), workspace.numel(),
+                                 ctypes.c_void_p(_stream(stream))))
+
+
+def qv_w4a8_swiglu(xq, sx, wq4_gu, sw_gu, a, workspace, stream=None):
+    """a [M, F] fp32 = silu(y_gate) * y_up of the interleaved int4 gate|up linear."""
+    M, K, F2 = _w4_shapes(xq, wq4_gu)
+    F = F2 // 2
+    _need(sx.shape == (M,) and sw_gu.shape == (F2,), "sx [M], sw_gu [2F]")
+    _need(a.shape == (M, F) and a.dtype == torch.float32, "a must be float32 [M, F]")
+    _need(workspace.dtype == torch.uint8, "workspace must be a uint8 tensor")
+    _check(load().qv_w4a8_swiglu(_ptr(xq), _ptr(sx), M, K, _ptr(wq4_gu), _ptr(sw_gu), F, _ptr(a),
+                                 _ptr(workspace), workspace.numel(), ctypes.c_void_p(_stream(stream))))
+
+
+def qv_w4a8_lm_head_argmax(xq, sx, wq4, sw, tokens, workspace, max_logit=None, stream=None):
+    """tokens [M] int32 = greedy argmax over the W4A8 LM-head logits."""
+    M, K, V = _w4_shapes(xq, wq4)
+    _need(sx.shape == (M,) and sw.shape == (V,), "sx [M], sw [V]")
+    _need(tokens.shape == (M,) and tokens.dtype == torch.int32, "tokens int32 [M]")
+    if max_logit is not None:
+        _need(max_logit.shape == (M,) and max_logit.dtype == torch.float32, "max_logit float32 [M]")
+    _need(workspace.dtype == torch.uint8, "workspace must be a uint8 tensor")
+    _check(load().qv_w4a8_lm_head_argmax(_ptr(xq), _ptr(sx), M, K, _ptr(wq4), _ptr(sw), V, _ptr(tokens),
+                                         _ptr(max_logit), _ptr(workspace), workspace.numel(),
+                                         ctypes.c_void_p(_stream(stream))))
 
 
 def qv_w8a8_linear_act(x, wq, sw, y, workspace, act_mul=None, stream=None):

@@ -92,6 +92,18 @@ def test_host_validation_without_gpu(lib):
     assert lib.qv_lm_head_argmax_act(fake, 1, None, 5, 256, fake, fake, 8, None, None, fake, 1 << 20, None) == qv.QV_ERR_INVALID_ARG
     assert b"tokens" in lib.qv_last_error()
     assert lib.qv_lm_head_argmax_act(fake, 1, None, 5, 250, fake, fake, 8, fake, None, fake, 1 << 20, None) == qv.QV_ERR_INVALID_ARG
+    # W4A8: K must be a multiple of 32 (two codes per byte, 16-byte rows)
+    assert lib.qv_w4a8_linear(fake, fake, 4, 272, fake, fake, 8, fake, 0, None, fake, 1 << 22, None) == qv.QV_ERR_INVALID_ARG
+    assert b"multiple of 32" in lib.qv_last_error()
+    assert lib.qv_w4a8_linear(fake, fake, 4, 256, fake, fake, 8, None, 0, None, fake, 1 << 22, None) == qv.QV_ERR_INVALID_ARG
+    assert lib.qv_w4a8_linear(fake, fake, 4, 256, fake, fake, 8, fake, 0, None, fake, 16, None) == qv.QV_ERR_WORKSPACE
+    assert lib.qv_w4a8_linear(fake, fake, 4, 133152, fake, fake, 8, fake, 0, None, fake, 1 << 22, None) == qv.QV_ERR_INVALID_ARG
+    assert lib.qv_w4a8_swiglu(fake, fake, 4, 256, fake, fake, 96, fake, fake, 1 << 22, None) == qv.QV_ERR_INVALID_ARG
+    assert lib.qv_w4a8_lm_head_argmax(fake, fake, 4, 256, fake, fake, 8, None, None, fake, 1 << 22, None) == qv.QV_ERR_INVALID_ARG
+    assert lib.qv_w4a8_lm_head_argmax(fake, fake, 4, 16, fake, fake, 8, fake, None, fake, 1 << 22, None) == qv.QV_ERR_INVALID_ARG
+    assert lib.qv_quantize_weight_w4(fake, 0, 8, 48, fake, fake, None) == qv.QV_ERR_INVALID_ARG
+    assert lib.qv_quantize_weight_w4(fake, 5, 8, 64, fake, fake, None) == qv.QV_ERR_INVALID_ARG
+    assert lib.qv_quantize_weight_w4(fake, 0, 8, 64, P(0x1008), fake, None) == qv.QV_ERR_INVALID_ARG
     # greedy tree verification
     assert lib.qv_tree_accept(None, fake, fake, 1, 16, fake, fake, None, None) == qv.QV_ERR_INVALID_ARG
     assert lib.qv_tree_accept(fake, fake, fake, 1, 1025, fake, fake, None, None) == qv.QV_ERR_INVALID_ARG
