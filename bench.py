@@ -488,6 +488,59 @@ def main():
         del tg, tstack
         torch.cuda.empty_cache()
 
+    # ---- W4A8: the same step with packed int4 weights (half the weight
+    # bytes), and its streaming GEMM over the step's 144 projections
+    w4a8 = None
+    if rank == 0:
+        w4s = VerifyStack(layers=args.layers, B=1, gamma=4, seed=1234 + rank, device=str(dev), wbits=4)
+        w4s.enqueue_two_call()
+        torch.cuda.synchronize()
+        w4s.drafts.copy_(synth.geometric_drafts(w4s.tokens.view(w4s.B, w4s.gamma + 1).cpu(), w4s.V, 0.7,
+                                                seed=99 + rank))
+        g4 = w4s.capture_two_call()
+        for _ in range(3):
+            g4.replay()
+        torch.cuda.synchronize()
+        w4_ms = time_graph(torch, g4, max(20, args.steps // 5), stream)
+        del g4
+        xq4 = []
+        for l in range(w4s.layers):
+            for p, (name, K, N) in enumerate(w4s.phases):
+                xq = torch.empty(M, K, dtype=torch.int8, device=dev)
+                sxp = torch.empty(M, device=dev)
+                qv.qv_quantize_act(w4s.inputs[l][p], xq, sxp)
+                xq4.append((xq, sxp))
+        torch.cuda.synchronize()
+
+        def lin4_seq(s):
+            j = 0
+            for l in range(w4s.layers):
+                for p, (name, K, N) in enumerate(w4s.phases):
+                    wq, sw = w4s.weights[l][p]
+                    qv.qv_w4a8_linear(xq4[j][0], xq4[j][1], wq, sw, w4s.y[: M * N].view(M, N), w4s.ws, stream=s)
+                    j += 1
+        g4l = VerifyStack._capture(lin4_seq, dev)
+        lin4_ms = time_graph(torch, g4l, args.kernel_reps, stream)
+        lin4_bytes = w4s.linear_launch_bytes(fused_act=False)
+        ach4 = sum(lin4_bytes) / (lin4_ms * 1e-3) / 1e9
+        log(f"W4A8 step {w4_ms:.4f} ms/step; w4a8 linear kernel {ach4:.1f} GB/s = {ach4 / peak:.3f}")
+        w4a8 = {"ms_per_step": w4_ms, "tokens_per_s": w4s.M / (w4_ms * 1e-3),
+                "weight_bytes_per_step": w4s.weight_bytes(),
+                "weight_stream_gbs": w4s.weight_bytes() / (w4_ms * 1e-3) / 1e9,
+                "speedup_vs_w8a8": ms / w4_ms,
+                "speedup_vs_bf16": (comparator["bf16_ms_per_step"] / w4_ms) if comparator else None,
+                "accept_len": int(w4s.accept_len[0]),
+                "linear_kernel": {"kernel": "w8a8_stream_kernel<1, Linear, W4> (int4 codes unpacked to int8 "
+                                            "mma.sync operands, qv_w4a8_linear)",
+                                  "achieved": ach4, "frac": ach4 / peak, "unit": "GB/s",
+                                  "bytes_per_launch": sum(lin4_bytes) / len(lin4_bytes),
+                                  "launch_ms_mean": lin4_ms / len(lin4_bytes),
+                                  "timing": "144 launches of the step's projections back to back in one CUDA graph"},
+                "path": "per projection qv_quantize_act + qv_w4a8_linear, qv_quantize_act + "
+                        "qv_w4a8_lm_head_argmax, qv_accept; one CUDA graph"}
+        del g4l, xq4, w4s
+        torch.cuda.empty_cache()
+
     if rank == 0 and world == 1 and not args.no_cpu:
         cpu = cpu_baseline(args.cpu_seconds)
 
@@ -517,6 +570,7 @@ def main():
             "layer_chain": layer_chain,
             "sampling_t_gt_0": sampling,
             "tree_verify": tree,
+            "w4a8": w4a8,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

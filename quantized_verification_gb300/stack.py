@@ -36,7 +36,9 @@ from . import qv, synth
 class VerifyStack:
     def __init__(self, model: dict = synth.QWEN3_8B, layers: int | None = None, B: int = 1,
                  gamma: int = 4, seed: int = 0, device: str = "cuda", keep_bf16: bool = False,
-                 y_dtype=torch.float32):
+                 y_dtype=torch.float32, wbits: int = 8):
+        assert wbits in (8, 4), "int8 or packed int4 weights"
+        self.wbits = wbits
         self.model = model
         self.layers = model["layers"] if layers is None else layers
         self.B, self.gamma = B, gamma
@@ -63,9 +65,7 @@ class VerifyStack:
                     # gate and up rows interleaved by 64 (qv_w8a8_swiglu's layout);
                     # the other paths only need some row order
                     w = qv.interleave_gate_up(w)
-                wq = torch.empty(N, K, dtype=torch.int8, device=dev)
-                sw = torch.empty(N, dtype=torch.float32, device=dev)
-                qv.qv_quantize_weight(w, wq, sw)
+                wq, sw = self._quantize_weight(w)
                 lw.append((wq, sw))
                 if keep_bf16:
                     lb.append(w)
@@ -77,9 +77,7 @@ class VerifyStack:
                 self.weights_bf16.append(lb)
             self.inputs.append(li)
         wl = synth.weights(self.V, h, synth.subseed(seed, "w", "lm_head"), device=dev)
-        self.lm_wq = torch.empty(self.V, h, dtype=torch.int8, device=dev)
-        self.lm_sw = torch.empty(self.V, dtype=torch.float32, device=dev)
-        qv.qv_quantize_weight(wl, self.lm_wq, self.lm_sw)
+        self.lm_wq, self.lm_sw = self._quantize_weight(wl)
         self.lm_bf16 = wl if keep_bf16 else None
         del wl
         self.h_final = synth.activations(self.M, h, synth.subseed(seed, "x", "final"), device=dev)
@@ -125,11 +123,41 @@ class VerifyStack:
         self.graph = None
         torch.cuda.synchronize(dev)
 
+    def _quantize_weight(self, w):
+        """int8 codes [N, K] (qv_quantize_weight) or packed int4 codes
+        [N, K/2] (qv_quantize_weight_w4), and the fp32 channel scales."""
+        N, K = w.shape
+        sw = torch.empty(N, dtype=torch.float32, device=w.device)
+        if self.wbits == 4:
+            wq = torch.empty(N, K // 2, dtype=torch.uint8, device=w.device)
+            qv.qv_quantize_weight_w4(w, wq, sw)
+        else:
+            wq = torch.empty(N, K, dtype=torch.int8, device=w.device)
+            qv.qv_quantize_weight(w, wq, sw)
+        return wq, sw
+
+    def _linear(self, xq, sx, wq, sw, y, ws, stream=None):
+        if self.wbits == 4:
+            qv.qv_w4a8_linear(xq, sx, wq, sw, y, ws, stream=stream)
+        else:
+            qv.qv_w8a8_linear(xq, sx, wq, sw, y, ws, stream=stream)
+
+    def _lm_head(self, xq, ws, stream=None):
+        fn = qv.qv_w4a8_lm_head_argmax if self.wbits == 4 else qv.qv_lm_head_argmax
+        fn(xq, self.sx, self.lm_wq, self.lm_sw, self.tokens, ws, max_logit=self.max_logit, stream=stream)
+
+    def _w8_only(self, what):
+        if self.wbits != 8:
+            raise NotImplementedError(f"{what} runs int8 weights only")
+
     # ------------------------------------------------------------------ sizes
+    def _wb(self, N, K) -> int:
+        return N * K * self.wbits // 8
+
     def weight_bytes(self) -> int:
-        """int8 weight bytes streamed by one step (linears + LM head)."""
-        per_layer = sum(N * K for (_, K, N) in self.phases)
-        return per_layer * self.layers + self.V * self.model["hidden"]
+        """Weight bytes streamed by one step (linears + LM head)."""
+        per_layer = sum(self._wb(N, K) for (_, K, N) in self.phases)
+        return per_layer * self.layers + self._wb(self.V, self.model["hidden"])
 
     def algorithmic_bytes(self) -> int:
         """All bytes one step must move at least: int8 weights and fp32
@@ -140,10 +168,10 @@ class VerifyStack:
         yb = 4 if self.y_dtype == torch.float32 else 2
         total = 0
         for (_, K, N) in self.phases:
-            total += N * K + 4 * N + M * K * 2 + M * N * yb
+            total += self._wb(N, K) + 4 * N + M * K * 2 + M * N * yb
         total *= self.layers
         h = self.model["hidden"]
-        total += self.V * h + 4 * self.V + M * h * 2 + 4 * M + 4 * M   # LM head: weights, x, tokens, max
+        total += self._wb(self.V, h) + 4 * self.V + M * h * 2 + 4 * M + 4 * M   # LM head: weights, x, tokens, max
         total += 4 * M + 4 * self.B * self.gamma + 4 * self.B + 4 * self.B * (self.gamma + 1)  # accept I/O
         return total
 
@@ -155,7 +183,7 @@ class VerifyStack:
         M = self.M
         yb = 4 if self.y_dtype == torch.float32 else 2
         xb = (lambda K: M * K * 2) if fused_act else (lambda K: M * K + 4 * M)
-        one = [N * K + 4 * N + xb(K) + M * N * yb for (_, K, N) in self.phases]
+        one = [self._wb(N, K) + 4 * N + xb(K) + M * N * yb for (_, K, N) in self.phases]
         return one * self.layers
 
     def _xq(self, K):
@@ -166,6 +194,7 @@ class VerifyStack:
         """Enqueue one verify step on `stream` (current stream if None): one
         qv_w8a8_linear_act per projection (quantization kernel + streaming
         GEMM), qv_lm_head_argmax_act, qv_accept."""
+        self._w8_only("the fused-quantization path")
         M = self.M
         ws = self.ws_act
         for l in range(self.layers):
@@ -189,11 +218,10 @@ class VerifyStack:
                 xq = self._xq(K)
                 qv.qv_quantize_act(self.inputs[l][p], xq, self.sx, stream=stream)
                 wq, sw = self.weights[l][p]
-                qv.qv_w8a8_linear(xq, self.sx, wq, sw, self.y[: M * N].view(M, N), ws, stream=stream)
+                self._linear(xq, self.sx, wq, sw, self.y[: M * N].view(M, N), ws, stream=stream)
         xq = self._xq(self.model["hidden"])
         qv.qv_quantize_act(self.h_final, xq, self.sx, stream=stream)
-        qv.qv_lm_head_argmax(xq, self.sx, self.lm_wq, self.lm_sw, self.tokens, ws,
-                             max_logit=self.max_logit, stream=stream)
+        self._lm_head(xq, ws, stream=stream)
         qv.qv_accept(self.tokens.view(self.B, self.gamma + 1), self.drafts if self.gamma > 0 else None,
                      self.accept_len, self.out_tokens, stream=stream)
 
@@ -201,6 +229,7 @@ class VerifyStack:
     def prepare_chain(self, eps: float = 1e-6):
         """Norm weights, the step's input residual stream and the output
         buffers of the chained step (enqueue_chain)."""
+        self._w8_only("the layer chain")
         h, M, F = self.model["hidden"], self.M, self.model["ffn"]
         dev = self.device
         self.eps = eps
@@ -264,6 +293,7 @@ class VerifyStack:
     def prepare_tree(self, parent: torch.Tensor, draft: torch.Tensor):
         """A draft tree over the step's M = N rows (B = 1): parent, draft [1, N]
         int32 (node 0 the root); row i's verifier token follows node i."""
+        self._w8_only("tree verification")
         assert self.B == 1 and parent.shape == (1, self.M) and draft.shape == (1, self.M)
         dev = self.device
         self.tree_parent = parent.to(dev, torch.int32).contiguous()
@@ -299,6 +329,7 @@ class VerifyStack:
         """Buffers of the T > 0 step (enqueue_sampled): fp32 logits, seeded
         draft distributions q (softmax of N(0, 2) logits) and drafts drawn
         from them, the qv_spec_sample workspace."""
+        self._w8_only("the sampled step")
         B, g, V, M = self.B, self.gamma, self.V, self.M
         dev = self.device
         self.temperature, self.sample_seed = temperature, seed
@@ -349,6 +380,7 @@ class VerifyStack:
 
     # ------------------------------------------------------------------ fused step
     def _fused_descs(self):
+        self._w8_only("qv_verify_stack")
         if getattr(self, "_descs", None) is None:
             M = self.M
             descs = []
@@ -429,6 +461,7 @@ class VerifyStack:
 
     # ------------------------------------------------------------------ comparator
     def prepare_bf16(self):
+        self._w8_only("the BF16 comparator")
         assert self.weights_bf16 is not None, "construct with keep_bf16=True"
         h = self.model["hidden"]
         ws_bytes = max([qv.qv_workspace_bytes(qv.QV_OP_BF16_LINEAR, self.M, K, N) for (_, K, N) in self.phases]

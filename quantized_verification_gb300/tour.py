@@ -3,11 +3,12 @@ profiler's launch list or a per-kernel capture.
 
     python -m quantized_verification_gb300.tour [--passes 2]
 
-Each pass makes the same 14 launches in the same order (the first pass is
-the warm-up a capture skips with ``-s 14``):
+Each pass makes the same 15 launches in the same order (the first pass is
+the warm-up a capture skips with ``-s 15``):
 
     quantize_rows_kernel                  per-token int8 activation codes, 5 x 4096
     w8a8_stream_kernel<1, Linear>         5 x 4096 -> 24576 (Qwen3-8B gate+up), fp32 out
+    w8a8_stream_kernel<1, Linear, W4>     the same shape with packed int4 weights (50.3 MB)
     w8a8_stream_kernel<1, SwiGLU>         the same weights interleaved, SiLU(g)*u fused
     w8a8_tc_kernel<64, Linear>            64 tokens, tcgen05 on widened codes
     bf16_stream_kernel<1>                 the BF16 comparator, 5 x 4096 -> 24576
@@ -18,7 +19,7 @@ the warm-up a capture skips with ``-s 14``):
     accept_kernel                         greedy acceptance, 1 x 5
 
 Inputs are seeded and synthetic and sit on the device before the first
-launch; the whole run holds about 0.4 GB.
+launch; the whole run holds about 0.5 GB.
 """
 import argparse
 
@@ -26,7 +27,7 @@ import torch
 
 from . import build, qv, synth
 
-LAUNCHES_PER_PASS = 14
+LAUNCHES_PER_PASS = 15
 
 
 def main(argv=None):
@@ -46,6 +47,9 @@ def main(argv=None):
     sw = torch.empty(N, device=dev)
     qv.qv_quantize_weight(w, wq, sw)
     wq_il, sw_il = qv.interleave_gate_up(wq), qv.interleave_gate_up(sw)
+    wq4 = torch.empty(N, K // 2, dtype=torch.uint8, device=dev)
+    sw4 = torch.empty(N, device=dev)
+    qv.qv_quantize_weight_w4(w, wq4, sw4)
     y = torch.empty(M, N, device=dev)
     a = torch.empty(M, F, device=dev)
     ws = qv.workspace(qv.QV_OP_LINEAR, 64, K, N)
@@ -77,6 +81,7 @@ def main(argv=None):
     for _ in range(args.passes):
         qv.qv_quantize_act(x, xq, sx)
         qv.qv_w8a8_linear(xq, sx, wq, sw, y, ws)
+        qv.qv_w4a8_linear(xq, sx, wq4, sw4, y, ws)
         qv.qv_w8a8_swiglu(xq, sx, wq_il, sw_il, a, ws)
         qv.qv_w8a8_linear(x64, sx64, wq, sw, y64, ws)
         qv.qv_bf16_linear(x, w, y, wsb)

@@ -227,3 +227,29 @@ def test_w4a8_rejects_bad_k(qv):
     y = torch.zeros(2, 16, device="cuda")
     with pytest.raises(qv.QVError):
         qv.qv_w4a8_linear(xq, torch.ones(2, device="cuda"), wq4, torch.ones(16, device="cuda"), y, ws)
+
+
+def test_w4a8_stack_step_matches_oracle(qv, oracle):
+    """A small stack with int4 weights, one two-call step (qv_quantize_act +
+    qv_w4a8_linear per projection, qv_quantize_act + qv_w4a8_lm_head_argmax,
+    qv_accept): the last projection's output, the tokens and the accepted
+    lengths equal the oracle's."""
+    from gpu_util import bf16_bits
+    from quantized_verification_gb300 import synth
+    from quantized_verification_gb300.stack import VerifyStack
+    model = {"hidden": 256, "kv": 64, "ffn": 512, "layers": 2, "vocab": 3000}
+    st = VerifyStack(model=model, B=2, gamma=3, seed=13, wbits=4)
+    st.drafts.copy_(synth.uniform_tokens((2, 3), 3000, seed=4).cuda())
+    st.enqueue_two_call()
+    torch.cuda.synchronize()
+    name, K, N = st.phases[-1]
+    wq4, sw = st.weights[-1][-1]
+    xq, sx = oracle.quantize_rows(bf16_bits(st.inputs[-1][-1]), bf16=True)
+    y_ref, _ = oracle.w4a8_linear(xq, sx, np_(wq4), np_(sw))
+    assert np.array_equal(np_(st.y[: st.M * N].view(st.M, N)).view(np.uint32), y_ref.view(np.uint32))
+    xh, sh = oracle.quantize_rows(bf16_bits(st.h_final), bf16=True)
+    t_ref, m_ref = oracle.w4a8_lm_head_argmax(xh, sh, np_(st.lm_wq), np_(st.lm_sw))
+    assert np.array_equal(np_(st.tokens), t_ref) and np.array_equal(np_(st.max_logit), m_ref)
+    l_ref, o_ref = oracle.accept(t_ref, np_(st.drafts), 2, 3)
+    assert np.array_equal(np_(st.accept_len), l_ref) and np.array_equal(np_(st.out_tokens), o_ref)
+    assert st.weight_bytes() == (sum(N * K for (_, K, N) in st.phases) * 2 + 3000 * 256) // 2
