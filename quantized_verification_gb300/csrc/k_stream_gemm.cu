@@ -266,23 +266,43 @@ __device__ __forceinline__ void w8a8_tile_mma(uint32_t wb, uint32_t xb, const Ti
 // W4A8 tile: 128 channels x 128 bytes of packed int4 codes (256 codes of K per
 // channel; byte j holds code 2j in its low nibble and 2j+1 in its high one)
 // against the activation tile, two 128-byte swizzled boxes of MP tokens x
-// 128 codes. The nibbles become int8 operands of the int8 m16n8k32 MMA
-// without a table: masking the high nibble in place gives 16 * code(2j+1),
-// shifting the low nibble up gives 16 * code(2j), both exact int8 values
-// (16 * [-7, 7]). Each thread's ldmatrix word of a 16-byte chunk holds codes
-// 32c + 8t .. 32c + 8t + 7 (t = lane % 4), so the MMA's K slots carry even
-// codes in its first half and odd codes in its second; the activation
-// operand is fetched in the same order (one 8-byte load of codes 8t .. 8t+7
-// per token, split into even and odd bytes), which leaves every dot product
-// unchanged. The sums are 16 times the true ones; the caller shifts them
-// back exactly (|sum| <= 16 * 7 * 127 * K < 2^31 for K <= 150975).
+// 128 codes. Both operands go through the f16 m16n8k16 MMA (four times the
+// int8 MMA's rate on this part, which would otherwise bound a 4-bit stream):
+//  - a 32-bit ldmatrix word holds codes 32c + 8t .. 32c + 8t + 7 of one row
+//    (t = lane % 4), nibble s at bits 4s and 16 + 4s for s = 0..3 holding
+//    codes 8t+s and 8t+4+s; ((word >> 4s) & 0x000F000F) ^ 0x64086408 is the
+//    f16 pair 1032 + code (two's complement nibble, bit 3 flipped under the
+//    exponent of 1024), and subtracting 1032 leaves the code exactly;
+//  - the activation codes 8t .. 8t+7 of each token come from one 8-byte
+//    load, regrouped into the same pairs and widened exactly to f16;
+//  - pairs s = 0, 1 feed one MMA (K slots 2t, 2t+1 and 2t+8, 2t+9), s = 2, 3
+//    the next, the same slots on both operands, so every dot product is the
+//    plain one.
+// Products are at most 7 * 127 and a tile sums 256 of them per output
+// (|sum| <= 227584 < 2^24): every fp32 partial is an exact integer, converted
+// to int32 after the tile.
 // ---------------------------------------------------------------------------
+__device__ __forceinline__ void int4x8_f16(uint32_t w, uint32_t (&h)[4]) {
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+        h[s] = ((w >> (4 * s)) & 0x000F000Fu) ^ 0x64086408u;
+        asm("sub.f16x2 %0, %0, %1;" : "+r"(h[s]) : "r"(0x64086408u));
+    }
+}
+
 template <int NG, int BPW, int MP>
 __device__ __forceinline__ void w4a8_tile_mma(uint32_t wb, uint32_t xb, const TileLanes<BPW>& L,
                                               const uint32_t (&x_off)[4], int32_t (&acci)[BPW][NG][4]) {
+    float accf[BPW][NG][4];
+#pragma unroll
+    for (int blk = 0; blk < BPW; ++blk)
+#pragma unroll
+        for (int gr = 0; gr < NG; ++gr)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) accf[blk][gr][e] = 0.f;
 #pragma unroll
     for (int P = 0; P < 4; ++P) {                 // packed chunks 2P, 2P+1: codes 64P .. 64P+63
-        uint32_t be[2][NG], bo[2][NG];
+        uint32_t bx[2][NG][4];                    // f16 pairs (x[8t+s], x[8t+4+s]) per chunk, token group
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             const int c = 2 * P + h;
@@ -290,25 +310,33 @@ __device__ __forceinline__ void w4a8_tile_mma(uint32_t wb, uint32_t xb, const Ti
             for (int gr = 0; gr < NG; ++gr) {
                 uint32_t lo, hi;
                 lds_v2_u32(xb + (uint32_t)((c >> 2) * MP * BKB + 8 * gr * BKB) + x_off[c & 3], lo, hi);
-                be[h][gr] = __byte_perm(lo, hi, 0x6420);   // codes 8t, 8t+2, 8t+4, 8t+6
-                bo[h][gr] = __byte_perm(lo, hi, 0x7531);   // codes 8t+1, 8t+3, 8t+5, 8t+7
+                widen_i8x4_f16(__byte_perm(lo, hi, 0x5140), bx[h][gr][0], bx[h][gr][1]);
+                widen_i8x4_f16(__byte_perm(lo, hi, 0x7362), bx[h][gr][2], bx[h][gr][3]);
             }
         }
 #pragma unroll
         for (int blk = 0; blk < BPW; ++blk) {
-            uint32_t r0, r1, r2, r3;     // rows g, g+8 of chunk 2P; rows g, g+8 of chunk 2P+1
-            ldmatrix_x4(wb + L.w_row_off[blk] + L.w_chunk_off[P], r0, r1, r2, r3);
-            const uint32_t e0 = (r0 << 4) & 0xF0F0F0F0u, o0 = r0 & 0xF0F0F0F0u;
-            const uint32_t e1 = (r1 << 4) & 0xF0F0F0F0u, o1 = r1 & 0xF0F0F0F0u;
-            const uint32_t e2 = (r2 << 4) & 0xF0F0F0F0u, o2 = r2 & 0xF0F0F0F0u;
-            const uint32_t e3 = (r3 << 4) & 0xF0F0F0F0u, o3 = r3 & 0xF0F0F0F0u;
+            uint32_t r[4];               // rows g, g+8 of chunk 2P; rows g, g+8 of chunk 2P+1
+            ldmatrix_x4(wb + L.w_row_off[blk] + L.w_chunk_off[P], r[0], r[1], r[2], r[3]);
 #pragma unroll
-            for (int gr = 0; gr < NG; ++gr) {
-                mma_s8_16832(acci[blk][gr], e0, e1, o0, o1, be[0][gr], bo[0][gr]);
-                mma_s8_16832(acci[blk][gr], e2, e3, o2, o3, be[1][gr], bo[1][gr]);
+            for (int h = 0; h < 2; ++h) {
+                uint32_t ag[4], ag8[4];
+                int4x8_f16(r[2 * h], ag);
+                int4x8_f16(r[2 * h + 1], ag8);
+#pragma unroll
+                for (int gr = 0; gr < NG; ++gr) {
+                    mma_f16_16816(accf[blk][gr], ag[0], ag8[0], ag[1], ag8[1], bx[h][gr][0], bx[h][gr][1]);
+                    mma_f16_16816(accf[blk][gr], ag[2], ag8[2], ag[3], ag8[3], bx[h][gr][2], bx[h][gr][3]);
+                }
             }
         }
     }
+#pragma unroll
+    for (int blk = 0; blk < BPW; ++blk)
+#pragma unroll
+        for (int gr = 0; gr < NG; ++gr)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acci[blk][gr][e] += __float2int_rn(accf[blk][gr][e]);
 }
 
 // ---------------------------------------------------------------------------
@@ -396,19 +424,14 @@ w8a8_stream_kernel(const __grid_constant__ CUtensorMap tmap_w,
         }
 
         // -------- segment end: stage the int32 sums [row][token] --------
-        // (W4: the sums are 16 times the true ones, multiples of 16, so the
-        // arithmetic shift is exact)
-        constexpr int SH = W4 ? 4 : 0;
 #pragma unroll
         for (int blk = 0; blk < BPW; ++blk) {
             const int r0 = RW * warp + 16 * blk + g;
 #pragma unroll
             for (int gr = 0; gr < NG; ++gr) {
                 const int col = 8 * gr + 2 * t4;
-                *reinterpret_cast<int2*>(&sm.stg[r0 * MP + col]) =
-                    make_int2(acci[blk][gr][0] >> SH, acci[blk][gr][1] >> SH);
-                *reinterpret_cast<int2*>(&sm.stg[(r0 + 8) * MP + col]) =
-                    make_int2(acci[blk][gr][2] >> SH, acci[blk][gr][3] >> SH);
+                *reinterpret_cast<int2*>(&sm.stg[r0 * MP + col]) = make_int2(acci[blk][gr][0], acci[blk][gr][1]);
+                *reinterpret_cast<int2*>(&sm.stg[(r0 + 8) * MP + col]) = make_int2(acci[blk][gr][2], acci[blk][gr][3]);
             }
         }
         consumer_sync<CW>();
