@@ -266,67 +266,121 @@ __device__ __forceinline__ void w8a8_tile_mma(uint32_t wb, uint32_t xb, const Ti
 // W4A8 tile: 128 channels x 128 bytes of packed int4 codes (256 codes of K per
 // channel; byte j holds code 2j in its low nibble and 2j+1 in its high one)
 // against the activation tile, two 128-byte swizzled boxes of MP tokens x
-// 128 codes. Both operands go through the f16 m16n8k16 MMA (four times the
-// int8 MMA's rate on this part, which would otherwise bound a 4-bit stream):
-//  - a 32-bit ldmatrix word holds codes 32c + 8t .. 32c + 8t + 7 of one row
-//    (t = lane % 4), nibble s at bits 4s and 16 + 4s for s = 0..3 holding
-//    codes 8t+s and 8t+4+s; ((word >> 4s) & 0x000F000F) ^ 0x64086408 is the
-//    f16 pair 1032 + code (two's complement nibble, bit 3 flipped under the
-//    exponent of 1024), and subtracting 1032 leaves the code exactly;
-//  - the activation codes 8t .. 8t+7 of each token come from one 8-byte
-//    load, regrouped into the same pairs and widened exactly to f16;
-//  - pairs s = 0, 1 feed one MMA (K slots 2t, 2t+1 and 2t+8, 2t+9), s = 2, 3
-//    the next, the same slots on both operands, so every dot product is the
-//    plain one.
-// Products are at most 7 * 127 and a tile sums 256 of them per output
-// (|sum| <= 227584 < 2^24): every fp32 partial is an exact integer, converted
-// to int32 after the tile.
+// 128 codes. A 32-bit ldmatrix word holds codes 32c + 8t .. 32c + 8t + 7 of
+// one row (t = lane % 4); the matching activation codes of each token come
+// from one 8-byte load. Chunk pairs P < S8P run on the int8 MMA, the others
+// on the f16 MMA:
+//  - int8 m16n8k32: masking a high nibble in place gives 16 * code(2j+1)
+//    and shifting a low nibble up gives 16 * code(2j), both exact int8
+//    operands; the activation bytes are split into even and odd codes to
+//    match (K slots carry even codes in the first half, odd codes in the
+//    second); the sums are 16 times the true ones and are shifted back
+//    exactly after the tile;
+//  - f16 m16n8k16: (w & 0x000F000F) ^ 0x64086408 is the f16 pair 1032 + code
+//    for the nibbles at bits 0 and 16 (two's complement nibble with bit 3
+//    flipped under the exponent of 1024), minus 1032 exactly; the nibbles at
+//    bits 4 and 20 give 1024 + 16 (code ^ 8) and one fused multiply-add by
+//    1/16 and -72 (exact) gives the code; the word shifted by 8 gives the
+//    other two pairs. Activation codes are regrouped into the same pairs and
+//    widened exactly to f16. Products are at most 7 * 127 and a tile sums at
+//    most 256 of them per output (|sum| < 2^24): every fp32 partial is an
+//    exact integer, converted to int32 after the tile.
+// On GB300 the int8 MMA runs at a quarter of the f16 rate and the f16 path
+// pays for its conversions in issue slots; the two costs add up rather than
+// overlap (measured: splitting a tile between them, interleaved or not, and
+// independent accumulator chains all land between the two). With one token
+// group (up to 8 tokens) the int8 path is faster, with more the f16 path.
 // ---------------------------------------------------------------------------
+template <int NG>
+__host__ __device__ constexpr int w4_s8_pairs() { return NG == 1 ? 4 : 0; }
+
+// f16 pairs (code 8t+s, code 8t+4+s), s = 0..3, of one packed word
 __device__ __forceinline__ void int4x8_f16(uint32_t w, uint32_t (&h)[4]) {
 #pragma unroll
-    for (int s = 0; s < 4; ++s) {
-        h[s] = ((w >> (4 * s)) & 0x000F000Fu) ^ 0x64086408u;
-        asm("sub.f16x2 %0, %0, %1;" : "+r"(h[s]) : "r"(0x64086408u));
+    for (int q = 0; q < 2; ++q) {
+        const uint32_t v = q ? (w >> 8) : w;
+        uint32_t lo = (v & 0x000F000Fu) ^ 0x64086408u;    // 1032 + code
+        uint32_t hi = (v & 0x00F000F0u) ^ 0x64806480u;    // 1024 + 16 (code ^ 8)
+        asm("sub.f16x2 %0, %0, %1;" : "+r"(lo) : "r"(0x64086408u));
+        asm("fma.rn.f16x2 %0, %0, %1, %2;" : "+r"(hi) : "r"(0x2C002C00u), "r"(0xD480D480u));   // * 1/16 - 72
+        h[2 * q] = lo;
+        h[2 * q + 1] = hi;
     }
 }
 
 template <int NG, int BPW, int MP>
 __device__ __forceinline__ void w4a8_tile_mma(uint32_t wb, uint32_t xb, const TileLanes<BPW>& L,
                                               const uint32_t (&x_off)[4], int32_t (&acci)[BPW][NG][4]) {
+    constexpr int S8P = w4_s8_pairs<NG>();
     float accf[BPW][NG][4];
+    int32_t acc16[BPW][NG][4];
 #pragma unroll
     for (int blk = 0; blk < BPW; ++blk)
 #pragma unroll
         for (int gr = 0; gr < NG; ++gr)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) accf[blk][gr][e] = 0.f;
+            for (int e = 0; e < 4; ++e) {
+                accf[blk][gr][e] = 0.f;
+                acc16[blk][gr][e] = 0;
+            }
 #pragma unroll
     for (int P = 0; P < 4; ++P) {                 // packed chunks 2P, 2P+1: codes 64P .. 64P+63
-        uint32_t bx[2][NG][4];                    // f16 pairs (x[8t+s], x[8t+4+s]) per chunk, token group
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int c = 2 * P + h;
-#pragma unroll
-            for (int gr = 0; gr < NG; ++gr) {
-                uint32_t lo, hi;
-                lds_v2_u32(xb + (uint32_t)((c >> 2) * MP * BKB + 8 * gr * BKB) + x_off[c & 3], lo, hi);
-                widen_i8x4_f16(__byte_perm(lo, hi, 0x5140), bx[h][gr][0], bx[h][gr][1]);
-                widen_i8x4_f16(__byte_perm(lo, hi, 0x7362), bx[h][gr][2], bx[h][gr][3]);
-            }
-        }
-#pragma unroll
-        for (int blk = 0; blk < BPW; ++blk) {
-            uint32_t r[4];               // rows g, g+8 of chunk 2P; rows g, g+8 of chunk 2P+1
-            ldmatrix_x4(wb + L.w_row_off[blk] + L.w_chunk_off[P], r[0], r[1], r[2], r[3]);
+        if (P < S8P) {
+            uint32_t be[2][NG], bo[2][NG];
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
-                uint32_t ag[4], ag8[4];
-                int4x8_f16(r[2 * h], ag);
-                int4x8_f16(r[2 * h + 1], ag8);
+                const int c = 2 * P + h;
 #pragma unroll
                 for (int gr = 0; gr < NG; ++gr) {
-                    mma_f16_16816(accf[blk][gr], ag[0], ag8[0], ag[1], ag8[1], bx[h][gr][0], bx[h][gr][1]);
-                    mma_f16_16816(accf[blk][gr], ag[2], ag8[2], ag[3], ag8[3], bx[h][gr][2], bx[h][gr][3]);
+                    uint32_t lo, hi;
+                    lds_v2_u32(xb + (uint32_t)((c >> 2) * MP * BKB + 8 * gr * BKB) + x_off[c & 3], lo, hi);
+                    be[h][gr] = __byte_perm(lo, hi, 0x6420);   // codes 8t, 8t+2, 8t+4, 8t+6
+                    bo[h][gr] = __byte_perm(lo, hi, 0x7531);   // codes 8t+1, 8t+3, 8t+5, 8t+7
+                }
+            }
+#pragma unroll
+            for (int blk = 0; blk < BPW; ++blk) {
+                uint32_t r0, r1, r2, r3;     // rows g, g+8 of chunk 2P; rows g, g+8 of chunk 2P+1
+                ldmatrix_x4(wb + L.w_row_off[blk] + L.w_chunk_off[P], r0, r1, r2, r3);
+                const uint32_t e0 = (r0 << 4) & 0xF0F0F0F0u, o0 = r0 & 0xF0F0F0F0u;
+                const uint32_t e1 = (r1 << 4) & 0xF0F0F0F0u, o1 = r1 & 0xF0F0F0F0u;
+                const uint32_t e2 = (r2 << 4) & 0xF0F0F0F0u, o2 = r2 & 0xF0F0F0F0u;
+                const uint32_t e3 = (r3 << 4) & 0xF0F0F0F0u, o3 = r3 & 0xF0F0F0F0u;
+#pragma unroll
+                for (int gr = 0; gr < NG; ++gr) {
+                    mma_s8_16832(acc16[blk][gr], e0, e1, o0, o1, be[0][gr], bo[0][gr]);
+                    mma_s8_16832(acc16[blk][gr], e2, e3, o2, o3, be[1][gr], bo[1][gr]);
+                }
+            }
+        } else {
+            uint32_t bx[2][NG][4];                // f16 pairs (x[8t+s], x[8t+4+s])
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int c = 2 * P + h;
+#pragma unroll
+                for (int gr = 0; gr < NG; ++gr) {
+                    uint32_t lo, hi;
+                    lds_v2_u32(xb + (uint32_t)((c >> 2) * MP * BKB + 8 * gr * BKB) + x_off[c & 3], lo, hi);
+                    widen_i8x4_f16(__byte_perm(lo, hi, 0x5140), bx[h][gr][0], bx[h][gr][1]);
+                    widen_i8x4_f16(__byte_perm(lo, hi, 0x7362), bx[h][gr][2], bx[h][gr][3]);
+                }
+            }
+#pragma unroll
+            for (int blk = 0; blk < BPW; ++blk) {
+                uint32_t r[4];
+                ldmatrix_x4(wb + L.w_row_off[blk] + L.w_chunk_off[P], r[0], r[1], r[2], r[3]);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t ag[4], ag8[4];
+                    int4x8_f16(r[2 * h], ag);
+                    int4x8_f16(r[2 * h + 1], ag8);
+#pragma unroll
+                    for (int gr = 0; gr < NG; ++gr) {
+                        mma_f16_16816(accf[blk][gr], ag[0], ag8[0], ag[1], ag8[1], bx[h][gr][0],
+                                      bx[h][gr][1]);
+                        mma_f16_16816(accf[blk][gr], ag[2], ag8[2], ag[3], ag8[3], bx[h][gr][2],
+                                      bx[h][gr][3]);
+                    }
                 }
             }
         }
@@ -336,8 +390,11 @@ __device__ __forceinline__ void w4a8_tile_mma(uint32_t wb, uint32_t xb, const Ti
 #pragma unroll
         for (int gr = 0; gr < NG; ++gr)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) acci[blk][gr][e] += __float2int_rn(accf[blk][gr][e]);
+            for (int e = 0; e < 4; ++e)
+                acci[blk][gr][e] += (S8P > 0 ? (acc16[blk][gr][e] >> 4) : 0) +
+                                    (S8P < 4 ? __float2int_rn(accf[blk][gr][e]) : 0);
 }
+
 
 // ---------------------------------------------------------------------------
 // W8A8 kernel (W4 = 1: the W4A8 kernel, packed int4 weights, same pipeline
