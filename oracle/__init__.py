@@ -86,6 +86,7 @@ class Oracle:
         L.qvo_quantize_rows_w4_f32.argtypes = [_P, _I, _I, _P, _P]
         L.qvo_pack_w4.argtypes = [_P, _I, _I, _P]
         L.qvo_unpack_w4.argtypes = [_P, _I, _I, _P]
+        L.qvo_logit_fidelity.argtypes = [_P, _P, _I, _I, _P, _P, _P]
         L.qvo_draw_index.restype = ctypes.c_int32
         L.qvo_draw_index.argtypes = [_P, _I, ctypes.c_uint64, ctypes.c_uint32]
 
@@ -340,6 +341,24 @@ class Oracle:
     def w4a8_lm_head_argmax(self, xq, sx, wq4, sw):
         """f4 with the a3 greedy argmax (lowest index on ties)."""
         return self.lm_head_argmax(xq, sx, self.unpack_w4(wq4), sw)
+
+
+    # -- f3': logit fidelity ------------------------------------------------
+    def logit_fidelity(self, a: np.ndarray, b: np.ndarray):
+        """KL(softmax(a) || softmax(b)) per row in binary64, and the top-1
+        indices of a and b (lowest index on ties). The summaries' fidelity
+        claim: negligible KL divergence between the full-precision and the
+        quantized verifier's logits (gist.science/fr summary, contributions
+        item 3). Returns (kl float64 [M], ta int32 [M], tb int32 [M])."""
+        a = np.ascontiguousarray(a, dtype=np.float32)
+        b = np.ascontiguousarray(b, dtype=np.float32)
+        assert a.shape == b.shape
+        M, V = a.shape
+        kl = np.empty(M, dtype=np.float64)
+        ta = np.empty(M, dtype=np.int32)
+        tb = np.empty(M, dtype=np.int32)
+        self._L.qvo_logit_fidelity(_ptr(a), _ptr(b), M, V, _ptr(kl), _ptr(ta), _ptr(tb))
+        return kl, ta, tb
 
 
 _default: Oracle | None = None

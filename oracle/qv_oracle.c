@@ -52,6 +52,13 @@
  *       -- tree-structured verification named as an extension by the
  *          summaries (gist.science/ja summary, section 4; shd-paper.top,
  *          outlook); the acceptance rule is a4's applied along each path.
+ *   f3' logit fidelity (diagnostic): KL(p || q) between the softmax of a
+ *       reference verifier's logits (p) and of the quantized verifier's (q),
+ *       and whether their top-1 tokens agree -- the summaries report that
+ *       quantization keeps the logit distribution (negligible KL divergence;
+ *       gist.science/fr summary, contributions item 3) and that the
+ *       quantized verifier keeps a high logit-distribution similarity
+ *       (paper-digest summary, core idea).
  *   f4  a lower-bit verifier, W4A8: int4 weights against the a1 int8
  *       activations, accumulated exactly in integers and dequantized as in a2
  *       -- lower bit widths (4-bit, 2-bit) named as the next step by the
@@ -705,4 +712,42 @@ void qvo_unpack_w4(const uint8_t* packed, int64_t rows, int64_t K, int8_t* q)
             q[r * K + 2 * j] = nibble_value(byte & 0xFu);
             q[r * K + 2 * j + 1] = nibble_value(byte >> 4);
         }
+}
+
+/* ------------------------------------------------------------------ */
+/* f3': logit fidelity, in binary64                                     */
+/* ------------------------------------------------------------------ */
+
+/* For each row m: p = softmax(a[m]), q = softmax(b[m]) (natural base),
+ * kl[m] = sum_v p_v (log p_v - log q_v), written out as the definition with
+ * log p_v = a_v - max a - log sum exp(a - max a) (likewise q), in binary64;
+ * ta[m], tb[m] = the first index of the maximum of a[m], b[m]. */
+void qvo_logit_fidelity(const float* a, const float* b, int64_t M, int64_t V,
+                        double* kl, int32_t* ta, int32_t* tb)
+{
+    for (int64_t m = 0; m < M; ++m) {
+        const float* ar = a + m * V;
+        const float* br = b + m * V;
+        int64_t ia = 0, ib = 0;
+        for (int64_t v = 1; v < V; ++v) {
+            if (ar[v] > ar[ia]) ia = v;
+            if (br[v] > br[ib]) ib = v;
+        }
+        const double ma = ar[ia], mb = br[ib];
+        double za = 0.0, zb = 0.0;
+        for (int64_t v = 0; v < V; ++v) {
+            za += exp((double)ar[v] - ma);
+            zb += exp((double)br[v] - mb);
+        }
+        const double lza = log(za), lzb = log(zb);
+        double s = 0.0;
+        for (int64_t v = 0; v < V; ++v) {
+            const double lp = (double)ar[v] - ma - lza;
+            const double lq = (double)br[v] - mb - lzb;
+            s += exp(lp) * (lp - lq);
+        }
+        kl[m] = s;
+        ta[m] = (int32_t)ia;
+        tb[m] = (int32_t)ib;
+    }
 }

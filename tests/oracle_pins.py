@@ -699,6 +699,48 @@ def pin_w4_linear_bruteforce(o):
                 assert y[m, n] == dequant_exact(tot, sx[m], sw[n])
 
 
+# ---------------------------------------------------------------------------
+# f3': logit fidelity
+# ---------------------------------------------------------------------------
+
+def pin_fidelity_closed_forms(o):
+    """KL of a distribution with itself is 0, softmax ignores a constant
+    shift of the logits, and two tokens give the textbook binary KL."""
+    rng = np.random.default_rng(5)
+    a = rng.normal(0, 3, (4, 1000)).astype(np.float32)
+    kl, ta, tb = o.logit_fidelity(a, a)
+    assert np.all(kl == 0.0) and np.array_equal(ta, tb)
+    kl, _, _ = o.logit_fidelity(a, (a + np.float32(4.0)).astype(np.float32))
+    assert np.all(np.abs(kl) < 1e-12)
+    import math
+    for x, y in ((0.3, -1.2), (2.0, 2.5), (-4.0, 1.0)):
+        x, y = float(np.float32(x)), float(np.float32(y))   # the logits the oracle sees
+        p1 = 1.0 / (1.0 + math.exp(-x))      # softmax of (x, 0)
+        q1 = 1.0 / (1.0 + math.exp(-y))
+        ref = p1 * math.log(p1 / q1) + (1 - p1) * math.log((1 - p1) / (1 - q1))
+        kl, ta, tb = o.logit_fidelity(np.float32([[x, 0.0]]), np.float32([[y, 0.0]]))
+        assert abs(kl[0] - ref) <= 1e-12 * max(1.0, ref), (x, y, kl[0], ref)
+        assert ta[0] == (0 if np.float32(x) > 0 else 1) and tb[0] == (0 if np.float32(y) > 0 else 1)
+
+
+def pin_fidelity_scipy(o):
+    """KL against scipy's relative entropy of the two softmax distributions,
+    and the top-1 indices against numpy's argmax (first index on ties)."""
+    from scipy.special import softmax
+    from scipy.stats import entropy
+    rng = np.random.default_rng(8)
+    a = rng.normal(0, 2, (6, 3000)).astype(np.float32)
+    b = (a + rng.normal(0, 0.3, a.shape)).astype(np.float32)
+    b[1] = rng.normal(0, 2, 3000)                   # an unrelated row
+    a[2, 17] = a[2, 1234] = a[2].max() + 1          # a tie: the first index wins
+    kl, ta, tb = o.logit_fidelity(a, b)
+    for m in range(a.shape[0]):
+        ref = entropy(softmax(a[m].astype(np.float64)), softmax(b[m].astype(np.float64)))
+        assert abs(kl[m] - ref) <= 1e-10 * max(1.0, ref), (m, kl[m], ref)
+    assert np.array_equal(ta, np.argmax(a, axis=1)) and np.array_equal(tb, np.argmax(b, axis=1))
+    assert ta[2] == 17
+
+
 ALL_PINS = [
     pin_worked_example,
     pin_quantize_exact_rational,
@@ -726,4 +768,6 @@ ALL_PINS = [
     pin_w4_quantize_exact_rational,
     pin_w4_pack_roundtrip,
     pin_w4_linear_bruteforce,
+    pin_fidelity_closed_forms,
+    pin_fidelity_scipy,
 ]

@@ -68,6 +68,9 @@ MUTANTS = [
     ("w4_unpack_unsigned", "return (int8_t)(n >= 8u ? (int)n - 16 : (int)n);", "return (int8_t)n;"),
     ("w4_unpack_high_first", "q[r * K + 2 * j] = nibble_value(byte & 0xFu);",
      "q[r * K + 2 * j] = nibble_value(byte >> 4);"),
+    ("kl_reversed", "s += exp(lp) * (lp - lq);", "s += exp(lq) * (lq - lp);"),
+    ("kl_no_normalisation", "const double lp = (double)ar[v] - ma - lza;", "const double lp = (double)ar[v] - ma;"),
+    ("fidelity_last_tie", "if (ar[v] > ar[ia]) ia = v;", "if (ar[v] >= ar[ia]) ia = v;"),
     ("residual_not_added",
      "hr[k] = qvo_f32_to_bf16_rne(qvo_bf16_to_f32(hr[k]) + qvo_bf16_to_f32(d[m * H + k]));",
      "hr[k] = hr[k];"),
