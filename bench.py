@@ -459,6 +459,26 @@ def main():
                             "(fp32 logits) + qv_spec_sample (lossless rejection sampling against seeded "
                             "draft distributions); one CUDA graph"}
 
+    # ---- logit fidelity of the quantized verifier against the BF16 one on
+    # the step's final hidden states (synthetic weights): KL(p_bf16 || p_q)
+    # per row and top-1 agreement
+    fidelity = None
+
+    def fid(ref, logits):
+        kl = torch.empty(ref.shape[0], device=dev)
+        ta = torch.empty(ref.shape[0], dtype=torch.int32, device=dev)
+        tb = torch.empty(ref.shape[0], dtype=torch.int32, device=dev)
+        qv.qv_logit_fidelity(ref, logits, kl, ta, tb)
+        torch.cuda.synchronize()
+        return {"kl_mean": float(kl.double().mean()), "kl_max": float(kl.max()),
+                "top1_agree": float((ta == tb).float().mean())}
+    if rank == 0 and comparator is not None and sampling is not None:
+        fidelity = {"w8a8_vs_bf16": fid(stack.logits_bf16, stack.logits),
+                    "note": "KL(softmax(BF16 logits) || softmax(quantized logits)) in nats over the LM-head "
+                            "logits of the step's M rows (synthetic weights and hidden states), and the fraction "
+                            "of rows whose top-1 tokens agree; qv_logit_fidelity"}
+        log(f"fidelity W8A8 vs BF16: {fidelity['w8a8_vs_bf16']}")
+
     # ---- a 16-node draft tree (root, 3 children, 2 grandchildren each, one
     # great-grandchild each) verified in one step, greedy
     tree = None
@@ -538,6 +558,16 @@ def main():
                                   "timing": "144 launches of the step's projections back to back in one CUDA graph"},
                 "path": "per projection qv_quantize_act + qv_w4a8_linear, qv_quantize_act + "
                         "qv_w4a8_lm_head_argmax, qv_accept; one CUDA graph"}
+        if fidelity is not None:
+            h = w4s.model["hidden"]
+            xqf = torch.empty(M, h, dtype=torch.int8, device=dev)
+            sxf = torch.empty(M, device=dev)
+            qv.qv_quantize_act(w4s.h_final, xqf, sxf)
+            logits4 = torch.empty(M, w4s.V, device=dev)
+            qv.qv_w4a8_linear(xqf, sxf, w4s.lm_wq, w4s.lm_sw, logits4, w4s.ws)
+            fidelity["w4a8_vs_bf16"] = fid(stack.logits_bf16, logits4)
+            log(f"fidelity W4A8 vs BF16: {fidelity['w4a8_vs_bf16']}")
+            del logits4
         del g4l, xq4, w4s
         torch.cuda.empty_cache()
 
@@ -571,6 +601,7 @@ def main():
             "sampling_t_gt_0": sampling,
             "tree_verify": tree,
             "w4a8": w4a8,
+            "logit_fidelity": fidelity,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

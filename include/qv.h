@@ -384,6 +384,26 @@ QV_API qv_status qv_quantize_weight(const void* w, qv_dtype w_dtype, int N, int 
                              int8_t* wq, float* sw, cudaStream_t stream);
 
 /*
+ * qv_logit_fidelity -- diagnostic: how far the quantized verifier's output
+ * distribution is from a reference verifier's, per row.
+ *   The Quasar summaries report negligible KL divergence between the
+ *   full-precision and the quantized verifier's logit distributions
+ *   (gist.science/fr summary, contributions item 3; paper-digest summary,
+ *   core idea).
+ *   ref_logits, logits [M*V] fp32 device, row-major (e.g. the BF16
+ *   verifier's and the W8A8 verifier's logits of the same tokens);
+ *   kl [M] fp32 out = KL(p || q) in nats, p = softmax(ref row),
+ *   q = softmax(row); top1_ref, top1 [M] int32 out = the first index of
+ *   each row's maximum (top-1 agreement = equality).
+ *   Computed as log1p(E_p[expm1(d - c)]) with d = logits - ref_logits and
+ *   c = E_p[d] (binary32 terms, binary64 block sums): relative error about
+ *   1e-3 of KL or better for KL down to 1e-8. Logits must be finite with
+ *   |d - c| < 80. 1 <= M <= 65535, 1 <= V <= 2^24.
+ */
+QV_API qv_status qv_logit_fidelity(const float* ref_logits, const float* logits, int M, int V,
+                                   float* kl, int32_t* top1_ref, int32_t* top1, cudaStream_t stream);
+
+/*
  * W4A8 -- the lower-bit verifier: int4 weights against the int8 activation
  * codes of qv_quantize_act.
  *   Lower bit widths (4-bit, 2-bit) for the verifier are the next step the

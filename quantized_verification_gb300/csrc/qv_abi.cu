@@ -576,6 +576,24 @@ qv_status qv_spec_sample(const float* logits, const int32_t* draft, const float*
     return ok();
 }
 
+qv_status qv_logit_fidelity(const float* ref_logits, const float* logits, int M, int V, float* kl,
+                            int32_t* top1_ref, int32_t* top1, cudaStream_t stream) {
+    if (!ref_logits || !logits || !kl || !top1_ref || !top1) return fail(QV_ERR_INVALID_ARG, "null pointer");
+    if (M < 1 || M > 65535) return fail(QV_ERR_INVALID_ARG, "M=%d outside [1, 65535]", M);
+    if (V < 1 || V > (1 << 24)) return fail(QV_ERR_INVALID_ARG, "V=%d outside [1, 2^24]", V);
+    if (!aligned(ref_logits, 4) || !aligned(logits, 4) || !aligned(kl, 4) || !aligned(top1_ref, 4) ||
+        !aligned(top1, 4))
+        return fail(QV_ERR_INVALID_ARG, "buffers must be 4-byte aligned");
+    QV_CHECK_DEV(ref_logits);
+    QV_CHECK_DEV(logits);
+    QV_CHECK_DEV(kl);
+    QV_CHECK_DEV(top1_ref);
+    QV_CHECK_DEV(top1);
+    cudaError_t e = qv::launch_logit_fidelity(ref_logits, logits, M, V, kl, top1_ref, top1, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "qv_logit_fidelity launch");
+    return ok();
+}
+
 qv_status qv_accept(const int32_t* verify_tokens, const int32_t* draft, int B, int gamma,
                     int32_t* accept_len, int32_t* out_tokens, cudaStream_t stream) {
     if (!verify_tokens || !accept_len || !out_tokens) return fail(QV_ERR_INVALID_ARG, "null pointer");

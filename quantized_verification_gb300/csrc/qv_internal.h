@@ -126,6 +126,11 @@ cudaError_t launch_quantize_weight_w4(const void* w, bool bf16, int N, int K, ui
 // rows per launch.
 constexpr int kMaxMPerLaunchW4 = 32;
 
+// Logit-fidelity diagnostic (k_fidelity.cu): per row KL(softmax(a) ||
+// softmax(b)) and both top-1 indices.
+cudaError_t launch_logit_fidelity(const float* a, const float* b, int M, int V, float* kl, int32_t* top_a,
+                                  int32_t* top_b, cudaStream_t s);
+
 // Speculative sampling at T > 0 (k_spec.cu): per-chunk maxima and sums, row
 // statistics and the decisions for M rows of V tokens (every call rewrites
 // all of it, so the workspace needs no initialisation).

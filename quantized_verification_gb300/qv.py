@@ -30,7 +30,7 @@ EXPORTS = ("qv_quantize_act", "qv_w8a8_linear", "qv_lm_head_argmax", "qv_accept"
            "qv_verify_stack", "qv_w8a8_linear_act", "qv_lm_head_argmax_act",
            "qv_rmsnorm_quant", "qv_swiglu_quant", "qv_w8a8_swiglu", "qv_spec_sample",
            "qv_tree_accept", "qv_quantize_weight_w4", "qv_w4a8_linear", "qv_w4a8_swiglu",
-           "qv_w4a8_lm_head_argmax")
+           "qv_w4a8_lm_head_argmax", "qv_logit_fidelity")
 MAX_STACK_M = 16
 
 
@@ -81,6 +81,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         L.qv_spec_sample.argtypes = [P, P, P, I, I, I, ctypes.c_float, ctypes.c_uint64, P, P, P, S, P]
         L.qv_tree_accept.argtypes = [P, P, P, I, I, P, P, P, P]
         L.qv_quantize_weight_w4.argtypes = [P, I, I, I, P, P, P]
+        L.qv_logit_fidelity.argtypes = [P, P, I, I, P, P, P, P]
         L.qv_w4a8_linear.argtypes = [P, P, I, I, P, P, I, P, I, P, P, S, P]
         L.qv_w4a8_swiglu.argtypes = [P, P, I, I, P, P, I, P, P, S, P]
         L.qv_w4a8_lm_head_argmax.argtypes = [P, P, I, I, P, P, I, P, P, P, S, P]
@@ -286,6 +287,19 @@ def qv_lm_head_argmax(xq, sx, wq, sw, tokens, workspace, max_logit=None, stream=
     _need(workspace.dtype == torch.uint8, "workspace must be a uint8 tensor")
     _check(load().qv_lm_head_argmax(_ptr(xq), _ptr(sx), M, K, _ptr(wq), _ptr(sw), V, _ptr(tokens),
                                     _ptr(max_logit), _ptr(workspace), workspace.numel(),
+                                    ctypes.c_void_p(_stream(stream))))
+
+
+def qv_logit_fidelity(ref_logits, logits, kl, top1_ref, top1, stream=None):
+    """Per row: kl [M] = KL(softmax(ref_logits) || softmax(logits)) in nats,
+    top1_ref / top1 [M] int32 = first index of each row's maximum."""
+    M, V = ref_logits.shape
+    _need(ref_logits.dtype == torch.float32 and logits.dtype == torch.float32 and logits.shape == (M, V),
+          "ref_logits and logits must be float32 [M, V]")
+    _need(kl.shape == (M,) and kl.dtype == torch.float32, "kl float32 [M]")
+    _need(top1_ref.shape == (M,) and top1.shape == (M,) and top1_ref.dtype == torch.int32 and
+          top1.dtype == torch.int32, "top1_ref, top1 int32 [M]")
+    _check(load().qv_logit_fidelity(_ptr(ref_logits), _ptr(logits), M, V, _ptr(kl), _ptr(top1_ref), _ptr(top1),
                                     ctypes.c_void_p(_stream(stream))))
 
 

@@ -104,6 +104,11 @@ def test_host_validation_without_gpu(lib):
     assert lib.qv_quantize_weight_w4(fake, 0, 8, 48, fake, fake, None) == qv.QV_ERR_INVALID_ARG
     assert lib.qv_quantize_weight_w4(fake, 5, 8, 64, fake, fake, None) == qv.QV_ERR_INVALID_ARG
     assert lib.qv_quantize_weight_w4(fake, 0, 8, 64, P(0x1008), fake, None) == qv.QV_ERR_INVALID_ARG
+    # logit fidelity
+    assert lib.qv_logit_fidelity(None, fake, 2, 10, fake, fake, fake, None) == qv.QV_ERR_INVALID_ARG
+    assert lib.qv_logit_fidelity(fake, fake, 0, 10, fake, fake, fake, None) == qv.QV_ERR_INVALID_ARG
+    assert lib.qv_logit_fidelity(fake, fake, 2, 0, fake, fake, fake, None) == qv.QV_ERR_INVALID_ARG
+    assert lib.qv_logit_fidelity(fake, P(0x1002), 2, 10, fake, fake, fake, None) == qv.QV_ERR_INVALID_ARG
     # greedy tree verification
     assert lib.qv_tree_accept(None, fake, fake, 1, 16, fake, fake, None, None) == qv.QV_ERR_INVALID_ARG
     assert lib.qv_tree_accept(fake, fake, fake, 1, 1025, fake, fake, None, None) == qv.QV_ERR_INVALID_ARG
