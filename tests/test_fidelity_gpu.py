@@ -36,6 +36,8 @@ def _run(qv, a, b):
 def test_logit_fidelity(qv, oracle, M, V, mode):
     rng = np.random.default_rng(M * 1000 + V % 977)
     a = rng.normal(0, 3, (M, V)).astype(np.float32)
+    if V > 40:
+        a[0, [11, 37]] = a[0].max() + 1                 # a tie: the first index wins
     if mode == "close":
         b = (a + rng.normal(0, 0.05, a.shape)).astype(np.float32)
     elif mode == "far":
@@ -44,8 +46,6 @@ def test_logit_fidelity(qv, oracle, M, V, mode):
         b = (a + np.float32(3.0)).astype(np.float32)
     else:
         b = a.copy()
-    if V > 40:
-        a[0, [11, 37]] = a[0].max() + 1                 # a tie: the first index wins
     kl, ta, tb = _run(qv, a, b)
     kl_ref, ta_ref, tb_ref = oracle.logit_fidelity(a, b)
     assert np.array_equal(ta, ta_ref) and np.array_equal(tb, tb_ref)
