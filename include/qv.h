@@ -284,7 +284,7 @@ QV_API qv_status qv_swiglu_quant(const float* gate_up, int M, int F, int8_t* xq,
  * qv_tree_accept -- greedy (T = 0) verification of a draft tree.
  *
  *   Tree-structured verification is the extension the summaries name for
- *   the drafts (gist.science/ja summary, section 4; shd-paper.top, outlook);
+ *   the drafts (gist.science/de and gist.science/ja summaries, section 5);
  *   along each root path the rule is qv_accept's.
  *
  * Tree b has N nodes, stored at [b*N + i]: node 0 is the root (the last
@@ -388,8 +388,8 @@ QV_API qv_status qv_quantize_weight(const void* w, qv_dtype w_dtype, int N, int 
  * distribution is from a reference verifier's, per row.
  *   The Quasar summaries report negligible KL divergence between the
  *   full-precision and the quantized verifier's logit distributions
- *   (gist.science/fr summary, contributions item 3; paper-digest summary,
- *   core idea).
+ *   (gist.science/fr summary, contributions item 3; shd-paper.top summary,
+ *   method details, core idea).
  *   ref_logits, logits [M*V] fp32 device, row-major (e.g. the BF16
  *   verifier's and the W8A8 verifier's logits of the same tokens);
  *   kl [M] fp32 out = KL(p || q) in nats, p = softmax(ref row),
@@ -407,9 +407,9 @@ QV_API qv_status qv_logit_fidelity(const float* ref_logits, const float* logits,
  * W4A8 -- the lower-bit verifier: int4 weights against the int8 activation
  * codes of qv_quantize_act.
  *   Lower bit widths (4-bit, 2-bit) for the verifier are the next step the
- *   Quasar summaries name (gist.science/it summary, conclusions;
- *   gist.science/de summary, outlook; shd-paper.top, future work); INT4 is
- *   among the widths the authors tried (paper-digest summary, key design).
+ *   Quasar summaries name (gist.science/it, gist.science/de and
+ *   gist.science/ja summaries, section 5); INT4 is among the widths the
+ *   authors tried (shd-paper.top summary, method details, key design).
  *   The pages give no int4 format; the one here keeps a2's exact integer
  *   accumulation and dequantization unchanged.
  *

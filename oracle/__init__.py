@@ -302,8 +302,9 @@ class Oracle:
     # -- f4: W4A8 ----------------------------------------------------------
     def quantize_rows_w4(self, w: np.ndarray, bf16: bool = False):
         """Per-output-channel symmetric int4 weights, the a0 rule with codes in
-        [-7, 7] (lower-bit verifiers: gist.science/it summary, conclusions;
-        INT4 among the widths tried, paper-digest summary, key design).
+        [-7, 7] (lower-bit verifiers: gist.science/it summary, section 5;
+        INT4 among the widths tried: shd-paper.top summary, method details,
+        key design).
         ``w`` float32 [N, K], or bf16 patterns with ``bf16=True`` (widened
         exactly). Returns (q int8 [N, K] codes, s float32 [N])."""
         if bf16:

@@ -50,21 +50,21 @@
  *       root path whose every drafted token equals the verifier's token after
  *       its parent is accepted, plus the verifier's token after its last node
  *       -- tree-structured verification named as an extension by the
- *          summaries (gist.science/ja summary, section 4; shd-paper.top,
- *          outlook); the acceptance rule is a4's applied along each path.
+ *          summaries (gist.science/de and gist.science/ja summaries,
+ *          section 5); the acceptance rule is a4's applied along each path.
  *   f3' logit fidelity (diagnostic): KL(p || q) between the softmax of a
  *       reference verifier's logits (p) and of the quantized verifier's (q),
  *       and whether their top-1 tokens agree -- the summaries report that
  *       quantization keeps the logit distribution (negligible KL divergence;
  *       gist.science/fr summary, contributions item 3) and that the
  *       quantized verifier keeps a high logit-distribution similarity
- *       (paper-digest summary, core idea).
+ *       (shd-paper.top summary, method details, core idea).
  *   f4  a lower-bit verifier, W4A8: int4 weights against the a1 int8
  *       activations, accumulated exactly in integers and dequantized as in a2
  *       -- lower bit widths (4-bit, 2-bit) named as the next step by the
- *          summaries (gist.science/it summary, conclusions; gist.science/de
- *          summary, outlook; shd-paper.top, future work), INT4 among the
- *          bit widths the authors tried (paper-digest summary, key design).
+ *          summaries (gist.science/it, gist.science/de and gist.science/ja
+ *          summaries, section 5), INT4 among the bit widths the authors
+ *          tried (shd-paper.top summary, method details, key design).
  *   a4  acceptance: the longest draft prefix equal to the verifier's tokens,
  *       plus one token from the verifier (so at least one token per step)
  *       -- gist.science/fr summary, lay explanation (a wrong guess is

@@ -4,8 +4,8 @@
 //
 //   The Quasar summaries report that quantizing the verifier keeps the logit
 //   distribution (negligible KL divergence: gist.science/fr summary,
-//   contributions item 3; high logit-distribution similarity: paper-digest
-//   summary, core idea). This kernel measures that on given logits.
+//   contributions item 3; high logit-distribution similarity: shd-paper.top
+//   summary, method details, core idea). This kernel measures that on given logits.
 //
 // One CTA per row, three passes over the row:
 //   1. the maxima of a and b with their lowest indices (64-bit keys,

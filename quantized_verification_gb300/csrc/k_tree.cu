@@ -1,7 +1,7 @@
 // k_tree.cu -- greedy (T = 0) verification of a draft tree.
 //
 //   Tree-structured verification is the extension the summaries name for
-//   the drafts (gist.science/ja summary, section 4; shd-paper.top, outlook);
+//   the drafts (gist.science/de and gist.science/ja summaries, section 5);
 //   along each root path the rule is the linear acceptance of
 //   gist.science/fr summary, lay explanation.
 //

@@ -2,9 +2,9 @@
 // like qv_quantize_weight).
 //
 //   Lower-bit verifiers (4-bit, 2-bit) are the next step the Quasar
-//   summaries name (gist.science/it summary, conclusions; gist.science/de
-//   summary, outlook); INT4 is among the bit widths the authors tried
-//   (paper-digest summary, key design). No format is given; the rule here
+//   summaries name (gist.science/it, gist.science/de and gist.science/ja
+//   summaries, section 5); INT4 is among the bit widths the authors tried
+//   (shd-paper.top summary, method details, key design). No format is given; the rule here
 //   is the int8 one with the code range [-7, 7]:
 //     s = fl32(amax / 7), q = clamp(rne(fl32(w / s)), -7, 7), q = 0 when
 //     s = 0; byte j of a row holds code 2j in bits 0-3 and code 2j+1 in bits
