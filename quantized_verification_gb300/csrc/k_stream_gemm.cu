@@ -97,9 +97,12 @@ struct Cfg {
     // would share the SM's bandwidth and finish last).
     static constexpr int Stages = NG == 1 ? 7 : NG == 2 ? 7 : NG == 4 ? 5 : 4;
     static constexpr int StgWords = BN * MP;                 // epilogue staging
+    // W4A8 f16 path: the tile's activation codes as f16 MMA fragments, one
+    // 16-byte word per (chunk, token group, lane), two tiles' worth
+    static constexpr int XfBytes = XB == 2 ? 2 * 8 * NG * 32 * 16 : 0;
     static constexpr int SmemBytes =
         1024 /*alignment slack*/ + Stages * StageBytes + StgWords * 4 +
-        2 * Stages * 8 + kMaxConsumerWarps * MP * 8 + MP * 4 + 64;
+        2 * Stages * 8 + kMaxConsumerWarps * MP * 8 + MP * 4 + 64 + 16 + XfBytes;
     static_assert(SmemBytes > (int)kMinSmemOneCtaPerSm, "one CTA per SM");
 };
 
@@ -115,6 +118,7 @@ struct Smem {
     float* sx;                // MP
     volatile int* abort;
     volatile int* flag;
+    uint8_t* xf;              // W4A8 f16 path: activation fragments (Cfg::XfBytes)
 
     __device__ __forceinline__ explicit Smem(uint8_t* raw) {
         uintptr_t base = (reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023);
@@ -133,6 +137,7 @@ struct Smem {
         p += MP * 4;
         abort = reinterpret_cast<volatile int*>(p);
         flag = reinterpret_cast<volatile int*>(p + 4);
+        xf = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p + 64) + 15) & ~uintptr_t(15));
     }
     __device__ __forceinline__ uint8_t* w_tile(int s) { return stages + s * StageBytes; }
     __device__ __forceinline__ uint8_t* x_tile(int s) { return stages + s * StageBytes + kWTileBytes; }
@@ -291,8 +296,11 @@ __device__ __forceinline__ void w8a8_tile_mma(uint32_t wb, uint32_t xb, const Ti
 // independent accumulator chains all land between the two). With one token
 // group (up to 8 tokens) the int8 path is faster, with more the f16 path.
 // ---------------------------------------------------------------------------
+#ifndef QV_W4_S8P_NG1
+#define QV_W4_S8P_NG1 4
+#endif
 template <int NG>
-__host__ __device__ constexpr int w4_s8_pairs() { return NG == 1 ? 4 : 0; }
+__host__ __device__ constexpr int w4_s8_pairs() { return NG == 1 ? QV_W4_S8P_NG1 : 0; }
 
 // f16 pairs (code 8t+s, code 8t+4+s), s = 0..3, of one packed word
 __device__ __forceinline__ void int4x8_f16(uint32_t w, uint32_t (&h)[4]) {
@@ -308,10 +316,32 @@ __device__ __forceinline__ void int4x8_f16(uint32_t w, uint32_t (&h)[4]) {
     }
 }
 
-template <int NG, int BPW, int MP>
+template <int NG, int BPW, int MP, int CW>
 __device__ __forceinline__ void w4a8_tile_mma(uint32_t wb, uint32_t xb, const TileLanes<BPW>& L,
-                                              const uint32_t (&x_off)[4], int32_t (&acci)[BPW][NG][4]) {
+                                              const uint32_t (&x_off)[4], uint32_t xfb, int warp, int lane,
+                                              int32_t (&acci)[BPW][NG][4]) {
     constexpr int S8P = w4_s8_pairs<NG>();
+    if constexpr (S8P < 4) {
+        // The f16 chunks' activation fragments are the same for every warp:
+        // warp w widens chunk w once for the CTA into shared memory (two
+        // tiles' buffers: a warp can run at most one tile ahead of the
+        // others, since each tile's barrier waits for all of them).
+        static_assert(CW == 8, "one 32-code chunk per consumer warp");
+        if (warp >= 2 * S8P) {
+            const int c = warp, g = lane >> 2, t4 = lane & 3;
+            const uint32_t off = (uint32_t)((c >> 2) * MP * BKB + g * BKB +
+                                            ((((2 * (c & 3)) + (t4 >> 1)) ^ g) << 4) + ((t4 & 1) << 3));
+#pragma unroll
+            for (int gr = 0; gr < NG; ++gr) {
+                uint32_t lo, hi, f0, f1, f2, f3;
+                lds_v2_u32(xb + off + (uint32_t)(8 * gr * BKB), lo, hi);
+                widen_i8x4_f16(__byte_perm(lo, hi, 0x5140), f0, f1);
+                widen_i8x4_f16(__byte_perm(lo, hi, 0x7362), f2, f3);
+                sts_v4_u32(xfb + (uint32_t)(((c * NG + gr) * 32 + lane) * 16), f0, f1, f2, f3);
+            }
+        }
+        consumer_sync<CW>();
+    }
     float accf[BPW][NG][4];
     int32_t acc16[BPW][NG][4];
 #pragma unroll
@@ -358,12 +388,9 @@ __device__ __forceinline__ void w4a8_tile_mma(uint32_t wb, uint32_t xb, const Ti
             for (int h = 0; h < 2; ++h) {
                 const int c = 2 * P + h;
 #pragma unroll
-                for (int gr = 0; gr < NG; ++gr) {
-                    uint32_t lo, hi;
-                    lds_v2_u32(xb + (uint32_t)((c >> 2) * MP * BKB + 8 * gr * BKB) + x_off[c & 3], lo, hi);
-                    widen_i8x4_f16(__byte_perm(lo, hi, 0x5140), bx[h][gr][0], bx[h][gr][1]);
-                    widen_i8x4_f16(__byte_perm(lo, hi, 0x7362), bx[h][gr][2], bx[h][gr][3]);
-                }
+                for (int gr = 0; gr < NG; ++gr)
+                    lds_v4_u32(xfb + (uint32_t)(((c * NG + gr) * 32 + lane) * 16), bx[h][gr][0], bx[h][gr][1],
+                               bx[h][gr][2], bx[h][gr][3]);
             }
 #pragma unroll
             for (int blk = 0; blk < BPW; ++blk) {
@@ -472,7 +499,9 @@ w8a8_stream_kernel(const __grid_constant__ CUtensorMap tmap_w,
             if (!mbar_wait_bounded(&sm.full[s], phase, sm.abort))
                 atomicOr(&g_stream_gemm_error, kErrFullWait);
             if constexpr (W4)
-                w4a8_tile_mma<NG, BPW, MP>(smem_u32(sm.w_tile(s)), smem_u32(sm.x_tile(s)), L, x_off, acci);
+                w4a8_tile_mma<NG, BPW, MP, CW>(smem_u32(sm.w_tile(s)), smem_u32(sm.x_tile(s)), L, x_off,
+                                               smem_u32(sm.xf) + (uint32_t)((i & 1) * (C::XfBytes / 2)), warp,
+                                               lane, acci);
             else
                 w8a8_tile_mma<NG, BPW, S8P>(smem_u32(sm.w_tile(s)), smem_u32(sm.x_tile(s)), L, acci);
             __syncwarp();

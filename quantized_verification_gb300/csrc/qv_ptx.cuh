@@ -170,6 +170,16 @@ __device__ __forceinline__ void allow_dependent_launch() {
 __device__ __forceinline__ void lds_v2_u32(uint32_t addr, uint32_t& r0, uint32_t& r1) {
     asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(addr));
 }
+// Four consecutive 32-bit words of shared memory (16-byte aligned address).
+__device__ __forceinline__ void lds_v4_u32(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                           uint32_t& r3) {
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
+}
+__device__ __forceinline__ void sts_v4_u32(uint32_t addr, uint32_t r0, uint32_t r1, uint32_t r2, uint32_t r3) {
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" :: "r"(addr), "r"(r0), "r"(r1), "r"(r2), "r"(r3)
+                 : "memory");
+}
 
 __device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& r0, uint32_t& r1,
                                             uint32_t& r2, uint32_t& r3) {
