@@ -41,8 +41,8 @@ FALLBACK_HBM_GBS = 6800.0
 # launch (4096 -> 24576, M = 5) over its algorithmic bytes. Valid only for the
 # kernel sources whose sha256 is recorded (kernel_source_sha); roofline.traffic
 # is null otherwise.
-NCU_TRAFFIC = {"source_sha256": "898062a35631d6031ba29eec4748142086f216488a64ef912c80f41d84058087",
-               "dram_bytes_per_algorithmic_byte": (101781248 + 2726400) / 101273620}
+NCU_TRAFFIC = {"source_sha256": "b9cc83a350ea7320eb4714ab31abaf08aa1b54e7060b86fa7f8b9732d3b8b90d",
+               "dram_bytes_per_algorithmic_byte": (101744896 + 2637824) / 101273620}
 
 
 def log(*a):
