@@ -87,6 +87,7 @@ class Oracle:
         L.qvo_pack_w4.argtypes = [_P, _I, _I, _P]
         L.qvo_unpack_w4.argtypes = [_P, _I, _I, _P]
         L.qvo_logit_fidelity.argtypes = [_P, _P, _I, _I, _P, _P, _P]
+        L.qvo_attention_verify.argtypes = [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, ctypes.c_double, _P]
         L.qvo_draw_index.restype = ctypes.c_int32
         L.qvo_draw_index.argtypes = [_P, _I, ctypes.c_uint64, ctypes.c_uint32]
 
@@ -343,6 +344,25 @@ class Oracle:
         """f4 with the a3 greedy argmax (lowest index on ties)."""
         return self.lm_head_argmax(xq, sx, self.unpack_w4(wq4), sw)
 
+
+    # -- f1': attention over a short KV cache --------------------------------
+    def attention_verify(self, qkv, kc, vc, lens, T: int, Hq: int, Hkv: int, D: int, scale: float):
+        """Causal grouped-query attention of the step's verify tokens over the
+        cache and the step's own keys, in binary64 from bf16 inputs (the
+        layer between the quantized linears: gist.science/ja summary,
+        section 2.2 item 3). qkv uint16 [B*T, (Hq+2Hkv)*D] (bf16 patterns),
+        kc, vc uint16 [B, Lmax, Hkv, D], lens int32 [B]. Returns float64
+        [B*T, Hq*D]."""
+        qkv = np.ascontiguousarray(qkv, dtype=np.uint16)
+        kc = np.ascontiguousarray(kc, dtype=np.uint16)
+        vc = np.ascontiguousarray(vc, dtype=np.uint16)
+        lens = np.ascontiguousarray(lens, dtype=np.int32)
+        B, Lmax = kc.shape[0], kc.shape[1]
+        assert qkv.shape == (B * T, (Hq + 2 * Hkv) * D) and kc.shape == (B, Lmax, Hkv, D) == vc.shape
+        out = np.empty((B * T, Hq * D), dtype=np.float64)
+        self._L.qvo_attention_verify(_ptr(qkv), _ptr(kc), _ptr(vc), _ptr(lens), B, T, Hq, Hkv, D, Lmax,
+                                     ctypes.c_double(scale), _ptr(out))
+        return out
 
     # -- f3': logit fidelity ------------------------------------------------
     def logit_fidelity(self, a: np.ndarray, b: np.ndarray):

@@ -52,6 +52,13 @@
  *       -- tree-structured verification named as an extension by the
  *          summaries (gist.science/de and gist.science/ja summaries,
  *          section 5); the acceptance rule is a4's applied along each path.
+ *   f1' attention over a short KV cache: for each verify token, grouped-query
+ *       scaled dot-product attention over the sequence's cached keys and
+ *       values and the step's own new ones up to and including itself
+ *       (causal) -- the decoder layer that the verify pass runs between the
+ *       quantized linears (gist.science/ja summary, section 2.2 item 3:
+ *       high-precision computation outside the INT8 GEMMs); the summaries
+ *       do not spell attention out, so this is the textbook form.
  *   f3' logit fidelity (diagnostic): KL(p || q) between the softmax of a
  *       reference verifier's logits (p) and of the quantized verifier's (q),
  *       and whether their top-1 tokens agree -- the summaries report that
@@ -750,4 +757,63 @@ void qvo_logit_fidelity(const float* a, const float* b, int64_t M, int64_t V,
         ta[m] = (int32_t)ia;
         tb[m] = (int32_t)ib;
     }
+}
+
+/* ------------------------------------------------------------------ */
+/* f1': attention over a short KV cache, in binary64                     */
+/* ------------------------------------------------------------------ */
+
+/*
+ * B sequences, each with T = gamma + 1 verify tokens. qkv holds, per token
+ * row m = b*T + j, the bf16 outputs of the qkv projection: Hq query heads,
+ * then Hkv key heads, then Hkv value heads, D values each (row stride
+ * (Hq + 2 Hkv) D). kc, vc: bf16 caches [B][Lmax][Hkv][D]; len[b] cached
+ * positions of sequence b. Query head h uses key/value head h / (Hq/Hkv).
+ * Token j of sequence b attends to the len[b] cached positions and to the
+ * step's tokens 0..j:
+ *   s_i = scale * sum_d q[d] k_i[d],  w_i = e^(s_i - max s) / sum e^(...),
+ *   out[m][h*D + d] = sum_i w_i v_i[d]     (binary64 throughout).
+ */
+void qvo_attention_verify(const uint16_t* qkv, const uint16_t* kc, const uint16_t* vc,
+                          const int32_t* len, int64_t B, int64_t T, int64_t Hq, int64_t Hkv,
+                          int64_t D, int64_t Lmax, double scale, double* out)
+{
+    const int64_t G = Hq / Hkv, W = (Hq + 2 * Hkv) * D;
+    double* s = (double*)malloc((size_t)(Lmax + T) * sizeof(double));
+    for (int64_t b = 0; b < B; ++b) {
+        const int64_t L = len[b];
+        for (int64_t j = 0; j < T; ++j) {
+            const uint16_t* row = qkv + (b * T + j) * W;
+            for (int64_t h = 0; h < Hq; ++h) {
+                const int64_t kh = h / G;
+                const uint16_t* q = row + h * D;
+                const int64_t n = L + j + 1;
+                double mx = -INFINITY;
+                for (int64_t i = 0; i < n; ++i) {
+                    const uint16_t* k = i < L ? kc + ((b * Lmax + i) * Hkv + kh) * D
+                                              : qkv + (b * T + (i - L)) * W + (Hq + kh) * D;
+                    double dot = 0.0;
+                    for (int64_t d = 0; d < D; ++d)
+                        dot += (double)qvo_bf16_to_f32(q[d]) * (double)qvo_bf16_to_f32(k[d]);
+                    s[i] = scale * dot;
+                    if (s[i] > mx) mx = s[i];
+                }
+                double z = 0.0;
+                for (int64_t i = 0; i < n; ++i) {
+                    s[i] = exp(s[i] - mx);
+                    z += s[i];
+                }
+                for (int64_t d = 0; d < D; ++d) {
+                    double acc = 0.0;
+                    for (int64_t i = 0; i < n; ++i) {
+                        const uint16_t* v = i < L ? vc + ((b * Lmax + i) * Hkv + kh) * D
+                                                  : qkv + (b * T + (i - L)) * W + (Hq + Hkv + kh) * D;
+                        acc += s[i] * (double)qvo_bf16_to_f32(v[d]);
+                    }
+                    out[(b * T + j) * Hq * D + h * D + d] = acc / z;
+                }
+            }
+        }
+    }
+    free(s);
 }

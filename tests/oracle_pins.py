@@ -741,6 +741,65 @@ def pin_fidelity_scipy(o):
     assert ta[2] == 17
 
 
+# ---------------------------------------------------------------------------
+# f1': attention over a short KV cache
+# ---------------------------------------------------------------------------
+
+def _attn_case(rng, B, T, Hq, Hkv, D, Lmax, lens):
+    f = lambda *s: _bf16_bits(np.round(rng.normal(0, 1, s) * 64).astype(np.float32) / np.float32(64))
+    return f(B * T, (Hq + 2 * Hkv) * D), f(B, Lmax, Hkv, D), f(B, Lmax, Hkv, D), np.array(lens, np.int32)
+
+
+def pin_attention_numpy(o):
+    """Against numpy matrix products and scipy's softmax over the visible
+    keys of each query (cache, then the step's tokens up to itself), with
+    query head h reading key/value head h // (Hq / Hkv)."""
+    from scipy.special import softmax
+    rng = np.random.default_rng(31)
+    B, T, Hq, Hkv, D, Lmax = 2, 3, 4, 2, 8, 5
+    qkv, kc, vc, lens = _attn_case(rng, B, T, Hq, Hkv, D, Lmax, [5, 2])
+    scale = float(np.float32(1.0) / np.sqrt(np.float32(D)))
+    out = o.attention_verify(qkv, kc, vc, lens, T, Hq, Hkv, D, scale)
+    w = lambda a: (a.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    Q = w(qkv[:, : Hq * D]).reshape(B, T, Hq, D)
+    Kn = w(qkv[:, Hq * D:(Hq + Hkv) * D]).reshape(B, T, Hkv, D)
+    Vn = w(qkv[:, (Hq + Hkv) * D:]).reshape(B, T, Hkv, D)
+    for b in range(B):
+        L = int(lens[b])
+        Kall = np.concatenate([w(kc[b, :L]), Kn[b]], axis=0)      # [L+T, Hkv, D]
+        Vall = np.concatenate([w(vc[b, :L]), Vn[b]], axis=0)
+        for j in range(T):
+            for h in range(Hq):
+                kh = h // (Hq // Hkv)
+                sc = scale * (Kall[: L + j + 1, kh] @ Q[b, j, h])
+                ref = softmax(sc) @ Vall[: L + j + 1, kh]
+                got = out[b * T + j, h * D:(h + 1) * D]
+                assert np.allclose(got, ref, rtol=1e-12, atol=1e-12), (b, j, h)
+
+
+def pin_attention_special_cases(o):
+    """One visible key returns its value exactly; equal keys average the
+    values; a later token's key and value never change an earlier token's
+    output."""
+    rng = np.random.default_rng(32)
+    B, T, Hq, Hkv, D, Lmax = 1, 3, 2, 1, 16, 4
+    qkv, kc, vc, lens = _attn_case(rng, B, T, Hq, Hkv, D, Lmax, [0])
+    out = o.attention_verify(qkv, kc, vc, lens, T, Hq, Hkv, D, 0.25)
+    v0 = (qkv[0, (Hq + Hkv) * D:].astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    assert np.array_equal(out[0, :D], v0) and np.array_equal(out[0, D:2 * D], v0)
+    qkv2, kc2, vc2, _ = _attn_case(rng, B, T, Hq, Hkv, D, Lmax, [4])
+    kc2[:] = kc2[0, 0]                                  # four equal cached keys, no new-key influence:
+    qkv2[:, Hq * D:(Hq + Hkv) * D] = kc2[0, 0, 0]       # the step's keys equal them too
+    out2 = o.attention_verify(qkv2, kc2, vc2, np.array([4], np.int32), T, Hq, Hkv, D, 0.25)
+    f = lambda a: (a.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    vals = np.concatenate([f(vc2[0, :4, 0]), f(qkv2[:1, (Hq + Hkv) * D:])], axis=0)
+    assert np.allclose(out2[0, :D], vals.mean(axis=0), rtol=1e-14, atol=1e-14)
+    qkv3 = qkv2.copy()
+    qkv3[2, Hq * D:] = qkv3[1, Hq * D:][::-1]           # change token 2's key and value
+    out3 = o.attention_verify(qkv3, kc2, vc2, np.array([4], np.int32), T, Hq, Hkv, D, 0.25)
+    assert np.array_equal(out3[:2], out2[:2]) and not np.array_equal(out3[2], out2[2])
+
+
 ALL_PINS = [
     pin_worked_example,
     pin_quantize_exact_rational,
@@ -770,4 +829,6 @@ ALL_PINS = [
     pin_w4_linear_bruteforce,
     pin_fidelity_closed_forms,
     pin_fidelity_scipy,
+    pin_attention_numpy,
+    pin_attention_special_cases,
 ]

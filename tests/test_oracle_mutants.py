@@ -71,6 +71,10 @@ MUTANTS = [
     ("kl_reversed", "s += exp(lp) * (lp - lq);", "s += exp(lq) * (lq - lp);"),
     ("kl_no_normalisation", "const double lp = (double)ar[v] - ma - lza;", "const double lp = (double)ar[v] - ma;"),
     ("fidelity_last_tie", "if (ar[v] > ar[ia]) ia = v;", "if (ar[v] >= ar[ia]) ia = v;"),
+    ("attention_not_causal", "const int64_t n = L + j + 1;", "const int64_t n = L + T;"),
+    ("attention_heads_interleaved", "const int64_t kh = h / G;", "const int64_t kh = h % Hkv;"),
+    ("attention_no_scale", "s[i] = scale * dot;", "s[i] = dot;"),
+    ("attention_values_from_keys", "(Hq + Hkv + kh) * D;\n                        acc", "(Hq + kh) * D;\n                        acc"),
     ("residual_not_added",
      "hr[k] = qvo_f32_to_bf16_rne(qvo_bf16_to_f32(hr[k]) + qvo_bf16_to_f32(d[m * H + k]));",
      "hr[k] = hr[k];"),
