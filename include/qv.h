@@ -384,6 +384,36 @@ QV_API qv_status qv_quantize_weight(const void* w, qv_dtype w_dtype, int N, int 
                              int8_t* wq, float* sw, cudaStream_t stream);
 
 /*
+ * qv_attention_verify -- attention over a short KV cache for the verify
+ * tokens: the attention between the qkv and o projections of the decoder
+ * layer that the verify pass runs (the non-GEMM computation stays in high
+ * precision: Quasar, gist.science/ja summary, section 2.2 item 3). The
+ * summaries do not spell attention out; this is causal grouped-query
+ * scaled dot-product attention.
+ *   qkv       [B*T][(Hq + 2 Hkv) * D] bf16 device, 16-byte aligned: the qkv
+ *             projection's rows (token-major, sequence-contiguous: row
+ *             b*T + j), Hq query heads, then Hkv key heads, then Hkv value
+ *             heads, D values each (no positional rotation is applied here)
+ *   k_cache, v_cache [B][Lmax][Hkv][D] bf16 device, 16-byte aligned (may be
+ *             NULL when Lmax == 0); cache_len [B] int32 device, each in
+ *             [0, Lmax] (values outside are clamped)
+ *   out       [B*T][Hq * D] fp32 device: for token j of sequence b and query
+ *             head h (key/value head h / (Hq/Hkv)), the softmax over the
+ *             cache_len[b] cached positions and the step's tokens 0..j of
+ *             scale * q . k, applied to the values
+ *   T * Hq/Hkv <= 32, D in {64, 128}, 1 <= B <= 65535, 0 <= Lmax <= 2^24
+ *   workspace qv_attention_workspace_bytes(B, T, Hq, Hkv, D, Lmax) bytes,
+ *             16-byte aligned, no initialisation needed (per-chunk partials)
+ * binary32 scores and sums (the products of bf16 values are exact): the
+ * outputs are within about 1e-5 of max |v| of the binary64 definition.
+ */
+QV_API size_t qv_attention_workspace_bytes(int B, int T, int Hq, int Hkv, int D, int Lmax);
+QV_API qv_status qv_attention_verify(const uint16_t* qkv, const uint16_t* k_cache, const uint16_t* v_cache,
+                                     const int32_t* cache_len, int B, int T, int Hq, int Hkv, int D,
+                                     int Lmax, float scale, float* out, void* workspace,
+                                     size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * qv_logit_fidelity -- diagnostic: how far the quantized verifier's output
  * distribution is from a reference verifier's, per row.
  *   The Quasar summaries report negligible KL divergence between the

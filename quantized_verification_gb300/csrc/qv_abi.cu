@@ -576,6 +576,52 @@ qv_status qv_spec_sample(const float* logits, const int32_t* draft, const float*
     return ok();
 }
 
+namespace {
+qv_status check_attention_shape(int B, int T, int Hq, int Hkv, int D, int Lmax) {
+    if (B < 1 || B > 65535) return fail(QV_ERR_INVALID_ARG, "B=%d outside [1, 65535]", B);
+    if (T < 1) return fail(QV_ERR_INVALID_ARG, "T=%d must be >= 1", T);
+    if (Hkv < 1 || Hkv > 65535 || Hq < Hkv || Hq % Hkv != 0)
+        return fail(QV_ERR_INVALID_ARG, "Hq=%d must be a positive multiple of Hkv=%d", Hq, Hkv);
+    if ((long long)T * (Hq / Hkv) > 32) return fail(QV_ERR_INVALID_ARG, "T * Hq / Hkv must be <= 32");
+    if (D != 64 && D != 128) return fail(QV_ERR_INVALID_ARG, "D=%d must be 64 or 128", D);
+    if (Lmax < 0 || Lmax > (1 << 24)) return fail(QV_ERR_INVALID_ARG, "Lmax=%d outside [0, 2^24]", Lmax);
+    return QV_OK;
+}
+}  // namespace
+
+size_t qv_attention_workspace_bytes(int B, int T, int Hq, int Hkv, int D, int Lmax) {
+    if (check_attention_shape(B, T, Hq, Hkv, D, Lmax) != QV_OK) return 0;
+    return (qv::attention_workspace_bytes(B, T, Hq, Hkv, D, Lmax) + 255) & ~size_t(255);
+}
+
+qv_status qv_attention_verify(const uint16_t* qkv, const uint16_t* k_cache, const uint16_t* v_cache,
+                              const int32_t* cache_len, int B, int T, int Hq, int Hkv, int D, int Lmax,
+                              float scale, float* out, void* workspace, size_t workspace_bytes,
+                              cudaStream_t stream) {
+    qv_status st = check_attention_shape(B, T, Hq, Hkv, D, Lmax);
+    if (st != QV_OK) return st;
+    if (!qkv || !cache_len || !out) return fail(QV_ERR_INVALID_ARG, "null pointer");
+    if (Lmax > 0 && (!k_cache || !v_cache)) return fail(QV_ERR_INVALID_ARG, "k_cache / v_cache null with Lmax > 0");
+    if (!(scale > 0.0f) || scale > 3.0e38f) return fail(QV_ERR_INVALID_ARG, "scale must be finite and > 0");
+    if (!aligned(qkv, 16) || (k_cache && !aligned(k_cache, 16)) || (v_cache && !aligned(v_cache, 16)) ||
+        !aligned(cache_len, 4) || !aligned(out, 4))
+        return fail(QV_ERR_INVALID_ARG, "qkv and the caches must be 16-byte aligned");
+    const size_t need = qv_attention_workspace_bytes(B, T, Hq, Hkv, D, Lmax);
+    if (!workspace) return fail(QV_ERR_WORKSPACE, "workspace is null (%zu bytes needed)", need);
+    if (!aligned(workspace, 16)) return fail(QV_ERR_WORKSPACE, "workspace must be 16-byte aligned");
+    if (workspace_bytes < need) return fail(QV_ERR_WORKSPACE, "workspace has %zu bytes, %zu needed", workspace_bytes, need);
+    QV_CHECK_DEV(qkv);
+    QV_CHECK_DEV(k_cache);
+    QV_CHECK_DEV(v_cache);
+    QV_CHECK_DEV(cache_len);
+    QV_CHECK_DEV(out);
+    QV_CHECK_DEV(workspace);
+    cudaError_t e = qv::launch_attention_verify(qkv, k_cache, v_cache, cache_len, B, T, Hq, Hkv, D, Lmax, scale, out,
+                                                workspace, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "qv_attention_verify launch");
+    return ok();
+}
+
 qv_status qv_logit_fidelity(const float* ref_logits, const float* logits, int M, int V, float* kl,
                             int32_t* top1_ref, int32_t* top1, cudaStream_t stream) {
     if (!ref_logits || !logits || !kl || !top1_ref || !top1) return fail(QV_ERR_INVALID_ARG, "null pointer");

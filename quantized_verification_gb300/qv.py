@@ -30,7 +30,8 @@ EXPORTS = ("qv_quantize_act", "qv_w8a8_linear", "qv_lm_head_argmax", "qv_accept"
            "qv_verify_stack", "qv_w8a8_linear_act", "qv_lm_head_argmax_act",
            "qv_rmsnorm_quant", "qv_swiglu_quant", "qv_w8a8_swiglu", "qv_spec_sample",
            "qv_tree_accept", "qv_quantize_weight_w4", "qv_w4a8_linear", "qv_w4a8_swiglu",
-           "qv_w4a8_lm_head_argmax", "qv_logit_fidelity")
+           "qv_w4a8_lm_head_argmax", "qv_logit_fidelity", "qv_attention_workspace_bytes",
+           "qv_attention_verify")
 MAX_STACK_M = 16
 
 
@@ -82,6 +83,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         L.qv_tree_accept.argtypes = [P, P, P, I, I, P, P, P, P]
         L.qv_quantize_weight_w4.argtypes = [P, I, I, I, P, P, P]
         L.qv_logit_fidelity.argtypes = [P, P, I, I, P, P, P, P]
+        L.qv_attention_workspace_bytes.argtypes = [I, I, I, I, I, I]
+        L.qv_attention_workspace_bytes.restype = S
+        L.qv_attention_verify.argtypes = [P, P, P, P, I, I, I, I, I, I, ctypes.c_float, P, P, S, P]
         L.qv_w4a8_linear.argtypes = [P, P, I, I, P, P, I, P, I, P, P, S, P]
         L.qv_w4a8_swiglu.argtypes = [P, P, I, I, P, P, I, P, P, S, P]
         L.qv_w4a8_lm_head_argmax.argtypes = [P, P, I, I, P, P, I, P, P, P, S, P]
@@ -301,6 +305,26 @@ def qv_logit_fidelity(ref_logits, logits, kl, top1_ref, top1, stream=None):
           top1.dtype == torch.int32, "top1_ref, top1 int32 [M]")
     _check(load().qv_logit_fidelity(_ptr(ref_logits), _ptr(logits), M, V, _ptr(kl), _ptr(top1_ref), _ptr(top1),
                                     ctypes.c_void_p(_stream(stream))))
+
+
+def qv_attention_workspace_bytes(B, T, Hq, Hkv, D, Lmax) -> int:
+    return int(load().qv_attention_workspace_bytes(B, T, Hq, Hkv, D, Lmax))
+
+
+def qv_attention_verify(qkv, k_cache, v_cache, cache_len, T, Hq, Hkv, scale, out, workspace, stream=None):
+    """Causal grouped-query attention of the verify tokens over the KV cache
+    and the step's own keys: qkv [B*T, (Hq+2Hkv)*D] bf16, k_cache / v_cache
+    [B, Lmax, Hkv, D] bf16, cache_len [B] int32 -> out [B*T, Hq*D] fp32."""
+    B, Lmax, hkv, D = k_cache.shape
+    _need(hkv == Hkv and v_cache.shape == k_cache.shape, "k_cache, v_cache must be [B, Lmax, Hkv, D]")
+    _need(qkv.dtype == torch.bfloat16 and qkv.shape == (B * T, (Hq + 2 * Hkv) * D), "qkv bf16 [B*T, (Hq+2Hkv)*D]")
+    _need(k_cache.dtype == torch.bfloat16 and v_cache.dtype == torch.bfloat16, "bf16 caches")
+    _need(cache_len.shape == (B,) and cache_len.dtype == torch.int32, "cache_len int32 [B]")
+    _need(out.shape == (B * T, Hq * D) and out.dtype == torch.float32, "out float32 [B*T, Hq*D]")
+    _check(load().qv_attention_verify(_ptr(qkv), _ptr(k_cache) if Lmax > 0 else None,
+                                      _ptr(v_cache) if Lmax > 0 else None, _ptr(cache_len), B, T, Hq, Hkv, D, Lmax,
+                                      ctypes.c_float(scale), _ptr(out), _ptr(workspace), workspace.numel(),
+                                      ctypes.c_void_p(_stream(stream))))
 
 
 # --- W4A8: packed int4 weights [N, K/2] uint8 (even k in the low nibble) ---

@@ -104,6 +104,16 @@ def test_host_validation_without_gpu(lib):
     assert lib.qv_quantize_weight_w4(fake, 0, 8, 48, fake, fake, None) == qv.QV_ERR_INVALID_ARG
     assert lib.qv_quantize_weight_w4(fake, 5, 8, 64, fake, fake, None) == qv.QV_ERR_INVALID_ARG
     assert lib.qv_quantize_weight_w4(fake, 0, 8, 64, P(0x1008), fake, None) == qv.QV_ERR_INVALID_ARG
+    # attention over a short KV cache
+    F32 = ctypes.c_float
+    assert lib.qv_attention_verify(None, fake, fake, fake, 1, 5, 32, 8, 128, 16, F32(0.1), fake, fake, 1 << 22, None) == qv.QV_ERR_INVALID_ARG
+    assert lib.qv_attention_verify(fake, fake, fake, fake, 1, 9, 32, 8, 128, 16, F32(0.1), fake, fake, 1 << 22, None) == qv.QV_ERR_INVALID_ARG
+    assert lib.qv_attention_verify(fake, None, fake, fake, 1, 5, 32, 8, 128, 16, F32(0.1), fake, fake, 1 << 22, None) == qv.QV_ERR_INVALID_ARG
+    assert lib.qv_attention_verify(fake, fake, fake, fake, 1, 5, 32, 8, 128, 16, F32(0.0), fake, fake, 1 << 22, None) == qv.QV_ERR_INVALID_ARG
+    assert lib.qv_attention_verify(fake, fake, fake, fake, 1, 5, 32, 8, 128, 16, F32(0.1), fake, fake, 16, None) == qv.QV_ERR_WORKSPACE
+    assert lib.qv_attention_verify(P(0x1008), fake, fake, fake, 1, 5, 32, 8, 128, 16, F32(0.1), fake, fake, 1 << 22, None) == qv.QV_ERR_INVALID_ARG
+    # four 128-key chunks for 500 cached + 5 new keys; 20 rows of 130 floats each
+    assert qv.qv_attention_workspace_bytes(1, 5, 32, 8, 128, 500) == (8 * 4 * 20 * 130 * 4 + 255) // 256 * 256
     # logit fidelity
     assert lib.qv_logit_fidelity(None, fake, 2, 10, fake, fake, fake, None) == qv.QV_ERR_INVALID_ARG
     assert lib.qv_logit_fidelity(fake, fake, 0, 10, fake, fake, fake, None) == qv.QV_ERR_INVALID_ARG
@@ -115,7 +125,6 @@ def test_host_validation_without_gpu(lib):
     assert lib.qv_tree_accept(fake, fake, fake, 0, 16, fake, fake, None, None) == qv.QV_ERR_INVALID_ARG
     assert lib.qv_tree_accept(fake, P(0x1002), fake, 1, 16, fake, fake, None, None) == qv.QV_ERR_INVALID_ARG
     # speculative sampling at T > 0
-    F32 = ctypes.c_float
     U64 = ctypes.c_uint64
     assert lib.qv_spec_sample(None, fake, fake, 1, 4, 1000, F32(1.0), U64(1), fake, fake, fake, 1 << 20, None) == qv.QV_ERR_INVALID_ARG
     assert lib.qv_spec_sample(fake, None, fake, 1, 4, 1000, F32(1.0), U64(1), fake, fake, fake, 1 << 20, None) == qv.QV_ERR_INVALID_ARG
