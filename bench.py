@@ -508,6 +508,43 @@ def main():
         del tg, tstack
         torch.cuda.empty_cache()
 
+    # ---- attention over a short KV cache (qv_attention_verify) for the
+    # step's verify tokens, every layer, at a 2048-position cache
+    attention = None
+    if rank == 0:
+        try:
+            D_ = 128
+            Hq_, Hkv_ = stack.model.get("q", stack.model["hidden"]) // D_, stack.model["kv"] // D_
+            T_, L_ = stack.gamma + 1, 2048
+            ga = torch.Generator(device=dev).manual_seed(11)
+            qkv_a = torch.randn(T_, (Hq_ + 2 * Hkv_) * D_, device=dev, generator=ga).to(torch.bfloat16)
+            kcs = [torch.randn(1, L_, Hkv_, D_, device=dev, generator=ga).to(torch.bfloat16) for _ in range(stack.layers)]
+            vcs = [torch.randn(1, L_, Hkv_, D_, device=dev, generator=ga).to(torch.bfloat16) for _ in range(stack.layers)]
+            ln_a = torch.full((1,), L_, dtype=torch.int32, device=dev)
+            ws_a = torch.empty(qv.qv_attention_workspace_bytes(1, T_, Hq_, Hkv_, D_, L_), dtype=torch.uint8, device=dev)
+            out_a = torch.empty(T_, Hq_ * D_, device=dev)
+            sc = float(1.0 / (D_ ** 0.5))
+
+            def attn_seq(s):
+                for l in range(stack.layers):
+                    qv.qv_attention_verify(qkv_a, kcs[l], vcs[l], ln_a, T_, Hq_, Hkv_, sc, out_a, ws_a, stream=s)
+            ga_graph = VerifyStack._capture(attn_seq, dev)
+            for _ in range(3):
+                ga_graph.replay()
+            torch.cuda.synchronize()
+            a_ms = time_graph(torch, ga_graph, 10, stream)
+            kv_b = 2 * L_ * Hkv_ * D_ * 2
+            attention = {"context": L_, "tokens": T_, "heads": [Hq_, Hkv_, D_], "us_per_layer": a_ms * 1e3 / stack.layers,
+                         "us_per_step": a_ms * 1e3, "kv_bytes_per_layer": kv_b,
+                         "kv_gbs": kv_b * stack.layers / (a_ms * 1e-3) / 1e9,
+                         "note": "not part of the timed step (its attention input is seeded); the layers' attention "
+                                 "over a 2048-position bf16 cache, qv_attention_verify, one CUDA graph"}
+            log(f"attention at L={L_}: {attention['us_per_layer']:.2f} us per layer")
+            del ga_graph, kcs, vcs
+            torch.cuda.empty_cache()
+        except Exception as exc:      # a measurement of an extra row must not lose the bench line
+            log(f"attention timing skipped: {exc}")
+
     # ---- W4A8: the same step with packed int4 weights (half the weight
     # bytes), and its streaming GEMM over the step's 144 projections
     w4a8 = None
@@ -602,6 +639,7 @@ def main():
             "tree_verify": tree,
             "w4a8": w4a8,
             "logit_fidelity": fidelity,
+            "attention_kv_cache": attention,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
