@@ -41,7 +41,7 @@ FALLBACK_HBM_GBS = 6800.0
 # launch (4096 -> 24576, M = 5) over its algorithmic bytes. Valid only for the
 # kernel sources whose sha256 is recorded (kernel_source_sha); roofline.traffic
 # is null otherwise.
-NCU_TRAFFIC = {"source_sha256": "b9cc83a350ea7320eb4714ab31abaf08aa1b54e7060b86fa7f8b9732d3b8b90d",
+NCU_TRAFFIC = {"source_sha256": "41d8daf06b7eb34414e0e3f24de057504abba4fdb22b3e914438d39cd5a6732b",
                "dram_bytes_per_algorithmic_byte": (101744896 + 2637824) / 101273620}
 
 
