@@ -3,8 +3,9 @@ profiler's launch list or a per-kernel capture.
 
     python -m quantized_verification_gb300.tour [--passes 2]
 
-Each pass makes the same 15 launches in the same order (the first pass is
-the warm-up a capture skips with ``-s 15``):
+Each pass makes the same 18 launches in the same order (the first pass is
+the warm-up a capture skips with ``-s 18``; a capture filtered with ``-k``
+skips the matching launches of one pass):
 
     quantize_rows_kernel                  per-token int8 activation codes, 5 x 4096
     w8a8_stream_kernel<1, Linear>         5 x 4096 -> 24576 (Qwen3-8B gate+up), fp32 out
@@ -17,9 +18,12 @@ the warm-up a capture skips with ``-s 15``):
     spec_{max,sums,decide,chunk,draw}     sampling at T > 0, 1 x (4 + 1) rows x 151936
     tree_accept_kernel                    a 16-node draft tree
     accept_kernel                         greedy acceptance, 1 x 5
+    attn_chunk_kernel, attn_combine_kernel attention of 5 tokens over a 2048-position
+                                          cache, 32/8 heads, D = 128
+    logit_fidelity_kernel                 KL and top-1 of 5 rows x 151936 logits
 
 Inputs are seeded and synthetic and sit on the device before the first
-launch; the whole run holds about 0.5 GB.
+launch; the whole run holds about 0.6 GB.
 """
 import argparse
 
@@ -27,7 +31,7 @@ import torch
 
 from . import build, qv, synth
 
-LAUNCHES_PER_PASS = 15
+LAUNCHES_PER_PASS = 18
 
 
 def main(argv=None):
@@ -78,6 +82,17 @@ def main(argv=None):
     tl = torch.empty(1, dtype=torch.int32, device=dev)
     to = torch.empty(1, 16, dtype=torch.int32, device=dev)
     vt = torch.randint(0, 100, (B, gm + 1), dtype=torch.int32, device=dev, generator=g)
+    Hq, Hkv, D, L = 32, 8, 128, 2048
+    qkv = torch.randn(gm + 1, (Hq + 2 * Hkv) * D, device=dev, generator=g).to(torch.bfloat16)
+    kc = torch.randn(1, L, Hkv, D, device=dev, generator=g).to(torch.bfloat16)
+    vc = torch.randn(1, L, Hkv, D, device=dev, generator=g).to(torch.bfloat16)
+    kv_len = torch.full((1,), L, dtype=torch.int32, device=dev)
+    wsa = torch.empty(qv.qv_attention_workspace_bytes(1, gm + 1, Hq, Hkv, D, L), dtype=torch.uint8, device=dev)
+    attn = torch.empty(gm + 1, Hq * D, device=dev)
+    logits2 = logits + torch.randn(logits.shape, device=dev, generator=g) * 0.1
+    kl = torch.empty(B * (gm + 1), device=dev)
+    t1 = torch.empty(B * (gm + 1), dtype=torch.int32, device=dev)
+    t2 = torch.empty(B * (gm + 1), dtype=torch.int32, device=dev)
     for _ in range(args.passes):
         qv.qv_quantize_act(x, xq, sx)
         qv.qv_w8a8_linear(xq, sx, wq, sw, y, ws)
@@ -90,6 +105,8 @@ def main(argv=None):
         qv.qv_spec_sample(logits, drafts, q, 0.8, 7, ln, out, wss)
         qv.qv_tree_accept(tt, td, tp, tl, to)
         qv.qv_accept(vt, drafts, ln, out)
+        qv.qv_attention_verify(qkv, kc, vc, kv_len, gm + 1, Hq, Hkv, 1.0 / D ** 0.5, attn, wsa)
+        qv.qv_logit_fidelity(logits, logits2, kl, t1, t2)
         torch.cuda.synchronize()
     print(f"ok: {LAUNCHES_PER_PASS} launches per pass, {args.passes} passes")
 
