@@ -112,10 +112,25 @@ __device__ __forceinline__ double block_sum_squares(FF v, FF* red, double* total
 }
 
 __device__ __forceinline__ uint32_t pack_codes4(float a, float b, float c, float d, float s, float r) {
-    return (uint32_t)(uint8_t)(int8_t)quant_code(a, s, r) |
-           ((uint32_t)(uint8_t)(int8_t)quant_code(b, s, r) << 8) |
-           ((uint32_t)(uint8_t)(int8_t)quant_code(c, s, r) << 16) |
-           ((uint32_t)(uint8_t)(int8_t)quant_code(d, s, r) << 24);
+    // the fast rule for all four, the IEEE quotient only near a half-integer
+    const float e[4] = {a, b, c, d};
+    int q[4];
+    unsigned near_mask = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        bool nb;
+        q[j] = quant_code_fast(e[j], r, nb);
+        near_mask |= (unsigned)nb << j;
+    }
+    if (s == 0.f) {
+        return 0u;
+    } else if (near_mask) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            if ((near_mask >> j) & 1u) q[j] = quant_code_exact(e[j], s);
+    }
+    return (uint32_t)(uint8_t)(int8_t)q[0] | ((uint32_t)(uint8_t)(int8_t)q[1] << 8) |
+           ((uint32_t)(uint8_t)(int8_t)q[2] << 16) | ((uint32_t)(uint8_t)(int8_t)q[3] << 24);
 }
 
 __global__ void __launch_bounds__(kLayerThreads)

@@ -57,13 +57,30 @@ __device__ __forceinline__ void apply_mul(float (&e)[E], const float* __restrict
 
 template <int E>
 __device__ __forceinline__ void store_codes(int8_t* qr, int v, const float (&e)[E], float s, float r) {
+    // fast rule for every element, the IEEE quotient only where some element
+    // of the vector lies near a half-integer (rare)
+    int c[E];
+    unsigned near_mask = 0;
+#pragma unroll
+    for (int j = 0; j < E; ++j) {
+        bool nb;
+        c[j] = quant_code_fast(e[j], r, nb);
+        near_mask |= (unsigned)nb << j;
+    }
+    if (s == 0.f) {
+#pragma unroll
+        for (int j = 0; j < E; ++j) c[j] = 0;
+    } else if (near_mask) {
+#pragma unroll
+        for (int j = 0; j < E; ++j)
+            if ((near_mask >> j) & 1u) c[j] = quant_code_exact(e[j], s);
+    }
     uint32_t packed[E / 4];
 #pragma unroll
     for (int w = 0; w < E / 4; ++w) {
         uint32_t word = 0;
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-            word |= (uint32_t)(uint8_t)(int8_t)quant_code(e[4 * w + j], s, r) << (8 * j);
+        for (int j = 0; j < 4; ++j) word |= (uint32_t)(uint8_t)(int8_t)c[4 * w + j] << (8 * j);
         packed[w] = word;
     }
     if constexpr (E == 8)
@@ -81,7 +98,7 @@ __device__ __forceinline__ void store_codes(int8_t* qr, int v, const float (&e)[
 template <bool BF16, int NT, int REGV, class Sync>
 __device__ __forceinline__ float quantize_row(const uint4* __restrict__ xr, int nvec,
                                               const float* __restrict__ mul, int8_t* __restrict__ qr,
-                                              int t, float* red, Sync sync) {
+                                              int t, float* red, Sync sync, int slice = -1) {
     using V = Vec<BF16>;
     constexpr int E = V::E;
     const bool in_regs = nvec <= NT * REGV;
@@ -126,12 +143,20 @@ __device__ __forceinline__ float quantize_row(const uint4* __restrict__ xr, int 
 #pragma unroll
         for (int u = 0; u < REGV; ++u) {
             const int v = t + u * NT;
-            if (v < nvec) {
+            if (v < nvec && (slice < 0 || u == slice)) {
                 float e[E];
                 V::unpack(rv[u], e);
                 apply_mul<E>(e, mul, v);
                 store_codes<E>(qr, v, e, s, r);
             }
+        }
+    } else if (slice >= 0) {
+        const int v = slice * NT + t;
+        if (v < nvec) {
+            float e[E];
+            V::unpack(__ldg(xr + v), e);
+            apply_mul<E>(e, mul, v);
+            store_codes<E>(qr, v, e, s, r);
         }
     } else {
         for (int v = t; v < nvec; v += NT) {

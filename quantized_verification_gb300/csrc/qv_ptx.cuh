@@ -248,6 +248,27 @@ static __device__ __noinline__ int quant_code_div(float x, float s) {
     const int qi = __float2int_rn(rintf(__fdiv_rn(x, s)));
     return qi > 127 ? 127 : (qi < -127 ? -127 : qi);
 }
+// The fast rule alone, for callers that batch the rare exact decisions: t is
+// rounded half-even by adding and removing 1.5 * 2^23 (exact for |t| < 2^22;
+// here |t| <= 127 (1 + 2^-22) unless s is subnormal, when r and t overflow and
+// `near` is set), the code is read from the sum's low bits and clamped, and
+// `near` is set when t lies within 2^-20 |t| of a half-integer (or is not
+// finite): the caller must then take quant_code_exact(x, s) instead.
+__device__ __forceinline__ int quant_code_fast(float x, float r, bool& near) {
+    const float t = __fmul_rn(x, r);
+    const float y = __fadd_rn(t, 12582912.0f);
+    const float n = __fsub_rn(y, 12582912.0f);
+    const float margin = __fsub_rn(0.5f, fabsf(__fsub_rn(t, n)));
+    near = !(margin > __fmul_rn(fabsf(t), 0x1p-20f));
+    const int qi = __float_as_int(y) - 0x4B400000;
+    return qi > 127 ? 127 : (qi < -127 ? -127 : qi);
+}
+// The IEEE-quotient decision, inline (callers branch to it rarely).
+__device__ __forceinline__ int quant_code_exact(float x, float s) {
+    const int qi = __float2int_rn(rintf(__fdiv_rn(x, s)));
+    return qi > 127 ? 127 : (qi < -127 ? -127 : qi);
+}
+
 __device__ __forceinline__ int quant_code(float x, float s, float r) {
     if (s == 0.f) return 0;
     const float t = __fmul_rn(x, r);
