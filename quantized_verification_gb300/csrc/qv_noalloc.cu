@@ -4,6 +4,7 @@
 // looks up its device address once per device, clears the part a call uses and
 // hands it to qv_w8a8_linear as the workspace.
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstdio>
@@ -23,30 +24,65 @@ namespace {
 // be handed to a kernel.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[QV_NOALLOC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
-void* g_scratch_ptr[kMaxDevices] = {nullptr};
+// Device address of the scratch buffer, per (device, context): a context
+// that is destroyed and created again (cudaDeviceReset, or the primary
+// context released and retained anew) loads the module again, and the
+// address may change, so the lookup is repeated whenever the current
+// context differs from the one the cached address came from.
+struct ScratchEntry {
+    int dev = -1;
+    CUcontext ctx = nullptr;
+    void* ptr = nullptr;
+};
+constexpr int kMaxEntries = 64;
+ScratchEntry g_entries[kMaxEntries];
 std::mutex g_scratch_mu;
+using PFN_ctxGetCurrent = CUresult (*)(CUcontext*);
+PFN_ctxGetCurrent g_ctx_get_current = nullptr;
 
-// Device address of the scratch buffer on the current device (looked up once
-// per device, with that device current).
+qv_status fail_cuda(const char* what, cudaError_t e) {
+    char msg[200];
+    snprintf(msg, sizeof msg, "qv_w8a8_linear_noalloc: %s: %s", what, cudaGetErrorString(e));
+    return qv::report_error(QV_ERR_CUDA, msg);
+}
+
+// Device address of the scratch buffer for the current device and context
+// (looked up with that device current, once per context).
 qv_status scratch_address(void** out) {
     int dev = -1;
     cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices)
-        return qv::report_error(QV_ERR_CUDA, "qv_w8a8_linear_noalloc: no usable current device");
+    if (e != cudaSuccess || dev < 0) return fail_cuda("no usable current device", e);
+    // make the device's primary context current (it is created if need be;
+    // nothing is allocated)
+    e = cudaSetDevice(dev);
+    if (e != cudaSuccess) return fail_cuda("context set-up failed", e);
     std::lock_guard<std::mutex> lk(g_scratch_mu);
-    if (!g_scratch_ptr[dev]) {
+    if (!g_ctx_get_current) {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        e = cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 12000, cudaEnableDefault, &q);
+        if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
+            return qv::report_error(QV_ERR_CUDA, "qv_w8a8_linear_noalloc: cuCtxGetCurrent is not available");
+        g_ctx_get_current = reinterpret_cast<PFN_ctxGetCurrent>(fn);
+    }
+    CUcontext ctx = nullptr;
+    if (g_ctx_get_current(&ctx) != CUDA_SUCCESS || !ctx)
+        return qv::report_error(QV_ERR_CUDA, "qv_w8a8_linear_noalloc: no current context");
+    ScratchEntry* slot = nullptr;
+    for (int i = 0; i < kMaxEntries; ++i) {
+        if (g_entries[i].dev == dev) { slot = &g_entries[i]; break; }
+        if (!slot && g_entries[i].dev < 0) slot = &g_entries[i];
+    }
+    if (!slot) return qv::report_error(QV_ERR_CUDA, "qv_w8a8_linear_noalloc: too many devices");
+    if (slot->dev != dev || slot->ctx != ctx || !slot->ptr) {
         void* p = nullptr;
         e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-        if (e != cudaSuccess || !p) {
-            char msg[160];
-            snprintf(msg, sizeof msg, "qv_w8a8_linear_noalloc: cudaGetSymbolAddress failed: %s",
-                     cudaGetErrorString(e));
-            return qv::report_error(QV_ERR_CUDA, msg);
-        }
-        g_scratch_ptr[dev] = p;
+        if (e != cudaSuccess || !p) return fail_cuda("cudaGetSymbolAddress failed", e);
+        slot->dev = dev;
+        slot->ctx = ctx;
+        slot->ptr = p;
     }
-    *out = g_scratch_ptr[dev];
+    *out = slot->ptr;
     return QV_OK;
 }
 
@@ -70,14 +106,12 @@ extern "C" qv_status qv_w8a8_linear_noalloc(const int8_t* xq, const float* sx, i
     void* scratch = nullptr;
     qv_status st = scratch_address(&scratch);
     if (st != QV_OK) return st;
-    // The GEMM needs a zero-filled workspace; clear what this call uses.
+    // The GEMM needs a zero-filled workspace. A call that completes leaves
+    // its part zeroed, but one that gave up on a wait limit (qv_device_error)
+    // can leave partial sums behind, and the caller has no way to clear this
+    // buffer: so every call clears what it uses, in stream order, first.
     cudaError_t e = cudaMemsetAsync(scratch, 0, need, stream);
-    if (e != cudaSuccess) {
-        char msg[160];
-        snprintf(msg, sizeof msg, "qv_w8a8_linear_noalloc: clearing the scratch failed: %s",
-                 cudaGetErrorString(e));
-        return qv::report_error(QV_ERR_CUDA, msg);
-    }
+    if (e != cudaSuccess) return fail_cuda("clearing the scratch failed", e);
     return qv_w8a8_linear(xq, sx, M, K, wq, sw, N, y, y_dtype, acc_debug, scratch,
                           QV_NOALLOC_SCRATCH_BYTES, stream);
 }

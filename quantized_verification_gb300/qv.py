@@ -31,7 +31,7 @@ EXPORTS = ("qv_quantize_act", "qv_w8a8_linear", "qv_lm_head_argmax", "qv_accept"
            "qv_rmsnorm_quant", "qv_swiglu_quant", "qv_w8a8_swiglu", "qv_spec_sample",
            "qv_tree_accept", "qv_quantize_weight_w4", "qv_w4a8_linear", "qv_w4a8_swiglu",
            "qv_w4a8_lm_head_argmax", "qv_logit_fidelity", "qv_attention_workspace_bytes",
-           "qv_attention_verify")
+           "qv_attention_verify", "qv_debug_set_slot_wait_ns", "qv_debug_drop_partials")
 MAX_STACK_M = 16
 
 
@@ -94,6 +94,10 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         L.qv_last_error.argtypes = []
         L.qv_last_error.restype = ctypes.c_char_p
         L.qv_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint)]
+        L.qv_debug_set_slot_wait_ns.argtypes = [ctypes.c_ulonglong]
+        L.qv_debug_set_slot_wait_ns.restype = None
+        L.qv_debug_drop_partials.argtypes = [I]
+        L.qv_debug_drop_partials.restype = None
         L.qv_num_sms.argtypes = []
         L.qv_num_sms.restype = I
         for name in ("qv_quantize_act", "qv_w8a8_linear", "qv_lm_head_argmax", "qv_accept",
@@ -274,7 +278,10 @@ def qv_w8a8_linear_noalloc(xq, sx, wq, sw, y, acc_debug=None, stream=None):
     N = wq.shape[0]
     _need(wq.shape == (N, K) and wq.dtype == torch.int8 and xq.dtype == torch.int8, "int8 xq [M,K], wq [N,K]")
     _need(sx.shape == (M,) and sw.shape == (N,), "sx [M], sw [N]")
+    _need(sx.dtype == torch.float32 and sw.dtype == torch.float32, "scales must be float32")
     _need(y.shape == (M, N), "y must be [M, N]")
+    if acc_debug is not None:
+        _need(acc_debug.shape == (M, N) and acc_debug.dtype == torch.int32, "acc_debug int32 [M, N]")
     _check(load().qv_w8a8_linear_noalloc(_ptr(xq), _ptr(sx), M, K, _ptr(wq), _ptr(sw), N, _ptr(y),
                                          _dtype(y), _ptr(acc_debug), ctypes.c_void_p(_stream(stream))))
 
@@ -475,6 +482,19 @@ def qv_device_error() -> int:
     code = ctypes.c_uint(0)
     _check(load().qv_device_error(ctypes.byref(code)))
     return int(code.value)
+
+
+QV_DEVICE_ERR_SLOT_WAIT = 32
+
+
+def qv_debug_set_slot_wait_ns(ns: int):
+    """Test hook: the split-K head's wait limit in later streaming launches (0 = default)."""
+    load().qv_debug_set_slot_wait_ns(int(ns))
+
+
+def qv_debug_drop_partials(n: int):
+    """Test hook: the next n streaming launches publish no split-K partial sums."""
+    load().qv_debug_drop_partials(int(n))
 
 
 def qv_num_sms() -> int:
