@@ -133,8 +133,19 @@ QV_API qv_status qv_quantize_act(const void* x, qv_dtype x_dtype, int M, int K,
  *     it zero-filled again when its work completes, so one workspace can be
  *     reused by any sequence of stream-ordered calls. Calls that run
  *     concurrently (different streams) need separate workspaces.
+ *     Recovery: a call that gives up on a wait limit (qv_device_error then
+ *     reports QV_DEVICE_ERR_SLOT_WAIT) has undefined outputs and may leave
+ *     partial sums in its workspace; zero-fill the workspace again before
+ *     the next call that uses it.
  *   1 <= M <= QV_MAX_M, N >= 1. Codes of -128 are accepted; the sums are
  *   exact whenever they fit int32, which codes in [-127, 127] guarantee.
+ *   Co-residency: the kernel runs at most one CTA per SM (no more CTAs than
+ *   SMs), and where a channel tile's K range is split between CTAs, the CTA
+ *   holding the tile's first K block waits at the end for the others'
+ *   partial sums. It therefore expects all of its CTAs to run at the same
+ *   time: if a kernel on another stream (or another process under MPS)
+ *   holds SMs for longer than the wait limit (about one second), the call
+ *   gives up with QV_DEVICE_ERR_SLOT_WAIT instead of waiting forever.
  */
 QV_API qv_status qv_w8a8_linear(const int8_t* xq, const float* sx, int M, int K,
                          const int8_t* wq, const float* sw, int N,
@@ -563,7 +574,29 @@ QV_API const char* qv_last_error(void);
  * undefined outputs. 0 means no such event since the last read.
  * Synchronizes the current device. Host function.
  */
+#define QV_DEVICE_ERR_FULL_WAIT  1u   /* a consumer waited too long for a tile    */
+#define QV_DEVICE_ERR_EMPTY_WAIT 2u   /* the producer waited too long for a slot  */
+#define QV_DEVICE_ERR_DRAIN_WAIT 4u   /* copies still in flight at the kernel end */
+#define QV_DEVICE_ERR_GRID_WAIT  8u   /* a grid barrier of qv_verify_stack        */
+#define QV_DEVICE_ERR_TC_WAIT    16u  /* the tensor-core pipeline (large M)       */
+#define QV_DEVICE_ERR_SLOT_WAIT  32u  /* a split-K head waited for partial sums   */
 QV_API qv_status qv_device_error(unsigned int* code);
+
+/*
+ * Test hooks. They let a test make a bounded in-kernel wait run out, without
+ * faulting or hanging the GPU, and check the error reporting and the
+ * recovery rule above; production code leaves them alone. Host functions;
+ * they affect calls enqueued (or captured) after them, on every thread.
+ *   qv_debug_set_slot_wait_ns(ns): limit, in ns of %globaltimer, of the
+ *     split-K head's wait for partial sums in the streaming kernels of
+ *     qv_w8a8_linear / qv_w8a8_swiglu / qv_lm_head_argmax and the W4A8 calls
+ *     (up to 32 token rows per launch); 0 restores the default (1 s).
+ *   qv_debug_drop_partials(n): the next n such launches publish no split-K
+ *     partial sums, so every split tile's head waits out its limit, sets
+ *     QV_DEVICE_ERR_SLOT_WAIT and finishes with incomplete sums.
+ */
+QV_API void qv_debug_set_slot_wait_ns(unsigned long long ns);
+QV_API void qv_debug_drop_partials(int n);
 
 /* Number of SMs the kernels size their grids for on the current device
  * (queried once per device). Host function. */
@@ -593,11 +626,18 @@ QV_API int qv_num_sms(void);
  *     larger than the buffer are rejected with QV_ERR_UNSUPPORTED. With the
  *     present workspace layout (split-K slots of at most 10.5 MB, at M > 32)
  *     every shape that qv_w8a8_linear accepts fits.
+ *   - The address is looked up again when the current context of the device
+ *     changes (after cudaDeviceReset the module, and the buffer, are loaded
+ *     anew).
  *   - Each call clears the part of the buffer it uses (cudaMemsetAsync on
- *     `stream`) before its kernel runs. All calls on a device share the one
- *     buffer: calls whose GPU work overlaps (different streams, no ordering
- *     between them) race on it and give wrong results. Order them on one
- *     stream, or use qv_w8a8_linear with a workspace per stream.
+ *     `stream`, 1.3 MB for up to 8 token rows, 10.5 MB above 32) before its
+ *     kernel runs: a completed call leaves that part zeroed, but a call that
+ *     gave up on a wait limit (qv_device_error reports it) may leave partial
+ *     sums behind, and the caller has no other way to clear the buffer.
+ *   - All calls on a device share the one buffer: calls whose GPU work
+ *     overlaps (different streams, no ordering between them) race on it and
+ *     give wrong results. Order them on one stream, or use qv_w8a8_linear
+ *     with a workspace per stream.
  */
 QV_API qv_status qv_w8a8_linear_noalloc(const int8_t* xq, const float* sx, int M, int K,
                                         const int8_t* wq, const float* sw, int N,

@@ -28,11 +28,15 @@
 //    through the f16 m16n8k16 MMA; products are at most 128^2 = 2^14, one
 //    tile sums 128 of them (|sum| <= 2^21), so every fp32 partial is an
 //    exact integer; after each tile it is converted to int32 and added.
-//  - A channel tile whose K range is split over CTAs is combined with int32
-//    atomic adds into the workspace (exact, so order does not matter); the
-//    CTA whose contribution completes the tile runs the epilogue, reading and
-//    zeroing the sums in one atomic exchange, so the workspace is left zeroed.
-//    No CTA ever waits for another.
+//  - A channel tile whose K range is split over CTAs is combined through
+//    per-CTA slots of tagged 64-bit words (stream_common.cuh): the segment
+//    that starts at K-tile 0 (the head, the last segment of its CTA) waits,
+//    with a 1 s %globaltimer limit, for the partial sums that the later CTAs
+//    covering the rest of the tile publish into their slots, adds them
+//    (exact integer sums), zeroes the slots and runs the epilogue, so the
+//    workspace is left zeroed. A CTA only ever waits on CTAs with a higher
+//    index, which publish before they wait on anything; a wait that runs
+//    out sets kErrSlotWait in the device error word.
 //  - The LM head reduces each finished channel tile to one 64-bit key per
 //    token, (order-preserving bits of y) << 32 | (0xFFFFFFFF - v), combined
 //    with atomicMax: the largest key is the largest logit and, among equal
@@ -48,9 +52,15 @@
 #include <cstdint>
 #include <cstring>
 
+#include "qv.h"
 #include "qv_internal.h"
 #include "qv_ptx.cuh"
 #include "stream_common.cuh"
+
+static_assert(qv::kErrFullWait == QV_DEVICE_ERR_FULL_WAIT && qv::kErrEmptyWait == QV_DEVICE_ERR_EMPTY_WAIT &&
+                  qv::kErrDrainWait == QV_DEVICE_ERR_DRAIN_WAIT && qv::kErrGridWait == QV_DEVICE_ERR_GRID_WAIT &&
+                  qv::kErrTcWait == QV_DEVICE_ERR_TC_WAIT && qv::kErrSlotWait == QV_DEVICE_ERR_SLOT_WAIT,
+              "device error bits of qv.h");
 
 namespace qv {
 
@@ -64,27 +74,10 @@ namespace {
 // rest are widened to binary16 and go through the f16 path. With 8 tokens or
 // fewer the int8 path alone keeps up with HBM; with more tokens it would be
 // the bottleneck and the f16 path is faster (measured on GB300).
-#ifndef QV_W8A8_WARPS
-#define QV_W8A8_WARPS 8
-#endif
-#ifndef QV_S8_PAIRS_NARROW
-#define QV_S8_PAIRS_NARROW 4
-#endif
-#ifndef QV_S8_PAIRS_WIDE
-#define QV_S8_PAIRS_WIDE 0
-#endif
-#ifndef QV_TILE_ILP
-#define QV_TILE_ILP 0
-#endif
-#ifndef QV_BF16_WARPS
-#define QV_BF16_WARPS 8
-#endif
-constexpr int kW8A8Warps = QV_W8A8_WARPS;
-constexpr int kBf16Warps = QV_BF16_WARPS;
+constexpr int kW8A8Warps = 8;
+constexpr int kBf16Warps = 8;
 template <int NG>
-__host__ __device__ constexpr int s8_pairs() { return NG == 1 ? QV_S8_PAIRS_NARROW : QV_S8_PAIRS_WIDE; }
-static_assert(kW8A8Warps == 4 || kW8A8Warps == 8, "4 or 8 consumer warps");
-static_assert(kBf16Warps == 4 || kBf16Warps == 8, "4 or 8 consumer warps");
+__host__ __device__ constexpr int s8_pairs() { return NG == 1 ? 4 : 0; }
 
 template <int NG, int XB = 1>
 struct Cfg {
@@ -187,19 +180,6 @@ __device__ __forceinline__ void w8a8_tile_mma(uint32_t wb, uint32_t xb, const Ti
         for (int gr = 0; gr < NG; ++gr)
 #pragma unroll
             for (int e = 0; e < 4; ++e) accf[blk][gr][e] = 0.f;
-#if QV_TILE_ILP
-    // one int32 accumulator per chunk pair: the int8 MMAs of a tile are
-    // independent and can overlap in the tensor pipe; summed exactly below
-    int32_t acc8[S8P > 0 ? S8P : 1][BPW][NG][4];
-#pragma unroll
-    for (int P = 0; P < (S8P > 0 ? S8P : 1); ++P)
-#pragma unroll
-        for (int blk = 0; blk < BPW; ++blk)
-#pragma unroll
-            for (int gr = 0; gr < NG; ++gr)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) acc8[P][blk][gr][e] = 0;
-#endif
 #pragma unroll
     for (int cq = 0; cq < 2; ++cq) {
         // Activation words (tokens = MMA columns) for chunks 4cq .. 4cq+3.
@@ -224,11 +204,7 @@ __device__ __forceinline__ void w8a8_tile_mma(uint32_t wb, uint32_t xb, const Ti
                 if (P < S8P) {
 #pragma unroll
                     for (int gr = 0; gr < NG; ++gr)
-#if QV_TILE_ILP
-                        mma_s8_16832(acc8[P][blk][gr], r0, r1, r2, r3, bw[gr][2 * cp], bw[gr][2 * cp + 1]);
-#else
                         mma_s8_16832(acci[blk][gr], r0, r1, r2, r3, bw[gr][2 * cp], bw[gr][2 * cp + 1]);
-#endif
                 } else {
                     uint32_t a0l, a0h, a1l, a1h;
                     widen_i8x4_f16(r0, a0l, a0h);   // row g,   chunk 2P
@@ -255,16 +231,6 @@ __device__ __forceinline__ void w8a8_tile_mma(uint32_t wb, uint32_t xb, const Ti
 #pragma unroll
                 for (int e = 0; e < 4; ++e) acci[blk][gr][e] += __float2int_rn(accf[blk][gr][e]);
     }
-#if QV_TILE_ILP
-#pragma unroll
-    for (int P = 0; P < S8P; ++P)
-#pragma unroll
-        for (int blk = 0; blk < BPW; ++blk)
-#pragma unroll
-            for (int gr = 0; gr < NG; ++gr)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) acci[blk][gr][e] += acc8[P][blk][gr][e];
-#endif
 }
 
 // ---------------------------------------------------------------------------
@@ -296,11 +262,8 @@ __device__ __forceinline__ void w8a8_tile_mma(uint32_t wb, uint32_t xb, const Ti
 // independent accumulator chains all land between the two). With one token
 // group (up to 8 tokens) the int8 path is faster, with more the f16 path.
 // ---------------------------------------------------------------------------
-#ifndef QV_W4_S8P_NG1
-#define QV_W4_S8P_NG1 4
-#endif
 template <int NG>
-__host__ __device__ constexpr int w4_s8_pairs() { return NG == 1 ? QV_W4_S8P_NG1 : 0; }
+__host__ __device__ constexpr int w4_s8_pairs() { return NG == 1 ? 4 : 0; }
 
 // f16 pairs (code 8t+s, code 8t+4+s), s = 0..3, of one packed word
 __device__ __forceinline__ void int4x8_f16(uint32_t w, uint32_t (&h)[4]) {
@@ -810,12 +773,9 @@ __device__ __forceinline__ void unpack_vec(const uint4& r, bool bf16, float (&e)
     }
 }
 
-#ifndef QV_STACK_L2_AHEAD
-#define QV_STACK_L2_AHEAD 24
-#endif
 // Weight tiles the L2 prefetch warp of the stack kernel runs ahead of the
 // shared-memory producer (per CTA; 24 tiles = 384 KB, 58 MB over 152 SMs).
-constexpr int kStackL2Ahead = QV_STACK_L2_AHEAD;
+constexpr int kStackL2Ahead = 24;
 
 template <int NG>
 __global__ void __launch_bounds__((kW8A8Warps + 2) * 32, 1)
@@ -1316,6 +1276,8 @@ cudaError_t launch_w8a8_stream(const W8A8Launch& a, int num_sms, cudaStream_t s)
     p.slots = reinterpret_cast<unsigned long long*>(ws + L.slots);
     p.keys = reinterpret_cast<unsigned long long*>(ws + L.keys);
     p.done = reinterpret_cast<unsigned*>(ws + L.done);
+    p.slot_wait_ns = debug_slot_wait_ns();
+    p.drop_partials = debug_take_drop_partials() ? 1 : 0;
     const int grid = stream_grid(p.T, num_sms);
 #define QV_W8A8_LAUNCH(NGV, EPIV, W4V)                                                       \
     launch_ex(w8a8_stream_kernel<NGV, (int)EPIV, W4V>, grid, (kW8A8Warps + 1) * 32,          \

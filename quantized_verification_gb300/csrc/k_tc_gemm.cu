@@ -412,6 +412,8 @@ cudaError_t launch_w8a8_tc(const W8A8Launch& a, int num_sms, cudaStream_t s) {
     p.tokens = a.tokens; p.max_logit = a.max_logit;
     uint8_t* ws = static_cast<uint8_t*>(a.ws);
     p.slots = reinterpret_cast<unsigned long long*>(ws + L.slots);
+    p.slot_wait_ns = kWaitLimitNs;
+    p.drop_partials = 0;
     p.keys = reinterpret_cast<unsigned long long*>(ws + L.keys);
     p.done = reinterpret_cast<unsigned*>(ws + L.done);
     const int grid = stream_grid(p.T, num_sms);

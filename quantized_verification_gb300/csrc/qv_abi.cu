@@ -10,6 +10,7 @@
 #include <cstdarg>
 #include <cstdint>
 #include <cstdio>
+#include <atomic>
 #include <mutex>
 
 #include "qv.h"
@@ -230,6 +231,19 @@ qv_status check_k_w4(int K) {
 namespace qv {
 // Lets other translation units of the library report through qv_last_error().
 qv_status report_error(qv_status st, const char* msg) { return fail(st, "%s", msg); }
+
+std::atomic<unsigned long long> g_debug_slot_wait_ns{0};
+std::atomic<int> g_debug_drop_partials{0};
+unsigned long long debug_slot_wait_ns() {
+    const unsigned long long v = g_debug_slot_wait_ns.load();
+    return v ? v : kWaitLimitNs;
+}
+bool debug_take_drop_partials() {
+    int n = g_debug_drop_partials.load();
+    while (n > 0 && !g_debug_drop_partials.compare_exchange_weak(n, n - 1)) {
+    }
+    return n > 0;
+}
 }  // namespace qv
 
 extern "C" {
@@ -792,6 +806,10 @@ qv_status qv_verify_stack(const qv_linear_desc* linears, int n_linears, const qv
     }
     return ok();
 }
+
+void qv_debug_set_slot_wait_ns(unsigned long long ns) { qv::g_debug_slot_wait_ns.store(ns); }
+
+void qv_debug_drop_partials(int n) { qv::g_debug_drop_partials.store(n > 0 ? n : 0); }
 
 qv_status qv_device_error(unsigned int* code) {
     if (!code) return fail(QV_ERR_INVALID_ARG, "code is null");

@@ -9,6 +9,11 @@
 
 namespace qv {
 
+// Upper bound on any wait inside a kernel, in nanoseconds of %globaltimer.
+// A wait that runs out sets a bit in the device error word and the kernel
+// finishes without waiting again.
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;
+
 // Streaming-GEMM tile: BN output channels x BK bytes of the reduction axis.
 constexpr int kTileN = 128;
 constexpr int kTileKBytes = 128;
@@ -103,6 +108,11 @@ struct StackLaunch {
 // Workspace bytes of qv_verify_stack and the offset of its int8 code buffer.
 size_t stack_ws_bytes(int mp, int M, int n_max, int kmax);
 size_t stack_xq_offset(int mp, int n_max);
+
+// Test hooks (qv_debug_set_slot_wait_ns, qv_debug_drop_partials in qv.h),
+// read when a streaming W8A8 / W4A8 launch is enqueued.
+unsigned long long debug_slot_wait_ns();
+bool debug_take_drop_partials();
 
 cudaError_t launch_w8a8_stream(const W8A8Launch& a, int num_sms, cudaStream_t s);
 cudaError_t launch_w8a8_tc(const W8A8Launch& a, int num_sms, cudaStream_t s);

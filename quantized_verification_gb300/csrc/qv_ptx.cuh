@@ -7,12 +7,10 @@
 #include <cstdint>
 #include <cuda.h>
 
+#include "qv_internal.h"
+
 namespace qv {
 
-// Upper bound on any wait inside a kernel, in nanoseconds of %globaltimer.
-// A wait that runs out sets a bit in the device error word and the kernel
-// finishes without waiting again.
-constexpr unsigned long long kWaitLimitNs = 1000000000ull;
 
 // Device error word bits.
 constexpr unsigned kErrFullWait = 1u;    // consumer waited too long for a stage

@@ -125,6 +125,8 @@ struct W8A8Params {
     unsigned long long* slots;   // split-K partials: one BN x MP slot per CTA
     unsigned long long* keys;
     unsigned* done;
+    unsigned long long slot_wait_ns;   // limit of the split-K head's wait (kWaitLimitNs by default)
+    int drop_partials;                 // test hook: publish no split-K partial sums
 };
 
 // ---------------------------------------------------------------------------
@@ -196,7 +198,7 @@ __device__ __forceinline__ int split_contributors_end(long long T, int KT, int b
 // The caller synchronises the consumers before and after.
 template <int MP, int CW, bool FLOAT, class SM>
 __device__ __forceinline__ void gather_partials(SM& sm, unsigned long long* slots, int M, int c2, int tid,
-                                                unsigned* err) {
+                                                unsigned* err, unsigned long long limit_ns = kWaitLimitNs) {
     constexpr int CT = CW * 32;
     constexpr int QP = 2;         // pairs of words per thread in flight
     constexpr int CB = 8;         // contributor slots per batch
@@ -238,7 +240,7 @@ __device__ __forceinline__ void gather_partials(SM& sm, unsigned long long* slot
                 if (!pending) break;
                 if (t0 == 0) {
                     t0 = global_timer_ns();
-                } else if (global_timer_ns() - t0 > kWaitLimitNs) {
+                } else if (global_timer_ns() - t0 > limit_ns) {
                     atomicOr(err, kErrSlotWait);
                     break;
                 }
@@ -392,11 +394,11 @@ __device__ __forceinline__ void segment_end(SM& sm, const W8A8Params& p, int nt,
                                             int tid, EpiState& st, unsigned* err) {
     if (seg_len != p.KT) {
         if (seg_begin != nt * p.KT) {                 // not the head: publish
-            publish_partial<MP, CW>(sm, p.slots, p.M, tid);
+            if (!p.drop_partials) publish_partial<MP, CW>(sm, p.slots, p.M, tid);
             consumer_sync<CW>();
             return;
         }
-        gather_partials<MP, CW, false>(sm, p.slots, p.M, st.c2, tid, err);
+        gather_partials<MP, CW, false>(sm, p.slots, p.M, st.c2, tid, err, p.slot_wait_ns);
         consumer_sync<CW>();
     }
     finish_tile<MP, CW, EPI>(sm, p, nt, tid, st);
