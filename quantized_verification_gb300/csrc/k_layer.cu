@@ -21,10 +21,12 @@
 // E is exp by Cody and Waite's range reduction and a degree-7 Taylor
 // polynomial (layer_exp); every step is one binary32 operation in
 // round-to-nearest-even (explicit _rn intrinsics, never contracted), so the
-// results are determined by the definition alone, except for the sum of
-// squares: the kernel adds the (exact) binary32 squares in float-float, which
-// agrees with the definition's binary64 sum to about 2^-47 relative, far
-// below the binary32 rounding of var that follows.
+// results are determined by the definition alone. The sum of squares is the
+// one place where the kernel takes another route: it adds the (exact)
+// binary32 squares in float-float, which agrees with the definition's
+// binary64 sum (index order) to about 2^-37 relative; var = fl32(ss / H) is
+// the same unless ss / H lies that close to a binary32 rounding boundary, and
+// there (about one row in 2000) one thread recomputes the definition's sum.
 //
 // One CTA of 512 threads per row; the row is held in registers (H up to
 // 16384, F up to 32768).
@@ -111,6 +113,45 @@ __device__ __forceinline__ double block_sum_squares(FF v, FF* red, double* total
     return *total;
 }
 
+// Whether a non-negative binary64 value q lies within 2^-36 q of a point
+// where rounding to binary32 changes (the midpoint between two neighbouring
+// binary32 values). Error bounds for ss: the sequential binary64 sum of the
+// definition is within (H - 1) 2^-53 ss <= 2^-39 ss of the exact sum for
+// H <= 16384; the float-float sum is within about 2^-38 ss of it (per-thread
+// lo parts gather at most n^2 2^-48 with n <= 32 terms, the tree merges add
+// less); q is then rounded once more to binary64. 2^-36 covers all three.
+__device__ __forceinline__ bool near_binary32_midpoint(double q) {
+    if (!(q > 0.0)) return false;
+    const float f = __double2float_rn(q);
+    const uint32_t b = __float_as_uint(f);
+    if (b >= 0x7F7FFFFFu) return false;                  // FLT_MAX or infinity: not a workload value
+    if (b == 0u) return true;                            // below half the least subnormal
+    const double fd = (double)f;
+    const double up = (double)__uint_as_float(b + 1u);
+    const double dn = (double)__uint_as_float(b - 1u);
+    const double mid_up = __dadd_rn(fd, __dmul_rn(__dsub_rn(up, fd), 0.5));
+    const double mid_dn = __dadd_rn(fd, __dmul_rn(__dsub_rn(dn, fd), 0.5));
+    const double d = fmin(fabs(__dsub_rn(q, mid_up)), fabs(__dsub_rn(q, mid_dn)));
+    return d <= __dmul_rn(q, 0x1p-36);
+}
+
+// The definition's sum of squares of a bf16 row: binary64, index order (one
+// thread; the rare exact path of the RMSNorm).
+__device__ __noinline__ double sum_squares_in_order(const uint4* hr, int nvec) {
+    double s = 0.0;
+    for (int v = 0; v < nvec; ++v) {
+        const uint4 w4 = hr[v];
+        const uint32_t w[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const double a = (double)bf16_lo(w[j]), b = (double)bf16_hi(w[j]);
+            s = __dadd_rn(s, __dmul_rn(a, a));
+            s = __dadd_rn(s, __dmul_rn(b, b));
+        }
+    }
+    return s;
+}
+
 __device__ __forceinline__ uint32_t pack_codes4(float a, float b, float c, float d, float s, float r) {
     // the fast rule for all four, the IEEE quotient only near a half-integer
     const float e[4] = {a, b, c, d};
@@ -184,7 +225,9 @@ residual_rmsnorm_quant_kernel(uint16_t* __restrict__ h, const uint16_t* __restri
     }
     const double sum = block_sum_squares(ss, red_ff, &ss_total);
     if (tid == 0) {
-        const float var = __double2float_rn(__ddiv_rn(sum, (double)H));
+        double q = __ddiv_rn(sum, (double)H);
+        if (near_binary32_midpoint(q)) q = __ddiv_rn(sum_squares_in_order(hr, nvec), (double)H);
+        const float var = __double2float_rn(q);
         rstd_s = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(var, eps)));
     }
     __syncthreads();

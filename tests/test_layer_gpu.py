@@ -200,3 +200,75 @@ def test_w8a8_swiglu(qv, oracle, M, K, F):
     torch.cuda.synchronize()
     assert np.array_equal(np_(a).view(np.uint32), a_ref.view(np.uint32))
     assert int(ws.count_nonzero()) == 0, "workspace not left zero-filled"
+
+
+def _to_bf16_f32(a: np.ndarray) -> np.ndarray:
+    """float32 values rounded to bf16 (nearest even), returned as float32."""
+    u = np.ascontiguousarray(a, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    r = ((u + 0x7FFF + ((u >> 16) & 1)) >> 16) << 16
+    return r.astype(np.uint32).view(np.float32)
+
+
+def _norm_x(h: np.ndarray, g: np.ndarray, var: np.float32, eps: float) -> np.ndarray:
+    """x = rne_bf16(g * rne_bf16(h * rstd)) with rstd from var (binary32 steps)."""
+    rstd = np.float32(1.0) / np.sqrt(np.float32(var) + np.float32(eps))
+    return _to_bf16_f32(g * _to_bf16_f32(h * rstd))
+
+
+def _near_boundary_row(H: int, g: np.ndarray, eps: float, rng, above: bool):
+    """A bf16 row whose sum of squares, added in binary64 in index order, puts
+    ss / H within 2^-48 (relative) of a binary32 rounding boundary, on the
+    given side; and such that the other rounding of var changes the
+    normalized output. The last 12 slots hold correction terms chosen
+    greedily (largest bf16 whose square fits the remaining gap)."""
+    while True:
+        h = _to_bf16_f32(rng.normal(0.0, 1.0, H).astype(np.float32))
+        h[-12:] = 0.0
+        ss = float(np.cumsum(h.astype(np.float64) ** 2)[-1])       # sequential, index order
+        f = np.float32(ss / H)
+        up = np.nextafter(f, np.float32(np.inf))
+        mid = (float(f) + float(up)) / 2.0
+        if mid <= ss / H:
+            mid = (float(up) + float(np.nextafter(up, np.float32(np.inf)))) / 2.0
+        target = mid * (1.0 + (2.0 ** -50 if above else -2.0 ** -50))
+        gap = target * H - ss
+        for j in range(H - 12, H):
+            if gap <= 0:
+                break
+            c = np.float32(np.sqrt(gap))
+            c = (np.array([c], np.float32).view(np.uint32) & np.uint32(0xFFFF0000)).view(np.float32)[0]
+            h[j] = c
+            gap -= float(c) * float(c)
+        ss = float(np.cumsum(h.astype(np.float64) ** 2)[-1])
+        q = ss / H
+        if abs(q - mid) > 2.0 ** -48 * q or (q > mid) != above:
+            continue
+        var = np.float32(q)
+        other = np.nextafter(var, np.float32(-np.inf) if above else np.float32(np.inf))
+        if not np.array_equal(_norm_x(h, g, var, eps), _norm_x(h, g, other, eps)):
+            return h
+
+
+def test_rmsnorm_quant_near_variance_rounding_boundary(qv, oracle):
+    """Rows whose variance sits within 2^-48 of a binary32 rounding boundary,
+    closer than a float-float sum of the squares resolves, so that only the
+    definition's binary64 sum rounds var the right way (and the other way
+    would change the normalized output): the normalized bf16 activations,
+    the codes and the scales equal the oracle's."""
+    rng = np.random.default_rng(2024)
+    M, H, eps = 8, 4096, 1e-6
+    g = _to_bf16_f32(rng.uniform(0.5, 1.5, H).astype(np.float32))
+    rows = [_near_boundary_row(H, g, eps, rng, above=(m % 2 == 0)) for m in range(M)]
+    h = _bf16(np.stack(rows))
+    gb = _bf16(g)
+    assert np.array_equal(_bits(h).view(np.uint16), _bits(_bf16(np.stack(rows))))     # rows are bf16 already
+    h_ref, q_ref, s_ref, x_ref = oracle.residual_rmsnorm_quant(_bits(h), None, _bits(gb), eps)
+    hd = h.cuda()
+    xq = torch.empty(M, H, dtype=torch.int8, device="cuda")
+    sx = torch.empty(M, device="cuda")
+    x_out = torch.empty(M, H, dtype=torch.bfloat16, device="cuda")
+    qv.qv_rmsnorm_quant(hd, gb.cuda(), xq, sx, eps=eps, x_out=x_out)
+    torch.cuda.synchronize()
+    assert np.array_equal(_bits(x_out), x_ref)
+    assert np.array_equal(np_(xq), q_ref)
+    assert np.array_equal(np_(sx).view(np.uint32), s_ref.view(np.uint32))
