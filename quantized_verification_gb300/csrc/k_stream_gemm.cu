@@ -89,7 +89,11 @@ struct Cfg {
     // an SM's shared memory, so no SM ever holds two CTAs of one launch (two
     // would share the SM's bandwidth and finish last).
     static constexpr int Stages = NG == 1 ? 7 : NG == 2 ? 7 : NG == 4 ? 5 : 4;
-    static constexpr int StgWords = BN * MP;                 // epilogue staging
+    // Epilogue staging [channel][token], row stride MP + 2: even, for the
+    // 8-byte pair stores, and two words off a multiple of 32 so that the
+    // per-channel reads of a warp spread over the banks.
+    static constexpr int SP = MP + 2;
+    static constexpr int StgWords = BN * SP;
     // W4A8 f16 path: the tile's activation codes as f16 MMA fragments, one
     // 16-byte word per (chunk, token group, lane), two tiles' worth
     static constexpr int XfBytes = XB == 2 ? 2 * 8 * NG * 32 * 16 : 0;
@@ -103,6 +107,7 @@ struct Cfg {
 // Shared-memory carve-up common to both kernels.
 template <int Stages, int StageBytes, int StgWords, int MP>
 struct Smem {
+    static constexpr int SP = MP + 2;   // staging row stride (Cfg::SP)
     uint8_t* stages;          // Stages x StageBytes, 1024-aligned
     int32_t* stg;             // BN x MP staging words
     uint64_t* full;
@@ -479,8 +484,8 @@ w8a8_stream_kernel(const __grid_constant__ CUtensorMap tmap_w,
 #pragma unroll
             for (int gr = 0; gr < NG; ++gr) {
                 const int col = 8 * gr + 2 * t4;
-                *reinterpret_cast<int2*>(&sm.stg[r0 * MP + col]) = make_int2(acci[blk][gr][0], acci[blk][gr][1]);
-                *reinterpret_cast<int2*>(&sm.stg[(r0 + 8) * MP + col]) = make_int2(acci[blk][gr][2], acci[blk][gr][3]);
+                *reinterpret_cast<int2*>(&sm.stg[r0 * C::SP + col]) = make_int2(acci[blk][gr][0], acci[blk][gr][1]);
+                *reinterpret_cast<int2*>(&sm.stg[(r0 + 8) * C::SP + col]) = make_int2(acci[blk][gr][2], acci[blk][gr][3]);
             }
         }
         consumer_sync<CW>();
@@ -606,8 +611,8 @@ bf16_stream_kernel(const __grid_constant__ CUtensorMap tmap_w,
 #pragma unroll
             for (int gr = 0; gr < NG; ++gr) {
                 const int col = 8 * gr + 2 * t4;
-                *reinterpret_cast<float2*>(&stgf[r0 * MP + col]) = make_float2(acc[blk][gr][0], acc[blk][gr][1]);
-                *reinterpret_cast<float2*>(&stgf[(r0 + 8) * MP + col]) = make_float2(acc[blk][gr][2], acc[blk][gr][3]);
+                *reinterpret_cast<float2*>(&stgf[r0 * C::SP + col]) = make_float2(acc[blk][gr][0], acc[blk][gr][1]);
+                *reinterpret_cast<float2*>(&stgf[(r0 + 8) * C::SP + col]) = make_float2(acc[blk][gr][2], acc[blk][gr][3]);
             }
         }
         consumer_sync<CW>();
@@ -625,7 +630,7 @@ bf16_stream_kernel(const __grid_constant__ CUtensorMap tmap_w,
         const int r = tid;
         const int n = nt * BN + r;
         if (r < BN && n < p.N) {
-            for (int m = 0; m < p.M; ++m) p.y[(size_t)m * p.N + n] = stgf[r * MP + m];
+            for (int m = 0; m < p.M; ++m) p.y[(size_t)m * p.N + n] = stgf[r * C::SP + m];
         }
         consumer_sync<CW>();
     }

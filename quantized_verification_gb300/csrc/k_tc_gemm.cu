@@ -70,7 +70,11 @@ struct TcCfg {
     static constexpr int StageBytes = kWTileBytes + XSlot;
     static constexpr int BSlot = 2 * NM * 128;            // two 64-element K blocks of f16 rows
     static constexpr int Stages = MP <= 16 ? 8 : MP == 32 ? 7 : 5;
-    static constexpr int StgWords = BN * MP;
+    // staging [channel][token] with an odd row stride: a warp's 32 channels
+    // of one token fall on 32 distinct banks (a stride of MP = 64 words put
+    // them all on one bank: 32-way conflicts in every staging access)
+    static constexpr int SP = MP + 1;
+    static constexpr int StgWords = BN * SP;
     static constexpr int DCol0 = kTcRing * kTcACols;      // first accumulator column
     static constexpr int TmemCols = 512;
     static constexpr int SmemBytes = 1024 + Stages * StageBytes + kTcRing * BSlot + StgWords * 4 +
@@ -84,6 +88,7 @@ struct TcCfg {
 template <int MP>
 struct TcSmem {
     using C = TcCfg<MP>;
+    static constexpr int SP = C::SP;
     uint8_t* stages;           // Stages x (W tile | X tile), 1024-aligned
     uint8_t* bring;            // kTcRing x BSlot f16 activation operands
     int32_t* stg;              // BN x MP staged sums
@@ -369,7 +374,7 @@ w8a8_tc_kernel(const __grid_constant__ CUtensorMap tmap_w,
 #pragma unroll
             for (int m = 0; m < MPH; ++m) {
                 const int tok = h * MPH + m;
-                if (tok < MP) sm.stg[row * MP + tok] = acc[m];
+                if (tok < MP) sm.stg[row * C::SP + tok] = acc[m];
             }
         }
         consumer_sync<kTcConv>();

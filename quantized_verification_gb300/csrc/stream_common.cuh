@@ -166,17 +166,19 @@ __device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long
     return v;
 }
 
-// Publish this CTA's staged partial sums (stg[row * MP + token], 32-bit
-// words) into its slot. The caller synchronises the consumers afterwards
+// Publish this CTA's staged partial sums (stg[row * SM::SP + token], 32-bit
+// words; SP is the staging row stride, MP plus a padding that keeps the
+// per-row accesses of a warp on distinct banks) into its slot. The caller synchronises the consumers afterwards
 // before stg is written again.
 template <int MP, int CW, class SM>
 __device__ __forceinline__ void publish_partial(SM& sm, unsigned long long* slots, int M, int tid) {
     constexpr int CT = CW * 32;
+    constexpr int SP = SM::SP;
     unsigned long long* slot = slots + (size_t)blockIdx.x * (BN * MP);
     const uint32_t* stg = reinterpret_cast<const uint32_t*>(sm.stg);
     for (int q = tid; q < M * (BN / 2); q += CT) {
         const int m = q / (BN / 2), r = 2 * (q - m * (BN / 2));
-        st_relaxed_v2_u64(slot + m * BN + r, kSlotTag | stg[r * MP + m], kSlotTag | stg[(r + 1) * MP + m]);
+        st_relaxed_v2_u64(slot + m * BN + r, kSlotTag | stg[r * SP + m], kSlotTag | stg[(r + 1) * SP + m]);
     }
 }
 
@@ -202,6 +204,7 @@ __device__ __forceinline__ void gather_partials(SM& sm, unsigned long long* slot
     constexpr int CT = CW * 32;
     constexpr int QP = 2;         // pairs of words per thread in flight
     constexpr int CB = 8;         // contributor slots per batch
+    constexpr int SP = SM::SP;
     const int c1 = blockIdx.x + 1;
     uint32_t* stg = reinterpret_cast<uint32_t*>(sm.stg);
     const int pairs = M * (BN / 2);
@@ -214,8 +217,8 @@ __device__ __forceinline__ void gather_partials(SM& sm, unsigned long long* slot
             const int m = q / (BN / 2), r = 2 * (q - m * (BN / 2));
             off[u] = m * BN + r;
             if (q < pairs) {
-                s[u][0] = stg[r * MP + m];
-                s[u][1] = stg[(r + 1) * MP + m];
+                s[u][0] = stg[r * SP + m];
+                s[u][1] = stg[(r + 1) * SP + m];
             }
         }
         for (int c = c1; c < c2; c += CB) {
@@ -272,8 +275,8 @@ __device__ __forceinline__ void gather_partials(SM& sm, unsigned long long* slot
             const int q = q0 + u * CT;
             if (q < pairs) {
                 const int m = q / (BN / 2), r = 2 * (q - m * (BN / 2));
-                stg[r * MP + m] = s[u][0];
-                stg[(r + 1) * MP + m] = s[u][1];
+                stg[r * SP + m] = s[u][0];
+                stg[(r + 1) * SP + m] = s[u][1];
             }
         }
     }
@@ -311,6 +314,7 @@ __device__ __forceinline__ void segment_start(EpiState& st, const W8A8Params& p,
 // Finish channel tile nt from its complete int32 sums in sm.stg.
 template <int MP, int CW, int EPI, class SM>
 __device__ __forceinline__ void finish_tile(SM& sm, const W8A8Params& p, int nt, int tid, EpiState& st) {
+    constexpr int SP = SM::SP;
     const int warp = tid >> 5, lane = tid & 31;
     // the first BN consumer threads (warps 0..3) own one output channel each
     const int r = tid;
@@ -322,7 +326,7 @@ __device__ __forceinline__ void finish_tile(SM& sm, const W8A8Params& p, int nt,
     if (valid) {
 #pragma unroll
         for (int m = 0; m < MP; ++m)
-            if (m < p.M) acc[m] = sm.stg[r * MP + m];
+            if (m < p.M) acc[m] = sm.stg[r * SP + m];
     }
     const float swn = st.swn;
     if (EPI == (int)Epi::Linear) {
@@ -349,8 +353,8 @@ __device__ __forceinline__ void finish_tile(SM& sm, const W8A8Params& p, int nt,
             for (int m = 0; m < MP; ++m) {
                 if (m < p.M) {
                     const float sxm = sm.sx[m];
-                    const float yg = __fmul_rn(__int2float_rn(sm.stg[r * MP + m]), __fmul_rn(sxm, swn));
-                    const float yu = __fmul_rn(__int2float_rn(sm.stg[(r + BN / 2) * MP + m]),
+                    const float yg = __fmul_rn(__int2float_rn(sm.stg[r * SP + m]), __fmul_rn(sxm, swn));
+                    const float yu = __fmul_rn(__int2float_rn(sm.stg[(r + BN / 2) * SP + m]),
                                                __fmul_rn(sxm, st.swn_up));
                     a[(size_t)m * F + f] = __fmul_rn(silu(yg), yu);
                 }
@@ -387,7 +391,7 @@ __device__ __forceinline__ void finish_tile(SM& sm, const W8A8Params& p, int nt,
 }
 
 // End of a segment: the channel tile nt's sums over K-tiles [seg_begin,
-// seg_begin + seg_len) (tile indices) are staged in sm.stg[row * MP + token]
+// seg_begin + seg_len) (tile indices) are staged in sm.stg[row * SM::SP + token]
 // and the consumers have synchronised.
 template <int MP, int CW, int EPI, class SM>
 __device__ __forceinline__ void segment_end(SM& sm, const W8A8Params& p, int nt, int seg_begin, int seg_len,
