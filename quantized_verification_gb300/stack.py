@@ -36,7 +36,10 @@ from . import qv, synth
 class VerifyStack:
     def __init__(self, model: dict = synth.QWEN3_8B, layers: int | None = None, B: int = 1,
                  gamma: int = 4, seed: int = 0, device: str = "cuda", keep_bf16: bool = False,
-                 y_dtype=torch.float32, wbits: int = 8):
+                 y_dtype=torch.float32, wbits: int = 8, share_weights: "VerifyStack | None" = None):
+        """share_weights: another stack of the same model whose resident
+        weights (int8 codes, scales, bf16 originals) this one uses, so a
+        stack for another batch shape costs only its inputs and buffers."""
         assert wbits in (8, 4), "int8 or packed int4 weights"
         self.wbits = wbits
         self.model = model
@@ -57,9 +60,19 @@ class VerifyStack:
         self.weights_bf16 = [] if keep_bf16 else None
         self.inputs = []       # per layer: list of bf16 [M, K] per phase
         dev = self.device
+        src = share_weights
+        if src is not None:
+            assert src.model == model and src.layers == self.layers and src.wbits == wbits
+            keep_bf16 = keep_bf16 and src.weights_bf16 is not None
+            self.weights_bf16 = src.weights_bf16 if keep_bf16 else None
         for l in range(self.layers):
             lw, lb, li = [], [], []
-            for (name, K, N) in self.phases:
+            for p_, (name, K, N) in enumerate(self.phases):
+                li_x = synth.activations(self.M, K, synth.subseed(seed, "x", l, name), device=dev)
+                if src is not None:
+                    lw.append(src.weights[l][p_])
+                    li.append(li_x)
+                    continue
                 w = synth.weights(N, K, synth.subseed(seed, "w", l, name), device=dev)
                 if name == "gate_up" and (N // 2) % 64 == 0:
                     # gate and up rows interleaved by 64 (qv_w8a8_swiglu's layout);
@@ -71,15 +84,19 @@ class VerifyStack:
                     lb.append(w)
                 else:
                     del w
-                li.append(synth.activations(self.M, K, synth.subseed(seed, "x", l, name), device=dev))
+                li.append(li_x)
             self.weights.append(lw)
-            if keep_bf16:
+            if keep_bf16 and src is None:
                 self.weights_bf16.append(lb)
             self.inputs.append(li)
-        wl = synth.weights(self.V, h, synth.subseed(seed, "w", "lm_head"), device=dev)
-        self.lm_wq, self.lm_sw = self._quantize_weight(wl)
-        self.lm_bf16 = wl if keep_bf16 else None
-        del wl
+        if src is not None:
+            self.lm_wq, self.lm_sw = src.lm_wq, src.lm_sw
+            self.lm_bf16 = src.lm_bf16 if keep_bf16 else None
+        else:
+            wl = synth.weights(self.V, h, synth.subseed(seed, "w", "lm_head"), device=dev)
+            self.lm_wq, self.lm_sw = self._quantize_weight(wl)
+            self.lm_bf16 = wl if keep_bf16 else None
+            del wl
         self.h_final = synth.activations(self.M, h, synth.subseed(seed, "x", "final"), device=dev)
         # Every per-step activation input becomes a view into one contiguous
         # buffer (each [M, K] bf16 slice starts 16-byte aligned because K is a
@@ -226,9 +243,13 @@ class VerifyStack:
                      self.accept_len, self.out_tokens, stream=stream)
 
     # ------------------------------------------------------------------ chained layers
-    def prepare_chain(self, eps: float = 1e-6):
+    def prepare_chain(self, eps: float = 1e-6, cache_len: int | None = None, head_dim: int = 128):
         """Norm weights, the step's input residual stream and the output
-        buffers of the chained step (enqueue_chain)."""
+        buffers of the chained step (enqueue_chain). With cache_len, every
+        layer also gets a seeded bf16 KV cache of cache_len positions per
+        sequence ([B, cache_len, Hkv, head_dim], N(0, 1)) and the chain runs
+        attention over it between the qkv and o projections; without it the
+        o projection takes the layer's seeded input."""
         self._w8_only("the layer chain")
         h, M, F = self.model["hidden"], self.M, self.model["ffn"]
         dev = self.device
@@ -243,25 +264,48 @@ class VerifyStack:
         self.y_o = torch.empty(M, h, dtype=torch.bfloat16, device=dev)
         self.a_glu = torch.empty(M, F, dtype=torch.float32, device=dev)
         self.y_down = torch.empty(M, h, dtype=torch.bfloat16, device=dev)
+        self.cache_len = cache_len
+        if cache_len is not None:
+            q = self.model.get("q", h)
+            kv = self.model["kv"]
+            assert q % head_dim == 0 and kv % head_dim == 0
+            self.head_dim, self.Hq, self.Hkv = head_dim, q // head_dim, kv // head_dim
+            shape = (self.B, cache_len, self.Hkv, head_dim)
+            self.k_cache = [synth.activations(self.B * cache_len, self.Hkv * head_dim,
+                                              synth.subseed(self.seed, "k_cache", l), device=dev,
+                                              outlier_frac=0.0).view(shape) for l in range(self.layers)]
+            self.v_cache = [synth.activations(self.B * cache_len, self.Hkv * head_dim,
+                                              synth.subseed(self.seed, "v_cache", l), device=dev,
+                                              outlier_frac=0.0).view(shape) for l in range(self.layers)]
+            self.cache_lens = torch.full((self.B,), cache_len, dtype=torch.int32, device=dev)
+            T = self.gamma + 1
+            self.ws_attn = torch.empty(qv.qv_attention_workspace_bytes(self.B, T, self.Hq, self.Hkv, head_dim,
+                                                                       cache_len), dtype=torch.uint8, device=dev)
+            # one output buffer per layer (kept for inspection; the chain reads each once)
+            self.attn_out = [torch.empty(M, self.Hq * head_dim, dtype=torch.float32, device=dev)
+                             for _ in range(self.layers)]
 
     def enqueue_chain(self, stream=None):
         """One verify step through chained decoder layers: the bf16 residual
         stream h runs through every layer, with the non-linear steps between
         the quantized linears fused with the next linear's quantization
         (gist.science/ja summary, section 2.2 item 3):
-          attention block: x = RMSNorm(h += down_prev) -> qkv; the attention
-            core itself is not modelled: the o projection takes the seeded
-            attention output of the layer; h += o's bf16 output, next block;
+          attention block: x = RMSNorm(h += down_prev) -> qkv (bf16); with a
+            KV cache, causal grouped-query attention of the verify tokens
+            over the cache and their own keys (qv_attention_verify, fp32),
+            its per-token quantization -> o; without one, o takes the
+            layer's seeded input; h += o's bf16 output, next block;
           MLP block: x = RMSNorm(h) -> gate|up with SiLU(gate)*up in its
             epilogue (fp32) -> per-token quantization -> down (bf16 output,
             added to h by the next RMSNorm);
           head: x = RMSNorm(h += down_last) -> LM head argmax -> acceptance.
-        Eight launches per layer (as in enqueue), plus the final three."""
+        Eight launches per layer (ten with attention), plus the final three."""
         M, h, F = self.M, self.model["hidden"], self.model["ffn"]
         ws = self.ws
         cur = torch.cuda.current_stream() if stream is None else stream
         with torch.cuda.stream(cur):
             self.h_res.copy_(self.h0)
+        attn = getattr(self, "cache_len", None) is not None
         for l in range(self.layers):
             g1, g2 = self.norm_w[l]
             xq = self._xq(h)
@@ -270,7 +314,13 @@ class VerifyStack:
             wq, sw = self.weights[l][0]
             qv.qv_w8a8_linear(xq, self.sx, wq, sw, self.y_qkv, ws, stream=stream)
             xq = self._xq(self.phases[1][1])
-            qv.qv_quantize_act(self.inputs[l][1], xq, self.sx, stream=stream)
+            if attn:
+                qv.qv_attention_verify(self.y_qkv, self.k_cache[l], self.v_cache[l], self.cache_lens,
+                                       self.gamma + 1, self.Hq, self.Hkv, 1.0 / self.head_dim ** 0.5,
+                                       self.attn_out[l], self.ws_attn, stream=stream)
+                qv.qv_quantize_act(self.attn_out[l], xq, self.sx, stream=stream)
+            else:
+                qv.qv_quantize_act(self.inputs[l][1], xq, self.sx, stream=stream)
             wq, sw = self.weights[l][1]
             qv.qv_w8a8_linear(xq, self.sx, wq, sw, self.y_o, ws, stream=stream)
             xq = self._xq(h)

@@ -272,3 +272,74 @@ def test_rmsnorm_quant_near_variance_rounding_boundary(qv, oracle):
     assert np.array_equal(_bits(x_out), x_ref)
     assert np.array_equal(np_(xq), q_ref)
     assert np.array_equal(np_(sx).view(np.uint32), s_ref.view(np.uint32))
+
+
+def test_chained_layers_with_attention_match_oracle(qv, oracle):
+    """Two chained decoder layers with attention over a 40-position bf16 KV
+    cache per sequence between the qkv and o projections, checked step by
+    step: each layer's qkv output equals the oracle's bit for bit; its
+    attention output is within 1e-4 max|v| of the oracle's binary64
+    attention of that qkv output (the bound of the attention tests); with the
+    GPU's attention output as input, every later step (its quantization, o,
+    RMSNorm, gate|up with SwiGLU, down, the final norm, the LM head and the
+    acceptance) equals the oracle's bit for bit, and the captured step
+    repeats it."""
+    from quantized_verification_gb300 import synth
+    from quantized_verification_gb300.stack import VerifyStack
+    model = {"hidden": 256, "kv": 64, "ffn": 512, "layers": 2, "vocab": 1000}
+    B, gamma, D, L = 2, 3, 64, 40
+    T, Hq, Hkv = gamma + 1, 256 // D, 64 // D
+    st = VerifyStack(model=model, B=B, gamma=gamma, seed=9)
+    st.prepare_chain(eps=1e-6, cache_len=L, head_dim=D)
+    st.drafts.copy_(synth.uniform_tokens((B, gamma), 1000, seed=4).cuda())
+    st.enqueue_chain()
+    torch.cuda.synchronize()
+
+    cpu = lambda t: t.cpu().numpy()
+    scale = float(np.float32(1.0 / np.sqrt(D)))
+    lens = np.full(B, L, dtype=np.int32)
+    h = _bits(st.h0)
+    yd = None
+    for l in range(model["layers"]):
+        g1, g2 = st.norm_w[l]
+        h, q, s, _ = oracle.residual_rmsnorm_quant(h, yd, _bits(g1), 1e-6)
+        wq, sw = st.weights[l][0]
+        y_qkv = oracle.f32_to_bf16(oracle.w8a8_linear(q, s, cpu(wq), cpu(sw))[0])
+        kc, vc = _bits(st.k_cache[l]).reshape(B, L, Hkv, D), _bits(st.v_cache[l]).reshape(B, L, Hkv, D)
+        att_ref = oracle.attention_verify(y_qkv, kc, vc, lens, T, Hq, Hkv, D, scale)
+        att = np_(st.attn_out[l])
+        vals = np.concatenate([(vc.astype(np.uint32) << 16).view(np.float32).ravel(),
+                               (y_qkv[:, (Hq + Hkv) * D:].astype(np.uint32) << 16).view(np.float32).ravel()])
+        assert np.all(np.isfinite(att))
+        assert float(np.abs(att.astype(np.float64) - att_ref).max()) <= 1e-4 * float(np.abs(vals).max()), l
+        qo, so = oracle.quantize_rows(att)                         # the chain continues from the GPU's output
+        wq, sw = st.weights[l][1]
+        y_o = oracle.f32_to_bf16(oracle.w8a8_linear(qo, so, cpu(wq), cpu(sw))[0])
+        h, q2, s2, _ = oracle.residual_rmsnorm_quant(h, y_o, _bits(g2), 1e-6)
+        wq, sw = st.weights[l][2]
+        y_il, _ = oracle.w8a8_linear(q2, s2, cpu(wq), cpu(sw))     # gate|up rows interleaved by 64
+        F = y_il.shape[1] // 2
+        blocks = y_il.reshape(-1, F // 64, 2, 64)
+        y_gu = np.concatenate([blocks[:, :, 0, :].reshape(-1, F), blocks[:, :, 1, :].reshape(-1, F)], axis=1)
+        q3, s3 = oracle.swiglu_quant(y_gu)
+        wq, sw = st.weights[l][3]
+        yd = oracle.f32_to_bf16(oracle.w8a8_linear(q3, s3, cpu(wq), cpu(sw))[0])
+        if l == model["layers"] - 1:
+            assert np.array_equal(_bits(st.y_qkv), y_qkv)
+            assert np.array_equal(_bits(st.y_o), y_o)
+            a_ref = _silu_times(oracle, y_gu[:, :F], y_gu[:, F:])
+            assert np.array_equal(np_(st.a_glu).view(np.uint32), a_ref.view(np.uint32))
+            assert np.array_equal(_bits(st.y_down), yd)
+    h, qf, sf, _ = oracle.residual_rmsnorm_quant(h, yd, _bits(st.norm_final), 1e-6)
+    assert np.array_equal(_bits(st.h_res), h)
+    tok, _ = oracle.lm_head_argmax(qf, sf, cpu(st.lm_wq), cpu(st.lm_sw))
+    assert np.array_equal(np_(st.tokens), tok)
+    ln, out = oracle.accept(tok, cpu(st.drafts), B, gamma)
+    assert np.array_equal(np_(st.accept_len), ln) and np.array_equal(np_(st.out_tokens), out)
+    att_last = np_(st.attn_out[-1]).copy()
+    g = st.capture_chain()
+    st.tokens.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert np.array_equal(np_(st.tokens), tok) and np.array_equal(_bits(st.h_res), h)
+    assert np.array_equal(np_(st.attn_out[-1]).view(np.uint32), att_last.view(np.uint32))   # deterministic
