@@ -437,6 +437,79 @@ def main():
         log(f"bf16 comparator {bf_ms:.4f} ms/step, speedup {bf_ms / ms:.3f}x")
         del gb
 
+    # ---- batched verify (the batched workload): B = 8 x (gamma + 1 = 8) =
+    # 64 and B = 16 x 5 = 80 tokens through the same 36-layer stack (its
+    # resident weights shared) + LM head + per-sequence acceptance; the
+    # W8A8 GEMM alone over the step's projections; the BF16 comparator
+    batched = None
+    if rank == 0:
+        batched = {}
+        for (Bb, gm) in ((8, 7), (16, 4)):
+            bs = VerifyStack(layers=args.layers, B=Bb, gamma=gm, seed=4321 + rank, device=str(dev),
+                             keep_bf16=comparator is not None, share_weights=stack)
+            bs.enqueue_two_call()
+            torch.cuda.synchronize()
+            bs.drafts.copy_(synth.geometric_drafts(bs.tokens.view(Bb, gm + 1).cpu(), bs.V, 0.7, seed=77 + rank))
+            gbt = bs.capture_two_call()
+            for _ in range(3):
+                gbt.replay()
+            torch.cuda.synchronize()
+            b_ms = time_graph(torch, gbt, max(10, args.steps // 10), stream)
+            del gbt
+            Mb = bs.M
+            bxq = []
+            for l in range(bs.layers):
+                for p_, (name, K, N) in enumerate(bs.phases):
+                    xq = torch.empty(Mb, K, dtype=torch.int8, device=dev)
+                    sxp = torch.empty(Mb, device=dev)
+                    qv.qv_quantize_act(bs.inputs[l][p_], xq, sxp)
+                    bxq.append((xq, sxp))
+            torch.cuda.synchronize()
+
+            def blin(s_, bs=bs, bxq=bxq, Mb=Mb):
+                j = 0
+                for l in range(bs.layers):
+                    for p_, (name, K, N) in enumerate(bs.phases):
+                        wq, sw = bs.weights[l][p_]
+                        qv.qv_w8a8_linear(bxq[j][0], bxq[j][1], wq, sw, bs.y[: Mb * N].view(Mb, N), bs.ws, stream=s_)
+                        j += 1
+            gl2 = VerifyStack._capture(blin, dev)
+            bl_ms = time_graph(torch, gl2, max(3, args.kernel_reps // 4), stream)
+            del gl2, bxq
+            bl_bytes = bs.linear_launch_bytes(fused_act=False)
+            b_ach = sum(bl_bytes) / (bl_ms * 1e-3) / 1e9
+            slices = (Mb + 63) // 64
+            entry = {"B": Bb, "gamma": gm, "M": Mb, "ms_per_step": b_ms, "tokens_per_s": Mb / (b_ms * 1e-3),
+                     "weight_stream_gbs": bs.weight_bytes() / (b_ms * 1e-3) / 1e9,
+                     "accept_len_mean": float(bs.accept_len.float().mean()),
+                     "roofline": {"bound": "hbm", "achieved": b_ach, "peak": peak, "unit": "GB/s",
+                                  "frac": b_ach / peak, "traffic": None,
+                                  "kernel": ("w8a8_tc_kernel<64> (tcgen05 on exactly widened codes)" if Mb == 64 else
+                                             "w8a8_tc_kernel<64> for rows 0-63 + w8a8_stream_kernel<2> for the rest"),
+                                  "launches_per_projection": slices,
+                                  "bytes_per_launch": sum(bl_bytes) / len(bl_bytes) / slices,
+                                  "launch_ms_mean": bl_ms / len(bl_bytes) / slices,
+                                  "timing": "144 projections of the step back to back in one CUDA graph (codes "
+                                            "quantized beforehand), CUDA events on the launching stream; algorithmic "
+                                            "bytes include each launch's own weight stream",
+                                  "peak_source": f"{peak_kind} hbm_gbs (copy, burst)"},
+                     "path": "per projection qv_quantize_act + qv_w8a8_linear, qv_quantize_act + qv_lm_head_argmax, "
+                             "qv_accept (per sequence); one CUDA graph"}
+            if comparator is not None:
+                bs.prepare_bf16()
+                gbb = VerifyStack._capture(bs.enqueue_bf16, dev)
+                for _ in range(3):
+                    gbb.replay()
+                bb_ms = time_graph(torch, gbb, max(5, args.steps // 20), stream)
+                entry["bf16_ms_per_step"] = bb_ms
+                entry["speedup_vs_bf16"] = bb_ms / b_ms
+                del gbb
+            log(f"batched M={Mb}: {b_ms:.3f} ms/step, W8A8 GEMMs {b_ach:.0f} GB/s; "
+                f"bf16 {entry.get('bf16_ms_per_step', float('nan')):.3f} ms")
+            batched[f"M{Mb}"] = entry
+            del bs
+            torch.cuda.empty_cache()
+
     # ---- e2e through the public API from host buffers
     host_in, host_d = stack.pinned_host_inputs()
     out_len = torch.empty(stack.B, dtype=torch.int32).pin_memory()
@@ -456,25 +529,35 @@ def main():
            "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3}
 
     cpu = None
-    # ---- chained decoder layers (residual stream, RMSNorm, SwiGLU between
-    # the linears): the same weights and launch count, a real layer chain
+    # ---- chained decoder layers (residual stream, RMSNorm, attention over a
+    # 2048-position KV cache, SwiGLU between the linears): the same weights, a
+    # real layer chain; and the same chain with the o projection on its
+    # seeded input instead of attention, for the attention's share
     layer_chain = None
     if rank == 0:
-        stack.prepare_chain()
-        chain_graph = stack.capture_chain()
-        for _ in range(3):
-            chain_graph.replay()
-        torch.cuda.synchronize()
-        chain_ms = time_graph(torch, chain_graph, max(20, args.steps // 5), stream)
-        log(f"layer chain {chain_ms:.4f} ms/step")
+        chain = {}
+        for label, cl in (("no_attention", None), ("attention", 2048)):
+            stack.prepare_chain(cache_len=cl)
+            chain_graph = stack.capture_chain()
+            for _ in range(3):
+                chain_graph.replay()
+            torch.cuda.synchronize()
+            chain[label] = time_graph(torch, chain_graph, max(20, args.steps // 5), stream)
+            del chain_graph
+            log(f"layer chain ({label}) {chain[label]:.4f} ms/step")
+        chain_ms = chain["attention"]
         layer_chain = {"ms_per_step": chain_ms, "tokens_per_s": stack.M / (chain_ms * 1e-3),
                        "weight_stream_gbs": stack.weight_bytes() / (chain_ms * 1e-3) / 1e9,
-                       "launches_per_step": 8 * stack.layers + 3,
-                       "path": "per layer: qv_rmsnorm_quant (residual add + RMSNorm + quant) -> qkv, "
-                               "qv_quantize_act (seeded attention output) -> o, qv_rmsnorm_quant -> qv_w8a8_swiglu "
-                               "(gate|up with SiLU(gate)*up in the epilogue) -> qv_quantize_act -> down (bf16); "
-                               "final qv_rmsnorm_quant -> LM head "
-                               "argmax -> accept; one CUDA graph"}
+                       "kv_cache_positions": 2048, "launches_per_step": 10 * stack.layers + 3,
+                       "ms_per_step_without_attention": chain["no_attention"],
+                       "attention_share": (chain_ms - chain["no_attention"]) / chain_ms,
+                       "path": "per layer: qv_rmsnorm_quant (residual add + RMSNorm + quant) -> qkv (bf16) -> "
+                               "qv_attention_verify over the layer's bf16 KV cache (2048 positions, 32/8 heads, "
+                               "D = 128) and the step's own keys -> qv_quantize_act -> o -> qv_rmsnorm_quant -> "
+                               "qv_w8a8_swiglu (gate|up with SiLU(gate)*up in the epilogue) -> qv_quantize_act -> "
+                               "down (bf16); final qv_rmsnorm_quant -> LM head argmax -> accept; one CUDA graph"}
+        del stack.k_cache, stack.v_cache
+        torch.cuda.empty_cache()
 
     # ---- T > 0: LM-head logits and lossless rejection sampling
     sampling = None
@@ -674,6 +757,7 @@ def main():
             "w4a8": w4a8,
             "logit_fidelity": fidelity,
             "attention_kv_cache": attention,
+            "batched_verify": batched,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
