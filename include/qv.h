@@ -413,10 +413,17 @@ QV_API qv_status qv_quantize_weight(const void* w, qv_dtype w_dtype, int N, int 
  *             cache_len[b] cached positions and the step's tokens 0..j of
  *             scale * q . k, applied to the values
  *   T * Hq/Hkv <= 32, D in {64, 128}, 1 <= B <= 65535, 0 <= Lmax <= 2^24
- *   workspace qv_attention_workspace_bytes(B, T, Hq, Hkv, D, Lmax) bytes,
- *             16-byte aligned, no initialisation needed (per-chunk partials)
- * binary32 scores and sums (the products of bf16 values are exact): the
- * outputs are within about 1e-5 of max |v| of the binary64 definition.
+ *   workspace, workspace_bytes: not used (may be NULL / 0); kept so that
+ *             callers sized by qv_attention_workspace_bytes keep working
+ *             (it returns 16 for a valid shape, 0 for an invalid one)
+ * One launch of 8-CTA thread-block clusters, one cluster per (sequence,
+ * key/value head): the CTAs split the key positions, score them and form
+ * P V on the bf16 tensor cores (fp32 accumulation; P is split into two bf16
+ * parts) with an online softmax, and merge their partials through
+ * distributed shared memory. Each CTA asks for about 180 KB of shared
+ * memory and a cluster needs 8 such SMs at once: where the device cannot
+ * place one (e.g. a small MPS partition) the call returns QV_ERR_CUDA.
+ * The outputs are within about 1e-5 of max |v| of the binary64 definition.
  */
 QV_API size_t qv_attention_workspace_bytes(int B, int T, int Hq, int Hkv, int D, int Lmax);
 QV_API qv_status qv_attention_verify(const uint16_t* qkv, const uint16_t* k_cache, const uint16_t* v_cache,

@@ -605,7 +605,7 @@ qv_status check_attention_shape(int B, int T, int Hq, int Hkv, int D, int Lmax) 
 
 size_t qv_attention_workspace_bytes(int B, int T, int Hq, int Hkv, int D, int Lmax) {
     if (check_attention_shape(B, T, Hq, Hkv, D, Lmax) != QV_OK) return 0;
-    return (qv::attention_workspace_bytes(B, T, Hq, Hkv, D, Lmax) + 255) & ~size_t(255);
+    return qv::attention_workspace_bytes(B, T, Hq, Hkv, D, Lmax);
 }
 
 qv_status qv_attention_verify(const uint16_t* qkv, const uint16_t* k_cache, const uint16_t* v_cache,
@@ -620,16 +620,13 @@ qv_status qv_attention_verify(const uint16_t* qkv, const uint16_t* k_cache, cons
     if (!aligned(qkv, 16) || (k_cache && !aligned(k_cache, 16)) || (v_cache && !aligned(v_cache, 16)) ||
         !aligned(cache_len, 4) || !aligned(out, 4))
         return fail(QV_ERR_INVALID_ARG, "qkv and the caches must be 16-byte aligned");
-    const size_t need = qv_attention_workspace_bytes(B, T, Hq, Hkv, D, Lmax);
-    if (!workspace) return fail(QV_ERR_WORKSPACE, "workspace is null (%zu bytes needed)", need);
-    if (!aligned(workspace, 16)) return fail(QV_ERR_WORKSPACE, "workspace must be 16-byte aligned");
-    if (workspace_bytes < need) return fail(QV_ERR_WORKSPACE, "workspace has %zu bytes, %zu needed", workspace_bytes, need);
+    (void)workspace;          // the kernel needs none (partials stay in distributed shared memory)
+    (void)workspace_bytes;
     QV_CHECK_DEV(qkv);
     QV_CHECK_DEV(k_cache);
     QV_CHECK_DEV(v_cache);
     QV_CHECK_DEV(cache_len);
     QV_CHECK_DEV(out);
-    QV_CHECK_DEV(workspace);
     cudaError_t e = qv::launch_attention_verify(qkv, k_cache, v_cache, cache_len, B, T, Hq, Hkv, D, Lmax, scale, out,
                                                 workspace, stream);
     if (e != cudaSuccess) return cuda_fail(e, "qv_attention_verify launch");

@@ -136,8 +136,7 @@ cudaError_t launch_quantize_weight_w4(const void* w, bool bf16, int N, int K, ui
 // rows per launch.
 constexpr int kMaxMPerLaunchW4 = 32;
 
-// Attention over a short KV cache (k_attn.cu): split-KV partials of 64 keys.
-int attention_splits(int Lmax, int T);
+// Attention over a short KV cache (k_attn.cu): one cluster launch, no workspace.
 size_t attention_workspace_bytes(int B, int T, int Hq, int Hkv, int D, int Lmax);
 cudaError_t launch_attention_verify(const uint16_t* qkv, const uint16_t* kc, const uint16_t* vc, const int32_t* len,
                                     int B, int T, int Hq, int Hkv, int D, int Lmax, float scale, float* out,

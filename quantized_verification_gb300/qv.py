@@ -318,7 +318,7 @@ def qv_attention_workspace_bytes(B, T, Hq, Hkv, D, Lmax) -> int:
     return int(load().qv_attention_workspace_bytes(B, T, Hq, Hkv, D, Lmax))
 
 
-def qv_attention_verify(qkv, k_cache, v_cache, cache_len, T, Hq, Hkv, scale, out, workspace, stream=None):
+def qv_attention_verify(qkv, k_cache, v_cache, cache_len, T, Hq, Hkv, scale, out, workspace=None, stream=None):
     """Causal grouped-query attention of the verify tokens over the KV cache
     and the step's own keys: qkv [B*T, (Hq+2Hkv)*D] bf16, k_cache / v_cache
     [B, Lmax, Hkv, D] bf16, cache_len [B] int32 -> out [B*T, Hq*D] fp32."""
@@ -330,7 +330,8 @@ def qv_attention_verify(qkv, k_cache, v_cache, cache_len, T, Hq, Hkv, scale, out
     _need(out.shape == (B * T, Hq * D) and out.dtype == torch.float32, "out float32 [B*T, Hq*D]")
     _check(load().qv_attention_verify(_ptr(qkv), _ptr(k_cache) if Lmax > 0 else None,
                                       _ptr(v_cache) if Lmax > 0 else None, _ptr(cache_len), B, T, Hq, Hkv, D, Lmax,
-                                      ctypes.c_float(scale), _ptr(out), _ptr(workspace), workspace.numel(),
+                                      ctypes.c_float(scale), _ptr(out), _ptr(workspace),
+                                      0 if workspace is None else workspace.numel(),
                                       ctypes.c_void_p(_stream(stream))))
 
 

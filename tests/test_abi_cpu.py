@@ -110,10 +110,10 @@ def test_host_validation_without_gpu(lib):
     assert lib.qv_attention_verify(fake, fake, fake, fake, 1, 9, 32, 8, 128, 16, F32(0.1), fake, fake, 1 << 22, None) == qv.QV_ERR_INVALID_ARG
     assert lib.qv_attention_verify(fake, None, fake, fake, 1, 5, 32, 8, 128, 16, F32(0.1), fake, fake, 1 << 22, None) == qv.QV_ERR_INVALID_ARG
     assert lib.qv_attention_verify(fake, fake, fake, fake, 1, 5, 32, 8, 128, 16, F32(0.0), fake, fake, 1 << 22, None) == qv.QV_ERR_INVALID_ARG
-    assert lib.qv_attention_verify(fake, fake, fake, fake, 1, 5, 32, 8, 128, 16, F32(0.1), fake, fake, 16, None) == qv.QV_ERR_WORKSPACE
     assert lib.qv_attention_verify(P(0x1008), fake, fake, fake, 1, 5, 32, 8, 128, 16, F32(0.1), fake, fake, 1 << 22, None) == qv.QV_ERR_INVALID_ARG
-    # eight 64-key chunks for 500 cached + 5 new keys, per key/value head; 20 rows of 130 floats each
-    assert qv.qv_attention_workspace_bytes(1, 5, 32, 8, 128, 500) == (8 * 8 * 20 * 130 * 4 + 255) // 256 * 256
+    # no workspace: 16 bytes for any valid shape, 0 for an invalid one
+    assert qv.qv_attention_workspace_bytes(1, 5, 32, 8, 128, 500) == 16
+    assert qv.qv_attention_workspace_bytes(1, 5, 32, 8, 96, 500) == 0
     # logit fidelity
     assert lib.qv_logit_fidelity(None, fake, 2, 10, fake, fake, fake, None) == qv.QV_ERR_INVALID_ARG
     assert lib.qv_logit_fidelity(fake, fake, 0, 10, fake, fake, fake, None) == qv.QV_ERR_INVALID_ARG

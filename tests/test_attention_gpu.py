@@ -64,9 +64,11 @@ def test_attention_rejects_bad_shapes(qv):
     assert qv.qv_attention_workspace_bytes(1, 9, 32, 8, 128, 100) == 0        # T * G > 32
     assert qv.qv_attention_workspace_bytes(1, 5, 32, 8, 96, 100) == 0         # D not 64 / 128
     assert qv.qv_attention_workspace_bytes(1, 5, 30, 8, 128, 100) == 0        # Hq % Hkv
-    with pytest.raises(qv.QVError):
+    out = torch.full((5, 4096), 7.0, device="cuda")
+    with pytest.raises(qv.QVError):                                              # scale must be > 0
         qv.qv_attention_verify(torch.zeros(5, 48 * 128, dtype=torch.bfloat16, device="cuda"),
                                torch.zeros(1, 4, 8, 128, dtype=torch.bfloat16, device="cuda"),
                                torch.zeros(1, 4, 8, 128, dtype=torch.bfloat16, device="cuda"),
-                               torch.zeros(1, dtype=torch.int32, device="cuda"), 5, 32, 8, 0.1,
-                               torch.zeros(5, 4096, device="cuda"), z)
+                               torch.zeros(1, dtype=torch.int32, device="cuda"), 5, 32, 8, 0.0, out, z)
+    torch.cuda.synchronize()
+    assert bool((out == 7.0).all())                                              # nothing was enqueued
