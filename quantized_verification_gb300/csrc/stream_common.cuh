@@ -202,8 +202,12 @@ template <int MP, int CW, bool FLOAT, class SM>
 __device__ __forceinline__ void gather_partials(SM& sm, unsigned long long* slots, int M, int c2, int tid,
                                                 unsigned* err, unsigned long long limit_ns = kWaitLimitNs) {
     constexpr int CT = CW * 32;
-    constexpr int QP = 2;         // pairs of words per thread in flight
-    constexpr int CB = 8;         // contributor slots per batch
+    // Pairs of words per thread and contributor slots per batch in flight:
+    // every round of loads is one L2 round trip, so with many token rows
+    // each thread keeps more pairs in flight (a split tile has few
+    // contributors then); QP * CB stays 16 to bound the registers.
+    constexpr int QP = MP >= 32 ? 4 : 2;
+    constexpr int CB = 16 / QP;
     constexpr int SP = SM::SP;
     const int c1 = blockIdx.x + 1;
     uint32_t* stg = reinterpret_cast<uint32_t*>(sm.stg);
