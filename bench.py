@@ -654,8 +654,9 @@ def main():
             attention = {"context": L_, "tokens": T_, "heads": [Hq_, Hkv_, D_], "us_per_layer": a_ms * 1e3 / stack.layers,
                          "us_per_step": a_ms * 1e3, "kv_bytes_per_layer": kv_b,
                          "kv_gbs": kv_b * stack.layers / (a_ms * 1e-3) / 1e9,
-                         "note": "not part of the timed step (its attention input is seeded); the layers' attention "
-                                 "over a 2048-position bf16 cache, qv_attention_verify, one CUDA graph"}
+                         "note": "the attention alone, 36 layers back to back (the chained step runs the same "
+                                 "per layer; the headline step has no attention); 2048-position bf16 cache, "
+                                 "qv_attention_verify (one cluster launch per layer), one CUDA graph"}
             log(f"attention at L={L_}: {attention['us_per_layer']:.2f} us per layer")
             del ga_graph, kcs, vcs
             torch.cuda.empty_cache()
