@@ -4,9 +4,10 @@ The Qwen3-8B-shaped verify step at M = 5 (batch 1, gamma = 4): q|k|v
 4096 -> 6144, o 4096 -> 4096, gate|up 4096 -> 24576, down 12288 -> 4096 per
 layer (two layers here; the bench runs 36 of the same shapes), the LM head
 4096 -> 151936 fused with the greedy argmax, and the acceptance, through the
-per-op path the bench times (qv_quantize_act + qv_w8a8_linear per projection,
-qv_quantize_act + qv_lm_head_argmax, qv_accept), eagerly and as the captured
-CUDA graph. Every output is compared with the oracle element by element:
+per-op paths the bench times (qv_quantize_act + qv_w8a8_linear per
+projection, qv_quantize_act + qv_lm_head_argmax, qv_accept; and the one-call
+qv_w8a8_linear_act / qv_lm_head_argmax_act), eagerly and as the captured CUDA
+graphs. Every output is compared with the oracle element by element:
 the weight codes and scales, every projection's fp32 output bit for bit,
 the argmax tokens and maximum logits over the whole vocabulary, the accepted
 lengths and tokens (Quasar, gist.science/ja summary, section 2.2 item 3;
@@ -36,8 +37,10 @@ def test_qwen3_8b_step_matches_oracle(qv, oracle):
     M, V, h = st.M, st.V, st.model["hidden"]
     assert [(K, N) for (_, K, N) in st.phases] == [(4096, 6144), (4096, 4096), (4096, 24576), (12288, 4096)]
 
-    # every projection through the per-op calls of the step, one output buffer each
-    ys = []
+    # every projection through the per-op calls of the step, one output buffer
+    # each: the two calls (qv_quantize_act + qv_w8a8_linear) and the one call
+    # (qv_w8a8_linear_act)
+    ys, ys_act = [], []
     for l in range(st.layers):
         for p, (name, K, N) in enumerate(st.phases):
             xq = st._xq(K)
@@ -46,6 +49,9 @@ def test_qwen3_8b_step_matches_oracle(qv, oracle):
             wq, sw = st.weights[l][p]
             qv.qv_w8a8_linear(xq, st.sx, wq, sw, y, st.ws)
             ys.append(y)
+            ya = torch.full((M, N), float("nan"), device="cuda")
+            qv.qv_w8a8_linear_act(st.inputs[l][p], wq, sw, ya, st.ws_act)
+            ys_act.append(ya)
     torch.cuda.synchronize()
 
     j = 0
@@ -58,6 +64,7 @@ def test_qwen3_8b_step_matches_oracle(qv, oracle):
             xq_r, sx_r = oracle.quantize_rows(bf16_bits(st.inputs[l][p]), bf16=True)
             y_r, _ = oracle.w8a8_linear(xq_r, sx_r, wq_r, sw_r)
             assert np.array_equal(np_(ys[j]).view(np.uint32), y_r.view(np.uint32)), f"layer {l} {name}"
+            assert np.array_equal(np_(ys_act[j]).view(np.uint32), y_r.view(np.uint32)), f"layer {l} {name} (act)"
             j += 1
 
     # the LM head over the whole vocabulary, then drafts that follow the
@@ -84,6 +91,22 @@ def test_qwen3_8b_step_matches_oracle(qv, oracle):
         assert np.array_equal(np_(st.tokens), t_r), rep
         assert np.array_equal(np_(st.max_logit).view(np.uint32), m_r.view(np.uint32)), rep
         assert np.array_equal(np_(st.accept_len), l_r) and np.array_equal(np_(st.out_tokens), o_r), rep
+        name, K, N = st.phases[-1]
+        assert np.array_equal(np_(st.y[: M * N].view(M, N)).view(np.uint32), np_(ys[-1]).view(np.uint32))
+
+    # the same step through the one-call path, eagerly and as a captured graph
+    st.tokens.fill_(-3); st.accept_len.fill_(-3)
+    st.enqueue()
+    torch.cuda.synchronize()
+    g = st.capture()
+    for rep in range(3):
+        if rep:
+            st.tokens.fill_(-3); st.max_logit.fill_(float("nan")); st.accept_len.fill_(-3); st.out_tokens.fill_(-3)
+            g.replay()
+            torch.cuda.synchronize()
+        assert np.array_equal(np_(st.tokens), t_r), ("act", rep)
+        assert np.array_equal(np_(st.max_logit).view(np.uint32), m_r.view(np.uint32)), ("act", rep)
+        assert np.array_equal(np_(st.accept_len), l_r) and np.array_equal(np_(st.out_tokens), o_r), ("act", rep)
         name, K, N = st.phases[-1]
         assert np.array_equal(np_(st.y[: M * N].view(M, N)).view(np.uint32), np_(ys[-1]).view(np.uint32))
     assert qv.qv_device_error() == 0

@@ -48,6 +48,9 @@ def _gemm_part_zero(qv, ws, op_base, M, K, N):
 
 LINEAR_ACT_CASES = [
     (5, 4096, 1024, torch.bfloat16, True),
+    (8, 16, 130, torch.bfloat16, True),       # one K-tile of 16 columns, all 8 rows
+    (2, 4096 + 48, 6 * 128, torch.float32, True),   # ragged last K-tile
+    (6, 12288, 4096, torch.float32, False),   # fp32 rows of 12288
     (5, 4096, 1024, torch.float32, False),
     (1, 16, 7, torch.bfloat16, False),
     (8, 272, 300, torch.float32, True),
@@ -105,6 +108,32 @@ def test_w8a8_linear_act_long_ranges(qv, oracle):
         torch.cuda.synchronize()
         assert np.array_equal(np_(y).view(np.uint32), y_ref.view(np.uint32))
         assert _gemm_part_zero(qv, ws, qv.QV_OP_LINEAR, M, K, N)
+
+
+@pytest.mark.parametrize("M,dtype", [(4, torch.float32), (8, torch.float32), (7, torch.bfloat16)])
+def test_w8a8_linear_act_near_ties(qv, oracle, M, dtype):
+    """Activations whose quotient x/s sits a few ulps from a half-integer,
+    where the product with fl(1/s) can round to the other integer: the codes
+    of the one-call path must still take the IEEE quotient's decision."""
+    K, N = 1024, 384
+    g = np.random.default_rng(23 + M)
+    x = np.zeros((M, K), np.float32)
+    for m in range(M):
+        amax = np.float32(g.uniform(0.5, 4.0))
+        s = np.float32(amax / np.float32(127))
+        j = g.integers(-126, 126, K).astype(np.float32)
+        q = (j + np.float32(0.5)) * s
+        x[m] = np.nextafter(q, np.where(g.random(K) < 0.5, np.inf, -np.inf).astype(np.float32))
+        x[m, 0] = amax
+    xt = torch.from_numpy(x).to(dtype)
+    q_ref, s_ref = _oracle_codes(oracle, xt, None)
+    wq = rand_codes((N, K), seed=M)
+    sw = rand_scales(N, seed=M + 1)
+    y_ref, _ = oracle.w8a8_linear(q_ref, s_ref, np_(wq), np_(sw))
+    y = torch.empty(M, N, device="cuda")
+    qv.qv_w8a8_linear_act(xt.cuda(), wq.cuda(), sw.cuda(), y, qv.workspace(qv.QV_OP_LINEAR_ACT, M, K, N))
+    torch.cuda.synchronize()
+    assert np.array_equal(np_(y).view(np.uint32), y_ref.view(np.uint32))
 
 
 LM_ACT_CASES = [(5, 4096, 3000, True), (1, 128, 130, False), (16, 256, 1000, True),
