@@ -478,14 +478,13 @@ def main():
             del gl2, bxq
             bl_bytes = bs.linear_launch_bytes(fused_act=False)
             b_ach = sum(bl_bytes) / (bl_ms * 1e-3) / 1e9
-            slices = (Mb + 63) // 64
+            slices = (Mb + 79) // 80
             entry = {"B": Bb, "gamma": gm, "M": Mb, "ms_per_step": b_ms, "tokens_per_s": Mb / (b_ms * 1e-3),
                      "weight_stream_gbs": bs.weight_bytes() / (b_ms * 1e-3) / 1e9,
                      "accept_len_mean": float(bs.accept_len.float().mean()),
                      "roofline": {"bound": "hbm", "achieved": b_ach, "peak": peak, "unit": "GB/s",
                                   "frac": b_ach / peak, "traffic": None,
-                                  "kernel": ("w8a8_tc_kernel<64> (tcgen05 on exactly widened codes)" if Mb == 64 else
-                                             "w8a8_tc_kernel<64> for rows 0-63 + w8a8_stream_kernel<2> for the rest"),
+                                  "kernel": f"w8a8_tc_kernel<{64 if Mb <= 64 else 80}> (tcgen05 on exactly widened codes)",
                                   "launches_per_projection": slices,
                                   "bytes_per_launch": sum(bl_bytes) / len(bl_bytes) / slices,
                                   "launch_ms_mean": bl_ms / len(bl_bytes) / slices,

@@ -27,15 +27,15 @@
 //    f16 buffer in the 128-byte-swizzled K-major layout (the B operand);
 //  - warp 8, one thread: issues the tile's eight M=128 x N x K=16 MMAs into a
 //    TMEM accumulator and commits them to an mbarrier;
-//  - the MMAs of up to four consecutive tiles of a channel tile (K = 512:
-//    |sum| <= 512 * 128^2 = 2^23, still exact in fp32) accumulate into one of
+//  - the MMAs of up to eight consecutive tiles of a channel tile (K = 1024:
+//    |sum| <= 1024 * 128^2 = 2^24, still exact in fp32) accumulate into one of
 //    two TMEM accumulators; the converters read a group's accumulator back
 //    (thread = channel, its half of the token columns) while they widen the
-//    next group, convert to int32 and accumulate; at the end of a channel
-//    tile's K range they stage the sums in shared memory for the common
-//    epilogue.
-// A and B rotate through four slots, so widening of tiles i+1..i+3 overlaps
-// the MMAs of tile i.
+//    next group, convert to int32 and add it to the channel tile's running
+//    sums, kept in the epilogue's shared-memory staging buffer, which the
+//    common epilogue reads at the end of the channel tile's K range.
+// A and B rotate through four slots (two at 80 tokens), so widening of the
+// next tiles overlaps the MMAs of tile i.
 
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -57,14 +57,16 @@ constexpr int kTcConv = 8;          // converter warps 0..7
 constexpr int kTcMmaWarp = 8;       // MMA issue and TMEM allocation
 constexpr int kTcProdWarp = 9;      // TMA producer
 constexpr int kTcThreads = 10 * 32;
-constexpr int kTcRing = 4;          // A / B slots
 constexpr int kTcACols = 64;        // TMEM columns of one A slot (128 f16 of K per lane)
-constexpr int kTcGroup = 4;         // tiles accumulated in TMEM before a readout
+constexpr int kTcGroup = 8;         // tiles accumulated in TMEM before a readout
 
 template <int MP>
 struct TcCfg {
     static constexpr int NM = MP < 16 ? 16 : MP;          // MMA N: tokens padded to 16
     static constexpr int MPH = NM / 2;                    // accumulator columns per converter thread
+    // A / B operand slots (four, two at 80 tokens for shared memory; two
+    // were measured as fast as four at 64 tokens)
+    static constexpr int R = MP > 64 ? 2 : 4;
     static constexpr int XBytes = MP * BKB;
     static constexpr int XSlot = ((XBytes + 1023) / 1024) * 1024;
     static constexpr int StageBytes = kWTileBytes + XSlot;
@@ -75,14 +77,15 @@ struct TcCfg {
     // them all on one bank: 32-way conflicts in every staging access)
     static constexpr int SP = MP + 1;
     static constexpr int StgWords = BN * SP;
-    static constexpr int DCol0 = kTcRing * kTcACols;      // first accumulator column
+    static constexpr int DCol0 = R * kTcACols;            // first accumulator column
     static constexpr int TmemCols = 512;
-    static constexpr int SmemBytes = 1024 + Stages * StageBytes + kTcRing * BSlot + StgWords * 4 +
-                                     (2 * Stages + 2 * kTcRing + 2) * 8 + kMaxConsumerWarps * MP * 8 +
+    static constexpr int SmemBytes = 1024 + Stages * StageBytes + R * BSlot + StgWords * 4 +
+                                     (2 * Stages + 2 * R + 2) * 8 + kMaxConsumerWarps * MP * 8 +
                                      MP * 4 + 64;
     static_assert(DCol0 + 2 * NM <= TmemCols, "TMEM budget");
     static_assert(SmemBytes <= 232448, "shared memory budget");
     static_assert(NM % 16 == 0 && NM <= 256, "MMA N");
+    static_assert(MPH % 8 == 0 && (MPH <= 32 || MPH == 40), "accumulator readout widths");
 };
 
 template <int MP>
@@ -90,7 +93,7 @@ struct TcSmem {
     using C = TcCfg<MP>;
     static constexpr int SP = C::SP;
     uint8_t* stages;           // Stages x (W tile | X tile), 1024-aligned
-    uint8_t* bring;            // kTcRing x BSlot f16 activation operands
+    uint8_t* bring;            // R x BSlot f16 activation operands
     int32_t* stg;              // BN x MP staged sums
     uint64_t* full;
     uint64_t* empty;
@@ -109,7 +112,7 @@ struct TcSmem {
         stages = p;
         p += C::Stages * C::StageBytes;
         bring = p;
-        p += kTcRing * C::BSlot;
+        p += C::R * C::BSlot;
         stg = reinterpret_cast<int32_t*>(p);
         p += C::StgWords * 4;
         full = reinterpret_cast<uint64_t*>(p);
@@ -117,9 +120,9 @@ struct TcSmem {
         empty = reinterpret_cast<uint64_t*>(p);
         p += C::Stages * 8;
         aready = reinterpret_cast<uint64_t*>(p);
-        p += kTcRing * 8;
+        p += C::R * 8;
         mdone = reinterpret_cast<uint64_t*>(p);
-        p += kTcRing * 8;
+        p += C::R * 8;
         dfull = reinterpret_cast<uint64_t*>(p);
         p += 2 * 8;
         red = reinterpret_cast<unsigned long long*>(p);
@@ -173,7 +176,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 w8a8_tc_kernel(const __grid_constant__ CUtensorMap tmap_w,
                const __grid_constant__ CUtensorMap tmap_x, const W8A8Params p) {
     using C = TcCfg<MP>;
-    constexpr int NM = C::NM, MPH = C::MPH, Stages = C::Stages, R = kTcRing;
+    constexpr int NM = C::NM, MPH = C::MPH, Stages = C::Stages, R = C::R;
     extern __shared__ uint8_t smem_raw[];
     TcSmem<MP> sm(smem_raw);
 
@@ -225,10 +228,10 @@ w8a8_tc_kernel(const __grid_constant__ CUtensorMap tmap_w,
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_f16_f32(128, NM);
             int gq = -1, pos = kTcGroup;
+            int kt = a % p.KT;                   // K-tile index of tile a + c
             for (int c = 0; c < n; ++c) {
                 const int j = c % R;
-                const int i = a + c;
-                if (c == 0 || i % p.KT == 0 || pos == kTcGroup) { ++gq; pos = 0; }
+                if (c == 0 || kt == 0 || pos == kTcGroup) { ++gq; pos = 0; }
                 if (!mbar_wait_bounded_sleep(&sm.aready[j], (unsigned)(c / R) & 1u, sm.abort, 32))
                     atomicOr(&g_tc_gemm_error, kErrTcWait);
                 tc_fence_after();
@@ -242,7 +245,8 @@ w8a8_tc_kernel(const __grid_constant__ CUtensorMap tmap_w,
                                 idesc, (pos > 0 || t > 0) ? 1u : 0u);
                 umma_commit(&sm.mdone[j]);
                 ++pos;
-                if (c + 1 == n || (i + 1) % p.KT == 0 || pos == kTcGroup) umma_commit(&sm.dfull[gq & 1]);
+                if (++kt == p.KT) kt = 0;
+                if (c + 1 == n || kt == 0 || pos == kTcGroup) umma_commit(&sm.dfull[gq & 1]);
             }
             // Tensor memory stays allocated until the last MMA has completed.
             if (n > 0 && !mbar_wait_timed(&sm.mdone[(n - 1) % R], (unsigned)((n - 1) / R) & 1u))
@@ -267,7 +271,10 @@ w8a8_tc_kernel(const __grid_constant__ CUtensorMap tmap_w,
     consumer_sync<kTcConv>();
     const bool has_tokens = h * MPH < p.M;  // warp-uniform
 
-    int32_t acc[MPH];
+    // The channel tile's running int32 sums live in this thread's part of the
+    // staging buffer (row `row`, tokens h * MPH .. +MPH-1; the odd row stride
+    // keeps a warp's accesses on distinct banks), which the epilogue reads.
+    int32_t* accs = sm.stg + row * C::SP + h * MPH;
     // Group g's accumulator (buffer g & 1) completes on dfull[g & 1], the
     // (g >> 1)-th phase of that barrier.
     auto read_group = [&](int g) {
@@ -275,16 +282,46 @@ w8a8_tc_kernel(const __grid_constant__ CUtensorMap tmap_w,
             atomicOr(&g_tc_gemm_error, kErrTcWait);
         tc_fence_after();
         if (has_tokens) {
-            uint32_t v[MPH];
-            tmem_ld<MPH>(lane_base + (uint32_t)(C::DCol0 + (g & 1) * NM + h * MPH), v);
+            const uint32_t col = lane_base + (uint32_t)(C::DCol0 + (g & 1) * NM + h * MPH);
+            constexpr int V0 = MPH > 32 ? 32 : MPH;   // columns in a first load, the rest (8) in a second
+            uint32_t v[V0], v2[8];
+            tmem_ld<V0>(col, v);
+            if constexpr (MPH > 32) tmem_ld<8>(col + 32, v2);
             tmem_ld_wait();
 #pragma unroll
-            for (int m = 0; m < MPH; ++m) acc[m] += __float2int_rn(__uint_as_float(v[m]));
+            for (int m = 0; m < V0; ++m)
+                if (h * MPH + m < MP) accs[m] += __float2int_rn(__uint_as_float(v[m]));
+            if constexpr (MPH > 32) {
+#pragma unroll
+                for (int m = 0; m < 8; ++m) accs[32 + m] += __float2int_rn(__uint_as_float(v2[m]));
+            }
         }
     };
     int gq = -1, pos = kTcGroup;             // group of the current tile, position in it
     int rq = 0;                              // next group to read out
 
+    // Shared-memory words of one tile held in registers: this thread's 64
+    // weight bytes and its share of the activation codes. Within a segment,
+    // tile c + 1's words are loaded (its stage waited for first) once tile
+    // c's A operand is stored, so their latency overlaps the B widening and
+    // the hand-off of tile c.
+    constexpr int XI = (MP * 8 + kTcConv * 32 - 1) / (kTcConv * 32);   // activation items per thread
+    auto load_tile = [&](int c, uint4 (&w)[4], uint4 (&x)[XI]) {
+        const int s = c % Stages;
+        if (!tc_wait(&sm.full[s], (unsigned)(c / Stages) & 1u, sm.abort))
+            atomicOr(&g_tc_gemm_error, kErrFullWait);
+        const uint8_t* wrow = sm.w_tile(s) + row * BKB;
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            w[u] = *reinterpret_cast<const uint4*>(wrow + (((4 * h + u) ^ (row & 7)) << 4));
+#pragma unroll
+        for (int q = 0; q < XI; ++q) {
+            const int e = tid + q * kTcConv * 32;
+            const int xr = e >> 3, xc = e & 7;
+            x[q] = e < MP * 8 ? *reinterpret_cast<const uint4*>(sm.x_tile(s) + xr * BKB + ((xc ^ (xr & 7)) << 4))
+                              : make_uint4(0u, 0u, 0u, 0u);
+        }
+    };
     int i = a;
     while (i < b) {
         const int nt = i / p.KT;
@@ -292,14 +329,15 @@ w8a8_tc_kernel(const __grid_constant__ CUtensorMap tmap_w,
         const int seg_end = min(b, (nt + 1) * p.KT);
         segment_start<EPI>(est, p, nt, tid);
 #pragma unroll
-        for (int m = 0; m < MPH; ++m) acc[m] = 0;
+        for (int m = 0; m < MPH; ++m)
+            if (h * MPH + m < MP) accs[m] = 0;
 
         for (; i < seg_end; ++i) {
             const int c = i - a;
             const int s = c % Stages, j = c % R;
-            if (c == 0 || i % p.KT == 0 || pos == kTcGroup) { ++gq; pos = 0; }
-            if (!tc_wait(&sm.full[s], (unsigned)(c / Stages) & 1u, sm.abort))
-                atomicOr(&g_tc_gemm_error, kErrFullWait);
+            if (i == seg_begin || pos == kTcGroup) { ++gq; pos = 0; }
+            uint4 wv[4], xv[XI];
+            load_tile(c, wv, xv);
             // Slot j is free once the MMAs of tile c - R have completed.
             if (c >= R && !tc_wait(&sm.mdone[j], (unsigned)((c - R) / R) & 1u, sm.abort))
                 atomicOr(&g_tc_gemm_error, kErrTcWait);
@@ -313,22 +351,6 @@ w8a8_tc_kernel(const __grid_constant__ CUtensorMap tmap_w,
                 while (rq < gq) read_group(rq++);
             ++pos;
 
-            // All shared-memory loads of the tile first (this thread's 64 weight
-            // bytes, its share of the activation codes), then the widening.
-            const uint8_t* wrow = sm.w_tile(s) + row * BKB;
-            uint4 wv[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u)
-                wv[u] = *reinterpret_cast<const uint4*>(wrow + (((4 * h + u) ^ (row & 7)) << 4));
-            constexpr int XI = (MP * 8 + kTcConv * 32 - 1) / (kTcConv * 32);   // items per thread
-            uint4 xv[XI];
-#pragma unroll
-            for (int q = 0; q < XI; ++q) {
-                const int e = tid + q * kTcConv * 32;
-                const int xr = e >> 3, xc = e & 7;
-                xv[q] = e < MP * 8 ? *reinterpret_cast<const uint4*>(sm.x_tile(s) + xr * BKB + ((xc ^ (xr & 7)) << 4))
-                                   : make_uint4(0u, 0u, 0u, 0u);
-            }
             // A: 32 f16x2 words into this thread's TMEM lane.
             uint32_t av[32];
 #pragma unroll
@@ -366,17 +388,11 @@ w8a8_tc_kernel(const __grid_constant__ CUtensorMap tmap_w,
                 mbar_arrive(&sm.empty[s]);
                 mbar_arrive(&sm.aready[j]);
             }
-        }
-        // Segment end: read the remaining accumulators of this channel tile.
-        while (rq <= gq) read_group(rq++);
 
-        if (has_tokens) {
-#pragma unroll
-            for (int m = 0; m < MPH; ++m) {
-                const int tok = h * MPH + m;
-                if (tok < MP) sm.stg[row * C::SP + tok] = acc[m];
-            }
         }
+        // Segment end: read the remaining accumulators of this channel tile
+        // (the sums are then complete in the staging buffer).
+        while (rq <= gq) read_group(rq++);
         consumer_sync<kTcConv>();
         segment_end<MP, kTcConv, EPI>(sm, p, nt, seg_begin, seg_end - seg_begin, tid, est, &g_tc_gemm_error);
     }
@@ -430,6 +446,7 @@ cudaError_t launch_w8a8_tc(const W8A8Launch& a, int num_sms, cudaStream_t s) {
                   : a.epi == Epi::SwiGLU ? QV_TC_LAUNCH(MPV, Epi::SwiGLU) : QV_TC_LAUNCH(MPV, Epi::Linear);
     switch (a.MP) {   // fewer tokens go to the mma.sync streaming kernel
         QV_TC_CASE(64)
+        QV_TC_CASE(80)
         default: return cudaErrorInvalidValue;
     }
 #undef QV_TC_CASE

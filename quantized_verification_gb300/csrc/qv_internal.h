@@ -18,9 +18,11 @@ constexpr unsigned long long kWaitLimitNs = 1000000000ull;
 constexpr int kTileN = 128;
 constexpr int kTileKBytes = 128;
 
-// Largest padded token count one streaming-GEMM launch handles; larger M is
-// processed in slices of this many rows.
-constexpr int kMaxMPerLaunch = 64;
+// Largest padded token count one W8A8 GEMM launch handles (the tcgen05
+// kernel takes 64 or 80 token columns); larger M is processed in slices of
+// this many rows. The BF16 comparator's launches take up to 64.
+constexpr int kMaxMPerLaunch = 80;
+constexpr int kMaxMPerLaunchBf16 = 64;
 
 inline int ceil_div(long long a, long long b) { return (int)((a + b - 1) / b); }
 inline int pad_tokens(int m) { return ((m + 7) / 8) * 8; }

@@ -206,7 +206,7 @@ __device__ __forceinline__ void gather_partials(SM& sm, unsigned long long* slot
     // every round of loads is one L2 round trip, so with many token rows
     // each thread keeps more pairs in flight (a split tile has few
     // contributors then); QP * CB stays 16 to bound the registers.
-    constexpr int QP = MP >= 32 ? 4 : 2;
+    constexpr int QP = MP >= 64 ? 8 : MP >= 32 ? 4 : 2;
     constexpr int CB = 16 / QP;
     constexpr int SP = SM::SP;
     const int c1 = blockIdx.x + 1;
@@ -310,8 +310,8 @@ struct EpiState {
 // finish needs, so that its latency hides behind the segment's MMAs.
 template <int EPI>
 __device__ __forceinline__ void segment_start(EpiState& st, const W8A8Params& p, int nt, int tid) {
-    const int n = nt * BN + tid;
-    st.swn = (tid < BN && n < p.N) ? __ldg(&p.sw[n]) : 0.f;
+    const int n = nt * BN + (tid & (BN - 1));
+    st.swn = n < p.N ? __ldg(&p.sw[n]) : 0.f;
     if (EPI == (int)Epi::SwiGLU) st.swn_up = (tid < BN / 2 && n + BN / 2 < p.N) ? __ldg(&p.sw[n + BN / 2]) : 0.f;
 }
 
@@ -320,30 +320,29 @@ template <int MP, int CW, int EPI, class SM>
 __device__ __forceinline__ void finish_tile(SM& sm, const W8A8Params& p, int nt, int tid, EpiState& st) {
     constexpr int SP = SM::SP;
     const int warp = tid >> 5, lane = tid & 31;
-    // the first BN consumer threads (warps 0..3) own one output channel each
+    // SwiGLU and the LM head: the first BN consumer threads (warps 0..3) own
+    // one output channel each
     const int r = tid;
     const int n = nt * BN + r;
     const bool valid = r < BN && n < p.N;
-    int32_t acc[MP];
-#pragma unroll
-    for (int m = 0; m < MP; ++m) acc[m] = 0;
-    if (valid) {
-#pragma unroll
-        for (int m = 0; m < MP; ++m)
-            if (m < p.M) acc[m] = sm.stg[r * SP + m];
-    }
     const float swn = st.swn;
     if (EPI == (int)Epi::Linear) {
-        if (valid) {
-#pragma unroll
-            for (int m = 0; m < MP; ++m) {
+        // TH threads per channel (all CW warps when there are many tokens),
+        // thread h of a channel taking tokens h, h + TH, ...
+        constexpr int TH = (MP >= 32 && CW * 32 >= 2 * BN) ? 2 : 1;
+        const int rr = tid & (BN - 1), h = tid / BN;
+        const int nn = nt * BN + rr;
+        if (h < TH && nn < p.N) {
+#pragma unroll 4
+            for (int m = h; m < MP; m += TH) {
                 if (m < p.M) {
-                    if (p.acc_debug) p.acc_debug[(size_t)m * p.N + n] = acc[m];
-                    const float yv = __fmul_rn(__int2float_rn(acc[m]), __fmul_rn(sm.sx[m], swn));
+                    const int32_t am = sm.stg[rr * SP + m];
+                    if (p.acc_debug) p.acc_debug[(size_t)m * p.N + nn] = am;
+                    const float yv = __fmul_rn(__int2float_rn(am), __fmul_rn(sm.sx[m], swn));
                     if (p.y_bf16)
-                        reinterpret_cast<__nv_bfloat16*>(p.y)[(size_t)m * p.N + n] = __float2bfloat16_rn(yv);
+                        reinterpret_cast<__nv_bfloat16*>(p.y)[(size_t)m * p.N + nn] = __float2bfloat16_rn(yv);
                     else
-                        reinterpret_cast<float*>(p.y)[(size_t)m * p.N + n] = yv;
+                        reinterpret_cast<float*>(p.y)[(size_t)m * p.N + nn] = yv;
                 }
             }
         }
@@ -365,27 +364,38 @@ __device__ __forceinline__ void finish_tile(SM& sm, const W8A8Params& p, int nt,
             }
         }
     } else {
-        if (r < BN) {
-#pragma unroll
-            for (int m = 0; m < MP; ++m) {
+        // TH threads per channel as in the linear epilogue: warp w covers
+        // channels 32 * (w % 4) .. +31 of the tile and tokens m = w / 4 mod TH.
+        // A token's best key over the warp's channels is the largest
+        // order-preserving logit bits, then the largest 0xFFFFFFFF - n among
+        // the lanes holding them (the lowest index), each one warp reduction.
+        constexpr int TH = (MP >= 32 && CW * 32 >= 2 * BN) ? 2 : 1;
+        const int rr = tid & (BN - 1), h = tid / BN;
+        const int nn = nt * BN + rr;
+        const bool ok = nn < p.N;
+        if (h < TH) {
+#pragma unroll 4
+            for (int m = h; m < MP; m += TH) {
                 if (m < p.M) {
-                    unsigned long long key = 0ull;
-                    if (valid) {
-                        const float yv = __fmul_rn(__int2float_rn(acc[m]), __fmul_rn(sm.sx[m], swn));
-                        key = ((unsigned long long)ordered_bits(yv) << 32) |
-                              (unsigned long long)(0xFFFFFFFFu - (unsigned)n);
+                    unsigned o = 0u, k2 = 0u;
+                    if (ok) {
+                        const float yv = __fmul_rn(__int2float_rn(sm.stg[rr * SP + m]), __fmul_rn(sm.sx[m], swn));
+                        o = ordered_bits(yv);
+                        k2 = 0xFFFFFFFFu - (unsigned)nn;
                     }
-                    key = warp_max_u64(key);
-                    if (lane == 0) sm.red[warp * MP + m] = key;
+                    const unsigned om = __reduce_max_sync(0xffffffffu, o);
+                    const unsigned km = __reduce_max_sync(0xffffffffu, o == om ? k2 : 0u);
+                    if (lane == 0) sm.red[warp * MP + m] = ((unsigned long long)om << 32) | km;
                 }
             }
         }
         consumer_sync<CW>();
         if (tid < p.M) {
-            unsigned long long k = sm.red[tid];
+            const int w0 = (tid % TH) * (BN / 32);
+            unsigned long long k = sm.red[w0 * MP + tid];
 #pragma unroll
             for (int w = 1; w < BN / 32; ++w) {
-                const unsigned long long o = sm.red[w * MP + tid];
+                const unsigned long long o = sm.red[(w0 + w) * MP + tid];
                 k = o > k ? o : k;
             }
             atomicMax(&p.keys[tid], k);

@@ -422,11 +422,11 @@ class VerifyStack:
     def launches_per_step(self, fused: bool = False) -> int:
         """Kernels one step launches. fused: the persistent qv_verify_stack
         path. Otherwise the per-op path: per projection and for the LM head a
-        quantization kernel and one GEMM launch per 64 tokens; plus qv_accept
+        quantization kernel and one GEMM launch per 80 tokens; plus qv_accept
         (the same count for enqueue and enqueue_two_call)."""
         if fused:
             return (self.layers * len(self.phases) + 1 + 149) // 150
-        return (self.layers * len(self.phases) + 1) * (1 + (self.M + 63) // 64) + 1
+        return (self.layers * len(self.phases) + 1) * (1 + (self.M + 79) // 80) + 1
 
     # ------------------------------------------------------------------ fused step
     def _fused_descs(self):

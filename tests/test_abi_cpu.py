@@ -45,7 +45,8 @@ def test_workspace_sizes(lib):
     assert qv.qv_workspace_bytes(qv.QV_OP_LINEAR, 5, 4096, 1000) == slots8
     assert qv.qv_workspace_bytes(qv.QV_OP_BF16_LINEAR, 5, 4096, 1000) == slots8
     assert qv.qv_workspace_bytes(qv.QV_OP_LINEAR, 17, 4096, 1000) == 4 * slots8       # MP = 32
-    assert qv.qv_workspace_bytes(qv.QV_OP_LINEAR, 200, 4096, 1000) == 8 * slots8      # 64-row slices
+    assert qv.qv_workspace_bytes(qv.QV_OP_LINEAR, 200, 4096, 1000) == 10 * slots8     # 80-row slices
+    assert qv.qv_workspace_bytes(qv.QV_OP_BF16_LINEAR, 200, 4096, 1000) == 8 * slots8  # 64-row slices
     # LM head: slots + per-token keys + the done counter on its own lines
     assert qv.qv_workspace_bytes(qv.QV_OP_LM_HEAD, 5, 4096, 151936) == slots8 + 8 * 8 + 5 * 128
     assert qv.qv_workspace_bytes(qv.QV_OP_LINEAR, 0, 4096, 16) == 0

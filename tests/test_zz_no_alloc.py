@@ -28,9 +28,9 @@ def _c(t):
     return ctypes.c_void_p(t.data_ptr()) if t is not None else None
 
 
-# (M, K, N, y dtype): up to 8, 16 and 64 token rows in one launch; 80 and
-# 256 rows take two and four launches in a row, each reusing the scratch
-# the one before it left zeroed; a bf16 output
+# (M, K, N, y dtype): up to 8, 16, 64 and 80 token rows in one launch; 256
+# rows take four launches in a row, each reusing the scratch the one before
+# it left zeroed; a bf16 output
 @pytest.mark.parametrize("M,K,N,ydt", [(5, 4096, 1024, torch.float32), (4, 256, 512, torch.float32),
                                        (16, 272, 1000, torch.float32), (64, 256, 200, torch.float32),
                                        (80, 512, 384, torch.float32), (256, 256, 300, torch.float32),
