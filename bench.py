@@ -41,8 +41,8 @@ FALLBACK_HBM_GBS = 6800.0
 # launch (4096 -> 24576, M = 5) over its algorithmic bytes. Valid only for the
 # kernel sources whose sha256 is recorded (kernel_source_sha); roofline.traffic
 # is null otherwise.
-NCU_TRAFFIC = {"source_sha256": "cebf5b3d717714bd0af8408eb180b006e00e18b47949377ca6b53dc29b4ff8b2",
-               "dram_bytes_per_algorithmic_byte": (101710848 + 2524416) / 101273620}
+NCU_TRAFFIC = {"source_sha256": "8e50837b19721d7e6a62555628b773956fb160fb28452c5116cb8829f7503c04",
+               "dram_bytes_per_algorithmic_byte": (101741312 + 2769152) / 101273620}
 
 
 def log(*a):
