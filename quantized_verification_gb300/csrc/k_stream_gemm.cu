@@ -1294,7 +1294,7 @@ cudaError_t launch_w8a8_stream(const W8A8Launch& a, int num_sms, cudaStream_t s)
 #define QV_W8A8_CASE(NGV)                                                                    \
     case NGV:                                                                                \
         return a.w4 ? QV_W8A8_EPI(NGV, 1) : QV_W8A8_EPI(NGV, 0);
-    switch (a.MP / 8) {   // up to 32 tokens; more go to the tcgen05 kernel
+    switch (a.MP / 8) {   // W8A8 up to 16 tokens (more go to the tcgen05 kernel), W4A8 up to 32
         QV_W8A8_CASE(1)
         QV_W8A8_CASE(2)
         QV_W8A8_CASE(4)

@@ -445,6 +445,7 @@ cudaError_t launch_w8a8_tc(const W8A8Launch& a, int num_sms, cudaStream_t s) {
         return lm ? QV_TC_LAUNCH(MPV, Epi::LmHead)                                                \
                   : a.epi == Epi::SwiGLU ? QV_TC_LAUNCH(MPV, Epi::SwiGLU) : QV_TC_LAUNCH(MPV, Epi::Linear);
     switch (a.MP) {   // fewer tokens go to the mma.sync streaming kernel
+        QV_TC_CASE(32)
         QV_TC_CASE(64)
         QV_TC_CASE(80)
         default: return cudaErrorInvalidValue;

@@ -113,15 +113,16 @@ qv_status encode_2d(CUtensorMap* map, CUtensorMapDataType dt, size_t elem_bytes,
     return QV_OK;
 }
 
-// W8A8 streaming GEMM kernel by padded token count. Up to 32 tokens the
-// int8 mma.sync kernel keeps pace with HBM (at 32 tokens it is still 10-15 %
-// faster than the tcgen05 kernel on every Qwen3-8B projection); at 64 tokens
-// mma.sync is compute-bound and the tcgen05 kernel (exact f16 widening, TMEM
-// accumulators), whose per-tile cost hardly grows with the token count, takes
-// over (measured on GB300).
+// W8A8 streaming GEMM kernel by padded token count. Up to 16 tokens the
+// int8 (8) or f16 (16) mma.sync kernel keeps pace with HBM; from 32 tokens
+// mma.sync is latency- or compute-bound and the tcgen05 kernel (exact f16
+// widening, TMEM accumulators), whose per-tile cost hardly grows with the
+// token count, is faster (measured on GB300 at 32 tokens: gate|up 33.8 vs
+// 36.8 us, LM head 166 vs 195 us, qkv level). Packed int4 weights always use
+// the streaming kernel.
 cudaError_t launch_w8a8(const qv::W8A8Launch& L, int sms, cudaStream_t s) {
     if (L.w4 && L.MP > qv::kMaxMPerLaunchW4) return cudaErrorInvalidValue;
-    if (L.MP >= 64) return qv::launch_w8a8_tc(L, sms, s);
+    if (!L.w4 && L.MP >= 32) return qv::launch_w8a8_tc(L, sms, s);
     return qv::launch_w8a8_stream(L, sms, s);
 }
 

@@ -183,7 +183,7 @@ def _silu_times(oracle, gate: np.ndarray, up: np.ndarray) -> np.ndarray:
 @pytest.mark.parametrize("M,K,F", [(5, 256, 64), (17, 512, 192), (5, 4096, 1024), (64, 256, 128), (80, 128, 256)])
 def test_w8a8_swiglu(qv, oracle, M, K, F):
     """The gate|up linear with SiLU(gate) * up in its epilogue (interleaved
-    rows; mma.sync kernel up to 32 tokens, tcgen05 at 64 and 80, 80-row
+    rows; mma.sync kernel up to 16 tokens, tcgen05 at 32, 64 and 80, 80-row
     slices beyond): a equals fl32(silu(y_gate) * y_up) of the oracle's linear."""
     from gpu_util import rand_codes, rand_scales
     xq = rand_codes((M, K), seed=M + 3 * K)

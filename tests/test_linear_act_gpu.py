@@ -1,7 +1,8 @@
 """qv_w8a8_linear_act / qv_lm_head_argmax_act (activation quantization kernel,
 then the streaming GEMM, in one call) against the oracle chain quantize_rows -> w8a8_linear
 / lm_head_argmax, bit for bit, and against the two-call GPU path. Covers the
-int8 mma.sync GEMM (up to 32 padded tokens) and the tcgen05 GEMM (64)."""
+int8 / f16 mma.sync GEMM (up to 16 padded tokens) and the tcgen05 GEMM (32
+to 80)."""
 import numpy as np
 import pytest
 import torch
@@ -57,12 +58,13 @@ LINEAR_ACT_CASES = [
     (9, 512, 384, torch.bfloat16, True),
     (16, 12288, 512, torch.bfloat16, True),
     (5, 12288, 4096, torch.bfloat16, True),
-    (17, 256, 200, torch.bfloat16, True),     # 32 padded tokens, mma.sync GEMM
+    (17, 256, 200, torch.bfloat16, True),     # 32 padded tokens, tcgen05 GEMM
     (64, 1024, 256, torch.float32, True),     # tcgen05 GEMM (separate quantization kernel)
     (3, 12288, 300, torch.float32, True),     # fp32 rows longer than the quantizer keeps in registers
     (20, 16, 7, torch.bfloat16, True),        # a single GEMM tile
     (9, 128, 130, torch.float32, False),      # two GEMM CTAs
-    (32, 4096, 1024, torch.bfloat16, True),   # 32 tokens, the most the mma.sync kernel takes
+    (32, 4096, 1024, torch.bfloat16, True),   # 32 tokens, the fewest the tcgen05 kernel takes
+    (16, 4096, 1024, torch.bfloat16, True),   # 16 tokens, the most the mma.sync kernel takes
 ]
 
 
