@@ -631,13 +631,13 @@ QV_API int qv_num_sms(void);
  *     that device (once); make that first call before any stream capture.
  *   - Shapes whose workspace, qv_workspace_bytes(QV_OP_LINEAR, M, K, N), is
  *     larger than the buffer are rejected with QV_ERR_UNSUPPORTED. With the
- *     present workspace layout (split-K slots of at most 10.5 MB, at M > 32)
+ *     present workspace layout (split-K slots of at most 13.1 MB, at M > 64)
  *     every shape that qv_w8a8_linear accepts fits.
  *   - The address is looked up again when the current context of the device
  *     changes (after cudaDeviceReset the module, and the buffer, are loaded
  *     anew).
  *   - Each call clears the part of the buffer it uses (cudaMemsetAsync on
- *     `stream`, 1.3 MB for up to 8 token rows, 10.5 MB above 32) before its
+ *     `stream`, 1.3 MB for up to 8 token rows, 13.1 MB above 64) before its
  *     kernel runs: a completed call leaves that part zeroed, but a call that
  *     gave up on a wait limit (qv_device_error reports it) may leave partial
  *     sums behind, and the caller has no other way to clear the buffer.
