@@ -514,7 +514,6 @@ bf16_stream_kernel(const __grid_constant__ CUtensorMap tmap_w,
     constexpr int MP = C::MP;
     constexpr int Stages = C::Stages;
     constexpr int CW = kBf16Warps;
-    constexpr int CT = CW * 32;
     constexpr int RW = BN / CW;
     constexpr int BPW = RW / 16;
     extern __shared__ uint8_t smem_raw[];
@@ -867,7 +866,7 @@ verify_stack_kernel(const __grid_constant__ StackParams sp) {
         const uint64_t pol_w = policy_evict_first();
         const uint64_t pol_x = policy_evict_last();
         prefetch_tensormap(&sp.tmap_x);
-        int pend_st[Stages], pend_ph[Stages], pend_kt[Stages];   // activation loads not yet issued
+        int pend_st[Stages] = {}, pend_ph[Stages] = {}, pend_kt[Stages] = {};   // activation loads not yet issued
         int pend_head = 0, pend_n = 0;
         int ready = -1;                                           // last phase with B(p) complete
         // Polls the barrier counter (one L2 round trip) only while an

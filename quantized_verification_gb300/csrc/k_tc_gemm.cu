@@ -401,6 +401,28 @@ w8a8_tc_kernel(const __grid_constant__ CUtensorMap tmap_w,
     named_bar_sync(2, (kTcConv + 1) * 32);
 }
 
+// Grid of the tcgen05 kernel: the fewest tiles per CTA s >= T / SMs that
+// divide the K-tiles of a channel tile, so that every CTA's range is one
+// segment of one channel tile, as long as that keeps at least 60 % of the
+// SMs busy (80 % at 32 tokens, where qkv on 96 CTAs measured 15.7 against
+// 14.7 us); otherwise one CTA per SM. With many tokens a split channel tile
+// moves MP x 128 partial sums per contributor, and a range that straddles two
+// channel tiles pays two segment ends: on the Qwen3-8B shapes at 64 tokens
+// this took o from 20.2 to 16.2 us (128 CTAs of 8 tiles), qkv from 19.9 to
+// 18.3 (96 x 16) and down from 29.9 to 27.0 (128 x 24). Ranges of whole
+// channel tiles (gate|up on 96 CTAs: 50.2 against 40.3 us) and a 50 % floor
+// (the Qwen3-32B shapes on 80 CTAs) measured slower.
+int tc_grid(long long T, int KT, int MP, int num_sms) {
+    const int g0 = stream_grid(T, num_sms);
+    const long long floor10 = MP <= 32 ? 8 : 6;   // tenths of the SMs
+    for (long long sz = (T + num_sms - 1) / num_sms; sz <= KT; ++sz) {
+        if (KT % sz != 0) continue;
+        const long long g = T / sz;
+        return (10 * g >= floor10 * num_sms && g <= g0) ? (int)g : g0;
+    }
+    return g0;
+}
+
 template <class P, class... Args>
 cudaError_t launch_tc(void (*kern)(Args...), int grid, int smem, cudaStream_t s,
                       const CUtensorMap& tw, const CUtensorMap& tx, const P& params) {
@@ -437,7 +459,7 @@ cudaError_t launch_w8a8_tc(const W8A8Launch& a, int num_sms, cudaStream_t s) {
     p.drop_partials = 0;
     p.keys = reinterpret_cast<unsigned long long*>(ws + L.keys);
     p.done = reinterpret_cast<unsigned*>(ws + L.done);
-    const int grid = stream_grid(p.T, num_sms);
+    const int grid = tc_grid(p.T, p.KT, a.MP, num_sms);
 #define QV_TC_LAUNCH(MPV, EPIV) \
     launch_tc(w8a8_tc_kernel<MPV, (int)EPIV>, grid, TcCfg<MPV>::SmemBytes, s, a.tmap_w, a.tmap_x, p)
 #define QV_TC_CASE(MPV)                                                                           \

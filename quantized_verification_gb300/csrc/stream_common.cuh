@@ -320,11 +320,8 @@ template <int MP, int CW, int EPI, class SM>
 __device__ __forceinline__ void finish_tile(SM& sm, const W8A8Params& p, int nt, int tid, EpiState& st) {
     constexpr int SP = SM::SP;
     const int warp = tid >> 5, lane = tid & 31;
-    // SwiGLU and the LM head: the first BN consumer threads (warps 0..3) own
-    // one output channel each
+    // SwiGLU: the first BN / 2 consumer threads own one feature each
     const int r = tid;
-    const int n = nt * BN + r;
-    const bool valid = r < BN && n < p.N;
     const float swn = st.swn;
     if (EPI == (int)Epi::Linear) {
         // TH threads per channel (all CW warps when there are many tokens),
