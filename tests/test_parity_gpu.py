@@ -81,6 +81,11 @@ LINEAR_CASES = [
     (9, 512, 384), (16, 384, 256), (17, 256, 200), (32, 640, 256), (33, 256, 129),
     (64, 512, 256), (65, 256, 128), (80, 512, 300), (256, 256, 136), (5, 16, 7),
     (24, 4096, 4096), (32, 12288, 3000),
+    # tcgen05 grids of whole segments (tiles per CTA dividing the 32 or 96
+    # K-tiles: 128 x 8, 96 x 16, 128 x 24) at Qwen3-8B sizes
+    (64, 4096, 4096), (80, 4096, 6144), (64, 12288, 4096),
+    # more than 80 rows: the fewest launches of equal row counts
+    (81, 256, 130), (96, 256, 300), (128, 512, 256), (161, 128, 200),
 ]
 
 
@@ -168,7 +173,8 @@ def test_w8a8_quantize_chain(qv, oracle):
 # a3 LM head + argmax
 # ---------------------------------------------------------------------------
 LM_CASES = [(4, 256, 1024), (5, 4096, 3000), (1, 128, 130), (9, 256, 1000), (64, 256, 513),
-            (80, 128, 777), (5, 512, 128 * 160 + 3), (32, 4096, 3000), (24, 512, 128 * 160 + 3)]
+            (80, 128, 777), (5, 512, 128 * 160 + 3), (32, 4096, 3000), (24, 512, 128 * 160 + 3),
+            (72, 512, 2000), (96, 256, 1000)]
 
 
 def _run_lm(qv, xq, sx, wq, sw):
