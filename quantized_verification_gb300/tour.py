@@ -3,22 +3,24 @@ profiler's launch list or a per-kernel capture.
 
     python -m quantized_verification_gb300.tour [--passes 2]
 
-Each pass makes the same 18 launches in the same order (the first pass is
-the warm-up a capture skips with ``-s 18``; a capture filtered with ``-k``
-skips the matching launches of one pass):
+Each pass makes the same 18 launches in the same order. Before the first
+pass the set-up quantizes the weights (one quantize_rows_kernel and one
+quantize_weight_w4_kernel launch), so a capture of the second pass filtered
+with ``-k`` on the kernels below skips 19 matching launches (``-s 19 -c 18``):
 
     quantize_rows_kernel                  per-token int8 activation codes, 5 x 4096
     w8a8_stream_kernel<1, Linear>         5 x 4096 -> 24576 (Qwen3-8B gate+up), fp32 out
     w8a8_stream_kernel<1, Linear, W4>     the same shape with packed int4 weights (50.3 MB)
     w8a8_stream_kernel<1, SwiGLU>         the same weights interleaved, SiLU(g)*u fused
     w8a8_tc_kernel<64, Linear>            64 tokens, tcgen05 on widened codes
+    w8a8_tc_kernel<80, Linear>            80 tokens, the same
     bf16_stream_kernel<1>                 the BF16 comparator, 5 x 4096 -> 24576
     residual_rmsnorm_quant_kernel         h += d, RMSNorm, int8 codes, 5 x 4096
     swiglu_quant_kernel                   SiLU(g)*u and its int8 codes, 5 x 12288
     spec_{max,sums,decide,chunk,draw}     sampling at T > 0, 1 x (4 + 1) rows x 151936
     tree_accept_kernel                    a 16-node draft tree
     accept_kernel                         greedy acceptance, 1 x 5
-    attn_chunk_kernel, attn_combine_kernel attention of 5 tokens over a 2048-position
+    attn_cluster_kernel<128, 8>           attention of 5 tokens over a 2048-position
                                           cache, 32/8 heads, D = 128
     logit_fidelity_kernel                 KL and top-1 of 5 rows x 151936 logits
 
@@ -56,10 +58,13 @@ def main(argv=None):
     qv.qv_quantize_weight_w4(w, wq4, sw4)
     y = torch.empty(M, N, device=dev)
     a = torch.empty(M, F, device=dev)
-    ws = qv.workspace(qv.QV_OP_LINEAR, 64, K, N)
+    ws = qv.workspace(qv.QV_OP_LINEAR, 80, K, N)
     x64 = torch.randint(-127, 128, (64, K), dtype=torch.int8, device=dev, generator=g)
     sx64 = torch.rand(64, device=dev, generator=g) * 1e-2
     y64 = torch.empty(64, N, device=dev)
+    x80 = torch.randint(-127, 128, (80, K), dtype=torch.int8, device=dev, generator=g)
+    sx80 = torch.rand(80, device=dev, generator=g) * 1e-2
+    y80 = torch.empty(80, N, device=dev)
     wsb = qv.workspace(qv.QV_OP_BF16_LINEAR, M, K, N)
     h = synth.activations(M, K, 3, device=dev)
     d = synth.activations(M, K, 4, device=dev)
@@ -99,6 +104,7 @@ def main(argv=None):
         qv.qv_w4a8_linear(xq, sx, wq4, sw4, y, ws)
         qv.qv_w8a8_swiglu(xq, sx, wq_il, sw_il, a, ws)
         qv.qv_w8a8_linear(x64, sx64, wq, sw, y64, ws)
+        qv.qv_w8a8_linear(x80, sx80, wq, sw, y80, ws)
         qv.qv_bf16_linear(x, w, y, wsb)
         qv.qv_rmsnorm_quant(h, gamma_w, xq2, sx2, delta=d)
         qv.qv_swiglu_quant(gu, xqf, sx2)
