@@ -659,9 +659,9 @@ cudaError_t launch_ex(void (*kern)(Args...), int grid, int threads, int smem, cu
 // one cooperative launch (one CTA per SM, all resident).
 //
 //  - The producer warp streams the weight tiles of every phase, in phase
-//    order, through a deep ring; weights never depend on activations, so it
-//    runs ahead across phase boundaries and HBM stays busy while consumers
-//    wait for the previous phase.
+//    order, through a 6-stage ring; weights never depend on activations, so
+//    it runs ahead across phase boundaries while consumers wait for the
+//    previous phase.
 //  - Consumers start phase p once every CTA has finished phase p-1 (a grid
 //    barrier: an arrival counter in the workspace, read with acquire loads,
 //    waited on for at most kWaitLimitNs). They compute the per-token scales of
@@ -707,7 +707,11 @@ struct StackCfg {
     static constexpr int XBytes = MP * BKB;
     static constexpr int XSlot = ((XBytes + 1023) / 1024) * 1024;
     static constexpr int StageBytes = kWTileBytes + XSlot;
-    static constexpr int Stages = NG == 1 ? 12 : 11;
+    // A deeper ring (12 stages, with a warp prefetching 24 tiles further into
+    // L2) made the step slower, 3.81 against 3.09 ms at 5 tokens: CTAs that
+    // finish a phase early stream the next one and take bandwidth from the
+    // ones the grid barrier waits for. 4 to 7 stages measured alike.
+    static constexpr int Stages = 6;
     static constexpr int StgWords = BN * MP;
     static constexpr int SmemBytes = 1024 + Stages * StageBytes + StgWords * 4 + 2 * Stages * 8 +
                                      kMaxConsumerWarps * MP * 8 + 3 * MP * 4 +
@@ -777,12 +781,8 @@ __device__ __forceinline__ void unpack_vec(const uint4& r, bool bf16, float (&e)
     }
 }
 
-// Weight tiles the L2 prefetch warp of the stack kernel runs ahead of the
-// shared-memory producer (per CTA; 24 tiles = 384 KB, 58 MB over 152 SMs).
-constexpr int kStackL2Ahead = 24;
-
 template <int NG>
-__global__ void __launch_bounds__((kW8A8Warps + 2) * 32, 1)
+__global__ void __launch_bounds__((kW8A8Warps + 1) * 32, 1)
 verify_stack_kernel(const __grid_constant__ StackParams sp) {
     using C = StackCfg<NG>;
     constexpr int MP = C::MP;
@@ -805,7 +805,6 @@ verify_stack_kernel(const __grid_constant__ StackParams sp) {
     float* s_amax = reinterpret_cast<float*>(s_tok + MP);        // [warp][MP]
     volatile int* abort = reinterpret_cast<volatile int*>(s_amax + kMaxConsumerWarps * MP);
     volatile int* flag = abort + 1;
-    volatile long long* s_issued = reinterpret_cast<volatile long long*>(abort + 2);   // 8-aligned
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
@@ -822,37 +821,9 @@ verify_stack_kernel(const __grid_constant__ StackParams sp) {
             mbar_init(&empty[st], CW);
         }
         *abort = 0;
-        *s_issued = 0;
         fence_barrier_init();
     }
     __syncthreads();
-
-    if (warp == CW + 1) {
-        // ---------------- L2 prefetch: the same tile order, ahead of the producer ----
-        // HBM keeps streaming while the consumers wait at phase boundaries; the
-        // producer's shared-memory loads then find the tiles in L2.
-        if (lane != 0) return;
-        long long n = 0;
-        for (int p = 0; p < P; ++p) {
-            const StackPhase& ph = sp.ph[p];
-            const CUtensorMap* tmap = &sp.tmap_w[p];
-            const long long T = (long long)ph.KT * ph.NT;
-            const int a = (int)((long long)blockIdx.x * T / G);
-            const int b = (int)((long long)(blockIdx.x + 1) * T / G);
-            for (int j = a; j < b; ++j, ++n) {
-                if (n - *s_issued > kStackL2Ahead) {
-                    const unsigned long long t0 = global_timer_ns();
-                    while (n - *s_issued > kStackL2Ahead) {
-                        if (*abort || global_timer_ns() - t0 > kWaitLimitNs) return;
-                        __nanosleep(200);
-                    }
-                }
-                const int nt = j / ph.KT, kt = j - nt * ph.KT;
-                tma_prefetch_l2_2d(tmap, kt * BKB, nt * BN);
-            }
-        }
-        return;
-    }
 
     // Grid barriers: every CTA arrives once per phase on B (its share of the
     // phase input is quantized) and once on A (its tiles of the phase are done).
@@ -928,7 +899,6 @@ verify_stack_kernel(const __grid_constant__ StackParams sp) {
                     if (pend_n == 1 || (issued & 3) == 0) refresh();
                 }
                 ++issued;
-                *s_issued = issued;
                 if (++st == Stages) { st = 0; ++round; }
             }
         }
@@ -1359,7 +1329,7 @@ cudaError_t launch_verify_stack(const StackLaunch& a, int num_sms, cudaStream_t 
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(num_sms);
-    cfg.blockDim = dim3((kW8A8Warps + 2) * 32);
+    cfg.blockDim = dim3((kW8A8Warps + 1) * 32);
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeCooperative;
