@@ -41,8 +41,8 @@ FALLBACK_HBM_GBS = 6800.0
 # launch (4096 -> 24576, M = 5) over its algorithmic bytes. Valid only for the
 # kernel sources whose sha256 is recorded (kernel_source_sha); roofline.traffic
 # is null otherwise.
-NCU_TRAFFIC = {"source_sha256": "f6c0ccdf0304f87932c77403abce583cc89a787bf06a64f76d811b9c63a7d929",
-               "dram_bytes_per_algorithmic_byte": (101728256 + 2770688) / 101273620}
+NCU_TRAFFIC = {"source_sha256": "52558e5f563b70e96adf5d2c41c1e1831a75a1381394b74b05186bade5b21e42",
+               "dram_bytes_per_algorithmic_byte": (101740288 + 2679296) / 101273620}
 
 
 def log(*a):

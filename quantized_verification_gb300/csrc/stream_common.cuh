@@ -48,8 +48,14 @@ __device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long v)
     return v;
 }
 
-// Producer: stream tiles [a, b) into the ring. Weight tiles of the first
-// ring fill are requested before the grid dependency wait. With tx == null
+// Weight tiles a producer requests before its grid dependency wait. Those
+// loads run while the previous kernel's last CTAs still stream their tiles;
+// a full 7-stage fill took bandwidth from them (the 5-token step measured
+// 1.942 ms with 7, 1.903-1.927 with 4-6, 1.98-2.05 with 0-2).
+constexpr int kPreWaitTiles = 5;
+
+// Producer: stream tiles [a, b) into the ring. The first kPreWaitTiles weight
+// tiles are requested before the grid dependency wait. With tx == null
 // only weight tiles travel (tx_bytes must then count the weight tile alone).
 // Each weight tile travels with XB activation boxes: box j of tile kt starts
 // at element (kt * XB + j) * kx_elems_per_tile of K (XB = 2 when a weight
@@ -63,7 +69,8 @@ __device__ __forceinline__ void produce(unsigned* err, SM& sm, const CUtensorMap
     const uint64_t pol_w = policy_evict_first();
     const uint64_t pol_x = policy_evict_last();
     const int n = b - a;
-    const int pre = n < Stages ? n : Stages;
+    const int pre0 = Stages < kPreWaitTiles ? Stages : kPreWaitTiles;
+    const int pre = n < pre0 ? n : pre0;
     for (int j = 0; j < pre; ++j) {
         const int tile = a + j, nt = tile / KT, kt = tile - nt * KT;
         mbar_arrive_expect_tx(&sm.full[j], tx_bytes);
