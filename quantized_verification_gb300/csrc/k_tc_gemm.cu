@@ -139,26 +139,10 @@ struct TcSmem {
     __device__ __forceinline__ uint8_t* b_slot(int j) { return bring + j * C::BSlot; }
 };
 
-// Hot-loop waits of this kernel. With QV_TC_SPIN the waiting thread polls with
-// the non-suspending test_wait instead of try_wait.
-#ifndef QV_TC_SPIN
-#define QV_TC_SPIN 0
-#endif
+// Hot-loop waits of this kernel (a non-suspending test_wait loop was
+// measured no faster).
 __device__ __forceinline__ bool tc_wait(uint64_t* bar, unsigned parity, volatile int* abort) {
-#if QV_TC_SPIN
-    if (mbar_test_wait(bar, parity)) return true;
-    const unsigned long long t0 = global_timer_ns();
-    while (true) {
-        if (mbar_test_wait(bar, parity)) return true;
-        if (*abort) return false;
-        if (global_timer_ns() - t0 > kWaitLimitNs) {
-            *abort = 1;
-            return false;
-        }
-    }
-#else
     return mbar_wait_bounded(bar, parity, abort);
-#endif
 }
 
 // Wait for an mbarrier phase for at most kWaitLimitNs, whatever the abort
