@@ -86,6 +86,9 @@ LINEAR_CASES = [
     (64, 4096, 4096), (80, 4096, 6144), (64, 12288, 4096),
     # more than 80 rows: the fewest launches of equal row counts
     (81, 256, 130), (96, 256, 300), (128, 512, 256), (161, 128, 200),
+    # up to 8 tokens: ragged K (33 K-tiles) with ragged N, wide N at 2
+    # K-tiles, a single token and a full group of 8
+    (5, 4096 + 48, 128 * 40 + 7), (1, 256, 128 * 200), (8, 1024, 128 * 100 + 1),
 ]
 
 
@@ -174,7 +177,7 @@ def test_w8a8_quantize_chain(qv, oracle):
 # ---------------------------------------------------------------------------
 LM_CASES = [(4, 256, 1024), (5, 4096, 3000), (1, 128, 130), (9, 256, 1000), (64, 256, 513),
             (80, 128, 777), (5, 512, 128 * 160 + 3), (32, 4096, 3000), (24, 512, 128 * 160 + 3),
-            (72, 512, 2000), (96, 256, 1000)]
+            (72, 512, 2000), (96, 256, 1000), (8, 1024, 128 * 100 + 1), (3, 4096 + 48, 128 * 40 + 7)]
 
 
 def _run_lm(qv, xq, sx, wq, sw):
