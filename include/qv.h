@@ -417,12 +417,15 @@ QV_API qv_status qv_quantize_weight(const void* w, qv_dtype w_dtype, int N, int 
  *             callers sized by qv_attention_workspace_bytes keep working
  *             (it returns 16 for a valid shape, 0 for an invalid one)
  * One launch of 8-CTA thread-block clusters, one cluster per (sequence,
- * key/value head): the CTAs split the key positions, score them and form
- * P V on the bf16 tensor cores (fp32 accumulation; P is split into two bf16
- * parts) with an online softmax, and merge their partials through
- * distributed shared memory. Each CTA asks for about 180 KB of shared
- * memory and a cluster needs 8 such SMs at once: where the device cannot
- * place one (e.g. a small MPS partition) the call returns QV_ERR_CUDA.
+ * key/value head): the CTAs split the key positions, load the caches with
+ * TMA, score them and form P V on the bf16 tensor cores (fp32
+ * accumulation; P is split into two bf16 parts) with an online softmax, and
+ * merge their partials through distributed shared memory. Cache positions
+ * at and past cache_len[b] are never read (they may hold anything). Each
+ * CTA asks for about 160 KB of shared memory and a cluster needs 8 such SMs
+ * at once: where the device cannot place one (e.g. a small MPS partition)
+ * the call returns QV_ERR_CUDA. A wait inside the kernel that runs out
+ * sets QV_DEVICE_ERR_FULL_WAIT (qv_device_error).
  * The outputs are within about 1e-5 of max |v| of the binary64 definition.
  */
 QV_API size_t qv_attention_workspace_bytes(int B, int T, int Hq, int Hkv, int D, int Lmax);

@@ -13,22 +13,35 @@
 // [B][Lmax][Hkv][D]. One launch; a thread-block cluster of C = 8 CTAs
 // per (sequence, key/value head) covers the R = T * G query rows of that
 // head group (G = Hq / Hkv):
-//   - the S = len + T key positions are cut into C equal ranges,
-//     one per CTA; a CTA streams its range in sub-chunks of kSub keys
-//     through a two-stage cp.async ring (keys and values together, 16-byte
-//     pieces, rows padded by 16 bytes so that ldmatrix rows fall on distinct
-//     banks);
-//   - scores Q K^T on the bf16 tensor cores (mma.sync m16n8k16, fp32
-//     accumulation: the bf16 products are exact, the sum is a binary32 sum),
-//     scaled and masked (causal, and key positions past S);
-//   - online softmax per row: running max m, running sum l, running output
-//     o rescaled by e^(m_old - m_new) at each sub-chunk;
-//   - P V on the tensor cores with P split into two bf16 parts,
-//     P = hi + mid + r with |r| <= 2^-18 P, so the product's error is below
-//     2^-18 max|v| (values are bf16, exact);
-//   - the cluster's partials (m, l, o per row) are exchanged through
-//     distributed shared memory: CTA k merges dims [k D / C, (k + 1) D / C)
-//     of every row as sum_c e^(m_c - M) o_c / sum_c e^(m_c - M) l_c and
+//   - the S = len + T key positions are cut into C equal ranges of whole
+//     16-key blocks, one range per CTA;
+//   - the range streams through a 4-stage ring of 64-key stages with 4-D
+//     TMA loads of the caches (one box per 16-key block and 64 values:
+//     64 values x 1 head x 16 positions x 1 sequence, 128-byte swizzle),
+//     keys and values of a stage on one mbarrier; thread 0 fills the ring,
+//     and the last of a stage's warps to finish with it (a shared counter)
+//     issues its refill, so no warp is set aside for copies. Positions at and
+//     past len are not the cache's: the warp that owns such a block
+//     overwrites those rows with the step's own key/value rows (or zeros
+//     past S) before it reads them, and blocks wholly past len load nothing;
+//   - warp w takes the 16-key blocks w, w + 8, ... and keeps its own online
+//     softmax for all R rows in registers (FlashAttention-2 style, no block
+//     barrier inside the loop). Keys are the M dimension of the bf16 tensor
+//     core products (mma.sync m16n8k16, fp32 accumulation) and query rows
+//     the N dimension, in n8 tiles (R = 20 takes 24 rows, not 32):
+//     S^T = K Q^T (the bf16 products are exact, the sum is a binary32 sum),
+//     scaled to base-2 units (2^(s log2 e) = e^s) and masked (causal, and
+//     key positions past the CTA's range); running max m, running sum l and
+//     output o^T rescaled by 2^(m_old - m_new) per block; o^T += V^T P^T
+//     with P split into two bf16 parts, P = hi + mid + r with
+//     |r| <= 2^-18 P, so the product's error is below 2^-18 max|v| (values
+//     are bf16, exact). The score fragments, transposed in registers
+//     (movmatrix), are the B operand of V^T P^T: P never leaves registers;
+//   - the 8 warps' partials merge in shared memory into the CTA's (m, l, o)
+//     and go out as pushes: CTA k owns dims [k D / C, (k + 1) D / C) and
+//     receives every CTA's rows of those dims and (m, l) in its shared
+//     memory (distributed shared-memory stores, one cluster barrier); it
+//     merges them as sum_c 2^(m_c - M) o_c / sum_c 2^(m_c - M) l_c and
 //     writes the fp32 outputs [token][Hq * D].
 // No workspace: nothing leaves the SMs but the outputs.
 
@@ -36,7 +49,9 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <climits>
 #include <cstdint>
+#include <cstring>
 
 #include "qv_internal.h"
 #include "qv_ptx.cuh"
@@ -44,63 +59,111 @@
 namespace cg = cooperative_groups;
 
 namespace qv {
+
+__device__ unsigned int g_attn_error;
+
 namespace {
 
-// CTAs per (sequence, key/value head). (16-CTA clusters of 225 KB CTAs with
-// 160-key sub-chunks measured slower on GB300: 24 us per layer at 2048 cached
-// positions against 19.5, and 21 against 9 at 512.)
+// CTAs per (sequence, key/value head). (16-CTA clusters measured slower on
+// GB300 with the earlier cp.async design: 24 us per layer at 2048 cached
+// positions against 19.5.)
 constexpr int kAttnCluster = 8;
-constexpr int kSub = 128;                  // keys per sub-chunk (8 groups of 16)
-constexpr int kAttnThreads = 256;          // 8 warps
-constexpr int kAttnWarps = kAttnThreads / 32;
-constexpr int kAttnMaxRows = 32;           // R = T * G, two m16 tiles
+constexpr int kSub = 64;                   // key positions per stage: 4 blocks of 16
+constexpr int kBlk = 16;                   // key positions per warp block (one k16 of P V)
+constexpr int kStages = 4;
+constexpr int kAttnWarps = 8;              // (255 registers a thread: a warp's o is 128 of them)
+constexpr int kGroupWarps = kSub / kBlk;   // warps per stage (4)
+constexpr int kAttnThreads = kAttnWarps * 32;
+constexpr int kAttnMaxRows = 32;           // R = T * G, at most four n8 tiles
+constexpr float kLog2e = 1.4426950408889634f;   // scores are carried in base-2 units: 2^(s log2 e) = e^s
+static_assert(kAttnWarps == 2 * kGroupWarps, "two warp groups take alternate stages");
 
 struct AttnArgs {
     const uint16_t* qkv;     // [B*T][(Hq + 2 Hkv) * D] bf16
-    const uint16_t* kc;      // [B][Lmax][Hkv][D] bf16
-    const uint16_t* vc;
     const int32_t* len;      // [B]
     int T, Hq, Hkv, Lmax;
+    int has_cache;           // 0: Lmax == 0, no tensor maps
     float scale;
     float* out;              // [B*T][Hq*D]
 };
 
 template <int D>
 struct AttnLayout {
-    static constexpr int RS = D + 8;                 // bf16 row stride of Q, K, V
-    static constexpr int SS = kSub + 4;              // fp32 row stride of the scores
-    static constexpr int PS = kSub + 8;              // bf16 row stride of P
-    static constexpr int Q = 0;
-    static constexpr int K = Q + kAttnMaxRows * RS * 2;
-    static constexpr int V = K + 2 * kSub * RS * 2;
-    static constexpr int S = V + 2 * kSub * RS * 2;
-    static constexpr int PH = S + kAttnMaxRows * SS * 4;
-    static constexpr int PM = PH + kAttnMaxRows * PS * 2;
-    static constexpr int M = PM + kAttnMaxRows * PS * 2;       // running max [32]
-    static constexpr int L = M + kAttnMaxRows * 4;             // running sum [32]
-    static constexpr int F = L + kAttnMaxRows * 4;             // rescale of this sub-chunk [32]
-    static constexpr int Bytes = F + kAttnMaxRows * 4;
-    // the partial output [32][D] fp32 for the cluster merge reuses stage 0 of K
-    static_assert(kAttnMaxRows * D * 4 <= kSub * RS * 2, "partial output fits a key stage");
-    static_assert(kSub % 32 == 0, "whole warps of keys per row");
+    static constexpr int H = D / 64;                       // 128-byte halves of a row
+    static constexpr int Box = kSub * 128;                 // 64 rows x 128 B, filled by 16-row boxes
+    static constexpr int StageBytes = 2 * H * Box;         // keys (H boxes), then values (H boxes)
+    static constexpr int RS = D + 8;                       // bf16 row stride of Q (padded)
+    static constexpr int Q = kStages * StageBytes;         // stages first: 1024-byte aligned boxes
+    static constexpr int DC = D / kAttnCluster;            // dims merged (and written) by each CTA
+    static constexpr int RV = Q + kAttnMaxRows * RS * 2;   // received o slices [C][DC][32] fp32
+    static constexpr int RM = RV + kAttnCluster * kAttnMaxRows * DC * 4;   // received m [C][32]
+    static constexpr int RL = RM + kAttnCluster * kAttnMaxRows * 4;        // received l [C][32]
+    static constexpr int WM = RL + kAttnCluster * kAttnMaxRows * 4;        // per-warp running max [8][32]
+    static constexpr int WL = WM + kAttnWarps * kAttnMaxRows * 4;   // per-warp running sum [8][32]
+    static constexpr int WW = WL + kAttnWarps * kAttnMaxRows * 4;   // per-warp merge weight [8][32]
+    static constexpr int M = WW + kAttnWarps * kAttnMaxRows * 4;    // the CTA's m [32]
+    static constexpr int CW = M + kAttnMaxRows * 4;        // cluster weights [32][C] and the denominator
+    static constexpr int Bar = CW + kAttnMaxRows * (kAttnCluster + 1) * 4;
+    static constexpr int Cnt = Bar + kStages * 8;          // warps done with each stage
+    static constexpr int Flag = Cnt + kStages * 4;         // abort word of the bounded waits
+    static constexpr int Bytes = Flag + 16;
+    static constexpr int Alloc = Bytes + 1024;             // slack to align the base to 1024 B
+    // the warps' partial outputs [8][32][D] fp32 reuse the (drained) stages
+    static_assert(kAttnWarps * kAttnMaxRows * D * 4 <= kStages * StageBytes, "partials fit the stages");
+    static_assert(Bar % 8 == 0 && RV % 16 == 0, "mbarrier and vector alignment");
+    static_assert(DC % 4 == 0, "whole float4 slices");
 };
+
+// Byte offset of 16-byte chunk c (of D / 8) of row r (0..63) of tensor kv
+// (0 keys, 1 values) in a stage: the TMA 128-byte swizzle puts chunk cc of a
+// 128-byte row at cc ^ (r mod 8) (boxes are 1024-byte aligned).
+template <int D>
+__device__ __forceinline__ uint32_t kv_off(int kv, int r, int c) {
+    using Ly = AttnLayout<D>;
+    const int h = c >> 3, cc = c & 7;
+    return (uint32_t)((kv * Ly::H + h) * Ly::Box + r * 128 + ((cc ^ (r & 7)) << 4));
+}
+
+// 4-D tiled load of the box at (x, head, position, sequence) into shared
+// memory; completion is signalled on `bar` as transaction bytes. x * 2 bytes
+// is a multiple of 16 (x is 0 or 64).
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, int x, int hd, int pos, int seq,
+                                            uint64_t* bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%2, %3, %4, %5}], [%6], %7;"
+        :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(hd), "r"(pos), "r"(seq),
+           "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;"
                  :: "r"(dst), "l"(src), "r"(valid ? 16 : 0) : "memory");
 }
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+__device__ __forceinline__ void ldmatrix_x2(uint32_t addr, uint32_t& r0, uint32_t& r1) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0, %1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(addr));
+}
+
+// Transpose of the 8x8 b16 matrix whose row lane / 4, columns 2 (lane % 4)
+// and 2 (lane % 4) + 1 this lane holds (the mma.sync fragment layout).
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
 
 __device__ __forceinline__ void ldmatrix_x4_trans(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
                                                   uint32_t& r3) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
                  : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
 }
-__device__ __forceinline__ void ldmatrix_x2_trans(uint32_t addr, uint32_t& r0, uint32_t& r1) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0, %1}, [%2];"
-                 : "=r"(r0), "=r"(r1) : "r"(addr));
+
+// Generic-proxy writes to shared memory before a later TMA write to it.
+__device__ __forceinline__ void fence_proxy_async_shared() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 __device__ __forceinline__ int seq_len(const AttnArgs& a, int b) {
@@ -108,275 +171,394 @@ __device__ __forceinline__ int seq_len(const AttnArgs& a, int b) {
     return L < 0 ? 0 : (L > a.Lmax ? a.Lmax : L);          // out-of-range lengths are clamped
 }
 
-// Key (kv = 0) or value (kv = 1) row at key position i of sequence b, head kh:
-// the cache below L, the step's own qkv rows from L on.
-template <int D>
-__device__ __forceinline__ const uint16_t* kv_row(const AttnArgs& a, int b, int L, int i, int kh, int kv) {
-    if (i < L) return (kv ? a.vc : a.kc) + (((size_t)b * a.Lmax + i) * a.Hkv + kh) * D;
-    const size_t W = (size_t)(a.Hq + 2 * a.Hkv) * D;
-    return a.qkv + ((size_t)b * a.T + (i - L)) * W + (size_t)(a.Hq + kv * a.Hkv + kh) * D;
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(lo)) |
+           ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(hi)) << 16);
 }
 
-// Issue the cp.async copies of the keys and values at positions
-// [p0, p0 + kSub) into stage st (zero rows at and past p_end).
+// p = hi + mid (+ a remainder below 2^-18 p): the two bf16 parts of a pair.
+__device__ __forceinline__ void split_pair(float p0, float p1, uint32_t& hi, uint32_t& mid) {
+    const __nv_bfloat16 h0 = __float2bfloat16_rn(p0), h1 = __float2bfloat16_rn(p1);
+    hi = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
+    mid = pack_bf16(p0 - __bfloat162float(h0), p1 - __bfloat162float(h1));
+}
+
+// Issue the TMA loads of sub-chunk sj (stage sj mod kStages). A stage whose
+// four blocks all start below L loads as one 64-position box per tensor and
+// 64 values; otherwise each block that starts below L loads as 16-position
+// boxes (a block wholly at or past L holds no cache rows). With no such
+// block the stage's phase completes without copies.
 template <int D>
-__device__ __forceinline__ void stage_kv(const AttnArgs& a, uint32_t sbase, int b, int L, int kh, int p0,
-                                         int p_end, int st) {
+__device__ __forceinline__ void issue_stage(uint32_t sbase, uint64_t* full, const KvMaps& tm, int has_cache, int sj,
+                                            int nblk, int p_begin, int L, int kh, int b, uint64_t pol) {
     using Ly = AttnLayout<D>;
-    constexpr int P = D / 8;                                 // 16-byte pieces per row
-    for (int e = threadIdx.x; e < 2 * kSub * P; e += kAttnThreads) {
-        const int kv = e / (kSub * P), rem = e - kv * kSub * P;
-        const int r = rem / P, c = rem - r * P;
-        const int pos = p0 + r;
-        const bool valid = pos < p_end;
-        const uint16_t* src = valid ? kv_row<D>(a, b, L, pos, kh, kv) + c * 8 : a.qkv;
-        const uint32_t dst = sbase + (uint32_t)((kv ? Ly::V : Ly::K) + ((st * kSub + r) * Ly::RS + c * 8) * 2);
-        cp_async16(dst, src, valid);
+    const int s = sj % kStages;
+    int nb = 0;
+#pragma unroll
+    for (int q = 0; q < kGroupWarps; ++q) {
+        const int j = sj * kGroupWarps + q;
+        nb += (has_cache && j < nblk && p_begin + j * kBlk < L) ? 1 : 0;
+    }
+    if (nb == 0) {
+        mbar_arrive(&full[s]);
+        return;
+    }
+    mbar_arrive_expect_tx(&full[s], (unsigned)(nb * 2 * Ly::H * kBlk * 128));
+    const uint32_t st = sbase + (uint32_t)(s * Ly::StageBytes);
+    if (nb == kGroupWarps) {
+        const int p0 = p_begin + sj * kSub;
+#pragma unroll
+        for (int h = 0; h < Ly::H; ++h) {
+            tma_load_4d(st + (uint32_t)(h * Ly::Box), &tm.k64, 64 * h, kh, p0, b, &full[s], pol);
+            tma_load_4d(st + (uint32_t)((Ly::H + h) * Ly::Box), &tm.v64, 64 * h, kh, p0, b, &full[s], pol);
+        }
+        return;
+    }
+#pragma unroll
+    for (int q = 0; q < kGroupWarps; ++q) {
+        const int j = sj * kGroupWarps + q, kp0 = p_begin + j * kBlk;
+        if (!(has_cache && j < nblk && kp0 < L)) continue;
+#pragma unroll
+        for (int h = 0; h < Ly::H; ++h) {
+            tma_load_4d(st + (uint32_t)(h * Ly::Box + q * kBlk * 128), &tm.k16, 64 * h, kh, kp0, b, &full[s], pol);
+            tma_load_4d(st + (uint32_t)((Ly::H + h) * Ly::Box + q * kBlk * 128), &tm.v16, 64 * h, kh, kp0, b,
+                        &full[s], pol);
+        }
     }
 }
 
-template <int D, int C>
-__global__ void __launch_bounds__(kAttnThreads, 1) attn_cluster_kernel(const AttnArgs a) {
-    using Ly = AttnLayout<D>;
-    constexpr int DPW = D / kAttnWarps;                      // output dims per warp (16 or 8)
-    constexpr int NTO = DPW / 8;                             // n8 tiles of the output per warp
-    extern __shared__ __align__(16) uint8_t attn_smem[];
-    cg::cluster_group cluster = cg::this_cluster();
-    allow_dependent_launch();
-    grid_dependency_wait();
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.aligned;" ::: "memory"); }
 
+template <int D, int C, int NR>
+__global__ void __launch_bounds__(kAttnThreads, 1)
+attn_cluster_kernel(const __grid_constant__ KvMaps tm, const AttnArgs a) {
+    using Ly = AttnLayout<D>;
+    constexpr int CH = D / 8;                                // 16-byte chunks of a row
+    extern __shared__ uint8_t attn_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(attn_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    cg::cluster_group cluster = cg::this_cluster();
     const int rank = (int)cluster.block_rank();
     const int kh = blockIdx.y, b = blockIdx.z, tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31, g = lane >> 2, t4 = lane & 3;
-    const int G = a.Hq / a.Hkv, R = a.T * G;
-    const int L = seq_len(a, b), S = L + a.T;
-    const int per = ((S + C - 1) / C + 15) & ~15;            // key positions per CTA
-    const int p_begin = rank * per, p_end = min(S, p_begin + per);
-    const int nsub = p_begin < p_end ? (p_end - p_begin + kSub - 1) / kSub : 0;
-    const uint32_t sbase = smem_u32(attn_smem);
-    float* s_sc = reinterpret_cast<float*>(attn_smem + Ly::S);
-    uint16_t* s_ph = reinterpret_cast<uint16_t*>(attn_smem + Ly::PH);
-    uint16_t* s_pm = reinterpret_cast<uint16_t*>(attn_smem + Ly::PM);
-    float* s_m = reinterpret_cast<float*>(attn_smem + Ly::M);
-    float* s_l = reinterpret_cast<float*>(attn_smem + Ly::L);
-    float* s_f = reinterpret_cast<float*>(attn_smem + Ly::F);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + Ly::Bar);
+    int* cnt = reinterpret_cast<int*>(smem + Ly::Cnt);
+    volatile int* abort = reinterpret_cast<volatile int*>(smem + Ly::Flag);
+    float* s_part = reinterpret_cast<float*>(smem);         // [8][D][32], after the stages drain
+    float* s_rv = reinterpret_cast<float*>(smem + Ly::RV);
+    float* s_rm = reinterpret_cast<float*>(smem + Ly::RM);
+    float* s_rl = reinterpret_cast<float*>(smem + Ly::RL);
+    float* s_wm = reinterpret_cast<float*>(smem + Ly::WM);
+    float* s_wl = reinterpret_cast<float*>(smem + Ly::WL);
+    float* s_ww = reinterpret_cast<float*>(smem + Ly::WW);
+    float* s_m = reinterpret_cast<float*>(smem + Ly::M);
+    float* s_cw = reinterpret_cast<float*>(smem + Ly::CW);
     const float NEG_INF = -__uint_as_float(0x7F800000u);
 
-    // query rows r = j * G + g' of heads kh * G + g' (rows R..31 zero)
+    if (tid == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&full[s], 1);
+            cnt[s] = 0;
+        }
+        *abort = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+    cluster_arrive_relaxed();       // waited for before the first store into another CTA
+    allow_dependent_launch();
+    grid_dependency_wait();
+
+    const int G = a.Hq / a.Hkv, R = a.T * G;
+    const int L = seq_len(a, b), S = L + a.T;
+    const int per = ((S + C - 1) / C + kBlk - 1) / kBlk * kBlk;   // key positions per CTA
+    const int p_begin = rank * per, p_end = min(S, p_begin + per);
+    const int nblk = p_begin < p_end ? (p_end - p_begin + kBlk - 1) / kBlk : 0;
+    const int nsub = (nblk + kGroupWarps - 1) / kGroupWarps;
+
+    const uint64_t pol = policy_evict_first();
     {
         const size_t W = (size_t)(a.Hq + 2 * a.Hkv) * D;
-        for (int e = tid; e < kAttnMaxRows * (D / 8); e += kAttnThreads) {
-            const int r = e / (D / 8), c = e - r * (D / 8);
+        // query rows r = j * G + g' of heads kh * G + g' (rows R..31 zero),
+        // requested before the stages so that they do not queue behind them
+        for (int e = tid; e < kAttnMaxRows * CH; e += kAttnThreads) {
+            const int r = e / CH, c = e - r * CH;
             const bool valid = r < R;
             const int j = valid ? r / G : 0, h = kh * G + (valid ? r - j * G : 0);
             cp_async16(sbase + (uint32_t)(Ly::Q + (r * Ly::RS + c * 8) * 2),
                        a.qkv + ((size_t)b * a.T + j) * W + (size_t)h * D + c * 8, valid);
         }
-    }
-    if (nsub > 0) stage_kv<D>(a, sbase, b, L, kh, p_begin, p_end, 0);
-    cp_async_commit();
-    if (nsub > 1) stage_kv<D>(a, sbase, b, L, kh, p_begin + kSub, p_end, 1);
-    cp_async_commit();
-    if (tid < kAttnMaxRows) {
-        s_m[tid] = NEG_INF;
-        s_l[tid] = 0.f;
-    }
-
-    float o[2][NTO][4];
-#pragma unroll
-    for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-        for (int nt = 0; nt < NTO; ++nt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) o[mt][nt][e] = 0.f;
-
-    const int mi = lane >> 3, ri = lane & 7;                 // ldmatrix: matrix and row of this lane
-    for (int sc = 0; sc < nsub; ++sc) {
-        const int st = sc & 1;
-        const int p0 = p_begin + sc * kSub;
-        cp_async_wait<1>();
+        // the first kStages sub-chunks, one warp each
+        if (lane == 0 && warp < kStages && warp < nsub) {
+            if (a.has_cache) {
+                prefetch_tensormap(&tm.k64);
+                prefetch_tensormap(&tm.v64);
+            }
+            issue_stage<D>(sbase, full, tm, a.has_cache, warp, nblk, p_begin, L, kh, b, pol);
+        }
+        cp_async_wait_all();
         __syncthreads();
 
-        // ---- scores: warp w covers the 16-key groups w, w + 8, ... of the sub-chunk, all 32 rows
-        for (int grp = warp; grp < kSub / 16; grp += kAttnWarps) {
-            float acc[2][2][4];
+        const int grp = warp / kGroupWarps, q = warp - grp * kGroupWarps;
+        const int mi = lane >> 3, ri = lane & 7;             // ldmatrix: matrix and row of this lane
+        const float sl2 = a.scale * kLog2e;                  // scores in base-2 units
+        // o^T: dims 16 dm + g (+8) x rows 8 nt + 2 t4 (+1)
+        float o[D / 16][NR][4];
+        float m_run[NR][2], l_run[NR][2];                    // rows 8 nt + 2 t4 + e
+        int lim[NR][2];                                      // visible key positions: [0, lim)
 #pragma unroll
-            for (int mt = 0; mt < 2; ++mt)
+        for (int nt = 0; nt < NR; ++nt) {
 #pragma unroll
-                for (int nt = 0; nt < 2; ++nt)
+            for (int dm = 0; dm < D / 16; ++dm)
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) acc[mt][nt][e] = 0.f;
-            const int n0 = 16 * grp;
+                for (int e = 0; e < 4; ++e) o[dm][nt][e] = 0.f;
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-                uint32_t qa[2][4];
-#pragma unroll
-                for (int mt = 0; mt < 2; ++mt)
-                    ldmatrix_x4(sbase + (uint32_t)(Ly::Q + ((mt * 16 + (mi & 1) * 8 + ri) * Ly::RS +
-                                                            kk * 16 + (mi >> 1) * 8) * 2),
-                                qa[mt][0], qa[mt][1], qa[mt][2], qa[mt][3]);
-                uint32_t kb0, kb1, kb2, kb3;
-                ldmatrix_x4(sbase + (uint32_t)(Ly::K + ((st * kSub + n0 + (mi >> 1) * 8 + ri) * Ly::RS +
-                                                        kk * 16 + (mi & 1) * 8) * 2),
-                            kb0, kb1, kb2, kb3);
-#pragma unroll
-                for (int mt = 0; mt < 2; ++mt) {
-                    mma_bf16_16816(acc[mt][0], qa[mt][0], qa[mt][1], qa[mt][2], qa[mt][3], kb0, kb1);
-                    mma_bf16_16816(acc[mt][1], qa[mt][0], qa[mt][1], qa[mt][2], qa[mt][3], kb2, kb3);
-                }
+            for (int e = 0; e < 2; ++e) {
+                const int r = 8 * nt + 2 * t4 + e;
+                m_run[nt][e] = NEG_INF;
+                l_run[nt][e] = 0.f;
+                lim[nt][e] = r < R ? min(L + r / G + 1, p_end) : INT_MIN;
             }
-#pragma unroll
-            for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                    for (int hh = 0; hh < 2; ++hh) {
-                        const int r = mt * 16 + g + 8 * hh;
-                        const int kl = n0 + nt * 8 + 2 * t4;
-                        float2 v;
-                        // causal, and inside this CTA's key range (the staged rows past it are zeros)
-                        const int lim = min(L + (r < R ? r / G : 0) + 1, p_end);
-                        v.x = (r < R && p0 + kl < lim) ? acc[mt][nt][2 * hh] * a.scale : NEG_INF;
-                        v.y = (r < R && p0 + kl + 1 < lim) ? acc[mt][nt][2 * hh + 1] * a.scale : NEG_INF;
-                        *reinterpret_cast<float2*>(s_sc + r * Ly::SS + kl) = v;
+        }
+        bool first = true;                                   // o is still zero
+
+        for (int sj = grp; sj < nsub; sj += 2) {
+            const int s = sj % kStages;
+            if (!mbar_wait_bounded(&full[s], (unsigned)((sj / kStages) & 1), abort)) {
+                atomicOr(&g_attn_error, kErrFullWait);
+                break;
+            }
+            const int j = sj * kGroupWarps + q;              // this warp's block of the stage
+            if (j < nblk) {
+                const uint32_t st = sbase + (uint32_t)(s * Ly::StageBytes);
+                const int kp0 = p_begin + j * kBlk;          // its first key position
+                const int r0 = q * kBlk;                     // its first row in the stage
+                const bool own_rows = kp0 + kBlk > L;
+                if (own_rows) {
+                    // rows at and past len: the step's key/value rows, zeros past S
+                    for (int e = lane; e < 2 * kBlk * CH; e += 32) {
+                        const int kv = e / (kBlk * CH), rem = e - kv * (kBlk * CH);
+                        const int r = rem / CH, c = rem - r * CH;
+                        const int pos = kp0 + r;
+                        if (pos < L) continue;
+                        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+                        if (pos < S)
+                            v = *reinterpret_cast<const uint4*>(a.qkv + ((size_t)b * a.T + (pos - L)) * W +
+                                                                (size_t)(a.Hq + kv * a.Hkv + kh) * D + c * 8);
+                        sts_v4_u32(st + kv_off<D>(kv, r0 + r, c), v.x, v.y, v.z, v.w);
                     }
-        }
-        __syncthreads();
-
-        // ---- online softmax: warp w takes rows w, w + 8, w + 16, w + 24
-        for (int r = warp; r < kAttnMaxRows; r += kAttnWarps) {
-            float sv[kSub / 32];
-            float mx = NEG_INF;
-#pragma unroll
-            for (int q = 0; q < kSub / 32; ++q) {
-                sv[q] = s_sc[r * Ly::SS + lane + 32 * q];
-                mx = fmaxf(mx, sv[q]);
-            }
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-            const float m_old = s_m[r];
-            const float m_new = fmaxf(m_old, mx);
-            const bool none = m_new == NEG_INF;                  // no visible key yet
-            float lsum = 0.f;
-#pragma unroll
-            for (int q = 0; q < kSub / 32; ++q) {
-                const float p = none ? 0.f : expf(sv[q] - m_new);
-                lsum += p;
-                const __nv_bfloat16 hi = __float2bfloat16_rn(p);
-                const __nv_bfloat16 mid = __float2bfloat16_rn(p - __bfloat162float(hi));
-                s_ph[r * Ly::PS + lane + 32 * q] = __bfloat16_as_ushort(hi);
-                s_pm[r * Ly::PS + lane + 32 * q] = __bfloat16_as_ushort(mid);
-            }
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
-            if (lane == 0) {
-                const float f = none ? 1.f : expf(m_old - m_new);   // e^(-inf) = 0 on the first keys
-                s_f[r] = f;
-                s_m[r] = m_new;
-                s_l[r] = s_l[r] * f + lsum;
-            }
-        }
-        __syncthreads();
-
-        // ---- o = o * f + P V: warp w covers dims [DPW w, DPW w + DPW), all 32 rows
-        {
-#pragma unroll
-            for (int mt = 0; mt < 2; ++mt) {
-                const float f0 = s_f[mt * 16 + g], f1 = s_f[mt * 16 + g + 8];
-#pragma unroll
-                for (int nt = 0; nt < NTO; ++nt) {
-                    o[mt][nt][0] *= f0;
-                    o[mt][nt][1] *= f0;
-                    o[mt][nt][2] *= f1;
-                    o[mt][nt][3] *= f1;
+                    __syncwarp();
                 }
-            }
-            const int d0 = DPW * warp;
+
+                // ---- S^T = K Q^T: the block's 16 keys (M) x the rows (N, NR tiles of 8)
+                float acc[NR][4];
 #pragma unroll
-            for (int ks = 0; ks < kSub / 16; ++ks) {
-                uint32_t vb[NTO][2];
-                if constexpr (NTO == 2) {
-                    ldmatrix_x4_trans(sbase + (uint32_t)(Ly::V + ((st * kSub + ks * 16 + (mi & 1) * 8 + ri) * Ly::RS +
-                                                                  d0 + (mi >> 1) * 8) * 2),
-                                      vb[0][0], vb[0][1], vb[1][0], vb[1][1]);
-                } else {
-                    ldmatrix_x2_trans(sbase + (uint32_t)(Ly::V + ((st * kSub + ks * 16 + (mi & 1) * 8 + ri) * Ly::RS +
-                                                                  d0) * 2),
-                                      vb[0][0], vb[0][1]);
-                }
+                for (int nt = 0; nt < NR; ++nt)
 #pragma unroll
-                for (int part = 0; part < 2; ++part) {
-                    const int base = part ? Ly::PM : Ly::PH;
+                    for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
 #pragma unroll
-                    for (int mt = 0; mt < 2; ++mt) {
-                        uint32_t pa0, pa1, pa2, pa3;
-                        ldmatrix_x4(sbase + (uint32_t)(base + ((mt * 16 + (mi & 1) * 8 + ri) * Ly::PS +
-                                                               ks * 16 + (mi >> 1) * 8) * 2),
-                                    pa0, pa1, pa2, pa3);
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    uint32_t ka0, ka1, ka2, ka3;                 // keys (mi & 1) * 8.., dims chunk kk * 2 + (mi >> 1)
+                    ldmatrix_x4(st + kv_off<D>(0, r0 + (mi & 1) * 8 + ri, kk * 2 + (mi >> 1)), ka0, ka1, ka2, ka3);
 #pragma unroll
-                        for (int nt = 0; nt < NTO; ++nt)
-                            mma_bf16_16816(o[mt][nt], pa0, pa1, pa2, pa3, vb[nt][0], vb[nt][1]);
+                    for (int nt = 0; nt < NR; ++nt) {
+                        uint32_t qb0, qb1;                       // rows 8 nt.., dims kk * 16 + (0 | 8)
+                        ldmatrix_x2(sbase + (uint32_t)(Ly::Q + ((8 * nt + ri) * Ly::RS + kk * 16 + (mi & 1) * 8) * 2),
+                                    qb0, qb1);
+                        mma_bf16_16816(acc[nt], ka0, ka1, ka2, ka3, qb0, qb1);
                     }
                 }
+
+                // ---- online softmax per row (base 2); P^T pairs transposed into the B operand of P V
+                uint32_t bh[NR][2], bm[NR][2];
+                float f[NR][2];
+#pragma unroll
+                for (int nt = 0; nt < NR; ++nt) {
+                    float p[4];
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        // keys g and g + 8 of row 8 nt + 2 t4 + e
+                        const float s0 = kp0 + g < lim[nt][e] ? acc[nt][e] * sl2 : NEG_INF;
+                        const float s1 = kp0 + g + 8 < lim[nt][e] ? acc[nt][2 + e] * sl2 : NEG_INF;
+                        float mx = fmaxf(s0, s1);
+                        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+                        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+                        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+                        const float m_old = m_run[nt][e];
+                        const float m_new = fmaxf(m_old, mx);
+                        const bool none = m_new == NEG_INF;          // no visible key yet
+                        f[nt][e] = none ? 1.f : exp2f(m_old - m_new);   // 2^(-inf) = 0 on the first keys
+                        p[e] = none ? 0.f : exp2f(s0 - m_new);
+                        p[2 + e] = none ? 0.f : exp2f(s1 - m_new);
+                        m_run[nt][e] = m_new;
+                        l_run[nt][e] = l_run[nt][e] * f[nt][e] + (p[e] + p[2 + e]);
+                    }
+                    uint32_t h01, m01, h23, m23;             // (key g | g + 8; rows 2 t4, 2 t4 + 1)
+                    split_pair(p[0], p[1], h01, m01);
+                    split_pair(p[2], p[3], h23, m23);
+                    bh[nt][0] = movmatrix_trans(h01);        // (row g; keys 2 t4, 2 t4 + 1)
+                    bh[nt][1] = movmatrix_trans(h23);        // (row g; keys 8 + 2 t4, 9 + 2 t4)
+                    bm[nt][0] = movmatrix_trans(m01);
+                    bm[nt][1] = movmatrix_trans(m23);
+                }
+                // rescale o unless every factor is 1 (or o is still zero)
+                bool ones = true;
+#pragma unroll
+                for (int nt = 0; nt < NR; ++nt) ones = ones && f[nt][0] == 1.f && f[nt][1] == 1.f;
+                if (!first && !__all_sync(0xffffffffu, ones)) {
+#pragma unroll
+                    for (int dm = 0; dm < D / 16; ++dm)
+#pragma unroll
+                        for (int nt = 0; nt < NR; ++nt) {
+                            o[dm][nt][0] *= f[nt][0];
+                            o[dm][nt][1] *= f[nt][1];
+                            o[dm][nt][2] *= f[nt][0];
+                            o[dm][nt][3] *= f[nt][1];
+                        }
+                }
+                first = false;
+
+                // ---- o^T += V^T P^T: dims (M, 16 per tile) x rows (N) over the block's 16 keys
+#pragma unroll
+                for (int dm = 0; dm < D / 16; ++dm) {
+                    uint32_t va0, va1, va2, va3;                 // keys (mi >> 1) * 8.., dims chunk dm * 2 + (mi & 1)
+                    ldmatrix_x4_trans(st + kv_off<D>(1, r0 + (mi >> 1) * 8 + ri, dm * 2 + (mi & 1)), va0, va1, va2,
+                                      va3);
+#pragma unroll
+                    for (int nt = 0; nt < NR; ++nt) {
+                        mma_bf16_16816(o[dm][nt], va0, va1, va2, va3, bh[nt][0], bh[nt][1]);
+                        mma_bf16_16816(o[dm][nt], va0, va1, va2, va3, bm[nt][0], bm[nt][1]);
+                    }
+                }
+                if (own_rows) fence_proxy_async_shared();    // before the stage's next TMA write
+            }
+            __syncwarp();
+            // the last of the stage's warps refills it with sub-chunk sj + kStages
+            // (the counter only grows: use u of the stage ends at 4 (u + 1) arrivals)
+            if (lane == 0 && atomicAdd(&cnt[s], 1) == kGroupWarps * (sj / kStages + 1) - 1) {
+                if (sj + kStages < nsub)
+                    issue_stage<D>(sbase, full, tm, a.has_cache, sj + kStages, nblk, p_begin, L, kh, b, pol);
             }
         }
-        __syncthreads();                                     // stage st and P are free again
-        if (sc + 2 < nsub) stage_kv<D>(a, sbase, b, L, kh, p0 + 2 * kSub, p_end, st);
-        cp_async_commit();
+
+        // this warp's running sums over the 8 lanes of a row, then its (m, l) per row
+#pragma unroll
+        for (int nt = 0; nt < NR; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                float l = l_run[nt][e];
+                l += __shfl_xor_sync(0xffffffffu, l, 4);
+                l += __shfl_xor_sync(0xffffffffu, l, 8);
+                l += __shfl_xor_sync(0xffffffffu, l, 16);
+                if (g == 0) {
+                    const int r = 8 * nt + 2 * t4 + e;
+                    s_wm[warp * kAttnMaxRows + r] = m_run[nt][e];
+                    s_wl[warp * kAttnMaxRows + r] = l;
+                }
+            }
+        // every stage this CTA loaded has been waited for: the ring may be reused
+        __syncthreads();
+        // this warp's o^T into [warp][D][32] (rows XOR-swizzled by dim: 2 wavefronts a store)
+#pragma unroll
+        for (int dm = 0; dm < D / 16; ++dm)
+#pragma unroll
+            for (int nt = 0; nt < NR; ++nt)
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    const int d = 16 * dm + g + 8 * hh;
+                    const int rw = (8 * nt + 2 * t4) ^ ((d & 7) << 2);
+                    *reinterpret_cast<float2*>(s_part + (warp * D + d) * kAttnMaxRows + rw) =
+                        make_float2(o[dm][nt][2 * hh], o[dm][nt][2 * hh + 1]);
+                }
     }
-    cp_async_wait<0>();
     __syncthreads();
 
-    // ---- this CTA's partial output, then the cluster merge
-    float* s_o = reinterpret_cast<float*>(attn_smem + Ly::K);   // [32][D]
-    {
-        const int d0 = DPW * warp;
+    // ---- the 8 warps' partials -> this CTA's (m, l, o), pushed to the cluster:
+    // the o rows of CTA k's dims go into CTA k's receive buffer, (m, l) to all
+    if (tid < kAttnWarps * kAttnMaxRows && (tid & 31) < 8 * NR) {
+        const int w = tid >> 5, r = tid & 31;
+        float M = NEG_INF;
 #pragma unroll
-        for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-            for (int nt = 0; nt < NTO; ++nt) {
-                const int col = d0 + nt * 8 + 2 * t4;
-                *reinterpret_cast<float2*>(s_o + (mt * 16 + g) * D + col) = make_float2(o[mt][nt][0], o[mt][nt][1]);
-                *reinterpret_cast<float2*>(s_o + (mt * 16 + g + 8) * D + col) = make_float2(o[mt][nt][2], o[mt][nt][3]);
-            }
+        for (int c = 0; c < kAttnWarps; ++c) M = fmaxf(M, s_wm[c * kAttnMaxRows + r]);
+        const float mw = s_wm[w * kAttnMaxRows + r];
+        s_ww[w * kAttnMaxRows + r] = mw == NEG_INF ? 0.f : exp2f(mw - M);   // a warp with no visible key
+        if (w == 0) s_m[r] = M;
     }
-    cluster.sync();
-    {
-        constexpr int DC = D / C;                            // dims merged by this CTA
-        const int dc0 = rank * DC;
-        for (int e = tid; e < R * DC; e += kAttnThreads) {
-            const int r = e / DC, d = dc0 + (e - r * DC);
-            float mc[C];
-            float M = NEG_INF;
+    __syncthreads();
+    cluster_wait();                                          // every CTA of the cluster has started
+    constexpr int DC = Ly::DC;
+    if (tid < R) {
+        float l = 0.f;
 #pragma unroll
-            for (int c = 0; c < C; ++c) {
-                mc[c] = *cluster.map_shared_rank(s_m + r, c);
-                M = fmaxf(M, mc[c]);
-            }
-            float num = 0.f, den = 0.f;
+        for (int c = 0; c < kAttnWarps; ++c) l += s_ww[c * kAttnMaxRows + tid] * s_wl[c * kAttnMaxRows + tid];
+        const float m = s_m[tid];
 #pragma unroll
-            for (int c = 0; c < C; ++c) {
-                const float w = mc[c] == NEG_INF ? 0.f : expf(mc[c] - M);   // a CTA with no visible key
-                num += w * *cluster.map_shared_rank(s_o + r * D + d, c);
-                den += w * *cluster.map_shared_rank(s_l + r, c);
-            }
-            const int j = r / G, h = kh * G + (r - j * G);
-            a.out[((size_t)b * a.T + j) * (size_t)a.Hq * D + (size_t)h * D + d] = num / den;
+        for (int k = 0; k < C; ++k) {
+            *cluster.map_shared_rank(s_rm + rank * kAttnMaxRows + tid, k) = m;
+            *cluster.map_shared_rank(s_rl + rank * kAttnMaxRows + tid, k) = l;
         }
     }
-    cluster.sync();                                          // no CTA leaves while others read its memory
+    {
+        const int R4 = (R + 3) / 4;                          // groups of 4 rows
+        for (int e = tid; e < D * R4; e += kAttnThreads) {
+            const int d = e / R4, r = 4 * (e - d * R4);
+            const int rw = r ^ ((d & 7) << 2);               // the four rows stay together
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int c = 0; c < kAttnWarps; ++c) {
+                const float4 w = *reinterpret_cast<const float4*>(s_ww + c * kAttnMaxRows + r);
+                const float4 v = *reinterpret_cast<const float4*>(s_part + (c * D + d) * kAttnMaxRows + rw);
+                acc.x += w.x * v.x;
+                acc.y += w.y * v.y;
+                acc.z += w.z * v.z;
+                acc.w += w.w * v.w;
+            }
+            const int k = d / DC;
+            *reinterpret_cast<float4*>(cluster.map_shared_rank(s_rv + (rank * DC + (d - k * DC)) * kAttnMaxRows + r, k)) =
+                acc;
+        }
+    }
+    cluster.sync();                                          // every push has landed
+
+    // ---- the cluster merge of this CTA's dims [rank DC, (rank + 1) DC) from its receive buffer
+    if (tid < R) {
+        float M = NEG_INF;
+#pragma unroll
+        for (int c = 0; c < C; ++c) M = fmaxf(M, s_rm[c * kAttnMaxRows + tid]);
+        float den = 0.f;
+#pragma unroll
+        for (int c = 0; c < C; ++c) {
+            const float mc = s_rm[c * kAttnMaxRows + tid];
+            const float w = mc == NEG_INF ? 0.f : exp2f(mc - M);  // a CTA with no visible key
+            s_cw[tid * (C + 1) + c] = w;
+            den += w * s_rl[c * kAttnMaxRows + tid];
+        }
+        s_cw[tid * (C + 1) + C] = den;
+    }
+    __syncthreads();
+    for (int e = tid; e < R * DC; e += kAttnThreads) {
+        const int dl = e / R, r = e - dl * R;
+        float num = 0.f;
+#pragma unroll
+        for (int c = 0; c < C; ++c) num += s_cw[r * (C + 1) + c] * s_rv[(c * DC + dl) * kAttnMaxRows + r];
+        const int j = r / G, h = kh * G + (r - j * G);
+        a.out[((size_t)b * a.T + j) * (size_t)a.Hq * D + (size_t)h * D + rank * DC + dl] = num / s_cw[r * (C + 1) + C];
+    }
+    // nothing reads another CTA's memory after the cluster barrier: no second one
 }
 
-template <int D, int C>
-cudaError_t launch_cluster(const AttnArgs& args, int B, cudaStream_t s) {
+template <int D, int C, int NR>
+cudaError_t launch_cluster(const KvMaps& tm, const AttnArgs& args, int B, cudaStream_t s) {
     using Ly = AttnLayout<D>;
-    cudaError_t e = cudaFuncSetAttribute(attn_cluster_kernel<D, C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         Ly::Bytes);
+    cudaError_t e = cudaFuncSetAttribute(attn_cluster_kernel<D, C, NR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Ly::Alloc);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(C, args.Hkv, B);
     cfg.blockDim = dim3(kAttnThreads);
-    cfg.dynamicSmemBytes = Ly::Bytes;
+    cfg.dynamicSmemBytes = Ly::Alloc;
     cfg.stream = s;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -387,24 +569,40 @@ cudaError_t launch_cluster(const AttnArgs& args, int B, cudaStream_t s) {
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, attn_cluster_kernel<D, C>, args);
+    return cudaLaunchKernelEx(&cfg, attn_cluster_kernel<D, C, NR>, tm, args);
 }
 
-static_assert(AttnLayout<128>::Bytes <= (int)kMaxDynSmem, "shared memory budget");
+static_assert(AttnLayout<128>::Alloc <= (int)kMaxDynSmem, "shared memory budget");
 
 }  // namespace
 
 size_t attention_workspace_bytes(int, int, int, int, int, int) { return 16; }
 
-cudaError_t launch_attention_verify(const uint16_t* qkv, const uint16_t* kc, const uint16_t* vc, const int32_t* len,
-                                    int B, int T, int Hq, int Hkv, int D, int Lmax, float scale, float* out,
-                                    void*, cudaStream_t s) {
+cudaError_t launch_attention_verify(const uint16_t* qkv, const KvMaps* maps, const int32_t* len, int B, int T, int Hq,
+                                    int Hkv, int D, int Lmax, float scale, float* out, cudaStream_t s) {
     AttnArgs a;
-    a.qkv = qkv; a.kc = kc; a.vc = vc; a.len = len;
+    a.qkv = qkv; a.len = len;
     a.T = T; a.Hq = Hq; a.Hkv = Hkv; a.Lmax = Lmax;
+    a.has_cache = maps ? 1 : 0;
     a.scale = scale;
     a.out = out;
-    return D == 128 ? launch_cluster<128, kAttnCluster>(a, B, s) : launch_cluster<64, kAttnCluster>(a, B, s);
+    KvMaps none;
+    memset(&none, 0, sizeof(none));
+    const KvMaps& tm = maps ? *maps : none;
+    const int nr = (T * (Hq / Hkv) + 7) / 8;                 // n8 tiles of query rows
+#define QV_ATTN_CASE(DV, NRV) \
+    if (D == DV && nr == NRV) return launch_cluster<DV, kAttnCluster, NRV>(tm, a, B, s);
+    QV_ATTN_CASE(128, 1) QV_ATTN_CASE(128, 2) QV_ATTN_CASE(128, 3) QV_ATTN_CASE(128, 4)
+    QV_ATTN_CASE(64, 1) QV_ATTN_CASE(64, 2) QV_ATTN_CASE(64, 3) QV_ATTN_CASE(64, 4)
+#undef QV_ATTN_CASE
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t read_and_clear_attn_error(unsigned* code) {
+    cudaError_t e = cudaMemcpyFromSymbol(code, g_attn_error, sizeof(unsigned));
+    if (e != cudaSuccess) return e;
+    const unsigned zero = 0;
+    return cudaMemcpyToSymbol(g_attn_error, &zero, sizeof(unsigned));
 }
 
 }  // namespace qv

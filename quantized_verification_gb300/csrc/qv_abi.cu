@@ -113,6 +113,23 @@ qv_status encode_2d(CUtensorMap* map, CUtensorMapDataType dt, size_t elem_bytes,
     return QV_OK;
 }
 
+// A [B][Lmax][Hkv][D] bf16 key or value cache as a 4-D tensor map (D, Hkv,
+// Lmax, B) with a box of 64 values x 1 head x box_pos positions x 1 sequence
+// and the 128-byte swizzle; positions past Lmax read as zero.
+qv_status encode_kv_cache(CUtensorMap* map, const void* base, int B, int Lmax, int Hkv, int D, unsigned box_pos) {
+    qv_status st = get_encoder();
+    if (st != QV_OK) return st;
+    const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)Hkv, (cuuint64_t)Lmax, (cuuint64_t)B};
+    const cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)Hkv * D * 2, (cuuint64_t)Lmax * Hkv * D * 2};
+    const cuuint32_t box[4] = {64, 1, box_pos, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(QV_ERR_CUDA, "cuTensorMapEncodeTiled (KV cache) failed (CUresult %d)", (int)r);
+    return QV_OK;
+}
+
 // W8A8 streaming GEMM kernel by padded token count. Up to 16 tokens the
 // int8 (8) or f16 (16) mma.sync kernel keeps pace with HBM; from 32 tokens
 // mma.sync is latency- or compute-bound and the tcgen05 kernel (exact f16
@@ -635,8 +652,16 @@ qv_status qv_attention_verify(const uint16_t* qkv, const uint16_t* k_cache, cons
     QV_CHECK_DEV(v_cache);
     QV_CHECK_DEV(cache_len);
     QV_CHECK_DEV(out);
-    cudaError_t e = qv::launch_attention_verify(qkv, k_cache, v_cache, cache_len, B, T, Hq, Hkv, D, Lmax, scale, out,
-                                                workspace, stream);
+    qv::KvMaps maps;
+    if (Lmax > 0) {
+        st = encode_kv_cache(&maps.k64, k_cache, B, Lmax, Hkv, D, 64);
+        if (st == QV_OK) st = encode_kv_cache(&maps.v64, v_cache, B, Lmax, Hkv, D, 64);
+        if (st == QV_OK) st = encode_kv_cache(&maps.k16, k_cache, B, Lmax, Hkv, D, 16);
+        if (st == QV_OK) st = encode_kv_cache(&maps.v16, v_cache, B, Lmax, Hkv, D, 16);
+        if (st != QV_OK) return st;
+    }
+    cudaError_t e = qv::launch_attention_verify(qkv, Lmax > 0 ? &maps : nullptr, cache_len, B, T, Hq, Hkv, D, Lmax,
+                                                scale, out, stream);
     if (e != cudaSuccess) return cuda_fail(e, "qv_attention_verify launch");
     return ok();
 }
@@ -820,11 +845,12 @@ qv_status qv_device_error(unsigned int* code) {
     if (!code) return fail(QV_ERR_INVALID_ARG, "code is null");
     cudaError_t e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
-    unsigned tc = 0;
+    unsigned tc = 0, at = 0;
     e = qv::read_and_clear_stream_gemm_error(code);
     if (e == cudaSuccess) e = qv::read_and_clear_tc_gemm_error(&tc);
+    if (e == cudaSuccess) e = qv::read_and_clear_attn_error(&at);
     if (e != cudaSuccess) return cuda_fail(e, "reading the device error word");
-    *code |= tc;
+    *code |= tc | at;
     return ok();
 }
 

@@ -139,10 +139,16 @@ cudaError_t launch_quantize_weight_w4(const void* w, bool bf16, int N, int K, ui
 constexpr int kMaxMPerLaunchW4 = 32;
 
 // Attention over a short KV cache (k_attn.cu): one cluster launch, no workspace.
+// The key and value caches as 4-D tensor maps (dims D, Hkv, Lmax, B; bf16,
+// 128-byte swizzle) with boxes of 64 values x 1 head x 64 positions x 1
+// sequence (k64, v64) and x 16 positions (k16, v16); NULL when Lmax == 0.
+struct KvMaps {
+    CUtensorMap k64, v64, k16, v16;
+};
 size_t attention_workspace_bytes(int B, int T, int Hq, int Hkv, int D, int Lmax);
-cudaError_t launch_attention_verify(const uint16_t* qkv, const uint16_t* kc, const uint16_t* vc, const int32_t* len,
-                                    int B, int T, int Hq, int Hkv, int D, int Lmax, float scale, float* out,
-                                    void* ws, cudaStream_t s);
+cudaError_t launch_attention_verify(const uint16_t* qkv, const KvMaps* maps, const int32_t* len, int B, int T, int Hq,
+                                    int Hkv, int D, int Lmax, float scale, float* out, cudaStream_t s);
+cudaError_t read_and_clear_attn_error(unsigned* code);
 
 // Logit-fidelity diagnostic (k_fidelity.cu): per row KL(softmax(a) ||
 // softmax(b)) and both top-1 indices.

@@ -6,8 +6,11 @@ exact in binary32 and a D-term binary32 dot product errs by at most about
 by at most that fraction of max |v|; expf adds a few ulp. So every output
 is within 1e-4 max |v| of the definition. Shapes: the Qwen3-8B layer
 (32 query heads, 8 key/value heads, D = 128) with 5 verify tokens, cache
-lengths on and around the 128-key chunk boundaries, no cache, the largest
-head group (T * Hq / Hkv = 32), D = 64, and a length above Lmax (clamped)."""
+lengths on and around the 16-key block and 64-key stage boundaries, the
+2048-position cache of the benchmark, no cache, the largest head group
+(T * Hq / Hkv = 32), D = 64, and a length above Lmax (clamped). Cache
+positions at and past a sequence's length hold NaN: the kernel must take the
+step's own rows there and never read a stale cache row."""
 import numpy as np
 import pytest
 import torch
@@ -33,6 +36,9 @@ CASES = [  # B, T, Hq, Hkv, D, Lmax, lens
     (2, 8, 16, 4, 128, 2000, [1999, 513]),
     (1, 4, 8, 1, 128, 257, [257]),
     (2, 2, 4, 2, 64, 100, [150, 100]),
+    (1, 5, 32, 8, 128, 2048, [2048]),
+    (2, 5, 32, 8, 128, 2100, [2043, 77]),
+    (3, 4, 16, 4, 64, 520, [511, 64, 1]),
 ]
 
 
@@ -43,6 +49,9 @@ def test_attention_verify(qv, oracle, B, T, Hq, Hkv, D, Lmax, lens):
     kc = torch.randn(B, Lmax, Hkv, D, generator=g).to(torch.bfloat16)
     vc = torch.randn(B, Lmax, Hkv, D, generator=g).to(torch.bfloat16)
     ln = torch.tensor(lens, dtype=torch.int32)
+    for bb, n in enumerate(lens):                     # stale cache rows: never read
+        kc[bb, max(0, min(n, Lmax)):] = float("nan")
+        vc[bb, max(0, min(n, Lmax)):] = float("nan")
     scale = float(np.float32(1.0) / np.sqrt(np.float32(D)))
     ws = torch.empty(qv.qv_attention_workspace_bytes(B, T, Hq, Hkv, D, Lmax), dtype=torch.uint8, device="cuda")
     out = torch.full((B * T, Hq * D), float("nan"), device="cuda")
@@ -52,7 +61,7 @@ def test_attention_verify(qv, oracle, B, T, Hq, Hkv, D, Lmax, lens):
     ref = oracle.attention_verify(bf16_bits(qkv).reshape(B * T, -1), bf16_bits(kc).reshape(B, Lmax, Hkv, D),
                                   bf16_bits(vc).reshape(B, Lmax, Hkv, D), clamped, T, Hq, Hkv, D,
                                   float(np.float32(scale)))
-    vmax = max(float(vc.float().abs().max()) if Lmax else 0.0,
+    vmax = max(float(vc.float().nan_to_num(0.0).abs().max()) if Lmax else 0.0,
                float(qkv[:, (Hq + Hkv) * D:].float().abs().max()))
     err = np.abs(np_(out).astype(np.float64) - ref)
     assert np.all(np.isfinite(np_(out)))
