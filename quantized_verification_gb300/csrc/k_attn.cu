@@ -100,8 +100,7 @@ struct AttnLayout {
     static constexpr int RL = RM + kAttnCluster * kAttnMaxRows * 4;        // received l [C][32]
     static constexpr int WM = RL + kAttnCluster * kAttnMaxRows * 4;        // per-warp running max [8][32]
     static constexpr int WL = WM + kAttnWarps * kAttnMaxRows * 4;   // per-warp running sum [8][32]
-    static constexpr int WW = WL + kAttnWarps * kAttnMaxRows * 4;   // per-warp merge weight [8][32]
-    static constexpr int M = WW + kAttnWarps * kAttnMaxRows * 4;    // the CTA's m [32]
+    static constexpr int M = WL + kAttnWarps * kAttnMaxRows * 4;    // the CTA's m [32]
     static constexpr int CW = M + kAttnMaxRows * 4;        // cluster weights [32][C] and the denominator
     static constexpr int Bar = CW + kAttnMaxRows * (kAttnCluster + 1) * 4;
     static constexpr int Cnt = Bar + kStages * 8;          // warps done with each stage
@@ -253,7 +252,6 @@ attn_cluster_kernel(const __grid_constant__ KvMaps tm, const AttnArgs a) {
     float* s_rl = reinterpret_cast<float*>(smem + Ly::RL);
     float* s_wm = reinterpret_cast<float*>(smem + Ly::WM);
     float* s_wl = reinterpret_cast<float*>(smem + Ly::WL);
-    float* s_ww = reinterpret_cast<float*>(smem + Ly::WW);
     float* s_m = reinterpret_cast<float*>(smem + Ly::M);
     float* s_cw = reinterpret_cast<float*>(smem + Ly::CW);
     const float NEG_INF = -__uint_as_float(0x7F800000u);
@@ -290,8 +288,9 @@ attn_cluster_kernel(const __grid_constant__ KvMaps tm, const AttnArgs a) {
             cp_async16(sbase + (uint32_t)(Ly::Q + (r * Ly::RS + c * 8) * 2),
                        a.qkv + ((size_t)b * a.T + j) * W + (size_t)h * D + c * 8, valid);
         }
-        // the first kStages sub-chunks, one warp each
-        if (lane == 0 && warp < kStages && warp < nsub) {
+        // sub-chunks 0 and 1 now (one warp each); 2 and 3 once 0 and 1 have
+        // landed, so that the first stages do not share HBM with the whole ring
+        if (lane == 0 && warp < 2 && warp < nsub) {
             if (a.has_cache) {
                 prefetch_tensormap(&tm.k64);
                 prefetch_tensormap(&tm.v64);
@@ -330,6 +329,8 @@ attn_cluster_kernel(const __grid_constant__ KvMaps tm, const AttnArgs a) {
                 atomicOr(&g_attn_error, kErrFullWait);
                 break;
             }
+            if (sj < 2 && q == 0 && lane == 0 && sj + 2 < nsub)
+                issue_stage<D>(sbase, full, tm, a.has_cache, sj + 2, nblk, p_begin, L, kh, b, pol);
             const int j = sj * kGroupWarps + q;              // this warp's block of the stage
             if (j < nblk) {
                 const uint32_t st = sbase + (uint32_t)(s * Ly::StageBytes);
@@ -460,7 +461,20 @@ attn_cluster_kernel(const __grid_constant__ KvMaps tm, const AttnArgs a) {
             }
         // every stage this CTA loaded has been waited for: the ring may be reused
         __syncthreads();
-        // this warp's o^T into [warp][D][32] (rows XOR-swizzled by dim: 2 wavefronts a store)
+        // this warp's o^T, scaled by 2^(m_w - M) for the CTA's row maxima M, into
+        // [warp][D][32] (rows XOR-swizzled by dim: 2 wavefronts a store)
+        float wt[NR][2];
+#pragma unroll
+        for (int nt = 0; nt < NR; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int r = 8 * nt + 2 * t4 + e;
+                float M = NEG_INF;
+#pragma unroll
+                for (int c = 0; c < kAttnWarps; ++c) M = fmaxf(M, s_wm[c * kAttnMaxRows + r]);
+                wt[nt][e] = m_run[nt][e] == NEG_INF ? 0.f : exp2f(m_run[nt][e] - M);   // no visible key: 0
+                if (warp == 0 && g == 0) s_m[r] = M;
+            }
 #pragma unroll
         for (int dm = 0; dm < D / 16; ++dm)
 #pragma unroll
@@ -470,30 +484,22 @@ attn_cluster_kernel(const __grid_constant__ KvMaps tm, const AttnArgs a) {
                     const int d = 16 * dm + g + 8 * hh;
                     const int rw = (8 * nt + 2 * t4) ^ ((d & 7) << 2);
                     *reinterpret_cast<float2*>(s_part + (warp * D + d) * kAttnMaxRows + rw) =
-                        make_float2(o[dm][nt][2 * hh], o[dm][nt][2 * hh + 1]);
+                        make_float2(o[dm][nt][2 * hh] * wt[nt][0], o[dm][nt][2 * hh + 1] * wt[nt][1]);
                 }
-    }
-    __syncthreads();
-
-    // ---- the 8 warps' partials -> this CTA's (m, l, o), pushed to the cluster:
-    // the o rows of CTA k's dims go into CTA k's receive buffer, (m, l) to all
-    if (tid < kAttnWarps * kAttnMaxRows && (tid & 31) < 8 * NR) {
-        const int w = tid >> 5, r = tid & 31;
-        float M = NEG_INF;
-#pragma unroll
-        for (int c = 0; c < kAttnWarps; ++c) M = fmaxf(M, s_wm[c * kAttnMaxRows + r]);
-        const float mw = s_wm[w * kAttnMaxRows + r];
-        s_ww[w * kAttnMaxRows + r] = mw == NEG_INF ? 0.f : exp2f(mw - M);   // a warp with no visible key
-        if (w == 0) s_m[r] = M;
     }
     __syncthreads();
     cluster_wait();                                          // every CTA of the cluster has started
     constexpr int DC = Ly::DC;
+    // ---- this CTA's (m, l, o), pushed to the cluster: the o rows of CTA k's
+    // dims go into CTA k's receive buffer, (m, l) to all
     if (tid < R) {
+        const float m = s_m[tid];
         float l = 0.f;
 #pragma unroll
-        for (int c = 0; c < kAttnWarps; ++c) l += s_ww[c * kAttnMaxRows + tid] * s_wl[c * kAttnMaxRows + tid];
-        const float m = s_m[tid];
+        for (int c = 0; c < kAttnWarps; ++c) {
+            const float mw = s_wm[c * kAttnMaxRows + tid];
+            l += (mw == NEG_INF ? 0.f : exp2f(mw - m)) * s_wl[c * kAttnMaxRows + tid];
+        }
 #pragma unroll
         for (int k = 0; k < C; ++k) {
             *cluster.map_shared_rank(s_rm + rank * kAttnMaxRows + tid, k) = m;
@@ -508,12 +514,11 @@ attn_cluster_kernel(const __grid_constant__ KvMaps tm, const AttnArgs a) {
             float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
             for (int c = 0; c < kAttnWarps; ++c) {
-                const float4 w = *reinterpret_cast<const float4*>(s_ww + c * kAttnMaxRows + r);
                 const float4 v = *reinterpret_cast<const float4*>(s_part + (c * D + d) * kAttnMaxRows + rw);
-                acc.x += w.x * v.x;
-                acc.y += w.y * v.y;
-                acc.z += w.z * v.z;
-                acc.w += w.w * v.w;
+                acc.x += v.x;
+                acc.y += v.y;
+                acc.z += v.z;
+                acc.w += v.w;
             }
             const int k = d / DC;
             *reinterpret_cast<float4*>(cluster.map_shared_rank(s_rv + (rank * DC + (d - k * DC)) * kAttnMaxRows + r, k)) =
