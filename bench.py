@@ -41,8 +41,8 @@ FALLBACK_HBM_GBS = 6800.0
 # launch (4096 -> 24576, M = 5) over its algorithmic bytes. Valid only for the
 # kernel sources whose sha256 is recorded (kernel_source_sha); roofline.traffic
 # is null otherwise.
-NCU_TRAFFIC = {"source_sha256": "52558e5f563b70e96adf5d2c41c1e1831a75a1381394b74b05186bade5b21e42",
-               "dram_bytes_per_algorithmic_byte": (101740288 + 2679296) / 101273620}
+NCU_TRAFFIC = {"source_sha256": "c33db13093284db1ab64f4a30464829e7d944d09ba12ef49416d9c1768b5da32",
+               "dram_bytes_per_algorithmic_byte": (101716224 + 2638848) / 101273620}
 
 
 def log(*a):
