@@ -15,18 +15,22 @@
 // head group (G = Hq / Hkv):
 //   - the S = len + T key positions are cut into C equal ranges of whole
 //     16-key blocks, one range per CTA;
-//   - the range streams through a 4-stage ring of 64-key stages with 4-D
-//     TMA loads of the caches (one box per 16-key block and 64 values:
-//     64 values x 1 head x 16 positions x 1 sequence, 128-byte swizzle),
-//     keys and values of a stage on one mbarrier; thread 0 fills the ring,
-//     and the last of a stage's warps to finish with it (a shared counter)
-//     issues its refill, so no warp is set aside for copies. Positions at and
-//     past len are not the cache's: the warp that owns such a block
-//     overwrites those rows with the step's own key/value rows (or zeros
-//     past S) before it reads them, and blocks wholly past len load nothing;
-//   - warp w takes the 16-key blocks w, w + 8, ... and keeps its own online
-//     softmax for all R rows in registers (FlashAttention-2 style, no block
-//     barrier inside the loop). Keys are the M dimension of the bf16 tensor
+//   - the range streams through a 5-stage ring of 64-key stages with 4-D
+//     TMA loads of the caches (a 64-position box per tensor and 64 values
+//     for a stage wholly below len, else one 16-position box per block;
+//     128-byte swizzle), keys and values of a stage on one mbarrier; two
+//     warps request the first two stages, the rest of the ring follows once
+//     those have landed, and the last of a stage's warps to finish with it (a
+//     shared counter) issues its refill, so no warp is set aside for copies.
+//     Positions at and past len are not the cache's: the warp that owns such
+//     a block overwrites those rows with the step's own key/value rows (or
+//     zeros past S) before it reads them, and blocks wholly past len load
+//     nothing;
+//   - warp 4 h + q takes block q of the stages of parity h (a range of one
+//     stage is shared: its blocks' P V is split by dims over all 8 warps)
+//     and keeps its own online softmax for all R rows in registers
+//     (FlashAttention-2 style, no block barrier inside the loop). Keys are
+//     the M dimension of the bf16 tensor
 //     core products (mma.sync m16n8k16, fp32 accumulation) and query rows
 //     the N dimension, in n8 tiles (R = 20 takes 24 rows, not 32):
 //     S^T = K Q^T (the bf16 products are exact, the sum is a binary32 sum),
@@ -70,7 +74,7 @@ namespace {
 constexpr int kAttnCluster = 8;
 constexpr int kSub = 64;                   // key positions per stage: 4 blocks of 16
 constexpr int kBlk = 16;                   // key positions per warp block (one k16 of P V)
-constexpr int kStages = 4;
+constexpr int kStages = 5;                 // 17 blocks of a 2048-position range in flight at once
 constexpr int kAttnWarps = 8;              // (255 registers a thread: a warp's o is 128 of them)
 constexpr int kGroupWarps = kSub / kBlk;   // warps per stage (4)
 constexpr int kAttnThreads = kAttnWarps * 32;
@@ -288,8 +292,8 @@ attn_cluster_kernel(const __grid_constant__ KvMaps tm, const AttnArgs a) {
             cp_async16(sbase + (uint32_t)(Ly::Q + (r * Ly::RS + c * 8) * 2),
                        a.qkv + ((size_t)b * a.T + j) * W + (size_t)h * D + c * 8, valid);
         }
-        // sub-chunks 0 and 1 now (one warp each); 2 and 3 once 0 and 1 have
-        // landed, so that the first stages do not share HBM with the whole ring
+        // sub-chunks 0 and 1 now (one warp each), the rest of the ring once 0
+        // and 1 have landed, so that the first stages do not share HBM with it
         if (lane == 0 && warp < 2 && warp < nsub) {
             if (a.has_cache) {
                 prefetch_tensormap(&tm.k64);
@@ -323,117 +327,135 @@ attn_cluster_kernel(const __grid_constant__ KvMaps tm, const AttnArgs a) {
         }
         bool first = true;                                   // o is still zero
 
-        for (int sj = grp; sj < nsub; sj += 2) {
+        // Rows at and past len of block kp0 (stage rows r0..r0+15): the step's
+        // key/value rows, zeros past S; threads t0, t0 + step, ... share the work.
+        auto own_rows = [&](uint32_t st, int r0, int kp0, int t0, int step) {
+            for (int e = t0; e < 2 * kBlk * CH; e += step) {
+                const int kv = e / (kBlk * CH), rem = e - kv * (kBlk * CH);
+                const int r = rem / CH, c = rem - r * CH;
+                const int pos = kp0 + r;
+                if (pos < L) continue;
+                uint4 v = make_uint4(0u, 0u, 0u, 0u);
+                if (pos < S)
+                    v = *reinterpret_cast<const uint4*>(a.qkv + ((size_t)b * a.T + (pos - L)) * W +
+                                                        (size_t)(a.Hq + kv * a.Hkv + kh) * D + c * 8);
+                sts_v4_u32(st + kv_off<D>(kv, r0 + r, c), v.x, v.y, v.z, v.w);
+            }
+        };
+        // One 16-key block (stage rows r0.., first position kp0) into this
+        // warp's softmax state; P V only for the dim tiles [dm0, dm1), and the
+        // block's probabilities added to l only if add_l (a block shared by
+        // several warps counts once in l and once per dim).
+        auto block = [&](uint32_t st, int r0, int kp0, int dm0, int dm1, bool add_l) {
+            // ---- S^T = K Q^T: the block's 16 keys (M) x the rows (N, NR tiles of 8)
+            float acc[NR][4];
+#pragma unroll
+            for (int nt = 0; nt < NR; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                uint32_t ka0, ka1, ka2, ka3;                 // keys (mi & 1) * 8.., dims chunk kk * 2 + (mi >> 1)
+                ldmatrix_x4(st + kv_off<D>(0, r0 + (mi & 1) * 8 + ri, kk * 2 + (mi >> 1)), ka0, ka1, ka2, ka3);
+#pragma unroll
+                for (int nt = 0; nt < NR; ++nt) {
+                    uint32_t qb0, qb1;                       // rows 8 nt.., dims kk * 16 + (0 | 8)
+                    ldmatrix_x2(sbase + (uint32_t)(Ly::Q + ((8 * nt + ri) * Ly::RS + kk * 16 + (mi & 1) * 8) * 2),
+                                qb0, qb1);
+                    mma_bf16_16816(acc[nt], ka0, ka1, ka2, ka3, qb0, qb1);
+                }
+            }
+
+            // ---- online softmax per row (base 2); P^T pairs transposed into the B operand of P V
+            uint32_t bh[NR][2], bm[NR][2];
+            float f[NR][2];
+#pragma unroll
+            for (int nt = 0; nt < NR; ++nt) {
+                float p[4];
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    // keys g and g + 8 of row 8 nt + 2 t4 + e
+                    const float s0 = kp0 + g < lim[nt][e] ? acc[nt][e] * sl2 : NEG_INF;
+                    const float s1 = kp0 + g + 8 < lim[nt][e] ? acc[nt][2 + e] * sl2 : NEG_INF;
+                    float mx = fmaxf(s0, s1);
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+                    const float m_old = m_run[nt][e];
+                    const float m_new = fmaxf(m_old, mx);
+                    const bool none = m_new == NEG_INF;          // no visible key yet
+                    f[nt][e] = none ? 1.f : exp2f(m_old - m_new);   // 2^(-inf) = 0 on the first keys
+                    p[e] = none ? 0.f : exp2f(s0 - m_new);
+                    p[2 + e] = none ? 0.f : exp2f(s1 - m_new);
+                    m_run[nt][e] = m_new;
+                    l_run[nt][e] = l_run[nt][e] * f[nt][e] + (add_l ? p[e] + p[2 + e] : 0.f);
+                }
+                uint32_t h01, m01, h23, m23;             // (key g | g + 8; rows 2 t4, 2 t4 + 1)
+                split_pair(p[0], p[1], h01, m01);
+                split_pair(p[2], p[3], h23, m23);
+                bh[nt][0] = movmatrix_trans(h01);        // (row g; keys 2 t4, 2 t4 + 1)
+                bh[nt][1] = movmatrix_trans(h23);        // (row g; keys 8 + 2 t4, 9 + 2 t4)
+                bm[nt][0] = movmatrix_trans(m01);
+                bm[nt][1] = movmatrix_trans(m23);
+            }
+            // rescale o unless every factor is 1 (or o is still zero)
+            bool ones = true;
+#pragma unroll
+            for (int nt = 0; nt < NR; ++nt) ones = ones && f[nt][0] == 1.f && f[nt][1] == 1.f;
+            if (!first && !__all_sync(0xffffffffu, ones)) {
+#pragma unroll
+                for (int dm = 0; dm < D / 16; ++dm)
+#pragma unroll
+                    for (int nt = 0; nt < NR; ++nt) {
+                        o[dm][nt][0] *= f[nt][0];
+                        o[dm][nt][1] *= f[nt][1];
+                        o[dm][nt][2] *= f[nt][0];
+                        o[dm][nt][3] *= f[nt][1];
+                    }
+            }
+            first = false;
+
+            // ---- o^T += V^T P^T: dims (M, 16 per tile) x rows (N) over the block's 16 keys
+#pragma unroll
+            for (int dm = 0; dm < D / 16; ++dm) {
+                if (dm < dm0 || dm >= dm1) continue;
+                uint32_t va0, va1, va2, va3;                 // keys (mi >> 1) * 8.., dims chunk dm * 2 + (mi & 1)
+                ldmatrix_x4_trans(st + kv_off<D>(1, r0 + (mi >> 1) * 8 + ri, dm * 2 + (mi & 1)), va0, va1, va2, va3);
+#pragma unroll
+                for (int nt = 0; nt < NR; ++nt) {
+                    mma_bf16_16816(o[dm][nt], va0, va1, va2, va3, bh[nt][0], bh[nt][1]);
+                    mma_bf16_16816(o[dm][nt], va0, va1, va2, va3, bm[nt][0], bm[nt][1]);
+                }
+            }
+        };
+
+        // A range of one stage (at most 4 blocks) would leave warp group 1
+        // idle: all 8 warps share its blocks instead (each block's scores and
+        // softmax in each of its warps, its P V split by dims among them).
+        // (Sharing the last of an odd number of stages measured slower at 2048
+        // and 8192 cached positions: there the last stage waits for its data.)
+        const bool shared_last = nsub == 1;
+        const int nsub_own = shared_last ? nsub - 1 : nsub;
+        for (int sj = grp; sj < nsub_own; sj += 2) {
             const int s = sj % kStages;
             if (!mbar_wait_bounded(&full[s], (unsigned)((sj / kStages) & 1), abort)) {
                 atomicOr(&g_attn_error, kErrFullWait);
                 break;
             }
-            if (sj < 2 && q == 0 && lane == 0 && sj + 2 < nsub)
-                issue_stage<D>(sbase, full, tm, a.has_cache, sj + 2, nblk, p_begin, L, kh, b, pol);
+            if (sj < 2 && q == 0 && lane == 0)               // the rest of the first fill
+                for (int x = sj + 2; x < kStages && x < nsub; x += 2)
+                    issue_stage<D>(sbase, full, tm, a.has_cache, x, nblk, p_begin, L, kh, b, pol);
             const int j = sj * kGroupWarps + q;              // this warp's block of the stage
             if (j < nblk) {
                 const uint32_t st = sbase + (uint32_t)(s * Ly::StageBytes);
                 const int kp0 = p_begin + j * kBlk;          // its first key position
-                const int r0 = q * kBlk;                     // its first row in the stage
-                const bool own_rows = kp0 + kBlk > L;
-                if (own_rows) {
-                    // rows at and past len: the step's key/value rows, zeros past S
-                    for (int e = lane; e < 2 * kBlk * CH; e += 32) {
-                        const int kv = e / (kBlk * CH), rem = e - kv * (kBlk * CH);
-                        const int r = rem / CH, c = rem - r * CH;
-                        const int pos = kp0 + r;
-                        if (pos < L) continue;
-                        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-                        if (pos < S)
-                            v = *reinterpret_cast<const uint4*>(a.qkv + ((size_t)b * a.T + (pos - L)) * W +
-                                                                (size_t)(a.Hq + kv * a.Hkv + kh) * D + c * 8);
-                        sts_v4_u32(st + kv_off<D>(kv, r0 + r, c), v.x, v.y, v.z, v.w);
-                    }
+                const bool fix = kp0 + kBlk > L;
+                if (fix) {
+                    own_rows(st, q * kBlk, kp0, lane, 32);
                     __syncwarp();
                 }
-
-                // ---- S^T = K Q^T: the block's 16 keys (M) x the rows (N, NR tiles of 8)
-                float acc[NR][4];
-#pragma unroll
-                for (int nt = 0; nt < NR; ++nt)
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    uint32_t ka0, ka1, ka2, ka3;                 // keys (mi & 1) * 8.., dims chunk kk * 2 + (mi >> 1)
-                    ldmatrix_x4(st + kv_off<D>(0, r0 + (mi & 1) * 8 + ri, kk * 2 + (mi >> 1)), ka0, ka1, ka2, ka3);
-#pragma unroll
-                    for (int nt = 0; nt < NR; ++nt) {
-                        uint32_t qb0, qb1;                       // rows 8 nt.., dims kk * 16 + (0 | 8)
-                        ldmatrix_x2(sbase + (uint32_t)(Ly::Q + ((8 * nt + ri) * Ly::RS + kk * 16 + (mi & 1) * 8) * 2),
-                                    qb0, qb1);
-                        mma_bf16_16816(acc[nt], ka0, ka1, ka2, ka3, qb0, qb1);
-                    }
-                }
-
-                // ---- online softmax per row (base 2); P^T pairs transposed into the B operand of P V
-                uint32_t bh[NR][2], bm[NR][2];
-                float f[NR][2];
-#pragma unroll
-                for (int nt = 0; nt < NR; ++nt) {
-                    float p[4];
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        // keys g and g + 8 of row 8 nt + 2 t4 + e
-                        const float s0 = kp0 + g < lim[nt][e] ? acc[nt][e] * sl2 : NEG_INF;
-                        const float s1 = kp0 + g + 8 < lim[nt][e] ? acc[nt][2 + e] * sl2 : NEG_INF;
-                        float mx = fmaxf(s0, s1);
-                        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-                        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-                        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-                        const float m_old = m_run[nt][e];
-                        const float m_new = fmaxf(m_old, mx);
-                        const bool none = m_new == NEG_INF;          // no visible key yet
-                        f[nt][e] = none ? 1.f : exp2f(m_old - m_new);   // 2^(-inf) = 0 on the first keys
-                        p[e] = none ? 0.f : exp2f(s0 - m_new);
-                        p[2 + e] = none ? 0.f : exp2f(s1 - m_new);
-                        m_run[nt][e] = m_new;
-                        l_run[nt][e] = l_run[nt][e] * f[nt][e] + (p[e] + p[2 + e]);
-                    }
-                    uint32_t h01, m01, h23, m23;             // (key g | g + 8; rows 2 t4, 2 t4 + 1)
-                    split_pair(p[0], p[1], h01, m01);
-                    split_pair(p[2], p[3], h23, m23);
-                    bh[nt][0] = movmatrix_trans(h01);        // (row g; keys 2 t4, 2 t4 + 1)
-                    bh[nt][1] = movmatrix_trans(h23);        // (row g; keys 8 + 2 t4, 9 + 2 t4)
-                    bm[nt][0] = movmatrix_trans(m01);
-                    bm[nt][1] = movmatrix_trans(m23);
-                }
-                // rescale o unless every factor is 1 (or o is still zero)
-                bool ones = true;
-#pragma unroll
-                for (int nt = 0; nt < NR; ++nt) ones = ones && f[nt][0] == 1.f && f[nt][1] == 1.f;
-                if (!first && !__all_sync(0xffffffffu, ones)) {
-#pragma unroll
-                    for (int dm = 0; dm < D / 16; ++dm)
-#pragma unroll
-                        for (int nt = 0; nt < NR; ++nt) {
-                            o[dm][nt][0] *= f[nt][0];
-                            o[dm][nt][1] *= f[nt][1];
-                            o[dm][nt][2] *= f[nt][0];
-                            o[dm][nt][3] *= f[nt][1];
-                        }
-                }
-                first = false;
-
-                // ---- o^T += V^T P^T: dims (M, 16 per tile) x rows (N) over the block's 16 keys
-#pragma unroll
-                for (int dm = 0; dm < D / 16; ++dm) {
-                    uint32_t va0, va1, va2, va3;                 // keys (mi >> 1) * 8.., dims chunk dm * 2 + (mi & 1)
-                    ldmatrix_x4_trans(st + kv_off<D>(1, r0 + (mi >> 1) * 8 + ri, dm * 2 + (mi & 1)), va0, va1, va2,
-                                      va3);
-#pragma unroll
-                    for (int nt = 0; nt < NR; ++nt) {
-                        mma_bf16_16816(o[dm][nt], va0, va1, va2, va3, bh[nt][0], bh[nt][1]);
-                        mma_bf16_16816(o[dm][nt], va0, va1, va2, va3, bm[nt][0], bm[nt][1]);
-                    }
-                }
-                if (own_rows) fence_proxy_async_shared();    // before the stage's next TMA write
+                block(st, q * kBlk, kp0, 0, D / 16, true);
+                if (fix) fence_proxy_async_shared();         // before the stage's next TMA write
             }
             __syncwarp();
             // the last of the stage's warps refills it with sub-chunk sj + kStages
@@ -441,6 +463,30 @@ attn_cluster_kernel(const __grid_constant__ KvMaps tm, const AttnArgs a) {
             if (lane == 0 && atomicAdd(&cnt[s], 1) == kGroupWarps * (sj / kStages + 1) - 1) {
                 if (sj + kStages < nsub)
                     issue_stage<D>(sbase, full, tm, a.has_cache, sj + kStages, nblk, p_begin, L, kh, b, pol);
+            }
+        }
+        if (shared_last) {
+            // never refilled (it is the last), so no release count is kept
+            const int sj = nsub - 1, s = sj % kStages;
+            const bool ok = mbar_wait_bounded(&full[s], (unsigned)((sj / kStages) & 1), abort);
+            if (!ok) atomicOr(&g_attn_error, kErrFullWait);
+            const uint32_t st = sbase + (uint32_t)(s * Ly::StageBytes);
+            const int nb = nblk - sj * kGroupWarps;          // 1..4 blocks
+            const int nbp = nb == 3 ? 4 : nb;                // warps split evenly: 8, 4 or 2 per block
+            const int wpb = kAttnWarps / nbp;
+            const int ns = wpb < D / 16 ? wpb : D / 16;      // dim slices per block
+            const int qb = warp % nbp, sl = warp / nbp;
+            if (ok) {
+                for (int qq = 0; qq < nb; ++qq) {
+                    const int kp0 = p_begin + (sj * kGroupWarps + qq) * kBlk;
+                    if (kp0 + kBlk > L) own_rows(st, qq * kBlk, kp0, tid, kAttnThreads);   // rows at or past len
+                }
+            }
+            __syncthreads();
+            const int j = sj * kGroupWarps + qb;
+            if (ok && j < nblk && sl < ns) {
+                const int tps = (D / 16) / ns;               // dim tiles per slice
+                block(st, qb * kBlk, p_begin + j * kBlk, sl * tps, sl * tps + tps, sl == 0);
             }
         }
 

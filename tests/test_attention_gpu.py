@@ -6,7 +6,8 @@ exact in binary32 and a D-term binary32 dot product errs by at most about
 by at most that fraction of max |v|; expf adds a few ulp. So every output
 is within 1e-4 max |v| of the definition. Shapes: the Qwen3-8B layer
 (32 query heads, 8 key/value heads, D = 128) with 5 verify tokens, cache
-lengths on and around the 16-key block and 64-key stage boundaries, the
+lengths on and around the 16-key block and 64-key stage boundaries (and
+ranges of a single stage, which all warps share), the
 2048-position cache of the benchmark, no cache, the largest head group
 (T * Hq / Hkv = 32), D = 64, and a length above Lmax (clamped). Cache
 positions at and past a sequence's length hold NaN: the kernel must take the
@@ -39,6 +40,14 @@ CASES = [  # B, T, Hq, Hkv, D, Lmax, lens
     (1, 5, 32, 8, 128, 2048, [2048]),
     (2, 5, 32, 8, 128, 2100, [2043, 77]),
     (3, 4, 16, 4, 64, 520, [511, 64, 1]),
+    # 10, 11 and 12 blocks of 16 keys per CTA (more stages than the ring
+    # holds, partial last stages); ranges of one stage (at most 4 blocks) are
+    # shared by all warps (300, 17, 77 and short lengths above)
+    (1, 5, 32, 8, 128, 1300, [1270]),
+    (1, 5, 32, 8, 128, 1400, [1395]),
+    (1, 5, 32, 8, 128, 1525, [1525]),
+    # 32 blocks per CTA: the ring is refilled as its stages drain
+    (1, 5, 32, 8, 128, 4096, [4000]),
 ]
 
 
