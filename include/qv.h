@@ -422,7 +422,7 @@ QV_API qv_status qv_quantize_weight(const void* w, qv_dtype w_dtype, int N, int 
  * accumulation; P is split into two bf16 parts) with an online softmax, and
  * merge their partials through distributed shared memory. Cache positions
  * at and past cache_len[b] are never read (they may hold anything). Each
- * CTA asks for about 160 KB of shared memory and a cluster needs 8 such SMs
+ * CTA asks for about 195 KB of shared memory and a cluster needs 8 such SMs
  * at once: where the device cannot place one (e.g. a small MPS partition)
  * the call returns QV_ERR_CUDA. A wait inside the kernel that runs out
  * sets QV_DEVICE_ERR_FULL_WAIT (qv_device_error).
