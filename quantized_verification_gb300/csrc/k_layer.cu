@@ -179,7 +179,6 @@ residual_rmsnorm_quant_kernel(uint16_t* __restrict__ h, const uint16_t* __restri
                               const uint16_t* __restrict__ gamma, float eps, const float* __restrict__ mul,
                               int H, int8_t* __restrict__ xq, float* __restrict__ sx,
                               uint16_t* __restrict__ x_out) {
-    allow_dependent_launch();
     const int row = blockIdx.x, tid = threadIdx.x;
     const int nvec = H / 8;
     uint4* hr = reinterpret_cast<uint4*>(h + (size_t)row * H);
@@ -189,6 +188,7 @@ residual_rmsnorm_quant_kernel(uint16_t* __restrict__ h, const uint16_t* __restri
         if (dr) asm volatile("prefetch.global.L2 [%0];" :: "l"(dr + v));
     }
     grid_dependency_wait();
+    allow_dependent_launch();   // the next GEMM starts after the previous kernel (as in k_quant.cu)
     __shared__ FF red_ff[kLayerThreads / 32];
     __shared__ float red_f[kLayerThreads / 32];
     __shared__ double ss_total;
@@ -280,7 +280,6 @@ residual_rmsnorm_quant_kernel(uint16_t* __restrict__ h, const uint16_t* __restri
 
 __global__ void __launch_bounds__(kLayerThreads)
 swiglu_quant_kernel(const float* __restrict__ gate_up, int F, int8_t* __restrict__ xq, float* __restrict__ sx) {
-    allow_dependent_launch();
     const int row = blockIdx.x, tid = threadIdx.x;
     const int nvec = F / 4;
     const float4* gr = reinterpret_cast<const float4*>(gate_up + (size_t)row * 2 * F);
@@ -290,6 +289,7 @@ swiglu_quant_kernel(const float* __restrict__ gate_up, int F, int8_t* __restrict
         asm volatile("prefetch.global.L2 [%0];" :: "l"(ur + v));
     }
     grid_dependency_wait();
+    allow_dependent_launch();   // the next GEMM starts after the previous kernel (as in k_quant.cu)
     __shared__ float red_f[kLayerThreads / 32];
 
     float4 av[kGluVecs];
