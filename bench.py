@@ -366,6 +366,20 @@ def main():
     alg_bytes = stack.algorithmic_bytes()
     log(f"step {ms:.4f} ms ({alg_bytes / (ms * 1e-3) / 1e9:.1f} GB/s algorithmic), clocks {clk}")
     assert qv.qv_device_error() == 0, "a kernel hit its wait limit"
+    # per-step spread, after the timed region: each step bracketed by its own
+    # pair of events on the launching stream
+    n_dist = min(args.steps, 200)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_dist)]
+    for e0, e1 in ev:
+        e0.record(stream)
+        step_graph.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    per_step = sorted(e0.elapsed_time(e1) for e0, e1 in ev)
+    step_dist = {"n": n_dist, "p10": per_step[n_dist // 10], "median": per_step[n_dist // 2],
+                 "p90": per_step[(9 * n_dist) // 10], "unit": "ms",
+                 "note": "each step timed alone with CUDA events, after the timed region"}
+    log(f"per-step ms p10 {step_dist['p10']:.4f} median {step_dist['median']:.4f} p90 {step_dist['p90']:.4f}")
     peak, peak_kind = read_peaks()
 
     # ---- dominant kernel: the W8A8 streaming GEMM on the step's 144
@@ -751,6 +765,7 @@ def main():
                        "samples": clk["samples"]},
             "comparator": comparator,
             "paths_ms_per_step": paths_ms,
+            "step_ms_distribution": step_dist,
             "layer_chain": layer_chain,
             "sampling_t_gt_0": sampling,
             "tree_verify": tree,
