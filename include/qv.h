@@ -604,9 +604,15 @@ QV_API qv_status qv_device_error(unsigned int* code);
  *   qv_debug_drop_partials(n): the next n such launches publish no split-K
  *     partial sums, so every split tile's head waits out its limit, sets
  *     QV_DEVICE_ERR_SLOT_WAIT and finishes with incomplete sums.
+ *   qv_debug_hold_attention_loads(n): the next n qv_attention_verify calls
+ *     request none of their key/value stages, so every stage wait runs out
+ *     (after the qv_debug_set_slot_wait_ns limit, else 1 s), sets
+ *     QV_DEVICE_ERR_FULL_WAIT and the outputs are undefined; no copy is left
+ *     in flight, and later calls are unaffected.
  */
 QV_API void qv_debug_set_slot_wait_ns(unsigned long long ns);
 QV_API void qv_debug_drop_partials(int n);
+QV_API void qv_debug_hold_attention_loads(int n);
 
 /* Number of SMs the kernels size their grids for on the current device
  * (queried once per device). Host function. */

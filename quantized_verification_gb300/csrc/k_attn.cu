@@ -89,6 +89,8 @@ struct AttnArgs {
     int has_cache;           // 0: Lmax == 0, no tensor maps
     float scale;
     float* out;              // [B*T][Hq*D]
+    int hold_loads;          // test hook: request no stage, so every stage wait runs out
+    unsigned long long wait_ns;   // limit of a stage wait (kWaitLimitNs by default)
 };
 
 template <int D>
@@ -164,6 +166,21 @@ __device__ __forceinline__ void ldmatrix_x4_trans(uint32_t addr, uint32_t& r0, u
                  : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
 }
 
+// mbar_wait_bounded with a limit given at run time.
+__device__ __forceinline__ bool stage_wait(uint64_t* bar, unsigned parity, volatile int* abort,
+                                           unsigned long long limit_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = global_timer_ns();
+    while (true) {
+        if (*abort) return false;
+        if (mbar_try_wait(bar, parity)) return true;
+        if (global_timer_ns() - t0 > limit_ns) {
+            *abort = 1;
+            return false;
+        }
+    }
+}
+
 // Generic-proxy writes to shared memory before a later TMA write to it.
 __device__ __forceinline__ void fence_proxy_async_shared() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -193,8 +210,9 @@ __device__ __forceinline__ void split_pair(float p0, float p1, uint32_t& hi, uin
 // block the stage's phase completes without copies.
 template <int D>
 __device__ __forceinline__ void issue_stage(uint32_t sbase, uint64_t* full, const KvMaps& tm, int has_cache, int sj,
-                                            int nblk, int p_begin, int L, int kh, int b, uint64_t pol) {
+                                            int nblk, int p_begin, int L, int kh, int b, uint64_t pol, int hold) {
     using Ly = AttnLayout<D>;
+    if (hold) return;                                        // test hook: the stage never completes
     const int s = sj % kStages;
     int nb = 0;
 #pragma unroll
@@ -299,7 +317,7 @@ attn_cluster_kernel(const __grid_constant__ KvMaps tm, const AttnArgs a) {
                 prefetch_tensormap(&tm.k64);
                 prefetch_tensormap(&tm.v64);
             }
-            issue_stage<D>(sbase, full, tm, a.has_cache, warp, nblk, p_begin, L, kh, b, pol);
+            issue_stage<D>(sbase, full, tm, a.has_cache, warp, nblk, p_begin, L, kh, b, pol, a.hold_loads);
         }
         cp_async_wait_all();
         __syncthreads();
@@ -438,13 +456,13 @@ attn_cluster_kernel(const __grid_constant__ KvMaps tm, const AttnArgs a) {
         const int nsub_own = shared_last ? nsub - 1 : nsub;
         for (int sj = grp; sj < nsub_own; sj += 2) {
             const int s = sj % kStages;
-            if (!mbar_wait_bounded(&full[s], (unsigned)((sj / kStages) & 1), abort)) {
+            if (!stage_wait(&full[s], (unsigned)((sj / kStages) & 1), abort, a.wait_ns)) {
                 atomicOr(&g_attn_error, kErrFullWait);
                 break;
             }
             if (sj < 2 && q == 0 && lane == 0)               // the rest of the first fill
                 for (int x = sj + 2; x < kStages && x < nsub; x += 2)
-                    issue_stage<D>(sbase, full, tm, a.has_cache, x, nblk, p_begin, L, kh, b, pol);
+                    issue_stage<D>(sbase, full, tm, a.has_cache, x, nblk, p_begin, L, kh, b, pol, a.hold_loads);
             const int j = sj * kGroupWarps + q;              // this warp's block of the stage
             if (j < nblk) {
                 const uint32_t st = sbase + (uint32_t)(s * Ly::StageBytes);
@@ -462,13 +480,13 @@ attn_cluster_kernel(const __grid_constant__ KvMaps tm, const AttnArgs a) {
             // (the counter only grows: use u of the stage ends at 4 (u + 1) arrivals)
             if (lane == 0 && atomicAdd(&cnt[s], 1) == kGroupWarps * (sj / kStages + 1) - 1) {
                 if (sj + kStages < nsub)
-                    issue_stage<D>(sbase, full, tm, a.has_cache, sj + kStages, nblk, p_begin, L, kh, b, pol);
+                    issue_stage<D>(sbase, full, tm, a.has_cache, sj + kStages, nblk, p_begin, L, kh, b, pol, a.hold_loads);
             }
         }
         if (shared_last) {
             // never refilled (it is the last), so no release count is kept
             const int sj = nsub - 1, s = sj % kStages;
-            const bool ok = mbar_wait_bounded(&full[s], (unsigned)((sj / kStages) & 1), abort);
+            const bool ok = stage_wait(&full[s], (unsigned)((sj / kStages) & 1), abort, a.wait_ns);
             if (!ok) atomicOr(&g_attn_error, kErrFullWait);
             const uint32_t st = sbase + (uint32_t)(s * Ly::StageBytes);
             const int nb = nblk - sj * kGroupWarps;          // 1..4 blocks
@@ -630,8 +648,11 @@ static_assert(AttnLayout<128>::Alloc <= (int)kMaxDynSmem, "shared memory budget"
 size_t attention_workspace_bytes(int, int, int, int, int, int) { return 16; }
 
 cudaError_t launch_attention_verify(const uint16_t* qkv, const KvMaps* maps, const int32_t* len, int B, int T, int Hq,
-                                    int Hkv, int D, int Lmax, float scale, float* out, cudaStream_t s) {
+                                    int Hkv, int D, int Lmax, float scale, float* out, int hold_loads,
+                                    unsigned long long wait_ns, cudaStream_t s) {
     AttnArgs a;
+    a.hold_loads = hold_loads;
+    a.wait_ns = wait_ns ? wait_ns : kWaitLimitNs;
     a.qkv = qkv; a.len = len;
     a.T = T; a.Hq = Hq; a.Hkv = Hkv; a.Lmax = Lmax;
     a.has_cache = maps ? 1 : 0;

@@ -258,6 +258,7 @@ qv_status report_error(qv_status st, const char* msg) { return fail(st, "%s", ms
 
 std::atomic<unsigned long long> g_debug_slot_wait_ns{0};
 std::atomic<int> g_debug_drop_partials{0};
+std::atomic<int> g_debug_hold_attention{0};
 unsigned long long debug_slot_wait_ns() {
     const unsigned long long v = g_debug_slot_wait_ns.load();
     return v ? v : kWaitLimitNs;
@@ -265,6 +266,12 @@ unsigned long long debug_slot_wait_ns() {
 bool debug_take_drop_partials() {
     int n = g_debug_drop_partials.load();
     while (n > 0 && !g_debug_drop_partials.compare_exchange_weak(n, n - 1)) {
+    }
+    return n > 0;
+}
+bool debug_take_hold_attention() {
+    int n = g_debug_hold_attention.load();
+    while (n > 0 && !g_debug_hold_attention.compare_exchange_weak(n, n - 1)) {
     }
     return n > 0;
 }
@@ -660,8 +667,9 @@ qv_status qv_attention_verify(const uint16_t* qkv, const uint16_t* k_cache, cons
         if (st == QV_OK) st = encode_kv_cache(&maps.v16, v_cache, B, Lmax, Hkv, D, 16);
         if (st != QV_OK) return st;
     }
+    const int hold = qv::debug_take_hold_attention() ? 1 : 0;
     cudaError_t e = qv::launch_attention_verify(qkv, Lmax > 0 ? &maps : nullptr, cache_len, B, T, Hq, Hkv, D, Lmax,
-                                                scale, out, stream);
+                                                scale, out, hold, qv::debug_slot_wait_ns(), stream);
     if (e != cudaSuccess) return cuda_fail(e, "qv_attention_verify launch");
     return ok();
 }
@@ -840,6 +848,8 @@ qv_status qv_verify_stack(const qv_linear_desc* linears, int n_linears, const qv
 void qv_debug_set_slot_wait_ns(unsigned long long ns) { qv::g_debug_slot_wait_ns.store(ns); }
 
 void qv_debug_drop_partials(int n) { qv::g_debug_drop_partials.store(n > 0 ? n : 0); }
+
+void qv_debug_hold_attention_loads(int n) { qv::g_debug_hold_attention.store(n > 0 ? n : 0); }
 
 qv_status qv_device_error(unsigned int* code) {
     if (!code) return fail(QV_ERR_INVALID_ARG, "code is null");

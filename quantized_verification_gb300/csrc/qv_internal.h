@@ -115,6 +115,7 @@ size_t stack_xq_offset(int mp, int n_max);
 // read when a streaming W8A8 / W4A8 launch is enqueued.
 unsigned long long debug_slot_wait_ns();
 bool debug_take_drop_partials();
+bool debug_take_hold_attention();
 
 cudaError_t launch_w8a8_stream(const W8A8Launch& a, int num_sms, cudaStream_t s);
 cudaError_t launch_w8a8_tc(const W8A8Launch& a, int num_sms, cudaStream_t s);
@@ -146,8 +147,11 @@ struct KvMaps {
     CUtensorMap k64, v64, k16, v16;
 };
 size_t attention_workspace_bytes(int B, int T, int Hq, int Hkv, int D, int Lmax);
+// hold_loads, wait_ns: test hook (qv_debug_hold_attention_loads) and the
+// stage-wait limit (0: kWaitLimitNs).
 cudaError_t launch_attention_verify(const uint16_t* qkv, const KvMaps* maps, const int32_t* len, int B, int T, int Hq,
-                                    int Hkv, int D, int Lmax, float scale, float* out, cudaStream_t s);
+                                    int Hkv, int D, int Lmax, float scale, float* out, int hold_loads,
+                                    unsigned long long wait_ns, cudaStream_t s);
 cudaError_t read_and_clear_attn_error(unsigned* code);
 
 // Logit-fidelity diagnostic (k_fidelity.cu): per row KL(softmax(a) ||

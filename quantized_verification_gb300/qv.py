@@ -31,7 +31,8 @@ EXPORTS = ("qv_quantize_act", "qv_w8a8_linear", "qv_lm_head_argmax", "qv_accept"
            "qv_rmsnorm_quant", "qv_swiglu_quant", "qv_w8a8_swiglu", "qv_spec_sample",
            "qv_tree_accept", "qv_quantize_weight_w4", "qv_w4a8_linear", "qv_w4a8_swiglu",
            "qv_w4a8_lm_head_argmax", "qv_logit_fidelity", "qv_attention_workspace_bytes",
-           "qv_attention_verify", "qv_debug_set_slot_wait_ns", "qv_debug_drop_partials")
+           "qv_attention_verify", "qv_debug_set_slot_wait_ns", "qv_debug_drop_partials",
+           "qv_debug_hold_attention_loads")
 MAX_STACK_M = 16
 
 
@@ -98,6 +99,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         L.qv_debug_set_slot_wait_ns.restype = None
         L.qv_debug_drop_partials.argtypes = [I]
         L.qv_debug_drop_partials.restype = None
+        L.qv_debug_hold_attention_loads.argtypes = [I]
+        L.qv_debug_hold_attention_loads.restype = None
         L.qv_num_sms.argtypes = []
         L.qv_num_sms.restype = I
         for name in ("qv_quantize_act", "qv_w8a8_linear", "qv_lm_head_argmax", "qv_accept",
@@ -485,6 +488,7 @@ def qv_device_error() -> int:
     return int(code.value)
 
 
+QV_DEVICE_ERR_FULL_WAIT = 1     # a consumer waited too long for a stage
 QV_DEVICE_ERR_SLOT_WAIT = 32
 
 
@@ -496,6 +500,11 @@ def qv_debug_set_slot_wait_ns(ns: int):
 def qv_debug_drop_partials(n: int):
     """Test hook: the next n streaming launches publish no split-K partial sums."""
     load().qv_debug_drop_partials(int(n))
+
+
+def qv_debug_hold_attention_loads(n: int):
+    """Test hook: the next n qv_attention_verify calls request no key/value stage."""
+    load().qv_debug_hold_attention_loads(int(n))
 
 
 def qv_num_sms() -> int:

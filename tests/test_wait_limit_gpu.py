@@ -70,3 +70,34 @@ def test_hooks_do_not_touch_later_calls(qv, oracle):
     y_ref, _ = oracle.w8a8_linear(np_(xq), np_(sx), np_(wq), np_(sw))
     assert np.array_equal(np_(y).view(np.uint32), y_ref.view(np.uint32))
     assert qv.qv_device_error() == 0
+
+
+def test_attention_stage_wait_runs_out_and_recovers(qv, oracle):
+    """The attention kernel's stage waits: with its key/value loads held back
+    (test hook) every wait runs out after the shortened limit, the device
+    error word says so, and the next call, with loads, is correct again."""
+    from test_attention_gpu import CASES, test_attention_verify
+    B, T, Hq, Hkv, D, Lmax, lens = CASES[0]
+    qkv = torch.randn(B * T, (Hq + 2 * Hkv) * D, generator=torch.Generator().manual_seed(5)).to(torch.bfloat16)
+    kc = torch.randn(B, Lmax, Hkv, D, generator=torch.Generator().manual_seed(6)).to(torch.bfloat16)
+    vc = torch.randn(B, Lmax, Hkv, D, generator=torch.Generator().manual_seed(7)).to(torch.bfloat16)
+    ln = torch.tensor(lens, dtype=torch.int32)
+    ws = torch.empty(qv.qv_attention_workspace_bytes(B, T, Hq, Hkv, D, Lmax), dtype=torch.uint8, device="cuda")
+    out = torch.zeros(B * T, Hq * D, device="cuda")
+    assert qv.qv_device_error() == 0
+    qv.qv_debug_set_slot_wait_ns(2_000_000)          # 2 ms instead of 1 s
+    qv.qv_debug_hold_attention_loads(1)
+    try:
+        t0 = time.perf_counter()
+        qv.qv_attention_verify(qkv.cuda(), kc.cuda(), vc.cuda(), ln.cuda(), T, Hq, Hkv, 1.0 / D ** 0.5, out, ws)
+        code = qv.qv_device_error()                  # synchronizes
+        elapsed = time.perf_counter() - t0
+    finally:
+        qv.qv_debug_set_slot_wait_ns(0)
+        qv.qv_debug_hold_attention_loads(0)
+    assert code & qv.QV_DEVICE_ERR_FULL_WAIT
+    assert elapsed < 0.5
+    # the context is usable and later calls load their stages again
+    test_attention_verify(qv, oracle, *CASES[0])
+    assert qv.qv_device_error() == 0
+
