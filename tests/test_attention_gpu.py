@@ -48,6 +48,9 @@ CASES = [  # B, T, Hq, Hkv, D, Lmax, lens
     (1, 5, 32, 8, 128, 1525, [1525]),
     # 32 blocks per CTA: the ring is refilled as its stages drain
     (1, 5, 32, 8, 128, 4096, [4000]),
+    # D = 64 with three and four n8 tiles of query rows (R = 20 and 32)
+    (1, 5, 32, 8, 64, 900, [850]),
+    (2, 8, 16, 4, 64, 700, [650, 333]),
 ]
 
 
