@@ -36,7 +36,9 @@
  *     running when the call is enqueued; qv_quantize_weight never lets its
  *     successor start early, so quantize-then-use on one stream is safe.
  *   - Results are deterministic: every call returns identical bits for
- *     identical inputs (the bf16 comparator excepted, see qv_bf16_linear).
+ *     identical inputs. The fp32 results of the bf16 comparator and of
+ *     attention also depend on how the work is split (the SM count, the
+ *     cluster size), so they are repeatable on one GPU model, not across.
  */
 #ifndef QV_H
 #define QV_H
