@@ -20,7 +20,7 @@ with ``-k`` on the kernels below skips 19 matching launches (``-s 19 -c 18``):
     spec_{max,sums,decide,chunk,draw}     sampling at T > 0, 1 x (4 + 1) rows x 151936
     tree_accept_kernel                    a 16-node draft tree
     accept_kernel                         greedy acceptance, 1 x 5
-    attn_cluster_kernel<128, 8>           attention of 5 tokens over a 2048-position
+    attn_cluster_kernel<128, 8, 3>        attention of 5 tokens over a 2048-position
                                           cache, 32/8 heads, D = 128
     logit_fidelity_kernel                 KL and top-1 of 5 rows x 151936 logits
 
