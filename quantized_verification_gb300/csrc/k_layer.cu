@@ -194,13 +194,16 @@ residual_rmsnorm_quant_kernel(uint16_t* __restrict__ h, const uint16_t* __restri
     __shared__ double ss_total;
     __shared__ float rstd_s;
 
-    uint4 hv[kNormVecs];
+    uint4 hv[kNormVecs], gv[kNormVecs];
     FF ss{0.0f, 0.0f};
 #pragma unroll
     for (int u = 0; u < kNormVecs; ++u) {
         const int v = tid + u * kLayerThreads;
         hv[u] = make_uint4(0u, 0u, 0u, 0u);
+        gv[u] = make_uint4(0u, 0u, 0u, 0u);
         if (v < nvec) {
+            // the norm weights travel with the row: their latency hides behind the reduction
+            gv[u] = reinterpret_cast<const uint4*>(gamma)[v];
             hv[u] = hr[v];
             if (dr) {
                 const uint4 dv = dr[v];
@@ -225,7 +228,13 @@ residual_rmsnorm_quant_kernel(uint16_t* __restrict__ h, const uint16_t* __restri
     }
     const double sum = block_sum_squares(ss, red_ff, &ss_total);
     if (tid == 0) {
-        double q = __ddiv_rn(sum, (double)H);
+        // ss / H; for H = 2^k that is the exact scaling by 2^-k (bits of the
+        // binary64 power of two: exponent field 1023 - k), no division
+        double q;
+        if ((H & (H - 1)) == 0)
+            q = __dmul_rn(sum, __longlong_as_double((long long)(1023 - (__ffs(H) - 1)) << 52));
+        else
+            q = __ddiv_rn(sum, (double)H);
         if (near_binary32_midpoint(q)) q = __ddiv_rn(sum_squares_in_order(hr, nvec), (double)H);
         const float var = __double2float_rn(q);
         rstd_s = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(var, eps)));
@@ -242,9 +251,8 @@ residual_rmsnorm_quant_kernel(uint16_t* __restrict__ h, const uint16_t* __restri
 #pragma unroll
         for (int j = 0; j < 8; ++j) xv[u][j] = 0.0f;
         if (v < nvec) {
-            const uint4 gv = reinterpret_cast<const uint4*>(gamma)[v];
             const uint32_t* w = reinterpret_cast<const uint32_t*>(&hv[u]);
-            const uint32_t* gw = reinterpret_cast<const uint32_t*>(&gv);
+            const uint32_t* gw = reinterpret_cast<const uint32_t*>(&gv[u]);
             uint32_t xb[4];
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
