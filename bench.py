@@ -41,8 +41,8 @@ FALLBACK_HBM_GBS = 6800.0
 # launch (4096 -> 24576, M = 5) over its algorithmic bytes. Valid only for the
 # kernel sources whose sha256 is recorded (kernel_source_sha); roofline.traffic
 # is null otherwise.
-NCU_TRAFFIC = {"source_sha256": "4d8ab48a545758fba3ef53a367dd1a297b9123bd1b9a1edc397f10bed6b93ff7",
-               "dram_bytes_per_algorithmic_byte": (101720064 + 2526208) / 101273620}
+NCU_TRAFFIC = {"source_sha256": "3b66904808d143d558e50f4dcecce916d92ef886825ab14f874a189550960754",
+               "dram_bytes_per_algorithmic_byte": (101714944 + 2645504) / 101273620}
 
 
 def log(*a):

@@ -48,10 +48,11 @@ __device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long v)
     return v;
 }
 
-// Weight tiles a producer requests before its grid dependency wait. Those
-// loads run while the previous kernel's last CTAs still stream their tiles;
-// a full 7-stage fill took bandwidth from them (the 5-token step measured
-// 1.942 ms with 7, 1.903-1.927 with 4-6, 1.98-2.05 with 0-2).
+// Weight tiles a producer requests before its grid dependency wait. Behind
+// the activation quantization (which lets the GEMM launch once the previous
+// GEMM has finished) they load during the quantization; 4 and 5 measured
+// best on the 5-token step, 6 and 7 slower (the full ring fill takes HBM
+// from the quantization's own reads and the previous kernel's last stores).
 constexpr int kPreWaitTiles = 5;
 
 // Producer: stream tiles [a, b) into the ring. The first kPreWaitTiles weight
