@@ -310,7 +310,8 @@ __device__ __forceinline__ void gather_partials(SM& sm, unsigned long long* slot
 struct EpiState {
     int c2 = 0;               // split_contributors_end of the CTA's range
     float swn = 0.f;          // channel scale of this thread's row in the current tile
-    float swn_up = 0.f;       // SwiGLU: the scale of row tid + 64 (the up feature of this gate row)
+                              // (SwiGLU: of gate row tid % 64)
+    float swn_up = 0.f;       // SwiGLU: the scale of up row tid % 64 + 64
     unsigned tiles_done = 0;  // LM head: channel tiles this CTA finished
 };
 
@@ -318,9 +319,14 @@ struct EpiState {
 // finish needs, so that its latency hides behind the segment's MMAs.
 template <int EPI>
 __device__ __forceinline__ void segment_start(EpiState& st, const W8A8Params& p, int nt, int tid) {
+    if (EPI == (int)Epi::SwiGLU) {
+        const int n = nt * BN + (tid & (BN / 2 - 1));          // gate row; its up row is n + 64
+        st.swn = n < p.N ? __ldg(&p.sw[n]) : 0.f;
+        st.swn_up = n + BN / 2 < p.N ? __ldg(&p.sw[n + BN / 2]) : 0.f;
+        return;
+    }
     const int n = nt * BN + (tid & (BN - 1));
     st.swn = n < p.N ? __ldg(&p.sw[n]) : 0.f;
-    if (EPI == (int)Epi::SwiGLU) st.swn_up = (tid < BN / 2 && n + BN / 2 < p.N) ? __ldg(&p.sw[n + BN / 2]) : 0.f;
 }
 
 // Finish channel tile nt from its complete int32 sums in sm.stg.
@@ -328,8 +334,6 @@ template <int MP, int CW, int EPI, class SM>
 __device__ __forceinline__ void finish_tile(SM& sm, const W8A8Params& p, int nt, int tid, EpiState& st) {
     constexpr int SP = SM::SP;
     const int warp = tid >> 5, lane = tid & 31;
-    // SwiGLU: the first BN / 2 consumer threads own one feature each
-    const int r = tid;
     const float swn = st.swn;
     if (EPI == (int)Epi::Linear) {
         // TH threads per channel (all CW warps when there are many tokens),
@@ -352,13 +356,16 @@ __device__ __forceinline__ void finish_tile(SM& sm, const W8A8Params& p, int nt,
             }
         }
     } else if (EPI == (int)Epi::SwiGLU) {
-        // rows r and r + 64 of the tile: gate and up of feature f
+        // rows r and r + 64 of the tile: gate and up of feature f; the
+        // CW * 32 / 64 threads of a feature take tokens h, h + TH, ...
+        constexpr int TH = CW * 32 / (BN / 2);
+        const int r = tid & (BN / 2 - 1), h = tid / (BN / 2);
         const int f = nt * (BN / 2) + r;
-        if (r < BN / 2 && 2 * f < p.N) {
+        if (h < TH && 2 * f < p.N) {
             float* a = reinterpret_cast<float*>(p.y);
             const int F = p.N / 2;
-#pragma unroll 8
-            for (int m = 0; m < MP; ++m) {
+#pragma unroll 4
+            for (int m = h; m < MP; m += TH) {
                 if (m < p.M) {
                     const float sxm = sm.sx[m];
                     const float yg = __fmul_rn(__int2float_rn(sm.stg[r * SP + m]), __fmul_rn(sxm, swn));
