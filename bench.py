@@ -41,8 +41,8 @@ FALLBACK_HBM_GBS = 6800.0
 # launch (4096 -> 24576, M = 5) over its algorithmic bytes. Valid only for the
 # kernel sources whose sha256 is recorded (kernel_source_sha); roofline.traffic
 # is null otherwise.
-NCU_TRAFFIC = {"source_sha256": "0dc26231095216a903d3e72881b284e837d922e75e653862288f7c7dec491064",
-               "dram_bytes_per_algorithmic_byte": (101657856 + 2394880) / 101273620}
+NCU_TRAFFIC = {"source_sha256": "f8c90da96ed0da604d6a28fd5d09247e0934840cfcf0617f0a3407307704e2fc",
+               "dram_bytes_per_algorithmic_byte": (101689856 + 2688768) / 101273620}
 
 
 def log(*a):

@@ -626,10 +626,12 @@ bf16_stream_kernel(const __grid_constant__ CUtensorMap tmap_w,
             gather_partials<MP, CW, true>(sm, p.slots, p.M, c2, tid, &g_stream_gemm_error);
             consumer_sync<CW>();
         }
-        const int r = tid;
+        // two threads per channel, as in the W8A8 finish: thread h takes tokens h, h + 2, ...
+        constexpr int TH = CW * 32 >= 2 * BN ? 2 : 1;
+        const int r = tid & (BN - 1), h = tid / BN;
         const int n = nt * BN + r;
-        if (r < BN && n < p.N) {
-            for (int m = 0; m < p.M; ++m) p.y[(size_t)m * p.N + n] = stgf[r * C::SP + m];
+        if (h < TH && n < p.N) {
+            for (int m = h; m < p.M; m += TH) p.y[(size_t)m * p.N + n] = stgf[r * C::SP + m];
         }
         consumer_sync<CW>();
     }
