@@ -523,21 +523,27 @@ def main():
             del bs
             torch.cuda.empty_cache()
 
-    # ---- e2e through the public API from host buffers
+    # ---- e2e through the public API from host buffers: one graph per step
+    # that copies the step's inputs in (the first layer's first, the rest on a
+    # parallel branch while the first layer runs), runs the step and copies
+    # the accepted lengths and tokens out; the host waits for them every step
     host_in, host_d = stack.pinned_host_inputs()
     out_len = torch.empty(stack.B, dtype=torch.int32).pin_memory()
     out_tok = torch.empty(stack.B, stack.gamma + 1, dtype=torch.int32).pin_memory()
+    e2e_graph, h2d, d2h = stack.capture_from_host(host_in, host_d, out_len, out_tok)
     for _ in range(3):
-        stack.step_from_host(host_in, host_d, out_len, out_tok, graph=step_graph)
+        e2e_graph.replay()
     torch.cuda.synchronize()
+    assert torch.equal(out_len, ref_len.cpu()) and torch.equal(out_tok, stack.out_tokens.cpu()), \
+        "the step from host buffers disagrees with the device-timed step"
     n_e2e = max(10, args.steps // 4)
-    h2d = d2h = 0
     t0 = time.perf_counter()
     for _ in range(n_e2e):
-        h2d, d2h = stack.step_from_host(host_in, host_d, out_len, out_tok, graph=step_graph)
+        e2e_graph.replay()
         torch.cuda.current_stream().synchronize()      # the host reads the step's result
         _ = int(out_len[0])
     e2e_s = (time.perf_counter() - t0) / n_e2e
+    del e2e_graph
     e2e = {"value": world * stack.M / e2e_s, "unit": UNIT, "h2d_bytes_per_step": h2d,
            "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3}
 

@@ -212,14 +212,19 @@ class VerifyStack:
         qv_w8a8_linear_act per projection (quantization kernel + streaming
         GEMM), qv_lm_head_argmax_act, qv_accept."""
         self._w8_only("the fused-quantization path")
+        self._enqueue_layers(0, self.layers, stream)
+        self._enqueue_head_accept(stream)
+
+    def _enqueue_layers(self, l0, l1, stream):
         M = self.M
-        ws = self.ws_act
-        for l in range(self.layers):
+        for l in range(l0, l1):
             for p, (name, K, N) in enumerate(self.phases):
                 wq, sw = self.weights[l][p]
-                qv.qv_w8a8_linear_act(self.inputs[l][p], wq, sw, self.y[: M * N].view(M, N), ws,
+                qv.qv_w8a8_linear_act(self.inputs[l][p], wq, sw, self.y[: M * N].view(M, N), self.ws_act,
                                       stream=stream)
-        qv.qv_lm_head_argmax_act(self.h_final, self.lm_wq, self.lm_sw, self.tokens, ws,
+
+    def _enqueue_head_accept(self, stream):
+        qv.qv_lm_head_argmax_act(self.h_final, self.lm_wq, self.lm_sw, self.tokens, self.ws_act,
                                  max_logit=self.max_logit, stream=stream)
         qv.qv_accept(self.tokens.view(self.B, self.gamma + 1), self.drafts if self.gamma > 0 else None,
                      self.accept_len, self.out_tokens, stream=stream)
@@ -494,6 +499,36 @@ class VerifyStack:
         drafts = torch.empty_like(self.drafts, device="cpu").pin_memory()
         drafts.copy_(self.drafts)
         return host, drafts
+
+    def capture_from_host(self, host_inputs, host_drafts, out_len, out_tokens):
+        """A CUDA graph of one whole step from host buffers: the first layer's
+        inputs and the drafts are copied to the device, the first layer runs
+        while the other layers' inputs are copied on a parallel branch (which
+        the second layer waits for), then the rest of the step, then the
+        accepted lengths and tokens are copied back into the pinned host
+        tensors. Returns (graph, h2d bytes, d2h bytes) per replay."""
+        self._w8_only("the fused-quantization path")
+        dev = torch.device(self.device)
+        n0 = sum(x.numel() for x in self.inputs[0])      # layer 0's inputs lead the buffer
+
+        def body(main):
+            side = torch.cuda.Stream(device=dev)
+            side.wait_stream(main)
+            self.in_buf[:n0].copy_(host_inputs[:n0], non_blocking=True)
+            self.drafts.copy_(host_drafts, non_blocking=True)
+            with torch.cuda.stream(side):
+                self.in_buf[n0:].copy_(host_inputs[n0:], non_blocking=True)
+            self._enqueue_layers(0, 1, main)
+            main.wait_stream(side)
+            self._enqueue_layers(1, self.layers, main)
+            self._enqueue_head_accept(main)
+            out_len.copy_(self.accept_len, non_blocking=True)
+            out_tokens.copy_(self.out_tokens, non_blocking=True)
+
+        g = self._capture(body, dev)
+        h2d = host_inputs.numel() * host_inputs.element_size() + host_drafts.numel() * host_drafts.element_size()
+        d2h = out_len.numel() * 4 + out_tokens.numel() * 4
+        return g, h2d, d2h
 
     def step_from_host(self, host_inputs, host_drafts, out_len, out_tokens, graph=None):
         """One verify step from host buffers: copy the step's inputs to the

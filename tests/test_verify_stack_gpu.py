@@ -208,6 +208,36 @@ def test_step_from_host_buffers(qv):
     assert torch.equal(out_len, l1.cpu()) and torch.equal(out_tok, o1.cpu())
 
 
+def test_step_graph_from_host_buffers(qv):
+    """The end-to-end step as one graph: the host inputs go in as two copies
+    (the first layer's, and the rest on a parallel branch that the second
+    layer waits for), the results come back into the pinned host tensors, and
+    they equal the device-resident step's, replay after replay, also when the
+    device copies of the inputs were cleared in between."""
+    from quantized_verification_gb300 import synth
+    from quantized_verification_gb300.stack import VerifyStack
+    model = {"hidden": 256, "kv": 128, "ffn": 512, "layers": 3, "vocab": 1000}
+    st = VerifyStack(model=model, B=1, gamma=4, seed=13)
+    st.drafts.copy_(synth.uniform_tokens((1, 4), 1000, seed=3).cuda())
+    g = st.capture()
+    g.replay()
+    torch.cuda.synchronize()
+    l1, o1 = st.accept_len.clone(), st.out_tokens.clone()
+    host_in, host_d = st.pinned_host_inputs()
+    out_len = torch.full((1,), -1, dtype=torch.int32).pin_memory()
+    out_tok = torch.full((1, 5), -1, dtype=torch.int32).pin_memory()
+    ge, h2d, d2h = st.capture_from_host(host_in, host_d, out_len, out_tok)
+    assert h2d == host_in.numel() * 2 + host_d.numel() * 4 and d2h == 4 + 20
+    for rep in range(3):
+        st.in_buf.zero_()
+        st.drafts.zero_()
+        out_len.fill_(-1)
+        out_tok.fill_(-1)
+        ge.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out_len, l1.cpu()) and torch.equal(out_tok, o1.cpu()), rep
+
+
 def test_verify_stack_rejects_large_m(qv):
     M, K, N = 17, 128, 128
     dev = "cuda"
