@@ -3,7 +3,8 @@ grouped-query attention of the verify tokens over the KV cache and the
 step's own keys. Tolerance from the arithmetic: bf16 x bf16 products are
 exact in binary32 and a D-term binary32 dot product errs by at most about
 (D - 1) 2^-24 sum |q k| (under 1e-4 of a score here), which moves the output
-by at most that fraction of max |v|; expf adds a few ulp. So every output
+by at most that fraction of max |v|; the base-2 exponentials (scores
+scaled by log2 e) add a few ulp. So every output
 is within 1e-4 max |v| of the definition. Shapes: the Qwen3-8B layer
 (32 query heads, 8 key/value heads, D = 128) with 5 verify tokens, cache
 lengths on and around the 16-key block and 64-key stage boundaries (and
