@@ -606,8 +606,19 @@ def main():
         tb = torch.empty(ref.shape[0], dtype=torch.int32, device=dev)
         qv.qv_logit_fidelity(ref, logits, kl, ta, tb)
         torch.cuda.synchronize()
-        return {"kl_mean": float(kl.double().mean()), "kl_max": float(kl.max()),
-                "top1_agree": float((ta == tb).float().mean())}
+        out = {"kl_mean": float(kl.double().mean()), "kl_max": float(kl.max()),
+               "top1_agree": float((ta == tb).float().mean())}
+        # the diagnostic's own latency: back-to-back calls on L2-resident logits
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        for _ in range(3):
+            qv.qv_logit_fidelity(ref, logits, kl, ta, tb)
+        e0.record()
+        for _ in range(50):
+            qv.qv_logit_fidelity(ref, logits, kl, ta, tb)
+        e1.record()
+        torch.cuda.synchronize()
+        out["us_per_call"] = e0.elapsed_time(e1) * 1e3 / 50
+        return out
     if rank == 0 and comparator is not None and sampling is not None:
         fidelity = {"w8a8_vs_bf16": fid(stack.logits_bf16, stack.logits),
                     "note": "KL(softmax(BF16 logits) || softmax(quantized logits)) in nats over the LM-head "

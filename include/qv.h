@@ -449,7 +449,7 @@ QV_API qv_status qv_attention_verify(const uint16_t* qkv, const uint16_t* k_cach
  *   q = softmax(row); top1_ref, top1 [M] int32 out = the first index of
  *   each row's maximum (top-1 agreement = equality).
  *   Computed as log1p(E_p[expm1(d - c)]) with d = logits - ref_logits and
- *   c = E_p[d] (binary32 terms, binary64 block sums): relative error about
+ *   c = E_p[d] (binary32 terms, sums of about 48 bits): relative error about
  *   1e-3 of KL or better for KL down to 1e-8. Logits must be finite with
  *   |d - c| < 80. 1 <= M <= 65535, 1 <= V <= 2^24.
  */
