@@ -524,12 +524,12 @@ def main():
             torch.cuda.empty_cache()
 
     # ---- e2e through the public API from host buffers: one graph per step
-    # that copies the step's inputs in (the first layer's first, the rest on a
-    # parallel branch while the first layer runs), runs the step and copies
-    # the accepted lengths and tokens out; the host waits for them every step
+    # that copies the step's inputs in (the drafts and the first layer's
+    # first, in one copy; the rest on a parallel branch while the first layer
+    # runs), runs the step and copies the accepted lengths and tokens out (one
+    # copy); the host waits for them every step
     host_in, host_d = stack.pinned_host_inputs()
-    out_len = torch.empty(stack.B, dtype=torch.int32).pin_memory()
-    out_tok = torch.empty(stack.B, stack.gamma + 1, dtype=torch.int32).pin_memory()
+    out_len, out_tok = stack.pinned_host_results()
     e2e_graph, h2d, d2h = stack.capture_from_host(host_in, host_d, out_len, out_tok)
     for _ in range(3):
         e2e_graph.replay()

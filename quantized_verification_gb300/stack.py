@@ -98,11 +98,16 @@ class VerifyStack:
             self.lm_bf16 = wl if keep_bf16 else None
             del wl
         self.h_final = synth.activations(self.M, h, synth.subseed(seed, "x", "final"), device=dev)
-        # Every per-step activation input becomes a view into one contiguous
-        # buffer (each [M, K] bf16 slice starts 16-byte aligned because K is a
-        # multiple of 16), so a step from host memory is one copy.
+        # Every per-step input becomes a view into one contiguous byte buffer:
+        # the drafts (int32, padded to 256 bytes), then every activation input
+        # (each [M, K] bf16 slice starts 16-byte aligned because K is a
+        # multiple of 16), so a step's inputs come from host memory in few
+        # copies.
         flat = [x for li in self.inputs for x in li] + [self.h_final]
-        self.in_buf = torch.empty(sum(x.numel() for x in flat), dtype=flat[0].dtype, device=dev)
+        self._draft_pad = (B * max(gamma, 0) * 4 + 255) // 256 * 256
+        n_act = sum(x.numel() for x in flat)
+        self.io_in = torch.zeros(self._draft_pad + n_act * flat[0].element_size(), dtype=torch.uint8, device=dev)
+        self.in_buf = self.io_in[self._draft_pad:].view(flat[0].dtype)
         views, off = [], 0
         for x in flat:
             v = self.in_buf[off: off + x.numel()].view(x.shape)
@@ -116,7 +121,7 @@ class VerifyStack:
                 k += 1
         self.h_final = views[k]
         del flat
-        self.drafts = torch.zeros(B, max(gamma, 0), dtype=torch.int32, device=dev)
+        self.drafts = self.io_in[: B * max(gamma, 0) * 4].view(torch.int32).view(B, max(gamma, 0))
 
         kmax = max(K for (_, K, _) in self.phases)
         nmax = max(N for (_, _, N) in self.phases)
@@ -125,8 +130,10 @@ class VerifyStack:
         self.y = torch.empty(self.M * nmax, dtype=y_dtype, device=dev)
         self.tokens = torch.empty(self.M, dtype=torch.int32, device=dev)
         self.max_logit = torch.empty(self.M, dtype=torch.float32, device=dev)
-        self.accept_len = torch.empty(B, dtype=torch.int32, device=dev)
-        self.out_tokens = torch.empty(B, gamma + 1, dtype=torch.int32, device=dev)
+        # the step's results, also one buffer: accepted lengths, then tokens
+        self.io_out = torch.empty(B * (gamma + 2), dtype=torch.int32, device=dev)
+        self.accept_len = self.io_out[:B]
+        self.out_tokens = self.io_out[B:].view(B, gamma + 1)
         ws_bytes = max([qv.qv_workspace_bytes(qv.QV_OP_LINEAR, self.M, K, N) for (_, K, N) in self.phases]
                        + [qv.qv_workspace_bytes(qv.QV_OP_LM_HEAD, self.M, h, self.V)])
         self.ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
@@ -492,21 +499,63 @@ class VerifyStack:
 
     # ------------------------------------------------------------------ host API
     def pinned_host_inputs(self):
-        """Pinned host copies of the per-step inputs: every activation input in
-        one buffer (laid out like the device buffer), and the drafts."""
-        host = torch.empty_like(self.in_buf, device="cpu").pin_memory()
-        host.copy_(self.in_buf)
-        drafts = torch.empty_like(self.drafts, device="cpu").pin_memory()
-        drafts.copy_(self.drafts)
-        return host, drafts
+        """Pinned host copies of the per-step inputs, laid out like the device
+        buffer (the drafts, then every activation input): returns the
+        activation inputs and the drafts as views of one pinned buffer."""
+        io = torch.empty_like(self.io_in, device="cpu").pin_memory()
+        io.copy_(self.io_in)
+        return io[self._draft_pad:].view(self.in_buf.dtype), io[: self.drafts.numel() * 4].view(
+            torch.int32).view(self.drafts.shape)
+
+    def pinned_host_results(self):
+        """Pinned host tensors for the step's results (accepted lengths
+        [B], output tokens [B, gamma+1]): views of one pinned buffer laid out
+        like the device's, so that they come back in one copy."""
+        io = torch.empty_like(self.io_out, device="cpu").pin_memory()
+        return io[: self.B], io[self.B:].view(self.B, self.gamma + 1)
+
+    @staticmethod
+    def _whole(t):
+        """The whole storage under a tensor, as bytes."""
+        return torch.empty(0, dtype=torch.uint8, device=t.device).set_(t.untyped_storage())
+
+    def _copy_inputs(self, host_inputs, host_drafts, n):
+        """Copy the drafts and in_buf[:n] from host memory: one copy when the
+        two host tensors lie in one buffer laid out like io_in (as
+        pinned_host_inputs makes them), else one copy each."""
+        same = (host_inputs.untyped_storage().data_ptr() == host_drafts.untyped_storage().data_ptr()
+                and host_drafts.storage_offset() == 0
+                and host_inputs.storage_offset() * host_inputs.element_size() == self._draft_pad)
+        if same:
+            nb = self._draft_pad + n * self.in_buf.element_size()
+            self.io_in[:nb].copy_(self._whole(host_inputs)[:nb], non_blocking=True)
+        else:
+            self.in_buf[:n].copy_(host_inputs[:n], non_blocking=True)
+            self.drafts.copy_(host_drafts, non_blocking=True)
+
+    def _copy_results(self, out_len, out_tokens):
+        """Copy the accepted lengths and output tokens to host memory: one
+        copy when the two host tensors lie in one buffer laid out like
+        io_out (as pinned_host_results makes them), else one copy each."""
+        same = (out_len.untyped_storage().data_ptr() == out_tokens.untyped_storage().data_ptr()
+                and out_len.storage_offset() == 0 and out_tokens.storage_offset() == self.B
+                and out_len.dtype == torch.int32 and out_tokens.dtype == torch.int32)
+        if same:
+            self._whole(out_len)[: self.io_out.numel() * 4].copy_(self.io_out.view(torch.uint8),
+                                                                 non_blocking=True)
+        else:
+            out_len.copy_(self.accept_len, non_blocking=True)
+            out_tokens.copy_(self.out_tokens, non_blocking=True)
 
     def capture_from_host(self, host_inputs, host_drafts, out_len, out_tokens):
-        """A CUDA graph of one whole step from host buffers: the first layer's
-        inputs and the drafts are copied to the device, the first layer runs
+        """A CUDA graph of one whole step from host buffers: the drafts and
+        the first layer's inputs are copied to the device (one copy when the
+        host tensors come from pinned_host_inputs), the first layer runs
         while the other layers' inputs are copied on a parallel branch (which
         the second layer waits for), then the rest of the step, then the
         accepted lengths and tokens are copied back into the pinned host
-        tensors. Returns (graph, h2d bytes, d2h bytes) per replay."""
+        tensors (one copy when they come from pinned_host_results). Returns
+        (graph, h2d bytes, d2h bytes) per replay."""
         self._w8_only("the fused-quantization path")
         dev = torch.device(self.device)
         n0 = sum(x.numel() for x in self.inputs[0])      # layer 0's inputs lead the buffer
@@ -514,16 +563,14 @@ class VerifyStack:
         def body(main):
             side = torch.cuda.Stream(device=dev)
             side.wait_stream(main)
-            self.in_buf[:n0].copy_(host_inputs[:n0], non_blocking=True)
-            self.drafts.copy_(host_drafts, non_blocking=True)
+            self._copy_inputs(host_inputs, host_drafts, n0)
             with torch.cuda.stream(side):
                 self.in_buf[n0:].copy_(host_inputs[n0:], non_blocking=True)
             self._enqueue_layers(0, 1, main)
             main.wait_stream(side)
             self._enqueue_layers(1, self.layers, main)
             self._enqueue_head_accept(main)
-            out_len.copy_(self.accept_len, non_blocking=True)
-            out_tokens.copy_(self.out_tokens, non_blocking=True)
+            self._copy_results(out_len, out_tokens)
 
         g = self._capture(body, dev)
         h2d = host_inputs.numel() * host_inputs.element_size() + host_drafts.numel() * host_drafts.element_size()
@@ -532,15 +579,12 @@ class VerifyStack:
 
     def step_from_host(self, host_inputs, host_drafts, out_len, out_tokens, graph=None):
         """One verify step from host buffers: copy the step's inputs to the
-        device (one copy for all activations, one for the drafts), run the
-        captured step, copy the accepted lengths and tokens back (into pinned
-        host tensors). Returns bytes copied (h2d, d2h)."""
-        self.in_buf.copy_(host_inputs, non_blocking=True)
-        self.drafts.copy_(host_drafts, non_blocking=True)
+        device, run the captured step, copy the accepted lengths and tokens
+        back (into pinned host tensors). Returns bytes copied (h2d, d2h)."""
+        self._copy_inputs(host_inputs, host_drafts, self.in_buf.numel())
         h2d = host_inputs.numel() * host_inputs.element_size() + host_drafts.numel() * host_drafts.element_size()
         (graph or self.graph).replay()
-        out_len.copy_(self.accept_len, non_blocking=True)
-        out_tokens.copy_(self.out_tokens, non_blocking=True)
+        self._copy_results(out_len, out_tokens)
         d2h = out_len.numel() * 4 + out_tokens.numel() * 4
         return h2d, d2h
 

@@ -183,9 +183,25 @@ def test_verify_stack_equals_per_op_calls(qv):
     assert torch.equal(st.tokens, t1)
 
 
-def test_step_from_host_buffers(qv):
-    """The end-to-end step: the packed host inputs, copied in one transfer and
-    run through the captured graph, give the same tokens as the device-resident
+def _host_io(st, layout):
+    """The pinned host tensors of a step from host memory: "merged" as the
+    stack lays them out (drafts and inputs in one buffer, both results in
+    one buffer: one copy each way), "separate" as unrelated pinned tensors
+    (one copy per tensor)."""
+    host_in, host_d = st.pinned_host_inputs()
+    if layout == "merged":
+        out_len, out_tok = st.pinned_host_results()
+    else:
+        host_in, host_d = host_in.clone().pin_memory(), host_d.clone().pin_memory()
+        out_len = torch.empty(st.B, dtype=torch.int32).pin_memory()
+        out_tok = torch.empty(st.B, st.gamma + 1, dtype=torch.int32).pin_memory()
+    return host_in, host_d, out_len, out_tok
+
+
+@pytest.mark.parametrize("layout", ["merged", "separate"])
+def test_step_from_host_buffers(qv, layout):
+    """The end-to-end step: the packed host inputs, copied in and run
+    through the captured graph, give the same tokens as the device-resident
     step, and the result lands in the pinned host tensors."""
     from quantized_verification_gb300 import synth
     from quantized_verification_gb300.stack import VerifyStack
@@ -196,24 +212,25 @@ def test_step_from_host_buffers(qv):
     g.replay()
     torch.cuda.synchronize()
     l1, o1 = st.accept_len.clone(), st.out_tokens.clone()
-    host_in, host_d = st.pinned_host_inputs()
+    host_in, host_d, out_len, out_tok = _host_io(st, layout)
     assert host_in.numel() == sum(x.numel() for li in st.inputs for x in li) + st.h_final.numel()
     st.in_buf.zero_()
     st.drafts.zero_()
-    out_len = torch.empty(1, dtype=torch.int32).pin_memory()
-    out_tok = torch.empty(1, 5, dtype=torch.int32).pin_memory()
+    out_len.fill_(-1)
+    out_tok.fill_(-1)
     h2d, d2h = st.step_from_host(host_in, host_d, out_len, out_tok, graph=g)
     torch.cuda.synchronize()
     assert h2d == host_in.numel() * 2 + host_d.numel() * 4 and d2h == 4 + 20
     assert torch.equal(out_len, l1.cpu()) and torch.equal(out_tok, o1.cpu())
 
 
-def test_step_graph_from_host_buffers(qv):
-    """The end-to-end step as one graph: the host inputs go in as two copies
-    (the first layer's, and the rest on a parallel branch that the second
-    layer waits for), the results come back into the pinned host tensors, and
-    they equal the device-resident step's, replay after replay, also when the
-    device copies of the inputs were cleared in between."""
+@pytest.mark.parametrize("layout", ["merged", "separate"])
+def test_step_graph_from_host_buffers(qv, layout):
+    """The end-to-end step as one graph: the host inputs go in as the first
+    layer's (with the drafts) and the rest on a parallel branch that the
+    second layer waits for, the results come back into the pinned host
+    tensors, and they equal the device-resident step's, replay after replay,
+    also when the device copies of the inputs were cleared in between."""
     from quantized_verification_gb300 import synth
     from quantized_verification_gb300.stack import VerifyStack
     model = {"hidden": 256, "kv": 128, "ffn": 512, "layers": 3, "vocab": 1000}
@@ -223,9 +240,7 @@ def test_step_graph_from_host_buffers(qv):
     g.replay()
     torch.cuda.synchronize()
     l1, o1 = st.accept_len.clone(), st.out_tokens.clone()
-    host_in, host_d = st.pinned_host_inputs()
-    out_len = torch.full((1,), -1, dtype=torch.int32).pin_memory()
-    out_tok = torch.full((1, 5), -1, dtype=torch.int32).pin_memory()
+    host_in, host_d, out_len, out_tok = _host_io(st, layout)
     ge, h2d, d2h = st.capture_from_host(host_in, host_d, out_len, out_tok)
     assert h2d == host_in.numel() * 2 + host_d.numel() * 4 and d2h == 4 + 20
     for rep in range(3):
