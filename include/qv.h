@@ -36,9 +36,10 @@
  *     running when the call is enqueued; qv_quantize_weight never lets its
  *     successor start early, so quantize-then-use on one stream is safe.
  *   - Results are deterministic: every call returns identical bits for
- *     identical inputs. The fp32 results of the bf16 comparator and of
- *     attention also depend on how the work is split (the SM count, the
- *     cluster size), so they are repeatable on one GPU model, not across.
+ *     identical inputs. The fp32 results of the bf16 comparator, of
+ *     attention and of the logit-fidelity diagnostic also depend on how the
+ *     work is split (the SM count, the cluster size), so they are repeatable
+ *     on one GPU model, not across.
  */
 #ifndef QV_H
 #define QV_H
@@ -452,6 +453,10 @@ QV_API qv_status qv_attention_verify(const uint16_t* qkv, const uint16_t* k_cach
  *   c = E_p[d] (binary32 terms, sums of about 48 bits): relative error about
  *   1e-3 of KL or better for KL down to 1e-8. Logits must be finite with
  *   |d - c| < 80. 1 <= M <= 65535, 1 <= V <= 2^24.
+ *   One launch of M thread-block clusters of 16 CTAs (a non-portable
+ *   cluster size: the GPU must fit 16 co-resident CTAs of 1024 threads in
+ *   one GPC, which GB300 does; QV_ERR_CUDA otherwise), up to about 200 KB
+ *   of shared memory per CTA; no workspace.
  */
 QV_API qv_status qv_logit_fidelity(const float* ref_logits, const float* logits, int M, int V,
                                    float* kl, int32_t* top1_ref, int32_t* top1, cudaStream_t stream);
