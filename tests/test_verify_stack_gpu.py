@@ -224,25 +224,28 @@ def test_step_from_host_buffers(qv, layout):
     assert torch.equal(out_len, l1.cpu()) and torch.equal(out_tok, o1.cpu())
 
 
-@pytest.mark.parametrize("layout", ["merged", "separate"])
-def test_step_graph_from_host_buffers(qv, layout):
+@pytest.mark.parametrize("layout,B,gamma", [("merged", 1, 4), ("separate", 1, 4), ("merged", 2, 3),
+                                             ("merged", 1, 0), ("separate", 3, 0)])
+def test_step_graph_from_host_buffers(qv, layout, B, gamma):
     """The end-to-end step as one graph: the host inputs go in as the first
     layer's (with the drafts) and the rest on a parallel branch that the
     second layer waits for, the results come back into the pinned host
     tensors, and they equal the device-resident step's, replay after replay,
-    also when the device copies of the inputs were cleared in between."""
+    also when the device copies of the inputs were cleared in between; with
+    several sequences and with no drafts (an empty drafts slice)."""
     from quantized_verification_gb300 import synth
     from quantized_verification_gb300.stack import VerifyStack
     model = {"hidden": 256, "kv": 128, "ffn": 512, "layers": 3, "vocab": 1000}
-    st = VerifyStack(model=model, B=1, gamma=4, seed=13)
-    st.drafts.copy_(synth.uniform_tokens((1, 4), 1000, seed=3).cuda())
+    st = VerifyStack(model=model, B=B, gamma=gamma, seed=13)
+    if gamma > 0:
+        st.drafts.copy_(synth.uniform_tokens((B, gamma), 1000, seed=3).cuda())
     g = st.capture()
     g.replay()
     torch.cuda.synchronize()
     l1, o1 = st.accept_len.clone(), st.out_tokens.clone()
     host_in, host_d, out_len, out_tok = _host_io(st, layout)
     ge, h2d, d2h = st.capture_from_host(host_in, host_d, out_len, out_tok)
-    assert h2d == host_in.numel() * 2 + host_d.numel() * 4 and d2h == 4 + 20
+    assert h2d == host_in.numel() * 2 + host_d.numel() * 4 and d2h == 4 * B * (gamma + 2)
     for rep in range(3):
         st.in_buf.zero_()
         st.drafts.zero_()
