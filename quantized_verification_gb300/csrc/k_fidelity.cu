@@ -126,8 +126,8 @@ __device__ __forceinline__ void warp0_sum(const float (&v)[NV], double (&out)[NV
 // float4-loaded part (the first 4*n4 entries), ft(v, x, y) on the scalar
 // rest. Src 0 reads the row; Src 1 reads it and keeps this thread's float4s
 // in shared memory (sa, sb); Src 2 reads them back from there and stores
-// what fv leaves in x and y in their place. A thread only ever reads back
-// what it stored itself.
+// what fv leaves in x and y in their place; Src 3 only reads them back. A
+// thread only ever reads back what it stored itself.
 template <int Src, class FV, class FT>
 __device__ __forceinline__ void for_slice(const float* __restrict__ ar, const float* __restrict__ br,
                                           float4* sa, float4* sb, int lo, int n4, int hi, FV&& fv, FT&& ft) {
@@ -136,7 +136,7 @@ __device__ __forceinline__ void for_slice(const float* __restrict__ ar, const fl
 #pragma unroll 4
     for (int i = threadIdx.x; i < n4; i += kFidThreads) {
         float4 x, y;
-        if (Src == 2) {
+        if (Src >= 2) {
             x = sa[i];
             y = sb[i];
         } else {
@@ -269,7 +269,7 @@ __global__ void __launch_bounds__(kFidThreads) logit_fidelity_kernel(const float
     auto excess = [&](int, float& x, float& y) { s2 += expf(x - ma) * expm1f((y - x) - c); };
     auto excess_kept = [&](int, float& e, float& d) { s2 += e * expm1f(d - c); };
     if (cached)
-        for_slice<2>(ar, br, sa, sb, lo, n4, hi, excess_kept, excess);
+        for_slice<3>(ar, br, sa, sb, lo, n4, hi, excess_kept, excess);
     else
         for_slice<0>(ar, br, sa, sb, lo, n4, hi, excess, excess);
     double s2s[1];
